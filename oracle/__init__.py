@@ -1,0 +1,180 @@
+"""CPU oracle for the draft-head path (test infrastructure only).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline / reference leg may
+import this package.  The product library never loads it, and it shares no code with the CUDA
+path.  ``build()`` compiles ``dh_oracle.cpp`` with g++ (OpenMP, no fp contraction) into
+``liboracle.so`` next to it; the wrappers below take numpy arrays / CPU torch tensors.
+
+Parity unpinned: the bf16 stage-1 scores of the full-size workloads are checked only through this
+oracle's own pins on smaller shapes (brute force, closed forms, hand-built trees).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "dh_oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+F32, BF16 = 0, 1
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (idempotent)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".{os.getpid()}.tmp"
+        cmd = ["g++", "-O2", "-std=c++17", "-fopenmp", "-ffp-contract=off", "-shared", "-fPIC",
+               _SRC, "-o", tmp]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def bind(path: str):
+    """Load an oracle shared library from ``path`` and declare its signatures."""
+    lib = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    lib.oracle_round_bf16.argtypes = [P, I, P]
+    lib.oracle_lowrank_project.argtypes = [P, P, I, I, I, I, P, I, P]
+    lib.oracle_lowrank_scores.argtypes = [P, P, P, I, I, I, I, I, P, I, P]
+    lib.oracle_lowrank_topk.argtypes = [P, P, P, I, I, I, I, I, I, P, I, P, P]
+    lib.oracle_exact_rescore.argtypes = [P, P, P, I, I, I, I, I, P, I, P, P]
+    lib.oracle_tree_accept.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P]
+    for f in ("oracle_round_bf16", "oracle_lowrank_project", "oracle_lowrank_scores",
+              "oracle_lowrank_topk", "oracle_exact_rescore", "oracle_tree_accept"):
+        getattr(lib, f).restype = I
+    return lib
+
+
+def load():
+    global _lib
+    if _lib is None:
+        _lib = bind(build())
+    return _lib
+
+
+def _raw(x):
+    """(contiguous numpy array holding the stored bits, dtype code) for a tensor or array."""
+    try:
+        import torch
+        if isinstance(x, torch.Tensor):
+            x = x.detach().cpu().contiguous()
+            if x.dtype == torch.bfloat16:
+                return np.ascontiguousarray(x.view(torch.int16).numpy().view(np.uint16)), BF16
+            if x.dtype == torch.float32:
+                return np.ascontiguousarray(x.numpy()), F32
+            if x.dtype == torch.int32:
+                return np.ascontiguousarray(x.numpy()), None
+            raise TypeError(f"unsupported tensor dtype {x.dtype}")
+    except ImportError:
+        pass
+    x = np.ascontiguousarray(x)
+    if x.dtype == np.float32:
+        return x, F32
+    if x.dtype == np.uint16:
+        return x, BF16
+    if x.dtype == np.int32:
+        return x, None
+    raise TypeError(f"unsupported array dtype {x.dtype}")
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _rows(rows, n_all):
+    if rows is None:
+        return None, n_all
+    r = np.ascontiguousarray(np.asarray(rows, dtype=np.int32))
+    return r, len(r)
+
+
+def _check(rc, what):
+    if rc not in (0, -2):
+        raise ValueError(f"oracle {what} rejected its arguments (rc={rc})")
+    return rc
+
+
+def round_bf16(x) -> np.ndarray:
+    x = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    out = np.empty_like(x)
+    _check(load().oracle_round_bf16(_ptr(x), x.size, _ptr(out)), "round_bf16")
+    return out
+
+
+def lowrank_project(h, U, rows=None) -> np.ndarray:
+    hh, dt = _raw(h)
+    uu, _ = _raw(U)
+    B, d = hh.shape
+    r = uu.shape[1]
+    rr, n = _rows(rows, B)
+    out = np.empty((n, r), dtype=np.float64)
+    _check(load().oracle_lowrank_project(_ptr(hh), _ptr(uu), B, d, r, dt,
+                                         None if rr is None else _ptr(rr), n, _ptr(out)), "project")
+    return out
+
+
+def lowrank_scores(h, U, V, rows=None) -> np.ndarray:
+    hh, dt = _raw(h)
+    uu, _ = _raw(U)
+    vv, _ = _raw(V)
+    B, d = hh.shape
+    r, vocab = vv.shape
+    rr, n = _rows(rows, B)
+    out = np.empty((n, vocab), dtype=np.float64)
+    _check(load().oracle_lowrank_scores(_ptr(hh), _ptr(uu), _ptr(vv), B, d, r, vocab, dt,
+                                        None if rr is None else _ptr(rr), n, _ptr(out)), "scores")
+    return out
+
+
+def lowrank_topk(h, U, V, K, rows=None):
+    hh, dt = _raw(h)
+    uu, _ = _raw(U)
+    vv, _ = _raw(V)
+    B, d = hh.shape
+    r, vocab = vv.shape
+    rr, n = _rows(rows, B)
+    idx = np.empty((n, K), dtype=np.int32)
+    sc = np.empty((n, K), dtype=np.float64)
+    _check(load().oracle_lowrank_topk(_ptr(hh), _ptr(uu), _ptr(vv), B, d, r, vocab, K, dt,
+                                      None if rr is None else _ptr(rr), n, _ptr(idx), _ptr(sc)),
+           "topk")
+    return idx, sc
+
+
+def exact_rescore(h, W, idx, rows=None):
+    hh, dt = _raw(h)
+    ww, _ = _raw(W)
+    ii, _ = _raw(idx)
+    B, d = hh.shape
+    vocab = ww.shape[0]
+    K = ii.shape[1]
+    rr, n = _rows(rows, B)
+    z = np.empty((n, K), dtype=np.float64)
+    p = np.empty((n, K), dtype=np.float64)
+    _check(load().oracle_exact_rescore(_ptr(hh), _ptr(ww), _ptr(ii), B, d, vocab, K, dt,
+                                       None if rr is None else _ptr(rr), n, _ptr(z), _ptr(p)),
+           "rescore")
+    return z, p
+
+
+def tree_accept(logits, parent, token, reqs=None):
+    ll, dt = _raw(logits)
+    pp, _ = _raw(parent)
+    tt, _ = _raw(token)
+    B, N, vocab = ll.shape
+    rr, n = _rows(reqs, B)
+    am = np.empty((n, N), dtype=np.int32)
+    path = np.empty((n, N), dtype=np.int32)
+    ln = np.empty((n,), dtype=np.int32)
+    bonus = np.empty((n,), dtype=np.int32)
+    _check(load().oracle_tree_accept(_ptr(ll), _ptr(pp), _ptr(tt), B, N, vocab, dt,
+                                     None if rr is None else _ptr(rr), n, _ptr(am), _ptr(path),
+                                     _ptr(ln), _ptr(bonus)), "tree_accept")
+    return {"argmax": am, "path": path, "len": ln, "bonus": bonus}

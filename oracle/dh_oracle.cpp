@@ -1,0 +1,226 @@
+// CPU oracle for the two-stage draft LM head and greedy draft-tree acceptance.
+//
+// TEST INFRASTRUCTURE ONLY.  This file is the slow, plain reference that the CUDA library is
+// checked against.  Only the tests, the package smoke check and the benchmark's CPU-baseline leg
+// load it; the product path never does.  It shares no code, header, table or helper with the CUDA
+// library: it reads the raw input arrays and writes its own outputs.
+//
+// Arithmetic: every dot product is accumulated in double from the stored (fp32 or bf16) values;
+// products of two stored values are exact in double, so only the running sums round.  Steps follow
+// the pages' order:
+//
+//   EAGLE-4 summary page (yuxiaoba.github.io/tech/en/eagle-4), section "Retrieve vocabulary
+//   candidates cheaply, then score them exactly": a low-rank head over the full vocabulary
+//   retrieves candidates, and the original full-rank head then gives their exact logits.
+//     1. t = h U, rounded to the activation dtype (bf16: round to nearest, ties to even).
+//     2. s = t V over the whole vocabulary (the factored order (hU)V, which is why the head is
+//        cheap; AlphaSignal "EAGLE-4 Triples Qwen3 Inference Speed...", section "Runtime-sized
+//        speculation", low-rank candidate head).
+//     3. the K candidates: the first K of all v ordered by (s desc, v asc).
+//     4. z = h W[idx]^T, the exact full-rank logits of the candidates.
+//     5. p = softmax(z) over the K candidates (temperature 1).
+//
+//   daily.dev "EAGLE-4 speeds up LLM inference with an adaptive speculative decoding drafter",
+//   section "How it works": the target checks every drafted token in one pass, matching tokens
+//   are kept and the first mismatch is replaced by the target's own token; EAGLE-4 summary page,
+//   section "Distribution preservation...": greedy decoding follows the target's choices.
+//     6. a[b,n] = argmax_v L[b,n,v] (ties -> lowest v), over the stored values;
+//        acc[0] = 1, acc[n] = acc[parent[n]] and token[n] == a[b,parent[n]];
+//        the deepest accepted node (ties -> lowest node index) ends the accepted path;
+//        len = its depth, path = root..node, bonus = a[b,node].
+//
+// Build: g++ -O2 -std=c++17 -fopenmp -ffp-contract=off -shared -fPIC dh_oracle.cpp
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <utility>
+#include <vector>
+
+namespace {
+
+enum { ORACLE_F32 = 0, ORACLE_BF16 = 1 };
+
+// A bf16 value is the upper half of an IEEE-754 binary32 value.
+double bf16_value(uint16_t x) {
+  uint32_t u = static_cast<uint32_t>(x) << 16;
+  float f;
+  std::memcpy(&f, &u, sizeof f);
+  return static_cast<double>(f);
+}
+
+double stored_value(const void* p, int dtype, size_t i) {
+  if (dtype == ORACLE_F32) return static_cast<double>(static_cast<const float*>(p)[i]);
+  return bf16_value(static_cast<const uint16_t*>(p)[i]);
+}
+
+// Nearest bf16 value to x, ties to the even significand.  bf16 keeps 8 significant bits and the
+// exponent range of binary32 (smallest normal 2^-126, subnormal quantum 2^-133).  Scaling by a
+// power of two is exact, nearbyint rounds to nearest-even in the default rounding mode.
+double round_to_bf16(double x) {
+  if (x == 0.0 || !std::isfinite(x)) return x;
+  int e = std::ilogb(x);
+  if (e < -126) e = -126;
+  double q = std::ldexp(x, 7 - e);
+  return std::ldexp(std::nearbyint(q), e - 7);
+}
+
+double round_to_dtype(double x, int dtype) {
+  if (dtype == ORACLE_F32) return static_cast<double>(static_cast<float>(x));
+  return round_to_bf16(x);
+}
+
+bool valid_dtype(int dtype) { return dtype == ORACLE_F32 || dtype == ORACLE_BF16; }
+
+// Step 1: t[j] = round( sum_i h[b,i] U[i,j] ).
+void project_row(const void* h, const void* U, int b, int d, int r, int dtype, double* t) {
+  for (int j = 0; j < r; ++j) {
+    double acc = 0.0;
+    for (int i = 0; i < d; ++i)
+      acc += stored_value(h, dtype, (size_t)b * d + i) * stored_value(U, dtype, (size_t)i * r + j);
+    t[j] = round_to_dtype(acc, dtype);
+  }
+}
+
+// Step 2: s[v] = sum_j t[j] V[j,v]; the sum runs over j in ascending order for every v.
+void score_row(const double* t, const void* V, int r, int vocab, int dtype, double* s) {
+  for (int v = 0; v < vocab; ++v) s[v] = 0.0;
+  for (int j = 0; j < r; ++j) {
+    const double tj = t[j];
+    for (int v = 0; v < vocab; ++v) s[v] += tj * stored_value(V, dtype, (size_t)j * vocab + v);
+  }
+}
+
+int row_of(const int32_t* rows, int i) { return rows ? rows[i] : i; }
+
+}  // namespace
+
+extern "C" {
+
+int oracle_version(void) { return 1; }
+
+// Nearest bf16 (ties to even) of each x, returned as a double.
+int oracle_round_bf16(const double* x, int n, double* out) {
+  for (int i = 0; i < n; ++i) out[i] = round_to_bf16(x[i]);
+  return 0;
+}
+
+// Step 1 for the listed rows (rows == nullptr: rows 0..n_rows-1).  t_out: n_rows x r doubles.
+int oracle_lowrank_project(const void* h, const void* U, int B, int d, int r, int dtype,
+                           const int32_t* rows, int n_rows, double* t_out) {
+  if (!valid_dtype(dtype) || B < 0 || d <= 0 || r <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_rows; ++i) project_row(h, U, row_of(rows, i), d, r, dtype, t_out + (size_t)i * r);
+  return 0;
+}
+
+// Steps 1-2 for the listed rows.  s_out: n_rows x vocab doubles.
+int oracle_lowrank_scores(const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
+                          int dtype, const int32_t* rows, int n_rows, double* s_out) {
+  if (!valid_dtype(dtype) || B < 0 || d <= 0 || r <= 0 || vocab <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_rows; ++i) {
+    std::vector<double> t(r);
+    project_row(h, U, row_of(rows, i), d, r, dtype, t.data());
+    score_row(t.data(), V, r, vocab, dtype, s_out + (size_t)i * vocab);
+  }
+  return 0;
+}
+
+// Steps 1-3 for the listed rows: idx_out / score_out are n_rows x K, ordered by (s desc, v asc).
+int oracle_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
+                        int K, int dtype, const int32_t* rows, int n_rows, int32_t* idx_out,
+                        double* score_out) {
+  if (!valid_dtype(dtype) || B < 0 || d <= 0 || r <= 0 || vocab <= 0 || K <= 0 || K > vocab) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_rows; ++i) {
+    std::vector<double> t(r), s(vocab);
+    project_row(h, U, row_of(rows, i), d, r, dtype, t.data());
+    score_row(t.data(), V, r, vocab, dtype, s.data());
+    std::vector<std::pair<double, int32_t>> order(vocab);  // (-s, v): ascending = (s desc, v asc)
+    for (int v = 0; v < vocab; ++v) order[v] = {-s[v], v};
+    std::partial_sort(order.begin(), order.begin() + K, order.end());
+    for (int k = 0; k < K; ++k) {
+      idx_out[(size_t)i * K + k] = order[k].second;
+      score_out[(size_t)i * K + k] = s[order[k].second];
+    }
+  }
+  return 0;
+}
+
+// Steps 4-5 for the listed rows: z = h W[idx]^T and p = softmax(z) over the K candidates.
+// Returns -2 if an index lies outside [0, vocab).
+int oracle_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
+                         int K, int dtype, const int32_t* rows, int n_rows, double* logits_out,
+                         double* probs_out) {
+  if (!valid_dtype(dtype) || B < 0 || d <= 0 || vocab <= 0 || K <= 0) return -1;
+  int bad = 0;
+#pragma omp parallel for schedule(dynamic, 1) reduction(+ : bad)
+  for (int i = 0; i < n_rows; ++i) {
+    const int b = row_of(rows, i);
+    double* z = logits_out + (size_t)i * K;
+    for (int k = 0; k < K; ++k) {
+      const int32_t v = idx[(size_t)b * K + k];
+      if (v < 0 || v >= vocab) { bad += 1; z[k] = NAN; continue; }
+      double acc = 0.0;
+      for (int c = 0; c < d; ++c)
+        acc += stored_value(h, dtype, (size_t)b * d + c) * stored_value(W, dtype, (size_t)v * d + c);
+      z[k] = acc;
+    }
+    if (probs_out) {
+      double m = -INFINITY;
+      for (int k = 0; k < K; ++k) m = std::max(m, z[k]);
+      double sum = 0.0;
+      for (int k = 0; k < K; ++k) sum += std::exp(z[k] - m);
+      for (int k = 0; k < K; ++k) probs_out[(size_t)i * K + k] = std::exp(z[k] - m) / sum;
+    }
+  }
+  return bad ? -2 : 0;
+}
+
+// Step 6 for the listed requests.  logits: B x N x vocab (request-major); outputs per listed
+// request i: argmax_out[i*N + n], path_out[i*N + j] (root first, -1 padded), len_out[i],
+// bonus_out[i].  A request whose parent array is not a tree rooted at node 0 with parents
+// preceding children gets len = -1, bonus = -1 and an all -1 path.
+int oracle_tree_accept(const void* logits, const int32_t* parent, const int32_t* token, int B, int N,
+                       int vocab, int dtype, const int32_t* reqs, int n_reqs, int32_t* argmax_out,
+                       int32_t* path_out, int32_t* len_out, int32_t* bonus_out) {
+  if (!valid_dtype(dtype) || B < 0 || N <= 0 || vocab <= 0) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int i = 0; i < n_reqs; ++i) {
+    const int b = row_of(reqs, i);
+    int32_t* a = argmax_out + (size_t)i * N;
+    for (int n = 0; n < N; ++n) {
+      const size_t base = ((size_t)b * N + n) * (size_t)vocab;
+      double best = stored_value(logits, dtype, base);
+      int32_t arg = 0;
+      for (int v = 1; v < vocab; ++v) {
+        const double x = stored_value(logits, dtype, base + v);
+        if (x > best) { best = x; arg = v; }
+      }
+      a[n] = arg;
+    }
+    const int32_t* par = parent + (size_t)b * N;
+    const int32_t* tok = token + (size_t)b * N;
+    int32_t* path = path_out + (size_t)i * N;
+    for (int n = 0; n < N; ++n) path[n] = -1;
+    bool ok = par[0] == -1;
+    for (int n = 1; n < N && ok; ++n) ok = par[n] >= 0 && par[n] < n;
+    if (!ok) { len_out[i] = -1; bonus_out[i] = -1; continue; }
+    std::vector<int> depth(N, 0);
+    std::vector<char> acc(N, 0);
+    acc[0] = 1;
+    int best = 0;
+    for (int n = 1; n < N; ++n) {
+      depth[n] = depth[par[n]] + 1;
+      acc[n] = acc[par[n]] && tok[n] == a[par[n]];
+      if (acc[n] && depth[n] > depth[best]) best = n;  // strict: ties keep the lower node index
+    }
+    len_out[i] = depth[best];
+    bonus_out[i] = a[best];
+    for (int n = best, j = depth[best]; n >= 0; n = par[n], --j) path[j] = n;
+  }
+  return 0;
+}
+
+}  // extern "C"
