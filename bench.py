@@ -1,0 +1,587 @@
+#!/usr/bin/env python3
+"""Benchmark of the GB300 draft-head path (prints one JSON line on rank 0).
+
+A step is one pass of the draft head over one batch: dh_lowrank_topk (projection, vocabulary-wide
+low-rank scores, exact top-K) followed by dh_exact_rescore (gathered full-rank logits + softmax),
+on the workload's synthetic inputs already resident in HBM.  ``--workload tree`` times
+dh_tree_accept instead.
+
+* value: rows per second over the whole job (sum over ranks / slowest rank's time); each step is
+  a CUDA-graph replay of the two calls; input sets rotate over enough independent copies that the
+  bytes touched between two uses of one copy exceed twice the L2 size.
+* e2e: the same metric through the public Python API with the step's per-call input (h, or the
+  tree inputs) copied from pinned host memory and the results copied back, synchronising each step.
+* roofline: the dominant kernel's algorithmic bytes (or flops) per launch over its CUDA-event
+  duration, from a second pass with per-kernel events on the launch stream.
+* cpu_baseline: the CPU oracle timed on host cores on a bounded sample of the same workload.
+* ``--impl reference``: the CPU oracle as the reference arm (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_decoding_draft_dh_gb300 import inputs  # noqa: E402
+
+METRIC = "draft-head rows/sec and µs per call (low-rank top-K + rescore); % of HBM roofline"
+TREE_METRIC = "tree-acceptance requests/sec and µs per call (per-node argmax + tree walk); % of HBM roofline"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200}
+DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    a = ap.parse_args()
+    if a.steps is None:
+        a.steps = DEFAULT_STEPS[a.workload]
+    if a.warmup is None:
+        a.warmup = DEFAULT_WARMUP[a.workload]
+    a.warmup = max(3, a.warmup)
+    return a
+
+
+# ------------------------------------------------------------------------------------------ env
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def dist_init(world, local):
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling in the background (every 50 ms)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={device_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.perf_counter(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        win = [s for t, s in self.samples if t0 - 0.1 <= t <= t1 + 0.1]
+        where = "timed region"
+        if len(win) < 2:
+            win = [s for _, s in self.samples]
+            where = "whole run (timed region shorter than the sampling interval)"
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in win if num(s[0]) is not None]
+        mx = [num(s[1]) for s in win if num(s[1]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in win for i in range(4)
+                          if len(s) > 4 + i and s[4 + i].lower().startswith("active")})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(win), "window": where,
+                "power_w_max": max([num(s[2]) for s in win if num(s[2]) is not None], default=None)}
+
+
+def kernel_source_digest(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "speculative_decoding_draft_dh_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profiles(kernel: str, workload: str, files):
+    """Per-launch DRAM bytes of `kernel` from the committed ncu summary, if the kernel source is
+    unchanged since it was taken."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        e = d.get(f"{workload}:{kernel}")
+        if e and e.get("source_digest") == kernel_source_digest(files):
+            return e.get("dram_bytes_per_launch")
+    except (ValueError, OSError):
+        return None
+    return None
+
+
+# ------------------------------------------------------------------------------------- head
+
+KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
+                "select": ["select.cu", "dh_internal.cuh"],
+                "rescore": ["rescore.cu", "dh_internal.cuh"],
+                "proj_partial": ["proj.cu", "dh_internal.cuh"],
+                "tree_argmax": ["tree.cu", "dh_internal.cuh"]}
+
+
+def head_bytes(cfg):
+    """Algorithmic HBM bytes of one call pair: U, V, h once and the B*K gathered rows of W."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    return {"U": cfg.d * cfg.r * e, "V": cfg.r * cfg.vocab * e, "h": cfg.B * cfg.d * e,
+            "W_rows": cfg.B * cfg.K * cfg.d * e}
+
+
+def kernel_algo(cfg, name):
+    """(bound, algorithmic bytes or flops per launch, unit) of a head kernel."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    if name == "scores_summary":
+        return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
+    if name in ("proj_partial",):
+        return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
+    if name == "rescore":
+        return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
+    if name == "select":
+        return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16, "GB/s"
+    return "hbm", 0, "GB/s"
+
+
+def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
+    from speculative_decoding_draft_dh_gb300 import binding as dh
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    hb = head_bytes(cfg)
+    per_step = sum(hb.values())
+    copies = max(2, min(8, math.ceil(2 * L2_BYTES / per_step)))
+    sets = []
+    for i in range(copies):
+        x = inputs.make_head(cfg, seed=a.seed + 1000 * rank + i, device=dev)
+        x["idx"] = torch.empty(cfg.B, cfg.K, dtype=torch.int32, device=dev)
+        x["score"] = torch.empty(cfg.B, cfg.K, dtype=torch.float32, device=dev)
+        x["logits"] = torch.empty(cfg.B, cfg.K, dtype=torch.float32, device=dev)
+        x["probs"] = torch.empty(cfg.B, cfg.K, dtype=torch.float32, device=dev)
+        sets.append(x)
+    ws = dh.Workspace()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(x):
+        dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, idx_out=x["idx"], score_out=x["score"],
+                        workspace=ws)
+        dh.exact_rescore(x["h"], x["W"], x["idx"], logits_out=x["logits"], probs_out=x["probs"],
+                         workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(a.warmup):
+            step(sets[i % copies])
+    torch.cuda.synchronize()
+    graphs = []
+    for x in sets:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            step(x)
+        graphs.append(g)
+    with torch.cuda.stream(stream):
+        for i in range(max(3, a.warmup)):
+            graphs[i % copies].replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    time.sleep(0.15)
+    with torch.cuda.stream(stream):
+        for i in range(min(a.warmup, 50)):
+            graphs[i % copies].replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for i in range(a.steps):
+            graphs[i % copies].replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    time.sleep(0.12)
+    sampler.stop()
+    ms = ev0.elapsed_time(ev1)
+    ms = max_over_ranks(ms, world)
+    us_per_call = ms * 1e3 / a.steps
+    value = cfg.B * a.steps * world / (ms / 1e3)
+
+    # per-kernel events on the launch stream (separate pass, eager launches)
+    n_prof = min(a.steps, 2000 if cfg.B <= 64 else 200)
+    dh.prof_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            step(sets[i % copies])
+    torch.cuda.synchronize()
+    dh.prof_enable(False)
+    prof = dh.prof_read()
+    stages = {k: {"us_avg": v[0] * 1e3 / v[1], "launches": v[1]} for k, v in prof.items()}
+    launches_per_step = sum(v[1] for v in prof.values()) / n_prof
+    dom = max(stages, key=lambda k: stages[k]["us_avg"])
+    bound, algo, unit = kernel_algo(cfg, dom)
+    dur_s = stages[dom]["us_avg"] * 1e-6
+    achieved = algo / dur_s / 1e9
+    peak = peaks["hbm_gbs"]
+    traffic = traffic_from_profiles(dom, cfg.name, KERNEL_FILES.get(dom, []))
+    roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak,
+                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "algorithmic_bytes_per_launch": algo, "us_per_launch": round(stages[dom]["us_avg"], 3),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+                else "fallback 6.8 TB/s"}
+    path_ach = per_step / (us_per_call * 1e-6) / 1e9
+    path_roofline = {"bound": "hbm", "bytes_per_call": per_step, "achieved": round(path_ach, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(path_ach / peak, 4),
+                     "ideal_us": round(per_step / (peak * 1e9) * 1e6, 3)}
+
+    # end to end through the public API with host buffers
+    e2e = None
+    if not a.no_e2e:
+        n_e2e = min(a.steps, 2000 if cfg.B <= 64 else 100)
+        hosts = [x["h"].cpu().pin_memory() for x in sets]
+        outs = [(torch.empty(cfg.B, cfg.K, dtype=torch.int32).pin_memory(),
+                 torch.empty(cfg.B, cfg.K, dtype=torch.float32).pin_memory(),
+                 torch.empty(cfg.B, cfg.K, dtype=torch.float32).pin_memory()) for _ in sets]
+        def e2e_step(i):
+            x = sets[i % copies]
+            with torch.cuda.stream(stream):
+                x["h"].copy_(hosts[i % copies], non_blocking=True)
+                step(x)
+                o = outs[i % copies]
+                o[0].copy_(x["idx"], non_blocking=True)
+                o[1].copy_(x["logits"], non_blocking=True)
+                o[2].copy_(x["probs"], non_blocking=True)
+            stream.synchronize()
+        for i in range(3):
+            e2e_step(i)
+        barrier(world)
+        te0 = time.perf_counter()
+        for i in range(n_e2e):
+            e2e_step(i)
+        te = max_over_ranks(time.perf_counter() - te0, world)
+        e2e = {"value": round(cfg.B * n_e2e * world / te, 2), "unit": "rows/s",
+               "us_per_call": round(te * 1e6 / n_e2e, 2), "steps": n_e2e,
+               "h2d_bytes_per_step": int(cfg.B * cfg.d * (2 if cfg.dtype == "bf16" else 4)),
+               "d2h_bytes_per_step": int(cfg.B * cfg.K * 12)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_head_baseline(cfg, sets[0], a.cpu_seconds)
+    clocks = sampler.summary(t0, t1)
+    return {
+        "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 6),
+        "us_per_call": round(us_per_call, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generators, random weights)",
+        "config": {"workload": cfg.name, "B": cfg.B, "d": cfg.d, "vocab": cfg.vocab, "r": cfg.r,
+                   "K": cfg.K, "seed": a.seed, "graph": "one CUDA graph per step",
+                   "l2": f"inputs rotate over {copies} independent copies "
+                         f"({copies * per_step / 2**20:.0f} MiB per cycle > 2x L2)",
+                   "parallelism": f"replicas x{world} (rows independent)"},
+        "roofline": roofline, "path_roofline": path_roofline, "stages": stages,
+        "gpu_launches": int(round(launches_per_step * a.steps)), "e2e": e2e,
+        "cpu_baseline": cpu, "clocks": clocks,
+    }
+
+
+def cpu_head_baseline(cfg, x, seconds):
+    import oracle
+    oracle.build()
+    hc, Uc, Vc, Wc = x["h"].cpu(), x["U"].cpu(), x["V"].cpu(), x["W"].cpu()
+    cores = len(os.sched_getaffinity(0))
+    rows_done = 0
+    t0 = time.perf_counter()
+    b = 0
+    while time.perf_counter() - t0 < seconds or rows_done == 0:
+        chunk = [(b + i) % cfg.B for i in range(min(cfg.B, cores))]
+        idx, _ = oracle.lowrank_topk(hc, Uc, Vc, cfg.K, rows=chunk)
+        full_idx = np.zeros((cfg.B, cfg.K), dtype=np.int32)
+        full_idx[chunk] = idx
+        oracle.exact_rescore(hc, Wc, full_idx, rows=chunk)
+        rows_done += len(chunk)
+        b += len(chunk)
+    dt = time.perf_counter() - t0
+    used = min(cfg.B, cores)
+    return {"value": round(rows_done / dt, 4), "unit": "rows/s", "cores": used, "kind": "oracle",
+            "sample": f"{rows_done} rows of the {cfg.name} workload (stage 1 + stage 2), "
+                      f"{dt:.1f} s, OpenMP over rows"}
+
+
+# ------------------------------------------------------------------------------------- tree
+
+def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
+    from speculative_decoding_draft_dh_gb300 import binding as dh
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    t = inputs.make_tree(tcfg, seed=a.seed + 1000 * rank, device=dev)
+    ws = dh.Workspace()
+    stream = torch.cuda.Stream(device=dev)
+    B, N, vocab = tcfg.B, tcfg.N, tcfg.vocab
+    elem = 2 if tcfg.dtype == "bf16" else 4
+    logit_bytes = B * N * vocab * elem
+
+    def step():
+        return dh.tree_accept(t["logits"], t["parent"], t["token"], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for _ in range(a.warmup):
+            step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        step()
+    sampler = ClockSampler(local)
+    time.sleep(0.15)
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            g.replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(a.steps):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    time.sleep(0.12)
+    sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    us = ms * 1e3 / a.steps
+    value = B * a.steps * world / (ms / 1e3)
+    n_prof = min(a.steps, 50)
+    dh.prof_enable(True)
+    with torch.cuda.stream(stream):
+        for _ in range(n_prof):
+            step()
+    torch.cuda.synchronize()
+    dh.prof_enable(False)
+    prof = dh.prof_read()
+    stages = {k: {"us_avg": v[0] * 1e3 / v[1], "launches": v[1]} for k, v in prof.items()}
+    dom = "tree_argmax"
+    achieved = logit_bytes / (stages[dom]["us_avg"] * 1e-6) / 1e9
+    peak = peaks["hbm_gbs"]
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": traffic_from_profiles(dom, tcfg.name, KERNEL_FILES[dom]),
+                "algorithmic_bytes_per_launch": logit_bytes,
+                "us_per_launch": round(stages[dom]["us_avg"], 3),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+    e2e = None
+    if not a.no_e2e:
+        n_e2e = min(a.steps, 10)
+        host = {k: t[k].cpu().pin_memory() for k in ("logits", "parent", "token")}
+        outs = {k: None for k in ("path", "len", "bonus")}
+        def e2e_step():
+            with torch.cuda.stream(stream):
+                for k in host:
+                    t[k].copy_(host[k], non_blocking=True)
+                o = step()
+                res = [o[k].to("cpu", non_blocking=True) for k in ("path", "len", "bonus")]
+            stream.synchronize()
+            return res
+        e2e_step()
+        te0 = time.perf_counter()
+        for _ in range(n_e2e):
+            e2e_step()
+        te = max_over_ranks(time.perf_counter() - te0, world)
+        e2e = {"value": round(B * n_e2e * world / te, 2), "unit": "requests/s",
+               "us_per_call": round(te * 1e6 / n_e2e, 1), "steps": n_e2e,
+               "h2d_bytes_per_step": int(logit_bytes + 2 * B * N * 4),
+               "d2h_bytes_per_step": int(B * N * 4 + 2 * B * 4)}
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_tree_baseline(tcfg, t, a.cpu_seconds)
+    return {
+        "metric": TREE_METRIC, "value": round(value, 2), "unit": "requests/s", "n_gpus": world,
+        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 6),
+        "us_per_call": round(us, 3), "node_rows_per_s": round(value * N, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": tcfg.dtype,
+        "data": "synthetic (seeded generators)",
+        "config": {"workload": tcfg.name, "B": B, "N": N, "vocab": vocab, "seed": a.seed,
+                   "graph": "one CUDA graph per step",
+                   "l2": f"logits {logit_bytes / 2**30:.2f} GiB per step > L2",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline, "stages": stages,
+        "gpu_launches": int(round(sum(v[1] for v in prof.values()) / n_prof * a.steps)),
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(t0, t1),
+    }
+
+
+def cpu_tree_baseline(tcfg, t, seconds):
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    n = min(tcfg.B, cores)
+    sl = t["logits"][:n].cpu()
+    pa, to = t["parent"][:n].cpu(), t["token"][:n].cpu()
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or done == 0:
+        oracle.tree_accept(sl, pa, to)
+        done += n
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 3), "unit": "requests/s", "cores": n, "kind": "oracle",
+            "sample": f"{done} requests (first {n} of the tree workload, repeated), {dt:.1f} s"}
+
+
+# -------------------------------------------------------------------------------- reference
+
+def run_reference(a, rank, world):
+    """The CPU oracle as the reference arm: bounded samples of the same workload on host cores."""
+    if rank != 0:
+        return None
+    budget = 60.0
+    if a.workload == "tree":
+        tcfg = inputs.TREE_CONFIGS["tree"]
+        small = inputs.tree_config("tree", B=min(16, tcfg.B))
+        t = inputs.make_tree(small, seed=a.seed, device="cpu")
+        import oracle
+        oracle.build()
+        cores = len(os.sched_getaffinity(0))
+        steps = 0
+        t0 = time.perf_counter()
+        while steps < a.steps and (time.perf_counter() - t0 < budget or steps == 0):
+            oracle.tree_accept(t["logits"], t["parent"], t["token"])
+            steps += 1
+        dt = time.perf_counter() - t0
+        value = small.B * steps / dt
+        unit, metric = "requests/s", TREE_METRIC
+        sample = f"{steps} steps of {small.B} requests of the tree workload (N=64, vocab=151936)"
+        cfgd = {"workload": "tree", "B": tcfg.B, "N": tcfg.N, "vocab": tcfg.vocab}
+        threads = min(small.B, cores)
+    else:
+        cfg = inputs.HEAD_CONFIGS[a.workload]
+        x = inputs.make_head(cfg, seed=a.seed, device="cuda" if torch.cuda.is_available() else "cpu")
+        x = {k: v.cpu() for k, v in x.items()}
+        import oracle
+        oracle.build()
+        cores = len(os.sched_getaffinity(0))
+        rows = list(range(min(cfg.B, cores)))
+        steps = 0
+        t0 = time.perf_counter()
+        while steps < a.steps and (time.perf_counter() - t0 < budget or steps == 0):
+            idx, _ = oracle.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, rows=rows)
+            full = np.zeros((cfg.B, cfg.K), dtype=np.int32)
+            full[rows] = idx
+            oracle.exact_rescore(x["h"], x["W"], full, rows=rows)
+            steps += 1
+        dt = time.perf_counter() - t0
+        value = len(rows) * steps / dt
+        unit, metric = "rows/s", METRIC
+        sample = f"{steps} steps of {len(rows)} rows of the {cfg.name} workload (stage 1 + stage 2)"
+        cfgd = {"workload": cfg.name, "B": cfg.B, "d": cfg.d, "vocab": cfg.vocab, "r": cfg.r, "K": cfg.K}
+        threads = len(rows)
+    return {"impl": "reference", "metric": metric, "value": round(value, 4), "unit": unit,
+            "n_gpus": world, "steps": steps, "warmup": 0, "ms_per_step": round(dt * 1e3 / steps, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded generators)", "config": cfgd,
+            "cpu_baseline": {"value": round(value, 4), "unit": unit, "kind": "oracle", "cores": threads,
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    a = parse_args()
+    rank, world, local = dist_env()
+    if a.impl == "reference":
+        line = run_reference(a, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    dist_init(world, local)
+    from speculative_decoding_draft_dh_gb300 import build
+    if rank == 0:
+        build.build()
+    barrier(world)
+    build.build()
+    peaks, src = load_peaks()
+    if a.workload == "tree":
+        line = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src)
+    else:
+        line = run_head_bench(a, inputs.HEAD_CONFIGS[a.workload], rank, world, local, peaks, src)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,160 @@
+/* dh.h - C ABI of the GB300 (sm_103a) two-stage draft LM head and greedy draft-tree acceptance.
+ *
+ * The method (EAGLE-4 summary page, yuxiaoba.github.io/tech/en/eagle-4, section "Retrieve
+ * vocabulary candidates cheaply, then score them exactly"): a low-rank head over the full
+ * vocabulary retrieves K candidates per row, and only those candidates are scored exactly with the
+ * original full-rank head.  Greedy acceptance (daily.dev "EAGLE-4 speeds up LLM inference with an
+ * adaptive speculative decoding drafter", section "How it works"): the target scores every drafted
+ * node in one pass, drafted tokens are kept while they equal the target's choice and the first
+ * mismatch is replaced by the target's own token.
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * - Pointers named as device pointers must point to device memory of the current CUDA device; the
+ *   caller owns every buffer.  The library allocates no device memory and keeps no per-call state
+ *   outside the caller's workspace.
+ * - `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).  Every call is
+ *   asynchronous on that stream: it returns after queuing its kernels and never synchronizes.
+ * - Arguments are validated on the host before anything is queued.  A rejected call returns a
+ *   non-zero dh_status and queues nothing.  A launch failure returns DH_ERR_CUDA.
+ * - Bad data that only the device can see (an index out of range, a parent array that is not a
+ *   tree) is reported in the outputs as documented per call; the kernels never trap.
+ * - dtype: DH_F32 (IEEE binary32) or DH_BF16 (bfloat16, stored as 16-bit words).  Arithmetic is
+ *   fp32 with fp32 accumulation for both.
+ * - Alignment: every tensor base pointer must be 16-byte aligned, and row lengths in bytes must be
+ *   multiples of 16 (bf16: d, r, vocab multiples of 8; fp32: multiples of 4).  Otherwise
+ *   DH_ERR_UNSUPPORTED.
+ * - Layouts are dense row-major with no padding between rows.
+ * - Workspace: caller-provided device memory of at least the size the matching *_workspace query
+ *   returns for the same arguments, 256-byte aligned.  Before its first use the workspace must be
+ *   zero-filled (for example with cudaMemset); every completed call leaves it ready for the next
+ *   call with the same or smaller arguments.  Calls that share a workspace must not overlap in
+ *   time (queue them on one stream).
+ */
+#ifndef DH_H
+#define DH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DH_OK = 0,
+  DH_ERR_INVALID_ARG = 1, /* null pointer, non-positive size, K outside [1, min(vocab, 1024)] */
+  DH_ERR_UNSUPPORTED = 2, /* alignment, dtype or a size above the documented limits          */
+  DH_ERR_WORKSPACE = 3,   /* workspace missing, too small or not 256-byte aligned            */
+  DH_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed                      */
+  DH_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up                     */
+  DH_ERR_BAD_INPUT = 6    /* per-row code written to err_out by dh_tree_accept                */
+} dh_status;
+
+typedef enum { DH_F32 = 0, DH_BF16 = 1 } dh_dtype;
+
+/* Limits checked on the host. */
+#define DH_MAX_K 1024
+#define DH_MAX_RANK 1024
+#define DH_MAX_VOCAB (1 << 21)
+#define DH_MAX_TREE_NODES 1024
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* dh_status_string(int status);
+
+/* Library version (major * 10000 + minor * 100 + patch). */
+int dh_version(void);
+
+/* ---------------------------------------------------------------------------------------------
+ * Stage 1: low-rank candidate retrieval.
+ *
+ * EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly"
+ * (the low-rank head selects candidates; its scores are not final probabilities); AlphaSignal
+ * "EAGLE-4 Triples Qwen3 Inference Speed by Adapting to Serving Load", section "Runtime-sized
+ * speculation" (low-rank candidate head: token prediction factored into smaller matrices).
+ *
+ * For every row b:
+ *   t[b,:]   = h[b,:] U                 (fp32 accumulation, then rounded to `dtype`, RNE)
+ *   s[b,v]   = t[b,:] V[:,v]            (fp32 accumulation) for every v in [0, vocab)
+ *   idx[b,:] = the K vocabulary ids with the largest s[b,v], ordered by (s desc, id asc)
+ *   score[b,k] = s[b, idx[b,k]]
+ * The B x vocab score matrix is never written to memory.
+ *
+ * h [B x d], U [d x r], V [r x vocab]: device, `dtype`.
+ * idx_out [B x K] int32, score_out [B x K] fp32: device.
+ * B = 0 is a no-op.  Limits: r <= DH_MAX_RANK, vocab <= DH_MAX_VOCAB, K <= min(vocab, DH_MAX_K).
+ * ------------------------------------------------------------------------------------------- */
+size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int K, int dtype);
+int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
+                    int K, int dtype, int32_t* idx_out, float* score_out, void* workspace,
+                    size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Stage 2: exact rescoring of the candidates with the full-rank head, and their softmax.
+ *
+ * EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly"
+ * (exact logits of the retrieved candidates from the original full-rank head); the products of
+ * these draft probabilities are the benefit estimate of section "Why a draft tree needs a cost
+ * model".  The softmax runs over the K candidates of a row at temperature 1.
+ *
+ *   logits[b,k] = h[b,:] . W[idx[b,k], :]   (fp32 accumulation)
+ *   probs[b,k]  = exp(logits[b,k] - m_b) / sum_k' exp(logits[b,k'] - m_b),  m_b = max_k logits[b,k]
+ *
+ * h [B x d], W [vocab x d]: device, `dtype`.  idx [B x K] int32: device.
+ * logits_out [B x K] fp32: device.  probs_out [B x K] fp32: device, may be NULL (no softmax).
+ * An index outside [0, vocab) is not dereferenced: its logit is NaN, which makes that row's
+ * probabilities NaN.  B = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+size_t dh_exact_rescore_workspace(int B, int d, int vocab, int K, int dtype);
+int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                     int dtype, float* logits_out, float* probs_out, void* workspace,
+                     size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Greedy draft-tree acceptance.
+ *
+ * daily.dev "EAGLE-4 speeds up LLM inference ...", section "How it works"; EAGLE-4 summary page,
+ * section "Distribution preservation has algorithmic and implementation conditions" (greedy
+ * decoding follows the target's choices); AlphaSignal page, section "Runtime-sized speculation"
+ * (top-k = 1 drafts a chain, larger k a tree).
+ *
+ * Node 0 of each request is the root (the last verified token; its token is ignored).  For node n
+ * the target's next-token logits after n are logits[b, n, :].
+ *   a[b,n]   = argmax_v logits[b,n,v]                      (ties -> lowest v, exact compare)
+ *   acc[0]   = 1;  acc[n] = acc[parent[n]] && token[n] == a[b, parent[n]]
+ *   last     = the accepted node of greatest depth          (ties -> lowest node index)
+ *   len[b]   = depth(last) = number of accepted draft tokens
+ *   path[b,:]= root .. last (len+1 node indices, root first), then -1
+ *   bonus[b] = a[b, last]   (the target's own token after the accepted path)
+ *
+ * logits [B x N x vocab]: device, `dtype`.  parent, token [B x N] int32: device; parent[0] = -1 and
+ * 0 <= parent[n] < n for n >= 1.
+ * argmax_out [B x N] int32 (may be NULL), path_out [B x N] int32, len_out [B] int32,
+ * bonus_out [B] int32, err_out [B] int32 (may be NULL): device.
+ * A request whose parent array breaks the rule gets len = -1, bonus = -1, an all -1 path and
+ * err = DH_ERR_BAD_INPUT (err = 0 otherwise).  N <= DH_MAX_TREE_NODES.  B = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+size_t dh_tree_accept_workspace(int B, int N, int vocab);
+int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* token, int B, int N,
+                   int vocab, int dtype, int32_t* argmax_out, int32_t* path_out, int32_t* len_out,
+                   int32_t* bonus_out, int32_t* err_out, void* workspace, size_t ws_bytes,
+                   void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Kernel timing for measurement (no counterpart on the pages).
+ *
+ * dh_prof_enable(1) makes every subsequent call record a CUDA event pair around each kernel it
+ * launches, on the caller's stream (this serialises the calls' kernels; do not enable it while a
+ * stream is being captured).  dh_prof_enable(0) stops recording.  dh_prof_read waits for the
+ * recorded events, and for up to max_kernels distinct kernels fills names (NUL-terminated, at most
+ * name_len bytes each, packed at stride name_len), total_ms and launches; it returns the number of
+ * distinct kernels (or -1 on a CUDA error) and clears the record.
+ * ------------------------------------------------------------------------------------------- */
+int dh_prof_enable(int on);
+int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int max_kernels);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DH_H */

@@ -1,0 +1,208 @@
+"""ctypes binding of libdh (include/dh.h).  Argument marshalling only: every step of the path runs
+in the CUDA library.  torch supplies device memory and the current stream.
+
+The library is loaded on first use from this package directory; if it is missing or cannot be
+loaded the call raises (there is no fallback).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libdh.so")
+
+DH_OK = 0
+STATUS = {0: "DH_OK", 1: "DH_ERR_INVALID_ARG", 2: "DH_ERR_UNSUPPORTED", 3: "DH_ERR_WORKSPACE",
+          4: "DH_ERR_CUDA", 5: "DH_ERR_TIMEOUT", 6: "DH_ERR_BAD_INPUT"}
+F32, BF16 = 0, 1
+
+EXPORTS = ["dh_status_string", "dh_version", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
+           "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
+           "dh_tree_accept", "dh_prof_enable", "dh_prof_read"]
+
+_lib = None
+_lock = threading.Lock()
+
+
+class DhError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load libdh.so and declare the C signatures (raises if the library is missing)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    with _lock:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"libdh.so not found at {p}: build it with "
+                               "`python -m speculative_decoding_draft_dh_gb300.build`")
+        lib = ctypes.CDLL(p)
+        P, I, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+        lib.dh_status_string.argtypes = [I]
+        lib.dh_status_string.restype = ctypes.c_char_p
+        lib.dh_version.restype = I
+        lib.dh_lowrank_topk_workspace.argtypes = [I, I, I, I, I, I]
+        lib.dh_lowrank_topk_workspace.restype = Z
+        lib.dh_lowrank_topk.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P]
+        lib.dh_lowrank_topk.restype = I
+        lib.dh_exact_rescore_workspace.argtypes = [I, I, I, I, I]
+        lib.dh_exact_rescore_workspace.restype = Z
+        lib.dh_exact_rescore.argtypes = [P, P, P, I, I, I, I, I, P, P, P, Z, P]
+        lib.dh_exact_rescore.restype = I
+        lib.dh_tree_accept_workspace.argtypes = [I, I, I]
+        lib.dh_tree_accept_workspace.restype = Z
+        lib.dh_tree_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
+        lib.dh_tree_accept.restype = I
+        lib.dh_prof_enable.argtypes = [I]
+        lib.dh_prof_enable.restype = I
+        lib.dh_prof_read.argtypes = [P, I, P, P, I]
+        lib.dh_prof_read.restype = I
+        if path is None:
+            _lib = lib
+        return lib
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _dev(t: torch.Tensor, name: str) -> torch.Tensor:
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Workspace:
+    """Zero-initialised device workspace, grown on demand (one per device and stream user)."""
+
+    def __init__(self):
+        self.buf = {}
+
+    def get(self, nbytes: int, device) -> torch.Tensor | None:
+        if nbytes == 0:
+            return None
+        key = torch.device(device)
+        cur = self.buf.get(key)
+        if cur is None or cur.numel() < nbytes:
+            cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=key)
+            self.buf[key] = cur
+        return cur
+
+
+_default_ws = Workspace()
+
+
+def _check(status, what):
+    if status != DH_OK:
+        raise DhError(status, what)
+
+
+def lowrank_topk(h, U, V, K, *, idx_out=None, score_out=None, workspace=None, stream=None):
+    """Stage 1: the K best low-rank scores per row.  Returns (idx int32 [B,K], score fp32 [B,K])."""
+    lib = load_library()
+    _dev(h, "h"), _dev(U, "U"), _dev(V, "V")
+    B, d = h.shape
+    r, vocab = V.shape
+    dt = _dtype_code(h)
+    if U.dtype != h.dtype or V.dtype != h.dtype or U.shape != (d, r):
+        raise ValueError("h, U, V must share a dtype and have shapes [B,d], [d,r], [r,vocab]")
+    if idx_out is None:
+        idx_out = torch.empty(B, K, dtype=torch.int32, device=h.device)
+    if score_out is None:
+        score_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    nbytes = lib.dh_lowrank_topk_workspace(B, d, r, vocab, K, dt)
+    ws = (workspace or _default_ws).get(nbytes, h.device)
+    _check(lib.dh_lowrank_topk(_ptr(h), _ptr(U), _ptr(V), B, d, r, vocab, K, dt, _ptr(idx_out),
+                               _ptr(score_out), _ptr(ws), nbytes, _stream(stream)), "dh_lowrank_topk")
+    return idx_out, score_out
+
+
+def exact_rescore(h, W, idx, *, with_probs=True, logits_out=None, probs_out=None, workspace=None,
+                  stream=None):
+    """Stage 2: exact logits of the candidates and (optionally) their softmax."""
+    lib = load_library()
+    _dev(h, "h"), _dev(W, "W"), _dev(idx, "idx")
+    B, d = h.shape
+    vocab = W.shape[0]
+    K = idx.shape[1]
+    dt = _dtype_code(h)
+    if W.dtype != h.dtype or W.shape[1] != d or idx.dtype != torch.int32 or idx.shape[0] != B:
+        raise ValueError("h [B,d], W [vocab,d] share a dtype; idx is int32 [B,K]")
+    if logits_out is None:
+        logits_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    if with_probs and probs_out is None:
+        probs_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    nbytes = lib.dh_exact_rescore_workspace(B, d, vocab, K, dt)
+    ws = (workspace or _default_ws).get(nbytes, h.device)
+    _check(lib.dh_exact_rescore(_ptr(h), _ptr(W), _ptr(idx), B, d, vocab, K, dt, _ptr(logits_out),
+                                _ptr(probs_out if with_probs else None), _ptr(ws), nbytes,
+                                _stream(stream)), "dh_exact_rescore")
+    return logits_out, (probs_out if with_probs else None)
+
+
+def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stream=None):
+    """Greedy acceptance over draft trees.  Returns dict(argmax, path, len, bonus, err)."""
+    lib = load_library()
+    _dev(logits, "logits"), _dev(parent, "parent"), _dev(token, "token")
+    B, N, vocab = logits.shape
+    dt = _dtype_code(logits)
+    if parent.dtype != torch.int32 or token.dtype != torch.int32 or parent.shape != (B, N) \
+            or token.shape != (B, N):
+        raise ValueError("parent and token must be int32 [B,N]")
+    dev = logits.device
+    out = {"argmax": torch.empty(B, N, dtype=torch.int32, device=dev) if with_argmax else None,
+           "path": torch.empty(B, N, dtype=torch.int32, device=dev),
+           "len": torch.empty(B, dtype=torch.int32, device=dev),
+           "bonus": torch.empty(B, dtype=torch.int32, device=dev),
+           "err": torch.empty(B, dtype=torch.int32, device=dev)}
+    nbytes = lib.dh_tree_accept_workspace(B, N, vocab)
+    ws = (workspace or _default_ws).get(nbytes, dev)
+    _check(lib.dh_tree_accept(_ptr(logits), _ptr(parent), _ptr(token), B, N, vocab, dt,
+                              _ptr(out["argmax"]), _ptr(out["path"]), _ptr(out["len"]),
+                              _ptr(out["bonus"]), _ptr(out["err"]), _ptr(ws), nbytes,
+                              _stream(stream)), "dh_tree_accept")
+    return out
+
+
+def prof_enable(on: bool):
+    load_library().dh_prof_enable(1 if on else 0)
+
+
+def prof_read(max_kernels: int = 64) -> dict:
+    """{kernel name: (total ms, launches)} recorded since the last read (waits for the events)."""
+    lib = load_library()
+    L = 64
+    names = ctypes.create_string_buffer(L * max_kernels)
+    tot = (ctypes.c_double * max_kernels)()
+    cnt = (ctypes.c_int * max_kernels)()
+    n = lib.dh_prof_read(names, L, tot, cnt, max_kernels)
+    if n < 0:
+        raise DhError(4, "dh_prof_read")
+    out = {}
+    for k in range(min(n, max_kernels)):
+        nm = names.raw[k * L:(k + 1) * L].split(b"\0", 1)[0].decode()
+        out[nm] = (tot[k], cnt[k])
+    return out

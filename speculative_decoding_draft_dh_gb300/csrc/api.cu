@@ -1,0 +1,233 @@
+// C ABI of libdh: argument validation, workspace layout and kernel sequencing (see include/dh.h).
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "dh_internal.cuh"
+
+namespace dh {
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+bool valid_dtype(int dt) { return dt == DH_F32 || dt == DH_BF16; }
+int elem_bytes(int dt) { return dt == DH_BF16 ? 2 : 4; }
+// row length in elements whose byte size is a multiple of 16
+bool row16(long long n, int dt) { return (n * elem_bytes(dt)) % 16 == 0; }
+
+// ---- workspace layouts (all offsets 256-byte aligned)
+
+struct TopkLayout {
+  size_t t, partial, recs, total;
+  int nsplit;
+};
+
+TopkLayout topk_layout(int B, int d, int r, int vocab) {
+  TopkLayout L;
+  Ctx dummy{0, 0, nullptr};
+  L.nsplit = proj_splits(dummy, B, d, r);
+  const size_t n_groups = (size_t)(vocab + GROUP - 1) / GROUP;
+  size_t off = 0;
+  L.t = off;
+  off = align_up(off + (size_t)B * r * 4, 256);
+  L.partial = off;
+  off = align_up(off + (size_t)L.nsplit * B * r * 4, 256);
+  L.recs = off;
+  off = align_up(off + (size_t)B * n_groups * sizeof(GroupRec), 256);
+  L.total = off;
+  return L;
+}
+
+// ---- profiling
+
+struct ProfRec {
+  const char* name;
+  cudaEvent_t a, b;
+};
+std::mutex g_prof_mu;
+bool g_prof = false;
+std::vector<ProfRec> g_prof_recs;
+
+}  // namespace
+
+bool get_ctx(void* stream, Ctx* ctx) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  ctx->device = dev;
+  ctx->stream = static_cast<cudaStream_t>(stream);
+  if (dev < kMaxDevices && g_sms[dev] > 0) {
+    ctx->num_sms = g_sms[dev];
+    return true;
+  }
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
+  if (dev < kMaxDevices) g_sms[dev] = sms;
+  ctx->num_sms = sms;
+  return true;
+}
+
+void prof_before(const char* name, cudaStream_t s) {
+  if (!g_prof) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  ProfRec r{name, nullptr, nullptr};
+  if (cudaEventCreate(&r.a) != cudaSuccess || cudaEventCreate(&r.b) != cudaSuccess) return;
+  cudaEventRecord(r.a, s);
+  g_prof_recs.push_back(r);
+}
+
+void prof_after(cudaStream_t s) {
+  if (!g_prof) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_recs.empty()) cudaEventRecord(g_prof_recs.back().b, s);
+}
+
+}  // namespace dh
+
+using namespace dh;
+
+extern "C" {
+
+const char* dh_status_string(int status) {
+  switch (status) {
+    case DH_OK: return "ok";
+    case DH_ERR_INVALID_ARG: return "invalid argument";
+    case DH_ERR_UNSUPPORTED: return "unsupported alignment, dtype or size";
+    case DH_ERR_WORKSPACE: return "workspace missing, too small or misaligned";
+    case DH_ERR_CUDA: return "CUDA error";
+    case DH_ERR_TIMEOUT: return "device-side wait timed out";
+    case DH_ERR_BAD_INPUT: return "bad input data";
+    default: return "unknown status";
+  }
+}
+
+int dh_version(void) { return 100; }
+
+// ------------------------------------------------------------------ stage 1
+
+size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int /*K*/, int /*dtype*/) {
+  if (B <= 0 || d <= 0 || r <= 0 || vocab <= 0) return 0;
+  return topk_layout(B, d, r, vocab).total;
+}
+
+int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
+                    int dtype, int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  if (B < 0 || d <= 0 || r <= 0 || vocab <= 0) return DH_ERR_INVALID_ARG;
+  if (K < 1 || K > vocab || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!h || !U || !V || !idx_out || !score_out) return DH_ERR_INVALID_ARG;
+  if (r > DH_MAX_RANK || vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(U) || !aligned16(V)) return DH_ERR_UNSUPPORTED;
+  if (!row16(d, dtype) || !row16(r, dtype) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
+  const TopkLayout L = topk_layout(B, d, r, vocab);
+  if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  void* t = ws + L.t;
+  float* partial = reinterpret_cast<float*>(ws + L.partial);
+  GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
+  if (launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t) != cudaSuccess) return DH_ERR_CUDA;
+  if (launch_scores_summary(c, t, V, B, r, vocab, dtype, recs) != cudaSuccess) return DH_ERR_CUDA;
+  if (launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out) != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ stage 2
+
+size_t dh_exact_rescore_workspace(int, int, int, int, int) { return 0; }
+
+int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                     int dtype, float* logits_out, float* probs_out, void* workspace, size_t ws_bytes,
+                     void* stream) {
+  (void)workspace;
+  (void)ws_bytes;
+  if (B < 0 || d <= 0 || vocab <= 0 || K < 1 || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!h || !W || !idx || !logits_out) return DH_ERR_INVALID_ARG;
+  if (vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(W) || !row16(d, dtype)) return DH_ERR_UNSUPPORTED;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out) != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ tree acceptance
+
+size_t dh_tree_accept_workspace(int B, int N, int /*vocab*/) {
+  if (B <= 0 || N <= 0) return 0;
+  return align_up((size_t)B * N * sizeof(int32_t), 256);
+}
+
+int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* token, int B, int N, int vocab,
+                   int dtype, int32_t* argmax_out, int32_t* path_out, int32_t* len_out, int32_t* bonus_out,
+                   int32_t* err_out, void* workspace, size_t ws_bytes, void* stream) {
+  if (B < 0 || N <= 0 || vocab <= 0) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!logits || !parent || !token || !path_out || !len_out || !bonus_out) return DH_ERR_INVALID_ARG;
+  if (N > DH_MAX_TREE_NODES || (long long)B * N > 0x7FFFFFFFLL) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(logits) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
+  const size_t need = dh_tree_accept_workspace(B, N, vocab);
+  if (!workspace || !aligned256(workspace) || ws_bytes < need) return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (launch_tree(c, logits, parent, token, B, N, vocab, dtype, static_cast<int32_t*>(workspace), argmax_out,
+                  path_out, len_out, bonus_out, err_out) != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ profiling
+
+int dh_prof_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof = on != 0;
+  return DH_OK;
+}
+
+int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int max_kernels) {
+  std::vector<ProfRec> recs;
+  {
+    std::lock_guard<std::mutex> lk(g_prof_mu);
+    recs.swap(g_prof_recs);
+  }
+  std::vector<std::string> keys;
+  std::vector<double> tot;
+  std::vector<int> cnt;
+  int rc = 0;
+  for (auto& r : recs) {
+    float ms = 0.f;
+    if (cudaEventSynchronize(r.b) != cudaSuccess || cudaEventElapsedTime(&ms, r.a, r.b) != cudaSuccess) rc = -1;
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+    size_t k = 0;
+    while (k < keys.size() && keys[k] != r.name) ++k;
+    if (k == keys.size()) { keys.push_back(r.name); tot.push_back(0.0); cnt.push_back(0); }
+    tot[k] += ms;
+    cnt[k] += 1;
+  }
+  if (rc) return -1;
+  const int n = (int)keys.size();
+  for (int k = 0; k < n && k < max_kernels; ++k) {
+    if (names && name_len > 0) {
+      std::string s = keys[k].substr(0, (size_t)name_len - 1);
+      std::copy(s.begin(), s.end(), names + (size_t)k * name_len);
+      names[(size_t)k * name_len + s.size()] = '\0';
+    }
+    if (total_ms) total_ms[k] = tot[k];
+    if (launches) launches[k] = cnt[k];
+  }
+  return n;
+}
+
+}  // extern "C"

@@ -1,0 +1,175 @@
+// Internal declarations shared by the CUDA translation units of libdh (not part of the ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dh.h"
+
+namespace dh {
+
+// Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
+// ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
+// third-best score.  The selection step works from these records; the full score row never
+// reaches memory.
+constexpr int GROUP = 64;
+constexpr uint32_t NO_OFFSET = 0xFFu;
+
+struct __align__(16) GroupRec {
+  float m1, m2, m3;  // best, second and third score in the group (-inf when absent)
+  uint32_t offs;     // offset in group of the best (bits 0-7) and the second (bits 8-15); 0xFF = absent
+};
+
+// ------------------------------------------------------------------ numeric helpers
+
+// Order-preserving map of a float onto uint32 (larger float -> larger key).  -0 is folded onto
+// +0 so that keys agree with float equality.
+__device__ __forceinline__ uint32_t fkey(float x) {
+  uint32_t u = __float_as_uint(x);
+  if (u == 0x80000000u) u = 0u;
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float fkey_inv(uint32_t k) {
+  uint32_t u = (k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k;
+  return __uint_as_float(u);
+}
+
+// (a_val, a_id) ranks before (b_val, b_id) in (score desc, id asc) order.
+__device__ __forceinline__ bool ranks_before(float av, uint32_t ai, float bv, uint32_t bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// Running summary of a stream of (score, id) pairs: the top two pairs and the third score.
+struct Top2 {
+  float v1, v2, v3;
+  uint32_t i1, i2;
+  __device__ __forceinline__ void init() {
+    v1 = v2 = v3 = -INFINITY;
+    i1 = i2 = 0xFFFFFFFFu;
+  }
+  // Pairs must arrive in increasing id order for ties to keep the lower id.
+  __device__ __forceinline__ void push(float x, uint32_t id) {
+    if (x > v1) {
+      v3 = v2; v2 = v1; i2 = i1; v1 = x; i1 = id;
+    } else if (x > v2) {
+      v3 = v2; v2 = x; i2 = id;
+    } else if (x > v3) {
+      v3 = x;
+    }
+  }
+  // Merge with another summary of a disjoint set of ids.
+  __device__ __forceinline__ void merge(float bv1, uint32_t bi1, float bv2, uint32_t bi2, float bv3) {
+    // the four known pairs sorted by (score desc, id asc): a1 >= a2 and b1 >= b2 already hold
+    float w1, w2, x3;
+    uint32_t j1, j2;
+    if (ranks_before(v1, i1, bv1, bi1)) {
+      w1 = v1; j1 = i1;
+      if (ranks_before(v2, i2, bv1, bi1)) { w2 = v2; j2 = i2; x3 = fmaxf(v3, bv1); }
+      else { w2 = bv1; j2 = bi1; x3 = fmaxf(v2, bv2); }
+    } else {
+      w1 = bv1; j1 = bi1;
+      if (ranks_before(v1, i1, bv2, bi2)) { w2 = v1; j2 = i1; x3 = fmaxf(v2, bv2); }
+      else { w2 = bv2; j2 = bi2; x3 = fmaxf(v1, bv3); }
+    }
+    x3 = fmaxf(x3, fmaxf(v3, bv3));
+    v1 = w1; i1 = j1; v2 = w2; i2 = j2; v3 = x3;
+  }
+  __device__ __forceinline__ void merge_shfl(unsigned mask, int lane_xor) {
+    float bv1 = __shfl_xor_sync(mask, v1, lane_xor);
+    float bv2 = __shfl_xor_sync(mask, v2, lane_xor);
+    float bv3 = __shfl_xor_sync(mask, v3, lane_xor);
+    uint32_t bi1 = __shfl_xor_sync(mask, i1, lane_xor);
+    uint32_t bi2 = __shfl_xor_sync(mask, i2, lane_xor);
+    merge(bv1, bi1, bv2, bi2, bv3);
+  }
+  // Record for the group starting at id g0.
+  __device__ __forceinline__ GroupRec record(uint32_t g0) const {
+    GroupRec r;
+    r.m1 = v1; r.m2 = v2; r.m3 = v3;
+    uint32_t o1 = (i1 == 0xFFFFFFFFu) ? NO_OFFSET : (i1 - g0);
+    uint32_t o2 = (i2 == 0xFFFFFFFFu) ? NO_OFFSET : (i2 - g0);
+    r.offs = o1 | (o2 << 8);
+    return r;
+  }
+};
+
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+  static constexpr int PER16 = 4;  // elements per 16-byte vector
+  __device__ __forceinline__ static void unpack(const uint4& u, float* out) {
+    out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
+    out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
+  }
+  __device__ __forceinline__ static float to_f(float x) { return x; }
+  __device__ __forceinline__ static float from_f(float x) { return x; }
+};
+template <> struct Elem<__nv_bfloat16> {
+  static constexpr int PER16 = 8;
+  __device__ __forceinline__ static void unpack(const uint4& u, float* out) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      out[2 * q] = __uint_as_float(w[q] << 16);
+      out[2 * q + 1] = __uint_as_float(w[q] & 0xFFFF0000u);
+    }
+  }
+  __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
+  __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+};
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// ------------------------------------------------------------------ host side
+
+struct Ctx {
+  int device;
+  int num_sms;
+  cudaStream_t stream;
+};
+
+bool get_ctx(void* stream, Ctx* ctx);
+
+// Kernel-launch bookkeeping for dh_prof_*: call before and after a launch.
+void prof_before(const char* name, cudaStream_t s);
+void prof_after(cudaStream_t s);
+
+// Launchers (one per translation unit).  All return cudaError_t of the launch.
+cudaError_t launch_proj(const Ctx& c, const void* h, const void* U, int B, int d, int r, int dtype,
+                        float* partial, int nsplit, void* t_out);
+int proj_splits(const Ctx& c, int B, int d, int r);
+
+cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
+                                  int dtype, GroupRec* recs);
+
+cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, const void* V, int B,
+                          int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out);
+
+cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
+                           int d, int vocab, int K, int dtype, float* logits, float* probs);
+
+cudaError_t launch_tree(const Ctx& c, const void* logits, const int32_t* parent, const int32_t* token,
+                        int B, int N, int vocab, int dtype, int32_t* argmax_ws, int32_t* argmax_out,
+                        int32_t* path, int32_t* len, int32_t* bonus, int32_t* err);
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Raises a kernel's dynamic shared memory limit to the device maximum, once per device (a plain
+// attribute call, so it is also safe while a stream is being captured).
+template <class Kernel>
+cudaError_t allow_max_smem(Kernel kernel, int device, unsigned long long* done_mask) {
+  if (device < 64 && ((*done_mask >> device) & 1ull)) return cudaSuccess;
+  int maxopt = 0;
+  cudaError_t e = cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxopt);
+  if (e == cudaSuccess && device < 64) *done_mask |= 1ull << device;
+  return e;
+}
+
+}  // namespace dh

@@ -1,0 +1,101 @@
+"""CPU-side checks of the C ABI: the library loads, exports every function that include/dh.h
+declares, sizes workspaces, and rejects bad arguments on the host before touching a device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_draft_dh_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "dh.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(dh_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_three_calls():
+    fns = declared_functions()
+    for name in ("dh_lowrank_topk", "dh_exact_rescore", "dh_tree_accept"):
+        assert name in fns
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [f for f in declared_functions() if not hasattr(lib, f)]
+    assert not missing, missing
+    assert sorted(binding.EXPORTS) == sorted(declared_functions())
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert lib.dh_status_string(code)
+    assert lib.dh_status_string(99) == b"unknown status"
+    assert lib.dh_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    # batch-1 draft head: t, projection partials and one 16-byte record per group of 64 ids
+    ws = lib.dh_lowrank_topk_workspace(1, 5120, 128, 151936, 64, binding.BF16)
+    assert ws >= 151936 // 64 * 16
+    assert ws % 256 == 0
+    big = lib.dh_lowrank_topk_workspace(512, 5120, 512, 151936, 256, binding.BF16)
+    assert big >= 512 * (151936 // 64) * 16
+    assert lib.dh_lowrank_topk_workspace(0, 5120, 128, 151936, 64, binding.BF16) == 0
+    assert lib.dh_tree_accept_workspace(256, 64, 151936) >= 256 * 64 * 4
+
+
+FAKE = 0x10000  # 16-byte aligned host-side stand-in; never dereferenced by rejected calls
+
+
+def _topk(lib, B=1, d=256, r=32, vocab=4096, K=16, dt=binding.F32, h=FAKE, U=FAKE, V=FAKE,
+          idx=FAKE, sc=FAKE, ws=FAKE * 16, nbytes=1 << 30):
+    P = ctypes.c_void_p
+    return lib.dh_lowrank_topk(P(h), P(U), P(V), B, d, r, vocab, K, dt, P(idx), P(sc), P(ws), nbytes,
+                               None)
+
+
+def test_topk_rejects_bad_arguments_on_host(lib):
+    assert _topk(lib, K=0) == 1
+    assert _topk(lib, K=4097) == 1                      # K > vocab
+    assert _topk(lib, vocab=8192, K=1025) == 1          # K > 1024
+    assert _topk(lib, d=0) == 1
+    assert _topk(lib, h=0) == 1                         # null pointer
+    assert _topk(lib, dt=7) == 2                        # unknown dtype
+    assert _topk(lib, h=FAKE + 4) == 2                  # misaligned base pointer
+    assert _topk(lib, dt=binding.BF16, r=36) == 2       # bf16 row of 72 bytes
+    assert _topk(lib, r=2048) == 2                      # above the rank limit
+    assert _topk(lib, ws=0) == 3
+    assert _topk(lib, ws=FAKE * 16 + 16) == 3           # workspace not 256-byte aligned
+    assert _topk(lib, nbytes=64) == 3                   # workspace too small
+    assert _topk(lib, B=0) == 0                         # empty batch: nothing to do
+
+
+def test_rescore_and_tree_reject_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    assert lib.dh_exact_rescore(P(FAKE), P(FAKE), P(FAKE), 1, 256, 4096, 0, 0, P(FAKE), None, None, 0,
+                                None) == 1
+    assert lib.dh_exact_rescore(P(FAKE), P(FAKE), P(FAKE), 1, 250, 4096, 4, 0, P(FAKE), None, None, 0,
+                                None) == 2
+    assert lib.dh_exact_rescore(P(FAKE), P(FAKE), P(FAKE), 0, 256, 4096, 4, 0, P(FAKE), None, None, 0,
+                                None) == 0
+    assert lib.dh_tree_accept(P(FAKE), P(FAKE), P(FAKE), 1, 2048, 4096, 0, None, P(FAKE), P(FAKE),
+                              P(FAKE), None, P(FAKE * 16), 1 << 20, None) == 2  # N above limit
+    assert lib.dh_tree_accept(P(FAKE), P(FAKE), P(FAKE), 1, 8, 4096, 0, None, None, P(FAKE),
+                              P(FAKE), None, P(FAKE * 16), 1 << 20, None) == 1  # path_out missing
+    assert lib.dh_tree_accept(P(FAKE), P(FAKE), P(FAKE), 4, 8, 4096, 0, None, P(FAKE), P(FAKE),
+                              P(FAKE), None, P(FAKE * 16), 8, None) == 3        # workspace too small
+
+
+def test_binding_fails_loudly_without_library(tmp_path):
+    with pytest.raises(RuntimeError, match="libdh.so not found"):
+        binding.load_library(str(tmp_path / "libdh.so"))

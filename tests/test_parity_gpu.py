@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on the same seeded
+inputs.  Small shapes are compared row by row in full; the full-size workloads are compared on
+sampled rows that the oracle computes one by one, plus properties checked on every row."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_decoding_draft_dh_gb300 import binding as dh
+from speculative_decoding_draft_dh_gb300 import inputs
+from tests.parity import check_candidates, check_logits
+from tests.test_oracle_pins import golden_tree_arrays, load_golden_trees
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from speculative_decoding_draft_dh_gb300 import build
+    build.build()
+    dh.load_library()
+    yield
+    torch.cuda.synchronize()
+
+
+def run_head(x, K, rows=None):
+    """GPU stage 1 + stage 2 on device tensors; oracle on the listed rows.  Returns stats."""
+    h, U, V, W = x["h"], x["U"], x["V"], x["W"]
+    idx, score = dh.lowrank_topk(h, U, V, K)
+    logits, probs = dh.exact_rescore(h, W, idx)
+    torch.cuda.synchronize()
+    B = h.shape[0]
+    rows = list(range(B)) if rows is None else rows
+    hc, Uc, Vc = h.cpu(), U.cpu(), V.cpu()
+    s_full = oracle.lowrank_scores(hc, Uc, Vc, rows=rows)
+    gi, gs = idx.cpu().numpy(), score.cpu().numpy()
+    for n, b in enumerate(rows):
+        check_candidates(gi[b], gs[b], s_full[n], K, where=f"row {b}")
+    # stage 2 on the same ids: the oracle rescoring the GPU's own candidates
+    Wc = W.cpu()
+    oz, op = oracle.exact_rescore(hc, Wc, idx.cpu(), rows=rows)
+    gl, gp = logits.cpu().numpy(), probs.cpu().numpy()
+    for n, b in enumerate(rows):
+        check_logits(gl[b], gp[b], oz[n], op[n], where=f"row {b}")
+    # properties on every row
+    assert np.all((gi >= 0) & (gi < V.shape[1]))
+    assert np.all(np.diff(gs, axis=1) <= 0)
+    np.testing.assert_allclose(gp.sum(axis=1), 1.0, atol=1e-4)
+    return idx, score, logits, probs
+
+
+# ---------------------------------------------------------------- small shapes, every row
+
+@pytest.mark.parametrize("B", [1, 2, 3, 4])
+def test_tiny_head(B):
+    cfg = inputs.head_config("tiny", B=B)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K)
+
+
+MID = inputs.HeadConfig("mid_bf16", 5, 512, 8200, 64, 32, "bf16", 0.1, True)  # ragged vocab tail
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_mid_bf16_ragged_vocab(seed):
+    x = inputs.make_head(MID, seed=seed, device=DEV)
+    run_head(x, MID.K)
+
+
+@pytest.mark.parametrize("K", [1, 7, 64, 1000, 1024])
+def test_tiny_head_K_range(K):
+    cfg = inputs.head_config("tiny", B=2, K=K)
+    x = inputs.make_head(cfg, seed=3, device=DEV)
+    run_head(x, K)
+
+
+def test_K_equals_vocab_uses_exact_fallback():
+    cfg = inputs.HeadConfig("k_eq_vocab", 2, 256, 1024, 32, 1024, "f32", 0.05, False)
+    x = inputs.make_head(cfg, seed=4, device=DEV)
+    idx, _, _, probs = run_head(x, cfg.K)
+    assert sorted(idx[0].cpu().tolist()) == list(range(1024))
+
+
+def _best_column(x):
+    s = oracle.lowrank_scores(x["h"][:1].cpu(), x["U"].cpu(), x["V"].cpu())[0]
+    return int(np.argmax(s))
+
+
+def test_clustered_candidates_are_refined():
+    """All top candidates inside one group of 64 ids: the group's third score reaches the
+    candidate threshold and the group is re-scored exactly."""
+    cfg = inputs.head_config("tiny", B=1, K=16)
+    x = inputs.make_head(cfg, seed=5, device=DEV)
+    v = _best_column(x)
+    base = x["V"][:, v].clone()
+    for j in range(64):
+        x["V"][:, 128 + j] = base * (1.0 + 0.01 * j)
+    run_head(x, cfg.K)
+
+
+def test_many_clustered_groups_use_full_rescan():
+    cfg = inputs.head_config("tiny", B=1, K=128)
+    x = inputs.make_head(cfg, seed=6, device=DEV)
+    v = _best_column(x)
+    base = x["V"][:, v].clone()
+    for g in range(40):
+        for q in range(3):
+            x["V"][:, 64 * g + q] = base * (2.0 + 0.001 * (3 * g + q))
+    run_head(x, cfg.K)
+
+
+def test_equal_scores_resolve_to_lowest_id():
+    cfg = inputs.head_config("tiny", B=1, K=16)
+    x = inputs.make_head(cfg, seed=7, device=DEV)
+    v = _best_column(x)
+    col = x["V"][:, v].clone() * 3.0
+    for c in (4000, 17, 2222, 640):
+        x["V"][:, c] = col
+    idx, score, _, _ = run_head(x, cfg.K)
+    assert idx[0, :4].cpu().tolist() == [17, 640, 2222, 4000]
+    assert len(set(score[0, :4].cpu().tolist())) == 1
+
+
+def test_empty_batch_is_a_noop():
+    cfg = inputs.head_config("tiny", B=1)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    h0 = x["h"][:0]
+    idx, score = dh.lowrank_topk(h0, x["U"], x["V"], cfg.K)
+    assert idx.shape == (0, cfg.K)
+    logits, probs = dh.exact_rescore(h0, x["W"], idx)
+    assert logits.shape == (0, cfg.K)
+
+
+def test_rescore_bad_index_gives_nan_row():
+    cfg = inputs.head_config("tiny", B=3)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    idx[1, 5] = cfg.vocab + 10
+    idx[2, 0] = -1
+    logits, probs = dh.exact_rescore(x["h"], x["W"], idx)
+    lg, pr = logits.cpu().numpy(), probs.cpu().numpy()
+    assert np.isnan(lg[1, 5]) and np.isnan(lg[2, 0])
+    assert np.isnan(pr[1]).all() and np.isnan(pr[2]).all()
+    assert np.isfinite(lg[0]).all() and np.isfinite(pr[0]).all()
+
+
+def test_rescore_without_probs():
+    cfg = inputs.head_config("tiny", B=2)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    logits, probs = dh.exact_rescore(x["h"], x["W"], idx, with_probs=False)
+    assert probs is None
+    oz, _ = oracle.exact_rescore(x["h"].cpu(), x["W"].cpu(), idx.cpu())
+    check_logits(logits.cpu().numpy(), None, oz, None)
+
+
+# ---------------------------------------------------------------- full-size workloads
+
+def test_batch1_full_size():
+    cfg = inputs.HEAD_CONFIGS["batch1"]
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K)
+
+
+def test_moderate_load_sampled_rows():
+    cfg = inputs.HEAD_CONFIGS["moderate"]
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K, rows=[0, 1, 17, 42, 63])
+
+
+def test_high_load_sampled_rows():
+    cfg = inputs.HEAD_CONFIGS["high"]
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K, rows=[0, 255, 511])
+
+
+# ---------------------------------------------------------------- trees
+
+def run_tree(t, reqs=None):
+    out = dh.tree_accept(t["logits"], t["parent"], t["token"])
+    torch.cuda.synchronize()
+    B = t["parent"].shape[0]
+    reqs = list(range(B)) if reqs is None else reqs
+    sel = torch.tensor(reqs)
+    o = oracle.tree_accept(t["logits"][sel.to(t["logits"].device)].cpu(), t["parent"][sel.to(DEV)].cpu(),
+                           t["token"][sel.to(DEV)].cpu())
+    g = {k: v.cpu().numpy() for k, v in out.items()}
+    np.testing.assert_array_equal(g["argmax"][reqs], o["argmax"])
+    np.testing.assert_array_equal(g["path"][reqs], o["path"])
+    np.testing.assert_array_equal(g["len"][reqs], o["len"])
+    np.testing.assert_array_equal(g["bonus"][reqs], o["bonus"])
+    # properties on every request
+    par = t["parent"].cpu().numpy()
+    for b in range(B):
+        L = g["len"][b]
+        assert g["err"][b] == 0 and L >= 0
+        p = g["path"][b]
+        assert p[0] == 0 and np.all(p[L + 1:] == -1)
+        for j in range(1, L + 1):
+            assert par[b, p[j]] == p[j - 1]
+        assert g["bonus"][b] == g["argmax"][b, p[L]]
+    return g
+
+
+def test_tiny_trees():
+    t = inputs.make_tree(inputs.TREE_CONFIGS["tiny_tree"], seed=0, device=DEV)
+    run_tree(t)
+
+
+@pytest.mark.parametrize("case", load_golden_trees(), ids=lambda c: c["name"])
+def test_golden_trees_on_gpu(case):
+    logits, parent, token = golden_tree_arrays(case)
+    # pad the vocabulary to a multiple of 4 fp32 values (16 bytes); padding never wins the argmax
+    out = dh.tree_accept(torch.from_numpy(logits).to(DEV), torch.from_numpy(parent).to(DEV),
+                         torch.from_numpy(token).to(DEV))
+    torch.cuda.synchronize()
+    N = parent.shape[1]
+    assert out["len"][0].item() == case["expect_len"][0]
+    assert out["bonus"][0].item() == case["expect_bonus"][0]
+    want = case["expect_path"] + [-1] * (N - len(case["expect_path"]))
+    assert out["path"][0].cpu().tolist() == want
+    assert out["err"][0].item() == (6 if case["expect_len"][0] < 0 else 0)
+
+
+def test_tree_bf16_ties_and_single_node():
+    tcfg = inputs.tree_config("tree", B=3, N=1, vocab=4096)
+    t = inputs.make_tree(tcfg, seed=2, device=DEV)
+    t["logits"][1, 0, :] = 0.5  # all equal: argmax is id 0
+    g = run_tree(t)
+    assert g["argmax"][1, 0] == 0 and g["len"].tolist() == [0, 0, 0]
+
+
+def test_tree_full_size_sampled():
+    t = inputs.make_tree(inputs.TREE_CONFIGS["tree"], seed=0, device=DEV)
+    g = run_tree(t, reqs=[0, 1, 100, 200, 255])
+    assert g["len"].mean() > 0.5
