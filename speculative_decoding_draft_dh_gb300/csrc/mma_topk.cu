@@ -1,0 +1,277 @@
+// Stage 1b (tensor-core path, bf16, B >= a few rows): S = T V on tcgen05 with the accumulator in
+// TMEM and a fused epilogue that folds every group of 64 vocabulary ids into a GroupRec, so the
+// B x vocab score matrix never reaches memory.
+//
+// EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
+// the low-rank head scores the whole vocabulary to retrieve candidates.  At high load the product
+// T [B x r] V [r x vocab] is a dense contraction (B*r flop per V byte), so it runs on the tensor
+// cores; the selection that follows is shared with the CUDA-core path.
+//
+// One CTA per SM owns a 128-row tile of T (kept resident in shared memory, r/64 TMA boxes of
+// 128 x 64 bf16 with 128-byte swizzle) and a contiguous range of 256-wide vocabulary tiles.
+// Warp roles:
+//   warp 0     TMA producer: streams V in stages of 64 (K) x 256 (N) bf16 (four 64 x 64 boxes).
+//   warp 1     TMEM allocator and MMA issuer: per vocabulary tile, r/16 tcgen05.mma
+//              (M=128, N=256, K=16, A K-major, B N-major) into one of two TMEM accumulators.
+//   warps 2-5  epilogue: tcgen05.ld 32x32b (thread = row), per-group top-two + third score,
+//              one 16-byte record store per (row, group).
+// Every mbarrier wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word;
+// the CTA then drains its outstanding copies and MMAs (again with bounded waits) and frees TMEM.
+#include "dh_internal.cuh"
+#include "sm100.cuh"
+
+namespace dh {
+namespace {
+
+using namespace sm100;
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int A_CHUNK_BYTES = BM * BK * 2;  // 16 KB: 128 rows x 128 bytes
+constexpr int B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 ids
+constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;
+constexpr int THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;  // two 128 x 256 fp32 accumulators
+constexpr uint64_t WAIT_NS = 2000000000ull;
+constexpr int MAX_STAGES = 8;
+
+struct MmaParams {
+  int B, r, vocab, n_groups, n_tiles, n_split, stages;
+  GroupRec* recs;
+  int* status;
+};
+
+__device__ __forceinline__ void raise_timeout(volatile int* s_abort, int* status) {
+  *s_abort = 1;
+  atomicOr(status, 1 << DH_ERR_TIMEOUT);
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_lowrank_mma(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, MmaParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[2 + 2 * MAX_STAGES + 4];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int s_abort;
+
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const int nkc = p.r / BK;
+  unsigned char* sA = base;
+  unsigned char* sB = sA + nkc * A_CHUNK_BYTES;
+  uint64_t* a_full = &bars[0];
+  uint64_t* drain = &bars[1];
+  uint64_t* b_full = &bars[2];
+  uint64_t* b_empty = &bars[2 + MAX_STAGES];
+  uint64_t* acc_full = &bars[2 + 2 * MAX_STAGES];
+  uint64_t* acc_empty = &bars[2 + 2 * MAX_STAGES + 2];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m = blockIdx.x / p.n_split, part = blockIdx.x % p.n_split;
+  const int nt0 = (int)((long long)p.n_tiles * part / p.n_split);
+  const int nt1 = (int)((long long)p.n_tiles * (part + 1) / p.n_split);
+  const int ntiles = nt1 - nt0;
+  const int stages = p.stages;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    mbar_init(a_full, 1);
+    mbar_init(drain, 1);
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&b_full[s], 1);
+      mbar_init(&b_empty[s], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 1);
+      mbar_init(&acc_empty[i], 4);
+    }
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ TMA producer
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      mbar_arrive_expect_tx(a_full, (uint32_t)(nkc * A_CHUNK_BYTES));
+      for (int kc = 0; kc < nkc; ++kc) tma_load_2d(sA + kc * A_CHUNK_BYTES, &tmA, kc * BK, m * BM, a_full);
+      uint32_t issued_parity = 0;  // bit s: parity of the last load issued into stage s
+      uint32_t issued_mask = 0;
+      int s = 0;
+      uint32_t ph = 0;
+      for (int t = 0; t < ntiles && !s_abort; ++t) {
+        const int n0 = (nt0 + t) * BN;
+        for (int kc = 0; kc < nkc; ++kc) {
+          if (!mbar_wait(&b_empty[s], ph ^ 1u, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
+          mbar_arrive_expect_tx(&b_full[s], B_STAGE_BYTES);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            tma_load_2d(sB + s * B_STAGE_BYTES + q * B_BOX_BYTES, &tmB, n0 + q * 64, kc * BK, &b_full[s]);
+          issued_mask |= 1u << s;
+          issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+      }
+      // every copy this CTA issued must land before the CTA can exit
+      mbar_wait(a_full, 0, WAIT_NS);
+      for (int q = 0; q < stages; ++q)
+        if ((issued_mask >> q) & 1u) mbar_wait(&b_full[q], (issued_parity >> q) & 1u, WAIT_NS);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, 0, 1);
+      bool ok = mbar_wait(a_full, 0, WAIT_NS);
+      if (!ok) raise_timeout(&s_abort, p.status);
+      tc_fence_after();
+      int s = 0;
+      uint32_t ph = 0;
+      for (int t = 0; t < ntiles && ok && !s_abort; ++t) {
+        const int buf = t & 1;
+        const uint32_t acc_ph = (uint32_t)(t >> 1) & 1u;
+        if (!mbar_wait(&acc_empty[buf], acc_ph ^ 1u, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(buf * BN);
+        for (int kc = 0; kc < nkc; ++kc) {
+          if (!mbar_wait(&b_full[s], ph, WAIT_NS)) { raise_timeout(&s_abort, p.status); ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + kc * A_CHUNK_BYTES);
+          const uint32_t b_base = smem_u32(sB + s * B_STAGE_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            // A: K-major, 128-byte rows, 8-row groups 1 KB apart; +32 bytes per K step of 16.
+            const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+            // B: N-major, 64-id (128-byte) atoms 8 KB apart, 8-row K groups 1 KB apart.
+            const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, B_BOX_BYTES, 1024);
+            mma_f16(d_tmem, ad, bd, idesc, (kc | kk) != 0 ? 1u : 0u);
+          }
+          mma_commit(&b_empty[s]);
+          if (++s == stages) { s = 0; ph ^= 1u; }
+        }
+        if (!ok) break;
+        mma_commit(&acc_full[buf]);
+      }
+      // all MMAs issued by this thread complete before TMEM is released
+      mma_commit(drain);
+      mbar_wait(drain, 0, WAIT_NS);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue (warps 2-5)
+    const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are accessible to this warp
+    const int row = m * BM + q * 32 + lane;
+    const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+    for (int t = 0; t < ntiles; ++t) {
+      const int buf = t & 1;
+      const uint32_t acc_ph = (uint32_t)(t >> 1) & 1u;
+      if (!mbar_wait(&acc_full[buf], acc_ph, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
+      tc_fence_after();
+      const int n0 = (nt0 + t) * BN;
+#pragma unroll 1
+      for (int g = 0; g < BN / GROUP; ++g) {
+        const int gc0 = n0 + g * GROUP;
+        Top2 sm;
+        sm.init();
+#pragma unroll
+        for (int h2 = 0; h2 < 2; ++h2) {
+          float v[32];
+          tmem_ld_32x32b_x32(lane_addr + (uint32_t)(buf * BN + g * GROUP + h2 * 32), v);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int c = gc0 + h2 * 32 + i;
+            if (c < p.vocab) sm.push(v[i], (uint32_t)c);
+          }
+        }
+        if (row < p.B && gc0 < p.vocab) p.recs[(size_t)row * p.n_groups + gc0 / GROUP] = sm.record((uint32_t)gc0);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[buf]);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// 2-D bf16 tensor map over a row-major [rows x cols] matrix, box [box_rows x box_cols], 128B swizzle.
+bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool mma_path_supported(int B, int r, int dtype) {
+  return dtype == DH_BF16 && B >= 1 && r % BK == 0 && r >= BK && r <= 512;
+}
+
+cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
+                               GroupRec* recs, int* status) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_lowrank_mma, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  int maxopt = 0;
+  e = cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
+  if (e != cudaSuccess) return e;
+  const int nkc = r / BK;
+  const int static_bytes = 1024;  // barriers, TMEM slot, abort flag (statically allocated)
+  const int avail = maxopt - static_bytes - 1024 /*alignment slack*/ - nkc * A_CHUNK_BYTES;
+  const int stages = min(MAX_STAGES, avail / B_STAGE_BYTES);
+  if (stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = 1024 + (size_t)nkc * A_CHUNK_BYTES + (size_t)stages * B_STAGE_BYTES;
+
+  CUtensorMap tmA, tmB;
+  if (!make_map(&tmA, t, (uint64_t)r, (uint64_t)B, BK, BM)) return cudaErrorInvalidValue;
+  if (!make_map(&tmB, V, (uint64_t)vocab, (uint64_t)r, 64, BK)) return cudaErrorInvalidValue;
+
+  MmaParams p;
+  p.B = B;
+  p.r = r;
+  p.vocab = vocab;
+  p.n_groups = (vocab + GROUP - 1) / GROUP;
+  p.n_tiles = (vocab + BN - 1) / BN;
+  const int num_m = (B + BM - 1) / BM;
+  p.n_split = max(1, min(p.n_tiles, c.num_sms / num_m));
+  p.stages = stages;
+  p.recs = recs;
+  p.status = status;
+  prof_before("lowrank_mma", c.stream);
+  k_lowrank_mma<<<num_m * p.n_split, THREADS, smem, c.stream>>>(tmA, tmB, p);
+  prof_after(c.stream);
+  return cudaGetLastError();
+}
+
+}  // namespace dh
