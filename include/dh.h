@@ -47,7 +47,7 @@ typedef enum {
   DH_ERR_UNSUPPORTED = 2, /* alignment, dtype or a size above the documented limits          */
   DH_ERR_WORKSPACE = 3,   /* workspace missing, too small or not 256-byte aligned            */
   DH_ERR_CUDA = 4,        /* a CUDA runtime call or kernel launch failed                      */
-  DH_ERR_TIMEOUT = 5,     /* reserved: a bounded device-side wait gave up                     */
+  DH_ERR_TIMEOUT = 5,     /* a bounded device-side wait gave up (see dh_workspace_status)     */
   DH_ERR_BAD_INPUT = 6    /* per-row code written to err_out by dh_tree_accept                */
 } dh_status;
 
@@ -139,6 +139,16 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
                    int vocab, int dtype, int32_t* argmax_out, int32_t* path_out, int32_t* len_out,
                    int32_t* bonus_out, int32_t* err_out, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Device-side status of a workspace (no counterpart on the pages).
+ *
+ * Kernels that wait on on-chip barriers give up after a bounded time instead of hanging; they then
+ * set bit (1 << DH_ERR_TIMEOUT) in the first word of the workspace they ran with, and their outputs
+ * for that call are unspecified.  dh_workspace_status copies that word to *status_out (0 = no
+ * event), clears it, and synchronises `stream`.  workspace: device, 256-byte aligned.
+ * ------------------------------------------------------------------------------------------- */
+int dh_workspace_status(void* workspace, void* stream, int* status_out);
 
 /* ---------------------------------------------------------------------------------------------
  * Kernel timing for measurement (no counterpart on the pages).

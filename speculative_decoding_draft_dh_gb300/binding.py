@@ -22,7 +22,7 @@ F32, BF16 = 0, 1
 
 EXPORTS = ["dh_status_string", "dh_version", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
-           "dh_tree_accept", "dh_prof_enable", "dh_prof_read"]
+           "dh_tree_accept", "dh_workspace_status", "dh_prof_enable", "dh_prof_read"]
 
 _lib = None
 _lock = threading.Lock()
@@ -61,6 +61,8 @@ def load_library(path: str | None = None):
         lib.dh_tree_accept_workspace.restype = Z
         lib.dh_tree_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
         lib.dh_tree_accept.restype = I
+        lib.dh_workspace_status.argtypes = [P, P, P]
+        lib.dh_workspace_status.restype = I
         lib.dh_prof_enable.argtypes = [I]
         lib.dh_prof_enable.restype = I
         lib.dh_prof_read.argtypes = [P, I, P, P, I]
@@ -185,6 +187,18 @@ def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stre
                               _ptr(out["bonus"]), _ptr(out["err"]), _ptr(ws), nbytes,
                               _stream(stream)), "dh_tree_accept")
     return out
+
+
+def workspace_status(workspace: "Workspace | None" = None, device=None, stream=None) -> int:
+    """Read and clear the device status word of a workspace (0 = no device-side event)."""
+    lib = load_library()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    ws = (workspace or _default_ws).buf.get(dev)
+    if ws is None:
+        return 0
+    out = ctypes.c_int(0)
+    _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
+    return out.value
 
 
 def prof_enable(on: bool):

@@ -1,4 +1,6 @@
 // C ABI of libdh: argument validation, workspace layout and kernel sequencing (see include/dh.h).
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -31,7 +33,7 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   Ctx dummy{0, 0, nullptr};
   L.nsplit = proj_splits(dummy, B, d, r);
   const size_t n_groups = (size_t)(vocab + GROUP - 1) / GROUP;
-  size_t off = 0;
+  size_t off = WS_HEADER;
   L.t = off;
   off = align_up(off + (size_t)B * r * 4, 256);
   L.partial = off;
@@ -40,6 +42,18 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   off = align_up(off + (size_t)B * n_groups * sizeof(GroupRec), 256);
   L.total = off;
   return L;
+}
+
+// Smallest batch that takes the tensor-core path for stage 1 (bf16, r a multiple of 64).
+// DH_FORCE_PATH=gemv|mma overrides the choice (used by tests and tuning).
+constexpr int MMA_MIN_B = 16;
+
+bool use_mma(int B, int r, int dtype) {
+  if (!mma_path_supported(B, r, dtype)) return false;
+  const char* f = std::getenv("DH_FORCE_PATH");
+  if (f && std::strcmp(f, "gemv") == 0) return false;
+  if (f && std::strcmp(f, "mma") == 0) return true;
+  return B >= MMA_MIN_B;
 }
 
 // ---- profiling
@@ -133,7 +147,12 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
   if (launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t) != cudaSuccess) return DH_ERR_CUDA;
-  if (launch_scores_summary(c, t, V, B, r, vocab, dtype, recs) != cudaSuccess) return DH_ERR_CUDA;
+  if (use_mma(B, r, dtype)) {
+    if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+      return DH_ERR_CUDA;
+  } else if (launch_scores_summary(c, t, V, B, r, vocab, dtype, recs) != cudaSuccess) {
+    return DH_ERR_CUDA;
+  }
   if (launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out) != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
@@ -141,22 +160,26 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
 
 // ------------------------------------------------------------------ stage 2
 
-size_t dh_exact_rescore_workspace(int, int, int, int, int) { return 0; }
+size_t dh_exact_rescore_workspace(int B, int, int, int, int) {
+  return B > 0 ? WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256) : 0;
+}
 
 int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
                      int dtype, float* logits_out, float* probs_out, void* workspace, size_t ws_bytes,
                      void* stream) {
-  (void)workspace;
-  (void)ws_bytes;
   if (B < 0 || d <= 0 || vocab <= 0 || K < 1 || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
   if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
   if (B == 0) return DH_OK;
   if (!h || !W || !idx || !logits_out) return DH_ERR_INVALID_ARG;
   if (vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
   if (!aligned16(h) || !aligned16(W) || !row16(d, dtype)) return DH_ERR_UNSUPPORTED;
+  if ((long long)B * K > 0x7FFFFFFFLL) return DH_ERR_UNSUPPORTED;
+  const size_t need = dh_exact_rescore_workspace(B, d, vocab, K, dtype);
+  if (!workspace || !aligned256(workspace) || ws_bytes < need) return DH_ERR_WORKSPACE;
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
-  if (launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out) != cudaSuccess)
+  uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
+  if (launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets) != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }
@@ -165,7 +188,7 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
 
 size_t dh_tree_accept_workspace(int B, int N, int /*vocab*/) {
   if (B <= 0 || N <= 0) return 0;
-  return align_up((size_t)B * N * sizeof(int32_t), 256);
+  return WS_HEADER + align_up((size_t)B * N * sizeof(int32_t), 256);
 }
 
 int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* token, int B, int N, int vocab,
@@ -181,9 +204,23 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
   if (!workspace || !aligned256(workspace) || ws_bytes < need) return DH_ERR_WORKSPACE;
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
-  if (launch_tree(c, logits, parent, token, B, N, vocab, dtype, static_cast<int32_t*>(workspace), argmax_out,
+  int32_t* am_ws = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + WS_HEADER);
+  if (launch_tree(c, logits, parent, token, B, N, vocab, dtype, am_ws, argmax_out,
                   path_out, len_out, bonus_out, err_out) != cudaSuccess)
     return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ device status
+
+int dh_workspace_status(void* workspace, void* stream, int* status_out) {
+  if (!workspace || !status_out || !aligned256(workspace)) return DH_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess) return DH_ERR_CUDA;
+  if (cudaMemsetAsync(workspace, 0, sizeof(int), s) != cudaSuccess) return DH_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DH_ERR_CUDA;
+  *status_out = v;
   return DH_OK;
 }
 

@@ -9,6 +9,10 @@
 
 namespace dh {
 
+// Every workspace starts with a 256-byte header whose first word collects device-side status bits
+// (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.
+constexpr size_t WS_HEADER = 256;
+
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
 // third-best score.  The selection step works from these records; the full score row never
@@ -144,6 +148,10 @@ cudaError_t launch_proj(const Ctx& c, const void* h, const void* U, int B, int d
                         float* partial, int nsplit, void* t_out);
 int proj_splits(const Ctx& c, int B, int d, int r);
 
+bool mma_path_supported(int B, int r, int dtype);
+cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
+                               GroupRec* recs, int* status);
+
 cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                   int dtype, GroupRec* recs);
 
@@ -151,7 +159,7 @@ cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, con
                           int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out);
 
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
-                           int d, int vocab, int K, int dtype, float* logits, float* probs);
+                           int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
 
 cudaError_t launch_tree(const Ctx& c, const void* logits, const int32_t* parent, const int32_t* token,
                         int B, int N, int vocab, int dtype, int32_t* argmax_ws, int32_t* argmax_out,

@@ -7,8 +7,8 @@
 // vocabulary-wide product.
 //
 // Split-d CUDA-core GEMV/GEMM: block (s, rb) accumulates rows [b0, b0+PB) of h against the d-slice s
-// of U in fp32 and writes a partial [B x r] slab; a second kernel sums the slabs in slice order
-// (deterministic) and rounds.  U (1.3-5.2 MB) is read exactly once.
+// of U in fp32 and writes its partial sums; a second kernel adds the slices of each output with one
+// warp in a fixed order (deterministic) and rounds.  U (1.3-5.2 MB) is read exactly once.
 #include "dh_internal.cuh"
 
 namespace dh {
@@ -52,21 +52,27 @@ __global__ void __launch_bounds__(256) k_proj_partial(const T* __restrict__ h, c
 #pragma unroll
     for (int b = 0; b < PB; ++b) {
       if (b < nb) {
-        float* o = partial + ((size_t)s * B + b0 + b) * r + 2 * jp;
+        // partial layout [B*r][nsplit]: the reduce reads each output's slices contiguously
+        float* o = partial + ((size_t)(b0 + b) * r + 2 * jp) * nsplit + s;
         o[0] = acc[b][0];
-        o[1] = acc[b][1];
+        o[nsplit] = acc[b][1];
       }
     }
   }
 }
 
+// One warp per output: lanes sum strided slices, then a fixed shuffle tree (deterministic).
 template <typename T>
 __global__ void k_proj_reduce(const float* __restrict__ partial, int BR, int nsplit, T* __restrict__ t) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  const int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
   if (e >= BR) return;
+  const float* p = partial + (size_t)e * nsplit;
   float acc = 0.f;
-  for (int s = 0; s < nsplit; ++s) acc += partial[(size_t)s * BR + e];
-  t[e] = Elem<T>::from_f(acc);
+  for (int s = lane; s < nsplit; s += 32) acc += p[s];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  if (lane == 0) t[e] = Elem<T>::from_f(acc);
 }
 
 template <typename T>
@@ -89,7 +95,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, int B, int d, int r,
   if (e != cudaSuccess) return e;
   const int BR = B * r;
   prof_before("proj_reduce", c.stream);
-  k_proj_reduce<T><<<(BR + 255) / 256, 256, 0, c.stream>>>(partial, BR, nsplit, static_cast<T*>(t_out));
+  k_proj_reduce<T><<<(BR + 7) / 8, 256, 0, c.stream>>>(partial, BR, nsplit, static_cast<T*>(t_out));
   prof_after(c.stream);
   return cudaGetLastError();
 }

@@ -5,79 +5,119 @@
 // needs a cost model": products of the resulting draft probabilities estimate the benefit of a
 // branch; the softmax here runs over the K candidates of a row at temperature 1.
 //
-// Gather-GEMV: one warp per (row, candidate) streams W[idx] (d contiguous values) and h[row] with
+// Gather-GEMV: one block per (row, candidate) streams W[idx] (d contiguous values) and h[row] with
 // 16-byte loads, accumulates in fp32 and reduces with warp shuffles.  An index outside [0, vocab)
-// is never dereferenced: its logit becomes NaN.
+// is never dereferenced: its logit becomes NaN (and so do the row's probabilities).
 #include "dh_internal.cuh"
 
 namespace dh {
 namespace {
 
-constexpr int WARPS = 4;
+constexpr int THREADS = 128;
+constexpr int MAXV = 8;  // 16-byte vectors per thread in flight per batch of the row
 
+// One block per (row, candidate).  Each thread issues up to MAXV 16-byte loads of the W row (and
+// the matching h chunk) before using any of them, so a 10 KB row costs one memory round trip.
+// With probs requested, the last block of a row to finish (atomic ticket in the workspace)
+// computes the row's softmax and resets the ticket for the next call.
 template <typename T>
-__global__ void __launch_bounds__(WARPS * 32) k_rescore(const T* __restrict__ h, const T* __restrict__ W,
-                                                        const int32_t* __restrict__ idx, int BK, int d,
-                                                        int vocab, int K, float* __restrict__ logits) {
+__global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, const T* __restrict__ W,
+                                                     const int32_t* __restrict__ idx, int d, int vocab, int K,
+                                                     float* __restrict__ logits, float* __restrict__ probs,
+                                                     uint32_t* __restrict__ tickets) {
   constexpr int PER = Elem<T>::PER16;
-  const int lane = threadIdx.x & 31;
-  const int pair = blockIdx.x * WARPS + (threadIdx.x >> 5);
-  if (pair >= BK) return;
+  __shared__ float red[THREADS / 32];
+  __shared__ float s_bcast;
+  __shared__ int s_last;
+  const int pair = blockIdx.x;
   const int b = pair / K;
   const int v = idx[pair];
-  if (v < 0 || v >= vocab) {
-    if (lane == 0) logits[pair] = __int_as_float(0x7FC00000);
-    return;
-  }
-  const T* w = W + (size_t)v * d;
-  const T* x = h + (size_t)b * d;
+  const bool ok = v >= 0 && v < vocab;
   float acc = 0.f;
-#pragma unroll 4
-  for (int c = lane * PER; c < d; c += 32 * PER) {
-    const uint4 wa = ld_nc_v4(w + c);
-    const uint4 xa = __ldg(reinterpret_cast<const uint4*>(x + c));
-    float wf[PER], xf[PER];
-    Elem<T>::unpack(wa, wf);
-    Elem<T>::unpack(xa, xf);
+  if (ok) {
+    const T* w = W + (size_t)v * d;
+    const T* x = h + (size_t)b * d;
+    for (int c0 = 0; c0 < d; c0 += THREADS * PER * MAXV) {
+      uint4 wa[MAXV], xa[MAXV];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+      for (int q = 0; q < MAXV; ++q) {
+        const int c = c0 + (q * THREADS + (int)threadIdx.x) * PER;
+        if (c < d) {
+          wa[q] = ld_nc_v4(w + c);
+          xa[q] = __ldg(reinterpret_cast<const uint4*>(x + c));
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < MAXV; ++q) {
+        const int c = c0 + (q * THREADS + (int)threadIdx.x) * PER;
+        if (c < d) {
+          float wf[PER], xf[PER];
+          Elem<T>::unpack(wa[q], wf);
+          Elem<T>::unpack(xa[q], xf);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+        }
+      }
+    }
   }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-  if (lane == 0) logits[pair] = acc;
-}
-
-// One warp per row: p = exp(z - max) / sum exp(z - max).  A NaN logit makes the sum, hence every
-// probability of the row, NaN.
-__global__ void k_softmax(const float* __restrict__ logits, int B, int K, float* __restrict__ probs) {
-  const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (row >= B) return;
-  const float* z = logits + (size_t)row * K;
+  if (lane == 0) red[warp] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float sum = 0.f;
+#pragma unroll
+    for (int i = 0; i < THREADS / 32; ++i) sum += red[i];
+    logits[pair] = ok ? sum : __int_as_float(0x7FC00000);
+    if (probs) {
+      __threadfence();
+      s_last = atomicAdd(&tickets[b], 1u) == (uint32_t)(K - 1);
+    }
+  }
+  if (!probs) return;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  // softmax over the row's K logits (written by other blocks: read through L2)
+  const float* z = logits + (size_t)b * K;
   float m = -INFINITY;
-  for (int k = lane; k < K; k += 32) m = fmaxf(m, z[k]);
+  for (int k = threadIdx.x; k < K; k += THREADS) m = fmaxf(m, __ldcg(z + k));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  float s = 0.f;
-  for (int k = lane; k < K; k += 32) s += expf(z[k] - m);
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = red[0];
+    for (int i = 1; i < THREADS / 32; ++i) mm = fmaxf(mm, red[i]);
+    s_bcast = mm;
+  }
+  __syncthreads();
+  m = s_bcast;
+  float ssum = 0.f;
+  for (int k = threadIdx.x; k < K; k += THREADS) ssum += expf(__ldcg(z + k) - m);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, o);
-  const float inv = 1.f / s;
-  for (int k = lane; k < K; k += 32) probs[(size_t)row * K + k] = expf(z[k] - m) * inv;
+  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = ssum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < THREADS / 32; ++i) tot += red[i];
+    s_bcast = 1.f / tot;
+    tickets[b] = 0u;
+  }
+  __syncthreads();
+  const float inv = s_bcast;
+  for (int k = threadIdx.x; k < K; k += THREADS) probs[(size_t)b * K + k] = expf(__ldcg(z + k) - m) * inv;
 }
 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
-                int K, float* logits, float* probs) {
-  const int BK = B * K;
+                int K, float* logits, float* probs, uint32_t* tickets) {
   prof_before("rescore", c.stream);
-  k_rescore<T><<<(BK + WARPS - 1) / WARPS, WARPS * 32, 0, c.stream>>>(
-      static_cast<const T*>(h), static_cast<const T*>(W), idx, BK, d, vocab, K, logits);
-  prof_after(c.stream);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || probs == nullptr) return e;
-  prof_before("softmax", c.stream);
-  k_softmax<<<(B + 3) / 4, 128, 0, c.stream>>>(logits, B, K, probs);
+  k_rescore<T><<<(unsigned)(B * K), THREADS, 0, c.stream>>>(static_cast<const T*>(h), static_cast<const T*>(W),
+                                                             idx, d, vocab, K, logits, probs, tickets);
   prof_after(c.stream);
   return cudaGetLastError();
 }
@@ -85,9 +125,9 @@ cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, 
 }  // namespace
 
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
-                           int vocab, int K, int dtype, float* logits, float* probs) {
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, W, idx, B, d, vocab, K, logits, probs);
-  return run<float>(c, h, W, idx, B, d, vocab, K, logits, probs);
+                           int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets);
+  return run<float>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets);
 }
 
 }  // namespace dh

@@ -25,7 +25,7 @@ constexpr int BITMAP_WORDS = (DH_MAX_VOCAB / GROUP + 31) / 32;
 
 struct Shared {
   uint32_t hist[256];
-  uint32_t digit, above, total, cnt, nref;
+  uint32_t digit, run, bincount, total, cnt, nref;
   int32_t rg[RMAX];
   uint32_t bitmap[BITMAP_WORDS];
   float t[DH_MAX_RANK];
@@ -34,19 +34,36 @@ struct Shared {
   uint32_t si[DH_MAX_K];
 };
 
-// k-th largest value of sel(key, id) over the entries for which sel returns true.
-// Returns it and sets *n_above to the number of included entries strictly above it.
-// Requires at least k included entries (sh.total reports how many there were).
+// Histogram increment aggregated over the lanes of a warp that hit the same bin (score keys
+// crowd into a few exponent bins, so plain atomics would serialise).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
+  const unsigned peers = __match_any_sync(__activemask(), bin);
+  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+}
+
+// Result of a radix selection of the k-th largest value x over the included entries.
+//   total      number of included entries (if total < k nothing else is meaningful)
+//   exact_ge   true: exactly k entries have x >= thr
+//              false: thr is the k-th largest value, `above` entries have x > thr and the
+//              `need` = k - above entries still to take have x == thr (more than `need` do)
+struct Kth {
+  uint32_t thr, above, total;
+  bool exact_ge;
+};
+
+// MSB-first radix select with 8-bit digits.  sel(key, id, x) decides inclusion and sets x.  Stops
+// early as soon as the bin holding the k-th value contains exactly the entries still needed.
 template <class Enum, class Sel>
-__device__ uint32_t radix_kth(Enum en, Sel sel, uint32_t k, uint32_t* n_above, Shared& sh) {
+__device__ Kth radix_kth(Enum en, Sel sel, uint32_t k, Shared& sh) {
   uint32_t prefix = 0, mask = 0, krem = k, above = 0;
   const int lane = threadIdx.x & 31;
+  Kth res;
   for (int shift = 24; shift >= 0; shift -= 8) {
     for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
     __syncthreads();
     en([&](uint32_t key, uint32_t id) {
       uint32_t x;
-      if (sel(key, id, x) && (x & mask) == prefix) atomicAdd(&sh.hist[(x >> shift) & 255u], 1u);
+      if (sel(key, id, x) && (x & mask) == prefix) hist_add(sh.hist, (x >> shift) & 255u);
     });
     __syncthreads();
     if (threadIdx.x < 32) {
@@ -65,41 +82,56 @@ __device__ uint32_t radix_kth(Enum en, Sel sel, uint32_t k, uint32_t* n_above, S
         uint32_t run = excl;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
-          if (run + c[q] >= krem) { sh.digit = 255u - 8u * lane - q; sh.above = run; break; }
+          if (run + c[q] >= krem) {
+            sh.digit = 255u - 8u * lane - q; sh.run = run; sh.bincount = c[q];
+            break;
+          }
           run += c[q];
         }
       }
-      if (lane == 31 && incl < krem) { sh.digit = 0; sh.above = incl; }
+      if (lane == 31 && incl < krem) { sh.digit = 0; sh.run = incl; sh.bincount = 0; }
     }
     __syncthreads();
-    const uint32_t dg = sh.digit, ab = sh.above;
+    const uint32_t dg = sh.digit, run = sh.run, bc = sh.bincount, total = sh.total;
+    __syncthreads();
+    if (shift == 24 && total < k) {
+      res.thr = 0; res.above = 0; res.total = total; res.exact_ge = false;
+      return res;
+    }
     prefix |= dg << shift;
     mask |= 0xFFu << shift;
-    krem -= ab;
-    above += ab;
-    __syncthreads();
+    krem -= run;
+    above += run;
+    if (bc == krem) {
+      res.thr = prefix; res.above = above; res.total = total; res.exact_ge = true;
+      return res;
+    }
   }
-  *n_above = above;
-  return prefix;
+  res.thr = prefix; res.above = above; res.total = sh.total; res.exact_ge = false;
+  return res;
 }
 
-// Selects the k best entries (score key desc, id asc) of en, sorts them and writes the row.
+// Selects the K best entries (score key desc, id asc) of en, sorts them and writes the row; the
+// K-th best key goes to *thr_out.  Returns false (and writes nothing) if en holds fewer than K.
 template <class Enum>
-__device__ void select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, float* score_out,
-                                  uint32_t* T_out, uint32_t* idthr_out) {
-  uint32_t above;
-  const uint32_t T = radix_kth(en, [](uint32_t key, uint32_t, uint32_t& x) { x = key; return true; },
-                               (uint32_t)K, &above, sh);
-  const uint32_t need = (uint32_t)K - above;  // entries with key == T to take, lowest ids first
-  uint32_t above2;
-  const uint32_t nid = radix_kth(
-      en, [T](uint32_t key, uint32_t id, uint32_t& x) { x = ~id; return key == T; }, need, &above2, sh);
-  const uint32_t idthr = ~nid;
-  if (T_out) { *T_out = T; *idthr_out = idthr; }
+__device__ bool select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, float* score_out,
+                                  uint32_t* thr_out) {
+  const Kth a = radix_kth(en, [](uint32_t key, uint32_t, uint32_t& x) { x = key; return true; },
+                          (uint32_t)K, sh);
+  if (a.total < (uint32_t)K) return false;
+  const uint32_t T = a.thr;
+  uint32_t idthr = 0;  // among key == T, take ~id >= idthr (the lowest ids)
+  if (!a.exact_ge) {
+    const Kth b = radix_kth(
+        en, [T](uint32_t key, uint32_t id, uint32_t& x) { x = ~id; return key == T; }, (uint32_t)K - a.above,
+        sh);
+    idthr = b.thr;
+  }
+  const bool exact = a.exact_ge;
   if (threadIdx.x == 0) sh.cnt = 0;
   __syncthreads();
   en([&](uint32_t key, uint32_t id) {
-    if (key > T || (key == T && id <= idthr)) {
+    if (exact ? key >= T : (key > T || (key == T && ~id >= idthr))) {
       const uint32_t pos = atomicAdd(&sh.cnt, 1u);
       if (pos < DH_MAX_K) { sh.sk[pos] = key; sh.si[pos] = id; }
     }
@@ -112,12 +144,12 @@ __device__ void select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
     for (int stride = size >> 1; stride > 0; stride >>= 1) {
       __syncthreads();
       for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int a = 2 * i - (i & (stride - 1));
-        const int b = a + stride;
-        const bool up = (a & size) == 0;
-        const uint32_t ka = sh.sk[a], kb = sh.sk[b], ia = sh.si[a], ib = sh.si[b];
+        const int a0 = 2 * i - (i & (stride - 1));
+        const int b0 = a0 + stride;
+        const bool up = (a0 & size) == 0;
+        const uint32_t ka = sh.sk[a0], kb = sh.sk[b0], ia = sh.si[a0], ib = sh.si[b0];
         const bool b_first = kb > ka || (kb == ka && ib < ia);
-        if (b_first == up) { sh.sk[a] = kb; sh.sk[b] = ka; sh.si[a] = ib; sh.si[b] = ia; }
+        if (b_first == up) { sh.sk[a0] = kb; sh.sk[b0] = ka; sh.si[a0] = ib; sh.si[b0] = ia; }
       }
     }
   }
@@ -126,7 +158,9 @@ __device__ void select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
     idx_out[k] = (int32_t)sh.si[k];
     score_out[k] = fkey_inv(sh.sk[k]);
   }
+  if (thr_out) *thr_out = sh.sk[K - 1];  // the exact K-th best key of en
   __syncthreads();
+  return true;
 }
 
 template <typename T>
@@ -169,23 +203,10 @@ __global__ void __launch_bounds__(THREADS) k_select(const GroupRec* __restrict__
     }
   };
 
-  // pool size: at least K pairs are needed for tau to exist
-  if (threadIdx.x == 0) sh.cnt = 0;
-  __syncthreads();
-  {
-    uint32_t mine = 0;
-    pool([&](uint32_t, uint32_t) { ++mine; });
-    atomicAdd(&sh.cnt, mine);
-  }
-  __syncthreads();
-  bool full = sh.cnt < (uint32_t)K;
-  __syncthreads();
-
-  if (!full) {
-    uint32_t above;
-    const uint32_t tau = radix_kth(pool, [](uint32_t key, uint32_t, uint32_t& x) { x = key; return true; },
-                                   (uint32_t)K, &above, sh);
-    // groups that may hide a member at or above tau
+  uint32_t tau = 0;
+  if (select_sort_write(pool, K, sh, idx_out, score_out, &tau)) {
+    // Certificate: groups that may hide a member ranking at or above tau (third score >= tau).
+    // tau is at or below the true K-th score, so without such groups the pool's top K is exact.
     for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
       if (fkey(src[g].m3) >= tau) {
         const uint32_t pos = atomicAdd(&sh.nref, 1u);
@@ -195,10 +216,7 @@ __global__ void __launch_bounds__(THREADS) k_select(const GroupRec* __restrict__
     }
     __syncthreads();
     const int nref = (int)sh.nref;
-    if (nref == 0) {
-      select_sort_write(pool, K, sh, idx_out, score_out, nullptr, nullptr);
-      return;
-    }
+    if (nref == 0) return;
     if (nref <= RMAX) {
       for (int e = threadIdx.x; e < nref * GROUP; e += blockDim.x) {
         const int c = sh.rg[e / GROUP] * GROUP + (e % GROUP);
@@ -206,22 +224,21 @@ __global__ void __launch_bounds__(THREADS) k_select(const GroupRec* __restrict__
       }
       __syncthreads();
       auto refined = [&](auto f) {
-        pool(f);
+        pool(f);  // skips the refined groups (bitmap)
         for (int e = threadIdx.x; e < nref * GROUP; e += blockDim.x) {
           const int c = sh.rg[e / GROUP] * GROUP + (e % GROUP);
           if (c < vocab) f(fkey(sh.rs[e]), (uint32_t)c);
         }
       };
-      select_sort_write(refined, K, sh, idx_out, score_out, nullptr, nullptr);
+      select_sort_write(refined, K, sh, idx_out, score_out, nullptr);
       return;
     }
-    full = true;
   }
   // exact fallback: every id of the row, re-scored on each pass
   auto all = [&](auto f) {
     for (int c = threadIdx.x; c < vocab; c += blockDim.x) f(fkey(score_col(sh.t, V, r, vocab, c)), (uint32_t)c);
   };
-  select_sort_write(all, K, sh, idx_out, score_out, nullptr, nullptr);
+  select_sort_write(all, K, sh, idx_out, score_out, nullptr);
 }
 
 template <typename T>

@@ -235,3 +235,58 @@ def test_tree_full_size_sampled():
     t = inputs.make_tree(inputs.TREE_CONFIGS["tree"], seed=0, device=DEV)
     g = run_tree(t, reqs=[0, 1, 100, 200, 255])
     assert g["len"].mean() > 0.5
+
+
+# ---------------------------------------------------------------- both stage-1 paths on each shape
+
+MMA_SHAPES = [
+    inputs.HeadConfig("mma_r64", 5, 512, 8200, 64, 32, "bf16", 0.1, True),      # ragged vocab tail
+    inputs.HeadConfig("mma_r128_b1", 1, 1024, 16384, 128, 64, "bf16", 0.1, True),
+    inputs.HeadConfig("mma_two_mtiles", 130, 512, 4096, 128, 16, "bf16", 0.1, True),  # 2 row tiles
+    inputs.HeadConfig("mma_r512", 40, 512, 6144, 512, 256, "bf16", 0.1, True),   # deepest K loop
+]
+
+
+@pytest.mark.parametrize("cfg", MMA_SHAPES, ids=lambda c: c.name)
+@pytest.mark.parametrize("path", ["mma", "gemv"])
+def test_forced_stage1_path(cfg, path, monkeypatch):
+    monkeypatch.setenv("DH_FORCE_PATH", path)
+    x = inputs.make_head(cfg, seed=11, device=DEV)
+    rows = list(range(cfg.B)) if cfg.B <= 8 else [0, 1, cfg.B // 2, cfg.B - 1]
+    run_head(x, cfg.K, rows=rows)
+    assert dh.workspace_status() == 0
+
+
+def test_moderate_load_forced_gemv(monkeypatch):
+    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+    cfg = inputs.HEAD_CONFIGS["moderate"]
+    x = inputs.make_head(cfg, seed=1, device=DEV)
+    run_head(x, cfg.K, rows=[3, 60])
+
+
+def test_mma_and_gemv_paths_agree_on_candidates(monkeypatch):
+    cfg = inputs.HeadConfig("agree", 24, 512, 16384, 128, 64, "bf16", 0.1, True)
+    x = inputs.make_head(cfg, seed=12, device=DEV)
+    monkeypatch.setenv("DH_FORCE_PATH", "mma")
+    i1, s1 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+    i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    torch.cuda.synchronize()
+    same = (i1 == i2).float().mean().item()
+    assert same > 0.99
+    np.testing.assert_allclose(s1.cpu().numpy(), s2.cpu().numpy(), rtol=1e-4, atol=1e-4)
+
+
+def test_repeated_calls_are_identical():
+    cfg = inputs.head_config("tiny", B=4)
+    x = inputs.make_head(cfg, seed=13, device=DEV)
+    outs = []
+    for _ in range(3):
+        idx, score = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+        logits, probs = dh.exact_rescore(x["h"], x["W"], idx)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (idx, score, logits, probs)])
+    for o in outs[1:]:
+        for a, b in zip(outs[0], o):
+            assert torch.equal(a, b)
+    assert dh.workspace_status() == 0
