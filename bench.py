@@ -55,6 +55,9 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--profile-run", action="store_true",
+                    help="for profilers: one input copy, eager launches of warmup+steps steps, "
+                         "no graphs, e2e, CPU baseline or clock sampling; prints a short line")
     a = ap.parse_args()
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
@@ -89,12 +92,19 @@ def barrier(world):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The slowest rank's value (max) on every rank."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(units_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job throughput: every rank processed units_per_step per step; time = slowest rank."""
+    return units_per_step * steps * world / (max_ms / 1e3)
 
 
 def load_peaks():
@@ -275,7 +285,7 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
     us_per_call = ms * 1e3 / a.steps
-    value = cfg.B * a.steps * world / (ms / 1e3)
+    value = weak_scaling_value(cfg.B, a.steps, world, ms)
 
     # per-kernel events on the launch stream (separate pass, eager launches)
     n_prof = min(a.steps, 2000 if cfg.B <= 64 else 200)
@@ -421,7 +431,7 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
     sampler.stop()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     us = ms * 1e3 / a.steps
-    value = B * a.steps * world / (ms / 1e3)
+    value = weak_scaling_value(B, a.steps, world, ms)
     n_prof = min(a.steps, 50)
     dh.prof_enable(True)
     with torch.cuda.stream(stream):
@@ -555,8 +565,31 @@ def run_reference(a, rank, world):
                     "d2h_bytes_per_step": 0}}
 
 
+def profile_run(a):
+    """Small, bounded run for ncu: the workload's kernels launched eagerly on one input copy."""
+    from speculative_decoding_draft_dh_gb300 import binding as dh
+    dev = torch.device("cuda", 0)
+    if a.workload == "tree":
+        t = inputs.make_tree(inputs.TREE_CONFIGS["tree"], seed=a.seed, device=dev)
+        for _ in range(a.warmup + a.steps):
+            dh.tree_accept(t["logits"], t["parent"], t["token"])
+    else:
+        cfg = inputs.HEAD_CONFIGS[a.workload]
+        x = inputs.make_head(cfg, seed=a.seed, device=dev)
+        for _ in range(a.warmup + a.steps):
+            idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+            dh.exact_rescore(x["h"], x["W"], idx)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_run": a.workload, "steps": a.warmup + a.steps}), flush=True)
+
+
 def main():
     a = parse_args()
+    if a.profile_run:
+        from speculative_decoding_draft_dh_gb300 import build
+        build.build()
+        profile_run(a)
+        return
     rank, world, local = dist_env()
     if a.impl == "reference":
         line = run_reference(a, rank, world)

@@ -65,6 +65,10 @@ const char* dh_status_string(int status);
 /* Library version (major * 10000 + minor * 100 + patch). */
 int dh_version(void);
 
+/* Description of the last CUDA failure behind a DH_ERR_CUDA returned to the calling thread
+ * ("" if none).  The string is owned by the library and overwritten by the next failure. */
+const char* dh_last_error(void);
+
 /* ---------------------------------------------------------------------------------------------
  * Stage 1: low-rank candidate retrieval.
  *

@@ -20,7 +20,7 @@ STATUS = {0: "DH_OK", 1: "DH_ERR_INVALID_ARG", 2: "DH_ERR_UNSUPPORTED", 3: "DH_E
           4: "DH_ERR_CUDA", 5: "DH_ERR_TIMEOUT", 6: "DH_ERR_BAD_INPUT"}
 F32, BF16 = 0, 1
 
-EXPORTS = ["dh_status_string", "dh_version", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
+EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
            "dh_tree_accept", "dh_workspace_status", "dh_prof_enable", "dh_prof_read"]
 
@@ -29,8 +29,9 @@ _lock = threading.Lock()
 
 
 class DhError(RuntimeError):
-    def __init__(self, status: int, what: str):
-        super().__init__(f"{what} failed: {STATUS.get(status, status)}")
+    def __init__(self, status: int, what: str, detail: str = ""):
+        msg = f"{what} failed: {STATUS.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.status = status
 
 
@@ -49,6 +50,7 @@ def load_library(path: str | None = None):
         lib.dh_status_string.argtypes = [I]
         lib.dh_status_string.restype = ctypes.c_char_p
         lib.dh_version.restype = I
+        lib.dh_last_error.restype = ctypes.c_char_p
         lib.dh_lowrank_topk_workspace.argtypes = [I, I, I, I, I, I]
         lib.dh_lowrank_topk_workspace.restype = Z
         lib.dh_lowrank_topk.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P]
@@ -98,18 +100,19 @@ def _stream(stream):
 
 
 class Workspace:
-    """Zero-initialised device workspace, grown on demand (one per device and stream user)."""
+    """Zero-initialised device workspaces, grown on demand: one buffer per (device, call kind), so
+    one object can serve all three calls.  Calls using the same object must not overlap in time."""
 
     def __init__(self):
         self.buf = {}
 
-    def get(self, nbytes: int, device) -> torch.Tensor | None:
+    def get(self, nbytes: int, device, kind: str) -> torch.Tensor | None:
         if nbytes == 0:
             return None
-        key = torch.device(device)
+        key = (torch.device(device), kind)
         cur = self.buf.get(key)
         if cur is None or cur.numel() < nbytes:
-            cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=key)
+            cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=key[0])
             self.buf[key] = cur
         return cur
 
@@ -119,7 +122,10 @@ _default_ws = Workspace()
 
 def _check(status, what):
     if status != DH_OK:
-        raise DhError(status, what)
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = (_lib.dh_last_error() or b"").decode(errors="replace")
+        raise DhError(status, what, detail)
 
 
 def lowrank_topk(h, U, V, K, *, idx_out=None, score_out=None, workspace=None, stream=None):
@@ -136,7 +142,7 @@ def lowrank_topk(h, U, V, K, *, idx_out=None, score_out=None, workspace=None, st
     if score_out is None:
         score_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_lowrank_topk_workspace(B, d, r, vocab, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device)
+    ws = (workspace or _default_ws).get(nbytes, h.device, "topk")
     _check(lib.dh_lowrank_topk(_ptr(h), _ptr(U), _ptr(V), B, d, r, vocab, K, dt, _ptr(idx_out),
                                _ptr(score_out), _ptr(ws), nbytes, _stream(stream)), "dh_lowrank_topk")
     return idx_out, score_out
@@ -158,7 +164,7 @@ def exact_rescore(h, W, idx, *, with_probs=True, logits_out=None, probs_out=None
     if with_probs and probs_out is None:
         probs_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_exact_rescore_workspace(B, d, vocab, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device)
+    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore")
     _check(lib.dh_exact_rescore(_ptr(h), _ptr(W), _ptr(idx), B, d, vocab, K, dt, _ptr(logits_out),
                                 _ptr(probs_out if with_probs else None), _ptr(ws), nbytes,
                                 _stream(stream)), "dh_exact_rescore")
@@ -181,7 +187,7 @@ def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stre
            "bonus": torch.empty(B, dtype=torch.int32, device=dev),
            "err": torch.empty(B, dtype=torch.int32, device=dev)}
     nbytes = lib.dh_tree_accept_workspace(B, N, vocab)
-    ws = (workspace or _default_ws).get(nbytes, dev)
+    ws = (workspace or _default_ws).get(nbytes, dev, "tree")
     _check(lib.dh_tree_accept(_ptr(logits), _ptr(parent), _ptr(token), B, N, vocab, dt,
                               _ptr(out["argmax"]), _ptr(out["path"]), _ptr(out["len"]),
                               _ptr(out["bonus"]), _ptr(out["err"]), _ptr(ws), nbytes,
@@ -190,15 +196,17 @@ def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stre
 
 
 def workspace_status(workspace: "Workspace | None" = None, device=None, stream=None) -> int:
-    """Read and clear the device status word of a workspace (0 = no device-side event)."""
+    """Read and clear the device status words of a workspace object (OR over its buffers)."""
     lib = load_library()
     dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
-    ws = (workspace or _default_ws).buf.get(dev)
-    if ws is None:
-        return 0
-    out = ctypes.c_int(0)
-    _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
-    return out.value
+    status = 0
+    for (d, _kind), ws in (workspace or _default_ws).buf.items():
+        if d != dev:
+            continue
+        out = ctypes.c_int(0)
+        _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
+        status |= out.value
+    return status
 
 
 def prof_enable(on: bool):

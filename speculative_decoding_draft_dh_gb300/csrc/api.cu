@@ -1,4 +1,5 @@
 // C ABI of libdh: argument validation, workspace layout and kernel sequencing (see include/dh.h).
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -68,6 +69,18 @@ std::vector<ProfRec> g_prof_recs;
 
 }  // namespace
 
+namespace {
+thread_local char g_last_error[256] = "";
+}
+
+cudaError_t note_error(cudaError_t e, const char* where) {
+  if (e != cudaSuccess) {
+    std::snprintf(g_last_error, sizeof g_last_error, "%s: %s (%s)", where, cudaGetErrorName(e),
+                  cudaGetErrorString(e));
+  }
+  return e;
+}
+
 bool get_ctx(void* stream, Ctx* ctx) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -120,6 +133,8 @@ const char* dh_status_string(int status) {
 
 int dh_version(void) { return 100; }
 
+const char* dh_last_error(void) { return g_last_error; }
+
 // ------------------------------------------------------------------ stage 1
 
 size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int /*K*/, int /*dtype*/) {
@@ -146,14 +161,16 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   void* t = ws + L.t;
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
-  if (launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t) != cudaSuccess) return DH_ERR_CUDA;
+  if (note_error(launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t), "projection") != cudaSuccess)
+    return DH_ERR_CUDA;
   if (use_mma(B, r, dtype)) {
     if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
-  } else if (launch_scores_summary(c, t, V, B, r, vocab, dtype, recs) != cudaSuccess) {
+  } else if (note_error(launch_scores_summary(c, t, V, B, r, vocab, dtype, recs), "scores") != cudaSuccess) {
     return DH_ERR_CUDA;
   }
-  if (launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out) != cudaSuccess)
+  if (note_error(launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
+      cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }
@@ -179,7 +196,8 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
-  if (launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets) != cudaSuccess)
+  if (note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets),
+                 "rescore") != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }
@@ -205,8 +223,9 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   int32_t* am_ws = reinterpret_cast<int32_t*>(static_cast<char*>(workspace) + WS_HEADER);
-  if (launch_tree(c, logits, parent, token, B, N, vocab, dtype, am_ws, argmax_out,
-                  path_out, len_out, bonus_out, err_out) != cudaSuccess)
+  if (note_error(launch_tree(c, logits, parent, token, B, N, vocab, dtype, am_ws, argmax_out, path_out, len_out,
+                             bonus_out, err_out),
+                 "tree") != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }

@@ -167,17 +167,35 @@ cudaError_t launch_tree(const Ctx& c, const void* logits, const int32_t* parent,
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Raises a kernel's dynamic shared memory limit to the device maximum, once per device (a plain
-// attribute call, so it is also safe while a stream is being captured).
+// Records the failing CUDA call of the current thread for dh_last_error(); returns e.
+cudaError_t note_error(cudaError_t e, const char* where);
+
+// Raises a kernel's dynamic shared memory limit to the device maximum minus its static shared
+// memory, once per device (a plain attribute call, so it is also safe during stream capture).
 template <class Kernel>
 cudaError_t allow_max_smem(Kernel kernel, int device, unsigned long long* done_mask) {
   if (device < 64 && ((*done_mask >> device) & 1ull)) return cudaSuccess;
   int maxopt = 0;
   cudaError_t e = cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, device);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, maxopt);
-  if (e == cudaSuccess && device < 64) *done_mask |= 1ull << device;
+  if (e != cudaSuccess) return note_error(e, "cudaDeviceGetAttribute(MaxSharedMemoryPerBlockOptin)");
+  cudaFuncAttributes fa;
+  e = cudaFuncGetAttributes(&fa, kernel);
+  if (e != cudaSuccess) return note_error(e, "cudaFuncGetAttributes");
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           maxopt - (int)fa.sharedSizeBytes);
+  if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(MaxDynamicSharedMemorySize)");
+  if (device < 64) *done_mask |= 1ull << device;
   return e;
+}
+
+// Dynamic shared memory available to `kernel` on `device` (opt-in maximum minus static usage).
+template <class Kernel>
+int max_dynamic_smem(Kernel kernel, int device) {
+  int maxopt = 0;
+  cudaFuncAttributes fa;
+  if (cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess) return 0;
+  if (cudaFuncGetAttributes(&fa, kernel) != cudaSuccess) return 0;
+  return maxopt - (int)fa.sharedSizeBytes;
 }
 
 }  // namespace dh

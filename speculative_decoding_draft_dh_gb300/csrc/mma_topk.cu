@@ -243,19 +243,18 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   static unsigned long long smem_done = 0;
   cudaError_t e = allow_max_smem(k_lowrank_mma, c.device, &smem_done);
   if (e != cudaSuccess) return e;
-  int maxopt = 0;
-  e = cudaDeviceGetAttribute(&maxopt, cudaDevAttrMaxSharedMemoryPerBlockOptin, c.device);
-  if (e != cudaSuccess) return e;
   const int nkc = r / BK;
-  const int static_bytes = 1024;  // barriers, TMEM slot, abort flag (statically allocated)
-  const int avail = maxopt - static_bytes - 1024 /*alignment slack*/ - nkc * A_CHUNK_BYTES;
+  // dynamic: 1 KB alignment slack + resident A + B stages
+  const int avail = max_dynamic_smem(k_lowrank_mma, c.device) - 1024 - nkc * A_CHUNK_BYTES;
   const int stages = min(MAX_STAGES, avail / B_STAGE_BYTES);
-  if (stages < 2) return cudaErrorInvalidConfiguration;
+  if (stages < 2) return note_error(cudaErrorInvalidConfiguration, "lowrank_mma: shared memory for 2 stages");
   const size_t smem = 1024 + (size_t)nkc * A_CHUNK_BYTES + (size_t)stages * B_STAGE_BYTES;
 
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, t, (uint64_t)r, (uint64_t)B, BK, BM)) return cudaErrorInvalidValue;
-  if (!make_map(&tmB, V, (uint64_t)vocab, (uint64_t)r, 64, BK)) return cudaErrorInvalidValue;
+  if (!make_map(&tmA, t, (uint64_t)r, (uint64_t)B, BK, BM))
+    return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(T)");
+  if (!make_map(&tmB, V, (uint64_t)vocab, (uint64_t)r, 64, BK))
+    return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(V)");
 
   MmaParams p;
   p.B = B;
@@ -271,7 +270,7 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   prof_before("lowrank_mma", c.stream);
   k_lowrank_mma<<<num_m * p.n_split, THREADS, smem, c.stream>>>(tmA, tmB, p);
   prof_after(c.stream);
-  return cudaGetLastError();
+  return note_error(cudaGetLastError(), "launch k_lowrank_mma");
 }
 
 }  // namespace dh

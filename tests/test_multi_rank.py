@@ -1,0 +1,104 @@
+"""Multi-rank host logic on CPU with gloo (world size 2).
+
+* bench.py's replica mode: barrier, max-over-ranks timing and the weak-scaling aggregate.
+* The vocabulary-parallel merge rule of the sharded head design: each rank takes a contiguous
+  vocabulary shard, finds its shard's top-K (here with the CPU oracle, ids offset to global ids),
+  the ranks all-gather their K (score, id) pairs, and the K best of the union in (score desc, id asc)
+  order equal the unsharded top-K.  Any global top-K member is in its own shard's top-K, so the
+  union always contains the answer.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _init(rank, world, port):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+
+
+def _bench_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    _init(rank, world, port)
+    try:
+        bench.barrier(world)
+        ms = 10.0 + 5.0 * rank  # rank 1 is the slowest
+        slowest = bench.max_over_ranks(ms, world)
+        value = bench.weak_scaling_value(64, 100, world, slowest)
+        q.put((rank, slowest, value))
+    finally:
+        dist.destroy_process_group()
+
+
+def _shard_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    import oracle
+    from speculative_decoding_draft_dh_gb300 import inputs
+    _init(rank, world, port)
+    try:
+        cfg = inputs.head_config("tiny", B=3, K=16)
+        x = inputs.make_head(cfg, seed=21, with_W=False)
+        lo = cfg.vocab * rank // world
+        hi = cfg.vocab * (rank + 1) // world
+        idx, sc = oracle.lowrank_topk(x["h"], x["U"], x["V"][:, lo:hi].contiguous(), cfg.K)
+        mine = torch.from_numpy(np.stack([sc, (idx + lo).astype(np.float64)], axis=-1))
+        gathered = [torch.empty_like(mine) for _ in range(world)]
+        dist.all_gather(gathered, mine)
+        union = torch.cat(gathered, dim=1).numpy()  # [B, world*K, 2]
+        merged = []
+        for b in range(cfg.B):
+            s, ids = union[b, :, 0], union[b, :, 1].astype(np.int64)
+            order = np.lexsort((ids, -s))[: cfg.K]
+            merged.append(ids[order])
+        q.put((rank, np.stack(merged)))
+    finally:
+        dist.destroy_process_group()
+
+
+def _run(worker, world=2):
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=worker, args=(r, world, port, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    out = [q.get(timeout=120) for _ in procs]
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    return sorted(out, key=lambda t: t[0])
+
+
+def test_replicas_take_the_slowest_rank_and_scale_weakly():
+    out = _run(_bench_worker)
+    for rank, slowest, value in out:
+        assert slowest == 15.0
+        assert value == pytest.approx(64 * 100 * 2 / 0.015)
+
+
+def test_vocab_sharded_merge_equals_unsharded_topk():
+    import oracle
+    from speculative_decoding_draft_dh_gb300 import inputs
+    out = _run(_shard_worker)
+    cfg = inputs.head_config("tiny", B=3, K=16)
+    x = inputs.make_head(cfg, seed=21, with_W=False)
+    idx, _ = oracle.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    for _, merged in out:
+        np.testing.assert_array_equal(merged, idx)
