@@ -2,6 +2,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -38,7 +39,9 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   L.t = off;
   off = align_up(off + (size_t)B * r * 4, 256);
   L.partial = off;
-  off = align_up(off + (size_t)L.nsplit * B * r * 4, 256);
+  size_t partial_floats = (size_t)L.nsplit * B * r;
+  if (B <= 8) partial_floats = std::max(partial_floats, small_b_partial_floats(B, r));
+  off = align_up(off + partial_floats * 4, 256);
   L.recs = off;
   off = align_up(off + (size_t)B * n_groups * sizeof(GroupRec), 256);
   L.total = off;
@@ -49,12 +52,19 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
 // DH_FORCE_PATH=gemv|mma overrides the choice (used by tests and tuning).
 constexpr int MMA_MIN_B = 16;
 
-bool use_mma(int B, int r, int dtype) {
-  if (!mma_path_supported(B, r, dtype)) return false;
+enum Path { PATH_GEMV, PATH_MMA, PATH_FUSED };
+
+// Stage-1 path: the cooperative small-batch kernel for B <= 8, the tensor-core kernel for larger
+// bf16 batches, the multi-kernel CUDA-core path otherwise.  DH_FORCE_PATH=gemv|mma|fused overrides
+// the choice when the forced path supports the shape (tests and tuning).
+Path choose_path(int B, int r, int dtype) {
   const char* f = std::getenv("DH_FORCE_PATH");
-  if (f && std::strcmp(f, "gemv") == 0) return false;
-  if (f && std::strcmp(f, "mma") == 0) return true;
-  return B >= MMA_MIN_B;
+  if (f && std::strcmp(f, "gemv") == 0) return PATH_GEMV;
+  if (f && std::strcmp(f, "mma") == 0 && mma_path_supported(B, r, dtype)) return PATH_MMA;
+  if (f && std::strcmp(f, "fused") == 0 && small_b_supported(B, r, dtype)) return PATH_FUSED;
+  if (small_b_supported(B, r, dtype)) return PATH_FUSED;
+  if (mma_path_supported(B, r, dtype) && B >= MMA_MIN_B) return PATH_MMA;
+  return PATH_GEMV;
 }
 
 // ---- profiling
@@ -161,9 +171,16 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   void* t = ws + L.t;
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
+  const Path path = choose_path(B, r, dtype);
+  if (path == PATH_FUSED) {
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, K, dtype, partial, t, recs, idx_out, score_out,
+                       ws + WS_BARRIER_OFFSET, reinterpret_cast<int*>(ws)) != cudaSuccess)
+      return DH_ERR_CUDA;
+    return DH_OK;
+  }
   if (note_error(launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t), "projection") != cudaSuccess)
     return DH_ERR_CUDA;
-  if (use_mma(B, r, dtype)) {
+  if (path == PATH_MMA) {
     if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
   } else if (note_error(launch_scores_summary(c, t, V, B, r, vocab, dtype, recs), "scores") != cudaSuccess) {

@@ -10,8 +10,10 @@
 namespace dh {
 
 // Every workspace starts with a 256-byte header whose first word collects device-side status bits
-// (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.
+// (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.  Bytes 64-71
+// hold the grid barrier of the cooperative small-batch kernel.
 constexpr size_t WS_HEADER = 256;
+constexpr size_t WS_BARRIER_OFFSET = 64;
 
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
@@ -149,6 +151,11 @@ cudaError_t launch_proj(const Ctx& c, const void* h, const void* U, int B, int d
 int proj_splits(const Ctx& c, int B, int d, int r);
 
 bool mma_path_supported(int B, int r, int dtype);
+bool small_b_supported(int B, int r, int dtype);
+size_t small_b_partial_floats(int B, int r);
+cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
+                           int vocab, int K, int dtype, float* partial, void* t_out, GroupRec* recs,
+                           int32_t* idx_out, float* score_out, void* bar, int* status);
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                GroupRec* recs, int* status);
 

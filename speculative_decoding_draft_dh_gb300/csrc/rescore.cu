@@ -31,20 +31,28 @@ __global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, co
   __shared__ int s_last;
   const int pair = blockIdx.x;
   const int b = pair / K;
+  const T* x = h + (size_t)b * d;
+  // h does not depend on the previous kernel on the stream: fetch its first chunk before waiting
+  uint4 xa[MAXV];
+#pragma unroll
+  for (int q = 0; q < MAXV; ++q) {
+    const int c = (q * THREADS + (int)threadIdx.x) * PER;
+    if (c < d) xa[q] = __ldg(reinterpret_cast<const uint4*>(x + c));
+  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
   const int v = idx[pair];
   const bool ok = v >= 0 && v < vocab;
   float acc = 0.f;
   if (ok) {
     const T* w = W + (size_t)v * d;
-    const T* x = h + (size_t)b * d;
     for (int c0 = 0; c0 < d; c0 += THREADS * PER * MAXV) {
-      uint4 wa[MAXV], xa[MAXV];
+      uint4 wa[MAXV];
 #pragma unroll
       for (int q = 0; q < MAXV; ++q) {
         const int c = c0 + (q * THREADS + (int)threadIdx.x) * PER;
         if (c < d) {
           wa[q] = ld_nc_v4(w + c);
-          xa[q] = __ldg(reinterpret_cast<const uint4*>(x + c));
+          if (c0 > 0) xa[q] = __ldg(reinterpret_cast<const uint4*>(x + c));
         }
       }
 #pragma unroll
@@ -115,10 +123,23 @@ __global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, co
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
                 int K, float* logits, float* probs, uint32_t* tickets) {
+  // Programmatic dependent launch: the blocks may start while the stage-1 kernel drains; they
+  // prefetch h and then wait (griddepcontrol.wait) for its results.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * K));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = c.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before("rescore", c.stream);
-  k_rescore<T><<<(unsigned)(B * K), THREADS, 0, c.stream>>>(static_cast<const T*>(h), static_cast<const T*>(W),
-                                                             idx, d, vocab, K, logits, probs, tickets);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_rescore<T>, static_cast<const T*>(h), static_cast<const T*>(W), idx,
+                                     d, vocab, K, logits, probs, tickets);
   prof_after(c.stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

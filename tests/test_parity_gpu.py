@@ -248,12 +248,36 @@ MMA_SHAPES = [
 
 
 @pytest.mark.parametrize("cfg", MMA_SHAPES, ids=lambda c: c.name)
-@pytest.mark.parametrize("path", ["mma", "gemv"])
+@pytest.mark.parametrize("path", ["mma", "gemv", "fused"])
 def test_forced_stage1_path(cfg, path, monkeypatch):
     monkeypatch.setenv("DH_FORCE_PATH", path)
     x = inputs.make_head(cfg, seed=11, device=DEV)
     rows = list(range(cfg.B)) if cfg.B <= 8 else [0, 1, cfg.B // 2, cfg.B - 1]
     run_head(x, cfg.K, rows=rows)
+    assert dh.workspace_status() == 0
+
+
+@pytest.mark.parametrize("B", [1, 4, 8])
+@pytest.mark.parametrize("path", ["gemv", "fused"])
+def test_small_batch_paths_fp32(B, path, monkeypatch):
+    monkeypatch.setenv("DH_FORCE_PATH", path)
+    cfg = inputs.head_config("tiny", B=B, K=32)
+    x = inputs.make_head(cfg, seed=20 + B, device=DEV)
+    run_head(x, cfg.K)
+    assert dh.workspace_status() == 0
+
+
+def test_batch1_forced_gemv(monkeypatch):
+    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+    cfg = inputs.HEAD_CONFIGS["batch1"]
+    x = inputs.make_head(cfg, seed=2, device=DEV)
+    run_head(x, cfg.K)
+
+
+def test_fused_path_batch8_bf16_full_vocab():
+    cfg = inputs.HeadConfig("b8", 8, 5120, 151936, 256, 64, "bf16", 0.1, True)
+    x = inputs.make_head(cfg, seed=3, device=DEV)
+    run_head(x, cfg.K, rows=[0, 7])
     assert dh.workspace_status() == 0
 
 
