@@ -232,7 +232,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
       for (int rb = 0; rb < spg; ++rb) {
         const int q = k * spg + rb;
-        if (!mbar_wait(&full[warp][q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS)) {
+        // the outcome is made warp-uniform so that the lanes never split around __syncwarp
+        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[warp][q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS))) {
           if (lane == 0) atomicOr(p.status, 1 << DH_ERR_TIMEOUT);
           s_fail = 1;
           goto drain;
