@@ -168,7 +168,11 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int t = 0; t < ntiles; ++t) {
       const int buf = t & 1;
       const uint32_t acc_ph = (uint32_t)(t >> 1) & 1u;
-      if (!mbar_wait(&acc_full[buf], acc_ph, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
+      // warp-uniform outcome: the TMEM loads below are .sync.aligned and need the whole warp
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&acc_full[buf], acc_ph, WAIT_NS))) {
+        raise_timeout(&s_abort, p.status);
+        break;
+      }
       tc_fence_after();
       const int n0 = (nt0 + t) * BN;
 #pragma unroll 1
