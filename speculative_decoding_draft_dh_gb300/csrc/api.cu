@@ -41,6 +41,8 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   L.partial = off;
   size_t partial_floats = (size_t)L.nsplit * B * r;
   if (B <= 8) partial_floats = std::max(partial_floats, small_b_partial_floats(B, r));
+  // tensor-core projection: split-K slices for up to 256 SMs
+  partial_floats = std::max(partial_floats, (size_t)proj_mma_splits(B, d, r, 256) * B * r);
   off = align_up(off + partial_floats * 4, 256);
   L.recs = off;
   off = align_up(off + (size_t)B * n_groups * sizeof(GroupRec), 256);
@@ -178,8 +180,13 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
       return DH_ERR_CUDA;
     return DH_OK;
   }
-  if (note_error(launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t), "projection") != cudaSuccess)
+  if (path == PATH_MMA && proj_mma_supported(B, d, r, dtype)) {
+    if (launch_proj_mma(c, h, U, B, d, r, partial, proj_mma_splits(B, d, r, 256), t, reinterpret_cast<int*>(ws)) !=
+        cudaSuccess)
+      return DH_ERR_CUDA;
+  } else if (note_error(launch_proj(c, h, U, B, d, r, dtype, partial, L.nsplit, t), "projection") != cudaSuccess) {
     return DH_ERR_CUDA;
+  }
   if (path == PATH_MMA) {
     if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;

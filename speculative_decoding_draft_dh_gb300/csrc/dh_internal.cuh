@@ -152,6 +152,10 @@ int proj_splits(const Ctx& c, int B, int d, int r);
 
 bool mma_path_supported(int B, int r, int dtype);
 bool small_b_supported(int B, int r, int dtype);
+bool proj_mma_supported(int B, int d, int r, int dtype);
+int proj_mma_splits(int B, int d, int r, int num_sms);
+cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
+                            int max_splits, void* t, int* status);
 size_t small_b_partial_floats(int B, int r);
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
                            int vocab, int K, int dtype, float* partial, void* t_out, GroupRec* recs,

@@ -205,6 +205,142 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
+// ------------------------------------------------------------------------------------------------
+// Stage 1a on the tensor cores (bf16, larger batches): partial[s] = h[:, K-slice s] U[K-slice s, :]
+// for a split-K grid of (row tile, column tile, slice) blocks; k_proj_reduce_mma then sums the
+// slices in a fixed order and rounds t to bf16.  A = h (K-major, streamed), B = U (N-major).
+// Warp roles as in k_lowrank_mma; one accumulator of 128 x BN fp32 in TMEM per block.
+
+struct ProjParams {
+  int B, d, r, BN, n_ntiles, splits;
+  float* partial;  // [splits][B][r]
+  int* status;
+};
+
+__global__ void __launch_bounds__(THREADS, 1)
+    k_proj_mma(const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmU, ProjParams p) {
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t bars[2 * MAX_STAGES + 2];
+  __shared__ uint32_t tmem_slot;
+  __shared__ volatile int s_abort;
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                         ~static_cast<uintptr_t>(1023));
+  const int nb = p.BN / 64;                        // 64-id boxes of U per stage
+  const int stage_bytes = A_CHUNK_BYTES + nb * B_BOX_BYTES;
+  uint64_t* full = &bars[0];
+  uint64_t* empty = &bars[MAX_STAGES];
+  uint64_t* acc_full = &bars[2 * MAX_STAGES];
+  uint64_t* drain = &bars[2 * MAX_STAGES + 1];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tiles_per_split = gridDim.x / p.splits;
+  const int split = blockIdx.x / tiles_per_split;
+  const int tile = blockIdx.x % tiles_per_split;
+  const int m = tile / p.n_ntiles, n = tile % p.n_ntiles;
+  const int nkc_all = p.d / BK;
+  const int kc0 = (int)((long long)nkc_all * split / p.splits);
+  const int kc1 = (int)((long long)nkc_all * (split + 1) / p.splits);
+  const int nkc = kc1 - kc0;
+  const int stages = min(MAX_STAGES, (int)(200 * 1024 / stage_bytes));
+  uint32_t tmem_cols = 32;  // TMEM allocations are powers of two >= 32 columns
+  while (tmem_cols < (uint32_t)p.BN) tmem_cols <<= 1;
+
+  if (threadIdx.x == 0) {
+    s_abort = 0;
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(drain, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(&tmem_slot, tmem_cols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tmH);
+      prefetch_tmap(&tmU);
+      uint32_t issued_parity = 0, issued_mask = 0, ph = 0;
+      int s = 0;
+      for (int kc = kc0; kc < kc1 && !s_abort; ++kc) {
+        if (!mbar_wait(&empty[s], ph ^ 1u, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
+        unsigned char* st = base + (size_t)s * stage_bytes;
+        mbar_arrive_expect_tx(&full[s], (uint32_t)stage_bytes);
+        tma_load_2d(st, &tmH, kc * BK, m * BM, &full[s]);
+        for (int q = 0; q < nb; ++q)
+          tma_load_2d(st + A_CHUNK_BYTES + q * B_BOX_BYTES, &tmU, n * p.BN + q * 64, kc * BK, &full[s]);
+        issued_mask |= 1u << s;
+        issued_parity = (issued_parity & ~(1u << s)) | (ph << s);
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+      for (int q = 0; q < stages; ++q)
+        if ((issued_mask >> q) & 1u) mbar_wait(&full[q], (issued_parity >> q) & 1u, WAIT_NS);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(BM, p.BN, 0, 1);
+      int s = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      for (int kc = 0; kc < nkc && !s_abort; ++kc) {
+        if (!mbar_wait(&full[s], ph, WAIT_NS)) { raise_timeout(&s_abort, p.status); ok = false; break; }
+        tc_fence_after();
+        const uint32_t a_base = smem_u32(base + (size_t)s * stage_bytes);
+        const uint32_t b_base = a_base + A_CHUNK_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / 16; ++kk) {
+          const uint64_t ad = smem_desc_sw128(a_base + kk * 32, 16, 1024);
+          const uint64_t bd = smem_desc_sw128(b_base + kk * 2048, B_BOX_BYTES, 1024);
+          mma_f16(tmem, ad, bd, idesc, (kc | kk) != 0 ? 1u : 0u);
+        }
+        mma_commit(&empty[s]);
+        if (++s == stages) { s = 0; ph ^= 1u; }
+      }
+      if (ok) mma_commit(acc_full);
+      mma_commit(drain);
+      mbar_wait(drain, 0, WAIT_NS);
+    }
+  } else {
+    const int q = warp & 3;
+    const int row = m * BM + q * 32 + lane;
+    if (__all_sync(0xFFFFFFFFu, mbar_wait(acc_full, 0, WAIT_NS))) {
+      tc_fence_after();
+      const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
+      float* out = p.partial + ((size_t)split * p.B + row) * p.r + (size_t)n * p.BN;
+      for (int c0 = 0; c0 < p.BN; c0 += 32) {
+        float v[32];
+        tmem_ld_32x32b_x32(lane_addr + (uint32_t)c0, v);
+        if (row < p.B) {
+#pragma unroll
+          for (int i = 0; i < 32; i += 4)
+            *reinterpret_cast<float4*>(out + c0 + i) = make_float4(v[i], v[i + 1], v[i + 2], v[i + 3]);
+        }
+      }
+    } else {
+      raise_timeout(&s_abort, p.status);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, tmem_cols);
+  }
+}
+
+// t[e] = bf16(sum over s of partial[s][e]), slices in ascending order (deterministic).
+__global__ void k_proj_reduce_mma(const float* __restrict__ partial, int BR, int splits, __nv_bfloat16* __restrict__ t) {
+  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  if (e >= BR) return;
+  float acc = 0.f;
+  for (int s = 0; s < splits; ++s) acc += __ldcg(partial + (size_t)s * BR + e);
+  t[e] = __float2bfloat16_rn(acc);
+}
+
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -240,6 +376,52 @@ bool make_map(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
 
 bool mma_path_supported(int B, int r, int dtype) {
   return dtype == DH_BF16 && B >= 1 && r % BK == 0 && r >= BK && r <= 512;
+}
+
+bool proj_mma_supported(int B, int d, int r, int dtype) {
+  return mma_path_supported(B, r, dtype) && d % BK == 0 && (r <= 256 || r % 256 == 0);
+}
+
+// Split-K slices of the tensor-core projection: enough blocks to cover the SMs, at most one
+// 64-wide K chunk per slice.  max_sms bounds the workspace independently of the device.
+int proj_mma_splits(int B, int d, int r, int num_sms) {
+  const int m_tiles = (B + BM - 1) / BM;
+  const int n_tiles = (r + 255) / 256;
+  return max(1, min(d / BK, num_sms / (m_tiles * n_tiles)));
+}
+
+cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
+                            int max_splits, void* t, int* status) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_proj_mma, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  ProjParams p;
+  p.B = B;
+  p.d = d;
+  p.r = r;
+  p.BN = r <= 256 ? r : 256;
+  p.n_ntiles = r / p.BN;
+  p.splits = min(max_splits, proj_mma_splits(B, d, r, c.num_sms));
+  p.partial = partial;
+  p.status = status;
+  const int stage_bytes = A_CHUNK_BYTES + (p.BN / 64) * B_BOX_BYTES;
+  const int stages = min(MAX_STAGES, 200 * 1024 / stage_bytes);
+  const size_t smem = 1024 + (size_t)stages * stage_bytes;
+  CUtensorMap tmH, tmU;
+  if (!make_map(&tmH, h, (uint64_t)d, (uint64_t)B, BK, BM)) return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(h)");
+  if (!make_map(&tmU, U, (uint64_t)r, (uint64_t)d, 64, BK)) return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(U)");
+  const int m_tiles = (B + BM - 1) / BM;
+  const int grid = p.splits * m_tiles * p.n_ntiles;
+  prof_before("proj_mma", c.stream);
+  k_proj_mma<<<grid, THREADS, smem, c.stream>>>(tmH, tmU, p);
+  prof_after(c.stream);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return note_error(e, "launch k_proj_mma");
+  const int BR = B * r;
+  prof_before("proj_reduce_mma", c.stream);
+  k_proj_reduce_mma<<<(BR + 255) / 256, 256, 0, c.stream>>>(partial, BR, p.splits, static_cast<__nv_bfloat16*>(t));
+  prof_after(c.stream);
+  return note_error(cudaGetLastError(), "launch k_proj_reduce_mma");
 }
 
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
