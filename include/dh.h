@@ -155,6 +155,18 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
 int dh_workspace_status(void* workspace, void* stream, int* status_out);
 
 /* ---------------------------------------------------------------------------------------------
+ * Self-test of the bounded device-side waits (no counterpart on the pages).
+ *
+ * Queues one small kernel that waits, with the same code the pipelined kernels use, on a
+ * condition that is never met: mode 0 an mbarrier nothing arrives at, mode 1 a grid barrier that
+ * expects one block more than the grid has.  The wait gives up after limit_us microseconds
+ * (1..1000000) and raises bit (1 << DH_ERR_TIMEOUT) in the workspace status word, which
+ * dh_workspace_status then reports; the CUDA context stays usable.  workspace: a zero-filled
+ * device buffer of at least 256 bytes, 256-byte aligned (its barrier counter is left at zero).
+ * ------------------------------------------------------------------------------------------- */
+int dh_selftest_wait_timeout(int mode, int limit_us, void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Kernel timing for measurement (no counterpart on the pages).
  *
  * dh_prof_enable(1) makes every subsequent call record a CUDA event pair around each kernel it

@@ -22,7 +22,7 @@ F32, BF16 = 0, 1
 
 EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
-           "dh_tree_accept", "dh_workspace_status", "dh_prof_enable", "dh_prof_read"]
+           "dh_tree_accept", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
 
 _lib = None
 _lock = threading.Lock()
@@ -65,6 +65,8 @@ def load_library(path: str | None = None):
         lib.dh_tree_accept.restype = I
         lib.dh_workspace_status.argtypes = [P, P, P]
         lib.dh_workspace_status.restype = I
+        lib.dh_selftest_wait_timeout.argtypes = [I, I, P, Z, P]
+        lib.dh_selftest_wait_timeout.restype = I
         lib.dh_prof_enable.argtypes = [I]
         lib.dh_prof_enable.restype = I
         lib.dh_prof_read.argtypes = [P, I, P, P, I]
@@ -207,6 +209,20 @@ def workspace_status(workspace: "Workspace | None" = None, device=None, stream=N
         _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
         status |= out.value
     return status
+
+
+def selftest_wait_timeout(mode: int, limit_us: int = 50000, stream=None) -> int:
+    """Run the bounded-wait self-test (mode 0: mbarrier, 1: grid barrier) on a fresh workspace and
+    return the status word it left (expected: 1 << DH_ERR_TIMEOUT)."""
+    lib = load_library()
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    _check(lib.dh_selftest_wait_timeout(mode, limit_us, _ptr(ws), 256, _stream(stream)),
+           "dh_selftest_wait_timeout")
+    out = ctypes.c_int(0)
+    _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
+    if int(ws[64:68].view(torch.int32).item()) != 0:
+        raise DhError(5, "dh_selftest_wait_timeout", "barrier counter not restored")
+    return out.value
 
 
 def prof_enable(on: bool):

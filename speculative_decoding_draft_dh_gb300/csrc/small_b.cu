@@ -23,6 +23,7 @@
 // Grid barriers are sense-reversing counters in the workspace; every wait (barrier or TMA) gives
 // up after two seconds, raises DH_ERR_TIMEOUT in the status word, and the block drains its own
 // outstanding copies before it exits.
+#include "grid_sync.cuh"
 #include "select.cuh"
 #include "sm100.cuh"
 
@@ -41,11 +42,6 @@ constexpr int CH = 40;        // projection rows per batch of loads in flight
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t STAGE_REGION = (size_t)SB_WARPS * NS * STAGE_BYTES;
 
-struct GridBar {
-  unsigned int count;
-  unsigned int gen;
-};
-
 struct SbParams {
   const void* h;
   const void* U;
@@ -59,40 +55,6 @@ struct SbParams {
   GridBar* bar;
   int* status;
 };
-
-__device__ __forceinline__ unsigned int ld_acquire(const unsigned int* p) {
-  unsigned int v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-
-// Sense-reversing grid barrier; false if it gave up (then DH_ERR_TIMEOUT is raised).
-__device__ bool grid_sync(GridBar* bar, int* status, volatile int* s_fail) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    const unsigned int g = ld_acquire(&bar->gen);
-    __threadfence();
-    const unsigned int arrived = atomicAdd(&bar->count, 1u) + 1u;
-    if (arrived == gridDim.x) {
-      bar->count = 0u;
-      __threadfence();
-      atomicAdd(&bar->gen, 1u);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      while (ld_acquire(&bar->gen) == g) {
-        if (globaltimer_ns() - t0 > WAIT_NS) {
-          atomicOr(status, 1 << DH_ERR_TIMEOUT);
-          *s_fail = 1;
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    __threadfence();
-  }
-  __syncthreads();
-  return *s_fail == 0;
-}
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -192,7 +154,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       }
     }
   }
-  if (!grid_sync(p.bar, p.status, &s_fail)) goto drain;
+  if (!grid_sync(p.bar, gridDim.x, WAIT_NS, p.status, &s_fail)) goto drain;
 
   // ---------------------------------------------------------------- P2: t, identical in every block
   {
@@ -283,7 +245,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       }
     }
   }
-  if (!grid_sync(p.bar, p.status, &s_fail)) goto drain;
+  if (!grid_sync(p.bar, gridDim.x, WAIT_NS, p.status, &s_fail)) goto drain;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   // ---------------------------------------------------------------- P4: exact top-K of row c

@@ -244,6 +244,7 @@ MMA_SHAPES = [
     inputs.HeadConfig("mma_r128_b1", 1, 1024, 16384, 128, 64, "bf16", 0.1, True),
     inputs.HeadConfig("mma_two_mtiles", 130, 512, 4096, 128, 16, "bf16", 0.1, True),  # 2 row tiles
     inputs.HeadConfig("mma_r512", 40, 512, 6144, 512, 256, "bf16", 0.1, True),   # deepest K loop
+    inputs.HeadConfig("mma_r192", 20, 768, 4096, 192, 32, "bf16", 0.1, True),    # 192-wide projection tile
 ]
 
 
@@ -314,3 +315,14 @@ def test_repeated_calls_are_identical():
         for a, b in zip(outs[0], o):
             assert torch.equal(a, b)
     assert dh.workspace_status() == 0
+
+
+# ---------------------------------------------------------------- bounded waits
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["mbarrier", "grid_barrier"])
+def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
+    status = dh.selftest_wait_timeout(mode, limit_us=20000)
+    assert status == (1 << 5)
+    cfg = inputs.head_config("tiny", B=2)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K)
