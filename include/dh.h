@@ -107,7 +107,7 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
  * h [B x d], W [vocab x d]: device, `dtype`.  idx [B x K] int32: device.
  * logits_out [B x K] fp32: device.  probs_out [B x K] fp32: device, may be NULL (no softmax).
  * An index outside [0, vocab) is not dereferenced: its logit is NaN, which makes that row's
- * probabilities NaN.  B = 0 is a no-op.
+ * probabilities NaN.  Limits: d <= 8192, K <= DH_MAX_K.  B = 0 is a no-op.
  * ------------------------------------------------------------------------------------------- */
 size_t dh_exact_rescore_workspace(int B, int d, int vocab, int K, int dtype);
 int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,

@@ -214,7 +214,7 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   if (!h || !W || !idx || !logits_out) return DH_ERR_INVALID_ARG;
   if (vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
   if (!aligned16(h) || !aligned16(W) || !row16(d, dtype)) return DH_ERR_UNSUPPORTED;
-  if ((long long)B * K > 0x7FFFFFFFLL) return DH_ERR_UNSUPPORTED;
+  if ((long long)B * K > 0x7FFFFFFFLL || !rescore_supported(d)) return DH_ERR_UNSUPPORTED;
   const size_t need = dh_exact_rescore_workspace(B, d, vocab, K, dtype);
   if (!workspace || !aligned256(workspace) || ws_bytes < need) return DH_ERR_WORKSPACE;
   Ctx c;

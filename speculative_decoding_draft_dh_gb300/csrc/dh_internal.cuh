@@ -169,6 +169,7 @@ cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, in
 cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, const void* V, int B,
                           int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out);
 
+bool rescore_supported(int d);
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
                            int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
 

@@ -29,20 +29,31 @@ template <typename T>
 __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restrict__ logits, int vocab,
                                                                 int32_t* __restrict__ am) {
   constexpr int PER = Elem<T>::PER16;
+  constexpr int BATCH = 8;  // 16-byte loads per thread in flight
   __shared__ unsigned long long red[ARGMAX_THREADS / 32];
   const size_t row = blockIdx.x;
   const T* p = logits + row * (size_t)vocab;
   unsigned long long best = 0ull;
-#pragma unroll 4
-  for (int c = threadIdx.x * PER; c < vocab; c += ARGMAX_THREADS * PER) {
-    const uint4 u = ld_nc_v4(p + c);
-    float x[PER];
-    Elem<T>::unpack(u, x);
+  for (int c0 = threadIdx.x * PER; c0 < vocab; c0 += ARGMAX_THREADS * PER * BATCH) {
+    uint4 u[BATCH];
 #pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const unsigned long long key =
-          ((unsigned long long)fkey(x[e]) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)(c + e));
-      best = umax64(best, key);
+    for (int q = 0; q < BATCH; ++q) {
+      const int c = c0 + q * ARGMAX_THREADS * PER;
+      if (c < vocab) u[q] = ld_nc_v4(p + c);
+    }
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      const int c = c0 + q * ARGMAX_THREADS * PER;
+      if (c < vocab) {
+        float x[PER];
+        Elem<T>::unpack(u[q], x);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) {
+          const unsigned long long key = ((unsigned long long)fkey(x[e]) << 32) |
+                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(c + e));
+          best = umax64(best, key);
+        }
+      }
     }
   }
 #pragma unroll
