@@ -27,8 +27,11 @@ constexpr int RMAX = 32;                 // refined groups re-scored in shared m
 constexpr int CACHE_GROUPS = 3072;       // records cached in shared memory up to this many groups
 constexpr int BITMAP_WORDS = (DH_MAX_VOCAB / GROUP + 31) / 32;
 
+constexpr int HIST_BINS = 4096;  // widest radix digit (12 bits)
+
 struct Shared {
-  uint32_t hist[256];
+  uint32_t hist[HIST_BINS];
+  uint32_t wsum[SEL_THREADS / 32];
   uint32_t digit, run, bincount, total, cnt, nref;
   int32_t rg[RMAX];
   uint32_t bitmap[BITMAP_WORDS];
@@ -49,61 +52,84 @@ __device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
 //   total      number of included entries (if total < k nothing else is meaningful)
 //   exact_ge   true: exactly k entries have x >= thr
 //              false: thr is the k-th largest value, `above` entries have x > thr and the
-//              `need` = k - above entries still to take have x == thr (more than `need` do)
+//              k - above entries still to take have x == thr (more than that many do)
 struct Kth {
   uint32_t thr, above, total;
   bool exact_ge;
 };
 
-// MSB-first radix select with 8-bit digits.  sel(key, id, x) decides inclusion and sets x.  Stops
-// early as soon as the bin holding the k-th value contains exactly the entries still needed.
+// Finds, over the bins of sh.hist[0..nbins) read from the highest down, the bin where the running
+// count reaches krem; sets sh.digit, sh.run (count above it), sh.bincount and, if set_total,
+// sh.total.  Each of the nbins / 8 first threads owns 8 consecutive bins.
+__device__ __forceinline__ void find_digit(Shared& sh, int nbins, uint32_t krem, bool set_total) {
+  const int users = nbins / 8;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t c[8], sum = 0;
+  if ((int)threadIdx.x < users) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q) { c[q] = sh.hist[nbins - 1 - 8 * (int)threadIdx.x - q]; sum += c[q]; }
+  }
+  uint32_t incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  uint32_t before = 0;
+  if (users > 32) {
+    if (lane == 31) sh.wsum[warp] = incl;
+    __syncthreads();
+    for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+  }
+  incl += before;
+  const uint32_t excl = incl - sum;
+  if ((int)threadIdx.x < users) {
+    if (set_total && (int)threadIdx.x == users - 1) sh.total = incl;
+    if (excl < krem && krem <= incl) {
+      uint32_t run = excl;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (run + c[q] >= krem) {
+          sh.digit = (uint32_t)(nbins - 1 - 8 * (int)threadIdx.x - q); sh.run = run; sh.bincount = c[q];
+          break;
+        }
+        run += c[q];
+      }
+    }
+    if ((int)threadIdx.x == users - 1 && incl < krem) { sh.digit = 0; sh.run = incl; sh.bincount = 0; }
+  }
+}
+
+// MSB-first radix select with digits of 12, 12 and 8 bits.  sel(key, id, x) decides inclusion and
+// sets x.  Stops as soon as the bin holding the k-th value contains exactly the entries still
+// needed.
 template <class Enum, class Sel>
 __device__ Kth radix_kth(Enum en, Sel sel, uint32_t k, Shared& sh) {
+  constexpr int SHIFTS[3] = {20, 8, 0};
+  constexpr int BITS[3] = {12, 12, 8};
   uint32_t prefix = 0, mask = 0, krem = k, above = 0;
-  const int lane = threadIdx.x & 31;
   Kth res;
-  for (int shift = 24; shift >= 0; shift -= 8) {
-    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh.hist[i] = 0;
+#pragma unroll 1
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = SHIFTS[pass], nbins = 1 << BITS[pass];
+    const uint32_t dmask = (uint32_t)nbins - 1u;
+    for (int i = threadIdx.x; i < nbins; i += blockDim.x) sh.hist[i] = 0;
     __syncthreads();
     en([&](uint32_t key, uint32_t id) {
       uint32_t x;
-      if (sel(key, id, x) && (x & mask) == prefix) hist_add(sh.hist, (x >> shift) & 255u);
+      if (sel(key, id, x) && (x & mask) == prefix) hist_add(sh.hist, (x >> shift) & dmask);
     });
     __syncthreads();
-    if (threadIdx.x < 32) {
-      uint32_t c[8], sum = 0;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) { c[q] = sh.hist[255 - 8 * lane - q]; sum += c[q]; }
-      uint32_t incl = sum;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      const uint32_t excl = incl - sum;
-      if (shift == 24 && lane == 31) sh.total = incl;
-      if (excl < krem && krem <= incl) {
-        uint32_t run = excl;
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          if (run + c[q] >= krem) {
-            sh.digit = 255u - 8u * lane - q; sh.run = run; sh.bincount = c[q];
-            break;
-          }
-          run += c[q];
-        }
-      }
-      if (lane == 31 && incl < krem) { sh.digit = 0; sh.run = incl; sh.bincount = 0; }
-    }
+    find_digit(sh, nbins, krem, pass == 0);
     __syncthreads();
     const uint32_t dg = sh.digit, run = sh.run, bc = sh.bincount, total = sh.total;
     __syncthreads();
-    if (shift == 24 && total < k) {
+    if (pass == 0 && total < k) {
       res.thr = 0; res.above = 0; res.total = total; res.exact_ge = false;
       return res;
     }
     prefix |= dg << shift;
-    mask |= 0xFFu << shift;
+    mask |= dmask << shift;
     krem -= run;
     above += run;
     if (bc == krem) {
@@ -113,6 +139,73 @@ __device__ Kth radix_kth(Enum en, Sel sel, uint32_t k, Shared& sh) {
   }
   res.thr = prefix; res.above = above; res.total = sh.total; res.exact_ge = false;
   return res;
+}
+
+// (key, id) ranks before (key2, id2): larger key first, then smaller id.
+__device__ __forceinline__ bool key_before(uint32_t ka, uint32_t ia, uint32_t kb, uint32_t ib) {
+  return ka > kb || (ka == kb && ia < ib);
+}
+
+// Sorts sh.sk/sh.si[0..K) (padded to a power of two) into ranking order.  K <= 64: one warp with
+// shuffles; larger K: a block-wide bitonic network in shared memory.
+__device__ inline void sort_selected(Shared& sh, int K) {
+  int P = 1;
+  while (P < K) P <<= 1;
+  for (int i = K + threadIdx.x; i < P; i += blockDim.x) { sh.sk[i] = 0u; sh.si[i] = 0xFFFFFFFFu; }
+  __syncthreads();
+  if (P <= 64) {
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      uint32_t k0 = 0, i0 = 0xFFFFFFFFu, k1 = 0, i1 = 0xFFFFFFFFu;
+      if (2 * lane < P) { k0 = sh.sk[2 * lane]; i0 = sh.si[2 * lane]; }
+      if (2 * lane + 1 < P) { k1 = sh.sk[2 * lane + 1]; i1 = sh.si[2 * lane + 1]; }
+      for (int size = 2; size <= 64; size <<= 1) {
+        for (int j = size >> 1; j > 0; j >>= 1) {
+          if (j == 1) {
+            const int p0 = 2 * lane;
+            const bool up = (p0 & size) == 0;
+            const bool b_first = key_before(k1, i1, k0, i0);
+            if (b_first == up) {
+              uint32_t tk = k0, ti = i0;
+              k0 = k1; i0 = i1; k1 = tk; i1 = ti;
+            }
+          } else {
+            const int src = lane ^ (j >> 1);
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              uint32_t& mk = e ? k1 : k0;
+              uint32_t& mi = e ? i1 : i0;
+              const uint32_t ok_ = __shfl_sync(0xFFFFFFFFu, mk, src);
+              const uint32_t oi = __shfl_sync(0xFFFFFFFFu, mi, src);
+              const int p = 2 * lane + e;
+              const bool up = (p & size) == 0;
+              const bool lower = (p & j) == 0;
+              const bool mine_first = key_before(mk, mi, ok_, oi);
+              const bool keep_first = (up == lower);
+              if (keep_first != mine_first) { mk = ok_; mi = oi; }
+            }
+          }
+        }
+      }
+      if (2 * lane < P) { sh.sk[2 * lane] = k0; sh.si[2 * lane] = i0; }
+      if (2 * lane + 1 < P) { sh.sk[2 * lane + 1] = k1; sh.si[2 * lane + 1] = i1; }
+    }
+    __syncthreads();
+    return;
+  }
+  for (int size = 2; size <= P; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      __syncthreads();
+      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
+        const int a0 = 2 * i - (i & (stride - 1));
+        const int b0 = a0 + stride;
+        const bool up = (a0 & size) == 0;
+        const uint32_t ka = sh.sk[a0], kb = sh.sk[b0], ia = sh.si[a0], ib = sh.si[b0];
+        if (key_before(kb, ib, ka, ia) == up) { sh.sk[a0] = kb; sh.sk[b0] = ka; sh.si[a0] = ib; sh.si[b0] = ia; }
+      }
+    }
+  }
+  __syncthreads();
 }
 
 // Selects the K best entries (score key desc, id asc) of en, sorts them and writes the row; the
@@ -141,23 +234,7 @@ __device__ bool select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
     }
   });
   __syncthreads();
-  int P = 1;
-  while (P < K) P <<= 1;
-  for (int i = K + threadIdx.x; i < P; i += blockDim.x) { sh.sk[i] = 0u; sh.si[i] = 0xFFFFFFFFu; }
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int a0 = 2 * i - (i & (stride - 1));
-        const int b0 = a0 + stride;
-        const bool up = (a0 & size) == 0;
-        const uint32_t ka = sh.sk[a0], kb = sh.sk[b0], ia = sh.si[a0], ib = sh.si[b0];
-        const bool b_first = kb > ka || (kb == ka && ib < ia);
-        if (b_first == up) { sh.sk[a0] = kb; sh.sk[b0] = ka; sh.si[a0] = ib; sh.si[b0] = ia; }
-      }
-    }
-  }
-  __syncthreads();
+  sort_selected(sh, K);
   for (int k = threadIdx.x; k < K; k += blockDim.x) {
     idx_out[k] = (int32_t)sh.si[k];
     score_out[k] = fkey_inv(sh.sk[k]);
@@ -195,8 +272,20 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
 
   for (int g = threadIdx.x; g < (int)BITMAP_WORDS; g += blockDim.x) sh.bitmap[g] = 0u;
   for (int j = threadIdx.x; j < r; j += blockDim.x) sh.t[j] = Elem<T>::to_f(t_row[j]);
-  if (cached)
-    for (int g = threadIdx.x; g < n_groups; g += blockDim.x) cache[g] = rrow[g];
+  if (cached) {
+    constexpr int PER_THREAD = (CACHE_GROUPS + SEL_THREADS - 1) / SEL_THREADS;
+    GroupRec tmp[PER_THREAD];
+#pragma unroll
+    for (int q = 0; q < PER_THREAD; ++q) {
+      const int g = threadIdx.x + q * SEL_THREADS;
+      if (g < n_groups) tmp[q] = rrow[g];
+    }
+#pragma unroll
+    for (int q = 0; q < PER_THREAD; ++q) {
+      const int g = threadIdx.x + q * SEL_THREADS;
+      if (g < n_groups) cache[g] = tmp[q];
+    }
+  }
   if (threadIdx.x == 0) sh.nref = 0;
   __syncthreads();
   const GroupRec* src = cached ? cache : rrow;
