@@ -197,6 +197,8 @@ def traffic_from_profiles(kernel: str, workload: str, files):
 # ------------------------------------------------------------------------------------- head
 
 KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
+                "small_b": ["small_b.cu", "select.cuh", "grid_sync.cuh", "sm100.cuh", "dh_internal.cuh"],
+                "lowrank_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
                 "select": ["select.cu", "dh_internal.cuh"],
                 "rescore": ["rescore.cu", "dh_internal.cuh"],
                 "proj_partial": ["proj.cu", "dh_internal.cuh"],
@@ -211,11 +213,18 @@ def head_bytes(cfg):
 
 
 def kernel_algo(cfg, name):
-    """(bound, algorithmic bytes or flops per launch, unit) of a head kernel."""
+    """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
+    or tensor FLOPs of the dense contraction (rows beyond B padded by the kernel are not counted)."""
     e = 2 if cfg.dtype == "bf16" else 4
+    if name == "small_b":  # projection + vocabulary scores + selection, one launch
+        return "hbm", cfg.d * cfg.r * e + cfg.r * cfg.vocab * e + cfg.B * cfg.d * e, "GB/s"
     if name == "scores_summary":
         return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
-    if name in ("proj_partial",):
+    if name == "lowrank_mma":
+        return "tensor", 2.0 * cfg.B * cfg.r * cfg.vocab, "TFLOP/s"
+    if name == "proj_mma":
+        return "tensor", 2.0 * cfg.B * cfg.d * cfg.r, "TFLOP/s"
+    if name == "proj_partial":
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
     if name == "rescore":
         return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
@@ -301,14 +310,19 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     dom = max(stages, key=lambda k: stages[k]["us_avg"])
     bound, algo, unit = kernel_algo(cfg, dom)
     dur_s = stages[dom]["us_avg"] * 1e-6
-    achieved = algo / dur_s / 1e9
-    peak = peaks["hbm_gbs"]
+    if bound == "tensor":
+        achieved = algo / dur_s / 1e12
+        peak = peaks["bf16_tflops"]
+        peak_src_s = f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"
+    else:
+        achieved = algo / dur_s / 1e9
+        peak = peaks["hbm_gbs"]
+        peak_src_s = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
     traffic = traffic_from_profiles(dom, cfg.name, KERNEL_FILES.get(dom, []))
     roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak,
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                "algorithmic_bytes_per_launch": algo, "us_per_launch": round(stages[dom]["us_avg"], 3),
-                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
-                else "fallback 6.8 TB/s"}
+                ("algorithmic_flops_per_launch" if bound == "tensor" else "algorithmic_bytes_per_launch"): algo,
+                "us_per_launch": round(stages[dom]["us_avg"], 3), "peak_source": peak_src_s}
     path_ach = per_step / (us_per_call * 1e-6) / 1e9
     path_roofline = {"bound": "hbm", "bytes_per_call": per_step, "achieved": round(path_ach, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(path_ach / peak, 4),
