@@ -54,15 +54,15 @@ struct Top2 {
     v1 = v2 = v3 = -INFINITY;
     i1 = i2 = 0xFFFFFFFFu;
   }
-  // Pairs must arrive in increasing id order for ties to keep the lower id.
+  // Pairs must arrive in increasing id order for ties to keep the lower id.  Branch-free (three
+  // compares and selects), so the lanes of a warp never diverge on their data.
   __device__ __forceinline__ void push(float x, uint32_t id) {
-    if (x > v1) {
-      v3 = v2; v2 = v1; i2 = i1; v1 = x; i1 = id;
-    } else if (x > v2) {
-      v3 = v2; v2 = x; i2 = id;
-    } else if (x > v3) {
-      v3 = x;
-    }
+    const bool c1 = x > v1, c2 = x > v2, c3 = x > v3;
+    v3 = c2 ? v2 : (c3 ? x : v3);
+    v2 = c1 ? v1 : (c2 ? x : v2);
+    i2 = c1 ? i1 : (c2 ? id : i2);
+    v1 = c1 ? x : v1;
+    i1 = c1 ? id : i1;
   }
   // Merge with another summary of a disjoint set of ids.
   __device__ __forceinline__ void merge(float bv1, uint32_t bi1, float bv2, uint32_t bi2, float bv3) {

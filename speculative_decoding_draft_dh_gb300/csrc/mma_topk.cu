@@ -13,8 +13,9 @@
 //   warp 0     TMA producer: streams V in stages of 64 (K) x 256 (N) bf16 (four 64 x 64 boxes).
 //   warp 1     TMEM allocator and MMA issuer: per vocabulary tile, r/16 tcgen05.mma
 //              (M=128, N=256, K=16, A K-major, B N-major) into one of two TMEM accumulators.
-//   warps 2-5  epilogue: tcgen05.ld 32x32b (thread = row), per-group top-two + third score,
-//              one 16-byte record store per (row, group).
+//   warps 2-9  epilogue: tcgen05.ld 32x32b (thread = row); two warps per TMEM lane quarter, each
+//              owning two of the tile's four 64-id groups; branch-free per-group top-two + third
+//              score; one 16-byte record store per (row, group).
 // Every mbarrier wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word;
 // the CTA then drains its outstanding copies and MMAs (again with bounded waits) and frees TMEM.
 #include "dh_internal.cuh"
@@ -31,7 +32,8 @@ constexpr int BK = 64;
 constexpr int A_CHUNK_BYTES = BM * BK * 2;  // 16 KB: 128 rows x 128 bytes
 constexpr int B_BOX_BYTES = BK * 64 * 2;    // 8 KB: 64 K-rows x 64 ids
 constexpr int B_STAGE_BYTES = 4 * B_BOX_BYTES;
-constexpr int THREADS = 192;
+constexpr int THREADS = 320;         // producer, MMA issuer, 8 epilogue warps
+constexpr int EPI_WARPS = 8;
 constexpr uint32_t TMEM_COLS = 512;  // two 128 x 256 fp32 accumulators
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr int MAX_STAGES = 8;
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], 4);
+      mbar_init(&acc_empty[i], EPI_WARPS);
     }
     fence_barrier_init();
   }
@@ -161,8 +163,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_wait(drain, 0, WAIT_NS);
     }
   } else {
-    // -------------------------------------------------------------- epilogue (warps 2-5)
-    const int q = warp & 3;  // TMEM lanes [32q, 32q + 32) are accessible to this warp
+    // -------------------------------------------------------------- epilogue (warps 2-9)
+    const int q = warp & 3;             // TMEM lanes [32q, 32q + 32) are accessible to this warp
+    const int half = (warp - 2) >> 2;   // groups 2*half and 2*half + 1 of each tile
     const int row = m * BM + q * 32 + lane;
     const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
     for (int t = 0; t < ntiles; ++t) {
@@ -176,7 +179,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int n0 = (nt0 + t) * BN;
 #pragma unroll 1
-      for (int g = 0; g < BN / GROUP; ++g) {
+      for (int gg = 0; gg < 2; ++gg) {
+        const int g = half * 2 + gg;
         const int gc0 = n0 + g * GROUP;
         Top2 sm;
         sm.init();
@@ -184,10 +188,13 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int h2 = 0; h2 < 2; ++h2) {
           float v[32];
           tmem_ld_32x32b_x32(lane_addr + (uint32_t)(buf * BN + g * GROUP + h2 * 32), v);
+          if (gc0 + GROUP <= p.vocab) {
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int c = gc0 + h2 * 32 + i;
-            if (c < p.vocab) sm.push(v[i], (uint32_t)c);
+            for (int i = 0; i < 32; ++i) sm.push(v[i], (uint32_t)(gc0 + h2 * 32 + i));
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+              if (gc0 + h2 * 32 + i < p.vocab) sm.push(v[i], (uint32_t)(gc0 + h2 * 32 + i));
           }
         }
         if (row < p.B && gc0 < p.vocab) p.recs[(size_t)row * p.n_groups + gc0 / GROUP] = sm.record((uint32_t)gc0);
@@ -304,7 +311,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       mma_commit(drain);
       mbar_wait(drain, 0, WAIT_NS);
     }
-  } else {
+  } else if (warp < 6) {  // warps 2-5 cover the four TMEM lane quarters
     const int q = warp & 3;
     const int row = m * BM + q * 32 + lane;
     if (__all_sync(0xFFFFFFFFu, mbar_wait(acc_full, 0, WAIT_NS))) {
