@@ -8,9 +8,10 @@
 // Inference Speed by Adapting to Serving Load", section "Runtime-sized speculation": top-k = 1
 // drafts a chain, larger k a tree.
 //
-// k_tree_argmax: one block per (request, node) row scans the vocabulary with 16-byte loads and
-// reduces a packed 64-bit key (order-preserving score bits, then the complement of the id) so that
-// ties resolve to the lowest id exactly.  This scan is all of the step's memory traffic.
+// k_tree_argmax: one block per (request, node) row scans the vocabulary with 16-byte loads, keeps
+// a running (max, id) per thread and reduces a packed 64-bit key (order-preserving score bits, then
+// the complement of the id) so that ties resolve to the lowest id exactly.  This scan is all of the
+// step's memory traffic.
 // k_tree_walk: one block per request; thread n checks its edge, pointer jumping gives every node
 // "all edges to the root accepted" and its depth, a block max picks the deepest accepted node
 // (lowest index on ties) and thread 0 writes the path.
@@ -25,6 +26,10 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
   return a > b ? a : b;
 }
 
+// Each thread scans its 16-byte vectors in increasing id order keeping (best value, its id).  Per
+// vector it takes the max with an fmax tree and only searches for the id when that max beats the
+// running best (strictly: an equal value later in the row has a larger id), which happens a few
+// times per thread.  The block then reduces (value, id) with ties to the lower id.
 template <typename T>
 __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restrict__ logits, int vocab,
                                                                 int32_t* __restrict__ am) {
@@ -33,7 +38,8 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restr
   __shared__ unsigned long long red[ARGMAX_THREADS / 32];
   const size_t row = blockIdx.x;
   const T* p = logits + row * (size_t)vocab;
-  unsigned long long best = 0ull;
+  float best = -INFINITY;
+  int best_id = -1;
   for (int c0 = threadIdx.x * PER; c0 < vocab; c0 += ARGMAX_THREADS * PER * BATCH) {
     uint4 u[BATCH];
 #pragma unroll
@@ -47,22 +53,30 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restr
       if (c < vocab) {
         float x[PER];
         Elem<T>::unpack(u[q], x);
+        float m = x[0];
 #pragma unroll
-        for (int e = 0; e < PER; ++e) {
-          const unsigned long long key = ((unsigned long long)fkey(x[e]) << 32) |
-                                         (unsigned long long)(0xFFFFFFFFu - (uint32_t)(c + e));
-          best = umax64(best, key);
+        for (int e = 1; e < PER; ++e) m = fmaxf(m, x[e]);
+        if (m > best || best_id < 0) {
+          int e0 = 0;
+#pragma unroll
+          for (int e = PER - 1; e >= 0; --e)
+            if (x[e] == m) e0 = e;  // first position holding the max
+          best = m;
+          best_id = c + e0;
         }
       }
     }
   }
+  unsigned long long key = best_id < 0 ? 0ull
+                                        : ((unsigned long long)fkey(best) << 32) |
+                                              (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_id);
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) best = umax64(best, __shfl_xor_sync(0xFFFFFFFFu, best, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = best;
+  for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = key;
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < ARGMAX_THREADS / 32; ++w) best = umax64(best, red[w]);
-    am[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(best & 0xFFFFFFFFull));
+    for (int w = 1; w < ARGMAX_THREADS / 32; ++w) key = umax64(key, red[w]);
+    am[row] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
   }
 }
 
