@@ -5,7 +5,7 @@ namespace dh {
 namespace {
 
 template <typename T>
-__global__ void __launch_bounds__(sel::SEL_THREADS) k_select(const GroupRec* __restrict__ recs,
+__global__ void __launch_bounds__(sel::SEL_THREADS, 1) k_select(const GroupRec* __restrict__ recs,
                                                             const T* __restrict__ t, const T* __restrict__ V,
                                                             int r, int vocab, int K, int32_t* __restrict__ idx_out,
                                                             float* __restrict__ score_out) {

@@ -41,12 +41,9 @@ struct Shared {
   uint32_t si[DH_MAX_K];
 };
 
-// Histogram increment aggregated over the lanes of a warp that hit the same bin (score keys
-// crowd into a few exponent bins, so plain atomics would serialise).
-__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) {
-  const unsigned peers = __match_any_sync(__activemask(), bin);
-  if ((int)(threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
-}
+// Histogram increment (shared-memory atomic; 12-bit digits spread the keys over enough bins that
+// conflicts stay low).
+__device__ __forceinline__ void hist_add(uint32_t* hist, uint32_t bin) { atomicAdd(&hist[bin], 1u); }
 
 // Result of a radix selection of the k-th largest value x over the included entries.
 //   total      number of included entries (if total < k nothing else is meaningful)
@@ -247,8 +244,49 @@ __device__ bool select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
 template <typename T>
 __device__ __forceinline__ float score_col(const float* t, const T* V, int r, int vocab, int c) {
   float acc = 0.f;
+#pragma unroll 16
   for (int j = 0; j < r; ++j) acc = fmaf(t[j], Elem<T>::to_f(V[(size_t)j * vocab + c]), acc);
   return acc;
+}
+
+// Exact scores of the 64 ids of group g (ids >= vocab give -inf) into out[0..64).  The block's
+// warps split the r rows of V: warp w covers rows [w*rw, (w+1)*rw) with all its loads in flight
+// (lane i reads the two ids 2i, 2i+1), then the per-warp partial sums are added in warp order
+// (a fixed order, so the result is deterministic).  scratch: SEL_THREADS / 32 * 64 floats.
+template <typename T>
+__device__ void score_group(const float* t, const T* __restrict__ V, int r, int vocab, int g, float* out,
+                            float* scratch) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  const int rw = (r + nw - 1) / nw;
+  const int j0 = warp * rw, j1 = min(r, j0 + rw);
+  const int c = g * GROUP + 2 * lane;
+  float a0 = 0.f, a1 = 0.f;
+  constexpr int BATCH = 16;
+  for (int jb = j0; jb < j1; jb += BATCH) {
+    float v0[BATCH], v1[BATCH];
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      const int j = jb + q;
+      v0[q] = (j < j1 && c < vocab) ? Elem<T>::to_f(V[(size_t)j * vocab + c]) : 0.f;
+      v1[q] = (j < j1 && c + 1 < vocab) ? Elem<T>::to_f(V[(size_t)j * vocab + c + 1]) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < BATCH; ++q) {
+      const int j = jb + q;
+      const float tj = (j < j1) ? t[j] : 0.f;
+      a0 = fmaf(tj, v0[q], a0);
+      a1 = fmaf(tj, v1[q], a1);
+    }
+  }
+  scratch[warp * 64 + 2 * lane] = a0;
+  scratch[warp * 64 + 2 * lane + 1] = a1;
+  __syncthreads();
+  if (threadIdx.x < 64) {
+    float s = 0.f;
+    for (int w = 0; w < nw; ++w) s += scratch[w * 64 + threadIdx.x];
+    out[threadIdx.x] = (g * GROUP + (int)threadIdx.x < vocab) ? s : -INFINITY;
+  }
+  __syncthreads();
 }
 
 
@@ -315,11 +353,8 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
     const int nref = (int)sh.nref;
     if (nref == 0) return;
     if (nref <= RMAX) {
-      for (int e = threadIdx.x; e < nref * GROUP; e += blockDim.x) {
-        const int c = sh.rg[e / GROUP] * GROUP + (e % GROUP);
-        sh.rs[e] = (c < vocab) ? score_col(sh.t, V, r, vocab, c) : -INFINITY;
-      }
-      __syncthreads();
+      for (int i = 0; i < nref; ++i)
+        score_group(sh.t, V, r, vocab, sh.rg[i], sh.rs + i * GROUP, reinterpret_cast<float*>(sh.hist));
       auto refined = [&](auto f) {
         pool(f);  // skips the refined groups (bitmap)
         for (int e = threadIdx.x; e < nref * GROUP; e += blockDim.x) {

@@ -63,6 +63,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64
 
 // ---------------------------------------------------------------- TMA
 
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy (TMA)
+// accesses to the same shared memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // 2-D tiled bulk tensor load into shared memory, completing on `bar` (transaction bytes).
 __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
   asm volatile(

@@ -8,16 +8,19 @@
 // plus every serial dependency: h U must finish before t V, and the global top-K before rescoring.
 // Running the steps in one resident grid removes the kernel boundaries between them.
 //
-// One block per SM (grid = SM count), 16 warps.  Each warp owns one or more groups of 64
-// vocabulary ids and three 4 KB TMA stages of V (64 ids x 32 bf16 rows, or 16 fp32 rows).
-//   P0  each warp issues the TMA loads of its first three stages (V does not depend on t).
+// One block per SM (grid = SM count), 16 warps.  Each block owns a contiguous run of 256-id
+// tiles and streams them in sets of four: a stage is four TMA boxes of 256 ids x 16 bf16 rows (8
+// fp32 rows) = 32 KB, i.e. 2 KB contiguous per V row, with six stages in flight.
+//   P0  thread 0 issues the TMA loads of the first six stages (V does not depend on t).
 //   P1  block c computes the partial products of h with the d-slice c of U for every (row, column)
 //       and writes them to the workspace; grid barrier.
 //   P2  every block sums the partials of every t element in the same fixed order (so all blocks
 //       hold bit-identical t), rounds to the activation dtype and keeps t in shared memory;
 //       block 0 also writes t for the selection's re-scoring step.
-//   P3  each warp streams its groups: lane i scores ids 2i and 2i+1 of the group for all rows,
-//       then a shuffle butterfly folds the 64 scores into the group record.  grid barrier.
+//   P3  warp w scores the 64-id group w of the current set: lane i accumulates ids 2i and 2i+1
+//       for all rows over the stages; after the last band a shuffle butterfly folds the 64
+//       scores into the group record.  A block barrier per stage frees its slot for the next
+//       TMA load.  grid barrier.
 //   P4  block b (< B) selects row b exactly from its records (select.cuh), reusing the V staging
 //       buffers as scratch.
 // Grid barriers are sense-reversing counters in the workspace; every wait (barrier or TMA) gives
@@ -34,19 +37,22 @@ using namespace sm100;
 
 constexpr int SB_THREADS = 512;
 constexpr int SB_WARPS = SB_THREADS / 32;
-constexpr int NS = 3;              // TMA stages per warp
-constexpr int STAGE_BYTES = 4096;  // one box of 64 ids x (4096 / (64 * sizeof(T))) rows
+constexpr int TILE = 256;            // vocabulary ids per TMA box
+constexpr int SET_TILES = 4;         // tiles streamed together (16 warps x 64 ids)
+constexpr int NS = 6;                // stages in flight
+constexpr int STAGE_BYTES = 32768;   // SET_TILES boxes of 256 ids x (32 KB / 4 / 256 / sizeof(T)) rows
 constexpr int MAX_B = 8;
 constexpr int MAX_BR = 2048;  // B * r values of t kept in shared memory
 constexpr int CH = 40;        // projection rows per batch of loads in flight
+constexpr int RED = 48;       // partial sums per lane in flight in the t reduction
 constexpr uint64_t WAIT_NS = 2000000000ull;
-constexpr size_t STAGE_REGION = (size_t)SB_WARPS * NS * STAGE_BYTES;
+constexpr size_t STAGE_REGION = (size_t)NS * STAGE_BYTES;
 
 struct SbParams {
   const void* h;
   const void* U;
   const void* V;
-  int B, d, r, vocab, K, n_groups;
+  int B, d, r, vocab, K, n_groups, n_tiles;
   float* partial;  // [B*r][gridDim.x]
   void* t_out;     // [B][r] in the activation dtype
   GroupRec* recs;  // [B][n_groups]
@@ -56,17 +62,30 @@ struct SbParams {
   int* status;
 };
 
-__device__ __forceinline__ void fence_proxy_async_smem() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+// Two adjacent values of row-major storage as floats (4-byte load for bf16, 8-byte for fp32).
+template <typename T>
+__device__ __forceinline__ void load_pair(const T* p, float& a, float& b);
+template <>
+__device__ __forceinline__ void load_pair<__nv_bfloat16>(const __nv_bfloat16* p, float& a, float& b) {
+  const uint32_t w = __ldg(reinterpret_cast<const unsigned int*>(p));
+  a = __uint_as_float(w << 16);
+  b = __uint_as_float(w & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void load_pair<float>(const float* p, float& a, float& b) {
+  const float2 f = __ldg(reinterpret_cast<const float2*>(p));
+  a = f.x;
+  b = f.y;
 }
 
 template <typename T>
 __global__ void __launch_bounds__(SB_THREADS, 1)
     k_small_b(const __grid_constant__ CUtensorMap tmV, SbParams p) {
-  constexpr int ROWS = STAGE_BYTES / (GROUP * (int)sizeof(T));  // V rows per stage
+  constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));  // V rows per stage
+  constexpr int ROW_BYTES = TILE * (int)sizeof(T);                        // one box row
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t full[SB_WARPS][NS];
-  __shared__ float st[MAX_BR];       // t as fp32, [B][r]
+  __shared__ uint64_t full[NS];
+  __shared__ float st[MAX_BR];        // t as fp32, [B][r]
   __shared__ float sh_h[MAX_B * CH];  // the block's slice of h
   __shared__ volatile int s_fail;
 
@@ -75,35 +94,36 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
   const int B = p.B, r = p.r, BR = p.B * p.r;
-  const int spg = r / ROWS;  // stages per group
+  const int bands = r / RB;  // stages per tile set
 
-  // this block's groups, and this warp's share of them
-  const int g0 = (int)((long long)p.n_groups * c / G), g1 = (int)((long long)p.n_groups * (c + 1) / G);
-  const int my_groups = (g1 - g0 > warp) ? (g1 - g0 - warp + SB_WARPS - 1) / SB_WARPS : 0;
-  const int total_stages = my_groups * spg;
+  // this block's 256-id tiles, streamed in sets of up to four
+  const int t0 = (int)((long long)p.n_tiles * c / G), t1 = (int)((long long)p.n_tiles * (c + 1) / G);
+  const int n_sets = (t1 - t0 + SET_TILES - 1) / SET_TILES;
+  const int total_stages = n_sets * bands;
 
   if (threadIdx.x == 0) {
     s_fail = 0;
-    for (int w = 0; w < SB_WARPS; ++w)
-      for (int s = 0; s < NS; ++s) mbar_init(&full[w][s], 1);
+    for (int s = 0; s < NS; ++s) mbar_init(&full[s], 1);
     fence_barrier_init();
   }
   __syncthreads();
 
-  unsigned char* wstage = stages + (size_t)warp * NS * STAGE_BYTES;
-  int issued = 0;    // stages this warp has asked TMA for (meaningful in lane 0)
-  int consumed = 0;  // stages this warp has waited for and read
-  auto issue = [&](int q) {  // stage q of this warp into slot q % NS (lane 0 only)
-    const int g = g0 + warp + (q / spg) * SB_WARPS;
-    const int row0 = (q % spg) * ROWS;
-    uint64_t* bar = &full[warp][q % NS];
-    mbar_arrive_expect_tx(bar, STAGE_BYTES);
-    tma_load_2d(wstage + (q % NS) * STAGE_BYTES, &tmV, g * GROUP, row0, bar);
+  int issued = 0;    // stages asked of TMA (thread 0)
+  int consumed = 0;  // stages read by the block
+  auto issue = [&](int q) {  // stage q into slot q % NS (thread 0 only)
+    const int set = q / bands, band = q % bands;
+    const int tile = t0 + set * SET_TILES;
+    const int nt = min(SET_TILES, t1 - tile);
+    uint64_t* bar = &full[q % NS];
+    mbar_arrive_expect_tx(bar, (uint32_t)(nt * TILE * RB * sizeof(T)));
+    for (int k = 0; k < nt; ++k)
+      tma_load_2d(stages + (size_t)(q % NS) * STAGE_BYTES + (size_t)k * RB * ROW_BYTES, &tmV, (tile + k) * TILE,
+                  band * RB, bar);
     issued = q + 1;
   };
 
   // ---------------------------------------------------------------- P0: V prefetch
-  if (lane == 0) {
+  if (threadIdx.x == 0) {
     prefetch_tmap(&tmV);
     for (int q = 0; q < NS && q < total_stages; ++q) issue(q);
   }
@@ -127,12 +147,8 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
         const T* up = U + (size_t)base * r + 2 * jp;
         float u[CH][2];
 #pragma unroll
-        for (int i = 0; i < CH; ++i) {
-          if (i < n) {
-            u[i][0] = Elem<T>::to_f(up[(size_t)i * r]);
-            u[i][1] = Elem<T>::to_f(up[(size_t)i * r + 1]);
-          }
-        }
+        for (int i = 0; i < CH; ++i)
+          if (i < n) load_pair<T>(up + (size_t)i * r, u[i][0], u[i][1]);
         float a0 = 0.f, a1 = 0.f;
 #pragma unroll
         for (int i = 0; i < CH; ++i) {
@@ -167,12 +183,12 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       float acc = 0.f;
       if (e < BR) {
         const float* src = p.partial + (size_t)e * G;
-        for (int k0 = sub; k0 < G; k0 += 16 * L) {
-          float v[16];
+        for (int k0 = sub; k0 < G; k0 += RED * L) {
+          float v[RED];
 #pragma unroll
-          for (int q = 0; q < 16; ++q) v[q] = (k0 + q * L < G) ? __ldcg(src + k0 + q * L) : 0.f;
+          for (int q = 0; q < RED; ++q) v[q] = (k0 + q * L < G) ? __ldcg(src + k0 + q * L) : 0.f;
 #pragma unroll
-          for (int q = 0; q < 16; ++q) acc += v[q];
+          for (int q = 0; q < RED; ++q) acc += v[q];
         }
       }
       for (int o = L / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
@@ -187,31 +203,36 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
 
   // ---------------------------------------------------------------- P3: stream V, group records
   {
-    for (int k = 0; k < my_groups; ++k) {
-      const int g = g0 + warp + k * SB_WARPS;
-      float acc[MAX_B][2];
+    // warp w scores group (w % 4) of tile (w / 4) of the current set; lane i owns ids 2i, 2i+1
+    const int k_tile = warp / 4, g_in_tile = warp % 4;
+    float acc[MAX_B][2];
 #pragma unroll
-      for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
-      for (int rb = 0; rb < spg; ++rb) {
-        const int q = k * spg + rb;
-        // the outcome is made warp-uniform so that the lanes never split around __syncwarp
-        if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[warp][q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS))) {
-          if (lane == 0) atomicOr(p.status, 1 << DH_ERR_TIMEOUT);
-          s_fail = 1;
-          goto drain;
-        }
-        consumed = q + 1;
-        const unsigned char* tile = wstage + (q % NS) * STAGE_BYTES;
-        const int j0 = rb * ROWS;
-#pragma unroll 8
-        for (int j = 0; j < ROWS; ++j) {
+    for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
+    for (int q = 0; q < total_stages; ++q) {
+      const int set = q / bands, band = q % bands;
+      const int tile = t0 + set * SET_TILES + k_tile;
+      const bool mine = tile < t1;
+      // the outcome is made warp-uniform so that the lanes never split around the barriers
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS))) {
+        if (lane == 0) atomicOr(p.status, 1 << DH_ERR_TIMEOUT);
+        s_fail = 1;
+      }
+      __syncthreads();
+      if (s_fail) goto drain;
+      consumed = q + 1;
+      if (mine) {
+        const unsigned char* box = stages + (size_t)(q % NS) * STAGE_BYTES + (size_t)k_tile * RB * ROW_BYTES +
+                                   (size_t)(g_in_tile * GROUP + 2 * lane) * sizeof(T);
+        const int j0 = band * RB;
+#pragma unroll
+        for (int j = 0; j < RB; ++j) {
           float v0, v1;
           if (sizeof(T) == 2) {
-            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(tile + j * 128 + lane * 4);
+            const uint32_t w2 = *reinterpret_cast<const uint32_t*>(box + j * ROW_BYTES);
             v0 = __uint_as_float(w2 << 16);
             v1 = __uint_as_float(w2 & 0xFFFF0000u);
           } else {
-            const float2 f2 = *reinterpret_cast<const float2*>(tile + j * 256 + lane * 8);
+            const float2 f2 = *reinterpret_cast<const float2*>(box + j * ROW_BYTES);
             v0 = f2.x;
             v1 = f2.y;
           }
@@ -224,24 +245,31 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             }
           }
         }
-        __syncwarp();
-        if (lane == 0 && q + NS < total_stages) {
-          fence_proxy_async_smem();
-          issue(q + NS);
-        }
       }
-      const uint32_t id0 = (uint32_t)(g * GROUP + 2 * lane);
+      __syncthreads();  // every warp is done with slot q % NS
+      if (threadIdx.x == 0 && q + NS < total_stages) {
+        fence_proxy_async_smem();
+        issue(q + NS);
+      }
+      if (band == bands - 1) {
+        if (mine) {
+          const int g = tile * (TILE / GROUP) + g_in_tile;
+          const uint32_t id0 = (uint32_t)(g * GROUP + 2 * lane);
 #pragma unroll
-      for (int b = 0; b < MAX_B; ++b) {
-        if (b < B) {
-          Top2 sm;
-          sm.init();
-          if ((int)id0 < p.vocab) sm.push(acc[b][0], id0);
-          if ((int)id0 + 1 < p.vocab) sm.push(acc[b][1], id0 + 1);
+          for (int b = 0; b < MAX_B; ++b) {
+            if (b < B) {
+              Top2 sm;
+              sm.init();
+              if ((int)id0 < p.vocab) sm.push(acc[b][0], id0);
+              if ((int)id0 + 1 < p.vocab) sm.push(acc[b][1], id0 + 1);
 #pragma unroll
-          for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
-          if (lane == 0) p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
+              for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
+              if (lane == 0 && g < p.n_groups) p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
+            }
+          }
         }
+#pragma unroll
+        for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
       }
     }
   }
@@ -257,10 +285,10 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   return;
 
 drain:
-  // a failed wait: let every copy this warp issued and did not read land before the block exits
-  if (lane == 0)
-    for (int q = consumed; q < issued; ++q) mbar_wait(&full[warp][q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS);
-  __syncwarp();
+  // a failed wait: let every copy the block issued and did not read land before it exits
+  if (threadIdx.x == 0)
+    for (int q = consumed; q < issued; ++q) mbar_wait(&full[q % NS], (uint32_t)(q / NS) & 1u, WAIT_NS);
+  __syncthreads();
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -282,7 +310,7 @@ EncodeTiledFn encode_fn() {
 
 template <typename T>
 cudaError_t run(const Ctx& c, const SbParams& p0) {
-  constexpr int ROWS = STAGE_BYTES / (GROUP * (int)sizeof(T));
+  constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
   static unsigned long long smem_done = 0;
   cudaError_t e = allow_max_smem(k_small_b<T>, c.device, &smem_done);
   if (e != cudaSuccess) return e;
@@ -298,7 +326,7 @@ cudaError_t run(const Ctx& c, const SbParams& p0) {
   CUtensorMap tmV;
   cuuint64_t dims[2] = {(cuuint64_t)p0.vocab, (cuuint64_t)p0.r};
   cuuint64_t strides[1] = {(cuuint64_t)p0.vocab * sizeof(T)};
-  cuuint32_t box[2] = {(cuuint32_t)GROUP, (cuuint32_t)ROWS};
+  cuuint32_t box[2] = {(cuuint32_t)TILE, (cuuint32_t)RB};
   cuuint32_t estr[2] = {1, 1};
   if (fn(&tmV, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
          const_cast<void*>(p0.V), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -327,7 +355,7 @@ cudaError_t run(const Ctx& c, const SbParams& p0) {
 }  // namespace
 
 bool small_b_supported(int B, int r, int dtype) {
-  const int rows = STAGE_BYTES / (GROUP * (dtype == DH_BF16 ? 2 : 4));
+  const int rows = STAGE_BYTES / (SET_TILES * TILE * (dtype == DH_BF16 ? 2 : 4));
   return B >= 1 && B <= MAX_B && B * r <= MAX_BR && r % rows == 0 && r % 2 == 0;
 }
 
@@ -346,6 +374,7 @@ cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const voi
   p.vocab = vocab;
   p.K = K;
   p.n_groups = (vocab + GROUP - 1) / GROUP;
+  p.n_tiles = (vocab + TILE - 1) / TILE;
   p.partial = partial;
   p.t_out = t_out;
   p.recs = recs;
