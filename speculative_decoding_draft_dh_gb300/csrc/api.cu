@@ -201,8 +201,11 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
 
 // ------------------------------------------------------------------ stage 2
 
-size_t dh_exact_rescore_workspace(int B, int, int, int, int) {
-  return B > 0 ? WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256) : 0;
+size_t dh_exact_rescore_workspace(int B, int d, int vocab, int K, int dtype) {
+  if (B <= 0 || K <= 0) return 0;
+  size_t n = WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256);
+  if (rescore_uniq_used(B, d, K, dtype)) n += rescore_uniq_bytes(B, vocab, K);
+  return n;
 }
 
 int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
@@ -220,9 +223,18 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
-  if (note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets),
-                 "rescore") != cudaSuccess)
+  const char* f = std::getenv("DH_FORCE_RESCORE");
+  // the distinct-row path is opt-in (DH_FORCE_RESCORE=uniq) until it beats the direct kernel
+  const bool uniq = rescore_uniq_used(B, d, K, dtype) && f && std::strcmp(f, "uniq") == 0;
+  if (uniq) {
+    void* area = static_cast<char*>(workspace) + WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256);
+    if (note_error(launch_rescore_uniq(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets, area),
+                   "rescore (distinct rows)") != cudaSuccess)
+      return DH_ERR_CUDA;
+  } else if (note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets),
+                        "rescore") != cudaSuccess) {
     return DH_ERR_CUDA;
+  }
   return DH_OK;
 }
 
