@@ -171,10 +171,13 @@ cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, con
 
 bool rescore_supported(int d);
 bool rescore_uniq_used(int B, int d, int K, int dtype);
+cudaError_t launch_rescore_stream(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
+                                  int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
+                                  int* status);
 size_t rescore_uniq_bytes(int B, int vocab, int K);
 cudaError_t launch_rescore_uniq(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                 int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
-                                void* area);
+                                void* area, int* status);
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
                            int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
 
