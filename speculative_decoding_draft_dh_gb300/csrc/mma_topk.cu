@@ -339,13 +339,30 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// t[e] = bf16(sum over s of partial[s][e]), slices in ascending order (deterministic).
+// t[e] = bf16(sum over s of partial[s][e]), slices in ascending order (deterministic).  Each
+// thread owns four consecutive outputs (B*r is a multiple of 64) and keeps 8 slices in flight.
 __global__ void k_proj_reduce_mma(const float* __restrict__ partial, int BR, int splits, __nv_bfloat16* __restrict__ t) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
+  const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (e >= BR) return;
-  float acc = 0.f;
-  for (int s = 0; s < splits; ++s) acc += __ldcg(partial + (size_t)s * BR + e);
-  t[e] = __float2bfloat16_rn(acc);
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int s0 = 0; s0 < splits; s0 += 8) {
+    float4 v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      if (s0 + q < splits) v[q] = __ldcg(reinterpret_cast<const float4*>(partial + (size_t)(s0 + q) * BR + e));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      if (s0 + q < splits) {
+        acc.x += v[q].x;
+        acc.y += v[q].y;
+        acc.z += v[q].z;
+        acc.w += v[q].w;
+      }
+    }
+  }
+  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y), hi = __floats2bfloat162_rn(acc.z, acc.w);
+  *reinterpret_cast<__nv_bfloat162*>(t + e) = lo;
+  *reinterpret_cast<__nv_bfloat162*>(t + e + 2) = hi;
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -389,12 +406,13 @@ bool proj_mma_supported(int B, int d, int r, int dtype) {
   return mma_path_supported(B, r, dtype) && d % BK == 0 && (r <= 256 || r % 256 == 0);
 }
 
-// Split-K slices of the tensor-core projection: enough blocks to cover the SMs, at most one
-// 64-wide K chunk per slice.  max_sms bounds the workspace independently of the device.
+// Split-K slices of the tensor-core projection: enough blocks to cover the SMs but at least four
+// 64-wide K chunks per slice (the reduction reads every slice).  num_sms = 256 bounds the
+// workspace independently of the device.
 int proj_mma_splits(int B, int d, int r, int num_sms) {
   const int m_tiles = (B + BM - 1) / BM;
   const int n_tiles = (r + 255) / 256;
-  return max(1, min(d / BK, num_sms / (m_tiles * n_tiles)));
+  return max(1, min(d / (4 * BK), num_sms / (m_tiles * n_tiles)));
 }
 
 cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
@@ -426,7 +444,7 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
   if (e != cudaSuccess) return note_error(e, "launch k_proj_mma");
   const int BR = B * r;
   prof_before("proj_reduce_mma", c.stream);
-  k_proj_reduce_mma<<<(BR + 255) / 256, 256, 0, c.stream>>>(partial, BR, p.splits, static_cast<__nv_bfloat16*>(t));
+  k_proj_reduce_mma<<<(BR / 4 + 255) / 256, 256, 0, c.stream>>>(partial, BR, p.splits, static_cast<__nv_bfloat16*>(t));
   prof_after(c.stream);
   return note_error(cudaGetLastError(), "launch k_proj_reduce_mma");
 }
