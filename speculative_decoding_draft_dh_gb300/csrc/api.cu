@@ -201,11 +201,9 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
 
 // ------------------------------------------------------------------ stage 2
 
-size_t dh_exact_rescore_workspace(int B, int d, int vocab, int K, int dtype) {
+size_t dh_exact_rescore_workspace(int B, int, int, int K, int) {
   if (B <= 0 || K <= 0) return 0;
-  size_t n = WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256);
-  if (rescore_uniq_used(B, d, K, dtype)) n += rescore_uniq_bytes(B, vocab, K);
-  return n;
+  return WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256);
 }
 
 int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
@@ -223,27 +221,8 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
-  // Stage-2 kernel: latency-optimised direct gather for small batches, the streaming ring kernel
-  // from 2048 pairs on, and the W-row-ordered stream from 32768 pairs on (repeated rows served by
-  // L2).  DH_FORCE_RESCORE=direct|stream|uniq overrides the choice (tests and tuning).
-  const bool lists = rescore_uniq_used(B, d, K, dtype);
-  const char* f = std::getenv("DH_FORCE_RESCORE");
-  int mode = (long long)B * K >= 32768 && lists ? 2 : (lists ? 1 : 0);
-  if (f && std::strcmp(f, "direct") == 0) mode = 0;
-  if (f && std::strcmp(f, "stream") == 0 && lists) mode = 1;
-  if (f && std::strcmp(f, "uniq") == 0 && lists) mode = 2;
-  int* status = static_cast<int*>(workspace);
-  cudaError_t e;
-  if (mode == 2) {
-    void* area = static_cast<char*>(workspace) + WS_HEADER + align_up((size_t)B * sizeof(uint32_t), 256);
-    e = note_error(launch_rescore_uniq(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets, area, status),
-                   "rescore (ordered stream)");
-  } else if (mode == 1) {
-    e = note_error(launch_rescore_stream(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets, status),
-                   "rescore (stream)");
-  } else {
-    e = note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
-  }
+  const cudaError_t e =
+      note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
   if (e != cudaSuccess) return DH_ERR_CUDA;
   return DH_OK;
 }

@@ -328,6 +328,46 @@ def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
     run_head(x, cfg.K)
 
 
+def test_rescore_large_batch_with_repeats():
+    """Stage 2 on a large batch whose rows draw from a small candidate pool (many repeated W rows),
+    with two out-of-range ids; a second call reuses the workspace tickets."""
+    cfg = inputs.HeadConfig("rescore_big", 256, 512, 4096, 64, 128, "bf16", 0.1, True)
+    x = inputs.make_head(cfg, seed=31, device=DEV)
+    g = torch.Generator(device="cpu").manual_seed(5)
+    idx = torch.randint(0, 600, (cfg.B, cfg.K), generator=g, dtype=torch.int32)
+    idx[3, 7] = cfg.vocab + 1
+    idx[200, 0] = -5
+    idx = idx.to(DEV)
+    logits, probs = dh.exact_rescore(x["h"], x["W"], idx)
+    torch.cuda.synchronize()
+    rows = [0, 3, 100, 200, 255]
+    oz, op = oracle.exact_rescore(x["h"].cpu(), x["W"].cpu(), idx.cpu(), rows=rows)
+    gl, gp = logits.cpu().numpy(), probs.cpu().numpy()
+    for n, b in enumerate(rows):
+        if b in (3, 200):
+            ib = idx[b].cpu().numpy()
+            ok = (ib >= 0) & (ib < cfg.vocab)
+            assert np.isnan(gl[b][~ok]).all() and np.isnan(gp[b]).all()
+            check_logits(gl[b][ok], None, oz[n][ok], None, where=f"row {b}")
+        else:
+            check_logits(gl[b], gp[b], oz[n], op[n], where=f"row {b}")
+    logits2, probs2 = dh.exact_rescore(x["h"], x["W"], idx)
+    torch.cuda.synchronize()
+    assert torch.equal(torch.nan_to_num(logits2), torch.nan_to_num(logits))
+    assert torch.equal(torch.nan_to_num(probs2), torch.nan_to_num(probs))
+
+
+# ---------------------------------------------------------------- bounded waits
+
+@pytest.mark.parametrize("mode", [0, 1], ids=["mbarrier", "grid_barrier"])
+def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
+    status = dh.selftest_wait_timeout(mode, limit_us=20000)
+    assert status == (1 << 5)
+    cfg = inputs.head_config("tiny", B=2)
+    x = inputs.make_head(cfg, seed=0, device=DEV)
+    run_head(x, cfg.K)
+
+
 @pytest.mark.parametrize("path", ["direct", "stream", "uniq"])
 def test_rescore_paths_large_batch(path, monkeypatch):
     """Both stage-2 kernels on a batch large enough for the distinct-row path, with duplicates
