@@ -40,7 +40,7 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   off = align_up(off + (size_t)B * r * 4, 256);
   L.partial = off;
   size_t partial_floats = (size_t)L.nsplit * B * r;
-  if (B <= 8) partial_floats = std::max(partial_floats, small_b_partial_floats(B, r));
+  if (B <= 8) partial_floats = std::max(partial_floats, small_b_fix_bytes(B, r) / 4);
   // tensor-core projection: split-K slices for up to 256 SMs
   partial_floats = std::max(partial_floats, (size_t)proj_mma_splits(B, d, r, 256) * B * r);
   off = align_up(off + partial_floats * 4, 256);
@@ -175,8 +175,10 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
   const Path path = choose_path(B, r, dtype);
   if (path == PATH_FUSED) {
-    if (launch_small_b(c, h, U, V, B, d, r, vocab, K, dtype, partial, t, recs, idx_out, score_out,
-                       ws + WS_BARRIER_OFFSET, reinterpret_cast<int*>(ws)) != cudaSuccess)
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, partial, reinterpret_cast<unsigned int*>(ws + WS_TICKET_OFFSET),
+                       t, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+      return DH_ERR_CUDA;
+    if (note_error(launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out), "select") != cudaSuccess)
       return DH_ERR_CUDA;
     return DH_OK;
   }

@@ -11,9 +11,10 @@ namespace dh {
 
 // Every workspace starts with a 256-byte header whose first word collects device-side status bits
 // (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.  Bytes 64-71
-// hold the grid barrier of the cooperative small-batch kernel.
+// hold a grid barrier (bounded-wait self-test), bytes 72-75 the small-batch projection's ticket.
 constexpr size_t WS_HEADER = 256;
 constexpr size_t WS_BARRIER_OFFSET = 64;
+constexpr size_t WS_TICKET_OFFSET = 72;
 
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
@@ -152,6 +153,14 @@ int proj_splits(const Ctx& c, int B, int d, int r);
 
 bool mma_path_supported(int B, int r, int dtype);
 bool small_b_supported(int B, int r, int dtype);
+bool proj_mma_supported(int B, int d, int r, int dtype);
+int proj_mma_splits(int B, int d, int r, int num_sms);
+cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
+                            int max_splits, void* t, int* status);
+size_t small_b_fix_bytes(int B, int r);
+cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
+                           int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
+                           int* status);
 bool proj_mma_supported(int B, int d, int r, int dtype);
 int proj_mma_splits(int B, int d, int r, int num_sms);
 cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,

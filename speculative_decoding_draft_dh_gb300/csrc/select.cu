@@ -10,6 +10,7 @@ __global__ void __launch_bounds__(sel::SEL_THREADS, 1) k_select(const GroupRec* 
                                                             int r, int vocab, int K, int32_t* __restrict__ idx_out,
                                                             float* __restrict__ score_out) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the previous kernel
   const int row = blockIdx.x;
   const int n_groups = (vocab + GROUP - 1) / GROUP;
   sel::select_row<T>(smem_raw, recs + (size_t)row * n_groups, t + (size_t)row * r, V, r, vocab, K,
@@ -24,10 +25,21 @@ cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, const void* V
   static unsigned long long smem_done = 0;
   cudaError_t e = allow_max_smem(k_select<T>, c.device, &smem_done);
   if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)B);
+  cfg.blockDim = dim3(sel::SEL_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before("select", c.stream);
-  k_select<T><<<B, sel::SEL_THREADS, smem, c.stream>>>(recs, static_cast<const T*>(t), static_cast<const T*>(V),
-                                                       r, vocab, K, idx_out, score_out);
+  e = cudaLaunchKernelEx(&cfg, k_select<T>, recs, static_cast<const T*>(t), static_cast<const T*>(V), r, vocab, K,
+                         idx_out, score_out);
   prof_after(c.stream);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

@@ -1,32 +1,24 @@
-// Stage 1 for small batches (B <= 8) in one cooperative launch: projection, vocabulary-wide
-// low-rank scores with group summaries, and the exact top-K, with V streamed by TMA from the first
-// instruction on.
+// Stage 1 for small batches (B <= 8): two kernels chained by programmatic dependent launch, so
+// that V streams from HBM while the projection that it will be multiplied with is still being
+// computed.
 //
 // EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
 // the low-rank head scores the whole vocabulary to retrieve K candidates, then the full-rank head
 // scores them.  At batch 1 the whole call moves about 40 MB (V dominates), so its cost is HBM time
 // plus every serial dependency: h U must finish before t V, and the global top-K before rescoring.
-// Running the steps in one resident grid removes the kernel boundaries between them.
 //
-// One block per SM (grid = SM count), 16 warps.  Each block owns a contiguous run of 256-id
-// tiles and streams them in sets of four: a stage is four TMA boxes of 256 ids x 16 bf16 rows (8
-// fp32 rows) = 32 KB, i.e. 2 KB contiguous per V row, with six stages in flight.
-//   P0  thread 0 issues the TMA loads of the first six stages (V does not depend on t).
-//   P1  block c computes the partial products of h with the d-slice c of U for every (row, column)
-//       and writes them to the workspace; grid barrier.
-//   P2  every block sums the partials of every t element in the same fixed order (so all blocks
-//       hold bit-identical t), rounds to the activation dtype and keeps t in shared memory;
-//       block 0 also writes t for the selection's re-scoring step.
-//   P3  warp w scores the 64-id group w of the current set: lane i accumulates ids 2i and 2i+1
-//       for all rows over the stages; after the last band a shuffle butterfly folds the 64
-//       scores into the group record.  A block barrier per stage frees its slot for the next
-//       TMA load.  grid barrier.
-//   P4  block b (< B) selects row b exactly from its records (select.cuh), reusing the V staging
-//       buffers as scratch.
-// Grid barriers are sense-reversing counters in the workspace; every wait (barrier or TMA) gives
-// up after two seconds, raises DH_ERR_TIMEOUT in the status word, and the block drains its own
-// outstanding copies before it exits.
-#include "grid_sync.cuh"
+// k_proj_small (grid: two blocks per SM, each a slice of d): loads its slice of U (and h), signals
+//   its dependents may launch, multiplies, and adds its partial t into a 64-bit fixed-point
+//   accumulator (scale 2^32) with integer atomics, which is exact and order independent, so t is
+//   deterministic.  The last block to finish converts the accumulator to t in the activation dtype
+//   and clears it for the next call.
+// k_scores_small (one block per SM, 16 warps): issues the TMA loads of its first six 32 KB stages
+//   of V before waiting for the projection (V does not depend on t), then streams its run of
+//   256-id tiles in sets of four: a stage is four boxes of 256 ids x 16 bf16 rows (8 fp32 rows),
+//   2 KB contiguous per V row.  Warp w folds the 64 scores of group w of the set into its record;
+//   a block barrier per stage frees the stage's slot for the next TMA load.
+// k_select (select.cu) then picks the exact top-K per row from the records.
+// Every TMA wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word.
 #include "select.cuh"
 #include "sm100.cuh"
 
@@ -36,31 +28,18 @@ namespace {
 using namespace sm100;
 
 constexpr int SB_THREADS = 512;
-constexpr int SB_WARPS = SB_THREADS / 32;
-constexpr int TILE = 256;            // vocabulary ids per TMA box
-constexpr int SET_TILES = 4;         // tiles streamed together (16 warps x 64 ids)
-constexpr int NS = 6;                // stages in flight
-constexpr int STAGE_BYTES = 32768;   // SET_TILES boxes of 256 ids x (32 KB / 4 / 256 / sizeof(T)) rows
+constexpr int TILE = 256;           // vocabulary ids per TMA box
+constexpr int SET_TILES = 4;        // tiles streamed together (16 warps x 64 ids)
+constexpr int NS = 6;               // stages in flight
+constexpr int STAGE_BYTES = 32768;  // SET_TILES boxes of 256 ids x (32 KB / 4 / 256 / sizeof(T)) rows
 constexpr int MAX_B = 8;
-constexpr int MAX_BR = 2048;  // B * r values of t kept in shared memory
-constexpr int CH = 40;        // projection rows per batch of loads in flight
-constexpr int RED = 48;       // partial sums per lane in flight in the t reduction
+constexpr int MAX_BR = 2048;        // B * r values of t
+constexpr int PJ_THREADS = 256;
+constexpr int PJ_GROUPS = 4;        // row groups per block in the projection (reduced in smem)
+constexpr int CH = 12;              // projection rows per thread in one batch of loads
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t STAGE_REGION = (size_t)NS * STAGE_BYTES;
-
-struct SbParams {
-  const void* h;
-  const void* U;
-  const void* V;
-  int B, d, r, vocab, K, n_groups, n_tiles;
-  float* partial;  // [B*r][gridDim.x]
-  void* t_out;     // [B][r] in the activation dtype
-  GroupRec* recs;  // [B][n_groups]
-  int32_t* idx_out;
-  float* score_out;
-  GridBar* bar;
-  int* status;
-};
+constexpr float FIX_SCALE = 4294967296.0f;  // 2^32
 
 // Two adjacent values of row-major storage as floats (4-byte load for bf16, 8-byte for fp32).
 template <typename T>
@@ -78,15 +57,110 @@ __device__ __forceinline__ void load_pair<float>(const float* p, float& a, float
   b = f.y;
 }
 
+struct ProjSmall {
+  const void* h;
+  const void* U;
+  int B, d, r;
+  unsigned long long* acc;  // [B*r] fixed-point accumulator (zero between calls)
+  unsigned int* ticket;     // blocks finished (zero between calls)
+  void* t_out;              // [B][r] in the activation dtype
+};
+
+template <typename T>
+__global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
+  __shared__ float sh_h[MAX_B * PJ_GROUPS * CH];
+  __shared__ float red[PJ_GROUPS][MAX_BR / 4];  // per-group partials of this block's (b, j) chunk
+  __shared__ int s_last;
+  const T* h = static_cast<const T*>(p.h);
+  const T* U = static_cast<const T*>(p.U);
+  const int B = p.B, r = p.r, BR = B * r, npairs = r / 2;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int i0 = (int)((long long)p.d * c / G), i1 = (int)((long long)p.d * (c + 1) / G);
+  const int rows = i1 - i0;
+  const int grp = threadIdx.x / (PJ_THREADS / PJ_GROUPS);  // row group of this thread
+  const int lt = threadIdx.x % (PJ_THREADS / PJ_GROUPS);
+  const int per_grp = (rows + PJ_GROUPS - 1) / PJ_GROUPS;
+  const int g0 = i0 + grp * per_grp, g1 = min(i1, g0 + per_grp);
+  bool triggered = false;
+  // work items: (b, column pair), PJ_THREADS / PJ_GROUPS per pass
+  for (int w0 = 0; w0 < B * npairs; w0 += PJ_THREADS / PJ_GROUPS) {
+    const int w = w0 + lt;
+    const int b = w / npairs, jp = w - (w / npairs) * npairs;
+    float a0 = 0.f, a1 = 0.f;
+    for (int base = g0; base < g1; base += CH) {
+      const int n = min(CH, g1 - base);
+      float u[CH][2], hv[CH];
+      if (w < B * npairs) {
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          if (i < n) {
+            load_pair<T>(U + (size_t)(base + i) * r + 2 * jp, u[i][0], u[i][1]);
+            hv[i] = Elem<T>::to_f(h[(size_t)b * p.d + base + i]);
+          }
+        }
+      }
+      if (!triggered) {  // U and h are in flight: the scores kernel may start streaming V
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        triggered = true;
+      }
+      if (w < B * npairs) {
+#pragma unroll
+        for (int i = 0; i < CH; ++i) {
+          if (i < n) {
+            a0 = fmaf(hv[i], u[i][0], a0);
+            a1 = fmaf(hv[i], u[i][1], a1);
+          }
+        }
+      }
+    }
+    // add the row groups' partials in a fixed order, then one integer atomic per (b, j)
+    if (w < B * npairs) {
+      red[grp][2 * lt] = a0;
+      red[grp][2 * lt + 1] = a1;
+    }
+    __syncthreads();
+    if (threadIdx.x < 2 * (PJ_THREADS / PJ_GROUPS)) {
+      const int e = 2 * w0 + threadIdx.x;  // == b * r + j for the pass's pairs
+      if (e < BR) {
+        float v = 0.f;
+#pragma unroll
+        for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][threadIdx.x];
+        const long long fx = __float2ll_rn(v * FIX_SCALE);
+        atomicAdd(p.acc + e, (unsigned long long)fx);
+      }
+    }
+    __syncthreads();
+  }
+  if (!triggered) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  // the last block converts the accumulator to t and clears it
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(p.ticket, 1u) == (unsigned)(G - 1);
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int e = threadIdx.x; e < BR; e += blockDim.x) {
+    const long long fx = (long long)atomicExch(p.acc + e, 0ull);
+    static_cast<T*>(p.t_out)[e] = Elem<T>::from_f((float)((double)fx * (1.0 / 4294967296.0)));
+  }
+  if (threadIdx.x == 0) *p.ticket = 0u;
+}
+
+struct ScoresSmall {
+  const void* t;  // [B][r] activation dtype
+  int B, r, vocab, n_groups, n_tiles;
+  GroupRec* recs;
+  int* status;
+};
+
 template <typename T>
 __global__ void __launch_bounds__(SB_THREADS, 1)
-    k_small_b(const __grid_constant__ CUtensorMap tmV, SbParams p) {
+    k_scores_small(const __grid_constant__ CUtensorMap tmV, ScoresSmall p) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));  // V rows per stage
   constexpr int ROW_BYTES = TILE * (int)sizeof(T);                        // one box row
   extern __shared__ unsigned char smem_raw[];
   __shared__ uint64_t full[NS];
-  __shared__ float st[MAX_BR];        // t as fp32, [B][r]
-  __shared__ float sh_h[MAX_B * CH];  // the block's slice of h
+  __shared__ float st[MAX_BR];  // t as fp32, [B][r]
   __shared__ volatile int s_fail;
 
   unsigned char* stages = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -95,8 +169,6 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   const int G = gridDim.x, c = blockIdx.x;
   const int B = p.B, r = p.r, BR = p.B * p.r;
   const int bands = r / RB;  // stages per tile set
-
-  // this block's 256-id tiles, streamed in sets of up to four
   const int t0 = (int)((long long)p.n_tiles * c / G), t1 = (int)((long long)p.n_tiles * (c + 1) / G);
   const int n_sets = (t1 - t0 + SET_TILES - 1) / SET_TILES;
   const int total_stages = n_sets * bands;
@@ -122,86 +194,15 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     issued = q + 1;
   };
 
-  // ---------------------------------------------------------------- P0: V prefetch
+  // V does not depend on t: start streaming before waiting for the projection
   if (threadIdx.x == 0) {
     prefetch_tmap(&tmV);
     for (int q = 0; q < NS && q < total_stages; ++q) issue(q);
   }
-
-  // ---------------------------------------------------------------- P1: projection partials
-  {
-    const T* h = static_cast<const T*>(p.h);
-    const T* U = static_cast<const T*>(p.U);
-    const int i0 = (int)((long long)p.d * c / G), i1 = (int)((long long)p.d * (c + 1) / G);
-    const int npairs = r / 2;
-    for (int base = i0; base < i1; base += CH) {
-      const int n = min(CH, i1 - base);
-      __syncthreads();
-      for (int e = threadIdx.x; e < B * n; e += blockDim.x) {
-        const int b = e / n, i = e - b * n;
-        sh_h[b * CH + i] = Elem<T>::to_f(h[(size_t)b * p.d + base + i]);
-      }
-      __syncthreads();
-      for (int w = threadIdx.x; w < npairs * B; w += blockDim.x) {
-        const int b = w / npairs, jp = w - b * npairs;
-        const T* up = U + (size_t)base * r + 2 * jp;
-        float u[CH][2];
-#pragma unroll
-        for (int i = 0; i < CH; ++i)
-          if (i < n) load_pair<T>(up + (size_t)i * r, u[i][0], u[i][1]);
-        float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-        for (int i = 0; i < CH; ++i) {
-          if (i < n) {
-            const float hv = sh_h[b * CH + i];
-            a0 = fmaf(hv, u[i][0], a0);
-            a1 = fmaf(hv, u[i][1], a1);
-          }
-        }
-        // several load batches of the same slice accumulate in place
-        float* o = p.partial + (size_t)(b * r + 2 * jp) * G + c;
-        if (base == i0) {
-          o[0] = a0;
-          o[G] = a1;
-        } else {
-          o[0] += a0;
-          o[G] += a1;
-        }
-      }
-    }
-  }
-  if (!grid_sync(p.bar, gridDim.x, WAIT_NS, p.status, &s_fail)) goto drain;
-
-  // ---------------------------------------------------------------- P2: t, identical in every block
-  {
-    int L = 1;  // lanes per output (power of two, <= 32)
-    while (L < 32 && L * 2 * BR <= SB_THREADS) L *= 2;
-    const int per_pass = SB_THREADS / L;
-    const int sub = lane % L;
-    for (int e0 = 0; e0 < BR; e0 += per_pass) {
-      const int e = e0 + (int)threadIdx.x / L;
-      float acc = 0.f;
-      if (e < BR) {
-        const float* src = p.partial + (size_t)e * G;
-        for (int k0 = sub; k0 < G; k0 += RED * L) {
-          float v[RED];
-#pragma unroll
-          for (int q = 0; q < RED; ++q) v[q] = (k0 + q * L < G) ? __ldcg(src + k0 + q * L) : 0.f;
-#pragma unroll
-          for (int q = 0; q < RED; ++q) acc += v[q];
-        }
-      }
-      for (int o = L / 2; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-      if (sub == 0 && e < BR) {
-        const T tv = Elem<T>::from_f(acc);
-        st[e] = Elem<T>::to_f(tv);
-        if (c == 0) static_cast<T*>(p.t_out)[e] = tv;
-      }
-    }
-  }
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = Elem<T>::to_f(static_cast<const T*>(p.t)[e]);
   __syncthreads();
 
-  // ---------------------------------------------------------------- P3: stream V, group records
   {
     // warp w scores group (w % 4) of tile (w / 4) of the current set; lane i owns ids 2i, 2i+1
     const int k_tile = warp / 4, g_in_tile = warp % 4;
@@ -273,15 +274,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
       }
     }
   }
-  if (!grid_sync(p.bar, gridDim.x, WAIT_NS, p.status, &s_fail)) goto drain;
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-
-  // ---------------------------------------------------------------- P4: exact top-K of row c
-  if (c < B) {
-    const T* tr = static_cast<const T*>(p.t_out) + (size_t)c * r;
-    sel::select_row<T>(stages, p.recs + (size_t)c * p.n_groups, tr, static_cast<const T*>(p.V), r, p.vocab,
-                       p.K, p.idx_out + (size_t)c * p.K, p.score_out + (size_t)c * p.K);
-  }
   return;
 
 drain:
@@ -309,47 +302,65 @@ EncodeTiledFn encode_fn() {
 }
 
 template <typename T>
-cudaError_t run(const Ctx& c, const SbParams& p0) {
+cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
+                void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs, int* status) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
   static unsigned long long smem_done = 0;
-  cudaError_t e = allow_max_smem(k_small_b<T>, c.device, &smem_done);
+  cudaError_t e = allow_max_smem(k_scores_small<T>, c.device, &smem_done);
   if (e != cudaSuccess) return e;
-  const size_t smem = STAGE_REGION + 1024;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_small_b<T>, SB_THREADS, smem);
-  if (e != cudaSuccess) return note_error(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor(k_small_b)");
-  const int G = min(c.num_sms * max(per_sm, 0), 1024);
-  if (G < 1) return note_error(cudaErrorInvalidConfiguration, "k_small_b: no resident block fits");
-
   EncodeTiledFn fn = encode_fn();
   if (!fn) return note_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   CUtensorMap tmV;
-  cuuint64_t dims[2] = {(cuuint64_t)p0.vocab, (cuuint64_t)p0.r};
-  cuuint64_t strides[1] = {(cuuint64_t)p0.vocab * sizeof(T)};
+  cuuint64_t dims[2] = {(cuuint64_t)vocab, (cuuint64_t)r};
+  cuuint64_t strides[1] = {(cuuint64_t)vocab * sizeof(T)};
   cuuint32_t box[2] = {(cuuint32_t)TILE, (cuuint32_t)RB};
   cuuint32_t estr[2] = {1, 1};
   if (fn(&tmV, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-         const_cast<void*>(p0.V), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-         CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+         const_cast<void*>(V), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(V, small batch)");
 
-  SbParams p = p0;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(G);
-  cfg.blockDim = dim3(SB_THREADS);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+
+  ProjSmall pp;
+  pp.h = h;
+  pp.U = U;
+  pp.B = B;
+  pp.d = d;
+  pp.r = r;
+  pp.acc = static_cast<unsigned long long*>(ws_fix);
+  pp.ticket = ticket;
+  pp.t_out = t_out;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)max(1, min(2 * c.num_sms, d / 4)));
+  cfg.blockDim = dim3(PJ_THREADS);
+  cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  prof_before("small_b", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_small_b<T>, tmV, p);
+  prof_before("proj_small", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_proj_small<T>, pp);
   prof_after(c.stream);
-  if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_small_b)");
-  return note_error(cudaGetLastError(), "k_small_b launch");
+  if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_proj_small)");
+
+  ScoresSmall sp;
+  sp.t = t_out;
+  sp.B = B;
+  sp.r = r;
+  sp.vocab = vocab;
+  sp.n_groups = (vocab + GROUP - 1) / GROUP;
+  sp.n_tiles = (vocab + TILE - 1) / TILE;
+  sp.recs = recs;
+  sp.status = status;
+  cfg.gridDim = dim3((unsigned)c.num_sms);
+  cfg.blockDim = dim3(SB_THREADS);
+  cfg.dynamicSmemBytes = STAGE_REGION + 1024;
+  prof_before("scores_small", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_scores_small<T>, tmV, sp);
+  prof_after(c.stream);
+  if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_scores_small)");
+  return note_error(cudaGetLastError(), "small-batch stage 1 launch");
 }
 
 }  // namespace
@@ -359,31 +370,13 @@ bool small_b_supported(int B, int r, int dtype) {
   return B >= 1 && B <= MAX_B && B * r <= MAX_BR && r % rows == 0 && r % 2 == 0;
 }
 
-size_t small_b_partial_floats(int B, int r) { return (size_t)1024 * B * r; }
+size_t small_b_fix_bytes(int B, int r) { return (size_t)B * r * sizeof(unsigned long long); }
 
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int K, int dtype, float* partial, void* t_out, GroupRec* recs,
-                           int32_t* idx_out, float* score_out, void* bar, int* status) {
-  SbParams p;
-  p.h = h;
-  p.U = U;
-  p.V = V;
-  p.B = B;
-  p.d = d;
-  p.r = r;
-  p.vocab = vocab;
-  p.K = K;
-  p.n_groups = (vocab + GROUP - 1) / GROUP;
-  p.n_tiles = (vocab + TILE - 1) / TILE;
-  p.partial = partial;
-  p.t_out = t_out;
-  p.recs = recs;
-  p.idx_out = idx_out;
-  p.score_out = score_out;
-  p.bar = static_cast<GridBar*>(bar);
-  p.status = status;
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, p);
-  return run<float>(c, p);
+                           int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
+                           int* status) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, U, V, B, d, r, vocab, ws_fix, ticket, t_out, recs, status);
+  return run<float>(c, h, U, V, B, d, r, vocab, ws_fix, ticket, t_out, recs, status);
 }
 
 }  // namespace dh
