@@ -26,7 +26,7 @@ bool row16(long long n, int dt) { return (n * elem_bytes(dt)) % 16 == 0; }
 // ---- workspace layouts (all offsets 256-byte aligned)
 
 struct TopkLayout {
-  size_t t, partial, recs, total;
+  size_t fix, t, partial, recs, total;
   int nsplit;
 };
 
@@ -35,12 +35,15 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   Ctx dummy{0, 0, nullptr};
   L.nsplit = proj_splits(dummy, B, d, r);
   const size_t n_groups = (size_t)(vocab + GROUP - 1) / GROUP;
+  // state that must be zero between calls sits at fixed offsets, so that a call with other
+  // arguments never finds another call's data there: the small-batch projection accumulator
   size_t off = WS_HEADER;
+  L.fix = off;
+  off = align_up(off + WS_FIX_BYTES, 256);
   L.t = off;
   off = align_up(off + (size_t)B * r * 4, 256);
   L.partial = off;
   size_t partial_floats = (size_t)L.nsplit * B * r;
-  if (B <= 8) partial_floats = std::max(partial_floats, small_b_fix_bytes(B, r) / 4);
   // tensor-core projection: split-K slices for up to 256 SMs
   partial_floats = std::max(partial_floats, (size_t)proj_mma_splits(B, d, r, 256) * B * r);
   off = align_up(off + partial_floats * 4, 256);
@@ -175,7 +178,7 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
   const Path path = choose_path(B, r, dtype);
   if (path == PATH_FUSED) {
-    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, partial, reinterpret_cast<unsigned int*>(ws + WS_TICKET_OFFSET),
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, ws + L.fix, reinterpret_cast<unsigned int*>(ws + WS_TICKET_OFFSET),
                        t, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
     if (note_error(launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out), "select") != cudaSuccess)

@@ -15,6 +15,9 @@ namespace dh {
 constexpr size_t WS_HEADER = 256;
 constexpr size_t WS_BARRIER_OFFSET = 64;
 constexpr size_t WS_TICKET_OFFSET = 72;
+// Fixed-point accumulator of the small-batch projection (B * r <= 2048 int64), right after the
+// header in the stage-1 workspace.
+constexpr size_t WS_FIX_BYTES = 2048 * 8;
 
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
@@ -157,7 +160,6 @@ bool proj_mma_supported(int B, int d, int r, int dtype);
 int proj_mma_splits(int B, int d, int r, int num_sms);
 cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
                             int max_splits, void* t, int* status);
-size_t small_b_fix_bytes(int B, int r);
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
                            int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
                            int* status);

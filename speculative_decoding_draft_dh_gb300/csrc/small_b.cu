@@ -370,8 +370,6 @@ bool small_b_supported(int B, int r, int dtype) {
   return B >= 1 && B <= MAX_B && B * r <= MAX_BR && r % rows == 0 && r % 2 == 0;
 }
 
-size_t small_b_fix_bytes(int B, int r) { return (size_t)B * r * sizeof(unsigned long long); }
-
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
                            int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
                            int* status) {

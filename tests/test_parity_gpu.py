@@ -302,6 +302,26 @@ def test_mma_and_gemv_paths_agree_on_candidates(monkeypatch):
     np.testing.assert_allclose(s1.cpu().numpy(), s2.cpu().numpy(), rtol=1e-4, atol=1e-4)
 
 
+def test_one_workspace_across_shapes():
+    """Calls of different shapes and paths sharing one workspace object: state that must be zero
+    between calls may not be left where another shape keeps its data."""
+    ws = dh.Workspace()
+    shapes = [inputs.head_config("tiny", B=4, K=16), inputs.head_config("tiny", B=1, K=1),
+              inputs.head_config("tiny", B=3, K=64), MID, inputs.head_config("tiny", B=2, K=7),
+              inputs.HeadConfig("wide", 20, 512, 4096, 128, 32, "bf16", 0.1, True), inputs.head_config("tiny", B=1, K=5)]
+    for n, cfg in enumerate(shapes):
+        x = inputs.make_head(cfg, seed=40 + n, device=DEV)
+        idx, score = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, workspace=ws)
+        logits, probs = dh.exact_rescore(x["h"], x["W"], idx, workspace=ws)
+        torch.cuda.synchronize()
+        s_full = oracle.lowrank_scores(x["h"].cpu(), x["U"].cpu(), x["V"].cpu())
+        oz, op = oracle.exact_rescore(x["h"].cpu(), x["W"].cpu(), idx.cpu())
+        for b in range(cfg.B):
+            check_candidates(idx[b].cpu().numpy(), score[b].cpu().numpy(), s_full[b], cfg.K, where=f"{cfg.name} row {b}")
+            check_logits(logits[b].cpu().numpy(), probs[b].cpu().numpy(), oz[b], op[b], where=f"{cfg.name} row {b}")
+    assert dh.workspace_status(ws) == 0
+
+
 def test_repeated_calls_are_identical():
     cfg = inputs.head_config("tiny", B=4)
     x = inputs.make_head(cfg, seed=13, device=DEV)
