@@ -145,6 +145,24 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
                    void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Greedy draft-tree acceptance without a caller-provided workspace (no counterpart on the pages:
+ * it is an interface for callers, not part of the method).
+ *
+ * For callers that cannot allocate device memory, such as code inside a serving engine's step
+ * where cudaMalloc is not allowed (it can synchronise the device), or a host program that only
+ * receives device pointers.  Same inputs, outputs and results as dh_tree_accept; the per-node
+ * scratch lives in a fixed array inside the library's device memory, so the call allocates
+ * nothing.  Limit: B * N <= DH_TREE_NOALLOC_MAX_NODES (larger calls return DH_ERR_UNSUPPORTED and
+ * dh_last_error says why).  The first call on each device (with that device current) looks up the
+ * array's device address; make it before any stream capture.  All calls on a device share the
+ * array, so calls whose kernels overlap on the GPU race on it: order them (one stream).
+ * ------------------------------------------------------------------------------------------- */
+#define DH_TREE_NOALLOC_MAX_NODES (1 << 18)
+int dh_tree_accept_noalloc(const void* logits, const int32_t* parent, const int32_t* token, int B, int N,
+                           int vocab, int dtype, int32_t* argmax_out, int32_t* path_out, int32_t* len_out,
+                           int32_t* bonus_out, int32_t* err_out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Device-side status of a workspace (no counterpart on the pages).
  *
  * Kernels that wait on on-chip barriers give up after a bounded time instead of hanging; they then

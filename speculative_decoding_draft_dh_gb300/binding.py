@@ -22,7 +22,7 @@ F32, BF16 = 0, 1
 
 EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
-           "dh_tree_accept", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
+           "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
 
 _lib = None
 _lock = threading.Lock()
@@ -63,6 +63,8 @@ def load_library(path: str | None = None):
         lib.dh_tree_accept_workspace.restype = Z
         lib.dh_tree_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
         lib.dh_tree_accept.restype = I
+        lib.dh_tree_accept_noalloc.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P]
+        lib.dh_tree_accept_noalloc.restype = I
         lib.dh_workspace_status.argtypes = [P, P, P]
         lib.dh_workspace_status.restype = I
         lib.dh_selftest_wait_timeout.argtypes = [I, I, P, Z, P]
