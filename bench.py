@@ -197,7 +197,8 @@ def traffic_from_profiles(kernel: str, workload: str, files):
 # ------------------------------------------------------------------------------------- head
 
 KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
-                "small_b": ["small_b.cu", "select.cuh", "grid_sync.cuh", "sm100.cuh", "dh_internal.cuh"],
+                "scores_small": ["small_b.cu", "sm100.cuh", "dh_internal.cuh"],
+                "proj_small": ["small_b.cu", "dh_internal.cuh"],
                 "lowrank_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
                 "select": ["select.cu", "dh_internal.cuh"],
                 "rescore": ["rescore.cu", "dh_internal.cuh"],
@@ -216,8 +217,10 @@ def kernel_algo(cfg, name):
     """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
     or tensor FLOPs of the dense contraction (rows beyond B padded by the kernel are not counted)."""
     e = 2 if cfg.dtype == "bf16" else 4
-    if name == "small_b":  # projection + vocabulary scores + selection, one launch
-        return "hbm", cfg.d * cfg.r * e + cfg.r * cfg.vocab * e + cfg.B * cfg.d * e, "GB/s"
+    if name == "scores_small":
+        return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
+    if name == "proj_small":
+        return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
     if name == "scores_summary":
         return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
     if name == "lowrank_mma":
