@@ -226,8 +226,17 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
+  // DH_FORCE_RESCORE=direct|ring overrides the choice by batch size (tests and tuning)
+  const char* f = std::getenv("DH_FORCE_RESCORE");
+  const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
+  bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
+  if (f && std::strcmp(f, "direct") == 0) ring = false;
+  if (f && std::strcmp(f, "ring") == 0) ring = ring_ok;
   const cudaError_t e =
-      note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
+      ring ? note_error(launch_rescore_ring(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
+                                            static_cast<int*>(workspace)),
+                        "rescore (ring)")
+           : note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
   if (e != cudaSuccess) return DH_ERR_CUDA;
   return DH_OK;
 }

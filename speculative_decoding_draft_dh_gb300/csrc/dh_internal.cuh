@@ -181,6 +181,10 @@ cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, con
                           int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out);
 
 bool rescore_supported(int d);
+bool rescore_ring_used(int B, int K, int d, int dtype);
+cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
+                                int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
+                                int* status);
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
                            int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
 

@@ -145,6 +145,21 @@ def test_rescore_bad_index_gives_nan_row():
     assert np.isfinite(lg[0]).all() and np.isfinite(pr[0]).all()
 
 
+@pytest.mark.parametrize("path", ["direct", "ring"])
+def test_rescore_paths_small_shapes(path, monkeypatch):
+    """Both stage-2 kernels on fp32 and bf16 rows, K not a multiple of the ring's chunk."""
+    monkeypatch.setenv("DH_FORCE_RESCORE", path)
+    for cfg in (inputs.head_config("tiny", B=3, K=45), inputs.HeadConfig("r", 5, 768, 4096, 64, 70, "bf16", 0.1, True)):
+        x = inputs.make_head(cfg, seed=17, device=DEV)
+        idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+        logits, probs = dh.exact_rescore(x["h"], x["W"], idx)
+        torch.cuda.synchronize()
+        oz, op = oracle.exact_rescore(x["h"].cpu(), x["W"].cpu(), idx.cpu())
+        for b in range(cfg.B):
+            check_logits(logits[b].cpu().numpy(), probs[b].cpu().numpy(), oz[b], op[b], where=f"{cfg.name} row {b}")
+    assert dh.workspace_status() == 0
+
+
 def test_rescore_without_probs():
     cfg = inputs.head_config("tiny", B=2)
     x = inputs.make_head(cfg, seed=0, device=DEV)
@@ -350,9 +365,11 @@ def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
     run_head(x, cfg.K)
 
 
-def test_rescore_large_batch_with_repeats():
+@pytest.mark.parametrize("path", ["direct", "ring"])
+def test_rescore_large_batch_with_repeats(path, monkeypatch):
     """Stage 2 on a large batch whose rows draw from a small candidate pool (many repeated W rows),
     with two out-of-range ids; a second call reuses the workspace tickets."""
+    monkeypatch.setenv("DH_FORCE_RESCORE", path)
     cfg = inputs.HeadConfig("rescore_big", 256, 512, 4096, 64, 128, "bf16", 0.1, True)
     x = inputs.make_head(cfg, seed=31, device=DEV)
     g = torch.Generator(device="cpu").manual_seed(5)
