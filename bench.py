@@ -198,10 +198,12 @@ def traffic_from_profiles(kernel: str, workload: str, files):
 
 KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
                 "scores_small": ["small_b.cu", "sm100.cuh", "dh_internal.cuh"],
+                "scores_lsu": ["small_b.cu", "dh_internal.cuh"],
                 "proj_small": ["small_b.cu", "dh_internal.cuh"],
                 "lowrank_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
-                "select": ["select.cu", "dh_internal.cuh"],
+                "select": ["select.cu", "select.cuh", "dh_internal.cuh"],
                 "rescore": ["rescore.cu", "dh_internal.cuh"],
+                "rescore_ring": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
                 "proj_partial": ["proj.cu", "dh_internal.cuh"],
                 "tree_argmax": ["tree.cu", "dh_internal.cuh"]}
 
@@ -217,7 +219,7 @@ def kernel_algo(cfg, name):
     """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
     or tensor FLOPs of the dense contraction (rows beyond B padded by the kernel are not counted)."""
     e = 2 if cfg.dtype == "bf16" else 4
-    if name == "scores_small":
+    if name in ("scores_small", "scores_lsu"):
         return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
     if name == "proj_small":
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
@@ -229,7 +231,7 @@ def kernel_algo(cfg, name):
         return "tensor", 2.0 * cfg.B * cfg.d * cfg.r, "TFLOP/s"
     if name == "proj_partial":
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
-    if name == "rescore":
+    if name in ("rescore", "rescore_ring"):
         return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name == "select":
         return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16, "GB/s"

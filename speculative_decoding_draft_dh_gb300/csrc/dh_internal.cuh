@@ -15,9 +15,9 @@ namespace dh {
 constexpr size_t WS_HEADER = 256;
 constexpr size_t WS_BARRIER_OFFSET = 64;
 constexpr size_t WS_TICKET_OFFSET = 72;
-// Fixed-point accumulator of the small-batch projection (B * r <= 2048 int64), right after the
-// header in the stage-1 workspace.
-constexpr size_t WS_FIX_BYTES = 2048 * 8;
+// Fixed-point accumulators of the small-batch projection (8 copies of B * r <= 2048 int64), right
+// after the header in the stage-1 workspace.
+constexpr size_t WS_FIX_BYTES = 8 * 2048 * 8;
 
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the

@@ -14,7 +14,7 @@
 namespace dh {
 namespace {
 
-constexpr int WARPS = 8;          // candidates per block (one warp each)
+constexpr int WARPS = 8;          // candidates per block (one warp each), larger batches
 constexpr int THREADS = WARPS * 32;
 constexpr int MAXW = 20;          // 16-byte W vectors per lane in flight (d = 5120 bf16 in one batch)
 constexpr int MAX_D_SMEM = 8192;  // h row staged in shared memory (bf16: 16 KB, fp32: 32 KB)
@@ -24,24 +24,24 @@ constexpr int MAX_D_SMEM = 8192;  // h row staged in shared memory (bf16: 16 KB,
 // its W row with MAXW 16-byte loads per lane in flight and reduces with shuffles.  With probs
 // requested, the block adds its candidate count to the row's ticket; the block completing the row
 // computes the softmax and resets the ticket.
-template <typename T>
-__global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, const T* __restrict__ W,
+template <typename T, int NWARP>
+__global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h, const T* __restrict__ W,
                                                      const int32_t* __restrict__ idx, int d, int vocab, int K,
                                                      float* __restrict__ logits, float* __restrict__ probs,
                                                      uint32_t* __restrict__ tickets) {
   constexpr int PER = Elem<T>::PER16;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* sh_h = reinterpret_cast<T*>(smem_raw);
-  __shared__ float red[WARPS];
+  __shared__ float red[NWARP];
   __shared__ float s_bcast;
   __shared__ int s_last;
-  const int kblocks = (K + WARPS - 1) / WARPS;
+  const int kblocks = (K + NWARP - 1) / NWARP;
   const int b = blockIdx.x / kblocks, kb = blockIdx.x % kblocks;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int k = kb * WARPS + warp;
-  const int n_here = min(WARPS, K - kb * WARPS);
+  const int k = kb * NWARP + warp;
+  const int n_here = min(NWARP, K - kb * NWARP);
   const T* x = h + (size_t)b * d;
-  for (int c = threadIdx.x * PER; c < d; c += THREADS * PER)
+  for (int c = threadIdx.x * PER; c < d; c += (NWARP * 32) * PER)
     *reinterpret_cast<uint4*>(sh_h + c) = __ldg(reinterpret_cast<const uint4*>(x + c));
   asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
   __syncthreads();
@@ -88,20 +88,20 @@ __global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, co
   // softmax over the row's K logits (written by other blocks: read through L2)
   const float* z = logits + (size_t)b * K;
   float m = -INFINITY;
-  for (int i = threadIdx.x; i < K; i += THREADS) m = fmaxf(m, __ldcg(z + i));
+  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) m = fmaxf(m, __ldcg(z + i));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   if (lane == 0) red[warp] = m;
   __syncthreads();
   if (threadIdx.x == 0) {
     float mm = red[0];
-    for (int i = 1; i < WARPS; ++i) mm = fmaxf(mm, red[i]);
+    for (int i = 1; i < NWARP; ++i) mm = fmaxf(mm, red[i]);
     s_bcast = mm;
   }
   __syncthreads();
   m = s_bcast;
   float ssum = 0.f;
-  for (int i = threadIdx.x; i < K; i += THREADS) ssum += expf(__ldcg(z + i) - m);
+  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) ssum += expf(__ldcg(z + i) - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
   __syncthreads();
@@ -109,13 +109,13 @@ __global__ void __launch_bounds__(THREADS) k_rescore(const T* __restrict__ h, co
   __syncthreads();
   if (threadIdx.x == 0) {
     float tot = 0.f;
-    for (int i = 0; i < WARPS; ++i) tot += red[i];
+    for (int i = 0; i < NWARP; ++i) tot += red[i];
     s_bcast = 1.f / tot;
     tickets[b] = 0u;
   }
   __syncthreads();
   const float inv = s_bcast;
-  for (int i = threadIdx.x; i < K; i += THREADS) probs[(size_t)b * K + i] = expf(__ldcg(z + i) - m) * inv;
+  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) probs[(size_t)b * K + i] = expf(__ldcg(z + i) - m) * inv;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -310,14 +310,17 @@ cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
                 int K, float* logits, float* probs, uint32_t* tickets) {
-  static unsigned long long smem_done = 0;
-  cudaError_t e = allow_max_smem(k_rescore<T>, c.device, &smem_done);
+  // Small problems use 2-warp blocks so that more SMs pull W rows; larger ones 8-warp blocks.
+  const int nw = (long long)B * K <= 512 ? 2 : WARPS;
+  static unsigned long long smem_done2 = 0, smem_done8 = 0;
+  cudaError_t e = nw == 2 ? allow_max_smem(k_rescore<T, 2>, c.device, &smem_done2)
+                          : allow_max_smem(k_rescore<T, WARPS>, c.device, &smem_done8);
   if (e != cudaSuccess) return e;
   // Programmatic dependent launch: the blocks may start while the stage-1 kernel drains; they
   // stage h and then wait (griddepcontrol.wait) for its results.
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(B * ((K + WARPS - 1) / WARPS)));
-  cfg.blockDim = dim3(THREADS);
+  cfg.gridDim = dim3((unsigned)(B * ((K + nw - 1) / nw)));
+  cfg.blockDim = dim3(nw * 32);
   cfg.dynamicSmemBytes = (size_t)d * sizeof(T);
   cfg.stream = c.stream;
   cudaLaunchAttribute attr[1];
@@ -326,8 +329,10 @@ cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, 
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before("rescore", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_rescore<T>, static_cast<const T*>(h), static_cast<const T*>(W), idx, d, vocab, K,
-                         logits, probs, tickets);
+  e = nw == 2 ? cudaLaunchKernelEx(&cfg, k_rescore<T, 2>, static_cast<const T*>(h), static_cast<const T*>(W), idx, d,
+                                   vocab, K, logits, probs, tickets)
+              : cudaLaunchKernelEx(&cfg, k_rescore<T, WARPS>, static_cast<const T*>(h), static_cast<const T*>(W), idx, d,
+                                   vocab, K, logits, probs, tickets);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -8,10 +8,10 @@
 // plus every serial dependency: h U must finish before t V, and the global top-K before rescoring.
 //
 // k_proj_small (grid: two blocks per SM, each a slice of d): loads its slice of U (and h), signals
-//   its dependents may launch, multiplies, and adds its partial t into a 64-bit fixed-point
-//   accumulator (scale 2^32) with integer atomics, which is exact and order independent, so t is
-//   deterministic.  The last block to finish converts the accumulator to t in the activation dtype
-//   and clears it for the next call.
+//   its dependents may launch, multiplies, and adds its partial t into one of eight 64-bit
+//   fixed-point accumulators (scale 2^32) with integer atomics, which are exact and order
+//   independent, so t is deterministic; eight copies keep the same-address atomics per element
+//   low.  The last block to finish sums the copies into t in the activation dtype and clears them.
 // k_scores_small (one block per SM, 16 warps): issues the TMA loads of its first six 32 KB stages
 //   of V before waiting for the projection (V does not depend on t), then streams its run of
 //   256-id tiles in sets of four: a stage is four boxes of 256 ids x 16 bf16 rows (8 fp32 rows),
@@ -19,6 +19,9 @@
 //   a block barrier per stage frees the stage's slot for the next TMA load.
 // k_select (select.cu) then picks the exact top-K per row from the records.
 // Every TMA wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word.
+#include <cstdlib>
+#include <cstring>
+
 #include "select.cuh"
 #include "sm100.cuh"
 
@@ -40,6 +43,7 @@ constexpr int CH = 12;              // projection rows per thread in one batch o
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t STAGE_REGION = (size_t)NS * STAGE_BYTES;
 constexpr float FIX_SCALE = 4294967296.0f;  // 2^32
+constexpr int NCOPY = 8;                    // accumulator copies (block c adds into copy c % NCOPY)
 
 // Two adjacent values of row-major storage as floats (4-byte load for bf16, 8-byte for fp32).
 template <typename T>
@@ -61,7 +65,7 @@ struct ProjSmall {
   const void* h;
   const void* U;
   int B, d, r;
-  unsigned long long* acc;  // [B*r] fixed-point accumulator (zero between calls)
+  unsigned long long* acc;  // [NCOPY][B*r] fixed-point accumulators (zero between calls)
   unsigned int* ticket;     // blocks finished (zero between calls)
   void* t_out;              // [B][r] in the activation dtype
 };
@@ -126,7 +130,7 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
 #pragma unroll
         for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][threadIdx.x];
         const long long fx = __float2ll_rn(v * FIX_SCALE);
-        atomicAdd(p.acc + e, (unsigned long long)fx);
+        atomicAdd(p.acc + (size_t)(c % NCOPY) * BR + e, (unsigned long long)fx);
       }
     }
     __syncthreads();
@@ -140,7 +144,9 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
   if (!s_last) return;
   __threadfence();
   for (int e = threadIdx.x; e < BR; e += blockDim.x) {
-    const long long fx = (long long)atomicExch(p.acc + e, 0ull);
+    long long fx = 0;
+#pragma unroll
+    for (int q = 0; q < NCOPY; ++q) fx += (long long)atomicExch(p.acc + (size_t)q * BR + e, 0ull);
     static_cast<T*>(p.t_out)[e] = Elem<T>::from_f((float)((double)fx * (1.0 / 4294967296.0)));
   }
   if (threadIdx.x == 0) *p.ticket = 0u;
@@ -153,7 +159,7 @@ struct ScoresSmall {
   int* status;
 };
 
-template <typename T>
+template <typename T, int NB>
 __global__ void __launch_bounds__(SB_THREADS, 1)
     k_scores_small(const __grid_constant__ CUtensorMap tmV, ScoresSmall p) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));  // V rows per stage
@@ -206,9 +212,9 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
   {
     // warp w scores group (w % 4) of tile (w / 4) of the current set; lane i owns ids 2i, 2i+1
     const int k_tile = warp / 4, g_in_tile = warp % 4;
-    float acc[MAX_B][2];
+    float acc[NB][2];
 #pragma unroll
-    for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
+    for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = 0.f;
     for (int q = 0; q < total_stages; ++q) {
       const int set = q / bands, band = q % bands;
       const int tile = t0 + set * SET_TILES + k_tile;
@@ -238,12 +244,10 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             v1 = f2.y;
           }
 #pragma unroll
-          for (int b = 0; b < MAX_B; ++b) {
-            if (b < B) {
-              const float tb = st[b * r + j0 + j];
-              acc[b][0] = fmaf(tb, v0, acc[b][0]);
-              acc[b][1] = fmaf(tb, v1, acc[b][1]);
-            }
+          for (int b = 0; b < NB; ++b) {
+            const float tb = st[b * r + j0 + j];
+            acc[b][0] = fmaf(tb, v0, acc[b][0]);
+            acc[b][1] = fmaf(tb, v1, acc[b][1]);
           }
         }
       }
@@ -257,20 +261,18 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
           const int g = tile * (TILE / GROUP) + g_in_tile;
           const uint32_t id0 = (uint32_t)(g * GROUP + 2 * lane);
 #pragma unroll
-          for (int b = 0; b < MAX_B; ++b) {
-            if (b < B) {
-              Top2 sm;
-              sm.init();
-              if ((int)id0 < p.vocab) sm.push(acc[b][0], id0);
-              if ((int)id0 + 1 < p.vocab) sm.push(acc[b][1], id0 + 1);
+          for (int b = 0; b < NB; ++b) {
+            Top2 sm;
+            sm.init();
+            if ((int)id0 < p.vocab) sm.push(acc[b][0], id0);
+            if ((int)id0 + 1 < p.vocab) sm.push(acc[b][1], id0 + 1);
 #pragma unroll
-              for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
-              if (lane == 0 && g < p.n_groups) p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
-            }
+            for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
+            if (lane == 0 && g < p.n_groups) p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
           }
         }
 #pragma unroll
-        for (int b = 0; b < MAX_B; ++b) acc[b][0] = acc[b][1] = 0.f;
+        for (int b = 0; b < NB; ++b) acc[b][0] = acc[b][1] = 0.f;
       }
     }
   }
@@ -301,13 +303,104 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// LSU variant of the scores kernel: one block per 256-id tile, four warps splitting the rank
+// dimension (warp w takes rows [w r/4, (w+1) r/4)).  Lane i owns ids 8i..8i+7 of the tile (one
+// 16-byte vector per row).  Each warp loads its first LSU_BATCH rows into registers before
+// waiting for the projection, so about half of V is already in flight when t arrives; the rest
+// streams in batches of LSU_BATCH rows.  The four warps' partial sums are added in a fixed order
+// through shared memory, then warp g folds group g of the tile into its record.
+constexpr int LSU_WARPS = 4;
+constexpr int LSU_BATCH = 16;
+
+template <typename T, int NB>
+__global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restrict__ V, ScoresSmall p) {
+  constexpr int PER = Elem<T>::PER16;   // ids per lane (8 bf16 / 4 fp32)
+  constexpr int TW = 32 * PER;          // ids per block tile
+  __shared__ float part[LSU_WARPS][NB][TW];
+  __shared__ float st[MAX_BR];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int B = p.B, r = p.r;
+  const int c0 = blockIdx.x * TW + lane * PER;
+  const bool valid = c0 < p.vocab;  // vocab is a multiple of PER
+  const int rq = r / LSU_WARPS;     // rows per warp (r is a multiple of 64 on this path)
+  const int j0 = warp * rq;
+  const T* vp = V + (valid ? c0 : 0);
+  uint4 raw[LSU_BATCH];
+#pragma unroll
+  for (int q = 0; q < LSU_BATCH; ++q)
+    raw[q] = (valid && q < rq) ? ld_nc_v4(vp + (size_t)(j0 + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // t comes from the projection kernel
+  for (int e = threadIdx.x; e < B * r; e += blockDim.x) st[e] = Elem<T>::to_f(static_cast<const T*>(p.t)[e]);
+  __syncthreads();
+  float acc[NB][PER];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc[b][e] = 0.f;
+  for (int jb = 0; jb < rq; jb += LSU_BATCH) {
+    if (jb > 0) {
+#pragma unroll
+      for (int q = 0; q < LSU_BATCH; ++q)
+        raw[q] = (valid && jb + q < rq) ? ld_nc_v4(vp + (size_t)(j0 + jb + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int q = 0; q < LSU_BATCH; ++q) {
+      if (jb + q < rq) {
+        float x[PER];
+        Elem<T>::unpack(raw[q], x);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float tb = st[b * r + j0 + jb + q];
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc[b][e] = fmaf(tb, x[e], acc[b][e]);
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int e = 0; e < PER; ++e) part[warp][b][lane * PER + e] = acc[b][e];
+  __syncthreads();
+  // warp g folds group g (64 ids): lane i takes ids 2i, 2i+1 of the group
+  constexpr int GROUPS = TW / GROUP;
+  for (int g = warp; g < GROUPS; g += LSU_WARPS) {
+    const int col = g * GROUP + 2 * lane;
+    const uint32_t id0 = (uint32_t)(blockIdx.x * TW + col);
+    const int gg = (int)(id0 / GROUP);
+#pragma unroll
+    for (int b = 0; b < NB; ++b) {
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int w = 0; w < LSU_WARPS; ++w) {
+        s0 += part[w][b][col];
+        s1 += part[w][b][col + 1];
+      }
+      Top2 sm;
+      sm.init();
+      if ((int)id0 < p.vocab) sm.push(s0, id0);
+      if ((int)id0 + 1 < p.vocab) sm.push(s1, id0 + 1);
+#pragma unroll
+      for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
+      if (lane == 0 && gg < p.n_groups) p.recs[(size_t)b * p.n_groups + gg] = sm.record((uint32_t)gg * GROUP);
+    }
+  }
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename T, int NB>
+cudaError_t launch_tma(const Ctx& c, cudaLaunchConfig_t& cfg, const CUtensorMap& tmV, const ScoresSmall& sp) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_scores_small<T, NB>, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, k_scores_small<T, NB>, tmV, sp);
+}
+
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
                 void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs, int* status) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
-  static unsigned long long smem_done = 0;
-  cudaError_t e = allow_max_smem(k_scores_small<T>, c.device, &smem_done);
-  if (e != cudaSuccess) return e;
+  cudaError_t e = cudaSuccess;
   EncodeTiledFn fn = encode_fn();
   if (!fn) return note_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
   CUtensorMap tmV;
@@ -353,11 +446,36 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   sp.n_tiles = (vocab + TILE - 1) / TILE;
   sp.recs = recs;
   sp.status = status;
+  const char* f = std::getenv("DH_SCORES_SMALL");
+  const bool lsu = r % (LSU_WARPS * 16) == 0 && !(f && std::strcmp(f, "tma") == 0);
+  if (lsu) {
+    constexpr int TW = 32 * Elem<T>::PER16;
+    cfg.gridDim = dim3((unsigned)((vocab + TW - 1) / TW));
+    cfg.blockDim = dim3(LSU_WARPS * 32);
+    cfg.dynamicSmemBytes = 0;
+    prof_before("scores_lsu", c.stream);
+    switch (B) {
+#define DH_LSU_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_scores_lsu<T, n>, static_cast<const T*>(V), sp); break;
+      DH_LSU_CASE(1) DH_LSU_CASE(2) DH_LSU_CASE(3) DH_LSU_CASE(4) DH_LSU_CASE(5) DH_LSU_CASE(6) DH_LSU_CASE(7)
+      DH_LSU_CASE(8)
+#undef DH_LSU_CASE
+      default: e = cudaErrorInvalidValue;
+    }
+    prof_after(c.stream);
+    if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_scores_lsu)");
+    return note_error(cudaGetLastError(), "small-batch stage 1 launch");
+  }
   cfg.gridDim = dim3((unsigned)c.num_sms);
   cfg.blockDim = dim3(SB_THREADS);
   cfg.dynamicSmemBytes = STAGE_REGION + 1024;
   prof_before("scores_small", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_scores_small<T>, tmV, sp);
+  switch (B) {
+#define DH_TMA_CASE(n) case n: e = launch_tma<T, n>(c, cfg, tmV, sp); break;
+    DH_TMA_CASE(1) DH_TMA_CASE(2) DH_TMA_CASE(3) DH_TMA_CASE(4) DH_TMA_CASE(5) DH_TMA_CASE(6) DH_TMA_CASE(7)
+    DH_TMA_CASE(8)
+#undef DH_TMA_CASE
+    default: e = cudaErrorInvalidValue;
+  }
   prof_after(c.stream);
   if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_scores_small)");
   return note_error(cudaGetLastError(), "small-batch stage 1 launch");
