@@ -178,10 +178,11 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
   const Path path = choose_path(B, r, dtype);
   if (path == PATH_FUSED) {
-    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, ws + L.fix, reinterpret_cast<unsigned int*>(ws + WS_TICKET_OFFSET),
-                       t, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+    unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
-    if (note_error(launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out), "select") != cudaSuccess)
+    if (note_error(launch_select(c, recs, nullptr, acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
+        cudaSuccess)
       return DH_ERR_CUDA;
     return DH_OK;
   }
@@ -198,7 +199,7 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   } else if (note_error(launch_scores_summary(c, t, V, B, r, vocab, dtype, recs), "scores") != cudaSuccess) {
     return DH_ERR_CUDA;
   }
-  if (note_error(launch_select(c, recs, t, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
+  if (note_error(launch_select(c, recs, t, nullptr, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
       cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;

@@ -19,6 +19,13 @@ constexpr size_t WS_TICKET_OFFSET = 72;
 // after the header in the stage-1 workspace.
 constexpr size_t WS_FIX_BYTES = 8 * 2048 * 8;
 
+// The small-batch projection's accumulator: ACC_COPIES copies of B*r (at most 2048) signed 64-bit
+// fixed-point values with scale 2^32 (projection block c adds into copy c mod ACC_COPIES, which
+// keeps the same-address atomics per element low).
+constexpr int ACC_COPIES = 8;
+constexpr int ACC_MAX_BR = 2048;
+static_assert(WS_FIX_BYTES >= (size_t)ACC_COPIES * ACC_MAX_BR * 8, "accumulator fits the fixed region");
+
 // Vocabulary columns summarised together by the stage-1 kernels.  Every group of GROUP consecutive
 // ids yields one GroupRec: its two best (score, id) pairs in (score desc, id asc) order and the
 // third-best score.  The selection step works from these records; the full score row never
@@ -128,6 +135,17 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Element e of t from the fixed-point accumulator copies (copy q at acc + q*BR), rounded to the
+// activation dtype.  The integer sum is exact and order independent, so every reader derives the
+// same t.  Read through L2 (the copies were written by atomics).
+template <typename T>
+__device__ __forceinline__ float acc_to_t(const unsigned long long* acc, int BR, int e) {
+  long long fx = 0;
+#pragma unroll
+  for (int q = 0; q < ACC_COPIES; ++q) fx += (long long)__ldcg(acc + (size_t)q * BR + e);
+  return Elem<T>::to_f(Elem<T>::from_f((float)((double)fx * (1.0 / 4294967296.0))));
+}
+
 __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
   uint4 r;
   asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -160,25 +178,22 @@ bool proj_mma_supported(int B, int d, int r, int dtype);
 int proj_mma_splits(int B, int d, int r, int num_sms);
 cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
                             int max_splits, void* t, int* status);
+// Small-batch stage 1: the projection leaves t in the fixed-point accumulators `acc` (ACC_COPIES
+// copies of B*r values, zero between calls); the scores kernel and the selection read t from there
+// and the selection clears them.
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
-                           int* status);
-bool proj_mma_supported(int B, int d, int r, int dtype);
-int proj_mma_splits(int B, int d, int r, int num_sms);
-cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, int d, int r, float* partial,
-                            int max_splits, void* t, int* status);
-size_t small_b_partial_floats(int B, int r);
-cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int K, int dtype, float* partial, void* t_out, GroupRec* recs,
-                           int32_t* idx_out, float* score_out, void* bar, int* status);
+                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, int* status);
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                GroupRec* recs, int* status);
 
 cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                   int dtype, GroupRec* recs);
 
-cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, const void* V, int B,
-                          int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out);
+// t: [B][r] in the activation dtype, or nullptr with acc set (small-batch path: t is derived from
+// the projection's fixed-point accumulators, which the selection then clears).
+cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc,
+                          const void* V, int B, int r, int vocab, int K, int dtype, int32_t* idx_out,
+                          float* score_out);
 
 bool rescore_supported(int d);
 bool rescore_ring_used(int B, int K, int d, int dtype);

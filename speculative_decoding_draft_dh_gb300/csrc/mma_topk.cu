@@ -94,21 +94,32 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // the selection kernel may launch now; it waits (griddepcontrol.wait) for this grid's records
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ TMA producer
       prefetch_tmap(&tmA);
       prefetch_tmap(&tmB);
-      mbar_arrive_expect_tx(a_full, (uint32_t)(nkc * A_CHUNK_BYTES));
-      for (int kc = 0; kc < nkc; ++kc) tma_load_2d(sA + kc * A_CHUNK_BYTES, &tmA, kc * BK, m * BM, a_full);
+      // V does not depend on the projection: the first round of stages is issued before waiting
+      // for the previous kernel (programmatic dependent launch), T (the A operand) after it.
+      bool a_issued = false;
+      auto issue_a = [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        mbar_arrive_expect_tx(a_full, (uint32_t)(nkc * A_CHUNK_BYTES));
+        for (int kc = 0; kc < nkc; ++kc) tma_load_2d(sA + kc * A_CHUNK_BYTES, &tmA, kc * BK, m * BM, a_full);
+        a_issued = true;
+      };
       uint32_t issued_parity = 0;  // bit s: parity of the last load issued into stage s
       uint32_t issued_mask = 0;
-      int s = 0;
+      int s = 0, n_issued = 0;
       uint32_t ph = 0;
       for (int t = 0; t < ntiles && !s_abort; ++t) {
         const int n0 = (nt0 + t) * BN;
         for (int kc = 0; kc < nkc; ++kc) {
+          if (!a_issued && n_issued == stages) issue_a();
+          ++n_issued;
           if (!mbar_wait(&b_empty[s], ph ^ 1u, WAIT_NS)) { raise_timeout(&s_abort, p.status); break; }
           mbar_arrive_expect_tx(&b_full[s], B_STAGE_BYTES);
 #pragma unroll
@@ -119,6 +130,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (++s == stages) { s = 0; ph ^= 1u; }
         }
       }
+      if (!a_issued) issue_a();
       // every copy this CTA issued must land before the CTA can exit
       mbar_wait(a_full, 0, WAIT_NS);
       for (int q = 0; q < stages; ++q)
@@ -266,6 +278,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // the reduce kernel may launch now; it waits (griddepcontrol.wait) for the partial sums
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   if (warp == 0) {
     if (lane == 0) {
@@ -341,7 +355,11 @@ __global__ void __launch_bounds__(THREADS, 1)
 
 // t[e] = bf16(sum over s of partial[s][e]), slices in ascending order (deterministic).  Each
 // thread owns four consecutive outputs (B*r is a multiple of 64) and keeps 8 slices in flight.
+// Launched with programmatic dependent launch: waits for the projection's partial sums, then lets
+// the scores kernel launch (it prefetches V and waits for t itself).
 __global__ void k_proj_reduce_mma(const float* __restrict__ partial, int BR, int splits, __nv_bfloat16* __restrict__ t) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int e = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
   if (e >= BR) return;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -443,9 +461,20 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
   e = cudaGetLastError();
   if (e != cudaSuccess) return note_error(e, "launch k_proj_mma");
   const int BR = B * r;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((BR / 4 + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before("proj_reduce_mma", c.stream);
-  k_proj_reduce_mma<<<(BR / 4 + 255) / 256, 256, 0, c.stream>>>(partial, BR, p.splits, static_cast<__nv_bfloat16*>(t));
+  e = cudaLaunchKernelEx(&cfg, k_proj_reduce_mma, static_cast<const float*>(partial), BR, p.splits,
+                         static_cast<__nv_bfloat16*>(t));
   prof_after(c.stream);
+  if (e != cudaSuccess) return note_error(e, "launch k_proj_reduce_mma");
   return note_error(cudaGetLastError(), "launch k_proj_reduce_mma");
 }
 
@@ -478,9 +507,21 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   p.stages = stages;
   p.recs = recs;
   p.status = status;
+  // programmatic dependent launch: set-up and the first V stages overlap the projection's tail
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(num_m * p.n_split));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   prof_before("lowrank_mma", c.stream);
-  k_lowrank_mma<<<num_m * p.n_split, THREADS, smem, c.stream>>>(tmA, tmB, p);
+  e = cudaLaunchKernelEx(&cfg, k_lowrank_mma, tmA, tmB, p);
   prof_after(c.stream);
+  if (e != cudaSuccess) return note_error(e, "launch k_lowrank_mma");
   return note_error(cudaGetLastError(), "launch k_lowrank_mma");
 }
 

@@ -8,6 +8,9 @@
 // Gather-GEMV: one warp per (row, candidate) streams W[idx] (d contiguous values) with 16-byte
 // loads against h[row] staged in shared memory, accumulates in fp32 and reduces with shuffles.  An index outside [0, vocab)
 // is never dereferenced: its logit becomes NaN (and so do the row's probabilities).
+#include <cstdlib>
+#include <cstring>
+
 #include "dh_internal.cuh"
 #include "sm100.cuh"
 
@@ -18,6 +21,37 @@ constexpr int WARPS = 8;          // candidates per block (one warp each), large
 constexpr int THREADS = WARPS * 32;
 constexpr int MAXW = 20;          // 16-byte W vectors per lane in flight (d = 5120 bf16 in one batch)
 constexpr int MAX_D_SMEM = 8192;  // h row staged in shared memory (bf16: 16 KB, fp32: 32 KB)
+
+// One warp's dot product of h (staged in shared memory) with W row v: each lane keeps MAXW
+// 16-byte loads of the row in flight, then the warp reduces with shuffles (every lane gets the sum).
+template <typename T>
+__device__ __forceinline__ float warp_row_dot(const T* __restrict__ W, int v, int d, const T* sh_h, int lane) {
+  constexpr int PER = Elem<T>::PER16;
+  const T* w = W + (size_t)v * d;
+  float acc = 0.f;
+  for (int c0 = 0; c0 < d; c0 += 32 * PER * MAXW) {
+    uint4 wa[MAXW];
+#pragma unroll
+    for (int q = 0; q < MAXW; ++q) {
+      const int c = c0 + (q * 32 + lane) * PER;
+      if (c < d) wa[q] = ld_nc_v4(w + c);
+    }
+#pragma unroll
+    for (int q = 0; q < MAXW; ++q) {
+      const int c = c0 + (q * 32 + lane) * PER;
+      if (c < d) {
+        float wf[PER], xf[PER];
+        Elem<T>::unpack(wa[q], wf);
+        Elem<T>::unpack(*reinterpret_cast<const uint4*>(sh_h + c), xf);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
+}
 
 // Block (b, kb) scores candidates kb*8 .. kb*8+7 of row b.  The block stages h[b] in shared
 // memory (before waiting on the previous kernel: h does not depend on it), then each warp streams
@@ -49,31 +83,7 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h,
     const int pair = b * K + k;
     const int v = idx[pair];
     const bool ok = v >= 0 && v < vocab;
-    float acc = 0.f;
-    if (ok) {
-      const T* w = W + (size_t)v * d;
-      for (int c0 = 0; c0 < d; c0 += 32 * PER * MAXW) {
-        uint4 wa[MAXW];
-#pragma unroll
-        for (int q = 0; q < MAXW; ++q) {
-          const int c = c0 + (q * 32 + lane) * PER;
-          if (c < d) wa[q] = ld_nc_v4(w + c);
-        }
-#pragma unroll
-        for (int q = 0; q < MAXW; ++q) {
-          const int c = c0 + (q * 32 + lane) * PER;
-          if (c < d) {
-            float wf[PER], xf[PER];
-            Elem<T>::unpack(wa[q], wf);
-            Elem<T>::unpack(*reinterpret_cast<const uint4*>(sh_h + c), xf);
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    const float acc = ok ? warp_row_dot<T>(W, v, d, sh_h, lane) : 0.f;
     if (lane == 0) logits[pair] = ok ? acc : __int_as_float(0x7FC00000);
   }
   if (!probs) return;
@@ -116,6 +126,139 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h,
   __syncthreads();
   const float inv = s_bcast;
   for (int i = threadIdx.x; i < K; i += (NWARP * 32)) probs[(size_t)b * K + i] = expf(__ldcg(z + i) - m) * inv;
+}
+
+// ------------------------------------------------------------------------------------------------
+// Cluster variant for small batches with K <= CL_MAX_K: one thread-block cluster of up to 8 CTAs
+// per row; warp w of cluster CTA c scores candidates c*NWARP + w, c*NWARP + w + CTAs*NWARP, ...
+// Each warp also stores its logit into the leader CTA's shared memory (distributed shared
+// memory); after a cluster barrier the leader computes the row's softmax from there, without
+// the global ticket and the L2 round trips of the ticket scheme.  Every CTA passes both cluster
+// barriers (no early exit), so the barriers always complete.
+constexpr int CL_MAX_K = 128;
+constexpr int CL_MAX_CTAS = 8;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+// Stores v at the same shared-memory offset as `local` in cluster CTA `rank`.
+__device__ __forceinline__ void st_cluster_f32(float* local, uint32_t rank, float v) {
+  uint32_t remote;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(sm100::smem_u32(local)), "r"(rank));
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(remote), "f"(v) : "memory");
+}
+
+template <typename T, int NWARP>
+__global__ void __launch_bounds__(NWARP * 32) k_rescore_cl(const T* __restrict__ h, const T* __restrict__ W,
+                                                        const int32_t* __restrict__ idx, int d, int vocab, int K,
+                                                        float* __restrict__ logits, float* __restrict__ probs) {
+  constexpr int PER = Elem<T>::PER16;
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  T* sh_h = reinterpret_cast<T*>(smem_raw);
+  __shared__ float s_z[CL_MAX_K];  // leader CTA: the row's logits
+  __shared__ float red[NWARP];
+  __shared__ float s_bcast;
+  const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
+  const int b = (int)(blockIdx.x / csize);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // phase 1 of the cluster barrier: this CTA is running (its shared memory may be written)
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+  const T* x = h + (size_t)b * d;
+  for (int c = threadIdx.x * PER; c < d; c += (NWARP * 32) * PER)
+    *reinterpret_cast<uint4*>(sh_h + c) = __ldg(reinterpret_cast<const uint4*>(x + c));
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.aligned;" ::: "memory");  // every CTA of the cluster is running
+  for (int k = (int)crank * NWARP + warp; k < K; k += (int)csize * NWARP) {
+    const int pair = b * K + k;
+    const int v = idx[pair];
+    const bool ok = v >= 0 && v < vocab;
+    const float acc = ok ? warp_row_dot<T>(W, v, d, sh_h, lane) : 0.f;
+    const float z = ok ? acc : __int_as_float(0x7FC00000);
+    if (lane == 0) {
+      logits[pair] = z;
+      st_cluster_f32(&s_z[k], 0, z);
+    }
+  }
+  // phase 2: the leader sees every logit of the row
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (crank != 0 || !probs) return;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < K; i += NWARP * 32) m = fmaxf(m, s_z[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = red[0];
+    for (int i = 1; i < NWARP; ++i) mm = fmaxf(mm, red[i]);
+    s_bcast = mm;
+  }
+  __syncthreads();
+  m = s_bcast;
+  float ssum = 0.f;
+  for (int i = threadIdx.x; i < K; i += NWARP * 32) ssum += expf(s_z[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = ssum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < NWARP; ++i) tot += red[i];
+    s_bcast = 1.f / tot;
+  }
+  __syncthreads();
+  const float inv = s_bcast;
+  for (int i = threadIdx.x; i < K; i += NWARP * 32) probs[(size_t)b * K + i] = expf(s_z[i] - m) * inv;
+}
+
+template <typename T, int NWARP>
+cudaError_t launch_cl(const Ctx& c, const T* h, const T* W, const int32_t* idx, int B, int d, int vocab, int K,
+                      float* logits, float* probs) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_rescore_cl<T, NWARP>, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  const int ctas = min(CL_MAX_CTAS, (K + NWARP - 1) / NWARP);
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = (unsigned)ctas;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * ctas));
+  cfg.blockDim = dim3(NWARP * 32);
+  cfg.dynamicSmemBytes = (size_t)d * sizeof(T);
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  prof_before("rescore_cluster", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_rescore_cl<T, NWARP>, h, W, idx, d, vocab, K, logits, probs);
+  prof_after(c.stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+// Smallest warp count per CTA with at most one candidate per warp on a full cluster.
+template <typename T>
+cudaError_t run_cl(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                   float* logits, float* probs) {
+  const T* hh = static_cast<const T*>(h);
+  const T* ww = static_cast<const T*>(W);
+  if (K <= 2 * CL_MAX_CTAS) return launch_cl<T, 2>(c, hh, ww, idx, B, d, vocab, K, logits, probs);
+  if (K <= 4 * CL_MAX_CTAS) return launch_cl<T, 4>(c, hh, ww, idx, B, d, vocab, K, logits, probs);
+  if (K <= 8 * CL_MAX_CTAS) return launch_cl<T, 8>(c, hh, ww, idx, B, d, vocab, K, logits, probs);
+  return launch_cl<T, 16>(c, hh, ww, idx, B, d, vocab, K, logits, probs);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -310,6 +453,10 @@ cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
                 int K, float* logits, float* probs, uint32_t* tickets) {
+  // K <= CL_MAX_K: the cluster kernel (DH_FORCE_RESCORE=ticket selects the ticket kernel instead)
+  const char* f = std::getenv("DH_FORCE_RESCORE");
+  if (K <= CL_MAX_K && !(f && std::strcmp(f, "ticket") == 0))
+    return run_cl<T>(c, h, W, idx, B, d, vocab, K, logits, probs);
   // Small problems use 2-warp blocks so that more SMs pull W rows; larger ones 8-warp blocks.
   const int nw = (long long)B * K <= 512 ? 2 : WARPS;
   static unsigned long long smem_done2 = 0, smem_done8 = 0;

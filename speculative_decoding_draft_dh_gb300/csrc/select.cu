@@ -6,20 +6,24 @@ namespace {
 
 template <typename T>
 __global__ void __launch_bounds__(sel::SEL_THREADS, 1) k_select(const GroupRec* __restrict__ recs,
-                                                            const T* __restrict__ t, const T* __restrict__ V,
-                                                            int r, int vocab, int K, int32_t* __restrict__ idx_out,
+                                                            const T* __restrict__ t, unsigned long long* acc,
+                                                            const T* __restrict__ V, int r, int vocab, int K,
+                                                            int32_t* __restrict__ idx_out,
                                                             float* __restrict__ score_out) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // the rescoring kernel may launch now (it stages h, then waits for this grid's candidates)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the previous kernel
   const int row = blockIdx.x;
   const int n_groups = (vocab + GROUP - 1) / GROUP;
-  sel::select_row<T>(smem_raw, recs + (size_t)row * n_groups, t + (size_t)row * r, V, r, vocab, K,
+  sel::select_row<T>(smem_raw, recs + (size_t)row * n_groups, t ? t + (size_t)row * r : nullptr,
+                     acc ? acc + (size_t)row * r : nullptr, (int)gridDim.x * r, V, r, vocab, K,
                      idx_out + (size_t)row * K, score_out + (size_t)row * K);
 }
 
 template <typename T>
-cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, const void* V, int B, int r, int vocab,
-                int K, int32_t* idx_out, float* score_out) {
+cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc, const void* V, int B,
+                int r, int vocab, int K, int32_t* idx_out, float* score_out) {
   const int n_groups = (vocab + GROUP - 1) / GROUP;
   const size_t smem = sel::select_smem_bytes(n_groups);
   static unsigned long long smem_done = 0;
@@ -36,8 +40,8 @@ cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, const void* V
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before("select", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_select<T>, recs, static_cast<const T*>(t), static_cast<const T*>(V), r, vocab, K,
-                         idx_out, score_out);
+  e = cudaLaunchKernelEx(&cfg, k_select<T>, recs, static_cast<const T*>(t), acc, static_cast<const T*>(V), r, vocab,
+                         K, idx_out, score_out);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -45,10 +49,11 @@ cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, const void* V
 
 }  // namespace
 
-cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, const void* V, int B, int r,
-                          int vocab, int K, int dtype, int32_t* idx_out, float* score_out) {
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, recs, t, V, B, r, vocab, K, idx_out, score_out);
-  return run<float>(c, recs, t, V, B, r, vocab, K, idx_out, score_out);
+cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc,
+                          const void* V, int B, int r, int vocab, int K, int dtype, int32_t* idx_out,
+                          float* score_out) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out);
+  return run<float>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out);
 }
 
 }  // namespace dh

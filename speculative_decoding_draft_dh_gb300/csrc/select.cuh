@@ -32,6 +32,7 @@ constexpr int HIST_BINS = 4096;  // widest radix digit (12 bits)
 struct Shared {
   uint32_t hist[HIST_BINS];
   uint32_t wsum[SEL_THREADS / 32];
+  uint32_t wmin[SEL_THREADS / 32], wmax[SEL_THREADS / 32];
   uint32_t digit, run, bincount, total, cnt, nref;
   int32_t rg[RMAX];
   uint32_t bitmap[BITMAP_WORDS];
@@ -143,63 +144,44 @@ __device__ __forceinline__ bool key_before(uint32_t ka, uint32_t ia, uint32_t kb
   return ka > kb || (ka == kb && ia < ib);
 }
 
-// Sorts sh.sk/sh.si[0..K) (padded to a power of two) into ranking order.  K <= 64: one warp with
-// shuffles; larger K: a block-wide bitonic network in shared memory.
+// Appends for the lanes whose pred is set: returns each such lane's position in the list whose
+// length is *counter (one shared atomic per warp).  Called by all 32 lanes of the warp.
+__device__ __forceinline__ uint32_t warp_append(bool pred, uint32_t* counter) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t b = __ballot_sync(0xFFFFFFFFu, pred);
+  uint32_t base = 0;
+  if (lane == 0 && b) base = atomicAdd(counter, (uint32_t)__popc(b));
+  base = __shfl_sync(0xFFFFFFFFu, base, 0);
+  return base + (uint32_t)__popc(b & ((1u << lane) - 1u));
+}
+
+// Sorts sh.sk/sh.si[0..K) into ranking order by counting: with (key, id) packed as
+// key << 32 | ~id (ranking order = descending packed value; ids are unique, so the packed values
+// are distinct), an entry's rank is the number of entries with a larger packed value.  P threads
+// share an entry (P = the largest power of two <= 32 with K * P <= blockDim.x), each counting over
+// K / P of the entries, and add their counts with shuffles.  Uses sh.hist as scratch.
 __device__ inline void sort_selected(Shared& sh, int K) {
-  int P = 1;
-  while (P < K) P <<= 1;
-  for (int i = K + threadIdx.x; i < P; i += blockDim.x) { sh.sk[i] = 0u; sh.si[i] = 0xFFFFFFFFu; }
+  unsigned long long* sp = reinterpret_cast<unsigned long long*>(sh.hist);  // K <= DH_MAX_K entries
+  for (int i = threadIdx.x; i < K; i += blockDim.x)
+    sp[i] = ((unsigned long long)sh.sk[i] << 32) | (unsigned long long)(~sh.si[i]);
   __syncthreads();
-  if (P <= 64) {
-    if (threadIdx.x < 32) {
-      const int lane = threadIdx.x;
-      uint32_t k0 = 0, i0 = 0xFFFFFFFFu, k1 = 0, i1 = 0xFFFFFFFFu;
-      if (2 * lane < P) { k0 = sh.sk[2 * lane]; i0 = sh.si[2 * lane]; }
-      if (2 * lane + 1 < P) { k1 = sh.sk[2 * lane + 1]; i1 = sh.si[2 * lane + 1]; }
-      for (int size = 2; size <= 64; size <<= 1) {
-        for (int j = size >> 1; j > 0; j >>= 1) {
-          if (j == 1) {
-            const int p0 = 2 * lane;
-            const bool up = (p0 & size) == 0;
-            const bool b_first = key_before(k1, i1, k0, i0);
-            if (b_first == up) {
-              uint32_t tk = k0, ti = i0;
-              k0 = k1; i0 = i1; k1 = tk; i1 = ti;
-            }
-          } else {
-            const int src = lane ^ (j >> 1);
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              uint32_t& mk = e ? k1 : k0;
-              uint32_t& mi = e ? i1 : i0;
-              const uint32_t ok_ = __shfl_sync(0xFFFFFFFFu, mk, src);
-              const uint32_t oi = __shfl_sync(0xFFFFFFFFu, mi, src);
-              const int p = 2 * lane + e;
-              const bool up = (p & size) == 0;
-              const bool lower = (p & j) == 0;
-              const bool mine_first = key_before(mk, mi, ok_, oi);
-              const bool keep_first = (up == lower);
-              if (keep_first != mine_first) { mk = ok_; mi = oi; }
-            }
-          }
-        }
-      }
-      if (2 * lane < P) { sh.sk[2 * lane] = k0; sh.si[2 * lane] = i0; }
-      if (2 * lane + 1 < P) { sh.sk[2 * lane + 1] = k1; sh.si[2 * lane + 1] = i1; }
+  int P = 1;
+  while (P < 32 && K * (2 * P) <= (int)blockDim.x) P <<= 1;
+  const int per = (K + P - 1) / P;
+  for (int base = 0; base < K * P; base += blockDim.x) {
+    const int t = base + (int)threadIdx.x;
+    const int i = t / P, h = t % P;
+    int rank = 0;
+    unsigned long long pi = 0;
+    if (i < K) {
+      pi = sp[i];
+      const int j1 = min(K, (h + 1) * per);
+      for (int j = h * per; j < j1; ++j) rank += sp[j] > pi ? 1 : 0;
     }
-    __syncthreads();
-    return;
-  }
-  for (int size = 2; size <= P; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < P / 2; i += blockDim.x) {
-        const int a0 = 2 * i - (i & (stride - 1));
-        const int b0 = a0 + stride;
-        const bool up = (a0 & size) == 0;
-        const uint32_t ka = sh.sk[a0], kb = sh.sk[b0], ia = sh.si[a0], ib = sh.si[b0];
-        if (key_before(kb, ib, ka, ia) == up) { sh.sk[a0] = kb; sh.sk[b0] = ka; sh.si[a0] = ib; sh.si[b0] = ia; }
-      }
+    for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    if (i < K && h == 0) {
+      sh.sk[rank] = (uint32_t)(pi >> 32);
+      sh.si[rank] = ~(uint32_t)pi;
     }
   }
   __syncthreads();
@@ -241,6 +223,134 @@ __device__ bool select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
   return true;
 }
 
+// Fast path for a pool that fits in registers (at most FP_ENT entries per thread).  MSB-first
+// radix select over y = key - (smallest key of the pool), with 2048 bins per level: level 0 takes
+// the 11 bits of y below its highest set bit of the pool's range (so the bins span the pool's
+// own key range, and the keys, which crowd into a narrow range of scores, spread over many bins),
+// each further level the next 11 bits.  The descent stops at the first level whose boundary bin
+// (the bin holding the K-th entry) has at most FP_RANK entries.  Entries above the boundary bin
+// are selected, the boundary bin's entries ranked by counting and the best K - above of them
+// taken.  Writes the sorted K and returns true; returns false (nothing written) when the pool has
+// fewer than K entries or the boundary bin still holds more than FP_BOUND entries after the last
+// level (many equal keys), and the caller then runs the generic radix selection.
+constexpr int FP_ENT = 12;
+constexpr int FP_BINS = 2048;
+constexpr int FP_BITS = 11;
+constexpr int FP_BOUND = 512;  // largest boundary bin ranked by counting (after the last level)
+constexpr int FP_RANK = 32;    // a level whose boundary bin holds at most this many ends the descent
+
+template <class Load>
+__device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int32_t* idx_out, float* score_out,
+                            uint32_t* thr_out) {
+  if (n_entries_max > FP_ENT * (int)blockDim.x) return false;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t key[FP_ENT], id[FP_ENT];
+  load(key, id);  // key 0 = no entry
+  // the pool's key range
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < FP_ENT; ++q)
+    if (key[q]) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  if (lane == 0) { sh.wmin[warp] = kmin; sh.wmax[warp] = kmax; }
+  __syncthreads();
+  for (int w = 0; w < nw; ++w) { kmin = min(kmin, sh.wmin[w]); kmax = max(kmax, sh.wmax[w]); }
+  if (kmax == 0u) return false;  // empty pool (uniform: every thread read the same values)
+#pragma unroll
+  for (int q = 0; q < FP_ENT; ++q) key[q] = key[q] ? key[q] - kmin + 1u : 0u;  // y + 1 (0 = no entry)
+  const uint32_t range = kmax - kmin + 1u;
+  int shift = max(0, (32 - __clz((int)range)) - FP_BITS);
+  if (range >= 0x80000000u) shift = 32 - FP_BITS;
+  uint32_t* hist = sh.hist;
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)K, above = 0, bc = 0;
+  bool first = true;
+#pragma unroll 1
+  for (;;) {
+    const uint32_t dmask = (uint32_t)FP_BINS - 1u;
+    for (int i = threadIdx.x; i < FP_BINS; i += blockDim.x) hist[i] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int q = 0; q < FP_ENT; ++q)
+      if (key[q] && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & dmask], 1u);
+    __syncthreads();
+    find_digit(sh, FP_BINS, krem, first);
+    __syncthreads();
+    const uint32_t D = sh.digit, run = sh.run, total = sh.total;
+    bc = sh.bincount;
+    __syncthreads();
+    if (first && total < (uint32_t)K) return false;
+    first = false;
+    prefix |= D << shift;
+    mask |= dmask << shift;
+    krem -= run;
+    above += run;
+    if (bc <= (uint32_t)FP_RANK || shift == 0) break;  // ranking the boundary bin by counting is cheap
+    shift = max(0, shift - FP_BITS);
+  }
+  if (bc > (uint32_t)FP_BOUND) return false;
+  // compaction: block scan of the per-thread counts (above the bin in the low 16 bits, in the
+  // boundary bin in the high 16 bits), then every thread writes its entries at its offsets
+  uint32_t nu = 0, nb = 0;
+#pragma unroll
+  for (int q = 0; q < FP_ENT; ++q) {
+    const uint32_t mk = key[q] & mask;
+    nu += (key[q] && mk > prefix) ? 1u : 0u;
+    nb += (key[q] && mk == prefix) ? 1u : 0u;
+  }
+  const uint32_t mine = nu | (nb << 16);
+  uint32_t incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sh.wsum[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0;
+  for (int w = 0; w < warp; ++w) before += sh.wsum[w];
+  const uint32_t excl = before + incl - mine;
+  uint32_t pu = excl & 0xFFFFu, pb = excl >> 16;
+  uint32_t* bk = reinterpret_cast<uint32_t*>(sh.rs);  // boundary bin: keys, then ids at + FP_BOUND
+  uint32_t* bi = bk + FP_BOUND;
+#pragma unroll
+  for (int q = 0; q < FP_ENT; ++q) {
+    const uint32_t mk = key[q] & mask;
+    const uint32_t k0 = key[q] - 1u + kmin;  // the original key
+    if (key[q] && mk > prefix) {
+      sh.sk[pu] = k0;
+      sh.si[pu] = id[q];
+      ++pu;
+    } else if (key[q] && mk == prefix) {
+      bk[pb] = k0;
+      bi[pb] = id[q];
+      ++pb;
+    }
+  }
+  __syncthreads();
+  // the boundary entries ranking below the first K - above of the bin are dropped; the others go
+  // to sk/si after the entries above the bin (their rank among the bin's entries is unique)
+  const int need = K - (int)above;
+  for (int i = threadIdx.x; i < (int)bc; i += blockDim.x) {
+    const uint32_t ki = bk[i], ii = bi[i];
+    int rank = 0;
+    for (int j = 0; j < (int)bc; ++j) rank += key_before(bk[j], bi[j], ki, ii) ? 1 : 0;
+    if (rank < need) {
+      sh.sk[above + rank] = ki;
+      sh.si[above + rank] = ii;
+    }
+  }
+  __syncthreads();
+  sort_selected(sh, K);
+  for (int k = threadIdx.x; k < K; k += blockDim.x) {
+    idx_out[k] = (int32_t)sh.si[k];
+    score_out[k] = fkey_inv(sh.sk[k]);
+  }
+  if (thr_out) *thr_out = sh.sk[K - 1];
+  __syncthreads();
+  return true;
+}
+
 template <typename T>
 __device__ __forceinline__ float score_col(const float* t, const T* V, int r, int vocab, int c) {
   float acc = 0.f;
@@ -249,37 +359,69 @@ __device__ __forceinline__ float score_col(const float* t, const T* V, int r, in
   return acc;
 }
 
+// Four consecutive values of a V row as floats (8-byte load for bf16, 16-byte for fp32; the
+// address is a multiple of 4 elements and rows start 16-byte aligned).
+template <typename T>
+__device__ __forceinline__ void load4(const T* p, float* x);
+template <>
+__device__ __forceinline__ void load4<__nv_bfloat16>(const __nv_bfloat16* p, float* x) {
+  const uint2 u = __ldg(reinterpret_cast<const uint2*>(p));
+  x[0] = __uint_as_float(u.x << 16);
+  x[1] = __uint_as_float(u.x & 0xFFFF0000u);
+  x[2] = __uint_as_float(u.y << 16);
+  x[3] = __uint_as_float(u.y & 0xFFFF0000u);
+}
+template <>
+__device__ __forceinline__ void load4<float>(const float* p, float* x) {
+  const float4 u = __ldg(reinterpret_cast<const float4*>(p));
+  x[0] = u.x;
+  x[1] = u.y;
+  x[2] = u.z;
+  x[3] = u.w;
+}
+
 // Exact scores of the 64 ids of group g (ids >= vocab give -inf) into out[0..64).  The block's
-// warps split the r rows of V: warp w covers rows [w*rw, (w+1)*rw) with all its loads in flight
-// (lane i reads the two ids 2i, 2i+1), then the per-warp partial sums are added in warp order
-// (a fixed order, so the result is deterministic).  scratch: SEL_THREADS / 32 * 64 floats.
+// warps split the r rows of V: warp w covers rows [w*rw, (w+1)*rw), two rows per instruction
+// (lanes 0-15 the even rows, 16-31 the odd ones; lane i loads ids 4(i mod 16) .. +3), with up to
+// 16 loads per lane in flight.  The two halves are added with one shuffle, then the per-warp
+// partial sums are added in warp order (a fixed order, so the result is deterministic).
+// scratch: SEL_THREADS / 32 * 64 floats.  vocab is a multiple of 4.
 template <typename T>
 __device__ void score_group(const float* t, const T* __restrict__ V, int r, int vocab, int g, float* out,
                             float* scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int rw = (r + nw - 1) / nw;
   const int j0 = warp * rw, j1 = min(r, j0 + rw);
-  const int c = g * GROUP + 2 * lane;
-  float a0 = 0.f, a1 = 0.f;
+  const int half = lane >> 4;
+  const int c = g * GROUP + 4 * (lane & 15);
+  const bool cok = c < vocab;
+  float a[4] = {0.f, 0.f, 0.f, 0.f};
   constexpr int BATCH = 16;
-  for (int jb = j0; jb < j1; jb += BATCH) {
-    float v0[BATCH], v1[BATCH];
+  for (int jb = j0; jb < j1; jb += 2 * BATCH) {
+    float v[BATCH][4];
 #pragma unroll
     for (int q = 0; q < BATCH; ++q) {
-      const int j = jb + q;
-      v0[q] = (j < j1 && c < vocab) ? Elem<T>::to_f(V[(size_t)j * vocab + c]) : 0.f;
-      v1[q] = (j < j1 && c + 1 < vocab) ? Elem<T>::to_f(V[(size_t)j * vocab + c + 1]) : 0.f;
+      const int j = jb + 2 * q + half;
+      if (j < j1 && cok) {
+        load4<T>(V + (size_t)j * vocab + c, v[q]);
+      } else {
+        v[q][0] = v[q][1] = v[q][2] = v[q][3] = 0.f;
+      }
     }
 #pragma unroll
     for (int q = 0; q < BATCH; ++q) {
-      const int j = jb + q;
+      const int j = jb + 2 * q + half;
       const float tj = (j < j1) ? t[j] : 0.f;
-      a0 = fmaf(tj, v0[q], a0);
-      a1 = fmaf(tj, v1[q], a1);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) a[e] = fmaf(tj, v[q][e], a[e]);
     }
   }
-  scratch[warp * 64 + 2 * lane] = a0;
-  scratch[warp * 64 + 2 * lane + 1] = a1;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
+  if (lane < 16) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) scratch[warp * 64 + 4 * lane + e] = a[e];
+  }
   __syncthreads();
   if (threadIdx.x < 64) {
     float s = 0.f;
@@ -289,8 +431,6 @@ __device__ void score_group(const float* t, const T* __restrict__ V, int r, int 
   __syncthreads();
 }
 
-
-
 // Shared memory select_row needs: the Shared block plus, when n_groups <= CACHE_GROUPS, a copy of
 // the row's records.
 __host__ __device__ constexpr size_t select_smem_bytes(int n_groups) {
@@ -298,21 +438,34 @@ __host__ __device__ constexpr size_t select_smem_bytes(int n_groups) {
 }
 
 // Exact top-K of one row.  smem: select_smem_bytes(n_groups) bytes, 16-byte aligned.
-// t_row: the row's projection (r values of the activation dtype); rrow: its n_groups records.
+// t_row: the row's projection (r values of the activation dtype), or nullptr with acc_row set: the
+// row's slice of the small-batch projection's fixed-point accumulators (copies BR apart), which
+// this block reads and then clears.  rrow: the row's n_groups records.
 template <typename T>
 __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rrow, const T* __restrict__ t_row,
-                           const T* __restrict__ V, int r, int vocab, int K, int32_t* __restrict__ idx_out,
-                           float* __restrict__ score_out) {
+                           unsigned long long* __restrict__ acc_row, int BR, const T* __restrict__ V, int r,
+                           int vocab, int K, int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
   Shared& sh = *reinterpret_cast<Shared*>(smem);
   GroupRec* cache = reinterpret_cast<GroupRec*>(smem + align_up(sizeof(Shared), 16));
   const int n_groups = (vocab + GROUP - 1) / GROUP;
   const bool cached = n_groups <= CACHE_GROUPS;
 
   for (int g = threadIdx.x; g < (int)BITMAP_WORDS; g += blockDim.x) sh.bitmap[g] = 0u;
-  for (int j = threadIdx.x; j < r; j += blockDim.x) sh.t[j] = Elem<T>::to_f(t_row[j]);
+  if (acc_row) {
+    for (int j = threadIdx.x; j < r; j += blockDim.x) {
+      sh.t[j] = acc_to_t<T>(acc_row, BR, j);
+#pragma unroll
+      for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;  // zero for the next call
+    }
+  } else {
+    for (int j = threadIdx.x; j < r; j += blockDim.x) sh.t[j] = Elem<T>::to_f(t_row[j]);
+  }
+  // the row's records: in registers (thread i holds groups i, i + SEL_THREADS, ...) for the fast
+  // path and the certificate, and copied to shared memory for the generic path and the refinement
+  constexpr int PER_THREAD = (CACHE_GROUPS + SEL_THREADS - 1) / SEL_THREADS;
+  static_assert(2 * PER_THREAD == FP_ENT, "fast path holds two pool entries per cached record");
+  GroupRec tmp[PER_THREAD];
   if (cached) {
-    constexpr int PER_THREAD = (CACHE_GROUPS + SEL_THREADS - 1) / SEL_THREADS;
-    GroupRec tmp[PER_THREAD];
 #pragma unroll
     for (int q = 0; q < PER_THREAD; ++q) {
       const int g = threadIdx.x + q * SEL_THREADS;
@@ -339,15 +492,41 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
   };
 
   uint32_t tau = 0;
-  if (select_sort_write(pool, K, sh, idx_out, score_out, &tau)) {
+  auto load_pool = [&](uint32_t* key, uint32_t* id) {
+#pragma unroll
+    for (int q = 0; q < PER_THREAD; ++q) {
+      const int g = threadIdx.x + q * SEL_THREADS;
+      key[2 * q] = key[2 * q + 1] = 0u;
+      id[2 * q] = id[2 * q + 1] = 0xFFFFFFFFu;
+      if (g < n_groups) {
+        const GroupRec rc = tmp[q];
+        const uint32_t o1 = rc.offs & 0xFFu, o2 = (rc.offs >> 8) & 0xFFu;
+        if (o1 != NO_OFFSET) { key[2 * q] = fkey(rc.m1); id[2 * q] = (uint32_t)g * GROUP + o1; }
+        if (o2 != NO_OFFSET) { key[2 * q + 1] = fkey(rc.m2); id[2 * q + 1] = (uint32_t)g * GROUP + o2; }
+      }
+    }
+  };
+  bool selected = cached && fast_select(load_pool, 2 * n_groups, K, sh, idx_out, score_out, &tau);
+  if (threadIdx.x == 0) sh.nref = 0;
+  __syncthreads();
+  if (!selected) selected = select_sort_write(pool, K, sh, idx_out, score_out, &tau);
+  if (selected) {
     // Certificate: groups that may hide a member ranking at or above tau (third score >= tau).
     // tau is at or below the true K-th score, so without such groups the pool's top K is exact.
-    for (int g = threadIdx.x; g < n_groups; g += blockDim.x) {
-      if (fkey(src[g].m3) >= tau) {
-        const uint32_t pos = atomicAdd(&sh.nref, 1u);
-        if (pos < RMAX) sh.rg[pos] = g;
-        atomicOr(&sh.bitmap[g >> 5], 1u << (g & 31));
+    auto mark = [&](int g) {
+      const uint32_t pos = atomicAdd(&sh.nref, 1u);
+      if (pos < RMAX) sh.rg[pos] = g;
+      atomicOr(&sh.bitmap[g >> 5], 1u << (g & 31));
+    };
+    if (cached) {
+#pragma unroll
+      for (int q = 0; q < PER_THREAD; ++q) {
+        const int g = threadIdx.x + q * SEL_THREADS;
+        if (g < n_groups && fkey(tmp[q].m3) >= tau) mark(g);
       }
+    } else {
+      for (int g = threadIdx.x; g < n_groups; g += blockDim.x)
+        if (fkey(src[g].m3) >= tau) mark(g);
     }
     __syncthreads();
     const int nref = (int)sh.nref;
@@ -355,6 +534,55 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
     if (nref <= RMAX) {
       for (int i = 0; i < nref; ++i)
         score_group(sh.t, V, r, vocab, sh.rg[i], sh.rs + i * GROUP, reinterpret_cast<float*>(sh.hist));
+      // Candidates: the K selected pool entries outside the refined groups (sh.sk/si still hold the
+      // selection) and the refined groups' members at or above tau.  Every entry of the exact top-K
+      // is among them; when they number at least K (always, unless re-scoring moved a selected
+      // score below tau by rounding) the top K by rank counting is the result.
+      uint32_t* ck = sh.hist;
+      uint32_t* ci = sh.hist + HIST_BINS / 2;
+      if (threadIdx.x == 0) sh.cnt = 0;
+      __syncthreads();
+      for (int k0 = 0; k0 < K; k0 += blockDim.x) {
+        const int k = k0 + threadIdx.x;
+        bool take = false;
+        if (k < K) {
+          const uint32_t g = sh.si[k] / GROUP;
+          take = !((sh.bitmap[g >> 5] >> (g & 31)) & 1u);
+        }
+        const uint32_t pos = warp_append(take, &sh.cnt);
+        if (take) {
+          ck[pos] = sh.sk[k];
+          ci[pos] = sh.si[k];
+        }
+      }
+      for (int e0 = 0; e0 < nref * GROUP; e0 += blockDim.x) {
+        const int e = e0 + threadIdx.x;
+        bool take = false;
+        uint32_t key = 0;
+        int c = 0;
+        if (e < nref * GROUP) {
+          c = sh.rg[e / GROUP] * GROUP + (e % GROUP);
+          key = fkey(sh.rs[e]);
+          take = c < vocab && key >= tau;
+        }
+        const uint32_t pos = warp_append(take, &sh.cnt);
+        if (take && pos < HIST_BINS / 2) { ck[pos] = key; ci[pos] = (uint32_t)c; }
+      }
+      __syncthreads();
+      const int n = (int)sh.cnt;
+      __syncthreads();
+      if (n >= K && n <= HIST_BINS / 2) {
+        for (int i = threadIdx.x; i < n; i += blockDim.x) {
+          const uint32_t ki = ck[i], ii = ci[i];
+          int rank = 0;
+          for (int j = 0; j < n; ++j) rank += key_before(ck[j], ci[j], ki, ii) ? 1 : 0;
+          if (rank < K) {
+            idx_out[rank] = (int32_t)ii;
+            score_out[rank] = fkey_inv(ki);
+          }
+        }
+        return;
+      }
       auto refined = [&](auto f) {
         pool(f);  // skips the refined groups (bitmap)
         for (int e = threadIdx.x; e < nref * GROUP; e += blockDim.x) {

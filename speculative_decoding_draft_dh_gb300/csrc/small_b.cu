@@ -7,18 +7,26 @@
 // scores them.  At batch 1 the whole call moves about 40 MB (V dominates), so its cost is HBM time
 // plus every serial dependency: h U must finish before t V, and the global top-K before rescoring.
 //
-// k_proj_small (grid: two blocks per SM, each a slice of d): loads its slice of U (and h), signals
-//   its dependents may launch, multiplies, and adds its partial t into one of eight 64-bit
-//   fixed-point accumulators (scale 2^32) with integer atomics, which are exact and order
-//   independent, so t is deterministic; eight copies keep the same-address atomics per element
-//   low.  The last block to finish sums the copies into t in the activation dtype and clears them.
-// k_scores_small (one block per SM, 16 warps): issues the TMA loads of its first six 32 KB stages
-//   of V before waiting for the projection (V does not depend on t), then streams its run of
-//   256-id tiles in sets of four: a stage is four boxes of 256 ids x 16 bf16 rows (8 fp32 rows),
-//   2 KB contiguous per V row.  Warp w folds the 64 scores of group w of the set into its record;
-//   a block barrier per stage frees the stage's slot for the next TMA load.
-// k_select (select.cu) then picks the exact top-K per row from the records.
-// Every TMA wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word.
+// k_proj_small (grid: two blocks per SM, each a slice of d): waits for the previous kernel (h may
+//   come from it), loads its slice of U (and h), signals its dependents may launch, multiplies, and
+//   adds its partial t into one of eight 64-bit fixed-point accumulator copies (scale 2^32) with
+//   integer atomics, which are exact and order independent, so t is deterministic.  There is no
+//   final pass: the readers of t sum the copies themselves (acc_to_t).
+// k_scores_lsu (default; r a multiple of 64; one 4-warp block per 256-id tile, all blocks resident):
+//   before waiting for the projection, each warp puts up to 32 of its V rows on chip, 16 in
+//   registers and 16 bulk-copied into shared memory (cp.async.bulk on an mbarrier), so at r = 128
+//   the whole of V is in flight while t is computed.  After the wait it derives t from the
+//   accumulators, multiplies, adds the four warps' partial sums in a fixed order and folds each
+//   group of 64 ids into its record.  Rows beyond 32 per warp stream through registers.
+// k_scores_small (TMA variant for other r; one block per SM, 16 warps): issues the TMA loads of its
+//   first six 32 KB stages of V before waiting for the projection, then streams its run of 256-id
+//   tiles in sets of four: a stage is four boxes of 256 ids x 16 bf16 rows (8 fp32 rows), 2 KB
+//   contiguous per V row.  Warp w folds the 64 scores of group w of the set into its record; a
+//   block barrier per stage frees the stage's slot for the next TMA load.
+// k_select (select.cu) then picks the exact top-K per row from the records, deriving t from the
+// accumulators for its refinement step, and clears the accumulators for the next call.
+// Every TMA or bulk-copy wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status
+// word.
 #include <cstdlib>
 #include <cstring>
 
@@ -36,14 +44,13 @@ constexpr int SET_TILES = 4;        // tiles streamed together (16 warps x 64 id
 constexpr int NS = 6;               // stages in flight
 constexpr int STAGE_BYTES = 32768;  // SET_TILES boxes of 256 ids x (32 KB / 4 / 256 / sizeof(T)) rows
 constexpr int MAX_B = 8;
-constexpr int MAX_BR = 2048;        // B * r values of t
+constexpr int MAX_BR = ACC_MAX_BR;  // B * r values of t
 constexpr int PJ_THREADS = 256;
 constexpr int PJ_GROUPS = 4;        // row groups per block in the projection (reduced in smem)
 constexpr int CH = 12;              // projection rows per thread in one batch of loads
 constexpr uint64_t WAIT_NS = 2000000000ull;
 constexpr size_t STAGE_REGION = (size_t)NS * STAGE_BYTES;
 constexpr float FIX_SCALE = 4294967296.0f;  // 2^32
-constexpr int NCOPY = 8;                    // accumulator copies (block c adds into copy c % NCOPY)
 
 // Two adjacent values of row-major storage as floats (4-byte load for bf16, 8-byte for fp32).
 template <typename T>
@@ -65,16 +72,12 @@ struct ProjSmall {
   const void* h;
   const void* U;
   int B, d, r;
-  unsigned long long* acc;  // [NCOPY][B*r] fixed-point accumulators (zero between calls)
-  unsigned int* ticket;     // blocks finished (zero between calls)
-  void* t_out;              // [B][r] in the activation dtype
+  unsigned long long* acc;  // [ACC_COPIES][B*r] fixed-point accumulators (zero between calls)
 };
 
 template <typename T>
 __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
-  __shared__ float sh_h[MAX_B * PJ_GROUPS * CH];
   __shared__ float red[PJ_GROUPS][MAX_BR / 4];  // per-group partials of this block's (b, j) chunk
-  __shared__ int s_last;
   const T* h = static_cast<const T*>(p.h);
   const T* U = static_cast<const T*>(p.U);
   const int B = p.B, r = p.r, BR = B * r, npairs = r / 2;
@@ -86,6 +89,8 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
   const int per_grp = (rows + PJ_GROUPS - 1) / PJ_GROUPS;
   const int g0 = i0 + grp * per_grp, g1 = min(i1, g0 + per_grp);
   bool triggered = false;
+  // launched with programmatic dependent launch: h may come from the kernel before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // work items: (b, column pair), PJ_THREADS / PJ_GROUPS per pass
   for (int w0 = 0; w0 < B * npairs; w0 += PJ_THREADS / PJ_GROUPS) {
     const int w = w0 + lt;
@@ -130,30 +135,16 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
 #pragma unroll
         for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][threadIdx.x];
         const long long fx = __float2ll_rn(v * FIX_SCALE);
-        atomicAdd(p.acc + (size_t)(c % NCOPY) * BR + e, (unsigned long long)fx);
+        atomicAdd(p.acc + (size_t)(c % ACC_COPIES) * BR + e, (unsigned long long)fx);
       }
     }
     __syncthreads();
   }
   if (!triggered) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  // the last block converts the accumulator to t and clears it
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) s_last = atomicAdd(p.ticket, 1u) == (unsigned)(G - 1);
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  for (int e = threadIdx.x; e < BR; e += blockDim.x) {
-    long long fx = 0;
-#pragma unroll
-    for (int q = 0; q < NCOPY; ++q) fx += (long long)atomicExch(p.acc + (size_t)q * BR + e, 0ull);
-    static_cast<T*>(p.t_out)[e] = Elem<T>::from_f((float)((double)fx * (1.0 / 4294967296.0)));
-  }
-  if (threadIdx.x == 0) *p.ticket = 0u;
 }
 
 struct ScoresSmall {
-  const void* t;  // [B][r] activation dtype
+  const unsigned long long* acc;  // the projection's accumulators: t = acc_to_t(acc, B*r, e)
   int B, r, vocab, n_groups, n_tiles;
   GroupRec* recs;
   int* status;
@@ -173,7 +164,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
                                                            ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
-  const int B = p.B, r = p.r, BR = p.B * p.r;
+  const int r = p.r, BR = p.B * p.r;
   const int bands = r / RB;  // stages per tile set
   const int t0 = (int)((long long)p.n_tiles * c / G), t1 = (int)((long long)p.n_tiles * (c + 1) / G);
   const int n_sets = (t1 - t0 + SET_TILES - 1) / SET_TILES;
@@ -206,7 +197,7 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
     for (int q = 0; q < NS && q < total_stages; ++q) issue(q);
   }
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = Elem<T>::to_f(static_cast<const T*>(p.t)[e]);
+  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = acc_to_t<T>(p.acc, BR, e);
   __syncthreads();
 
   {
@@ -303,60 +294,104 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// LSU variant of the scores kernel: one block per 256-id tile, four warps splitting the rank
-// dimension (warp w takes rows [w r/4, (w+1) r/4)).  Lane i owns ids 8i..8i+7 of the tile (one
-// 16-byte vector per row).  Each warp loads its first LSU_BATCH rows into registers before
-// waiting for the projection, so about half of V is already in flight when t arrives; the rest
-// streams in batches of LSU_BATCH rows.  The four warps' partial sums are added in a fixed order
-// through shared memory, then warp g folds group g of the tile into its record.
+// LSU variant of the scores kernel: one block per 256-id tile (bf16; 128 ids for fp32), four warps
+// splitting the rank dimension (warp w takes rows [w r/4, (w+1) r/4)).  Lane i owns ids
+// PER*i .. PER*i + PER-1 of the tile, one 16-byte vector per row.  Before waiting for the
+// projection each warp puts its first LSU_BATCH rows into registers and bulk-copies the next
+// LSU_SROWS rows (one contiguous segment of the tile per row) into shared memory; rows beyond
+// those stream through registers after the wait.  The four warps' partial sums are added in a
+// fixed order through shared memory (aliasing the staged rows), then warp g folds group g of the
+// tile into its record.
 constexpr int LSU_WARPS = 4;
-constexpr int LSU_BATCH = 16;
+constexpr int LSU_BATCH = 16;  // rows per warp in registers
+constexpr int LSU_SROWS = 16;  // rows per warp staged in shared memory
+constexpr int LSU_SEG = 512;   // bytes of one row segment of a tile (32 lanes x 16 bytes)
 
 template <typename T, int NB>
 __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restrict__ V, ScoresSmall p) {
   constexpr int PER = Elem<T>::PER16;   // ids per lane (8 bf16 / 4 fp32)
   constexpr int TW = 32 * PER;          // ids per block tile
-  __shared__ float part[LSU_WARPS][NB][TW];
+  static_assert(TW * (int)sizeof(T) == LSU_SEG, "a tile row is one 512-byte segment");
+  static_assert(LSU_WARPS * NB * TW * 4 <= LSU_WARPS * LSU_SROWS * LSU_SEG, "partial sums fit the staging area");
+  __shared__ __align__(128) unsigned char vs[LSU_WARPS][LSU_SROWS][LSU_SEG];
   __shared__ float st[MAX_BR];
+  __shared__ uint64_t vbar[LSU_WARPS];
+  __shared__ int s_fail;
+  float(*part)[NB][TW] = reinterpret_cast<float(*)[NB][TW]>(&vs[0][0][0]);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = p.B, r = p.r;
-  const int c0 = blockIdx.x * TW + lane * PER;
+  const int B = p.B, r = p.r, BR = B * r;
+  const int tile0 = blockIdx.x * TW;
+  const int c0 = tile0 + lane * PER;
   const bool valid = c0 < p.vocab;  // vocab is a multiple of PER
   const int rq = r / LSU_WARPS;     // rows per warp (r is a multiple of 64 on this path)
   const int j0 = warp * rq;
+  const int nreg = min(LSU_BATCH, rq);
+  const int nsm = min(LSU_SROWS, rq - nreg);
   const T* vp = V + (valid ? c0 : 0);
   uint4 raw[LSU_BATCH];
 #pragma unroll
   for (int q = 0; q < LSU_BATCH; ++q)
-    raw[q] = (valid && q < rq) ? ld_nc_v4(vp + (size_t)(j0 + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+    raw[q] = (valid && q < nreg) ? ld_nc_v4(vp + (size_t)(j0 + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+  if (threadIdx.x == 0) s_fail = 0;
+  // staged rows: lane 0 of each warp bulk-copies them on the warp's own mbarrier
+  const uint32_t seg_bytes = (uint32_t)(min(TW, p.vocab - tile0) * (int)sizeof(T));  // multiple of 16
+  if (lane == 0) {
+    sm100::mbar_init(&vbar[warp], 1);
+    sm100::fence_barrier_init();
+    if (nsm > 0) {
+      sm100::mbar_arrive_expect_tx(&vbar[warp], (uint32_t)nsm * seg_bytes);
+      for (int i = 0; i < nsm; ++i)
+        sm100::bulk_load(&vs[warp][i][0], V + (size_t)(j0 + nreg + i) * p.vocab + tile0, seg_bytes, &vbar[warp]);
+    }
+  }
+  __syncwarp();
   asm volatile("griddepcontrol.wait;" ::: "memory");  // t comes from the projection kernel
-  for (int e = threadIdx.x; e < B * r; e += blockDim.x) st[e] = Elem<T>::to_f(static_cast<const T*>(p.t)[e]);
+  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = acc_to_t<T>(p.acc, BR, e);
   __syncthreads();
   float acc[NB][PER];
 #pragma unroll
   for (int b = 0; b < NB; ++b)
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[b][e] = 0.f;
-  for (int jb = 0; jb < rq; jb += LSU_BATCH) {
-    if (jb > 0) {
+  auto fma_row = [&](const uint4& u, int j) {
+    float x[PER];
+    Elem<T>::unpack(u, x);
 #pragma unroll
-      for (int q = 0; q < LSU_BATCH; ++q)
-        raw[q] = (valid && jb + q < rq) ? ld_nc_v4(vp + (size_t)(j0 + jb + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+    for (int b = 0; b < NB; ++b) {
+      const float tb = st[b * r + j];
+#pragma unroll
+      for (int e = 0; e < PER; ++e) acc[b][e] = fmaf(tb, x[e], acc[b][e]);
     }
+  };
 #pragma unroll
-    for (int q = 0; q < LSU_BATCH; ++q) {
-      if (jb + q < rq) {
-        float x[PER];
-        Elem<T>::unpack(raw[q], x);
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float tb = st[b * r + j0 + jb + q];
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc[b][e] = fmaf(tb, x[e], acc[b][e]);
-        }
+  for (int q = 0; q < LSU_BATCH; ++q)
+    if (q < nreg) fma_row(raw[q], j0 + q);
+  bool ok = true;
+  if (nsm > 0) {
+    // warp-uniform outcome of the bounded wait
+    ok = __all_sync(0xFFFFFFFFu, sm100::mbar_wait(&vbar[warp], 0, WAIT_NS));
+    if (!ok) {
+      if (lane == 0) {
+        atomicOr(p.status, 1 << DH_ERR_TIMEOUT);
+        s_fail = 1;
+        sm100::mbar_wait(&vbar[warp], 0, WAIT_NS);  // let the copies land before the block moves on
       }
+      __syncwarp();
+    } else if (valid) {
+      for (int i = 0; i < nsm; ++i)
+        fma_row(*reinterpret_cast<const uint4*>(&vs[warp][i][lane * 16]), j0 + nreg + i);
     }
   }
+  for (int jb = nreg + nsm; jb < rq; jb += LSU_BATCH) {
+#pragma unroll
+    for (int q = 0; q < LSU_BATCH; ++q)
+      raw[q] = (valid && jb + q < rq) ? ld_nc_v4(vp + (size_t)(j0 + jb + q) * p.vocab) : make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int q = 0; q < LSU_BATCH; ++q)
+      if (jb + q < rq) fma_row(raw[q], j0 + jb + q);
+  }
+  __syncthreads();  // every warp is done with the staged rows: the partial sums reuse the area
+  const bool write = s_fail == 0;
 #pragma unroll
   for (int b = 0; b < NB; ++b)
 #pragma unroll
@@ -366,7 +401,7 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
   constexpr int GROUPS = TW / GROUP;
   for (int g = warp; g < GROUPS; g += LSU_WARPS) {
     const int col = g * GROUP + 2 * lane;
-    const uint32_t id0 = (uint32_t)(blockIdx.x * TW + col);
+    const uint32_t id0 = (uint32_t)(tile0 + col);
     const int gg = (int)(id0 / GROUP);
 #pragma unroll
     for (int b = 0; b < NB; ++b) {
@@ -382,7 +417,7 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
       if ((int)id0 + 1 < p.vocab) sm.push(s1, id0 + 1);
 #pragma unroll
       for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
-      if (lane == 0 && gg < p.n_groups) p.recs[(size_t)b * p.n_groups + gg] = sm.record((uint32_t)gg * GROUP);
+      if (lane == 0 && gg < p.n_groups && write) p.recs[(size_t)b * p.n_groups + gg] = sm.record((uint32_t)gg * GROUP);
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -398,7 +433,7 @@ cudaError_t launch_tma(const Ctx& c, cudaLaunchConfig_t& cfg, const CUtensorMap&
 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
-                void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs, int* status) {
+                unsigned long long* acc, GroupRec* recs, int* status) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
   cudaError_t e = cudaSuccess;
   EncodeTiledFn fn = encode_fn();
@@ -423,9 +458,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   pp.B = B;
   pp.d = d;
   pp.r = r;
-  pp.acc = static_cast<unsigned long long*>(ws_fix);
-  pp.ticket = ticket;
-  pp.t_out = t_out;
+  pp.acc = acc;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)max(1, min(2 * c.num_sms, d / 4)));
   cfg.blockDim = dim3(PJ_THREADS);
@@ -438,7 +471,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_proj_small)");
 
   ScoresSmall sp;
-  sp.t = t_out;
+  sp.acc = acc;
   sp.B = B;
   sp.r = r;
   sp.vocab = vocab;
@@ -489,10 +522,9 @@ bool small_b_supported(int B, int r, int dtype) {
 }
 
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int dtype, void* ws_fix, unsigned int* ticket, void* t_out, GroupRec* recs,
-                           int* status) {
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, U, V, B, d, r, vocab, ws_fix, ticket, t_out, recs, status);
-  return run<float>(c, h, U, V, B, d, r, vocab, ws_fix, ticket, t_out, recs, status);
+                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, int* status) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, U, V, B, d, r, vocab, acc, recs, status);
+  return run<float>(c, h, U, V, B, d, r, vocab, acc, recs, status);
 }
 
 }  // namespace dh
