@@ -51,6 +51,9 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree"])
+    ap.add_argument("--api", default="head", choices=["head", "split"],
+                    help="head: dh_draft_head (both stages in one call); split: dh_lowrank_topk + "
+                         "dh_exact_rescore")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -205,6 +208,7 @@ KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
                 "rescore": ["rescore.cu", "dh_internal.cuh"],
                 "rescore_ring": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
                 "rescore_cluster": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
+                "head_cluster": ["head_cl.cu", "select.cuh", "dh_internal.cuh"],
                 "proj_partial": ["proj.cu", "dh_internal.cuh"],
                 "tree_argmax": ["tree.cu", "dh_internal.cuh"]}
 
@@ -232,6 +236,8 @@ def kernel_algo(cfg, name):
         return "tensor", 2.0 * cfg.B * cfg.d * cfg.r, "TFLOP/s"
     if name == "proj_partial":
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
+    if name == "head_cluster":  # records read once, the candidates' W rows, h
+        return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16 + cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name in ("rescore", "rescore_ring", "rescore_cluster"):
         return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name == "select":
@@ -257,11 +263,16 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
 
-    def step(x):
-        dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, idx_out=x["idx"], score_out=x["score"],
-                        workspace=ws)
-        dh.exact_rescore(x["h"], x["W"], x["idx"], logits_out=x["logits"], probs_out=x["probs"],
-                         workspace=ws)
+    def step(x, idx=None, logits=None, probs=None):
+        idx = x["idx"] if idx is None else idx
+        logits = x["logits"] if logits is None else logits
+        probs = x["probs"] if probs is None else probs
+        if a.api == "head":
+            dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K, idx_out=idx, score_out=x["score"],
+                          logits_out=logits, probs_out=probs, workspace=ws)
+        else:
+            dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, idx_out=idx, score_out=x["score"], workspace=ws)
+            dh.exact_rescore(x["h"], x["W"], idx, logits_out=logits, probs_out=probs, workspace=ws)
 
     with torch.cuda.stream(stream):
         for i in range(a.warmup):
@@ -357,18 +368,21 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     if not a.no_e2e:
         n_e2e = min(a.steps, 2000 if cfg.B <= 64 else 100)
         hosts = [x["h"].cpu().pin_memory() for x in sets]
-        outs = [(torch.empty(cfg.B, cfg.K, dtype=torch.int32).pin_memory(),
-                 torch.empty(cfg.B, cfg.K, dtype=torch.float32).pin_memory(),
-                 torch.empty(cfg.B, cfg.K, dtype=torch.float32).pin_memory()) for _ in sets]
+        # the three outputs live in one device buffer (idx, logits, probs as int32 / fp32 views),
+        # so one device-to-host copy returns a step's results
+        BK = cfg.B * cfg.K
+        packed = [torch.empty(3 * BK, dtype=torch.int32, device=dev) for _ in sets]
+        outs = [torch.empty(3 * BK, dtype=torch.int32).pin_memory() for _ in sets]
+        views = [(p[:BK].view(cfg.B, cfg.K), p[BK:2 * BK].view(torch.float32).view(cfg.B, cfg.K),
+                  p[2 * BK:].view(torch.float32).view(cfg.B, cfg.K)) for p in packed]
         def e2e_step(i):
-            x = sets[i % copies]
+            j = i % copies
+            x = sets[j]
+            idx, logits, probs = views[j]
             with torch.cuda.stream(stream):
-                x["h"].copy_(hosts[i % copies], non_blocking=True)
-                step(x)
-                o = outs[i % copies]
-                o[0].copy_(x["idx"], non_blocking=True)
-                o[1].copy_(x["logits"], non_blocking=True)
-                o[2].copy_(x["probs"], non_blocking=True)
+                x["h"].copy_(hosts[j], non_blocking=True)
+                step(x, idx, logits, probs)
+                outs[j].copy_(packed[j], non_blocking=True)
             stream.synchronize()
         for i in range(3):
             e2e_step(i)
@@ -392,7 +406,8 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
         "us_per_call": round(us_per_call, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generators, random weights)",
         "config": {"workload": cfg.name, "B": cfg.B, "d": cfg.d, "vocab": cfg.vocab, "r": cfg.r,
-                   "K": cfg.K, "seed": a.seed, "graph": f"CUDA graphs of {S} steps",
+                   "K": cfg.K, "seed": a.seed, "api": "dh_draft_head" if a.api == "head" else
+                   "dh_lowrank_topk + dh_exact_rescore", "graph": f"CUDA graphs of {S} steps",
                    "l2": f"inputs rotate over {copies} independent copies "
                          f"({copies * per_step / 2**20:.0f} MiB per cycle > 2x L2)",
                    "parallelism": f"replicas x{world} (rows independent)"},
@@ -615,8 +630,11 @@ def profile_run(a):
         cfg = inputs.HEAD_CONFIGS[a.workload]
         x = inputs.make_head(cfg, seed=a.seed, device=dev)
         for _ in range(a.warmup + a.steps):
-            idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
-            dh.exact_rescore(x["h"], x["W"], idx)
+            if a.api == "head":
+                dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K)
+            else:
+                idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+                dh.exact_rescore(x["h"], x["W"], idx)
     torch.cuda.synchronize()
     print(json.dumps({"profile_run": a.workload, "steps": a.warmup + a.steps}), flush=True)
 

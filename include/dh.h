@@ -115,6 +115,26 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
                      size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Both stages in one call: dh_lowrank_topk followed by dh_exact_rescore on its candidates.
+ *
+ * EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
+ * the two stages of the draft head, the low-rank retrieval of K candidates and their exact
+ * rescoring, computed as one head.  Outputs and their meaning are exactly those of the two calls:
+ * idx_out / score_out as dh_lowrank_topk, logits_out / probs_out as dh_exact_rescore (probs_out
+ * may be NULL).  h [B x d], U [d x r], V [r x vocab], W [vocab x d]: device, `dtype`, 16-byte
+ * aligned, with d, r and vocab rows a multiple of 16 bytes; d <= 8192; limits and error codes as
+ * for the two calls.  For small batches the selection and the rescoring run as one kernel (a
+ * thread-block cluster per row), which removes a kernel boundary from the critical path.
+ * The workspace (dh_draft_head_workspace bytes, 256-byte aligned, caller-owned) must be zero-filled
+ * before its first use and not shared by calls that overlap in time; the library leaves it ready
+ * for the next call.
+ * ------------------------------------------------------------------------------------------- */
+size_t dh_draft_head_workspace(int B, int d, int r, int vocab, int K, int dtype);
+int dh_draft_head(const void* h, const void* U, const void* V, const void* W, int B, int d, int r, int vocab,
+                  int K, int dtype, int32_t* idx_out, float* score_out, float* logits_out, float* probs_out,
+                  void* workspace, size_t ws_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Greedy draft-tree acceptance.
  *
  * daily.dev "EAGLE-4 speeds up LLM inference ...", section "How it works"; EAGLE-4 summary page,

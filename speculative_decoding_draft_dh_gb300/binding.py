@@ -21,7 +21,8 @@ STATUS = {0: "DH_OK", 1: "DH_ERR_INVALID_ARG", 2: "DH_ERR_UNSUPPORTED", 3: "DH_E
 F32, BF16 = 0, 1
 
 EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
-           "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_tree_accept_workspace",
+           "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_draft_head_workspace", "dh_draft_head",
+           "dh_tree_accept_workspace",
            "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
 
 _lib = None
@@ -59,6 +60,10 @@ def load_library(path: str | None = None):
         lib.dh_exact_rescore_workspace.restype = Z
         lib.dh_exact_rescore.argtypes = [P, P, P, I, I, I, I, I, P, P, P, Z, P]
         lib.dh_exact_rescore.restype = I
+        lib.dh_draft_head_workspace.argtypes = [I, I, I, I, I, I]
+        lib.dh_draft_head_workspace.restype = Z
+        lib.dh_draft_head.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, Z, P]
+        lib.dh_draft_head.restype = I
         lib.dh_tree_accept_workspace.argtypes = [I, I, I]
         lib.dh_tree_accept_workspace.restype = Z
         lib.dh_tree_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
@@ -173,6 +178,35 @@ def exact_rescore(h, W, idx, *, with_probs=True, logits_out=None, probs_out=None
                                 _ptr(probs_out if with_probs else None), _ptr(ws), nbytes,
                                 _stream(stream)), "dh_exact_rescore")
     return logits_out, (probs_out if with_probs else None)
+
+
+def draft_head(h, U, V, W, K, *, with_probs=True, idx_out=None, score_out=None, logits_out=None,
+               probs_out=None, workspace=None, stream=None):
+    """Both stages in one call.  Returns (idx int32 [B,K], score fp32 [B,K], logits fp32 [B,K],
+    probs fp32 [B,K] or None)."""
+    lib = load_library()
+    _dev(h, "h"), _dev(U, "U"), _dev(V, "V"), _dev(W, "W")
+    B, d = h.shape
+    r, vocab = V.shape
+    dt = _dtype_code(h)
+    if U.dtype != h.dtype or V.dtype != h.dtype or W.dtype != h.dtype or U.shape != (d, r) \
+            or W.shape != (vocab, d):
+        raise ValueError("h, U, V, W must share a dtype and have shapes [B,d], [d,r], [r,vocab], [vocab,d]")
+    dev = h.device
+    if idx_out is None:
+        idx_out = torch.empty(B, K, dtype=torch.int32, device=dev)
+    if score_out is None:
+        score_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    if logits_out is None:
+        logits_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    if with_probs and probs_out is None:
+        probs_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    nbytes = lib.dh_draft_head_workspace(B, d, r, vocab, K, dt)
+    ws = (workspace or _default_ws).get(nbytes, dev, "head")
+    _check(lib.dh_draft_head(_ptr(h), _ptr(U), _ptr(V), _ptr(W), B, d, r, vocab, K, dt, _ptr(idx_out),
+                             _ptr(score_out), _ptr(logits_out), _ptr(probs_out if with_probs else None),
+                             _ptr(ws), nbytes, _stream(stream)), "dh_draft_head")
+    return idx_out, score_out, logits_out, (probs_out if with_probs else None)
 
 
 def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stream=None):

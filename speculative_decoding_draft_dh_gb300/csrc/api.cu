@@ -3,6 +3,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <algorithm>
+#include <atomic>
 #include <mutex>
 #include <string>
 #include <vector>
@@ -79,7 +80,7 @@ struct ProfRec {
   cudaEvent_t a, b;
 };
 std::mutex g_prof_mu;
-bool g_prof = false;
+std::atomic<bool> g_prof{false};
 std::vector<ProfRec> g_prof_recs;
 
 }  // namespace
@@ -152,27 +153,11 @@ const char* dh_last_error(void) { return g_last_error; }
 
 // ------------------------------------------------------------------ stage 1
 
-size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int /*K*/, int /*dtype*/) {
-  if (B <= 0 || d <= 0 || r <= 0 || vocab <= 0) return 0;
-  return topk_layout(B, d, r, vocab).total;
-}
+namespace {
 
-int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
-                    int dtype, int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
-                    void* stream) {
-  if (B < 0 || d <= 0 || r <= 0 || vocab <= 0) return DH_ERR_INVALID_ARG;
-  if (K < 1 || K > vocab || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
-  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
-  if (B == 0) return DH_OK;
-  if (!h || !U || !V || !idx_out || !score_out) return DH_ERR_INVALID_ARG;
-  if (r > DH_MAX_RANK || vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
-  if (!aligned16(h) || !aligned16(U) || !aligned16(V)) return DH_ERR_UNSUPPORTED;
-  if (!row16(d, dtype) || !row16(r, dtype) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
-  const TopkLayout L = topk_layout(B, d, r, vocab);
-  if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return DH_ERR_WORKSPACE;
-  Ctx c;
-  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
-  char* ws = static_cast<char*>(workspace);
+// Stage 1 after validation: projection, scores with group summaries, selection.
+int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
+             int dtype, int32_t* idx_out, float* score_out, char* ws, const TopkLayout& L) {
   void* t = ws + L.t;
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
@@ -205,6 +190,48 @@ int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, i
   return DH_OK;
 }
 
+// Stage 2 after validation: the ring kernel from 2048 pairs, the direct kernels below.
+// DH_FORCE_RESCORE=direct|ring overrides the choice by batch size (tests and tuning).
+int run_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                int dtype, float* logits_out, float* probs_out, uint32_t* tickets, int* status) {
+  const char* f = std::getenv("DH_FORCE_RESCORE");
+  const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
+  bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
+  if (f && std::strcmp(f, "direct") == 0) ring = false;
+  if (f && std::strcmp(f, "ring") == 0) ring = ring_ok;
+  const cudaError_t e =
+      ring ? note_error(launch_rescore_ring(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
+                                            status),
+                        "rescore (ring)")
+           : note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
+  return e == cudaSuccess ? DH_OK : DH_ERR_CUDA;
+}
+
+}  // namespace
+
+size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int /*K*/, int /*dtype*/) {
+  if (B <= 0 || d <= 0 || r <= 0 || vocab <= 0) return 0;
+  return topk_layout(B, d, r, vocab).total;
+}
+
+int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
+                    int dtype, int32_t* idx_out, float* score_out, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  if (B < 0 || d <= 0 || r <= 0 || vocab <= 0) return DH_ERR_INVALID_ARG;
+  if (K < 1 || K > vocab || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!h || !U || !V || !idx_out || !score_out) return DH_ERR_INVALID_ARG;
+  if (r > DH_MAX_RANK || vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(U) || !aligned16(V)) return DH_ERR_UNSUPPORTED;
+  if (!row16(d, dtype) || !row16(r, dtype) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
+  const TopkLayout L = topk_layout(B, d, r, vocab);
+  if (!workspace || !aligned256(workspace) || ws_bytes < L.total) return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  return run_topk(c, h, U, V, B, d, r, vocab, K, dtype, idx_out, score_out, static_cast<char*>(workspace), L);
+}
+
 // ------------------------------------------------------------------ stage 2
 
 size_t dh_exact_rescore_workspace(int B, int, int, int K, int) {
@@ -227,19 +254,59 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   uint32_t* tickets = reinterpret_cast<uint32_t*>(static_cast<char*>(workspace) + WS_HEADER);
-  // DH_FORCE_RESCORE=direct|ring overrides the choice by batch size (tests and tuning)
-  const char* f = std::getenv("DH_FORCE_RESCORE");
-  const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
-  bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
-  if (f && std::strcmp(f, "direct") == 0) ring = false;
-  if (f && std::strcmp(f, "ring") == 0) ring = ring_ok;
-  const cudaError_t e =
-      ring ? note_error(launch_rescore_ring(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
-                                            static_cast<int*>(workspace)),
-                        "rescore (ring)")
-           : note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
-  if (e != cudaSuccess) return DH_ERR_CUDA;
-  return DH_OK;
+  return run_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
+                     static_cast<int*>(workspace));
+}
+
+// ------------------------------------------------------------------ both stages
+
+namespace {
+// Both stages' workspaces: stage 1's layout, then the rescoring tickets.
+size_t head_rescore_offset(int B, int d, int r, int vocab) { return align_up(topk_layout(B, d, r, vocab).total, 256); }
+}  // namespace
+
+size_t dh_draft_head_workspace(int B, int d, int r, int vocab, int K, int /*dtype*/) {
+  if (B <= 0 || d <= 0 || r <= 0 || vocab <= 0 || K <= 0) return 0;
+  return head_rescore_offset(B, d, r, vocab) + align_up((size_t)B * sizeof(uint32_t), 256);
+}
+
+int dh_draft_head(const void* h, const void* U, const void* V, const void* W, int B, int d, int r, int vocab,
+                  int K, int dtype, int32_t* idx_out, float* score_out, float* logits_out, float* probs_out,
+                  void* workspace, size_t ws_bytes, void* stream) {
+  if (B < 0 || d <= 0 || r <= 0 || vocab <= 0) return DH_ERR_INVALID_ARG;
+  if (K < 1 || K > vocab || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!h || !U || !V || !W || !idx_out || !score_out || !logits_out) return DH_ERR_INVALID_ARG;
+  if (r > DH_MAX_RANK || vocab > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(U) || !aligned16(V) || !aligned16(W)) return DH_ERR_UNSUPPORTED;
+  if (!row16(d, dtype) || !row16(r, dtype) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
+  if ((long long)B * K > 0x7FFFFFFFLL || !rescore_supported(d)) return DH_ERR_UNSUPPORTED;
+  const TopkLayout L = topk_layout(B, d, r, vocab);
+  const size_t roff = head_rescore_offset(B, d, r, vocab);
+  if (!workspace || !aligned256(workspace) || ws_bytes < dh_draft_head_workspace(B, d, r, vocab, K, dtype))
+    return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  // small batches: the scores kernels, then selection and rescoring in one cluster kernel
+  const char* f = std::getenv("DH_FORCE_HEAD");
+  const bool split = f && std::strcmp(f, "split") == 0;
+  if (!split && choose_path(B, r, dtype) == PATH_FUSED && head_cluster_supported(B, d, vocab, K, dtype)) {
+    unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
+    GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+      return DH_ERR_CUDA;
+    if (note_error(launch_head_cluster(c, recs, acc, V, h, W, B, d, r, vocab, K, dtype, idx_out, score_out,
+                                       logits_out, probs_out),
+                   "selection and rescoring (cluster)") != cudaSuccess)
+      return DH_ERR_CUDA;
+    return DH_OK;
+  }
+  const int st = run_topk(c, h, U, V, B, d, r, vocab, K, dtype, idx_out, score_out, ws, L);
+  if (st != DH_OK) return st;
+  return run_rescore(c, h, W, idx_out, B, d, vocab, K, dtype, logits_out, probs_out,
+                     reinterpret_cast<uint32_t*>(ws + roff), reinterpret_cast<int*>(ws));
 }
 
 // ------------------------------------------------------------------ tree acceptance

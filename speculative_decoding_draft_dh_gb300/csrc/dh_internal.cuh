@@ -195,6 +195,12 @@ cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, uns
                           const void* V, int B, int r, int vocab, int K, int dtype, int32_t* idx_out,
                           float* score_out);
 
+// Small batches: selection and rescoring in one thread-block cluster per row (head_cl.cu).
+bool head_cluster_supported(int B, int d, int vocab, int K, int dtype);
+cudaError_t launch_head_cluster(const Ctx& c, const GroupRec* recs, unsigned long long* acc, const void* V,
+                                const void* h, const void* W, int B, int d, int r, int vocab, int K, int dtype,
+                                int32_t* idx_out, float* score_out, float* logits, float* probs);
+
 bool rescore_supported(int d);
 bool rescore_ring_used(int B, int K, int d, int dtype);
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,

@@ -1,0 +1,416 @@
+// Small batches: selection and exact rescoring fused into one kernel, one thread-block cluster of
+// HC_CTAS CTAs per row.
+//
+// EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
+// the K candidates of a row are its K best low-rank scores (score desc, id asc); their exact
+// logits come from the full-rank head, and the softmax runs over the K candidates.
+//
+// At batch 1 the selection is a short chain of dependent steps over about 4700 pool entries, and
+// each kernel boundary in the pipeline costs one to two microseconds.  Here the cluster's CTAs
+// split the row's group records (HC_RPT per thread) and select cooperatively through distributed
+// shared memory: the histograms, the candidate lists and the control words live in the leader
+// CTA (rank 0); the other CTAs reach them with remote atomics and loads.  The steps are those of
+// the register fast path of the selection kernel (radix levels over the pool's own key range,
+// compaction, ranking by counting), each ended by a cluster barrier.  The leader writes the sorted
+// candidates, every CTA then scores its share of them against h (staged in shared memory before
+// the wait on the previous kernel) and stores the logits into the leader, which computes the
+// softmax.  A row whose certificate finds groups to re-score, or whose pool is degenerate, is
+// selected again by the leader alone with the block selection (select_row: exact, with
+// refinement and full rescan) before the rescoring step.
+//
+// Cluster barriers are hardware barriers that every CTA passes unconditionally, so they always
+// complete.
+#include <cooperative_groups.h>
+
+#include "select.cuh"
+
+namespace dh {
+namespace {
+
+namespace cg = cooperative_groups;
+
+constexpr int HC_CTAS = 8;
+constexpr int HC_THREADS = 256;
+constexpr int HC_WARPS = HC_THREADS / 32;
+constexpr int HC_RPT = 2;                                      // group records per thread
+constexpr int HC_ENT = 2 * HC_RPT;                             // pool entries per thread
+constexpr int HC_MAX_GROUPS = HC_CTAS * HC_THREADS * HC_RPT;  // 4096 groups: vocab <= 262144
+constexpr int HC_MAX_K = 256;
+constexpr int HC_BINS = 256;
+constexpr int HC_BITS = 8;
+constexpr int HC_RANK = 64;    // a level whose boundary bin holds at most this many ends the descent
+constexpr int HC_BOUND = 512;  // largest boundary bin ranked by counting
+
+// Control block: every CTA has one; the leader's is the one in use.
+struct HeadCtl {
+  uint32_t hist[HC_BINS];
+  uint32_t kmin, kmax;
+  uint32_t digit, run, bincount, total;
+  uint32_t n_above, n_bound, nref, tau_key;
+  uint32_t wmin[HC_WARPS], wmax[HC_WARPS];
+  alignas(16) unsigned long long sp[HC_MAX_K];  // the K winners, packed key << 32 | ~id
+  alignas(16) unsigned long long bp[HC_BOUND];  // the boundary bin
+  float z[HC_MAX_K];                            // the row's logits
+};
+
+struct HeadParams {
+  const GroupRec* recs;     // [B][n_groups]
+  unsigned long long* acc;  // the projection's fixed-point accumulators (cleared here)
+  const void* V;
+  const void* h;
+  const void* W;
+  int B, d, r, vocab, K, n_groups;
+  int32_t* idx_out;
+  float* score_out;
+  float* logits;
+  float* probs;  // may be null
+};
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t id) {
+  return ((unsigned long long)key << 32) | (unsigned long long)(~id);
+}
+
+// Dynamic shared memory layout: control block, h, then the block selection's area (leader only).
+__host__ __device__ constexpr size_t hc_h_offset() { return align_up(sizeof(HeadCtl), 128); }
+__host__ __device__ constexpr size_t hc_fb_offset(int d, int elem) {
+  return hc_h_offset() + align_up((size_t)d * elem, 128);
+}
+
+template <typename T>
+__global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
+  constexpr int PER = Elem<T>::PER16;
+  extern __shared__ __align__(128) unsigned char smem[];
+  cg::cluster_group cl = cg::this_cluster();
+  const uint32_t crank = cl.block_rank();
+  const bool leader = crank == 0;
+  const int b = (int)(blockIdx.x / HC_CTAS);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K, n_groups = p.n_groups, BR = p.B * p.r;
+  HeadCtl& my = *reinterpret_cast<HeadCtl*>(smem);
+  HeadCtl& L = *cl.map_shared_rank(&my, 0u);
+  T* hs = reinterpret_cast<T*>(smem + hc_h_offset());
+  unsigned char* fb = smem + hc_fb_offset(p.d, (int)sizeof(T));
+  const GroupRec* rrow = p.recs + (size_t)b * n_groups;
+  unsigned long long* acc_row = p.acc + (size_t)b * p.r;
+
+  // zero this CTA's control block; the barrier's wait (below) makes the leader's visible
+  for (int i = threadIdx.x; i < HC_BINS; i += HC_THREADS) my.hist[i] = 0u;
+  if (threadIdx.x == 0) {
+    my.kmin = 0xFFFFFFFFu;
+    my.kmax = 0u;
+    my.n_above = my.n_bound = my.nref = 0u;
+  }
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // h does not depend on the previous kernels
+  const T* hrow = static_cast<const T*>(p.h) + (size_t)b * p.d;
+  for (int c = threadIdx.x * PER; c < p.d; c += HC_THREADS * PER)
+    *reinterpret_cast<uint4*>(hs + c) = __ldg(reinterpret_cast<const uint4*>(hrow + c));
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the scores kernel
+
+  // this CTA's slice of the row's groups
+  const int slice = (n_groups + HC_CTAS - 1) / HC_CTAS;
+  const int g0 = (int)crank * slice, g1 = min(n_groups, g0 + slice);
+  GroupRec rec[HC_RPT];
+  uint32_t key[HC_ENT], id[HC_ENT];
+#pragma unroll
+  for (int q = 0; q < HC_RPT; ++q) {
+    const int g = g0 + threadIdx.x + q * HC_THREADS;
+    key[2 * q] = key[2 * q + 1] = 0u;
+    id[2 * q] = id[2 * q + 1] = 0xFFFFFFFFu;
+    rec[q].m3 = -INFINITY;
+    if (g < g1) {
+      rec[q] = rrow[g];
+      const uint32_t o1 = rec[q].offs & 0xFFu, o2 = (rec[q].offs >> 8) & 0xFFu;
+      if (o1 != NO_OFFSET) { key[2 * q] = fkey(rec[q].m1); id[2 * q] = (uint32_t)g * GROUP + o1; }
+      if (o2 != NO_OFFSET) { key[2 * q + 1] = fkey(rec[q].m2); id[2 * q + 1] = (uint32_t)g * GROUP + o2; }
+    }
+  }
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < HC_ENT; ++q)
+    if (key[q]) { kmin = min(kmin, key[q]); kmax = max(kmax, key[q]); }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  if (lane == 0) { my.wmin[warp] = kmin; my.wmax[warp] = kmax; }
+  __syncthreads();
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");  // every control block is zeroed
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < HC_WARPS; ++w) { kmin = min(kmin, my.wmin[w]); kmax = max(kmax, my.wmax[w]); }
+    if (kmax) {
+      atomicMin(&L.kmin, kmin);
+      atomicMax(&L.kmax, kmax);
+    }
+  }
+  cluster_sync_all();
+  kmin = L.kmin;
+  kmax = L.kmax;
+
+  // ---------------------------------------------------------------- cooperative radix descent
+  bool fallback = kmax == 0u;  // empty pool
+  uint32_t prefix = 0, mask = 0, krem = (uint32_t)K, above = 0, bc = 0;
+  if (!fallback) {
+#pragma unroll
+    for (int q = 0; q < HC_ENT; ++q) key[q] = key[q] ? key[q] - kmin + 1u : 0u;  // y + 1 (0 = no entry)
+    const uint32_t range = kmax - kmin + 1u;
+    int shift = range >= 0x80000000u ? 32 - HC_BITS : max(0, (32 - __clz((int)range)) - HC_BITS);
+    const uint32_t dmask = (uint32_t)HC_BINS - 1u;
+    bool first = true;
+#pragma unroll 1
+    for (;;) {
+#pragma unroll
+      for (int q = 0; q < HC_ENT; ++q)
+        if (key[q] && (key[q] & mask) == prefix) atomicAdd(&L.hist[(key[q] >> shift) & dmask], 1u);
+      cluster_sync_all();
+      if (leader && warp == 0) {
+        // lane i owns bins 255 - 8i down to 248 - 8i; scan from the highest bin
+        uint32_t c[8], sum = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) { c[q] = my.hist[HC_BINS - 1 - 8 * lane - q]; sum += c[q]; }
+        uint32_t incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - sum;
+        if (first && lane == 31) my.total = incl;
+        if (excl < krem && krem <= incl) {
+          uint32_t run = excl;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            if (run + c[q] >= krem) {
+              my.digit = (uint32_t)(HC_BINS - 1 - 8 * lane - q); my.run = run; my.bincount = c[q];
+              break;
+            }
+            run += c[q];
+          }
+        }
+        if (lane == 31 && incl < krem) { my.digit = 0; my.run = incl; my.bincount = 0; }
+        __syncwarp();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) my.hist[8 * lane + q] = 0u;  // for the next level
+      }
+      cluster_sync_all();
+      const uint32_t D = L.digit, run = L.run, total = L.total;
+      bc = L.bincount;
+      if (first && total < (uint32_t)K) { fallback = true; break; }
+      first = false;
+      prefix |= D << shift;
+      mask |= dmask << shift;
+      krem -= run;
+      above += run;
+      if (bc <= (uint32_t)HC_RANK || shift == 0) break;
+      shift = max(0, shift - HC_BITS);
+    }
+    if (bc > (uint32_t)HC_BOUND) fallback = true;
+  }
+  // every CTA took the same decisions from the same leader values
+
+  if (!fallback) {
+    // compaction into the leader's lists (positions from warp ballots, one remote atomic per warp)
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int q = 0; q < HC_ENT; ++q) {
+      const uint32_t mk = key[q] & mask;
+      const bool up = key[q] && mk > prefix, bd = key[q] && mk == prefix;
+      const uint32_t bu = __ballot_sync(0xFFFFFFFFu, up), bb = __ballot_sync(0xFFFFFFFFu, bd);
+      uint32_t base_u = 0, base_b = 0;
+      if (lane == 0) {
+        if (bu) base_u = atomicAdd(&L.n_above, (uint32_t)__popc(bu));
+        if (bb) base_b = atomicAdd(&L.n_bound, (uint32_t)__popc(bb));
+      }
+      base_u = __shfl_sync(0xFFFFFFFFu, base_u, 0);
+      base_b = __shfl_sync(0xFFFFFFFFu, base_b, 0);
+      const uint32_t k0 = key[q] - 1u + kmin;
+      if (up) L.sp[base_u + __popc(bu & below)] = pack(k0, id[q]);
+      else if (bd) L.bp[base_b + __popc(bb & below)] = pack(k0, id[q]);
+    }
+    cluster_sync_all();
+    if (leader) {
+      // the boundary bin's best K - above, then every winner ranked by counting and written out
+      const int need = K - (int)above;
+      for (int i = threadIdx.x; i < (int)bc; i += HC_THREADS) {
+        const unsigned long long pi = my.bp[i];
+        int rank = 0;
+        for (int j = 0; j < (int)bc; ++j) rank += my.bp[j] > pi ? 1 : 0;
+        if (rank < need) my.sp[above + rank] = pi;
+      }
+      __syncthreads();
+      int P = 1;
+      while (P < 32 && K * (2 * P) <= HC_THREADS) P <<= 1;
+      const int per = (K + P - 1) / P;
+      for (int base = 0; base < K * P; base += HC_THREADS) {
+        const int t = base + (int)threadIdx.x;
+        const int i = t / P, hh = t % P;
+        int rank = 0;
+        unsigned long long pi = 0;
+        if (i < K) {
+          pi = my.sp[i];
+          const int j1 = min(K, (hh + 1) * per);
+          for (int j = hh * per; j < j1; ++j) rank += my.sp[j] > pi ? 1 : 0;
+        }
+        for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        if (i < K && hh == 0) {
+          const uint32_t kk = (uint32_t)(pi >> 32);
+          p.idx_out[(size_t)b * K + rank] = (int32_t)(~(uint32_t)pi);
+          p.score_out[(size_t)b * K + rank] = fkey_inv(kk);
+          if (rank == K - 1) my.tau_key = kk;
+        }
+      }
+    }
+    cluster_sync_all();
+    // certificate: a group whose third score reaches tau may hide a member of the top K
+    const uint32_t tau = L.tau_key;
+    bool mine = false;
+#pragma unroll
+    for (int q = 0; q < HC_RPT; ++q) mine |= fkey(rec[q].m3) >= tau && (g0 + (int)threadIdx.x + q * HC_THREADS) < g1;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0 && bm) atomicAdd(&L.nref, (uint32_t)__popc(bm));
+    cluster_sync_all();
+    fallback = L.nref != 0u;
+  }
+  if (fallback) {
+    // the leader selects the row alone: exact, with refinement or a full rescan as needed
+    if (leader)
+      sel::select_row<T, HC_THREADS>(fb, rrow, nullptr, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
+                                     p.idx_out + (size_t)b * K, p.score_out + (size_t)b * K);
+    cluster_sync_all();
+  } else if (leader) {
+    // zero the row's accumulators for the next call (select_row does it on the other branch)
+    for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
+#pragma unroll
+      for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+  }
+
+  // ---------------------------------------------------------------- exact logits and softmax
+  const int32_t* cand = p.idx_out + (size_t)b * K;
+  const T* W = static_cast<const T*>(p.W);
+  for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+    const int v = cand[k];
+    const bool ok = v >= 0 && v < p.vocab;
+    float acc = 0.f;
+    if (ok) {
+      const T* w = W + (size_t)v * p.d;
+      constexpr int MAXW = 20;
+      for (int c0 = 0; c0 < p.d; c0 += 32 * PER * MAXW) {
+        uint4 wa[MAXW];
+#pragma unroll
+        for (int q = 0; q < MAXW; ++q) {
+          const int c = c0 + (q * 32 + lane) * PER;
+          if (c < p.d) wa[q] = ld_nc_v4(w + c);
+        }
+#pragma unroll
+        for (int q = 0; q < MAXW; ++q) {
+          const int c = c0 + (q * 32 + lane) * PER;
+          if (c < p.d) {
+            float wf[PER], xf[PER];
+            Elem<T>::unpack(wa[q], wf);
+            Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
+#pragma unroll
+            for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    const float z = ok ? acc : __int_as_float(0x7FC00000);
+    if (lane == 0) {
+      p.logits[(size_t)b * K + k] = z;
+      L.z[k] = z;
+    }
+  }
+  cluster_sync_all();
+  if (!leader || !p.probs) return;
+  __shared__ float red[HC_WARPS];
+  __shared__ float s_bcast;
+  float m = -INFINITY;
+  for (int i = threadIdx.x; i < K; i += HC_THREADS) m = fmaxf(m, my.z[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  if (lane == 0) red[warp] = m;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float mm = red[0];
+    for (int i = 1; i < HC_WARPS; ++i) mm = fmaxf(mm, red[i]);
+    s_bcast = mm;
+  }
+  __syncthreads();
+  m = s_bcast;
+  float ssum = 0.f;
+  for (int i = threadIdx.x; i < K; i += HC_THREADS) ssum += expf(my.z[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+  __syncthreads();
+  if (lane == 0) red[warp] = ssum;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.f;
+    for (int i = 0; i < HC_WARPS; ++i) tot += red[i];
+    s_bcast = 1.f / tot;
+  }
+  __syncthreads();
+  const float inv = s_bcast;
+  for (int i = threadIdx.x; i < K; i += HC_THREADS) p.probs[(size_t)b * K + i] = expf(my.z[i] - m) * inv;
+}
+
+template <typename T>
+cudaError_t run(const Ctx& c, const HeadParams& p) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_head_cl<T>, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(p.B * HC_CTAS));
+  cfg.blockDim = dim3(HC_THREADS);
+  cfg.dynamicSmemBytes = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_before("head_cluster", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_head_cl<T>, p);
+  prof_after(c.stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
+  const int n_groups = (vocab + GROUP - 1) / GROUP;
+  const size_t smem = hc_fb_offset(d, dtype == DH_BF16 ? 2 : 4) + sel::select_smem_bytes(n_groups);
+  return B >= 1 && K <= HC_MAX_K && n_groups <= HC_MAX_GROUPS && n_groups <= sel::CACHE_GROUPS &&
+         d <= 8192 && smem <= 200 * 1024;
+}
+
+cudaError_t launch_head_cluster(const Ctx& c, const GroupRec* recs, unsigned long long* acc, const void* V,
+                                const void* h, const void* W, int B, int d, int r, int vocab, int K, int dtype,
+                                int32_t* idx_out, float* score_out, float* logits, float* probs) {
+  HeadParams p;
+  p.recs = recs;
+  p.acc = acc;
+  p.V = V;
+  p.h = h;
+  p.W = W;
+  p.B = B;
+  p.d = d;
+  p.r = r;
+  p.vocab = vocab;
+  p.K = K;
+  p.n_groups = (vocab + GROUP - 1) / GROUP;
+  p.idx_out = idx_out;
+  p.score_out = score_out;
+  p.logits = logits;
+  p.probs = probs;
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, p);
+  return run<float>(c, p);
+}
+
+}  // namespace dh

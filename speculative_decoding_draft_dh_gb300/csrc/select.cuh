@@ -17,6 +17,8 @@
 //  4. The K winners are sorted by (score desc, id asc) with a bitonic network.
 #pragma once
 
+#include <cstddef>
+
 #include "dh_internal.cuh"
 
 namespace dh {
@@ -30,17 +32,19 @@ constexpr int BITMAP_WORDS = (DH_MAX_VOCAB / GROUP + 31) / 32;
 constexpr int HIST_BINS = 4096;  // widest radix digit (12 bits)
 
 struct Shared {
-  uint32_t hist[HIST_BINS];
+  alignas(16) uint32_t hist[HIST_BINS];  // also the fast path's packed 64-bit entries
   uint32_t wsum[SEL_THREADS / 32];
   uint32_t wmin[SEL_THREADS / 32], wmax[SEL_THREADS / 32];
-  uint32_t digit, run, bincount, total, cnt, nref;
+  uint32_t digit, run, bincount, total, cnt, nref, tau_key;
   int32_t rg[RMAX];
   uint32_t bitmap[BITMAP_WORDS];
   float t[DH_MAX_RANK];
-  float rs[RMAX * GROUP];
-  uint32_t sk[DH_MAX_K];
+  alignas(16) float rs[RMAX * GROUP];  // also the fast path's packed boundary entries
+  alignas(16) uint32_t sk[DH_MAX_K];
   uint32_t si[DH_MAX_K];
 };
+
+static_assert(offsetof(Shared, rs) % 8 == 0 && offsetof(Shared, hist) % 8 == 0, "64-bit views need 8-byte alignment");
 
 // Histogram increment (shared-memory atomic; 12-bit digits spread the keys over enough bins that
 // conflicts stay low).
@@ -58,15 +62,16 @@ struct Kth {
 
 // Finds, over the bins of sh.hist[0..nbins) read from the highest down, the bin where the running
 // count reaches krem; sets sh.digit, sh.run (count above it), sh.bincount and, if set_total,
-// sh.total.  Each of the nbins / 8 first threads owns 8 consecutive bins.
+// sh.total.  Each of the first nbins / per threads owns per consecutive bins (per = 8, or more when
+// the block has fewer than nbins / 8 threads).
 __device__ __forceinline__ void find_digit(Shared& sh, int nbins, uint32_t krem, bool set_total) {
-  const int users = nbins / 8;
+  const int per = max(8, nbins / (int)blockDim.x);
+  const int users = nbins / per;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint32_t c[8], sum = 0;
-  if ((int)threadIdx.x < users) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q) { c[q] = sh.hist[nbins - 1 - 8 * (int)threadIdx.x - q]; sum += c[q]; }
-  }
+  const int top = nbins - 1 - per * (int)threadIdx.x;  // this thread's highest bin
+  uint32_t sum = 0;
+  if ((int)threadIdx.x < users)
+    for (int q = 0; q < per; ++q) sum += sh.hist[top - q];
   uint32_t incl = sum;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -85,13 +90,13 @@ __device__ __forceinline__ void find_digit(Shared& sh, int nbins, uint32_t krem,
     if (set_total && (int)threadIdx.x == users - 1) sh.total = incl;
     if (excl < krem && krem <= incl) {
       uint32_t run = excl;
-#pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        if (run + c[q] >= krem) {
-          sh.digit = (uint32_t)(nbins - 1 - 8 * (int)threadIdx.x - q); sh.run = run; sh.bincount = c[q];
+      for (int q = 0; q < per; ++q) {
+        const uint32_t cq = sh.hist[top - q];
+        if (run + cq >= krem) {
+          sh.digit = (uint32_t)(top - q); sh.run = run; sh.bincount = cq;
           break;
         }
-        run += c[q];
+        run += cq;
       }
     }
     if ((int)threadIdx.x == users - 1 && incl < krem) { sh.digit = 0; sh.run = incl; sh.bincount = 0; }
@@ -224,28 +229,37 @@ __device__ bool select_sort_write(Enum en, int K, Shared& sh, int32_t* idx_out, 
 }
 
 // Fast path for a pool that fits in registers (at most FP_ENT entries per thread).  MSB-first
-// radix select over y = key - (smallest key of the pool), with 2048 bins per level: level 0 takes
-// the 11 bits of y below its highest set bit of the pool's range (so the bins span the pool's
-// own key range, and the keys, which crowd into a narrow range of scores, spread over many bins),
-// each further level the next 11 bits.  The descent stops at the first level whose boundary bin
-// (the bin holding the K-th entry) has at most FP_RANK entries.  Entries above the boundary bin
-// are selected, the boundary bin's entries ranked by counting and the best K - above of them
-// taken.  Writes the sorted K and returns true; returns false (nothing written) when the pool has
-// fewer than K entries or the boundary bin still holds more than FP_BOUND entries after the last
-// level (many equal keys), and the caller then runs the generic radix selection.
+// radix select over y = key - (smallest key of the pool), 256 bins per level: level 0 takes the 8
+// bits of y below the top bit of the pool's key range (so the bins span the pool's own range; the
+// pool holds each group's best two scores, and its keys crowd into a narrow band of the float
+// range), each further level the next 8 bits.  The descent stops at the first level whose boundary
+// bin (the bin holding the K-th entry) has at most FP_RANK entries.  Entries above the boundary
+// bin are selected, the boundary bin's entries ranked by counting and the best K - above of them
+// taken; the K winners are then ranked by counting and written out in order.  Entries are packed
+// as key << 32 | ~id, so ranking order is descending packed value.  With 256 bins one warp scans a
+// level's histogram, and a level costs two block barriers.  Returns false (nothing written) when
+// the pool has fewer than K entries or the boundary bin still holds more than FP_BOUND entries
+// after the last level (many equal keys); the caller then runs the generic radix selection.  On
+// success the K selected entries are also left in sh.sk/sh.si, in ranking order.
 constexpr int FP_ENT = 12;
-constexpr int FP_BINS = 2048;
-constexpr int FP_BITS = 11;
+constexpr int FP_BINS = 256;
+constexpr int FP_BITS = 8;
 constexpr int FP_BOUND = 512;  // largest boundary bin ranked by counting (after the last level)
-constexpr int FP_RANK = 32;    // a level whose boundary bin holds at most this many ends the descent
+constexpr int FP_RANK = 64;    // a level whose boundary bin holds at most this many ends the descent
+
+__device__ __forceinline__ unsigned long long pack_entry(uint32_t key, uint32_t id) {
+  return ((unsigned long long)key << 32) | (unsigned long long)(~id);
+}
 
 template <class Load>
 __device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int32_t* idx_out, float* score_out,
                             uint32_t* thr_out) {
   if (n_entries_max > FP_ENT * (int)blockDim.x) return false;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  uint32_t* hist = sh.hist;
   uint32_t key[FP_ENT], id[FP_ENT];
   load(key, id);  // key 0 = no entry
+  for (int i = threadIdx.x; i < FP_BINS; i += blockDim.x) hist[i] = 0;  // visible after the next barrier
   // the pool's key range
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
@@ -260,25 +274,20 @@ __device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int
 #pragma unroll
   for (int q = 0; q < FP_ENT; ++q) key[q] = key[q] ? key[q] - kmin + 1u : 0u;  // y + 1 (0 = no entry)
   const uint32_t range = kmax - kmin + 1u;
-  int shift = max(0, (32 - __clz((int)range)) - FP_BITS);
-  if (range >= 0x80000000u) shift = 32 - FP_BITS;
-  uint32_t* hist = sh.hist;
+  int shift = range >= 0x80000000u ? 32 - FP_BITS : max(0, (32 - __clz((int)range)) - FP_BITS);
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)K, above = 0, bc = 0;
+  const uint32_t dmask = (uint32_t)FP_BINS - 1u;
   bool first = true;
 #pragma unroll 1
   for (;;) {
-    const uint32_t dmask = (uint32_t)FP_BINS - 1u;
-    for (int i = threadIdx.x; i < FP_BINS; i += blockDim.x) hist[i] = 0;
-    __syncthreads();
 #pragma unroll
     for (int q = 0; q < FP_ENT; ++q)
       if (key[q] && (key[q] & mask) == prefix) atomicAdd(&hist[(key[q] >> shift) & dmask], 1u);
     __syncthreads();
-    find_digit(sh, FP_BINS, krem, first);
+    find_digit(sh, FP_BINS, krem, first);  // 256 bins: one warp, no barrier inside
     __syncthreads();
     const uint32_t D = sh.digit, run = sh.run, total = sh.total;
     bc = sh.bincount;
-    __syncthreads();
     if (first && total < (uint32_t)K) return false;
     first = false;
     prefix |= D << shift;
@@ -287,10 +296,14 @@ __device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int
     above += run;
     if (bc <= (uint32_t)FP_RANK || shift == 0) break;  // ranking the boundary bin by counting is cheap
     shift = max(0, shift - FP_BITS);
+    for (int i = threadIdx.x; i < FP_BINS; i += blockDim.x) hist[i] = 0;  // the scan is done with it
+    __syncthreads();
   }
   if (bc > (uint32_t)FP_BOUND) return false;
   // compaction: block scan of the per-thread counts (above the bin in the low 16 bits, in the
   // boundary bin in the high 16 bits), then every thread writes its entries at its offsets
+  unsigned long long* sp = reinterpret_cast<unsigned long long*>(sh.hist);  // the K winners
+  unsigned long long* bp = reinterpret_cast<unsigned long long*>(sh.rs);    // the boundary bin
   uint32_t nu = 0, nb = 0;
 #pragma unroll
   for (int q = 0; q < FP_ENT; ++q) {
@@ -311,43 +324,51 @@ __device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int
   for (int w = 0; w < warp; ++w) before += sh.wsum[w];
   const uint32_t excl = before + incl - mine;
   uint32_t pu = excl & 0xFFFFu, pb = excl >> 16;
-  uint32_t* bk = reinterpret_cast<uint32_t*>(sh.rs);  // boundary bin: keys, then ids at + FP_BOUND
-  uint32_t* bi = bk + FP_BOUND;
 #pragma unroll
   for (int q = 0; q < FP_ENT; ++q) {
     const uint32_t mk = key[q] & mask;
     const uint32_t k0 = key[q] - 1u + kmin;  // the original key
-    if (key[q] && mk > prefix) {
-      sh.sk[pu] = k0;
-      sh.si[pu] = id[q];
-      ++pu;
-    } else if (key[q] && mk == prefix) {
-      bk[pb] = k0;
-      bi[pb] = id[q];
-      ++pb;
-    }
+    if (key[q] && mk > prefix) sp[pu++] = pack_entry(k0, id[q]);
+    else if (key[q] && mk == prefix) bp[pb++] = pack_entry(k0, id[q]);
   }
   __syncthreads();
   // the boundary entries ranking below the first K - above of the bin are dropped; the others go
-  // to sk/si after the entries above the bin (their rank among the bin's entries is unique)
+  // after the entries above the bin (their rank among the bin's entries is unique)
   const int need = K - (int)above;
   for (int i = threadIdx.x; i < (int)bc; i += blockDim.x) {
-    const uint32_t ki = bk[i], ii = bi[i];
+    const unsigned long long pi = bp[i];
     int rank = 0;
-    for (int j = 0; j < (int)bc; ++j) rank += key_before(bk[j], bi[j], ki, ii) ? 1 : 0;
-    if (rank < need) {
-      sh.sk[above + rank] = ki;
-      sh.si[above + rank] = ii;
+    for (int j = 0; j < (int)bc; ++j) rank += bp[j] > pi ? 1 : 0;
+    if (rank < need) sp[above + rank] = pi;
+  }
+  __syncthreads();
+  // rank the K winners by counting (P threads per entry, partial counts added with shuffles) and
+  // write them out in order
+  int P = 1;
+  while (P < 32 && K * (2 * P) <= (int)blockDim.x) P <<= 1;
+  const int per = (K + P - 1) / P;
+  for (int base = 0; base < K * P; base += blockDim.x) {
+    const int t = base + (int)threadIdx.x;
+    const int i = t / P, h = t % P;
+    int rank = 0;
+    unsigned long long pi = 0;
+    if (i < K) {
+      pi = sp[i];
+      const int j1 = min(K, (h + 1) * per);
+      for (int j = h * per; j < j1; ++j) rank += sp[j] > pi ? 1 : 0;
+    }
+    for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    if (i < K && h == 0) {
+      const uint32_t kk = (uint32_t)(pi >> 32), ii = ~(uint32_t)pi;
+      idx_out[rank] = (int32_t)ii;
+      score_out[rank] = fkey_inv(kk);
+      sh.sk[rank] = kk;
+      sh.si[rank] = ii;
+      if (rank == K - 1) sh.tau_key = kk;
     }
   }
   __syncthreads();
-  sort_selected(sh, K);
-  for (int k = threadIdx.x; k < K; k += blockDim.x) {
-    idx_out[k] = (int32_t)sh.si[k];
-    score_out[k] = fkey_inv(sh.sk[k]);
-  }
-  if (thr_out) *thr_out = sh.sk[K - 1];
-  __syncthreads();
+  if (thr_out) *thr_out = sh.tau_key;
   return true;
 }
 
@@ -380,52 +401,57 @@ __device__ __forceinline__ void load4<float>(const float* p, float* x) {
   x[3] = u.w;
 }
 
-// Exact scores of the 64 ids of group g (ids >= vocab give -inf) into out[0..64).  The block's
-// warps split the r rows of V: warp w covers rows [w*rw, (w+1)*rw), two rows per instruction
-// (lanes 0-15 the even rows, 16-31 the odd ones; lane i loads ids 4(i mod 16) .. +3), with up to
-// 16 loads per lane in flight.  The two halves are added with one shuffle, then the per-warp
-// partial sums are added in warp order (a fixed order, so the result is deterministic).
-// scratch: SEL_THREADS / 32 * 64 floats.  vocab is a multiple of 4.
+// Exact scores of the 64 ids of group g (ids >= vocab give -inf) into out[0..64).  The r rows of
+// V are split over SG_PARTS parts (part w covers rows [w*rw, (w+1)*rw)); the block's warps take
+// the parts in turn, two rows per instruction (lanes 0-15 the even rows, 16-31 the odd ones; lane i
+// loads ids 4(i mod 16) .. +3), with up to 16 loads per lane in flight.  The two halves are added
+// with one shuffle, then the parts' partial sums in part order: a fixed order whatever the block
+// size, so blocks of 256 and 512 threads give the same scores.
+// scratch: SG_PARTS * 64 floats.  vocab is a multiple of 4.
+constexpr int SG_PARTS = 16;
+
 template <typename T>
 __device__ void score_group(const float* t, const T* __restrict__ V, int r, int vocab, int g, float* out,
                             float* scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  const int rw = (r + nw - 1) / nw;
-  const int j0 = warp * rw, j1 = min(r, j0 + rw);
+  const int rw = (r + SG_PARTS - 1) / SG_PARTS;
   const int half = lane >> 4;
   const int c = g * GROUP + 4 * (lane & 15);
   const bool cok = c < vocab;
-  float a[4] = {0.f, 0.f, 0.f, 0.f};
-  constexpr int BATCH = 16;
-  for (int jb = j0; jb < j1; jb += 2 * BATCH) {
-    float v[BATCH][4];
+  for (int part = warp; part < SG_PARTS; part += nw) {
+    const int j0 = part * rw, j1 = min(r, j0 + rw);
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+    constexpr int BATCH = 16;
+    for (int jb = j0; jb < j1; jb += 2 * BATCH) {
+      float v[BATCH][4];
 #pragma unroll
-    for (int q = 0; q < BATCH; ++q) {
-      const int j = jb + 2 * q + half;
-      if (j < j1 && cok) {
-        load4<T>(V + (size_t)j * vocab + c, v[q]);
-      } else {
-        v[q][0] = v[q][1] = v[q][2] = v[q][3] = 0.f;
+      for (int q = 0; q < BATCH; ++q) {
+        const int j = jb + 2 * q + half;
+        if (j < j1 && cok) {
+          load4<T>(V + (size_t)j * vocab + c, v[q]);
+        } else {
+          v[q][0] = v[q][1] = v[q][2] = v[q][3] = 0.f;
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < BATCH; ++q) {
+        const int j = jb + 2 * q + half;
+        const float tj = (j < j1) ? t[j] : 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) a[e] = fmaf(tj, v[q][e], a[e]);
       }
     }
 #pragma unroll
-    for (int q = 0; q < BATCH; ++q) {
-      const int j = jb + 2 * q + half;
-      const float tj = (j < j1) ? t[j] : 0.f;
+    for (int e = 0; e < 4; ++e) a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
+    if (lane < 16) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) a[e] = fmaf(tj, v[q][e], a[e]);
+      for (int e = 0; e < 4; ++e) scratch[part * 64 + 4 * lane + e] = a[e];
     }
-  }
-#pragma unroll
-  for (int e = 0; e < 4; ++e) a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
-  if (lane < 16) {
-#pragma unroll
-    for (int e = 0; e < 4; ++e) scratch[warp * 64 + 4 * lane + e] = a[e];
   }
   __syncthreads();
   if (threadIdx.x < 64) {
     float s = 0.f;
-    for (int w = 0; w < nw; ++w) s += scratch[w * 64 + threadIdx.x];
+    for (int w = 0; w < SG_PARTS; ++w) s += scratch[w * 64 + threadIdx.x];
     out[threadIdx.x] = (g * GROUP + (int)threadIdx.x < vocab) ? s : -INFINITY;
   }
   __syncthreads();
@@ -437,11 +463,13 @@ __host__ __device__ constexpr size_t select_smem_bytes(int n_groups) {
   return align_up(sizeof(Shared), 16) + (n_groups <= CACHE_GROUPS ? (size_t)n_groups * sizeof(GroupRec) : 0);
 }
 
-// Exact top-K of one row.  smem: select_smem_bytes(n_groups) bytes, 16-byte aligned.
-// t_row: the row's projection (r values of the activation dtype), or nullptr with acc_row set: the
-// row's slice of the small-batch projection's fixed-point accumulators (copies BR apart), which
-// this block reads and then clears.  rrow: the row's n_groups records.
-template <typename T>
+// Exact top-K of one row by a block of NT threads (NT = blockDim.x).  smem: select_smem_bytes(n_groups)
+// bytes, 16-byte aligned.  t_row: the row's projection (r values of the activation dtype), or
+// nullptr with acc_row set: the row's slice of the small-batch projection's fixed-point
+// accumulators (copies BR apart), which this block reads and then clears.  rrow: the row's
+// n_groups records.  The register fast path is used when NT threads can hold the cached records
+// (SEL_THREADS threads); otherwise the generic radix path.
+template <typename T, int NT = SEL_THREADS>
 __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rrow, const T* __restrict__ t_row,
                            unsigned long long* __restrict__ acc_row, int BR, const T* __restrict__ V, int r,
                            int vocab, int K, int32_t* __restrict__ idx_out, float* __restrict__ score_out) {
@@ -460,22 +488,25 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
   } else {
     for (int j = threadIdx.x; j < r; j += blockDim.x) sh.t[j] = Elem<T>::to_f(t_row[j]);
   }
-  // the row's records: in registers (thread i holds groups i, i + SEL_THREADS, ...) for the fast
-  // path and the certificate, and copied to shared memory for the generic path and the refinement
-  constexpr int PER_THREAD = (CACHE_GROUPS + SEL_THREADS - 1) / SEL_THREADS;
-  static_assert(2 * PER_THREAD == FP_ENT, "fast path holds two pool entries per cached record");
-  GroupRec tmp[PER_THREAD];
-  if (cached) {
+  // the row's records: in registers (thread i holds groups i, i + NT, ...) for the fast path and
+  // the certificate, and copied to shared memory for the generic path and the refinement
+  constexpr int PER_THREAD = (CACHE_GROUPS + NT - 1) / NT;
+  constexpr bool FAST = 2 * PER_THREAD <= FP_ENT;
+  constexpr int REGS = FAST ? PER_THREAD : 1;
+  GroupRec tmp[REGS];
+  if (cached && FAST) {
 #pragma unroll
-    for (int q = 0; q < PER_THREAD; ++q) {
-      const int g = threadIdx.x + q * SEL_THREADS;
+    for (int q = 0; q < REGS; ++q) {
+      const int g = threadIdx.x + q * NT;
       if (g < n_groups) tmp[q] = rrow[g];
     }
 #pragma unroll
-    for (int q = 0; q < PER_THREAD; ++q) {
-      const int g = threadIdx.x + q * SEL_THREADS;
+    for (int q = 0; q < REGS; ++q) {
+      const int g = threadIdx.x + q * NT;
       if (g < n_groups) cache[g] = tmp[q];
     }
+  } else if (cached) {
+    for (int g = threadIdx.x; g < n_groups; g += NT) cache[g] = rrow[g];
   }
   if (threadIdx.x == 0) sh.nref = 0;
   __syncthreads();
@@ -494,11 +525,11 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
   uint32_t tau = 0;
   auto load_pool = [&](uint32_t* key, uint32_t* id) {
 #pragma unroll
-    for (int q = 0; q < PER_THREAD; ++q) {
-      const int g = threadIdx.x + q * SEL_THREADS;
+    for (int q = 0; q < FP_ENT / 2; ++q) {
+      const int g = threadIdx.x + q * NT;
       key[2 * q] = key[2 * q + 1] = 0u;
       id[2 * q] = id[2 * q + 1] = 0xFFFFFFFFu;
-      if (g < n_groups) {
+      if (q < REGS && g < n_groups) {
         const GroupRec rc = tmp[q];
         const uint32_t o1 = rc.offs & 0xFFu, o2 = (rc.offs >> 8) & 0xFFu;
         if (o1 != NO_OFFSET) { key[2 * q] = fkey(rc.m1); id[2 * q] = (uint32_t)g * GROUP + o1; }
@@ -506,7 +537,7 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
       }
     }
   };
-  bool selected = cached && fast_select(load_pool, 2 * n_groups, K, sh, idx_out, score_out, &tau);
+  bool selected = FAST && cached && fast_select(load_pool, 2 * n_groups, K, sh, idx_out, score_out, &tau);
   if (threadIdx.x == 0) sh.nref = 0;
   __syncthreads();
   if (!selected) selected = select_sort_write(pool, K, sh, idx_out, score_out, &tau);
@@ -518,10 +549,10 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
       if (pos < RMAX) sh.rg[pos] = g;
       atomicOr(&sh.bitmap[g >> 5], 1u << (g & 31));
     };
-    if (cached) {
+    if (cached && FAST) {
 #pragma unroll
-      for (int q = 0; q < PER_THREAD; ++q) {
-        const int g = threadIdx.x + q * SEL_THREADS;
+      for (int q = 0; q < REGS; ++q) {
+        const int g = threadIdx.x + q * NT;
         if (g < n_groups && fkey(tmp[q].m3) >= tau) mark(g);
       }
     } else {

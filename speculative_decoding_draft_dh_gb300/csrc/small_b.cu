@@ -436,18 +436,6 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
                 unsigned long long* acc, GroupRec* recs, int* status) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
   cudaError_t e = cudaSuccess;
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return note_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
-  CUtensorMap tmV;
-  cuuint64_t dims[2] = {(cuuint64_t)vocab, (cuuint64_t)r};
-  cuuint64_t strides[1] = {(cuuint64_t)vocab * sizeof(T)};
-  cuuint32_t box[2] = {(cuuint32_t)TILE, (cuuint32_t)RB};
-  cuuint32_t estr[2] = {1, 1};
-  if (fn(&tmV, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-         const_cast<void*>(V), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(V, small batch)");
-
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
@@ -498,6 +486,18 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
     if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_scores_lsu)");
     return note_error(cudaGetLastError(), "small-batch stage 1 launch");
   }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return note_error(cudaErrorNotSupported, "cuTensorMapEncodeTiled entry point");
+  CUtensorMap tmV;
+  cuuint64_t dims[2] = {(cuuint64_t)vocab, (cuuint64_t)r};
+  cuuint64_t strides[1] = {(cuuint64_t)vocab * sizeof(T)};
+  cuuint32_t box[2] = {(cuuint32_t)TILE, (cuuint32_t)RB};
+  cuuint32_t estr[2] = {1, 1};
+  if (fn(&tmV, sizeof(T) == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+         const_cast<void*>(V), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(V, small batch)");
+
   cfg.gridDim = dim3((unsigned)c.num_sms);
   cfg.blockDim = dim3(SB_THREADS);
   cfg.dynamicSmemBytes = STAGE_REGION + 1024;

@@ -96,6 +96,24 @@ def test_rescore_and_tree_reject_bad_arguments_on_host(lib):
                               P(FAKE), None, P(FAKE * 16), 8, None) == 3        # workspace too small
 
 
+def test_draft_head_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+
+    def call(B=1, d=256, r=32, vocab=4096, K=16, dt=binding.F32, W=FAKE, ws=FAKE * 16, nbytes=1 << 30):
+        return lib.dh_draft_head(P(FAKE), P(FAKE), P(FAKE), P(W), B, d, r, vocab, K, dt, P(FAKE), P(FAKE),
+                                 P(FAKE), None, P(ws) if ws else None, nbytes, None)
+    assert call(K=0) == 1
+    assert call(W=0) == 1                    # W missing
+    assert call(dt=7) == 2
+    assert call(d=250) == 2                  # fp32 row of 1000 bytes
+    assert call(d=16384) == 2                # above the rescoring limit
+    assert call(nbytes=64) == 3
+    assert call(B=0) == 0
+    need = lib.dh_draft_head_workspace(1, 5120, 128, 151936, 64, binding.BF16)
+    assert need >= lib.dh_lowrank_topk_workspace(1, 5120, 128, 151936, 64, binding.BF16)
+    assert need % 256 == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="libdh.so not found"):
         binding.load_library(str(tmp_path / "libdh.so"))

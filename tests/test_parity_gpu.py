@@ -24,11 +24,15 @@ def _lib():
     torch.cuda.synchronize()
 
 
-def run_head(x, K, rows=None):
-    """GPU stage 1 + stage 2 on device tensors; oracle on the listed rows.  Returns stats."""
+def run_head(x, K, rows=None, api="split"):
+    """GPU stage 1 + stage 2 on device tensors (the two calls, or dh_draft_head with api="head");
+    oracle on the listed rows.  Returns the GPU outputs."""
     h, U, V, W = x["h"], x["U"], x["V"], x["W"]
-    idx, score = dh.lowrank_topk(h, U, V, K)
-    logits, probs = dh.exact_rescore(h, W, idx)
+    if api == "head":
+        idx, score, logits, probs = dh.draft_head(h, U, V, W, K)
+    else:
+        idx, score = dh.lowrank_topk(h, U, V, K)
+        logits, probs = dh.exact_rescore(h, W, idx)
     torch.cuda.synchronize()
     B = h.shape[0]
     rows = list(range(B)) if rows is None else rows
@@ -52,29 +56,33 @@ def run_head(x, K, rows=None):
 
 # ---------------------------------------------------------------- small shapes, every row
 
+@pytest.mark.parametrize("api", ["split", "head"])
 @pytest.mark.parametrize("B", [1, 2, 3, 4])
-def test_tiny_head(B):
+def test_tiny_head(B, api):
     cfg = inputs.head_config("tiny", B=B)
     x = inputs.make_head(cfg, seed=0, device=DEV)
-    run_head(x, cfg.K)
+    run_head(x, cfg.K, api=api)
 
 
 MID = inputs.HeadConfig("mid_bf16", 5, 512, 8200, 64, 32, "bf16", 0.1, True)  # ragged vocab tail
 
 
+@pytest.mark.parametrize("api", ["split", "head"])
 @pytest.mark.parametrize("seed", [0, 1])
-def test_mid_bf16_ragged_vocab(seed):
+def test_mid_bf16_ragged_vocab(seed, api):
     x = inputs.make_head(MID, seed=seed, device=DEV)
-    run_head(x, MID.K)
+    run_head(x, MID.K, api=api)
 
 
 @pytest.mark.parametrize("K", [1, 2, 3, 7, 16, 17, 33, 64, 65, 100, 128, 129, 1000, 1024])
-def test_tiny_head_K_range(K):
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_tiny_head_K_range(K, api):
     """K across the selection's sort regimes and every cluster shape of the small-batch rescore
-    (1 to 8 CTAs of 2, 4, 8 or 16 warps), then the ticket kernel above K = 128."""
+    (1 to 8 CTAs of 2, 4, 8 or 16 warps), then the ticket kernel above K = 128; with api="head"
+    the fused cluster kernel up to K = 256 and the two-call path above."""
     cfg = inputs.head_config("tiny", B=2, K=K)
     x = inputs.make_head(cfg, seed=3, device=DEV)
-    run_head(x, K)
+    run_head(x, K, api=api)
 
 
 def test_K_equals_vocab_uses_exact_fallback():
@@ -89,7 +97,8 @@ def _best_column(x):
     return int(np.argmax(s))
 
 
-def test_clustered_candidates_are_refined():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_clustered_candidates_are_refined(api):
     """All top candidates inside one group of 64 ids: the group's third score reaches the
     candidate threshold and the group is re-scored exactly."""
     cfg = inputs.head_config("tiny", B=1, K=16)
@@ -98,10 +107,11 @@ def test_clustered_candidates_are_refined():
     base = x["V"][:, v].clone()
     for j in range(64):
         x["V"][:, 128 + j] = base * (1.0 + 0.01 * j)
-    run_head(x, cfg.K)
+    run_head(x, cfg.K, api=api)
 
 
-def test_many_clustered_groups_use_full_rescan():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_many_clustered_groups_use_full_rescan(api):
     cfg = inputs.head_config("tiny", B=1, K=128)
     x = inputs.make_head(cfg, seed=6, device=DEV)
     v = _best_column(x)
@@ -109,17 +119,18 @@ def test_many_clustered_groups_use_full_rescan():
     for g in range(40):
         for q in range(3):
             x["V"][:, 64 * g + q] = base * (2.0 + 0.001 * (3 * g + q))
-    run_head(x, cfg.K)
+    run_head(x, cfg.K, api=api)
 
 
-def test_equal_scores_resolve_to_lowest_id():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_equal_scores_resolve_to_lowest_id(api):
     cfg = inputs.head_config("tiny", B=1, K=16)
     x = inputs.make_head(cfg, seed=7, device=DEV)
     v = _best_column(x)
     col = x["V"][:, v].clone() * 3.0
     for c in (4000, 17, 2222, 640):
         x["V"][:, c] = col
-    idx, score, _, _ = run_head(x, cfg.K)
+    idx, score, _, _ = run_head(x, cfg.K, api=api)
     assert idx[0, :4].cpu().tolist() == [17, 640, 2222, 4000]
     assert len(set(score[0, :4].cpu().tolist())) == 1
 
@@ -175,10 +186,44 @@ def test_rescore_without_probs():
 
 # ---------------------------------------------------------------- full-size workloads
 
-def test_batch1_full_size():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_batch1_full_size(api):
     cfg = inputs.HEAD_CONFIGS["batch1"]
     x = inputs.make_head(cfg, seed=0, device=DEV)
-    run_head(x, cfg.K)
+    run_head(x, cfg.K, api=api)
+
+
+@pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64)])
+def test_draft_head_matches_the_two_calls(name, B):
+    """dh_draft_head (the fused cluster kernel for small batches, the two-call sequence otherwise)
+    gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same selection rule on
+    the same records and the same per-candidate dot product order; twice in a row with one
+    workspace (its state resets itself)."""
+    cfg = inputs.head_config(name, B=B)
+    x = inputs.make_head(cfg, seed=11, device=DEV)
+    h, U, V, W = x["h"], x["U"], x["V"], x["W"]
+    idx, score = dh.lowrank_topk(h, U, V, cfg.K)
+    logits, probs = dh.exact_rescore(h, W, idx)
+    ws = dh.Workspace()
+    for _ in range(2):
+        i2, s2, l2, p2 = dh.draft_head(h, U, V, W, cfg.K, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(i2, idx)
+        assert torch.equal(s2, score)
+        assert torch.equal(l2, logits)
+        assert torch.equal(p2, probs)
+    assert dh.workspace_status(ws) == 0
+
+
+def test_draft_head_without_probs_and_bad_rows():
+    cfg = inputs.head_config("tiny", B=3)
+    x = inputs.make_head(cfg, seed=12, device=DEV)
+    i2, s2, l2, p2 = dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K, with_probs=False)
+    torch.cuda.synchronize()
+    assert p2 is None
+    oz, _ = oracle.exact_rescore(x["h"].cpu(), x["W"].cpu(), i2.cpu())
+    for b in range(cfg.B):
+        check_logits(l2[b].cpu().numpy(), None, oz[b], None, where=f"row {b}")
 
 
 def test_moderate_load_sampled_rows():
