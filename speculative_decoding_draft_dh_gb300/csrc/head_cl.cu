@@ -12,11 +12,11 @@
 // CTA (rank 0); the other CTAs reach them with remote atomics and loads.  The steps are those of
 // the register fast path of the selection kernel (radix levels over the pool's own key range,
 // compaction, ranking by counting), each ended by a cluster barrier.  The leader writes the sorted
-// candidates, every CTA then scores its share of them against h (staged in shared memory before
+// candidates; every CTA then scores its share of them against h (staged in shared memory before
 // the wait on the previous kernel) and stores the logits into the leader, which computes the
 // softmax.  A row whose certificate finds groups to re-score, or whose pool is degenerate, is
-// selected again by the leader alone with the block selection (select_row: exact, with
-// refinement and full rescan) before the rescoring step.
+// selected again by the leader alone with the block selection (select_row: exact, with refinement
+// and full rescan) before the rescoring step.
 //
 // Cluster barriers are hardware barriers that every CTA passes unconditionally, so they always
 // complete.
@@ -210,7 +210,6 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     if (bc > (uint32_t)HC_BOUND) fallback = true;
   }
   // every CTA took the same decisions from the same leader values
-
   if (!fallback) {
     // compaction into the leader's lists (positions from warp ballots, one remote atomic per warp)
     const uint32_t below = (1u << lane) - 1u;
