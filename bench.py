@@ -210,7 +210,10 @@ KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
                 "rescore_cluster": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
                 "head_cluster": ["head_cl.cu", "select.cuh", "dh_internal.cuh"],
                 "proj_partial": ["proj.cu", "dh_internal.cuh"],
-                "tree_argmax": ["tree.cu", "dh_internal.cuh"]}
+                "proj_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
+                "proj_reduce_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
+                "tree_argmax": ["tree.cu", "dh_internal.cuh"],
+                "tree_walk": ["tree.cu", "dh_internal.cuh"]}
 
 
 def head_bytes(cfg):
