@@ -333,6 +333,39 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     us_per_call = ms * 1e3 / a.steps
     value = weak_scaling_value(cfg.B, a.steps, world, ms)
 
+    # spread: each replay of the S-step graph timed on its own (after the headline measurement)
+    n_rep = max(5, min(50, a.steps // S))
+    rep_us = []
+    with torch.cuda.stream(stream):
+        for _ in range(n_rep):
+            r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            r0.record(stream)
+            g_full.replay()
+            r1.record(stream)
+            rep_us.append((r0, r1))
+    torch.cuda.synchronize()
+    rep_us = sorted(r0.elapsed_time(r1) * 1e3 / S for r0, r1 in rep_us)
+    spread = {"us_per_call_p10": round(rep_us[len(rep_us) // 10], 3),
+              "us_per_call_median": round(rep_us[len(rep_us) // 2], 3),
+              "us_per_call_p90": round(rep_us[(9 * len(rep_us)) // 10], 3), "replays": n_rep,
+              "steps_per_replay": S}
+    # stream-queued: the same calls launched eagerly back to back (no graph)
+    n_eager = min(a.steps, 1000 if cfg.B <= 64 else 50)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            step(sets[i % copies])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(n_eager):
+            step(sets[i % copies])
+        e1.record(stream)
+    torch.cuda.synchronize()
+    spread["us_per_call_stream_queued"] = round(e0.elapsed_time(e1) * 1e3 / n_eager, 3)
+    # distinct W rows among the candidates of one step (stage 2 reads each once from HBM; repeats
+    # may hit L2)
+    e_sz = 2 if cfg.dtype == "bf16" else 4
+    uniq = int(torch.unique(sets[0]["idx"]).numel())
+
     # per-kernel events on the launch stream (separate pass, eager launches)
     n_prof = min(a.steps, 2000 if cfg.B <= 64 else 200)
     dh.prof_enable(True)
@@ -365,6 +398,10 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     path_roofline = {"bound": "hbm", "bytes_per_call": per_step, "achieved": round(path_ach, 1),
                      "peak": hbm, "unit": "GB/s", "frac": round(path_ach / hbm, 4),
                      "ideal_us": round(per_step / (hbm * 1e9) * 1e6, 3)}
+    uniq_bytes = per_step - hb["W_rows"] + uniq * cfg.d * e_sz
+    path_roofline["unique_w_rows"] = uniq
+    path_roofline["bytes_per_call_unique_rows"] = uniq_bytes
+    path_roofline["frac_unique_rows"] = round(uniq_bytes / (us_per_call * 1e-6) / 1e9 / hbm, 4)
 
     # end to end through the public API with host buffers
     e2e = None
@@ -406,7 +443,8 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
         "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 6),
-        "us_per_call": round(us_per_call, 3), "higher_is_better": True, "scaling": "weak",
+        "us_per_call": round(us_per_call, 3), "timing_spread": spread, "higher_is_better": True,
+        "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generators, random weights)",
         "config": {"workload": cfg.name, "B": cfg.B, "d": cfg.d, "vocab": cfg.vocab, "r": cfg.r,
                    "K": cfg.K, "seed": a.seed, "api": "dh_draft_head" if a.api == "head" else

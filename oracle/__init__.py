@@ -46,6 +46,7 @@ def bind(path: str):
     lib.oracle_lowrank_topk.argtypes = [P, P, P, I, I, I, I, I, I, P, I, P, P]
     lib.oracle_exact_rescore.argtypes = [P, P, P, I, I, I, I, I, P, I, P, P]
     lib.oracle_tree_accept.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P]
+    lib.oracle_expand_children.argtypes = [P, P, P, I, I, I, ctypes.c_float, P, P, P]
     for f in ("oracle_round_bf16", "oracle_lowrank_project", "oracle_lowrank_scores",
               "oracle_lowrank_topk", "oracle_exact_rescore", "oracle_tree_accept"):
         getattr(lib, f).restype = I
@@ -178,3 +179,19 @@ def tree_accept(logits, parent, token, reqs=None):
                                      None if rr is None else _ptr(rr), n, _ptr(am), _ptr(path),
                                      _ptr(ln), _ptr(bonus)), "tree_accept")
     return {"argmax": am, "path": path, "len": ln, "bonus": bonus}
+
+
+def expand_children(probs, idx, w, parent_prob=None, min_benefit=0.0):
+    """Step 7: the w children of each frontier node by exact probability.  probs fp32 [B, K],
+    idx int32 [B, K], parent_prob fp32 [B] or None (1).  Returns (child_token int32 [B, w],
+    child_prob fp32 [B, w], n_keep int32 [B])."""
+    pp = np.ascontiguousarray(np.asarray(probs, dtype=np.float32))
+    ii = np.ascontiguousarray(np.asarray(idx, dtype=np.int32))
+    B, K = pp.shape
+    par = None if parent_prob is None else np.ascontiguousarray(np.asarray(parent_prob, dtype=np.float32))
+    tok = np.empty((B, w), dtype=np.int32)
+    cp = np.empty((B, w), dtype=np.float32)
+    keep = np.empty((B,), dtype=np.int32)
+    _check(load().oracle_expand_children(_ptr(pp), _ptr(ii), None if par is None else _ptr(par), B, K, w,
+                                         float(min_benefit), _ptr(tok), _ptr(cp), _ptr(keep)), "expand_children")
+    return tok, cp, keep

@@ -29,6 +29,16 @@
 //        the deepest accepted node (ties -> lowest node index) ends the accepted path;
 //        len = its depth, path = root..node, bonus = a[b,node].
 //
+//   EAGLE-4 summary page, section "Why a draft tree needs a cost model": products of draft
+//   probabilities approximate the benefit of a branch, and a branch is worth computing when its
+//   benefit A over its latency cost C passes a threshold (the page's formula itself is lost; this
+//   is its plainest reading, with the caller supplying threshold x C); AlphaSignal page, section
+//   "Runtime-sized speculation": a top-k of 1 drafts a chain, larger k a tree.
+//     7. expanding a frontier node b: its children are its w candidates of highest exact
+//        probability p (ties -> lower token id; a NaN probability ranks below every number),
+//        child path probability = parent path probability x p (rounded to fp32), and the node
+//        keeps its first n_keep children, those whose path probability exceeds min_benefit.
+//
 // Build: g++ -O2 -std=c++17 -fopenmp -ffp-contract=off -shared -fPIC dh_oracle.cpp
 #include <algorithm>
 #include <cmath>
@@ -219,6 +229,37 @@ int oracle_tree_accept(const void* logits, const int32_t* parent, const int32_t*
     len_out[i] = depth[best];
     bonus_out[i] = a[best];
     for (int n = best, j = depth[best]; n >= 0; n = par[n], --j) path[j] = n;
+  }
+  return 0;
+}
+
+// Step 7 for every row.  probs, idx: B x K (the row's candidates and their exact probabilities);
+// parent_prob: B (null = 1); outputs child_token, child_prob: B x w; n_keep: B (may be null).
+int oracle_expand_children(const float* probs, const int32_t* idx, const float* parent_prob, int B, int K, int w,
+                           float min_benefit, int32_t* child_token, float* child_prob, int32_t* n_keep) {
+  if (B < 0 || K <= 0 || w <= 0 || w > K) return -1;
+  for (int b = 0; b < B; ++b) {
+    const float* p = probs + (size_t)b * K;
+    const int32_t* tk = idx + (size_t)b * K;
+    // (probability desc, token asc); NaN below every number
+    std::vector<int> order(K);
+    for (int k = 0; k < K; ++k) order[k] = k;
+    std::stable_sort(order.begin(), order.end(), [&](int x, int y) {
+      const bool nx = std::isnan(p[x]), ny = std::isnan(p[y]);
+      if (nx != ny) return ny;  // the number ranks first
+      if (!nx && p[x] != p[y]) return p[x] > p[y];
+      return tk[x] < tk[y];
+    });
+    const double par = parent_prob ? (double)parent_prob[b] : 1.0;
+    int keep = 0;
+    for (int c = 0; c < w; ++c) {
+      const int k = order[c];
+      const float a = (float)(par * (double)p[k]);  // the exact product, rounded once to fp32
+      child_token[(size_t)b * w + c] = tk[k];
+      child_prob[(size_t)b * w + c] = a;
+      if (a > min_benefit) ++keep;
+    }
+    if (n_keep) n_keep[b] = keep;
   }
   return 0;
 }

@@ -6,6 +6,10 @@
   the ranks all-gather their K (score, id) pairs, and the K best of the union in (score desc, id asc)
   order equal the unsharded top-K.  Any global top-K member is in its own shard's top-K, so the
   union always contains the answer.
+* Tree acceptance with vocabulary-sharded target logits: each rank packs its shard's per-node
+  maximum as (order-preserving value key << 32 | ~global id) into a 64-bit integer, one all-reduce
+  MAX gives the global argmax with ties to the lowest id, and the walk on the merged argmax equals
+  the unsharded acceptance.
 """
 import os
 import socket
@@ -72,6 +76,38 @@ def _shard_worker(rank, world, port, q):
         dist.destroy_process_group()
 
 
+def _packed_max(vals, lo):
+    """(value key << 32 | ~global id) per row of vals [rows, n] (fp32); the row maximum."""
+    bits = vals.astype(np.float32).view(np.uint32).astype(np.uint64)
+    neg = (bits >> np.uint64(31)) == 1
+    key = np.where(neg, (~bits) & np.uint64(0xFFFFFFFF), bits | np.uint64(0x80000000))
+    ids = np.arange(vals.shape[1], dtype=np.uint64) + np.uint64(lo)
+    packed = (key << np.uint64(32)) | ((~ids) & np.uint64(0xFFFFFFFF))
+    return packed.max(axis=1)
+
+
+def _tree_shard_worker(rank, world, port, q):
+    import sys
+    sys.path.insert(0, ROOT)
+    from speculative_decoding_draft_dh_gb300 import inputs
+    _init(rank, world, port)
+    try:
+        tcfg = inputs.tree_config("tiny_tree")
+        t = inputs.make_tree(tcfg, seed=5)
+        L = t["logits"].float().numpy()
+        B, N, vocab = L.shape
+        lo, hi = vocab * rank // world, vocab * (rank + 1) // world
+        local = _packed_max(L[:, :, lo:hi].reshape(B * N, hi - lo), lo)
+        # the packed keys fit a signed int64 only after flipping the top bit (order preserving)
+        ten = torch.from_numpy((local ^ np.uint64(1 << 63)).view(np.int64).copy())
+        dist.all_reduce(ten, op=dist.ReduceOp.MAX)
+        merged = ten.numpy().view(np.uint64) ^ np.uint64(1 << 63)
+        argmax = (~(merged & np.uint64(0xFFFFFFFF)) & np.uint64(0xFFFFFFFF)).astype(np.int64).reshape(B, N)
+        q.put((rank, argmax))
+    finally:
+        dist.destroy_process_group()
+
+
 def _run(worker, world=2):
     ctx = mp.get_context("spawn")
     q = ctx.Queue()
@@ -102,3 +138,14 @@ def test_vocab_sharded_merge_equals_unsharded_topk():
     idx, _ = oracle.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
     for _, merged in out:
         np.testing.assert_array_equal(merged, idx)
+
+
+def test_vocab_sharded_tree_argmax_equals_unsharded():
+    import oracle
+    from speculative_decoding_draft_dh_gb300 import inputs
+    out = _run(_tree_shard_worker)
+    tcfg = inputs.tree_config("tiny_tree")
+    t = inputs.make_tree(tcfg, seed=5)
+    ref = oracle.tree_accept(t["logits"], t["parent"], t["token"])
+    for _, argmax in out:
+        np.testing.assert_array_equal(argmax, ref["argmax"])

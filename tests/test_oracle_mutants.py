@@ -34,6 +34,14 @@ MUTANTS = [
      ["test_golden_trees"]),
     ("deepest_tie_highest_index", "depth[n] > depth[best]", "depth[n] >= depth[best]",
      ["test_golden_trees"]),
+    ("expand_ties_by_position", "return tk[x] < tk[y];", "return x < y;",
+     ["test_golden_expansions", "test_expansion_matches_lexsort"]),
+    ("expand_ascending", "return p[x] > p[y];", "return p[x] < p[y];",
+     ["test_golden_expansions", "test_expansion_matches_lexsort"]),
+    ("expand_drops_parent", "(float)(par * (double)p[k])", "(float)((double)p[k])",
+     ["test_golden_expansions", "test_expansion_matches_lexsort"]),
+    ("expand_keeps_at_threshold", "if (a > min_benefit) ++keep;", "if (a >= min_benefit) ++keep;",
+     ["test_golden_expansions"]),
 ]
 
 

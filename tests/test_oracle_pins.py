@@ -283,3 +283,61 @@ def test_tree_generator_shape_limits():
             depth[n] = depth[par[b, n]] + 1
             kids[par[b, n]] += 1
         assert max(depth) <= 10 and max(kids) <= 4
+
+
+# ---------------------------------------------------------------- step 7: expanding a frontier node
+
+def load_golden_expansions():
+    cases, cur = [], None
+    with open(os.path.join(GOLDEN, "expand.txt")) as f:
+        for line in f:
+            line = line.split("#", 1)[0].strip()
+            if not line:
+                continue
+            key, *vals = line.split()
+            if key == "case":
+                cur = {"name": vals[0]}
+            elif key == "end":
+                cases.append(cur)
+                cur = None
+            elif key in ("tokens", "expect_tokens"):
+                cur[key] = [int(v) for v in vals]
+            elif key in ("w", "expect_keep"):
+                cur[key] = int(vals[0])
+            elif key in ("parent", "min_benefit"):
+                cur[key] = float(vals[0])
+            else:
+                cur[key] = [float(v) for v in vals]
+    return cases
+
+
+@pytest.mark.parametrize("case", load_golden_expansions(), ids=lambda c: c["name"])
+def test_golden_expansions(case):
+    tok, cp, keep = oracle.expand_children(np.array([case["probs"]], dtype=np.float32),
+                                           np.array([case["tokens"]], dtype=np.int32), case["w"],
+                                           parent_prob=np.array([case["parent"]], dtype=np.float32),
+                                           min_benefit=case["min_benefit"])
+    assert tok[0].tolist() == case["expect_tokens"]
+    np.testing.assert_array_equal(cp[0], np.array(case["expect_probs"], dtype=np.float32))
+    assert keep[0] == case["expect_keep"]
+
+
+@pytest.mark.parametrize("w", [1, 4, 64])
+def test_expansion_matches_lexsort(w):
+    """Against numpy: lexsort by (probability desc, token asc), fp32 products, a prefix count."""
+    rng = np.random.default_rng(40 + w)
+    B, K = 6, 64
+    p = rng.dirichlet(np.ones(K), size=B).astype(np.float32)
+    p[:, 5] = p[:, 9]  # exact ties between candidates
+    p[2, :8] = p[2, 8]
+    tok = np.stack([rng.permutation(100000)[:K] for _ in range(B)]).astype(np.int32)
+    par = rng.uniform(0.1, 1.0, size=B).astype(np.float32)
+    thr = 0.01
+    ct, cp, keep = oracle.expand_children(p, tok, w, parent_prob=par, min_benefit=thr)
+    for b in range(B):
+        order = np.lexsort((tok[b], -p[b].astype(np.float64)))[:w]
+        assert ct[b].tolist() == tok[b][order].tolist()
+        want = (np.float32(par[b]) * p[b][order]).astype(np.float32)
+        np.testing.assert_array_equal(cp[b], want)
+        assert keep[b] == int(np.sum(want > np.float32(thr)))
+        assert np.all(np.diff(cp[b]) <= 0)
