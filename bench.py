@@ -40,8 +40,9 @@ METRIC = "draft-head rows/sec and µs per call (low-rank top-K + rescore); % of 
 TREE_METRIC = "tree-acceptance requests/sec and µs per call (per-node argmax + tree walk); % of HBM roofline"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200}
-DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5}
+DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200, "level": 10000}
+DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5, "level": 100}
+EXPAND_W = {"level": 4}  # children per frontier node in the draft-level workload
 
 
 def parse_args():
@@ -50,7 +51,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree"])
+    ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree", "level"])
     ap.add_argument("--api", default="split", choices=["head", "split"],
                     help="head: dh_draft_head (both stages in one call); split: dh_lowrank_topk + "
                          "dh_exact_rescore")
@@ -209,6 +210,7 @@ KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
                 "rescore_ring": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
                 "rescore_cluster": ["rescore.cu", "sm100.cuh", "dh_internal.cuh"],
                 "head_cluster": ["head_cl.cu", "select.cuh", "dh_internal.cuh"],
+                "expand": ["expand.cu", "dh_internal.cuh"],
                 "proj_partial": ["proj.cu", "dh_internal.cuh"],
                 "proj_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
                 "proj_reduce_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
@@ -239,6 +241,8 @@ def kernel_algo(cfg, name):
         return "tensor", 2.0 * cfg.B * cfg.d * cfg.r, "TFLOP/s"
     if name == "proj_partial":
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
+    if name == "expand":  # candidates' probabilities and ids in, children out
+        return "hbm", cfg.B * cfg.K * 8 + cfg.B * 4 * 8 + cfg.B * 8, "GB/s"
     if name == "head_cluster":  # records read once, the candidates' W rows, h
         return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16 + cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name in ("rescore", "rescore_ring", "rescore_cluster"):
@@ -266,6 +270,14 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
 
+    expand_w = EXPAND_W.get(cfg.name, 0)
+    for x in sets:
+        if expand_w:
+            x["par"] = torch.linspace(1.0, 0.25, cfg.B, device=dev, dtype=torch.float32)
+            x["ctok"] = torch.empty(cfg.B, expand_w, dtype=torch.int32, device=dev)
+            x["cprob"] = torch.empty(cfg.B, expand_w, dtype=torch.float32, device=dev)
+            x["keep"] = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+
     def step(x, idx=None, logits=None, probs=None):
         idx = x["idx"] if idx is None else idx
         logits = x["logits"] if logits is None else logits
@@ -276,6 +288,9 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
         else:
             dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, idx_out=idx, score_out=x["score"], workspace=ws)
             dh.exact_rescore(x["h"], x["W"], idx, logits_out=logits, probs_out=probs, workspace=ws)
+        if expand_w:  # one draft level: the frontier nodes' children by exact probability
+            dh.expand_children(probs, idx, expand_w, parent_prob=x["par"], min_benefit=1e-3,
+                               child_token=x["ctok"], child_prob=x["cprob"], n_keep=x["keep"])
 
     with torch.cuda.stream(stream):
         for i in range(a.warmup):
@@ -471,14 +486,16 @@ def cpu_head_baseline(cfg, x, seconds):
         idx, _ = oracle.lowrank_topk(hc, Uc, Vc, cfg.K, rows=chunk)
         full_idx = np.zeros((cfg.B, cfg.K), dtype=np.int32)
         full_idx[chunk] = idx
-        oracle.exact_rescore(hc, Wc, full_idx, rows=chunk)
+        _, p = oracle.exact_rescore(hc, Wc, full_idx, rows=chunk)
+        if EXPAND_W.get(cfg.name, 0):
+            oracle.expand_children(p.astype(np.float32), idx, EXPAND_W[cfg.name], min_benefit=1e-3)
         rows_done += len(chunk)
         b += len(chunk)
     dt = time.perf_counter() - t0
     used = min(cfg.B, cores)
+    what = "stage 1 + stage 2" + (" + expansion" if EXPAND_W.get(cfg.name, 0) else "")
     return {"value": round(rows_done / dt, 4), "unit": "rows/s", "cores": used, "kind": "oracle",
-            "sample": f"{rows_done} rows of the {cfg.name} workload (stage 1 + stage 2), "
-                      f"{dt:.1f} s, OpenMP over rows"}
+            "sample": f"{rows_done} rows of the {cfg.name} workload ({what}), {dt:.1f} s, OpenMP over rows"}
 
 
 # ------------------------------------------------------------------------------------- tree

@@ -135,6 +135,33 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
                   void* workspace, size_t ws_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Expanding frontier nodes of the draft tree.
+ *
+ * EAGLE-4 summary page, section "Why a draft tree needs a cost model": products of draft
+ * probabilities approximate a branch's benefit A, and a branch is worth computing when A over its
+ * latency cost C passes a threshold (the page's formula is lost; here a child is kept when
+ * A > min_benefit, and the caller supplies min_benefit = threshold x C from its latency table for
+ * the batch and width).  AlphaSignal page, section "Runtime-sized speculation": a top-k of 1
+ * drafts a chain, larger k a tree.
+ *
+ * Row b is a frontier node with K candidates: idx[b,:] (token ids, e.g. from dh_lowrank_topk) and
+ * their exact probabilities probs[b,:] (e.g. from dh_exact_rescore).
+ *   order      = the candidates by (probability desc, token asc, position asc); a NaN probability
+ *                ranks below every number
+ *   child_token[b,c] = idx[b, order[c]],  c < w
+ *   child_prob[b,c]  = fp32(parent_prob[b] * probs[b, order[c]])   (parent_prob NULL: 1)
+ *   n_keep[b]  = number of c < w with child_prob[b,c] > min_benefit (a prefix; min_benefit <= 0
+ *                with finite probabilities keeps all w)
+ * probs, child_prob: fp32; idx, child_token, n_keep: int32; all device.  probs, idx [B x K];
+ * parent_prob [B] (may be NULL); child_* [B x w]; n_keep [B] (may be NULL).  1 <= w <= K <= DH_MAX_K.
+ * No workspace.  Launched with programmatic dependent launch after a rescoring call on the same
+ * stream.  B = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+int dh_expand_children(const float* probs, const int32_t* idx, const float* parent_prob, int B, int K, int w,
+                       float min_benefit, int32_t* child_token, float* child_prob, int32_t* n_keep,
+                       void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Greedy draft-tree acceptance.
  *
  * daily.dev "EAGLE-4 speeds up LLM inference ...", section "How it works"; EAGLE-4 summary page,

@@ -22,6 +22,7 @@ F32, BF16 = 0, 1
 
 EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_workspace", "dh_lowrank_topk",
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_draft_head_workspace", "dh_draft_head",
+           "dh_expand_children",
            "dh_tree_accept_workspace",
            "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
 
@@ -64,6 +65,8 @@ def load_library(path: str | None = None):
         lib.dh_draft_head_workspace.restype = Z
         lib.dh_draft_head.argtypes = [P, P, P, P, I, I, I, I, I, I, P, P, P, P, P, Z, P]
         lib.dh_draft_head.restype = I
+        lib.dh_expand_children.argtypes = [P, P, P, I, I, I, ctypes.c_float, P, P, P, P]
+        lib.dh_expand_children.restype = I
         lib.dh_tree_accept_workspace.argtypes = [I, I, I]
         lib.dh_tree_accept_workspace.restype = Z
         lib.dh_tree_accept.argtypes = [P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
@@ -207,6 +210,32 @@ def draft_head(h, U, V, W, K, *, with_probs=True, idx_out=None, score_out=None, 
                              _ptr(score_out), _ptr(logits_out), _ptr(probs_out if with_probs else None),
                              _ptr(ws), nbytes, _stream(stream)), "dh_draft_head")
     return idx_out, score_out, logits_out, (probs_out if with_probs else None)
+
+
+def expand_children(probs, idx, w, *, parent_prob=None, min_benefit=0.0, child_token=None, child_prob=None,
+                    n_keep=None, stream=None):
+    """The w children of each frontier node by exact probability.  Returns (child_token int32
+    [B,w], child_prob fp32 [B,w], n_keep int32 [B])."""
+    lib = load_library()
+    _dev(probs, "probs"), _dev(idx, "idx")
+    if probs.dtype != torch.float32 or idx.dtype != torch.int32 or probs.shape != idx.shape:
+        raise ValueError("probs fp32 [B,K] and idx int32 [B,K]")
+    B, K = probs.shape
+    dev = probs.device
+    if parent_prob is not None:
+        _dev(parent_prob, "parent_prob")
+        if parent_prob.dtype != torch.float32 or parent_prob.shape != (B,):
+            raise ValueError("parent_prob must be fp32 [B]")
+    if child_token is None:
+        child_token = torch.empty(B, w, dtype=torch.int32, device=dev)
+    if child_prob is None:
+        child_prob = torch.empty(B, w, dtype=torch.float32, device=dev)
+    if n_keep is None:
+        n_keep = torch.empty(B, dtype=torch.int32, device=dev)
+    _check(lib.dh_expand_children(_ptr(probs), _ptr(idx), _ptr(parent_prob), B, K, w, float(min_benefit),
+                                  _ptr(child_token), _ptr(child_prob), _ptr(n_keep), _stream(stream)),
+           "dh_expand_children")
+    return child_token, child_prob, n_keep
 
 
 def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stream=None):

@@ -309,6 +309,21 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
                      reinterpret_cast<uint32_t*>(ws + roff), reinterpret_cast<int*>(ws));
 }
 
+// ------------------------------------------------------------------ expanding frontier nodes
+
+int dh_expand_children(const float* probs, const int32_t* idx, const float* parent_prob, int B, int K, int w,
+                       float min_benefit, int32_t* child_token, float* child_prob, int32_t* n_keep, void* stream) {
+  if (B < 0 || K < 1 || K > DH_MAX_K || w < 1 || w > K) return DH_ERR_INVALID_ARG;
+  if (B == 0) return DH_OK;
+  if (!probs || !idx || !child_token || !child_prob) return DH_ERR_INVALID_ARG;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (note_error(launch_expand(c, probs, idx, parent_prob, B, K, w, min_benefit, child_token, child_prob, n_keep),
+                 "expand") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
 // ------------------------------------------------------------------ tree acceptance
 
 size_t dh_tree_accept_workspace(int B, int N, int /*vocab*/) {

@@ -201,6 +201,10 @@ cudaError_t launch_head_cluster(const Ctx& c, const GroupRec* recs, unsigned lon
                                 const void* h, const void* W, int B, int d, int r, int vocab, int K, int dtype,
                                 int32_t* idx_out, float* score_out, float* logits, float* probs);
 
+cudaError_t launch_expand(const Ctx& c, const float* probs, const int32_t* idx, const float* parent_prob, int B,
+                          int K, int w, float min_benefit, int32_t* child_token, float* child_prob,
+                          int32_t* n_keep);
+
 bool rescore_supported(int d);
 bool rescore_ring_used(int B, int K, int d, int dtype);
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,

@@ -72,6 +72,8 @@ HEAD_CONFIGS = {
     "batch1": HeadConfig("batch1", 1, 5120, 151936, 128, 64, "bf16", 0.1, True),
     "moderate": HeadConfig("moderate", 64, 5120, 151936, 256, 128, "bf16", 0.1, True),
     "high": HeadConfig("high", 512, 5120, 151936, 512, 256, "bf16", 0.1, True),
+    # one draft level: eight frontier nodes through the head, then four children each
+    "level": HeadConfig("level", 8, 5120, 151936, 128, 64, "bf16", 0.1, True),
 }
 
 TREE_CONFIGS = {

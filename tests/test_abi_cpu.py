@@ -114,6 +114,21 @@ def test_draft_head_rejects_bad_arguments_on_host(lib):
     assert need % 256 == 0
 
 
+def test_expand_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = ctypes.c_float
+
+    def call(B=2, K=16, w=4, probs=FAKE, out=FAKE):
+        return lib.dh_expand_children(P(probs) if probs else None, P(FAKE), None, B, K, w, f(0.0),
+                                      P(out) if out else None, P(FAKE), None, None)
+    assert call(w=0) == 1
+    assert call(w=17) == 1        # more children than candidates
+    assert call(K=2048, w=4) == 1  # above DH_MAX_K
+    assert call(probs=0) == 1
+    assert call(out=0) == 1
+    assert call(B=0) == 0
+
+
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="libdh.so not found"):
         binding.load_library(str(tmp_path / "libdh.so"))

@@ -9,6 +9,7 @@ import oracle
 from speculative_decoding_draft_dh_gb300 import binding as dh
 from speculative_decoding_draft_dh_gb300 import inputs
 from tests.parity import check_candidates, check_logits
+from tests import test_oracle_pins as pins
 from tests.test_oracle_pins import golden_tree_arrays, load_golden_trees
 
 pytestmark = pytest.mark.gpu
@@ -442,3 +443,58 @@ def test_rescore_large_batch_with_repeats(path, monkeypatch):
     torch.cuda.synchronize()
     assert torch.equal(torch.nan_to_num(logits2), torch.nan_to_num(logits))
     assert torch.equal(torch.nan_to_num(probs2), torch.nan_to_num(probs))
+
+
+# ---------------------------------------------------------------- expanding frontier nodes
+
+@pytest.mark.parametrize("case", pins.load_golden_expansions(), ids=lambda c: c["name"])
+def test_expand_golden_on_gpu(case):
+    tok, cp, keep = dh.expand_children(torch.tensor([case["probs"]], dtype=torch.float32, device=DEV),
+                                       torch.tensor([case["tokens"]], dtype=torch.int32, device=DEV), case["w"],
+                                       parent_prob=torch.tensor([case["parent"]], dtype=torch.float32, device=DEV),
+                                       min_benefit=case["min_benefit"])
+    torch.cuda.synchronize()
+    assert tok[0].cpu().tolist() == case["expect_tokens"]
+    np.testing.assert_array_equal(cp[0].cpu().numpy(), np.array(case["expect_probs"], dtype=np.float32))
+    assert int(keep[0]) == case["expect_keep"]
+
+
+@pytest.mark.parametrize("K,w", [(1, 1), (17, 4), (64, 1), (64, 4), (64, 64), (256, 8), (1024, 32)])
+def test_expand_matches_oracle(K, w):
+    """Random probabilities with exact ties, a NaN row and repeated tokens: bit-exact against the
+    oracle (tokens, fp32 path probabilities, kept counts)."""
+    rng = np.random.default_rng(K * 7 + w)
+    B = 9
+    p = rng.dirichlet(np.ones(K), size=B).astype(np.float32)
+    if K > 3:
+        p[:, 1] = p[:, 3]
+        p[4, : K // 2] = p[4, 0]
+    p[6, K // 2] = np.nan
+    tok = rng.integers(0, 151936, size=(B, K)).astype(np.int32)
+    tok[5, :] = 42  # one token repeated: positions decide
+    par = rng.uniform(0.05, 1.0, size=B).astype(np.float32)
+    thr = float(np.float32(0.3 / K))
+    et, ep, ek = oracle.expand_children(p, tok, w, parent_prob=par, min_benefit=thr)
+    gt, gp, gk = dh.expand_children(torch.from_numpy(p).to(DEV), torch.from_numpy(tok).to(DEV), w,
+                                    parent_prob=torch.from_numpy(par).to(DEV), min_benefit=thr)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(gt.cpu().numpy(), et)
+    np.testing.assert_array_equal(gp.cpu().numpy(), ep)
+    np.testing.assert_array_equal(gk.cpu().numpy(), ek)
+
+
+def test_draft_level_step_matches_oracle():
+    """One draft level: the head's candidates and probabilities for every frontier node, then their
+    children; the expansion checked against the oracle on the GPU's own probabilities, the head as
+    in the other parity tests."""
+    cfg = inputs.head_config("tiny", B=4, K=16)
+    x = inputs.make_head(cfg, seed=33, device=DEV)
+    idx, score, logits, probs = run_head(x, cfg.K, api="head")
+    par = torch.tensor([1.0, 0.5, 0.25, 0.125], dtype=torch.float32, device=DEV)
+    tok, cp, keep = dh.expand_children(probs, idx, 4, parent_prob=par, min_benefit=0.01)
+    torch.cuda.synchronize()
+    et, ep, ek = oracle.expand_children(probs.cpu().numpy(), idx.cpu().numpy(), 4,
+                                        parent_prob=par.cpu().numpy(), min_benefit=0.01)
+    np.testing.assert_array_equal(tok.cpu().numpy(), et)
+    np.testing.assert_array_equal(cp.cpu().numpy(), ep)
+    np.testing.assert_array_equal(keep.cpu().numpy(), ek)
