@@ -77,65 +77,73 @@ struct ProjSmall {
 
 template <typename T>
 __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
-  __shared__ float red[PJ_GROUPS][MAX_BR / 4];  // per-group partials of this block's (b, j) chunk
+  constexpr int PAIRS = PJ_THREADS / PJ_GROUPS;  // column pairs per pass
+  __shared__ float red[PJ_GROUPS][MAX_B * 2 * PAIRS];  // per-group partials of this pass, [b][2 * pair]
   const T* h = static_cast<const T*>(p.h);
   const T* U = static_cast<const T*>(p.U);
   const int B = p.B, r = p.r, BR = B * r, npairs = r / 2;
   const int G = gridDim.x, c = blockIdx.x;
   const int i0 = (int)((long long)p.d * c / G), i1 = (int)((long long)p.d * (c + 1) / G);
   const int rows = i1 - i0;
-  const int grp = threadIdx.x / (PJ_THREADS / PJ_GROUPS);  // row group of this thread
-  const int lt = threadIdx.x % (PJ_THREADS / PJ_GROUPS);
+  const int grp = threadIdx.x / PAIRS;  // row group of this thread
+  const int lt = threadIdx.x % PAIRS;
   const int per_grp = (rows + PJ_GROUPS - 1) / PJ_GROUPS;
   const int g0 = i0 + grp * per_grp, g1 = min(i1, g0 + per_grp);
   bool triggered = false;
   // launched with programmatic dependent launch: h may come from the kernel before this one
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // work items: (b, column pair), PJ_THREADS / PJ_GROUPS per pass
-  for (int w0 = 0; w0 < B * npairs; w0 += PJ_THREADS / PJ_GROUPS) {
-    const int w = w0 + lt;
-    const int b = w / npairs, jp = w - (w / npairs) * npairs;
-    float a0 = 0.f, a1 = 0.f;
+  // each thread owns one column pair for every row of the batch, so U is read once
+  for (int jp0 = 0; jp0 < npairs; jp0 += PAIRS) {
+    const int jp = jp0 + lt;
+    const bool on = jp < npairs;
+    float a[MAX_B][2];
+#pragma unroll
+    for (int bb = 0; bb < MAX_B; ++bb) a[bb][0] = a[bb][1] = 0.f;
     for (int base = g0; base < g1; base += CH) {
       const int n = min(CH, g1 - base);
-      float u[CH][2], hv[CH];
-      if (w < B * npairs) {
+      float u[CH][2];
+      if (on) {
 #pragma unroll
-        for (int i = 0; i < CH; ++i) {
-          if (i < n) {
-            load_pair<T>(U + (size_t)(base + i) * r + 2 * jp, u[i][0], u[i][1]);
-            hv[i] = Elem<T>::to_f(h[(size_t)b * p.d + base + i]);
-          }
-        }
+        for (int i = 0; i < CH; ++i)
+          if (i < n) load_pair<T>(U + (size_t)(base + i) * r + 2 * jp, u[i][0], u[i][1]);
       }
-      if (!triggered) {  // U and h are in flight: the scores kernel may start streaming V
+      if (!triggered) {  // U is in flight: the scores kernel may start streaming V
         asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         triggered = true;
       }
-      if (w < B * npairs) {
+      if (on) {
 #pragma unroll
         for (int i = 0; i < CH; ++i) {
           if (i < n) {
-            a0 = fmaf(hv[i], u[i][0], a0);
-            a1 = fmaf(hv[i], u[i][1], a1);
+#pragma unroll
+            for (int bb = 0; bb < MAX_B; ++bb) {
+              if (bb < B) {
+                const float hv = Elem<T>::to_f(h[(size_t)bb * p.d + base + i]);
+                a[bb][0] = fmaf(hv, u[i][0], a[bb][0]);
+                a[bb][1] = fmaf(hv, u[i][1], a[bb][1]);
+              }
+            }
           }
         }
       }
     }
     // add the row groups' partials in a fixed order, then one integer atomic per (b, j)
-    if (w < B * npairs) {
-      red[grp][2 * lt] = a0;
-      red[grp][2 * lt + 1] = a1;
+#pragma unroll
+    for (int bb = 0; bb < MAX_B; ++bb) {
+      if (bb < B) {
+        red[grp][bb * 2 * PAIRS + 2 * lt] = a[bb][0];
+        red[grp][bb * 2 * PAIRS + 2 * lt + 1] = a[bb][1];
+      }
     }
     __syncthreads();
-    if (threadIdx.x < 2 * (PJ_THREADS / PJ_GROUPS)) {
-      const int e = 2 * w0 + threadIdx.x;  // == b * r + j for the pass's pairs
-      if (e < BR) {
+    for (int q2 = threadIdx.x; q2 < B * 2 * PAIRS; q2 += PJ_THREADS) {
+      const int bb = q2 / (2 * PAIRS), jj = 2 * jp0 + (q2 % (2 * PAIRS));
+      if (jj < r) {
         float v = 0.f;
 #pragma unroll
-        for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][threadIdx.x];
+        for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][q2];
         const long long fx = __float2ll_rn(v * FIX_SCALE);
-        atomicAdd(p.acc + (size_t)(c % ACC_COPIES) * BR + e, (unsigned long long)fx);
+        atomicAdd(p.acc + (size_t)(c % ACC_COPIES) * BR + bb * r + jj, (unsigned long long)fx);
       }
     }
     __syncthreads();

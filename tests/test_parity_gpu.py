@@ -339,7 +339,12 @@ def test_batch1_forced_gemv(monkeypatch):
     run_head(x, cfg.K)
 
 
-def test_fused_path_batch8_bf16_full_vocab():
+@pytest.mark.parametrize("path", ["fused", "auto"])
+def test_fused_path_batch8_bf16_full_vocab(path, monkeypatch):
+    """Eight rows at full size: the small-batch pipeline (forced) and the automatic choice (the
+    tensor-core path from five rows on)."""
+    if path == "fused":
+        monkeypatch.setenv("DH_FORCE_PATH", "fused")
     cfg = inputs.HeadConfig("b8", 8, 5120, 151936, 256, 64, "bf16", 0.1, True)
     x = inputs.make_head(cfg, seed=3, device=DEV)
     run_head(x, cfg.K, rows=[0, 7])
