@@ -135,6 +135,23 @@ template <> struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
 };
 
+// Softmax over z[0..K) by one warp (lane i takes elements i, i + 32, ...; max and sum by xor
+// shuffles, so every lane gets the same values): out[k] = exp(z[k] - max) / sum.  For the small
+// K of the cluster kernels this avoids a block barrier per reduction.
+__device__ __forceinline__ void warp_softmax(const float* z, int K, float* out) {
+  const int lane = threadIdx.x & 31;
+  float m = -INFINITY;
+  for (int i = lane; i < K; i += 32) m = fmaxf(m, z[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+  float ssum = 0.f;
+  for (int i = lane; i < K; i += 32) ssum += expf(z[i] - m);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+  const float inv = 1.f / ssum;
+  for (int i = lane; i < K; i += 32) out[i] = expf(z[i] - m) * inv;
+}
+
 // Element e of t from the fixed-point accumulator copies (copy q at acc + q*BR), rounded to the
 // activation dtype.  The integer sum is exact and order independent, so every reader derives the
 // same t.  Read through L2 (the copies were written by atomics).

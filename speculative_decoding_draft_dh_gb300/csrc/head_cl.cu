@@ -325,37 +325,8 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     }
   }
   cluster_sync_all();
-  if (!leader || !p.probs) return;
-  __shared__ float red[HC_WARPS];
-  __shared__ float s_bcast;
-  float m = -INFINITY;
-  for (int i = threadIdx.x; i < K; i += HC_THREADS) m = fmaxf(m, my.z[i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int i = 1; i < HC_WARPS; ++i) mm = fmaxf(mm, red[i]);
-    s_bcast = mm;
-  }
-  __syncthreads();
-  m = s_bcast;
-  float ssum = 0.f;
-  for (int i = threadIdx.x; i < K; i += HC_THREADS) ssum += expf(my.z[i] - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = ssum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < HC_WARPS; ++i) tot += red[i];
-    s_bcast = 1.f / tot;
-  }
-  __syncthreads();
-  const float inv = s_bcast;
-  for (int i = threadIdx.x; i < K; i += HC_THREADS) p.probs[(size_t)b * K + i] = expf(my.z[i] - m) * inv;
+  if (!leader || !p.probs || warp != 0) return;
+  warp_softmax(my.z, K, p.probs + (size_t)b * K);
 }
 
 template <typename T>

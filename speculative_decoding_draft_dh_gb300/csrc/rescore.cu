@@ -132,8 +132,8 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h,
 // Cluster variant for small batches with K <= CL_MAX_K: one thread-block cluster of up to 8 CTAs
 // per row; warp w of cluster CTA c scores candidates c*NWARP + w, c*NWARP + w + CTAs*NWARP, ...
 // Each warp also stores its logit into the leader CTA's shared memory (distributed shared
-// memory); after a cluster barrier the leader computes the row's softmax from there, without
-// the global ticket and the L2 round trips of the ticket scheme.  Every CTA passes both cluster
+// memory); after a cluster barrier one warp of the leader computes the row's softmax from there,
+// without the global ticket and the L2 round trips of the ticket scheme.  Every CTA passes both cluster
 // barriers (no early exit), so the barriers always complete.
 constexpr int CL_MAX_K = 128;
 constexpr int CL_MAX_CTAS = 8;
@@ -163,8 +163,6 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore_cl(const T* __restrict__
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* sh_h = reinterpret_cast<T*>(smem_raw);
   __shared__ float s_z[CL_MAX_K];  // leader CTA: the row's logits
-  __shared__ float red[NWARP];
-  __shared__ float s_bcast;
   const uint32_t crank = cluster_ctarank(), csize = cluster_nctarank();
   const int b = (int)(blockIdx.x / csize);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -190,35 +188,8 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore_cl(const T* __restrict__
   // phase 2: the leader sees every logit of the row
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  if (crank != 0 || !probs) return;
-  float m = -INFINITY;
-  for (int i = threadIdx.x; i < K; i += NWARP * 32) m = fmaxf(m, s_z[i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int i = 1; i < NWARP; ++i) mm = fmaxf(mm, red[i]);
-    s_bcast = mm;
-  }
-  __syncthreads();
-  m = s_bcast;
-  float ssum = 0.f;
-  for (int i = threadIdx.x; i < K; i += NWARP * 32) ssum += expf(s_z[i] - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = ssum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < NWARP; ++i) tot += red[i];
-    s_bcast = 1.f / tot;
-  }
-  __syncthreads();
-  const float inv = s_bcast;
-  for (int i = threadIdx.x; i < K; i += NWARP * 32) probs[(size_t)b * K + i] = expf(s_z[i] - m) * inv;
+  if (crank != 0 || !probs || warp != 0) return;
+  warp_softmax(s_z, K, probs + (size_t)b * K);
 }
 
 template <typename T, int NWARP>

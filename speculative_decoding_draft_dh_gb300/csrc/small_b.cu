@@ -353,6 +353,8 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
     }
   }
   __syncwarp();
+  // the selection kernel may launch now (it waits for this grid's records itself)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // t comes from the projection kernel
   for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = acc_to_t<T>(p.acc, BR, e);
   __syncthreads();
