@@ -16,6 +16,12 @@
 //   warps 2-9  epilogue: tcgen05.ld 32x32b (thread = row); two warps per TMEM lane quarter, each
 //              owning two of the tile's four 64-id groups; branch-free per-group top-two + third
 //              score; one 16-byte record store per (row, group).
+// With at most 64 rows of T (one row tile), the A tile holds 2 or 4 copies of T's rows, so the
+// MMA computes every score 2 or 4 times over the lane quarters.  A warp can read only its own lane
+// quarter of TMEM, so with one copy all of a small batch's folding would fall on the two warps of
+// one quarter; with copies, each copy folds a different share of the tile's groups and the two
+// warps of a quarter take alternate tiles.  The tensor cores have time to spare at these sizes;
+// the epilogue does not.
 // Every mbarrier wait gives up after two seconds and raises DH_ERR_TIMEOUT in the status word;
 // the CTA then drains its outstanding copies and MMAs (again with bounded waits) and frees TMEM.
 #include "dh_internal.cuh"
@@ -40,6 +46,7 @@ constexpr int MAX_STAGES = 8;
 
 struct MmaParams {
   int B, r, vocab, n_groups, n_tiles, n_split, stages;
+  int rep;  // copies of T's rows in the 128-row A tile (1, 2 or 4; see the epilogue)
   GroupRec* recs;
   int* status;
 };
@@ -85,7 +92,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_empty[i], EPI_WARPS);
+      mbar_init(&acc_empty[i], p.rep == 1 ? EPI_WARPS : EPI_WARPS / 2);  // the warps that take the tile
     }
     fence_barrier_init();
   }
@@ -108,7 +115,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       auto issue_a = [&]() {
         asm volatile("griddepcontrol.wait;" ::: "memory");
         mbar_arrive_expect_tx(a_full, (uint32_t)(nkc * A_CHUNK_BYTES));
-        for (int kc = 0; kc < nkc; ++kc) tma_load_2d(sA + kc * A_CHUNK_BYTES, &tmA, kc * BK, m * BM, a_full);
+        // rep copies of T's first BM / rep rows, one per BM / rep smem rows (128 bytes per row)
+        const int rows_rep = BM / p.rep;
+        for (int kc = 0; kc < nkc; ++kc)
+          for (int q = 0; q < p.rep; ++q)
+            tma_load_2d(sA + kc * A_CHUNK_BYTES + q * rows_rep * 128, &tmA, kc * BK, m * BM, a_full);
         a_issued = true;
       };
       uint32_t issued_parity = 0;  // bit s: parity of the last load issued into stage s
@@ -177,10 +188,18 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue (warps 2-9)
     const int q = warp & 3;             // TMEM lanes [32q, 32q + 32) are accessible to this warp
-    const int half = (warp - 2) >> 2;   // groups 2*half and 2*half + 1 of each tile
-    const int row = m * BM + q * 32 + lane;
+    const int half = (warp - 2) >> 2;
+    // rep = 1: every tile, groups 2*half and 2*half + 1.  rep > 1 (one row tile holding rep copies
+    // of T's rows): the lane quarters of copy c take groups [c*4/rep, (c+1)*4/rep) and the two
+    // halves take alternate tiles, so each warp folds 4/rep times fewer scores per tile.
+    const int rows_rep = BM / p.rep;
+    const int copy = (q * 32) / rows_rep;
+    const int row = m * BM + (q * 32) % rows_rep + lane;
+    const int n_g = p.rep == 1 ? 2 : 4 / p.rep;
+    const int g_first = p.rep == 1 ? 2 * half : copy * n_g;
+    const int t_first = p.rep == 1 ? 0 : half, t_step = p.rep == 1 ? 1 : 2;
     const uint32_t lane_addr = tmem + ((uint32_t)(q * 32) << 16);
-    for (int t = 0; t < ntiles; ++t) {
+    for (int t = t_first; t < ntiles; t += t_step) {
       const int buf = t & 1;
       const uint32_t acc_ph = (uint32_t)(t >> 1) & 1u;
       // warp-uniform outcome: the TMEM loads below are .sync.aligned and need the whole warp
@@ -191,8 +210,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       tc_fence_after();
       const int n0 = (nt0 + t) * BN;
 #pragma unroll 1
-      for (int gg = 0; gg < 2; ++gg) {
-        const int g = half * 2 + gg;
+      for (int gg = 0; gg < n_g; ++gg) {
+        const int g = g_first + gg;
         const int gc0 = n0 + g * GROUP;
         Top2 sm;
         sm.init();
@@ -490,8 +509,11 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   if (stages < 2) return note_error(cudaErrorInvalidConfiguration, "lowrank_mma: shared memory for 2 stages");
   const size_t smem = 1024 + (size_t)nkc * A_CHUNK_BYTES + (size_t)stages * B_STAGE_BYTES;
 
+  const int num_m = (B + BM - 1) / BM;
+  // one row tile: replicate T's rows over the lane quarters (see the epilogue)
+  const int rep = num_m == 1 && B <= BM / 4 ? 4 : (num_m == 1 && B <= BM / 2 ? 2 : 1);
   CUtensorMap tmA, tmB;
-  if (!make_map(&tmA, t, (uint64_t)r, (uint64_t)B, BK, BM))
+  if (!make_map(&tmA, t, (uint64_t)r, (uint64_t)B, BK, BM / rep))
     return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(T)");
   if (!make_map(&tmB, V, (uint64_t)vocab, (uint64_t)r, 64, BK))
     return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(V)");
@@ -502,8 +524,8 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   p.vocab = vocab;
   p.n_groups = (vocab + GROUP - 1) / GROUP;
   p.n_tiles = (vocab + BN - 1) / BN;
-  const int num_m = (B + BM - 1) / BM;
   p.n_split = max(1, min(p.n_tiles, c.num_sms / num_m));
+  p.rep = rep;
   p.stages = stages;
   p.recs = recs;
   p.status = status;
