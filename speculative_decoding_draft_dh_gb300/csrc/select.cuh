@@ -401,24 +401,28 @@ __device__ __forceinline__ void load4<float>(const float* p, float* x) {
   x[3] = u.w;
 }
 
-// Exact scores of the 64 ids of group g (ids >= vocab give -inf) into out[0..64).  The r rows of
-// V are split over SG_PARTS parts (part w covers rows [w*rw, (w+1)*rw)); the block's warps take
-// the parts in turn, two rows per instruction (lanes 0-15 the even rows, 16-31 the odd ones; lane i
-// loads ids 4(i mod 16) .. +3), with up to 16 loads per lane in flight.  The two halves are added
-// with one shuffle, then the parts' partial sums in part order: a fixed order whatever the block
-// size, so blocks of 256 and 512 threads give the same scores.
-// scratch: SG_PARTS * 64 floats.  vocab is a multiple of 4.
+// Exact scores of the 64 ids of each of the n groups gs[0..n) (ids >= vocab give -inf) into
+// out[i*64 .. i*64 + 64), n <= SG_BATCH.  The r rows of V are split over SG_PARTS parts (part w
+// covers rows [w*rw, (w+1)*rw)); the block's warps take the (group, part) items in turn, so the
+// loads of every group are in flight together, two rows per instruction (lanes 0-15 the even rows,
+// 16-31 the odd ones; lane i loads ids 4(i mod 16) .. +3), up to 16 loads per lane.  The two halves
+// are added with one shuffle, then each group's parts in part order: a fixed order whatever the
+// block size, so blocks of 256 and 512 threads give the same scores.
+// scratch: SG_BATCH * SG_PARTS * 64 floats.  vocab is a multiple of 4.
 constexpr int SG_PARTS = 16;
+constexpr int SG_BATCH = 4;
+static_assert(SG_BATCH * SG_PARTS * 64 <= HIST_BINS, "the scratch is the histogram area");
 
 template <typename T>
-__device__ void score_group(const float* t, const T* __restrict__ V, int r, int vocab, int g, float* out,
-                            float* scratch) {
+__device__ void score_groups(const float* t, const T* __restrict__ V, int r, int vocab, const int32_t* gs, int n,
+                             float* out, float* scratch) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
   const int rw = (r + SG_PARTS - 1) / SG_PARTS;
   const int half = lane >> 4;
-  const int c = g * GROUP + 4 * (lane & 15);
-  const bool cok = c < vocab;
-  for (int part = warp; part < SG_PARTS; part += nw) {
+  for (int item = warp; item < n * SG_PARTS; item += nw) {
+    const int gi = item / SG_PARTS, part = item % SG_PARTS;
+    const int c = gs[gi] * GROUP + 4 * (lane & 15);
+    const bool cok = c < vocab;
     const int j0 = part * rw, j1 = min(r, j0 + rw);
     float a[4] = {0.f, 0.f, 0.f, 0.f};
     constexpr int BATCH = 16;
@@ -445,14 +449,15 @@ __device__ void score_group(const float* t, const T* __restrict__ V, int r, int 
     for (int e = 0; e < 4; ++e) a[e] += __shfl_xor_sync(0xFFFFFFFFu, a[e], 16);
     if (lane < 16) {
 #pragma unroll
-      for (int e = 0; e < 4; ++e) scratch[part * 64 + 4 * lane + e] = a[e];
+      for (int e = 0; e < 4; ++e) scratch[item * 64 + 4 * lane + e] = a[e];
     }
   }
   __syncthreads();
-  if (threadIdx.x < 64) {
-    float s = 0.f;
-    for (int w = 0; w < SG_PARTS; ++w) s += scratch[w * 64 + threadIdx.x];
-    out[threadIdx.x] = (g * GROUP + (int)threadIdx.x < vocab) ? s : -INFINITY;
+  for (int e = threadIdx.x; e < n * 64; e += blockDim.x) {
+    const int gi = e / 64, col = e % 64;
+    float sum = 0.f;
+    for (int w = 0; w < SG_PARTS; ++w) sum += scratch[(gi * SG_PARTS + w) * 64 + col];
+    out[e] = (gs[gi] * GROUP + col < vocab) ? sum : -INFINITY;
   }
   __syncthreads();
 }
@@ -563,8 +568,9 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
     const int nref = (int)sh.nref;
     if (nref == 0) return;
     if (nref <= RMAX) {
-      for (int i = 0; i < nref; ++i)
-        score_group(sh.t, V, r, vocab, sh.rg[i], sh.rs + i * GROUP, reinterpret_cast<float*>(sh.hist));
+      for (int i = 0; i < nref; i += SG_BATCH)
+        score_groups(sh.t, V, r, vocab, sh.rg + i, min(SG_BATCH, nref - i), sh.rs + i * GROUP,
+                     reinterpret_cast<float*>(sh.hist));
       // Candidates: the K selected pool entries outside the refined groups (sh.sk/si still hold the
       // selection) and the refined groups' members at or above tau.  Every entry of the exact top-K
       // is among them; when they number at least K (always, unless re-scoring moved a selected
