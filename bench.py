@@ -52,7 +52,7 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree", "level"])
-    ap.add_argument("--api", default="split", choices=["head", "split"],
+    ap.add_argument("--api", default="head", choices=["head", "split"],
                     help="head: dh_draft_head (both stages in one call); split: dh_lowrank_topk + "
                          "dh_exact_rescore")
     ap.add_argument("--seed", type=int, default=0)

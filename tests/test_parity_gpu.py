@@ -194,12 +194,16 @@ def test_batch1_full_size(api):
     run_head(x, cfg.K, api=api)
 
 
-@pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64)])
-def test_draft_head_matches_the_two_calls(name, B):
-    """dh_draft_head (the fused cluster kernel for small batches, the two-call sequence otherwise)
-    gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same selection rule on
-    the same records and the same per-candidate dot product order; twice in a row with one
-    workspace (its state resets itself)."""
+@pytest.mark.parametrize("mode", ["auto", "cluster"])
+@pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
+                                    ("high", 512)])
+def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
+    """dh_draft_head gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same
+    selection rule on the same records and the same per-candidate dot product order; twice in a
+    row with one workspace (its state resets itself).  "cluster" takes the fused cluster kernel
+    (selection and rescoring in one launch) where the batch is small enough."""
+    if mode != "auto":
+        monkeypatch.setenv("DH_FORCE_HEAD", mode)
     cfg = inputs.head_config(name, B=B)
     x = inputs.make_head(cfg, seed=11, device=DEV)
     h, U, V, W = x["h"], x["U"], x["V"], x["W"]
@@ -233,10 +237,11 @@ def test_moderate_load_sampled_rows():
     run_head(x, cfg.K, rows=[0, 1, 17, 42, 63])
 
 
-def test_high_load_sampled_rows():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_high_load_sampled_rows(api):
     cfg = inputs.HEAD_CONFIGS["high"]
     x = inputs.make_head(cfg, seed=0, device=DEV)
-    run_head(x, cfg.K, rows=[0, 255, 511])
+    run_head(x, cfg.K, rows=[0, 151, 152, 255, 303, 304, 511], api=api)
 
 
 # ---------------------------------------------------------------- trees
