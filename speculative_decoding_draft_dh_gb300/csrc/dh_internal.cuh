@@ -65,14 +65,21 @@ struct Top2 {
     v1 = v2 = v3 = -INFINITY;
     i1 = i2 = 0xFFFFFFFFu;
   }
-  // Pairs must arrive in increasing id order for ties to keep the lower id.  Branch-free (three
-  // compares and selects), so the lanes of a warp never diverge on their data.
+  // Pairs must arrive in increasing id order for ties to keep the lower id.  Branch-free, so the
+  // lanes of a warp never diverge on their data: the three values by a min/max insertion network,
+  // the two ids by two compares.  A NaN x changes nothing: it fails both compares, the inner
+  // minima propagate it and the outer maxima then keep the stored values.
+  __device__ __forceinline__ static float min_nan(float a, float b) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
+    return r;
+  }
   __device__ __forceinline__ void push(float x, uint32_t id) {
-    const bool c1 = x > v1, c2 = x > v2, c3 = x > v3;
-    v3 = c2 ? v2 : (c3 ? x : v3);
-    v2 = c1 ? v1 : (c2 ? x : v2);
+    const bool c1 = x > v1, c2 = x > v2;
+    v3 = fmaxf(v3, min_nan(v2, x));
+    v2 = fmaxf(v2, min_nan(v1, x));
     i2 = c1 ? i1 : (c2 ? id : i2);
-    v1 = c1 ? x : v1;
+    v1 = fmaxf(v1, x);
     i1 = c1 ? id : i1;
   }
   // Merge with another summary of a disjoint set of ids.
