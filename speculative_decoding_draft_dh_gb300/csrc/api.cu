@@ -291,11 +291,11 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  // DH_FORCE_HEAD=cluster: for small batches, selection and rescoring in one cluster kernel (no
-  // faster than the two kernels, so not the default)
+  // small batches: the scores kernels, then selection and rescoring in one cluster kernel
+  // (DH_FORCE_HEAD=split: the selection and rescoring kernels instead)
   const char* f = std::getenv("DH_FORCE_HEAD");
-  const bool cluster = f && std::strcmp(f, "cluster") == 0;
-  if (cluster && choose_path(B, r, dtype) == PATH_FUSED && head_cluster_supported(B, d, vocab, K, dtype)) {
+  const bool split = f && std::strcmp(f, "split") == 0;
+  if (!split && choose_path(B, r, dtype) == PATH_FUSED && head_cluster_supported(B, d, vocab, K, dtype)) {
     unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
     GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
     if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)

@@ -10,9 +10,10 @@
 //
 // k_expand: one block per node.  Every candidate's rank is counted against the others in the order
 // (probability desc, token asc, position asc), with a NaN probability below every number; P threads
-// share a candidate and add their counts with shuffles.  Candidate of rank c < w becomes child c:
-// its token, and its path probability parent x p rounded once to fp32.  n_keep counts the children
-// whose path probability is strictly above min_benefit, which is always a prefix.
+// share a candidate (interleaved over the others) and add their counts with shuffles.  Candidate
+// of rank c < w becomes child c: its token, and its path probability parent x p rounded once to
+// fp32.  n_keep counts the children whose path probability is strictly above min_benefit, which
+// is always a prefix.
 #include "dh_internal.cuh"
 
 namespace dh {
@@ -42,7 +43,6 @@ __global__ void __launch_bounds__(EX_THREADS) k_expand(const float* __restrict__
   const float par = parent_prob ? parent_prob[b] : 1.0f;
   int P = 1;
   while (P < 32 && K * (2 * P) <= EX_THREADS) P <<= 1;
-  const int per = (K + P - 1) / P;
   for (int base = 0; base < K * P; base += EX_THREADS) {
     const int t = base + (int)threadIdx.x;
     const int i = t / P, h = t % P;
@@ -50,8 +50,8 @@ __global__ void __launch_bounds__(EX_THREADS) k_expand(const float* __restrict__
     if (i < K) {
       const uint32_t ki = sk[i];
       const int32_t ti = st[i];
-      const int j1 = min(K, (h + 1) * per);
-      for (int j = h * per; j < j1; ++j) {
+      // thread h counts over j = h, h + P, ...: the P threads of a candidate read consecutive words
+      for (int j = h; j < K; j += P) {
         const uint32_t kj = sk[j];
         const int32_t tj = st[j];
         rank += (kj > ki || (kj == ki && (tj < ti || (tj == ti && j < i)))) ? 1 : 0;

@@ -242,18 +242,11 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
       __syncthreads();
       int P = 1;
       while (P < 32 && K * (2 * P) <= HC_THREADS) P <<= 1;
-      const int per = (K + P - 1) / P;
       for (int base = 0; base < K * P; base += HC_THREADS) {
         const int t = base + (int)threadIdx.x;
         const int i = t / P, hh = t % P;
-        int rank = 0;
-        unsigned long long pi = 0;
-        if (i < K) {
-          pi = my.sp[i];
-          const int j1 = min(K, (hh + 1) * per);
-          for (int j = hh * per; j < j1; ++j) rank += my.sp[j] > pi ? 1 : 0;
-        }
-        for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+        unsigned long long pi;
+        const int rank = sel::rank_by_count(my.sp, K, P, i, hh, &pi);
         if (i < K && hh == 0) {
           const uint32_t kk = (uint32_t)(pi >> 32);
           p.idx_out[(size_t)b * K + rank] = (int32_t)(~(uint32_t)pi);

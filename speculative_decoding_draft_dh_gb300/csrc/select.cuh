@@ -144,11 +144,6 @@ __device__ Kth radix_kth(Enum en, Sel sel, uint32_t k, Shared& sh) {
   return res;
 }
 
-// (key, id) ranks before (key2, id2): larger key first, then smaller id.
-__device__ __forceinline__ bool key_before(uint32_t ka, uint32_t ia, uint32_t kb, uint32_t ib) {
-  return ka > kb || (ka == kb && ia < ib);
-}
-
 // Appends for the lanes whose pred is set: returns each such lane's position in the list whose
 // length is *counter (one shared atomic per warp).  Called by all 32 lanes of the warp.
 __device__ __forceinline__ uint32_t warp_append(bool pred, uint32_t* counter) {
@@ -160,11 +155,33 @@ __device__ __forceinline__ uint32_t warp_append(bool pred, uint32_t* counter) {
   return base + (uint32_t)__popc(b & ((1u << lane) - 1u));
 }
 
+// Rank of entry i among sp[0..K) by counting (the number of larger packed values), with P threads
+// per entry: thread h of the entry counts over j = h, h + P, h + 2P, ... (the P threads of an
+// entry read consecutive words, so their loads do not collide in a shared-memory bank), and the
+// P partial counts are added with shuffles.  Every thread of the warp takes part.
+__device__ __forceinline__ int rank_by_count(const unsigned long long* sp, int K, int P, int i, int h,
+                                             unsigned long long* pi_out) {
+  int rank = 0;
+  unsigned long long pi = 0;
+  if (i < K) {
+    pi = sp[i];
+    if (K <= 8 * P) {  // at most 8 steps: a plain loop measured faster than an unrolled one
+      for (int j = h; j < K; j += P) rank += sp[j] > pi ? 1 : 0;
+    } else {
+#pragma unroll 8
+      for (int j = h; j < K; j += P) rank += sp[j] > pi ? 1 : 0;
+    }
+  }
+  for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+  *pi_out = pi;
+  return rank;
+}
+
 // Sorts sh.sk/sh.si[0..K) into ranking order by counting: with (key, id) packed as
 // key << 32 | ~id (ranking order = descending packed value; ids are unique, so the packed values
 // are distinct), an entry's rank is the number of entries with a larger packed value.  P threads
-// share an entry (P = the largest power of two <= 32 with K * P <= blockDim.x), each counting over
-// K / P of the entries, and add their counts with shuffles.  Uses sh.hist as scratch.
+// share an entry (P = the largest power of two <= 32 with K * P <= blockDim.x).  Uses sh.hist as
+// scratch.
 __device__ inline void sort_selected(Shared& sh, int K) {
   unsigned long long* sp = reinterpret_cast<unsigned long long*>(sh.hist);  // K <= DH_MAX_K entries
   for (int i = threadIdx.x; i < K; i += blockDim.x)
@@ -172,18 +189,11 @@ __device__ inline void sort_selected(Shared& sh, int K) {
   __syncthreads();
   int P = 1;
   while (P < 32 && K * (2 * P) <= (int)blockDim.x) P <<= 1;
-  const int per = (K + P - 1) / P;
   for (int base = 0; base < K * P; base += blockDim.x) {
     const int t = base + (int)threadIdx.x;
     const int i = t / P, h = t % P;
-    int rank = 0;
-    unsigned long long pi = 0;
-    if (i < K) {
-      pi = sp[i];
-      const int j1 = min(K, (h + 1) * per);
-      for (int j = h * per; j < j1; ++j) rank += sp[j] > pi ? 1 : 0;
-    }
-    for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    unsigned long long pi;
+    const int rank = rank_by_count(sp, K, P, i, h, &pi);
     if (i < K && h == 0) {
       sh.sk[rank] = (uint32_t)(pi >> 32);
       sh.si[rank] = ~(uint32_t)pi;
@@ -335,29 +345,27 @@ __device__ bool fast_select(Load load, int n_entries_max, int K, Shared& sh, int
   // the boundary entries ranking below the first K - above of the bin are dropped; the others go
   // after the entries above the bin (their rank among the bin's entries is unique)
   const int need = K - (int)above;
-  for (int i = threadIdx.x; i < (int)bc; i += blockDim.x) {
-    const unsigned long long pi = bp[i];
-    int rank = 0;
-    for (int j = 0; j < (int)bc; ++j) rank += bp[j] > pi ? 1 : 0;
-    if (rank < need) sp[above + rank] = pi;
+  {
+    int P = 1;
+    while (P < 32 && (int)bc * (2 * P) <= (int)blockDim.x) P <<= 1;
+    for (int base = 0; base < (int)bc * P; base += blockDim.x) {
+      const int t = base + (int)threadIdx.x;
+      const int i = t / P, h = t % P;
+      unsigned long long pi;
+      const int rank = rank_by_count(bp, (int)bc, P, i, h, &pi);
+      if (i < (int)bc && h == 0 && rank < need) sp[above + rank] = pi;
+    }
   }
   __syncthreads();
   // rank the K winners by counting (P threads per entry, partial counts added with shuffles) and
   // write them out in order
   int P = 1;
   while (P < 32 && K * (2 * P) <= (int)blockDim.x) P <<= 1;
-  const int per = (K + P - 1) / P;
   for (int base = 0; base < K * P; base += blockDim.x) {
     const int t = base + (int)threadIdx.x;
     const int i = t / P, h = t % P;
-    int rank = 0;
-    unsigned long long pi = 0;
-    if (i < K) {
-      pi = sp[i];
-      const int j1 = min(K, (h + 1) * per);
-      for (int j = h * per; j < j1; ++j) rank += sp[j] > pi ? 1 : 0;
-    }
-    for (int o = 1; o < P; o <<= 1) rank += __shfl_xor_sync(0xFFFFFFFFu, rank, o);
+    unsigned long long pi;
+    const int rank = rank_by_count(sp, K, P, i, h, &pi);
     if (i < K && h == 0) {
       const uint32_t kk = (uint32_t)(pi >> 32), ii = ~(uint32_t)pi;
       idx_out[rank] = (int32_t)ii;
@@ -575,8 +583,8 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
       // selection) and the refined groups' members at or above tau.  Every entry of the exact top-K
       // is among them; when they number at least K (always, unless re-scoring moved a selected
       // score below tau by rounding) the top K by rank counting is the result.
-      uint32_t* ck = sh.hist;
-      uint32_t* ci = sh.hist + HIST_BINS / 2;
+      unsigned long long* cp = reinterpret_cast<unsigned long long*>(sh.hist);  // packed candidates
+      constexpr int CMAX = HIST_BINS / 2;
       if (threadIdx.x == 0) sh.cnt = 0;
       __syncthreads();
       for (int k0 = 0; k0 < K; k0 += blockDim.x) {
@@ -587,10 +595,7 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
           take = !((sh.bitmap[g >> 5] >> (g & 31)) & 1u);
         }
         const uint32_t pos = warp_append(take, &sh.cnt);
-        if (take) {
-          ck[pos] = sh.sk[k];
-          ci[pos] = sh.si[k];
-        }
+        if (take) cp[pos] = pack_entry(sh.sk[k], sh.si[k]);
       }
       for (int e0 = 0; e0 < nref * GROUP; e0 += blockDim.x) {
         const int e = e0 + threadIdx.x;
@@ -603,19 +608,23 @@ __device__ void select_row(unsigned char* smem, const GroupRec* __restrict__ rro
           take = c < vocab && key >= tau;
         }
         const uint32_t pos = warp_append(take, &sh.cnt);
-        if (take && pos < HIST_BINS / 2) { ck[pos] = key; ci[pos] = (uint32_t)c; }
+        if (take && pos < CMAX) cp[pos] = pack_entry(key, (uint32_t)c);
       }
       __syncthreads();
       const int n = (int)sh.cnt;
       __syncthreads();
-      if (n >= K && n <= HIST_BINS / 2) {
-        for (int i = threadIdx.x; i < n; i += blockDim.x) {
-          const uint32_t ki = ck[i], ii = ci[i];
-          int rank = 0;
-          for (int j = 0; j < n; ++j) rank += key_before(ck[j], ci[j], ki, ii) ? 1 : 0;
-          if (rank < K) {
-            idx_out[rank] = (int32_t)ii;
-            score_out[rank] = fkey_inv(ki);
+      if (n >= K && n <= CMAX) {
+        // rank every candidate among the n by counting, P threads per candidate
+        int P = 1;
+        while (P < 32 && n * (2 * P) <= (int)blockDim.x) P <<= 1;
+        for (int base = 0; base < n * P; base += blockDim.x) {
+          const int t = base + (int)threadIdx.x;
+          const int i = t / P, h = t % P;
+          unsigned long long pi;
+          const int rank = rank_by_count(cp, n, P, i, h, &pi);
+          if (i < n && h == 0 && rank < K) {
+            idx_out[rank] = (int32_t)(~(uint32_t)pi);
+            score_out[rank] = fkey_inv((uint32_t)(pi >> 32));
           }
         }
         return;

@@ -194,14 +194,15 @@ def test_batch1_full_size(api):
     run_head(x, cfg.K, api=api)
 
 
-@pytest.mark.parametrize("mode", ["auto", "cluster"])
+@pytest.mark.parametrize("mode", ["auto", "cluster", "split"])
 @pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
                                     ("high", 512)])
 def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
     """dh_draft_head gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same
     selection rule on the same records and the same per-candidate dot product order; twice in a
-    row with one workspace (its state resets itself).  "cluster" takes the fused cluster kernel
-    (selection and rescoring in one launch) where the batch is small enough."""
+    row with one workspace (its state resets itself).  "cluster" forces the fused cluster kernel
+    (selection and rescoring in one launch) where the batch is small enough, "split" the two
+    kernels."""
     if mode != "auto":
         monkeypatch.setenv("DH_FORCE_HEAD", mode)
     cfg = inputs.head_config(name, B=B)
@@ -218,6 +219,22 @@ def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
         assert torch.equal(l2, logits)
         assert torch.equal(p2, probs)
     assert dh.workspace_status(ws) == 0
+
+
+@pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
+def test_fused_head_matches_the_two_calls_over_K(K, monkeypatch):
+    """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
+    of candidates per CTA, and beyond one candidate per warp)."""
+    monkeypatch.setenv("DH_FORCE_HEAD", "cluster")
+    cfg = inputs.head_config("tiny", B=3, K=K)
+    x = inputs.make_head(cfg, seed=21, device=DEV)
+    h, U, V, W = x["h"], x["U"], x["V"], x["W"]
+    idx, score = dh.lowrank_topk(h, U, V, K)
+    logits, probs = dh.exact_rescore(h, W, idx)
+    i2, s2, l2, p2 = dh.draft_head(h, U, V, W, K)
+    torch.cuda.synchronize()
+    assert torch.equal(i2, idx) and torch.equal(s2, score)
+    assert torch.equal(l2, logits) and torch.equal(p2, probs)
 
 
 def test_draft_head_without_probs_and_bad_rows():
