@@ -48,9 +48,12 @@ struct HeadCtl {
   uint32_t digit, run, bincount, total;
   uint32_t n_above, n_bound, nref, tau_key;
   uint32_t wmin[HC_WARPS], wmax[HC_WARPS];
-  alignas(16) unsigned long long sp[HC_MAX_K];  // the K winners, packed key << 32 | ~id
+  alignas(16) unsigned long long sp[HC_MAX_K];  // the K winners, packed key << 32 | ~id (unsorted)
   alignas(16) unsigned long long bp[HC_BOUND];  // the boundary bin
-  float z[HC_MAX_K];                            // the row's logits
+  alignas(16) unsigned long long wb[HC_MAX_K];  // the boundary bin's winners, best first
+  float z[HC_MAX_K];                            // the row's logits in rank order (leader)
+  float zu[HC_MAX_K];                           // the logits by winner position (leader)
+  int32_t rk[HC_MAX_K];                         // rank of each winner position (leader)
 };
 
 struct HeadParams {
@@ -73,6 +76,39 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t id) {
   return ((unsigned long long)key << 32) | (unsigned long long)(~id);
+}
+
+// One warp's dot product of h (in shared memory) with W row v, in the rescoring kernels' order:
+// each lane keeps MAXW 16-byte loads of the row in flight, accumulates in fp32, and the warp
+// reduces with xor shuffles (every lane gets the sum).  The same order gives bit-identical logits.
+template <typename T>
+__device__ __forceinline__ float row_dot(const T* __restrict__ W, int v, int d, const T* hs, int lane) {
+  constexpr int PER = Elem<T>::PER16;
+  constexpr int MAXW = 20;
+  const T* w = W + (size_t)v * d;
+  float acc = 0.f;
+  for (int c0 = 0; c0 < d; c0 += 32 * PER * MAXW) {
+    uint4 wa[MAXW];
+#pragma unroll
+    for (int q = 0; q < MAXW; ++q) {
+      const int c = c0 + (q * 32 + lane) * PER;
+      if (c < d) wa[q] = ld_nc_v4(w + c);
+    }
+#pragma unroll
+    for (int q = 0; q < MAXW; ++q) {
+      const int c = c0 + (q * 32 + lane) * PER;
+      if (c < d) {
+        float wf[PER], xf[PER];
+        Elem<T>::unpack(wa[q], wf);
+        Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
+#pragma unroll
+        for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+      }
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
 }
 
 // Dynamic shared memory layout: control block, h, then the block selection's area (leader only).
@@ -211,7 +247,8 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
   }
   // every CTA took the same decisions from the same leader values
   if (!fallback) {
-    // compaction into the leader's lists (positions from warp ballots, one remote atomic per warp)
+    // compaction into every CTA's lists (positions from warp ballots, one remote atomic per warp
+    // on the leader's counters, each entry stored into all CTAs)
     const uint32_t below = (1u << lane) - 1u;
 #pragma unroll
     for (int q = 0; q < HC_ENT; ++q) {
@@ -225,21 +262,41 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
       }
       base_u = __shfl_sync(0xFFFFFFFFu, base_u, 0);
       base_b = __shfl_sync(0xFFFFFFFFu, base_b, 0);
-      const uint32_t k0 = key[q] - 1u + kmin;
-      if (up) L.sp[base_u + __popc(bu & below)] = pack(k0, id[q]);
-      else if (bd) L.bp[base_b + __popc(bb & below)] = pack(k0, id[q]);
+      if (up || bd) {
+        const unsigned long long e = pack(key[q] - 1u + kmin, id[q]);
+        unsigned long long* dst = up ? &my.sp[base_u + __popc(bu & below)] : &my.bp[base_b + __popc(bb & below)];
+#pragma unroll
+        for (int c = 0; c < HC_CTAS; ++c) *cl.map_shared_rank(dst, (unsigned)c) = e;
+      }
     }
     cluster_sync_all();
-    if (leader) {
-      // the boundary bin's best K - above, then every winner ranked by counting and written out
-      const int need = K - (int)above;
-      for (int i = threadIdx.x; i < (int)bc; i += HC_THREADS) {
-        const unsigned long long pi = my.bp[i];
-        int rank = 0;
-        for (int j = 0; j < (int)bc; ++j) rank += my.bp[j] > pi ? 1 : 0;
-        if (rank < need) my.sp[above + rank] = pi;
+    // Every CTA now holds the winners above the boundary bin (sp[0, above)) and the boundary bin
+    // (bp[0, bc)).  Each ranks the bin itself, so it knows all K winners, and tau (the K-th best
+    // key: the worst boundary winner) without waiting for the leader's sort.
+    const int need = K - (int)above;  // at least one: the boundary bin holds the K-th entry
+    {
+      int P = 1;
+      while (P < 32 && (int)bc * (2 * P) <= HC_THREADS) P <<= 1;
+      for (int base = 0; base < (int)bc * P; base += HC_THREADS) {
+        const int t = base + (int)threadIdx.x;
+        const int i = t / P, hh = t % P;
+        unsigned long long pi;
+        const int rank = sel::rank_by_count(my.bp, (int)bc, P, i, hh, &pi);
+        if (i < (int)bc && hh == 0 && rank < need) my.wb[rank] = pi;
       }
-      __syncthreads();
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < need; i += HC_THREADS) my.sp[above + i] = my.wb[i];
+    const uint32_t tau = (uint32_t)(my.wb[need - 1] >> 32);
+    // certificate: a group whose third score reaches tau may hide a member of the top K
+    bool mine = false;
+#pragma unroll
+    for (int q = 0; q < HC_RPT; ++q) mine |= fkey(rec[q].m3) >= tau && (g0 + (int)threadIdx.x + q * HC_THREADS) < g1;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, mine);
+    if (lane == 0 && bm) atomicAdd(&L.nref, (uint32_t)__popc(bm));
+    __syncthreads();  // sp[0, K) complete in this CTA
+    if (leader) {
+      // the winners' order: rank by counting, outputs written in rank order
       int P = 1;
       while (P < 32 && K * (2 * P) <= HC_THREADS) P <<= 1;
       for (int base = 0; base < K * P; base += HC_THREADS) {
@@ -248,69 +305,50 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
         unsigned long long pi;
         const int rank = sel::rank_by_count(my.sp, K, P, i, hh, &pi);
         if (i < K && hh == 0) {
-          const uint32_t kk = (uint32_t)(pi >> 32);
           p.idx_out[(size_t)b * K + rank] = (int32_t)(~(uint32_t)pi);
-          p.score_out[(size_t)b * K + rank] = fkey_inv(kk);
-          if (rank == K - 1) my.tau_key = kk;
+          p.score_out[(size_t)b * K + rank] = fkey_inv((uint32_t)(pi >> 32));
+          my.rk[i] = rank;
         }
       }
     }
-    cluster_sync_all();
-    // certificate: a group whose third score reaches tau may hide a member of the top K
-    const uint32_t tau = L.tau_key;
-    bool mine = false;
-#pragma unroll
-    for (int q = 0; q < HC_RPT; ++q) mine |= fkey(rec[q].m3) >= tau && (g0 + (int)threadIdx.x + q * HC_THREADS) < g1;
-    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, mine);
-    if (lane == 0 && bm) atomicAdd(&L.nref, (uint32_t)__popc(bm));
+    // exact logits of the winners by position, into the leader, while it sorts; they are used
+    // unless the certificate sends the row to the leader's block selection
+    for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+      const int v = (int)(~(uint32_t)my.sp[k]);
+      const bool ok = v >= 0 && v < p.vocab;
+      const float acc = ok ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
+      if (lane == 0) L.zu[k] = ok ? acc : __int_as_float(0x7FC00000);
+    }
     cluster_sync_all();
     fallback = L.nref != 0u;
-  }
-  if (fallback) {
-    // the leader selects the row alone: exact, with refinement or a full rescan as needed
-    if (leader)
-      sel::select_row<T, HC_THREADS>(fb, rrow, nullptr, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
-                                     p.idx_out + (size_t)b * K, p.score_out + (size_t)b * K);
-    cluster_sync_all();
-  } else if (leader) {
-    // zero the row's accumulators for the next call (select_row does it on the other branch)
-    for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
+    if (!fallback) {
+      if (!leader) return;
+      // zero the row's accumulators for the next call (select_row does it on the other branch)
+      for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
 #pragma unroll
-      for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+        for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+      for (int k = threadIdx.x; k < K; k += HC_THREADS) {
+        const float z = my.zu[k];
+        my.z[my.rk[k]] = z;
+        p.logits[(size_t)b * K + my.rk[k]] = z;
+      }
+      __syncthreads();
+      if (p.probs && warp == 0) warp_softmax(my.z, K, p.probs + (size_t)b * K);
+      return;
+    }
   }
+  // the leader selects the row alone: exact, with refinement or a full rescan as needed
+  if (leader)
+    sel::select_row<T, HC_THREADS>(fb, rrow, nullptr, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
+                                   p.idx_out + (size_t)b * K, p.score_out + (size_t)b * K);
+  cluster_sync_all();
 
   // ---------------------------------------------------------------- exact logits and softmax
   const int32_t* cand = p.idx_out + (size_t)b * K;
-  const T* W = static_cast<const T*>(p.W);
   for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
     const int v = cand[k];
     const bool ok = v >= 0 && v < p.vocab;
-    float acc = 0.f;
-    if (ok) {
-      const T* w = W + (size_t)v * p.d;
-      constexpr int MAXW = 20;
-      for (int c0 = 0; c0 < p.d; c0 += 32 * PER * MAXW) {
-        uint4 wa[MAXW];
-#pragma unroll
-        for (int q = 0; q < MAXW; ++q) {
-          const int c = c0 + (q * 32 + lane) * PER;
-          if (c < p.d) wa[q] = ld_nc_v4(w + c);
-        }
-#pragma unroll
-        for (int q = 0; q < MAXW; ++q) {
-          const int c = c0 + (q * 32 + lane) * PER;
-          if (c < p.d) {
-            float wf[PER], xf[PER];
-            Elem<T>::unpack(wa[q], wf);
-            Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
-#pragma unroll
-            for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-          }
-        }
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    const float acc = ok ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
     const float z = ok ? acc : __int_as_float(0x7FC00000);
     if (lane == 0) {
       p.logits[(size_t)b * K + k] = z;
