@@ -38,12 +38,14 @@ constexpr int HC_MAX_GROUPS = HC_CTAS * HC_THREADS * HC_RPT;  // 4096 groups: vo
 constexpr int HC_MAX_K = 256;
 constexpr int HC_BINS = 256;
 constexpr int HC_BITS = 8;
+static_assert(HC_BINS == HC_THREADS, "one bin per thread in the level scan");
 constexpr int HC_RANK = 64;    // a level whose boundary bin holds at most this many ends the descent
 constexpr int HC_BOUND = 512;  // largest boundary bin ranked by counting
 
 // Control block: every CTA has one; the leader's is the one in use.
 struct HeadCtl {
-  uint32_t hist[HC_BINS];
+  uint32_t hist[2][HC_BINS];  // this CTA's histograms (even and odd levels)
+  uint32_t wsc[HC_WARPS];     // per-warp totals of the bin scan
   uint32_t kmin, kmax;
   uint32_t digit, run, bincount, total;
   uint32_t n_above, n_bound, nref, tau_key;
@@ -135,7 +137,7 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
   unsigned long long* acc_row = p.acc + (size_t)b * p.r;
 
   // zero this CTA's control block; the barrier's wait (below) makes the leader's visible
-  for (int i = threadIdx.x; i < HC_BINS; i += HC_THREADS) my.hist[i] = 0u;
+  for (int i = threadIdx.x; i < HC_BINS; i += HC_THREADS) my.hist[0][i] = my.hist[1][i] = 0u;
   if (threadIdx.x == 0) {
     my.kmin = 0xFFFFFFFFu;
     my.kmax = 0u;
@@ -196,45 +198,48 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     int shift = range >= 0x80000000u ? 32 - HC_BITS : max(0, (32 - __clz((int)range)) - HC_BITS);
     const uint32_t dmask = (uint32_t)HC_BINS - 1u;
     bool first = true;
+    int lvl = 0;
 #pragma unroll 1
     for (;;) {
+      // each CTA histograms its own entries; after the barrier every CTA sums the CTAs' histograms
+      // and finds the digit itself, so a level costs one cluster barrier
+      uint32_t* hb = my.hist[lvl & 1];
 #pragma unroll
       for (int q = 0; q < HC_ENT; ++q)
-        if (key[q] && (key[q] & mask) == prefix) atomicAdd(&L.hist[(key[q] >> shift) & dmask], 1u);
+        if (key[q] && (key[q] & mask) == prefix) atomicAdd(&hb[(key[q] >> shift) & dmask], 1u);
       cluster_sync_all();
-      if (leader && warp == 0) {
-        // lane i owns bins 255 - 8i down to 248 - 8i; scan from the highest bin
-        uint32_t c[8], sum = 0;
+      const int bin = HC_BINS - 1 - (int)threadIdx.x;  // thread t takes bin 255 - t: scan from the top
+      uint32_t cnt = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) { c[q] = my.hist[HC_BINS - 1 - 8 * lane - q]; sum += c[q]; }
-        uint32_t incl = sum;
+      for (int c = 0; c < HC_CTAS; ++c) cnt += cl.map_shared_rank(hb, (unsigned)c)[bin];
+      // the other buffer was last read (by every CTA) before this level's barrier
+      my.hist[(lvl & 1) ^ 1][threadIdx.x] = 0u;
+      uint32_t incl = cnt;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-          if (lane >= o) incl += y;
-        }
-        const uint32_t excl = incl - sum;
-        if (first && lane == 31) my.total = incl;
-        if (excl < krem && krem <= incl) {
-          uint32_t run = excl;
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            if (run + c[q] >= krem) {
-              my.digit = (uint32_t)(HC_BINS - 1 - 8 * lane - q); my.run = run; my.bincount = c[q];
-              break;
-            }
-            run += c[q];
-          }
-        }
-        if (lane == 31 && incl < krem) { my.digit = 0; my.run = incl; my.bincount = 0; }
-        __syncwarp();
-#pragma unroll
-        for (int q = 0; q < 8; ++q) my.hist[8 * lane + q] = 0u;  // for the next level
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
       }
-      cluster_sync_all();
-      const uint32_t D = L.digit, run = L.run, total = L.total;
-      bc = L.bincount;
+      if (lane == 31) my.wsc[warp] = incl;
+      __syncthreads();
+      uint32_t before = 0, total = 0;
+#pragma unroll
+      for (int w = 0; w < HC_WARPS; ++w) {
+        const uint32_t x = my.wsc[w];
+        before += w < warp ? x : 0u;
+        total += x;
+      }
+      incl += before;
+      if (incl - cnt < krem && krem <= incl) {
+        my.digit = (uint32_t)bin;
+        my.run = incl - cnt;
+        my.bincount = cnt;
+      }
+      __syncthreads();
+      ++lvl;
       if (first && total < (uint32_t)K) { fallback = true; break; }
+      const uint32_t D = my.digit, run = my.run;
+      bc = my.bincount;
       first = false;
       prefix |= D << shift;
       mask |= dmask << shift;
@@ -245,7 +250,7 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     }
     if (bc > (uint32_t)HC_BOUND) fallback = true;
   }
-  // every CTA took the same decisions from the same leader values
+  // every CTA took the same decisions from the same histograms
   if (!fallback) {
     // compaction into every CTA's lists (positions from warp ballots, one remote atomic per warp
     // on the leader's counters, each entry stored into all CTAs)
