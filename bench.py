@@ -408,6 +408,19 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
                 "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 ("algorithmic_flops_per_launch" if bound == "tensor" else "algorithmic_bytes_per_launch"): algo,
                 "us_per_launch": round(stages[dom]["us_avg"], 3), "peak_source": peak_src_s}
+    # the kernel that moves the most bytes, against the copy bandwidth (when it is not the one above)
+    roofline_stream = None
+    hbm_k = [k for k in stages if kernel_algo(cfg, k)[0] == "hbm" and kernel_algo(cfg, k)[1] > 0]
+    if hbm_k:
+        sk = max(hbm_k, key=lambda k: kernel_algo(cfg, k)[1])
+        if sk != dom:
+            s_algo = kernel_algo(cfg, sk)[1]
+            s_ach = s_algo / (stages[sk]["us_avg"] * 1e-6) / 1e9
+            roofline_stream = {"kernel": sk, "bound": "hbm", "achieved": round(s_ach, 1), "peak": peaks["hbm_gbs"],
+                               "unit": "GB/s", "frac": round(s_ach / peaks["hbm_gbs"], 4),
+                               "traffic": traffic_from_profiles(sk, cfg.name, KERNEL_FILES.get(sk, [])),
+                               "algorithmic_bytes_per_launch": s_algo,
+                               "us_per_launch": round(stages[sk]["us_avg"], 3)}
     path_ach = per_step / (us_per_call * 1e-6) / 1e9
     hbm = peaks["hbm_gbs"]
     path_roofline = {"bound": "hbm", "bytes_per_call": per_step, "achieved": round(path_ach, 1),
@@ -467,7 +480,7 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
                    "l2": f"inputs rotate over {copies} independent copies "
                          f"({copies * per_step / 2**20:.0f} MiB per cycle > 2x L2)",
                    "parallelism": f"replicas x{world} (rows independent)"},
-        "roofline": roofline, "path_roofline": path_roofline, "stages": stages,
+        "roofline": roofline, "roofline_stream": roofline_stream, "path_roofline": path_roofline, "stages": stages,
         "gpu_launches": int(round(launches_per_step * a.steps)), "e2e": e2e,
         "cpu_baseline": cpu, "clocks": clocks,
     }
