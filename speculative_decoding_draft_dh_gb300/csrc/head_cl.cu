@@ -76,6 +76,12 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Bulk prefetch of [p, p + bytes) into L2 (p 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t id) {
   return ((unsigned long long)key << 32) | (unsigned long long)(~id);
 }
@@ -292,6 +298,14 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     }
     __syncthreads();
     for (int i = threadIdx.x; i < need; i += HC_THREADS) my.sp[above + i] = my.wb[i];
+    // this CTA's candidates' W rows start towards L2 now (the certificate, and in the leader the
+    // sort, come before the dot products)
+    if (lane == 0)
+      for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+        const int v = (int)(~(uint32_t)(k < (int)above ? my.sp[k] : my.wb[k - (int)above]));
+        if (v >= 0 && v < p.vocab)
+          prefetch_l2(static_cast<const T*>(p.W) + (size_t)v * p.d, (uint32_t)(p.d * sizeof(T)));
+      }
     const uint32_t tau = (uint32_t)(my.wb[need - 1] >> 32);
     // certificate: a group whose third score reaches tau may hide a member of the top K
     bool mine = false;
