@@ -1,5 +1,5 @@
 // Small batches: selection and exact rescoring fused into one kernel, one thread-block cluster of
-// HC_CTAS CTAs per row.
+// 16 (or 8) CTAs per row.
 //
 // EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
 // the K candidates of a row are its K best low-rank scores (score desc, id asc); their exact
@@ -7,20 +7,28 @@
 //
 // At batch 1 the selection is a short chain of dependent steps over about 4700 pool entries, and
 // each kernel boundary in the pipeline costs one to two microseconds.  Here the cluster's CTAs
-// split the row's group records (HC_RPT per thread) and select cooperatively through distributed
-// shared memory: the histograms, the candidate lists and the control words live in the leader
-// CTA (rank 0); the other CTAs reach them with remote atomics and loads.  The steps are those of
-// the register fast path of the selection kernel (radix levels over the pool's own key range,
-// compaction, ranking by counting), each ended by a cluster barrier.  The leader writes the sorted
-// candidates; every CTA then scores its share of them against h (staged in shared memory before
-// the wait on the previous kernel) and stores the logits into the leader, which computes the
-// softmax.  A row whose certificate finds groups to re-score, or whose pool is degenerate, is
-// selected again by the leader alone with the block selection (select_row: exact, with refinement
-// and full rescan) before the rescoring step.
+// split the row's group records and select cooperatively through distributed shared memory, with
+// the steps of the register fast path of the selection kernel (radix levels over the pool's own
+// key range, compaction, ranking by counting):
+//  - the key range is combined in the leader CTA (rank 0) behind one cluster barrier;
+//  - each radix level: every CTA histograms its own entries locally, and after one cluster barrier
+//    every CTA sums the CTAs' histograms and finds the boundary bin itself;
+//  - compaction writes the entries above and in the boundary bin into every CTA's lists;
+//  - every CTA ranks the boundary bin itself, so it knows the K winners and tau, checks the
+//    certificate on its groups and scores its share of the winners against h (staged in shared
+//    memory before the wait on the previous kernel), storing the logits into the leader, while the
+//    leader ranks the winners and writes them in order;
+//  - after one more barrier the leader orders the logits and computes the softmax.
+// A row whose certificate finds groups to re-score, or whose pool is degenerate, is selected again
+// by the leader alone with the block selection (select_row: exact, with refinement and full
+// rescan) and then rescored.
 //
 // Cluster barriers are hardware barriers that every CTA passes unconditionally, so they always
 // complete.
 #include <cooperative_groups.h>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
 
 #include "select.cuh"
 
@@ -29,12 +37,13 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int HC_CTAS = 8;
+// A cluster has 16 CTAs where the GPU can schedule such clusters (a non-portable size: the CTAs
+// must share a GPC), else 8; each thread holds 16 / CTAS group records, so both cover 4096 groups.
+// Spreading the candidates' W rows over 16 SMs halves each SM's share of the rescoring loads
+// (20.1 against 20.4 µs per call at batch 1).
 constexpr int HC_THREADS = 256;
 constexpr int HC_WARPS = HC_THREADS / 32;
-constexpr int HC_RPT = 2;                                      // group records per thread
-constexpr int HC_ENT = 2 * HC_RPT;                             // pool entries per thread
-constexpr int HC_MAX_GROUPS = HC_CTAS * HC_THREADS * HC_RPT;  // 4096 groups: vocab <= 262144
+constexpr int HC_MAX_GROUPS = 16 * HC_THREADS;  // 4096 groups: vocab <= 262144
 constexpr int HC_MAX_K = 256;
 constexpr int HC_BINS = 256;
 constexpr int HC_BITS = 8;
@@ -125,8 +134,10 @@ __host__ __device__ constexpr size_t hc_fb_offset(int d, int elem) {
   return hc_h_offset() + align_up((size_t)d * elem, 128);
 }
 
-template <typename T>
-__global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
+template <typename T, int HC_CTAS>
+__global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
+  constexpr int HC_RPT = 16 / HC_CTAS;  // group records per thread
+  constexpr int HC_ENT = 2 * HC_RPT;    // pool entries per thread
   constexpr int PER = Elem<T>::PER16;
   extern __shared__ __align__(128) unsigned char smem[];
   cg::cluster_group cl = cg::this_cluster();
@@ -301,7 +312,7 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     // this CTA's candidates' W rows start towards L2 now (the certificate, and in the leader the
     // sort, come before the dot products)
     if (lane == 0)
-      for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+      for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
         const int v = (int)(~(uint32_t)(k < (int)above ? my.sp[k] : my.wb[k - (int)above]));
         if (v >= 0 && v < p.vocab)
           prefetch_l2(static_cast<const T*>(p.W) + (size_t)v * p.d, (uint32_t)(p.d * sizeof(T)));
@@ -332,7 +343,7 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
     }
     // exact logits of the winners by position, into the leader, while it sorts; they are used
     // unless the certificate sends the row to the leader's block selection
-    for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+    for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
       const int v = (int)(~(uint32_t)my.sp[k]);
       const bool ok = v >= 0 && v < p.vocab;
       const float acc = ok ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
@@ -364,7 +375,7 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
 
   // ---------------------------------------------------------------- exact logits and softmax
   const int32_t* cand = p.idx_out + (size_t)b * K;
-  for (int k = (int)crank * HC_WARPS + warp; k < K; k += HC_CTAS * HC_WARPS) {
+  for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
     const int v = cand[k];
     const bool ok = v >= 0 && v < p.vocab;
     const float acc = ok ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
@@ -379,26 +390,74 @@ __global__ void __cluster_dims__(HC_CTAS, 1, 1) __launch_bounds__(HC_THREADS, 1)
   warp_softmax(my.z, K, p.probs + (size_t)b * K);
 }
 
-template <typename T>
-cudaError_t run(const Ctx& c, const HeadParams& p) {
-  static unsigned long long smem_done = 0;
-  cudaError_t e = allow_max_smem(k_head_cl<T>, c.device, &smem_done);
-  if (e != cudaSuccess) return e;
-  cudaLaunchAttribute attr[1];
+template <typename T, int CTAS>
+cudaError_t launch(const Ctx& c, const HeadParams& p, size_t smem) {
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = CTAS;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(p.B * HC_CTAS));
+  cfg.gridDim = dim3((unsigned)(p.B * CTAS));
   cfg.blockDim = dim3(HC_THREADS);
-  cfg.dynamicSmemBytes = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = c.stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   prof_before("head_cluster", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_head_cl<T>, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, k_head_cl<T, CTAS>, p);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
+}
+
+// Whether clusters of 16 CTAs with this shared memory can run on the device (set up once per
+// device and element type: shared memory limit, the non-portable size, then the occupancy query).
+template <typename T>
+bool sixteen_fit(int device, size_t smem) {
+  static std::mutex mu;
+  static int state[64] = {};  // 0 unknown, 1 yes, 2 no
+  static size_t smem_at[64] = {};
+  if (device < 0 || device >= 64) return false;
+  std::lock_guard<std::mutex> lk(mu);
+  if (state[device] != 0 && smem_at[device] >= smem) return state[device] == 1;
+  bool ok = cudaFuncSetAttribute(k_head_cl<T, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+            cudaSuccess;
+  if (ok) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 16;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(16);
+    cfg.blockDim = dim3(HC_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    ok = cudaOccupancyMaxActiveClusters(&n, k_head_cl<T, 16>, &cfg) == cudaSuccess && n >= 1;
+  }
+  (void)cudaGetLastError();  // a refused query leaves no sticky error behind
+  state[device] = ok ? 1 : 2;
+  smem_at[device] = smem;
+  return ok;
+}
+
+template <typename T>
+cudaError_t run(const Ctx& c, const HeadParams& p) {
+  static unsigned long long smem_done8 = 0, smem_done16 = 0;
+  cudaError_t e = allow_max_smem(k_head_cl<T, 8>, c.device, &smem_done8);
+  if (e != cudaSuccess) return e;
+  e = allow_max_smem(k_head_cl<T, 16>, c.device, &smem_done16);
+  if (e != cudaSuccess) return e;
+  const size_t smem = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
+  const char* f = std::getenv("DH_HEAD_CTAS");  // "8": the portable cluster size (tests)
+  const bool force8 = f && std::strcmp(f, "8") == 0;
+  if (!force8 && sixteen_fit<T>(c.device, smem)) return launch<T, 16>(c, p, smem);
+  return launch<T, 8>(c, p, smem);
 }
 
 }  // namespace

@@ -194,16 +194,18 @@ def test_batch1_full_size(api):
     run_head(x, cfg.K, api=api)
 
 
-@pytest.mark.parametrize("mode", ["auto", "cluster", "split"])
+@pytest.mark.parametrize("mode", ["auto", "cluster8", "split"])
 @pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
                                     ("high", 512)])
 def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
     """dh_draft_head gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same
     selection rule on the same records and the same per-candidate dot product order; twice in a
-    row with one workspace (its state resets itself).  "cluster" forces the fused cluster kernel
-    (selection and rescoring in one launch) where the batch is small enough, "split" the two
-    kernels."""
-    if mode != "auto":
+    row with one workspace (its state resets itself).  "auto" takes the fused cluster kernel
+    (selection and rescoring in one launch) where the batch is small enough, "cluster8" the same
+    with 8-CTA clusters, "split" the two kernels."""
+    if mode == "cluster8":
+        monkeypatch.setenv("DH_HEAD_CTAS", "8")
+    elif mode != "auto":
         monkeypatch.setenv("DH_FORCE_HEAD", mode)
     cfg = inputs.head_config(name, B=B)
     x = inputs.make_head(cfg, seed=11, device=DEV)
@@ -221,11 +223,15 @@ def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
     assert dh.workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("ctas", ["auto", "8"])
 @pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
-def test_fused_head_matches_the_two_calls_over_K(K, monkeypatch):
+def test_fused_head_matches_the_two_calls_over_K(K, ctas, monkeypatch):
     """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
-    of candidates per CTA, and beyond one candidate per warp)."""
+    of candidates per CTA, and beyond one candidate per warp), with 16-CTA clusters where they fit
+    and with the portable 8."""
     monkeypatch.setenv("DH_FORCE_HEAD", "cluster")
+    if ctas != "auto":
+        monkeypatch.setenv("DH_HEAD_CTAS", ctas)
     cfg = inputs.head_config("tiny", B=3, K=K)
     x = inputs.make_head(cfg, seed=21, device=DEV)
     h, U, V, W = x["h"], x["U"], x["V"], x["W"]
