@@ -157,20 +157,28 @@ const char* dh_last_error(void) { return g_last_error; }
 
 namespace {
 
-// Stage 1 after validation: projection, scores with group summaries, selection.
-int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
-             int dtype, int32_t* idx_out, float* score_out, char* ws, const TopkLayout& L) {
+// Where stage 1 leaves t for the selection: in the small-batch projection's accumulators (acc) or
+// in the activation dtype (t); and the group records.
+struct Stage1 {
+  const void* t;
+  unsigned long long* acc;
+  GroupRec* recs;
+};
+
+// Stage 1 up to the group records: projection and scores with group summaries.
+int run_records(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
+                int dtype, char* ws, const TopkLayout& L, Stage1* out) {
   void* t = ws + L.t;
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
+  out->recs = recs;
   const Path path = choose_path(B, r, dtype);
   if (path == PATH_FUSED) {
     unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
     if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
-    if (note_error(launch_select(c, recs, nullptr, acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
-        cudaSuccess)
-      return DH_ERR_CUDA;
+    out->t = nullptr;
+    out->acc = acc;
     return DH_OK;
   }
   if (path == PATH_MMA && proj_mma_supported(B, d, r, dtype)) {
@@ -186,7 +194,18 @@ int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, i
   } else if (note_error(launch_scores_summary(c, t, V, B, r, vocab, dtype, recs), "scores") != cudaSuccess) {
     return DH_ERR_CUDA;
   }
-  if (note_error(launch_select(c, recs, t, nullptr, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
+  out->t = t;
+  out->acc = nullptr;
+  return DH_OK;
+}
+
+// Stage 1 after validation: projection, scores with group summaries, selection.
+int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
+             int dtype, int32_t* idx_out, float* score_out, char* ws, const TopkLayout& L) {
+  Stage1 s1;
+  const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
+  if (st != DH_OK) return st;
+  if (note_error(launch_select(c, s1.recs, s1.t, s1.acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
       cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
@@ -291,23 +310,26 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
-  // small batches: the scores kernels, then selection and rescoring in one cluster kernel
-  // (DH_FORCE_HEAD=split: the selection and rescoring kernels instead)
+  // Batches whose rows the fused cluster head takes in one wave: the stage-1 kernels, then
+  // selection and rescoring in one cluster kernel; larger batches (or DH_FORCE_HEAD=split): the
+  // selection and rescoring kernels.
   const char* f = std::getenv("DH_FORCE_HEAD");
   const bool split = f && std::strcmp(f, "split") == 0;
-  if (!split && choose_path(B, r, dtype) == PATH_FUSED && head_cluster_supported(B, d, vocab, K, dtype)) {
-    unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
-    GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
-    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
-      return DH_ERR_CUDA;
-    if (note_error(launch_head_cluster(c, recs, acc, V, h, W, B, d, r, vocab, K, dtype, idx_out, score_out,
-                                       logits_out, probs_out),
+  const int ctas = split || !head_cluster_supported(B, d, vocab, K, dtype) ? 0
+                                                                          : head_cluster_ctas(c, B, d, vocab, dtype);
+  Stage1 s1;
+  const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
+  if (st != DH_OK) return st;
+  if (ctas) {
+    if (note_error(launch_head_cluster(c, ctas, s1.recs, s1.acc, s1.t, V, h, W, B, d, r, vocab, K, dtype, idx_out,
+                                       score_out, logits_out, probs_out),
                    "selection and rescoring (cluster)") != cudaSuccess)
       return DH_ERR_CUDA;
     return DH_OK;
   }
-  const int st = run_topk(c, h, U, V, B, d, r, vocab, K, dtype, idx_out, score_out, ws, L);
-  if (st != DH_OK) return st;
+  if (note_error(launch_select(c, s1.recs, s1.t, s1.acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
+      cudaSuccess)
+    return DH_ERR_CUDA;
   return run_rescore(c, h, W, idx_out, B, d, vocab, K, dtype, logits_out, probs_out,
                      reinterpret_cast<uint32_t*>(ws + roff), reinterpret_cast<int*>(ws));
 }

@@ -69,7 +69,8 @@ struct HeadCtl {
 
 struct HeadParams {
   const GroupRec* recs;     // [B][n_groups]
-  unsigned long long* acc;  // the projection's fixed-point accumulators (cleared here)
+  unsigned long long* acc;  // the small-batch projection's fixed-point accumulators (cleared here), or
+  const void* t;            // t [B][r] in the activation dtype (tensor-core stage 1)
   const void* V;
   const void* h;
   const void* W;
@@ -151,7 +152,8 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   T* hs = reinterpret_cast<T*>(smem + hc_h_offset());
   unsigned char* fb = smem + hc_fb_offset(p.d, (int)sizeof(T));
   const GroupRec* rrow = p.recs + (size_t)b * n_groups;
-  unsigned long long* acc_row = p.acc + (size_t)b * p.r;
+  unsigned long long* acc_row = p.acc ? p.acc + (size_t)b * p.r : nullptr;
+  const T* t_row = p.acc ? nullptr : static_cast<const T*>(p.t) + (size_t)b * p.r;
 
   // zero this CTA's control block; the barrier's wait (below) makes the leader's visible
   for (int i = threadIdx.x; i < HC_BINS; i += HC_THREADS) my.hist[0][i] = my.hist[1][i] = 0u;
@@ -354,9 +356,10 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     if (!fallback) {
       if (!leader) return;
       // zero the row's accumulators for the next call (select_row does it on the other branch)
-      for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
+      if (acc_row)
+        for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
 #pragma unroll
-        for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+          for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
       for (int k = threadIdx.x; k < K; k += HC_THREADS) {
         const float z = my.zu[k];
         my.z[my.rk[k]] = z;
@@ -369,7 +372,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   }
   // the leader selects the row alone: exact, with refinement or a full rescan as needed
   if (leader)
-    sel::select_row<T, HC_THREADS>(fb, rrow, nullptr, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
+    sel::select_row<T, HC_THREADS>(fb, rrow, t_row, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
                                    p.idx_out + (size_t)b * K, p.score_out + (size_t)b * K);
   cluster_sync_all();
 
@@ -413,54 +416,74 @@ cudaError_t launch(const Ctx& c, const HeadParams& p, size_t smem) {
   return cudaGetLastError();
 }
 
-// Whether clusters of 16 CTAs with this shared memory can run on the device (set up once per
-// device and element type: shared memory limit, the non-portable size, then the occupancy query).
+// Clusters of CTAS CTAs with this shared memory that run at once on the device (0 if none).
+template <typename T, int CTAS>
+int clusters_at_once(int device, size_t smem) {
+  unsigned long long done = 0;  // the query needs the kernel's shared memory limit raised
+  if (allow_max_smem(k_head_cl<T, CTAS>, device, &done) != cudaSuccess) return 0;
+  if (CTAS > 8 &&
+      cudaFuncSetAttribute(k_head_cl<T, CTAS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return 0;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CTAS;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CTAS);
+  cfg.blockDim = dim3(HC_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, k_head_cl<T, CTAS>, &cfg) != cudaSuccess) n = 0;
+  return n;
+}
+
+// Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
+// clusters of 8 do, else 0 (the batch goes to the selection and rescoring kernels).  The device's
+// capacities are queried once per device and element type (set-up calls: shared memory limit,
+// the non-portable size, the occupancy query).  DH_HEAD_CTAS=8 skips the 16-CTA form (tests).
 template <typename T>
-bool sixteen_fit(int device, size_t smem) {
+int choose_ctas(const Ctx& c, int B, int d, int n_groups) {
+  const size_t smem = hc_fb_offset(d, (int)sizeof(T)) + sel::select_smem_bytes(n_groups);
   static std::mutex mu;
-  static int state[64] = {};  // 0 unknown, 1 yes, 2 no
+  static int cap[64][2] = {};  // [device]: clusters of 16 and of 8 at once, +1 (0: not queried)
   static size_t smem_at[64] = {};
-  if (device < 0 || device >= 64) return false;
-  std::lock_guard<std::mutex> lk(mu);
-  if (state[device] != 0 && smem_at[device] >= smem) return state[device] == 1;
-  bool ok = cudaFuncSetAttribute(k_head_cl<T, 16>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
-            cudaSuccess;
-  if (ok) {
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 16;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(16);
-    cfg.blockDim = dim3(HC_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    ok = cudaOccupancyMaxActiveClusters(&n, k_head_cl<T, 16>, &cfg) == cudaSuccess && n >= 1;
+  if (c.device < 0 || c.device >= 64) return 0;
+  int n16, n8;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    if (cap[c.device][0] == 0 || smem_at[c.device] < smem) {
+      cap[c.device][0] = clusters_at_once<T, 16>(c.device, smem) + 1;
+      cap[c.device][1] = clusters_at_once<T, 8>(c.device, smem) + 1;
+      smem_at[c.device] = smem;
+      (void)cudaGetLastError();  // a refused query leaves no sticky error behind
+    }
+    n16 = cap[c.device][0] - 1;
+    n8 = cap[c.device][1] - 1;
   }
-  (void)cudaGetLastError();  // a refused query leaves no sticky error behind
-  state[device] = ok ? 1 : 2;
-  smem_at[device] = smem;
-  return ok;
+  const char* f = std::getenv("DH_HEAD_CTAS");
+  const bool force8 = f && std::strcmp(f, "8") == 0;
+  if (!force8 && B <= n16) return 16;
+  if (B <= n8) return 8;
+  return 0;
 }
 
 template <typename T>
-cudaError_t run(const Ctx& c, const HeadParams& p) {
-  static unsigned long long smem_done8 = 0, smem_done16 = 0;
-  cudaError_t e = allow_max_smem(k_head_cl<T, 8>, c.device, &smem_done8);
-  if (e != cudaSuccess) return e;
-  e = allow_max_smem(k_head_cl<T, 16>, c.device, &smem_done16);
-  if (e != cudaSuccess) return e;
+cudaError_t run(const Ctx& c, const HeadParams& p, int ctas) {
   const size_t smem = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
-  const char* f = std::getenv("DH_HEAD_CTAS");  // "8": the portable cluster size (tests)
-  const bool force8 = f && std::strcmp(f, "8") == 0;
-  if (!force8 && sixteen_fit<T>(c.device, smem)) return launch<T, 16>(c, p, smem);
-  return launch<T, 8>(c, p, smem);
+  return ctas == 16 ? launch<T, 16>(c, p, smem) : launch<T, 8>(c, p, smem);
 }
 
 }  // namespace
+
+int head_cluster_ctas(const Ctx& c, int B, int d, int vocab, int dtype) {
+  // a wave of clusters holds at most one row per 8 SMs: larger batches need no query
+  if (B > c.num_sms / 8) return 0;
+  const int n_groups = (vocab + GROUP - 1) / GROUP;
+  return dtype == DH_BF16 ? choose_ctas<__nv_bfloat16>(c, B, d, n_groups) : choose_ctas<float>(c, B, d, n_groups);
+}
 
 bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
   const int n_groups = (vocab + GROUP - 1) / GROUP;
@@ -469,12 +492,15 @@ bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
          d <= 8192 && smem <= 200 * 1024;
 }
 
-cudaError_t launch_head_cluster(const Ctx& c, const GroupRec* recs, unsigned long long* acc, const void* V,
-                                const void* h, const void* W, int B, int d, int r, int vocab, int K, int dtype,
-                                int32_t* idx_out, float* score_out, float* logits, float* probs) {
+cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, unsigned long long* acc,
+                                const void* t, const void* V, const void* h, const void* W, int B, int d, int r,
+                                int vocab, int K, int dtype, int32_t* idx_out, float* score_out, float* logits,
+                                float* probs) {
+  if (ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
   HeadParams p;
   p.recs = recs;
   p.acc = acc;
+  p.t = t;
   p.V = V;
   p.h = h;
   p.W = W;
@@ -488,8 +514,8 @@ cudaError_t launch_head_cluster(const Ctx& c, const GroupRec* recs, unsigned lon
   p.score_out = score_out;
   p.logits = logits;
   p.probs = probs;
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, p);
-  return run<float>(c, p);
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, p, ctas);
+  return run<float>(c, p, ctas);
 }
 
 }  // namespace dh

@@ -111,6 +111,26 @@ def test_clustered_candidates_are_refined(api):
     run_head(x, cfg.K, api=api)
 
 
+@pytest.mark.parametrize("B", [1, 8])
+def test_tensor_core_path_fused_head_refines_clustered_rows(B, monkeypatch):
+    """Tensor-core stage 1 (t in bf16) followed by the fused cluster head, on rows whose top
+    candidates crowd one group (refinement by the leader's block selection) and on plain rows:
+    against the oracle, and bit for bit against the two calls."""
+    monkeypatch.setenv("DH_FORCE_PATH", "mma")
+    cfg = inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=32)
+    x = inputs.make_head(cfg, seed=8, device=DEV)
+    v = _best_column(x)
+    base = x["V"][:, v].clone()
+    for j in range(64):
+        x["V"][:, 128 + j] = base * (1.0 + 0.01 * j)
+    idx, score, logits, probs = run_head(x, cfg.K, api="head")
+    i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    l2, p2 = dh.exact_rescore(x["h"], x["W"], i2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, i2) and torch.equal(score, s2)
+    assert torch.equal(logits, l2) and torch.equal(probs, p2)
+
+
 @pytest.mark.parametrize("api", ["split", "head"])
 def test_many_clustered_groups_use_full_rescan(api):
     cfg = inputs.head_config("tiny", B=1, K=128)
