@@ -75,10 +75,12 @@ struct ProjSmall {
   unsigned long long* acc;  // [ACC_COPIES][B*r] fixed-point accumulators (zero between calls)
 };
 
-template <typename T>
+// NB = B (1..MAX_B): the accumulators are sized for the batch, so that at batch 1 a projection
+// block holds few registers and the scores kernel's blocks, launched early, fit beside it.
+template <typename T, int NB>
 __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
   constexpr int PAIRS = PJ_THREADS / PJ_GROUPS;  // column pairs per pass
-  __shared__ float red[PJ_GROUPS][MAX_B * 2 * PAIRS];  // per-group partials of this pass, [b][2 * pair]
+  __shared__ float red[PJ_GROUPS][NB * 2 * PAIRS];  // per-group partials of this pass, [b][2 * pair]
   const T* h = static_cast<const T*>(p.h);
   const T* U = static_cast<const T*>(p.U);
   const int B = p.B, r = p.r, BR = B * r, npairs = r / 2;
@@ -96,9 +98,9 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
   for (int jp0 = 0; jp0 < npairs; jp0 += PAIRS) {
     const int jp = jp0 + lt;
     const bool on = jp < npairs;
-    float a[MAX_B][2];
+    float a[NB][2];
 #pragma unroll
-    for (int bb = 0; bb < MAX_B; ++bb) a[bb][0] = a[bb][1] = 0.f;
+    for (int bb = 0; bb < NB; ++bb) a[bb][0] = a[bb][1] = 0.f;
     for (int base = g0; base < g1; base += CH) {
       const int n = min(CH, g1 - base);
       float u[CH][2];
@@ -116,12 +118,10 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
         for (int i = 0; i < CH; ++i) {
           if (i < n) {
 #pragma unroll
-            for (int bb = 0; bb < MAX_B; ++bb) {
-              if (bb < B) {
-                const float hv = Elem<T>::to_f(h[(size_t)bb * p.d + base + i]);
-                a[bb][0] = fmaf(hv, u[i][0], a[bb][0]);
-                a[bb][1] = fmaf(hv, u[i][1], a[bb][1]);
-              }
+            for (int bb = 0; bb < NB; ++bb) {
+              const float hv = Elem<T>::to_f(h[(size_t)bb * p.d + base + i]);
+              a[bb][0] = fmaf(hv, u[i][0], a[bb][0]);
+              a[bb][1] = fmaf(hv, u[i][1], a[bb][1]);
             }
           }
         }
@@ -129,11 +129,9 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
     }
     // add the row groups' partials in a fixed order, then one integer atomic per (b, j)
 #pragma unroll
-    for (int bb = 0; bb < MAX_B; ++bb) {
-      if (bb < B) {
-        red[grp][bb * 2 * PAIRS + 2 * lt] = a[bb][0];
-        red[grp][bb * 2 * PAIRS + 2 * lt + 1] = a[bb][1];
-      }
+    for (int bb = 0; bb < NB; ++bb) {
+      red[grp][bb * 2 * PAIRS + 2 * lt] = a[bb][0];
+      red[grp][bb * 2 * PAIRS + 2 * lt + 1] = a[bb][1];
     }
     __syncthreads();
     for (int q2 = threadIdx.x; q2 < B * 2 * PAIRS; q2 += PJ_THREADS) {
@@ -464,7 +462,12 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before("proj_small", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_proj_small<T>, pp);
+  switch (B) {
+#define DH_PJ_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_proj_small<T, n>, pp); break;
+    DH_PJ_CASE(1) DH_PJ_CASE(2) DH_PJ_CASE(3) DH_PJ_CASE(4) DH_PJ_CASE(5) DH_PJ_CASE(6) DH_PJ_CASE(7) DH_PJ_CASE(8)
+#undef DH_PJ_CASE
+    default: e = cudaErrorInvalidValue;
+  }
   prof_after(c.stream);
   if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_proj_small)");
 
