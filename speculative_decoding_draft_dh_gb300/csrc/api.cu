@@ -317,7 +317,7 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   const char* f = std::getenv("DH_FORCE_HEAD");
   const bool split = f && std::strcmp(f, "split") == 0;
   const int ctas = split || !head_cluster_supported(B, d, vocab, K, dtype) ? 0
-                                                                          : head_cluster_ctas(c, B, d, vocab, dtype);
+                                                                          : head_cluster_ctas(c, B, K, d, vocab, dtype);
   Stage1 s1;
   const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
   if (st != DH_OK) return st;

@@ -221,9 +221,9 @@ cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, uns
 
 // Small batches: selection and rescoring in one thread-block cluster per row (head_cl.cu).
 bool head_cluster_supported(int B, int d, int vocab, int K, int dtype);
-// Cluster size (16 or 8 CTAs) with which the fused head runs all B rows in one wave on this
-// device, or 0 when it cannot.
-int head_cluster_ctas(const Ctx& c, int B, int d, int vocab, int dtype);
+// Cluster size (16, 8 or 4 CTAs) with which the fused head runs all B rows in one wave on this
+// device, or 0 when it cannot (or when the two kernels are faster for B rows of K candidates).
+int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype);
 // Fused selection and rescoring with clusters of `ctas` CTAs: t from the small-batch accumulators
 // (acc) or, with acc null, from t [B][r] in the activation dtype.
 cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, unsigned long long* acc,

@@ -1,5 +1,5 @@
 // Small batches: selection and exact rescoring fused into one kernel, one thread-block cluster of
-// 16 (or 8) CTAs per row.
+// 16, 8 or 4 CTAs per row.
 //
 // EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
 // the K candidates of a row are its K best low-rank scores (score desc, id asc); their exact
@@ -38,9 +38,9 @@ namespace {
 namespace cg = cooperative_groups;
 
 // A cluster has 16 CTAs where the GPU can schedule such clusters (a non-portable size: the CTAs
-// must share a GPC), else 8; each thread holds 16 / CTAS group records, so both cover 4096 groups.
-// Spreading the candidates' W rows over 16 SMs halves each SM's share of the rescoring loads
-// (20.1 against 20.4 µs per call at batch 1).
+// must share a GPC), else 8 or 4; each thread holds 16 / CTAS group records, so every size covers
+// 4096 groups.  Spreading the candidates' W rows over 16 SMs halves each SM's share of the
+// rescoring loads (20.1 against 20.4 µs per call at batch 1).
 constexpr int HC_THREADS = 256;
 constexpr int HC_WARPS = HC_THREADS / 32;
 constexpr int HC_MAX_GROUPS = 16 * HC_THREADS;  // 4096 groups: vocab <= 262144
@@ -441,48 +441,57 @@ int clusters_at_once(int device, size_t smem) {
 }
 
 // Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
-// clusters of 8 do, else 0 (the batch goes to the selection and rescoring kernels).  The device's
-// capacities are queried once per device and element type (set-up calls: shared memory limit,
-// the non-portable size, the occupancy query).  DH_HEAD_CTAS=8 skips the 16-CTA form (tests).
+// clusters of 8 do, else 4 for up to 2048 (row, candidate) pairs when all B clusters of 4 do, else
+// 0 (the batch goes to the selection and rescoring kernels).  Four CTAs score eight or more
+// candidates per warp, one row after another; that pays against the two kernels up to about 2048
+// pairs (32 rows x 64: 31.0 against 39.0 µs per call; 16 x 64: 29.3 against 32.6) but not beyond
+// (64 x 128: 77.6 against 56.4).  The device's capacities are queried once per device and element
+// type (set-up calls: shared memory limit, the non-portable size, the occupancy query).
+// DH_HEAD_CTAS=8 or 4 skips the larger forms (tests).
 template <typename T>
-int choose_ctas(const Ctx& c, int B, int d, int n_groups) {
+int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const size_t smem = hc_fb_offset(d, (int)sizeof(T)) + sel::select_smem_bytes(n_groups);
   static std::mutex mu;
-  static int cap[64][2] = {};  // [device]: clusters of 16 and of 8 at once, +1 (0: not queried)
+  static int cap[64][3] = {};  // [device]: clusters of 16, 8 and 4 at once, +1 (0: not queried)
   static size_t smem_at[64] = {};
   if (c.device < 0 || c.device >= 64) return 0;
-  int n16, n8;
+  int n16, n8, n4;
   {
     std::lock_guard<std::mutex> lk(mu);
     if (cap[c.device][0] == 0 || smem_at[c.device] < smem) {
       cap[c.device][0] = clusters_at_once<T, 16>(c.device, smem) + 1;
       cap[c.device][1] = clusters_at_once<T, 8>(c.device, smem) + 1;
+      cap[c.device][2] = clusters_at_once<T, 4>(c.device, smem) + 1;
       smem_at[c.device] = smem;
       (void)cudaGetLastError();  // a refused query leaves no sticky error behind
     }
     n16 = cap[c.device][0] - 1;
     n8 = cap[c.device][1] - 1;
+    n4 = cap[c.device][2] - 1;
   }
   const char* f = std::getenv("DH_HEAD_CTAS");
-  const bool force8 = f && std::strcmp(f, "8") == 0;
-  if (!force8 && B <= n16) return 16;
-  if (B <= n8) return 8;
+  const int most = f ? std::atoi(f) : 16;
+  if (most >= 16 && B <= n16) return 16;
+  if (most >= 8 && B <= n8) return 8;
+  if (most >= 4 && B <= n4 && (long long)B * K <= 2048) return 4;
   return 0;
 }
 
 template <typename T>
 cudaError_t run(const Ctx& c, const HeadParams& p, int ctas) {
   const size_t smem = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
+  if (ctas == 4) return launch<T, 4>(c, p, smem);
   return ctas == 16 ? launch<T, 16>(c, p, smem) : launch<T, 8>(c, p, smem);
 }
 
 }  // namespace
 
-int head_cluster_ctas(const Ctx& c, int B, int d, int vocab, int dtype) {
-  // a wave of clusters holds at most one row per 8 SMs: larger batches need no query
-  if (B > c.num_sms / 8) return 0;
+int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype) {
+  // a wave of clusters holds at most one row per 4 SMs: larger batches need no query
+  if (B > c.num_sms / 4) return 0;
   const int n_groups = (vocab + GROUP - 1) / GROUP;
-  return dtype == DH_BF16 ? choose_ctas<__nv_bfloat16>(c, B, d, n_groups) : choose_ctas<float>(c, B, d, n_groups);
+  return dtype == DH_BF16 ? choose_ctas<__nv_bfloat16>(c, B, K, d, n_groups)
+                          : choose_ctas<float>(c, B, K, d, n_groups);
 }
 
 bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
@@ -496,7 +505,7 @@ cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, un
                                 const void* t, const void* V, const void* h, const void* W, int B, int d, int r,
                                 int vocab, int K, int dtype, int32_t* idx_out, float* score_out, float* logits,
                                 float* probs) {
-  if (ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
+  if (ctas != 4 && ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
   HeadParams p;
   p.recs = recs;
   p.acc = acc;

@@ -243,12 +243,12 @@ def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
     assert dh.workspace_status(ws) == 0
 
 
-@pytest.mark.parametrize("ctas", ["auto", "8"])
+@pytest.mark.parametrize("ctas", ["auto", "8", "4"])
 @pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
 def test_fused_head_matches_the_two_calls_over_K(K, ctas, monkeypatch):
     """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
     of candidates per CTA, and beyond one candidate per warp), with 16-CTA clusters where they fit
-    and with the portable 8."""
+    and with 8 and 4."""
     monkeypatch.setenv("DH_FORCE_HEAD", "cluster")
     if ctas != "auto":
         monkeypatch.setenv("DH_HEAD_CTAS", ctas)
@@ -261,6 +261,22 @@ def test_fused_head_matches_the_two_calls_over_K(K, ctas, monkeypatch):
     torch.cuda.synchronize()
     assert torch.equal(i2, idx) and torch.equal(s2, score)
     assert torch.equal(l2, logits) and torch.equal(p2, probs)
+
+
+@pytest.mark.parametrize("B", [16, 32])
+def test_fused_head_four_cta_clusters(B):
+    """Batches of 16 and 32 rows of 64 candidates (the four-CTA clusters where eight- and
+    sixteen-CTA ones do not fit one wave): against the oracle on every row, logits bit for bit
+    against the two calls (same per-candidate dot product order); the softmax of the two calls'
+    bulk-copy kernel adds in another order, so probabilities agree to rounding."""
+    cfg = inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=64)
+    x = inputs.make_head(cfg, seed=9, device=DEV)
+    idx, score, logits, probs = run_head(x, cfg.K, api="head")
+    i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    l2, p2 = dh.exact_rescore(x["h"], x["W"], i2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, i2) and torch.equal(score, s2) and torch.equal(logits, l2)
+    torch.testing.assert_close(probs, p2, rtol=0, atol=1e-6)
 
 
 def test_draft_head_without_probs_and_bad_rows():
