@@ -123,11 +123,13 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
  * idx_out / score_out as dh_lowrank_topk, logits_out / probs_out as dh_exact_rescore (probs_out
  * may be NULL).  h [B x d], U [d x r], V [r x vocab], W [vocab x d]: device, `dtype`, 16-byte
  * aligned, with d, r and vocab rows a multiple of 16 bytes; d <= 8192; limits and error codes as
- * for the two calls, bit for bit.  When the device runs one thread-block cluster per row for all
- * B rows at once (about a dozen rows on a GB300), the selection and the rescoring run as one
- * kernel, which removes a kernel boundary from the critical path; on the first call per device the
- * library queries how many such clusters fit (the environment variable DH_FORCE_HEAD=split runs the
- * two calls' kernels instead).
+ * for the two calls (bit for bit, except that where the two calls would use their bulk-copy
+ * rescoring kernel, from 2048 (row, candidate) pairs, probabilities agree to rounding).  When the
+ * device runs one thread-block cluster of 16, 8 or 4 CTAs per row for all B rows at once (with 4
+ * CTAs, for at most 2048 pairs: up to 32 rows of 64 candidates on a GB300), the selection and the
+ * rescoring run as one kernel, which removes a kernel boundary from the critical path; on the
+ * first call per device the library queries how many such clusters fit (the environment variable
+ * DH_FORCE_HEAD=split runs the two calls' kernels instead).
  * The workspace (dh_draft_head_workspace bytes, 256-byte aligned, caller-owned) must be zero-filled
  * before its first use and not shared by calls that overlap in time; the library leaves it ready
  * for the next call.

@@ -186,8 +186,8 @@ def exact_rescore(h, W, idx, *, with_probs=True, logits_out=None, probs_out=None
 def draft_head(h, U, V, W, K, *, with_probs=True, idx_out=None, score_out=None, logits_out=None,
                probs_out=None, workspace=None, stream=None):
     """Both stages in one call (dh_draft_head: the outputs of lowrank_topk followed by
-    exact_rescore, bit for bit, with selection and rescoring fused into one cluster kernel for
-    batches of up to about a dozen rows).  Returns (idx int32 [B,K], score fp32 [B,K],
+    exact_rescore, with selection and rescoring fused into one cluster kernel for small batches:
+    up to 32 rows of 64 candidates on a GB300).  Returns (idx int32 [B,K], score fp32 [B,K],
     logits fp32 [B,K], probs fp32 [B,K] or None)."""
     lib = load_library()
     _dev(h, "h"), _dev(U, "U"), _dev(V, "V"), _dev(W, "W")
