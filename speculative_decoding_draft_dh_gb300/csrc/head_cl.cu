@@ -311,10 +311,17 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     }
     __syncthreads();
     for (int i = threadIdx.x; i < need; i += HC_THREADS) my.sp[above + i] = my.wb[i];
-    // this CTA's candidates' W rows start towards L2 now (the certificate, and in the leader the
-    // sort, come before the dot products)
+    // Candidate positions of this CTA's warps: when the other CTAs have a warp for every
+    // candidate, the leader, which sorts, scores none; otherwise every CTA scores.  Warp w of
+    // scoring CTA c takes k = w * n_sc + c, k + n_sc * HC_WARPS, ...
+    const bool leader_sorts_only = K <= (HC_CTAS - 1) * HC_WARPS;
+    const int n_sc = leader_sorts_only ? HC_CTAS - 1 : HC_CTAS;
+    const int c_sc = leader_sorts_only ? (int)crank - 1 : (int)crank;  // -1: the leader
+    const int k_first = c_sc < 0 ? K : warp * n_sc + c_sc;
+    // this CTA's candidates' W rows start towards L2 now (the certificate comes before the dot
+    // products)
     if (lane == 0)
-      for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
+      for (int k = k_first; k < K; k += n_sc * HC_WARPS) {
         const int v = (int)(~(uint32_t)(k < (int)above ? my.sp[k] : my.wb[k - (int)above]));
         if (v >= 0 && v < p.vocab)
           prefetch_l2(static_cast<const T*>(p.W) + (size_t)v * p.d, (uint32_t)(p.d * sizeof(T)));
@@ -345,7 +352,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     }
     // exact logits of the winners by position, into the leader, while it sorts; they are used
     // unless the certificate sends the row to the leader's block selection
-    for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
+    for (int k = k_first; k < K; k += n_sc * HC_WARPS) {
       const int v = (int)(~(uint32_t)my.sp[k]);
       const bool ok = v >= 0 && v < p.vocab;
       const float acc = ok ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
