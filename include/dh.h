@@ -87,6 +87,14 @@ const char* dh_last_error(void);
  * h [B x d], U [d x r], V [r x vocab]: device, `dtype`.
  * idx_out [B x K] int32, score_out [B x K] fp32: device.
  * B = 0 is a no-op.  Limits: r <= DH_MAX_RANK, vocab <= DH_MAX_VOCAB, K <= min(vocab, DH_MAX_K).
+ *
+ * Precision of t on the small-batch path (bf16 with B <= 3, fp32 with B <= 8, r a multiple of 16):
+ * the projection is split over G <= 3 x (SM count) slices of d, each slice summed in fp32 and then
+ * added exactly as a 64-bit fixed-point number with 32 fraction bits, so t is bit-identical from
+ * call to call.  Range: every slice's partial sum and every |t[b,j]| must stay below 2^31; a slice
+ * beyond it raises bit (1 << DH_ERR_UNSUPPORTED) in the workspace status word (dh_workspace_status)
+ * and the call's outputs are unspecified.  Resolution: the fixed-point step adds at most G x 2^-33
+ * absolute error (under 1e-7 on a GB300) before t is rounded to `dtype`.
  * ------------------------------------------------------------------------------------------- */
 size_t dh_lowrank_topk_workspace(int B, int d, int r, int vocab, int K, int dtype);
 int dh_lowrank_topk(const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
@@ -128,8 +136,8 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
  * device runs one thread-block cluster of 16, 8 or 4 CTAs per row for all B rows at once (with 4
  * CTAs, for at most 2048 pairs: up to 32 rows of 64 candidates on a GB300), the selection and the
  * rescoring run as one kernel, which removes a kernel boundary from the critical path; on the
- * first call per device the library queries how many such clusters fit (the environment variable
- * DH_FORCE_HEAD=split runs the two calls' kernels instead).
+ * first call per device the library queries how many such clusters fit (the switch DH_FORCE_HEAD=split,
+ * see dh_set_tuning, runs the two calls' kernels instead).
  * The workspace (dh_draft_head_workspace bytes, 256-byte aligned, caller-owned) must be zero-filled
  * before its first use and not shared by calls that overlap in time; the library leaves it ready
  * for the next call.
@@ -176,7 +184,8 @@ int dh_expand_children(const float* probs, const int32_t* idx, const float* pare
  *
  * Node 0 of each request is the root (the last verified token; its token is ignored).  For node n
  * the target's next-token logits after n are logits[b, n, :].
- *   a[b,n]   = argmax_v logits[b,n,v]                      (ties -> lowest v, exact compare)
+ *   a[b,n]   = argmax_v logits[b,n,v]                      (ties -> lowest v, exact compare; a NaN
+ *              ranks below every number, and a row holding only NaN gives 0)
  *   acc[0]   = 1;  acc[n] = acc[parent[n]] && token[n] == a[b, parent[n]]
  *   last     = the accepted node of greatest depth          (ties -> lowest node index)
  *   len[b]   = depth(last) = number of accepted draft tokens
@@ -205,9 +214,10 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
  * receives device pointers.  Same inputs, outputs and results as dh_tree_accept; the per-node
  * scratch lives in a fixed array inside the library's device memory, so the call allocates
  * nothing.  Limit: B * N <= DH_TREE_NOALLOC_MAX_NODES (larger calls return DH_ERR_UNSUPPORTED and
- * dh_last_error says why).  The first call on each device (with that device current) looks up the
- * array's device address; make it before any stream capture.  All calls on a device share the
- * array, so calls whose kernels overlap on the GPU race on it: order them (one stream).
+ * dh_last_error says why).  Every call looks up the array's device address in the current context
+ * (a host-side query, so the address stays right after a device reset); the first call on a device
+ * may load the library's device code, so make it before any stream capture.  All calls on a device
+ * share the array, so calls whose kernels overlap on the GPU race on it: order them (one stream).
  * ------------------------------------------------------------------------------------------- */
 #define DH_TREE_NOALLOC_MAX_NODES (1 << 18)
 int dh_tree_accept_noalloc(const void* logits, const int32_t* parent, const int32_t* token, int B, int N,
@@ -227,12 +237,11 @@ int dh_workspace_status(void* workspace, void* stream, int* status_out);
 /* ---------------------------------------------------------------------------------------------
  * Self-test of the bounded device-side waits (no counterpart on the pages).
  *
- * Queues one small kernel that waits, with the same code the pipelined kernels use, on a
- * condition that is never met: mode 0 an mbarrier nothing arrives at, mode 1 a grid barrier that
- * expects one block more than the grid has.  The wait gives up after limit_us microseconds
- * (1..1000000) and raises bit (1 << DH_ERR_TIMEOUT) in the workspace status word, which
- * dh_workspace_status then reports; the CUDA context stays usable.  workspace: a zero-filled
- * device buffer of at least 256 bytes, 256-byte aligned (its barrier counter is left at zero).
+ * Queues one small kernel that waits, with the code the pipelined kernels use for their TMA,
+ * bulk-copy and MMA completions, on an mbarrier that nothing arrives at (mode must be 0).  The wait
+ * gives up after limit_us microseconds (1..1000000) and raises bit (1 << DH_ERR_TIMEOUT) in the
+ * workspace status word, which dh_workspace_status then reports; the CUDA context stays usable.
+ * workspace: a zero-filled device buffer of at least 256 bytes, 256-byte aligned.
  * ------------------------------------------------------------------------------------------- */
 int dh_selftest_wait_timeout(int mode, int limit_us, void* workspace, size_t ws_bytes, void* stream);
 
@@ -248,6 +257,22 @@ int dh_selftest_wait_timeout(int mode, int limit_us, void* workspace, size_t ws_
  * ------------------------------------------------------------------------------------------- */
 int dh_prof_enable(int on);
 int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int max_kernels);
+
+/* ---------------------------------------------------------------------------------------------
+ * Test and tuning switches (no counterpart on the pages): which kernels serve a call.  Results do
+ * not depend on them beyond the choice of kernels.
+ *
+ * Each switch is read once per process from the environment variable of the same name, on the
+ * library's first use of it, and afterwards changes only through this call.  name / value:
+ *   "DH_FORCE_PATH"    "auto" | "gemv" | "mma" | "fused"  stage-1 path, when it supports the shape
+ *   "DH_FORCE_HEAD"    "auto" | "split"                  dh_draft_head without the cluster head
+ *   "DH_HEAD_CTAS"     "16" | "8" | "4"                  largest cluster of the fused head
+ *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket"  stage-2 kernel
+ *   "DH_SCORES_SMALL"  "lsu" | "tma"                     small-batch scores kernel
+ * value NULL or "" restores the default.  Unknown names or values return DH_ERR_INVALID_ARG.  Not
+ * synchronised with calls running on other host threads: set switches before such calls.
+ * ------------------------------------------------------------------------------------------- */
+int dh_set_tuning(const char* name, const char* value);
 
 #ifdef __cplusplus
 }

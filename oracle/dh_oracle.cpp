@@ -24,7 +24,8 @@
 //   section "How it works": the target checks every drafted token in one pass, matching tokens
 //   are kept and the first mismatch is replaced by the target's own token; EAGLE-4 summary page,
 //   section "Distribution preservation...": greedy decoding follows the target's choices.
-//     6. a[b,n] = argmax_v L[b,n,v] (ties -> lowest v), over the stored values;
+//     6. a[b,n] = argmax_v L[b,n,v] (ties -> lowest v), over the stored values (a NaN ranks
+//        below every number; a row of NaN only gives 0);
 //        acc[0] = 1, acc[n] = acc[parent[n]] and token[n] == a[b,parent[n]];
 //        the deepest accepted node (ties -> lowest node index) ends the accepted path;
 //        len = its depth, path = root..node, bonus = a[b,node].
@@ -201,14 +202,16 @@ int oracle_tree_accept(const void* logits, const int32_t* parent, const int32_t*
     const int b = row_of(reqs, i);
     int32_t* a = argmax_out + (size_t)i * N;
     for (int n = 0; n < N; ++n) {
+      // NaN ranks below every number: it never becomes the argmax; a row holding only NaN gives 0
       const size_t base = ((size_t)b * N + n) * (size_t)vocab;
-      double best = stored_value(logits, dtype, base);
-      int32_t arg = 0;
-      for (int v = 1; v < vocab; ++v) {
+      double best = 0.0;
+      int32_t arg = -1;
+      for (int v = 0; v < vocab; ++v) {
         const double x = stored_value(logits, dtype, base + v);
-        if (x > best) { best = x; arg = v; }
+        if (std::isnan(x)) continue;
+        if (arg < 0 || x > best) { best = x; arg = v; }
       }
-      a[n] = arg;
+      a[n] = arg < 0 ? 0 : arg;
     }
     const int32_t* par = parent + (size_t)b * N;
     const int32_t* tok = token + (size_t)b * N;

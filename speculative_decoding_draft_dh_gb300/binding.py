@@ -24,7 +24,8 @@ EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_w
            "dh_exact_rescore_workspace", "dh_exact_rescore", "dh_draft_head_workspace", "dh_draft_head",
            "dh_expand_children",
            "dh_tree_accept_workspace",
-           "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read"]
+           "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read",
+           "dh_set_tuning"]
 
 _lib = None
 _lock = threading.Lock()
@@ -81,6 +82,8 @@ def load_library(path: str | None = None):
         lib.dh_prof_enable.restype = I
         lib.dh_prof_read.argtypes = [P, I, P, P, I]
         lib.dh_prof_read.restype = I
+        lib.dh_set_tuning.argtypes = [ctypes.c_char_p, ctypes.c_char_p]
+        lib.dh_set_tuning.restype = I
         if path is None:
             _lib = lib
         return lib
@@ -278,18 +281,22 @@ def workspace_status(workspace: "Workspace | None" = None, device=None, stream=N
     return status
 
 
-def selftest_wait_timeout(mode: int, limit_us: int = 50000, stream=None) -> int:
-    """Run the bounded-wait self-test (mode 0: mbarrier, 1: grid barrier) on a fresh workspace and
-    return the status word it left (expected: 1 << DH_ERR_TIMEOUT)."""
+def selftest_wait_timeout(limit_us: int = 50000, stream=None) -> int:
+    """Run the bounded-wait self-test (an mbarrier wait that nothing completes) on a fresh workspace
+    and return the status word it left (expected: 1 << DH_ERR_TIMEOUT)."""
     lib = load_library()
     ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
-    _check(lib.dh_selftest_wait_timeout(mode, limit_us, _ptr(ws), 256, _stream(stream)),
+    _check(lib.dh_selftest_wait_timeout(0, limit_us, _ptr(ws), 256, _stream(stream)),
            "dh_selftest_wait_timeout")
     out = ctypes.c_int(0)
     _check(lib.dh_workspace_status(_ptr(ws), _stream(stream), ctypes.byref(out)), "dh_workspace_status")
-    if int(ws[64:68].view(torch.int32).item()) != 0:
-        raise DhError(5, "dh_selftest_wait_timeout", "barrier counter not restored")
     return out.value
+
+
+def set_tuning(name: str, value: str | None):
+    """Set one test or tuning switch (kernel choice only; None restores the default)."""
+    lib = load_library()
+    _check(lib.dh_set_tuning(name.encode(), None if value is None else str(value).encode()), "dh_set_tuning")
 
 
 def prof_enable(on: bool):

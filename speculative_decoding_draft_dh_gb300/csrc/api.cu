@@ -63,13 +63,13 @@ enum Path { PATH_GEMV, PATH_MMA, PATH_FUSED };
 
 // Stage-1 path: the small-batch pipeline (projection + scores kernels) up to SMALL_MAX_B rows where
 // the tensor-core path applies and up to 8 rows otherwise, the tensor-core kernels for larger bf16
-// batches, the multi-kernel CUDA-core path for the rest.  DH_FORCE_PATH=gemv|mma|fused overrides
-// the choice when the forced path supports the shape (tests and tuning).
+// batches, the multi-kernel CUDA-core path for the rest.  The DH_FORCE_PATH switch (gemv, mma or
+// fused) overrides the choice when the forced path supports the shape (tests and tuning).
 Path choose_path(int B, int r, int dtype) {
-  const char* f = std::getenv("DH_FORCE_PATH");
-  if (f && std::strcmp(f, "gemv") == 0) return PATH_GEMV;
-  if (f && std::strcmp(f, "mma") == 0 && mma_path_supported(B, r, dtype)) return PATH_MMA;
-  if (f && std::strcmp(f, "fused") == 0 && small_b_supported(B, r, dtype)) return PATH_FUSED;
+  const Tuning::Path f = tuning().force_path;
+  if (f == Tuning::PATH_GEMV) return PATH_GEMV;
+  if (f == Tuning::PATH_MMA && mma_path_supported(B, r, dtype)) return PATH_MMA;
+  if (f == Tuning::PATH_FUSED && small_b_supported(B, r, dtype)) return PATH_FUSED;
   // from SMALL_MAX_B rows on, the tensor-core path is faster where it applies (bf16)
   if (small_b_supported(B, r, dtype) && !(B > SMALL_MAX_B && mma_path_supported(B, r, dtype))) return PATH_FUSED;
   if (mma_path_supported(B, r, dtype) && B > SMALL_MAX_B) return PATH_MMA;
@@ -212,15 +212,15 @@ int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, i
   return DH_OK;
 }
 
-// Stage 2 after validation: the ring kernel from 2048 pairs, the direct kernels below.
-// DH_FORCE_RESCORE=direct|ring overrides the choice by batch size (tests and tuning).
+// Stage 2 after validation: the ring kernel from 2048 pairs, the direct kernels below.  The
+// DH_FORCE_RESCORE switch (direct or ring) overrides the choice by batch size (tests and tuning).
 int run_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
                 int dtype, float* logits_out, float* probs_out, uint32_t* tickets, int* status) {
-  const char* f = std::getenv("DH_FORCE_RESCORE");
+  const Tuning::Rescore f = tuning().rescore;
   const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
   bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
-  if (f && std::strcmp(f, "direct") == 0) ring = false;
-  if (f && std::strcmp(f, "ring") == 0) ring = ring_ok;
+  if (f == Tuning::RESCORE_DIRECT || f == Tuning::RESCORE_TICKET) ring = false;
+  if (f == Tuning::RESCORE_RING) ring = ring_ok;
   const cudaError_t e =
       ring ? note_error(launch_rescore_ring(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
                                             status),
@@ -312,10 +312,9 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   char* ws = static_cast<char*>(workspace);
   // Batches whose rows the fused cluster head takes in one wave: the stage-1 kernels, then
-  // selection and rescoring in one cluster kernel; larger batches (or DH_FORCE_HEAD=split): the
-  // selection and rescoring kernels.
-  const char* f = std::getenv("DH_FORCE_HEAD");
-  const bool split = f && std::strcmp(f, "split") == 0;
+  // selection and rescoring in one cluster kernel; larger batches (or the DH_FORCE_HEAD=split
+  // switch): the selection and rescoring kernels.
+  const bool split = tuning().head_split;
   const int ctas = split || !head_cluster_supported(B, d, vocab, K, dtype) ? 0
                                                                           : head_cluster_ctas(c, B, K, d, vocab, dtype);
   Stage1 s1;

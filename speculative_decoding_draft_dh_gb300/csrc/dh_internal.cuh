@@ -10,11 +10,8 @@
 namespace dh {
 
 // Every workspace starts with a 256-byte header whose first word collects device-side status bits
-// (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.  Bytes 64-71
-// hold a grid barrier (bounded-wait self-test), bytes 72-75 the small-batch projection's ticket.
+// (1 << dh_status) raised by bounded waits; dh_workspace_status reads and clears it.
 constexpr size_t WS_HEADER = 256;
-constexpr size_t WS_BARRIER_OFFSET = 64;
-constexpr size_t WS_TICKET_OFFSET = 72;
 // Fixed-point accumulators of the small-batch projection (8 copies of B * r <= 2048 int64), right
 // after the header in the stage-1 workspace.
 constexpr size_t WS_FIX_BYTES = 8 * 2048 * 8;
@@ -178,6 +175,19 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 }
 
 // ------------------------------------------------------------------ host side
+
+// Test and tuning switches (tuning.cu): read from the environment once per process, changed only by
+// dh_set_tuning.  They select kernels; results do not depend on them.
+struct Tuning {
+  enum Path { PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_FUSED };
+  enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET };
+  Path force_path = PATH_AUTO;      // stage-1 path, when the forced one supports the shape
+  bool head_split = false;          // dh_draft_head: the two calls' kernels, not the cluster head
+  int head_ctas_max = 16;           // largest cluster of the fused head (16, 8 or 4)
+  Rescore rescore = RESCORE_AUTO;   // stage-2 kernel choice
+  bool scores_tma = false;          // small-batch scores: the TMA variant for every rank
+};
+const Tuning& tuning();
 
 struct Ctx {
   int device;

@@ -331,8 +331,12 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     bool mine = false;
 #pragma unroll
     for (int q = 0; q < HC_RPT; ++q) mine |= fkey(rec[q].m3) >= tau && (g0 + (int)threadIdx.x + q * HC_THREADS) < g1;
+    // every CTA's own count gets the flags, so that after the barrier below each CTA reads only
+    // its own shared memory (the leader may exit as soon as it has passed that barrier)
     const uint32_t bm = __ballot_sync(0xFFFFFFFFu, mine);
-    if (lane == 0 && bm) atomicAdd(&L.nref, (uint32_t)__popc(bm));
+    if (lane == 0 && bm)
+#pragma unroll
+      for (int c = 0; c < HC_CTAS; ++c) atomicAdd(cl.map_shared_rank(&my.nref, (unsigned)c), (uint32_t)__popc(bm));
     __syncthreads();  // sp[0, K) complete in this CTA
     if (leader) {
       // the winners' order: rank by counting, outputs written in rank order
@@ -359,7 +363,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
       if (lane == 0) L.zu[k] = ok ? acc : __int_as_float(0x7FC00000);
     }
     cluster_sync_all();
-    fallback = L.nref != 0u;
+    fallback = my.nref != 0u;
     if (!fallback) {
       if (!leader) return;
       // zero the row's accumulators for the next call (select_row does it on the other branch)
@@ -454,7 +458,7 @@ int clusters_at_once(int device, size_t smem) {
 // pairs (32 rows x 64: 31.0 against 39.0 µs per call; 16 x 64: 29.3 against 32.6) but not beyond
 // (64 x 128: 77.6 against 56.4).  The device's capacities are queried once per device and element
 // type (set-up calls: shared memory limit, the non-portable size, the occupancy query).
-// DH_HEAD_CTAS=8 or 4 skips the larger forms (tests).
+// The DH_HEAD_CTAS switch (8 or 4) skips the larger forms (tests).
 template <typename T>
 int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const size_t smem = hc_fb_offset(d, (int)sizeof(T)) + sel::select_smem_bytes(n_groups);
@@ -476,8 +480,7 @@ int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
     n8 = cap[c.device][1] - 1;
     n4 = cap[c.device][2] - 1;
   }
-  const char* f = std::getenv("DH_HEAD_CTAS");
-  const int most = f ? std::atoi(f) : 16;
+  const int most = tuning().head_ctas_max;
   if (most >= 16 && B <= n16) return 16;
   if (most >= 8 && B <= n8) return 8;
   if (most >= 4 && B <= n4 && (long long)B * K <= 2048) return 4;

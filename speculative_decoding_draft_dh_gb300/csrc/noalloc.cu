@@ -10,13 +10,13 @@
 // is allocated at call time.
 //
 // Host code cannot use the array's name as a device address (on the host it names a stand-in
-// object), so the first call on each device, with that device current, asks the runtime for the
-// array's device address with cudaGetSymbolAddress and keeps it for later calls.  That first call
-// should therefore happen before any stream capture.  Every call on a device shares the one array:
-// calls whose kernels overlap on the GPU (for example on two streams) race on it and must be
-// ordered by the caller.
-#include <mutex>
-
+// object), so every call asks the runtime for the array's device address on the current device with
+// cudaGetSymbolAddress (a host-side lookup: no allocation, no synchronisation).  Asking on every
+// call, rather than caching the address, keeps it right after cudaDeviceReset or a new primary
+// context, which load the module again, possibly at another address.  The first call on a device
+// may load the module, so it should come before any stream capture.  Every call on a device shares
+// the one array: calls whose kernels overlap on the GPU (for example on two streams) race on it and
+// must be ordered by the caller.
 #include "dh_internal.cuh"
 
 namespace dh {
@@ -25,22 +25,13 @@ namespace {
 // Per-node argmax scratch: DH_TREE_NOALLOC_MAX_NODES int32 entries (B * N nodes per call).
 static __device__ __align__(256) int32_t g_tree_scratch[DH_TREE_NOALLOC_MAX_NODES];
 
-constexpr int kMaxDev = 64;
-std::mutex g_mu;
-int32_t* g_scratch_ptr[kMaxDev];  // device address of g_tree_scratch per device (nullptr: not set up)
-
-// Returns the device address of the scratch array on `device` (the current device), setting it up
-// on first use.  nullptr if the runtime cannot resolve the symbol.
-int32_t* scratch_for(int device) {
-  std::lock_guard<std::mutex> lk(g_mu);
-  if (device < 0 || device >= kMaxDev) return nullptr;
-  if (!g_scratch_ptr[device]) {
-    void* p = nullptr;
-    cudaError_t e = cudaGetSymbolAddress(&p, g_tree_scratch);
-    if (note_error(e, "cudaGetSymbolAddress(tree scratch)") != cudaSuccess) return nullptr;
-    g_scratch_ptr[device] = static_cast<int32_t*>(p);
-  }
-  return g_scratch_ptr[device];
+// Device address of g_tree_scratch in the current context; nullptr if the runtime cannot resolve
+// the symbol (the failure is recorded for dh_last_error).
+int32_t* scratch_address() {
+  void* p = nullptr;
+  if (note_error(cudaGetSymbolAddress(&p, g_tree_scratch), "cudaGetSymbolAddress(tree scratch)") != cudaSuccess)
+    return nullptr;
+  return static_cast<int32_t*>(p);
 }
 
 }  // namespace
@@ -64,7 +55,7 @@ extern "C" int dh_tree_accept_noalloc(const void* logits, const int32_t* parent,
     return DH_ERR_UNSUPPORTED;
   Ctx c;
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
-  int32_t* scratch = scratch_for(c.device);
+  int32_t* scratch = scratch_address();
   if (!scratch) return DH_ERR_CUDA;
   if (note_error(launch_tree(c, logits, parent, token, B, N, vocab, dtype, scratch, argmax_out, path_out, len_out,
                              bonus_out, err_out),

@@ -424,9 +424,8 @@ cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
                 int K, float* logits, float* probs, uint32_t* tickets) {
-  // K <= CL_MAX_K: the cluster kernel (DH_FORCE_RESCORE=ticket selects the ticket kernel instead)
-  const char* f = std::getenv("DH_FORCE_RESCORE");
-  if (K <= CL_MAX_K && !(f && std::strcmp(f, "ticket") == 0))
+  // K <= CL_MAX_K: the cluster kernel (the DH_FORCE_RESCORE=ticket switch selects the ticket kernel)
+  if (K <= CL_MAX_K && tuning().rescore != Tuning::RESCORE_TICKET)
     return run_cl<T>(c, h, W, idx, B, d, vocab, K, logits, probs);
   // Small problems use 2-warp blocks so that more SMs pull W rows; larger ones 8-warp blocks.
   const int nw = (long long)B * K <= 512 ? 2 : WARPS;

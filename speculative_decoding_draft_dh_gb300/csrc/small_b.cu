@@ -73,7 +73,14 @@ struct ProjSmall {
   const void* U;
   int B, d, r;
   unsigned long long* acc;  // [ACC_COPIES][B*r] fixed-point accumulators (zero between calls)
+  int* status;              // workspace status word
 };
+
+// Fixed-point range: a block's partial v converts to round(v * 2^32) in a signed 64-bit integer,
+// so |v| must stay below 2^31; the integer sums are exact (modulo 2^64) as long as every final
+// |t| stays below 2^31 too.  Beyond that the conversion saturates: the block raises
+// DH_ERR_UNSUPPORTED in the status word and the call's outputs are unspecified.
+constexpr float FIX_LIMIT = 2147483648.0f;  // 2^31
 
 // NB = B (1..MAX_B): the accumulators are sized for the batch, so that at batch 1 a projection
 // block holds few registers and the scores kernel's blocks, launched early, fit beside it.
@@ -140,6 +147,7 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
         float v = 0.f;
 #pragma unroll
         for (int q = 0; q < PJ_GROUPS; ++q) v += red[q][q2];
+        if (!(fabsf(v) < FIX_LIMIT)) atomicOr(p.status, 1 << DH_ERR_UNSUPPORTED);
         const long long fx = __float2ll_rn(v * FIX_SCALE);
         atomicAdd(p.acc + (size_t)(c % ACC_COPIES) * BR + bb * r + jj, (unsigned long long)fx);
       }
@@ -455,6 +463,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   pp.d = d;
   pp.r = r;
   pp.acc = acc;
+  pp.status = status;
   cudaLaunchConfig_t cfg = {};
   // three blocks per SM: more row slices keep more of U in flight (batch 1, µs per call: 21.5 with
   // one block per SM, 19.4 with two, 19.05 with three, 19.2 with four)
@@ -482,8 +491,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   sp.n_tiles = (vocab + TILE - 1) / TILE;
   sp.recs = recs;
   sp.status = status;
-  const char* f = std::getenv("DH_SCORES_SMALL");
-  const bool lsu = r % (LSU_WARPS * 16) == 0 && !(f && std::strcmp(f, "tma") == 0);
+  const bool lsu = r % (LSU_WARPS * 16) == 0 && !tuning().scores_tma;
   if (lsu) {
     constexpr int TW = 32 * Elem<T>::PER16;
     cfg.gridDim = dim3((unsigned)((vocab + TW - 1) / TW));

@@ -29,7 +29,10 @@ __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsig
 // Each thread scans its 16-byte vectors in increasing id order keeping (best value, its id).  Per
 // vector it takes the max with an fmax tree and only searches for the id when that max beats the
 // running best (strictly: an equal value later in the row has a larger id), which happens a few
-// times per thread.  The block then reduces (value, id) with ties to the lower id.
+// times per thread.  The block then reduces (value, id) with ties to the lower id.  NaN ranks below
+// every number: fmaxf drops NaN operands, a vector of NaN only (max NaN) is skipped, and a thread
+// that saw no number keeps its first id with key 0, below the key of any number, so a row holding
+// only NaN gives its lowest id, 0.
 template <typename T>
 __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restrict__ logits, int vocab,
                                                                 int32_t* __restrict__ am) {
@@ -56,7 +59,7 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restr
         float m = x[0];
 #pragma unroll
         for (int e = 1; e < PER; ++e) m = fmaxf(m, x[e]);
-        if (m > best || best_id < 0) {
+        if (m > best || (best_id < 0 && m == m)) {
           int e0 = 0;
 #pragma unroll
           for (int e = PER - 1; e >= 0; --e)
@@ -67,9 +70,13 @@ __global__ void __launch_bounds__(ARGMAX_THREADS) k_tree_argmax(const T* __restr
       }
     }
   }
-  unsigned long long key = best_id < 0 ? 0ull
-                                        : ((unsigned long long)fkey(best) << 32) |
-                                              (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_id);
+  // fkey of any number is at least fkey(-inf) = 0x007FFFFF > 0, so a thread without a number
+  // (key high word 0) ranks below every thread with one
+  const int first_id = (int)threadIdx.x * PER;
+  unsigned long long key = best_id >= 0 ? ((unsigned long long)fkey(best) << 32) |
+                                              (unsigned long long)(0xFFFFFFFFu - (uint32_t)best_id)
+                           : first_id < vocab ? (unsigned long long)(0xFFFFFFFFu - (uint32_t)first_id)
+                                              : 0ull;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) key = umax64(key, __shfl_xor_sync(0xFFFFFFFFu, key, o));
   if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = key;

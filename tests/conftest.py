@@ -24,3 +24,18 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture
+def tune():
+    """Sets a library tuning switch (dh_set_tuning) for one test and restores the default after it."""
+    from speculative_decoding_draft_dh_gb300 import binding as dh
+    changed = []
+
+    def set_switch(name, value):
+        dh.set_tuning(name, value)
+        changed.append(name)
+
+    yield set_switch
+    for name in changed:
+        dh.set_tuning(name, None)

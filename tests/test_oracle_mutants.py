@@ -30,8 +30,10 @@ MUTANTS = [
      ["test_K_equals_vocab_reduces_to_full_softmax", "test_softmax_invariants"]),
     ("tree_compares_own_argmax", "tok[n] == a[par[n]]", "tok[n] == a[n]",
      ["test_golden_trees", "test_random_trees_against_brute_force"]),
-    ("argmax_last_tie", "if (x > best) { best = x; arg = v; }", "if (x >= best) { best = x; arg = v; }",
-     ["test_golden_trees"]),
+    ("argmax_last_tie", "if (arg < 0 || x > best) { best = x; arg = v; }",
+     "if (arg < 0 || x >= best) { best = x; arg = v; }", ["test_golden_trees"]),
+    ("argmax_takes_nan", "if (std::isnan(x)) continue;", "",
+     ["test_tree_argmax_nan_ranks_below_numbers"]),
     ("deepest_tie_highest_index", "depth[n] > depth[best]", "depth[n] >= depth[best]",
      ["test_golden_trees"]),
     ("expand_ties_by_position", "return tk[x] < tk[y];", "return x < y;",

@@ -272,6 +272,36 @@ def test_random_trees_against_brute_force(tcfg):
     assert total_len > 0  # the 0.7 boost makes acceptance non-trivial
 
 
+def _brute_argmax_nan_last(row):
+    """Lowest id holding the largest number of the row; NaN never wins; 0 if the row has no number."""
+    best = None
+    for v, x in enumerate(row.tolist()):
+        if x != x:
+            continue
+        if best is None or x > row[best]:
+            best = v
+    return 0 if best is None else best
+
+
+def test_tree_argmax_nan_ranks_below_numbers():
+    nan, inf = np.nan, np.inf
+    rows = np.array([[nan, 1.0, 3.0, 3.0, -2.0, nan, 0.5, 2.0],
+                     [3.0, nan, 3.0, 1.0, nan, nan, 9.0, nan],
+                     [nan] * 8,
+                     [nan, -inf, -inf, nan, nan, nan, nan, nan],
+                     [-inf, nan, 5.0, nan, 5.0, -1.0, nan, 4.0],
+                     [nan, nan, nan, nan, nan, nan, nan, -7.0]], dtype=np.float32)
+    N = rows.shape[0]
+    logits = rows.reshape(1, N, 8)
+    parent = np.array([[-1] + list(range(N - 1))], dtype=np.int32)
+    want = [_brute_argmax_nan_last(r) for r in rows]
+    assert want == [2, 6, 0, 1, 2, 7]
+    token = np.array([[0] + want[:-1]], dtype=np.int32)  # every edge matches: a chain
+    out = oracle.tree_accept(logits, parent, token)
+    assert out["argmax"][0].tolist() == want
+    assert out["len"][0] == N - 1 and out["bonus"][0] == want[-1]
+
+
 def test_tree_generator_shape_limits():
     tcfg = inputs.tree_config("tree", B=8, vocab=1024)
     par = inputs.make_parents(tcfg.B, tcfg.N, 0, tcfg.max_depth, tcfg.max_children)

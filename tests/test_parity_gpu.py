@@ -112,11 +112,11 @@ def test_clustered_candidates_are_refined(api):
 
 
 @pytest.mark.parametrize("B", [1, 8])
-def test_tensor_core_path_fused_head_refines_clustered_rows(B, monkeypatch):
+def test_tensor_core_path_fused_head_refines_clustered_rows(B, tune):
     """Tensor-core stage 1 (t in bf16) followed by the fused cluster head, on rows whose top
     candidates crowd one group (refinement by the leader's block selection) and on plain rows:
     against the oracle, and bit for bit against the two calls."""
-    monkeypatch.setenv("DH_FORCE_PATH", "mma")
+    tune("DH_FORCE_PATH", "mma")
     cfg = inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=32)
     x = inputs.make_head(cfg, seed=8, device=DEV)
     v = _best_column(x)
@@ -180,10 +180,10 @@ def test_rescore_bad_index_gives_nan_row():
 
 
 @pytest.mark.parametrize("path", ["direct", "ring", "ticket"])
-def test_rescore_paths_small_shapes(path, monkeypatch):
+def test_rescore_paths_small_shapes(path, tune):
     """Each stage-2 kernel (direct = the cluster kernel for K <= 128) on fp32 and bf16 rows, K not a
     multiple of the ring's chunk nor of the cluster's warps."""
-    monkeypatch.setenv("DH_FORCE_RESCORE", path)
+    tune("DH_FORCE_RESCORE", path)
     for cfg in (inputs.head_config("tiny", B=3, K=45), inputs.HeadConfig("r", 5, 768, 4096, 64, 70, "bf16", 0.1, True)):
         x = inputs.make_head(cfg, seed=17, device=DEV)
         idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
@@ -217,16 +217,16 @@ def test_batch1_full_size(api):
 @pytest.mark.parametrize("mode", ["auto", "cluster8", "split"])
 @pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
                                     ("high", 512)])
-def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
+def test_draft_head_matches_the_two_calls(name, B, mode, tune):
     """dh_draft_head gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same
     selection rule on the same records and the same per-candidate dot product order; twice in a
     row with one workspace (its state resets itself).  "auto" takes the fused cluster kernel
     (selection and rescoring in one launch) where the batch is small enough, "cluster8" the same
     with 8-CTA clusters, "split" the two kernels."""
     if mode == "cluster8":
-        monkeypatch.setenv("DH_HEAD_CTAS", "8")
+        tune("DH_HEAD_CTAS", "8")
     elif mode != "auto":
-        monkeypatch.setenv("DH_FORCE_HEAD", mode)
+        tune("DH_FORCE_HEAD", mode)
     cfg = inputs.head_config(name, B=B)
     x = inputs.make_head(cfg, seed=11, device=DEV)
     h, U, V, W = x["h"], x["U"], x["V"], x["W"]
@@ -245,13 +245,13 @@ def test_draft_head_matches_the_two_calls(name, B, mode, monkeypatch):
 
 @pytest.mark.parametrize("ctas", ["auto", "8", "4"])
 @pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
-def test_fused_head_matches_the_two_calls_over_K(K, ctas, monkeypatch):
+def test_fused_head_matches_the_two_calls_over_K(K, ctas, tune):
     """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
     of candidates per CTA, and beyond one candidate per warp), with 16-CTA clusters where they fit
     and with 8 and 4."""
-    monkeypatch.setenv("DH_FORCE_HEAD", "cluster")
+    tune("DH_FORCE_HEAD", "cluster")
     if ctas != "auto":
-        monkeypatch.setenv("DH_HEAD_CTAS", ctas)
+        tune("DH_HEAD_CTAS", ctas)
     cfg = inputs.head_config("tiny", B=3, K=K)
     x = inputs.make_head(cfg, seed=21, device=DEV)
     h, U, V, W = x["h"], x["U"], x["V"], x["W"]
@@ -359,9 +359,28 @@ def test_tree_bf16_ties_and_single_node():
     assert g["argmax"][1, 0] == 0 and g["len"].tolist() == [0, 0, 0]
 
 
-def test_tree_full_size_sampled():
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_tree_argmax_nan_rows(dtype):
+    """NaN ranks below every number (a row of NaN only gives id 0), as in the oracle."""
+    tcfg = inputs.tree_config("tree", B=2, N=8, vocab=4104, dtype=dtype)
+    t = inputs.make_tree(tcfg, seed=5, device=DEV)
+    L = t["logits"]
+    nan = float("nan")
+    L[0, 0, :64] = nan                # NaN vectors first in every thread's scan
+    L[0, 1, :] = nan                  # NaN only
+    L[0, 2, 1::2] = nan               # NaN in every vector
+    L[0, 3, :] = float("-inf")
+    L[0, 3, 7::11] = nan              # -inf numbers beat NaN
+    L[1, 4, 4096:] = nan              # NaN in the ragged tail
+    L[1, 5, :] = nan                  # one number left, in the tail
+    L[1, 5, 4101] = -3.0
+    g = run_tree(t)
+    assert g["argmax"][0, 1] == 0 and g["argmax"][0, 3] == 0 and g["argmax"][1, 5] == 4101
+
+
+def test_tree_full_size_every_request():
     t = inputs.make_tree(inputs.TREE_CONFIGS["tree"], seed=0, device=DEV)
-    g = run_tree(t, reqs=[0, 1, 100, 200, 255])
+    g = run_tree(t)
     assert g["len"].mean() > 0.5
 
 
@@ -378,8 +397,8 @@ MMA_SHAPES = [
 
 @pytest.mark.parametrize("cfg", MMA_SHAPES, ids=lambda c: c.name)
 @pytest.mark.parametrize("path", ["mma", "gemv", "fused"])
-def test_forced_stage1_path(cfg, path, monkeypatch):
-    monkeypatch.setenv("DH_FORCE_PATH", path)
+def test_forced_stage1_path(cfg, path, tune):
+    tune("DH_FORCE_PATH", path)
     x = inputs.make_head(cfg, seed=11, device=DEV)
     rows = list(range(cfg.B)) if cfg.B <= 8 else [0, 1, cfg.B // 2, cfg.B - 1]
     run_head(x, cfg.K, rows=rows)
@@ -388,46 +407,84 @@ def test_forced_stage1_path(cfg, path, monkeypatch):
 
 @pytest.mark.parametrize("B", [1, 4, 8])
 @pytest.mark.parametrize("path", ["gemv", "fused"])
-def test_small_batch_paths_fp32(B, path, monkeypatch):
-    monkeypatch.setenv("DH_FORCE_PATH", path)
+def test_small_batch_paths_fp32(B, path, tune):
+    tune("DH_FORCE_PATH", path)
     cfg = inputs.head_config("tiny", B=B, K=32)
     x = inputs.make_head(cfg, seed=20 + B, device=DEV)
     run_head(x, cfg.K)
     assert dh.workspace_status() == 0
 
 
-def test_batch1_forced_gemv(monkeypatch):
-    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+@pytest.mark.parametrize("scale", [1e-4, 1e4])
+@pytest.mark.parametrize("B", [1, 3])
+def test_small_batch_projection_scaled_h(scale, B, tune):
+    """The small-batch projection's fixed-point sum (32 fraction bits) against the oracle with h far
+    from its usual scale: small values keep their relative precision, large ones stay in range."""
+    tune("DH_FORCE_PATH", "fused")
+    cfg = inputs.head_config("batch1", B=B, vocab=16384)
+    x = inputs.make_head(cfg, seed=3, device=DEV)
+    x["h"] = (x["h"].float() * scale).to(torch.bfloat16)
+    ws = dh.Workspace()
+    idx, score = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.workspace_status(ws) == 0
+    s_full = oracle.lowrank_scores(x["h"].cpu(), x["U"].cpu(), x["V"].cpu())
+    for b in range(B):
+        check_candidates(idx[b].cpu().numpy(), score[b].cpu().numpy(), s_full[b], cfg.K, where=f"scale {scale} row {b}")
+
+
+def test_small_batch_projection_overflow_is_reported(tune):
+    """A projection beyond the fixed-point range (|t| >= 2^31) raises DH_ERR_UNSUPPORTED in the
+    workspace status word instead of passing silently."""
+    tune("DH_FORCE_PATH", "fused")
+    cfg = inputs.head_config("batch1", vocab=16384)
+    x = inputs.make_head(cfg, seed=3, device=DEV)
+    x["h"] = (x["h"].float() * 1e12).to(torch.bfloat16)
+    ws = dh.Workspace()
+    dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.workspace_status(ws) & (1 << 2)
+    # the workspace stays usable: a call at the usual scale is exact again
+    x2 = inputs.make_head(cfg, seed=4, device=DEV)
+    idx, score = dh.lowrank_topk(x2["h"], x2["U"], x2["V"], cfg.K, workspace=ws)
+    torch.cuda.synchronize()
+    assert dh.workspace_status(ws) == 0
+    s_full = oracle.lowrank_scores(x2["h"].cpu(), x2["U"].cpu(), x2["V"].cpu())
+    check_candidates(idx[0].cpu().numpy(), score[0].cpu().numpy(), s_full[0], cfg.K, where="after overflow")
+
+
+def test_batch1_forced_gemv(tune):
+    tune("DH_FORCE_PATH", "gemv")
     cfg = inputs.HEAD_CONFIGS["batch1"]
     x = inputs.make_head(cfg, seed=2, device=DEV)
     run_head(x, cfg.K)
 
 
 @pytest.mark.parametrize("path", ["fused", "auto"])
-def test_fused_path_batch8_bf16_full_vocab(path, monkeypatch):
+def test_fused_path_batch8_bf16_full_vocab(path, tune):
     """Eight rows at full size: the small-batch pipeline (forced) and the automatic choice (the
     tensor-core path from five rows on)."""
     if path == "fused":
-        monkeypatch.setenv("DH_FORCE_PATH", "fused")
+        tune("DH_FORCE_PATH", "fused")
     cfg = inputs.HeadConfig("b8", 8, 5120, 151936, 256, 64, "bf16", 0.1, True)
     x = inputs.make_head(cfg, seed=3, device=DEV)
     run_head(x, cfg.K, rows=[0, 7])
     assert dh.workspace_status() == 0
 
 
-def test_moderate_load_forced_gemv(monkeypatch):
-    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+def test_moderate_load_forced_gemv(tune):
+    tune("DH_FORCE_PATH", "gemv")
     cfg = inputs.HEAD_CONFIGS["moderate"]
     x = inputs.make_head(cfg, seed=1, device=DEV)
     run_head(x, cfg.K, rows=[3, 60])
 
 
-def test_mma_and_gemv_paths_agree_on_candidates(monkeypatch):
+def test_mma_and_gemv_paths_agree_on_candidates(tune):
     cfg = inputs.HeadConfig("agree", 24, 512, 16384, 128, 64, "bf16", 0.1, True)
     x = inputs.make_head(cfg, seed=12, device=DEV)
-    monkeypatch.setenv("DH_FORCE_PATH", "mma")
+    tune("DH_FORCE_PATH", "mma")
     i1, s1 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
-    monkeypatch.setenv("DH_FORCE_PATH", "gemv")
+    tune("DH_FORCE_PATH", "gemv")
     i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
     torch.cuda.synchronize()
     # the paths round t from different fp32 summation orders, so near-equal scores may swap places;
@@ -474,9 +531,8 @@ def test_repeated_calls_are_identical():
 
 # ---------------------------------------------------------------- bounded waits
 
-@pytest.mark.parametrize("mode", [0, 1], ids=["mbarrier", "grid_barrier"])
-def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
-    status = dh.selftest_wait_timeout(mode, limit_us=20000)
+def test_bounded_waits_time_out_and_leave_the_context_usable():
+    status = dh.selftest_wait_timeout(limit_us=20000)
     assert status == (1 << 5)
     cfg = inputs.head_config("tiny", B=2)
     x = inputs.make_head(cfg, seed=0, device=DEV)
@@ -484,10 +540,10 @@ def test_bounded_waits_time_out_and_leave_the_context_usable(mode):
 
 
 @pytest.mark.parametrize("path", ["direct", "ring", "ticket"])
-def test_rescore_large_batch_with_repeats(path, monkeypatch):
+def test_rescore_large_batch_with_repeats(path, tune):
     """Stage 2 on a large batch whose rows draw from a small candidate pool (many repeated W rows),
     with two out-of-range ids; a second call reuses the workspace tickets."""
-    monkeypatch.setenv("DH_FORCE_RESCORE", path)
+    tune("DH_FORCE_RESCORE", path)
     cfg = inputs.HeadConfig("rescore_big", 256, 512, 4096, 64, 128, "bf16", 0.1, True)
     x = inputs.make_head(cfg, seed=31, device=DEV)
     g = torch.Generator(device="cpu").manual_seed(5)
