@@ -1,20 +1,28 @@
 #!/usr/bin/env python3
 """Benchmark of the GB300 draft-head path (prints one JSON line on rank 0).
 
-A step is one pass of the draft head over one batch: dh_lowrank_topk (projection, vocabulary-wide
-low-rank scores, exact top-K) followed by dh_exact_rescore (gathered full-rank logits + softmax),
-on the workload's synthetic inputs already resident in HBM.  ``--workload tree`` times
-dh_tree_accept instead.
+A step is one pass of the draft head over one batch: dh_draft_head (projection, vocabulary-wide
+low-rank scores, exact top-K, gathered full-rank logits and their softmax), on the workload's
+synthetic inputs already resident in HBM.  The headline workload is ``batch1`` (B=1, d=5120,
+vocab=151936, r=128, K=64, bf16), timed for exactly ``--steps`` steps.  The same line carries a
+``workloads`` object with the other workloads (moderate, high, the draft level, tree acceptance),
+each timed for at least 100 ms.
 
-* value: rows per second over the whole job (sum over ranks / slowest rank's time); each step is
-  a CUDA-graph replay of the two calls; input sets rotate over enough independent copies that the
-  bytes touched between two uses of one copy exceed twice the L2 size.
-* e2e: the same metric through the public Python API with the step's per-call input (h, or the
-  tree inputs) copied from pinned host memory and the results copied back, synchronising each step.
-* roofline: the dominant kernel's algorithmic bytes (or flops) per launch over its CUDA-event
-  duration, from a second pass with per-kernel events on the launch stream.
+* value: rows per second over the whole job (sum over ranks / slowest rank's time); steps run as
+  CUDA-graph replays; input sets rotate over enough independent copies that the bytes touched
+  between two uses of one copy exceed twice the L2 size.
+* path_roofline: the path's ideal time per the hot-path measurement rule (per stage, the larger of
+  its HBM bytes over the measured copy bandwidth and its FLOPs over the peak of the unit that runs
+  it; stage 2 charged at the distinct W rows the step gathers) over the measured time.
+* roofline: one named kernel per workload, its algorithmic bytes (or FLOPs) per launch over its
+  CUDA-event duration (a separate pass with per-kernel events on the launch stream).
+* e2e: the same metric through the public API with each step's input h copied from pinned host
+  memory and the step's results copied back, all in stream order (one graph replay per step); the
+  per-step synchronised form and the eager Python-level form are reported beside it.
 * cpu_baseline: the CPU oracle timed on host cores on a bounded sample of the same workload.
 * ``--impl reference``: the CPU oracle as the reference arm (rank 0 only).
+* ``--gpus N`` without a launcher: spawns N ranks (one per GPU) on this node; replicas need no
+  collective in the data path, only the barrier and the max over ranks of the timing.
 """
 from __future__ import annotations
 
@@ -23,6 +31,8 @@ import hashlib
 import json
 import math
 import os
+import platform
+import socket
 import subprocess
 import sys
 import threading
@@ -40,18 +50,26 @@ METRIC = "draft-head rows/sec and µs per call (low-rank top-K + rescore); % of 
 TREE_METRIC = "tree-acceptance requests/sec and µs per call (per-node argmax + tree walk); % of HBM roofline"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz
+FP32_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200, "level": 10000}
 DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5, "level": 100}
+EXTRA_WORKLOADS = ["moderate", "high", "level", "tree"]
+MIN_TIMED_S = 0.1  # every added workload's timed region
 EXPAND_W = {"level": 4}  # children per frontier node in the draft-level workload
+# the kernel each workload's `roofline` reports (the one that moves the step's bytes)
+ROOFLINE_KERNEL = {"batch1": "scores_lsu", "moderate": "rescore_ring", "high": "rescore_ring",
+                   "level": "lowrank_mma", "tree": "tree_argmax"}
 
 
-def parse_args():
+def parse_args(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree", "level"])
+    ap.add_argument("--only", action="store_true", help="time the named workload alone (no `workloads`)")
     ap.add_argument("--api", default="head", choices=["head", "split"],
                     help="head: dh_draft_head (both stages in one call); split: dh_lowrank_topk + "
                          "dh_exact_rescore")
@@ -59,10 +77,13 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--dry-run", action="store_true",
+                    help="no GPU: the ranks meet over gloo, time a host loop and report (tests the "
+                         "multi-rank plumbing)")
     ap.add_argument("--profile-run", action="store_true",
                     help="for profilers: one input copy, eager launches of warmup+steps steps, "
                          "no graphs, e2e, CPU baseline or clock sampling; prints a short line")
-    a = ap.parse_args()
+    a = ap.parse_args(argv)
     if a.steps is None:
         a.steps = DEFAULT_STEPS[a.workload]
     if a.warmup is None:
@@ -80,11 +101,12 @@ def dist_env():
     return rank, world, local
 
 
-def dist_init(world, local):
+def dist_init(world, local, backend=None):
     if world > 1:
         import torch.distributed as dist
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if torch.cuda.is_available():
+        if backend is None:
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
             torch.cuda.set_device(local)
         dist.init_process_group(backend=backend)
 
@@ -109,6 +131,42 @@ def max_over_ranks(x: float, world: int) -> float:
 def weak_scaling_value(units_per_step: int, steps: int, world: int, max_ms: float) -> float:
     """Whole-job throughput: every rank processed units_per_step per step; time = slowest rank."""
     return units_per_step * steps * world / (max_ms / 1e3)
+
+
+def free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def spawn_ranks(n: int, argv) -> int:
+    """Runs this script as n ranks on this node (RANK / LOCAL_RANK / WORLD_SIZE / MASTER_* set as a
+    launcher would, rendezvous on 127.0.0.1); returns the worst exit code."""
+    port = free_port()
+    procs = []
+    for r in range(n):
+        env = dict(os.environ, RANK=str(r), LOCAL_RANK=str(r), WORLD_SIZE=str(n), LOCAL_WORLD_SIZE=str(n),
+                   MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+        procs.append(subprocess.Popen([sys.executable, os.path.abspath(__file__), *argv], env=env))
+    rcs = [p.wait() for p in procs]
+    return max(rcs, key=abs)
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.processor() or platform.machine()
 
 
 def load_peaks():
@@ -159,6 +217,7 @@ class ClockSampler:
             where = "whole run (timed region shorter than the sampling interval)"
         if not win:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+
         def num(x):
             try:
                 return float(x)
@@ -219,28 +278,51 @@ KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
 
 
 def head_bytes(cfg):
-    """Algorithmic HBM bytes of one call pair: U, V, h once and the B*K gathered rows of W."""
+    """HBM bytes of one call: U, V, h once and the B*K gathered rows of W."""
     e = 2 if cfg.dtype == "bf16" else 4
     return {"U": cfg.d * cfg.r * e, "V": cfg.r * cfg.vocab * e, "h": cfg.B * cfg.d * e,
             "W_rows": cfg.B * cfg.K * cfg.d * e}
 
 
-def kernel_algo(cfg, name):
-    """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
-    or tensor FLOPs of the dense contraction (rows beyond B padded by the kernel are not counted)."""
+def stage1_on_tensor_cores(cfg) -> bool:
+    """The library runs stage 1 on the tensor cores for bf16 batches above three rows."""
+    return cfg.dtype == "bf16" and cfg.B > 3
+
+
+def path_ideal(cfg, unique_rows, peaks):
+    """Ideal time of one call per the measurement rule: per stage max(bytes / copy bandwidth,
+    FLOPs / peak of the unit that runs it), summed; stage 2 reads each distinct W row once."""
     e = 2 if cfg.dtype == "bf16" else 4
-    if name in ("scores_small", "scores_lsu"):
+    bw = peaks["hbm_gbs"] * 1e9
+    s1_bytes = cfg.d * cfg.r * e + cfg.r * cfg.vocab * e + cfg.B * cfg.d * e
+    s1_flops = 2.0 * cfg.B * (cfg.d * cfg.r + cfg.r * cfg.vocab)
+    s1_peak = (peaks["bf16_tflops"] if stage1_on_tensor_cores(cfg) else FP32_CORE_TFLOPS) * 1e12
+    s2_bytes = unique_rows * cfg.d * e + cfg.B * cfg.d * e
+    s2_flops = 2.0 * cfg.B * cfg.K * cfg.d
+    s2_peak = FP32_CORE_TFLOPS * 1e12
+    t1 = max(s1_bytes / bw, s1_flops / s1_peak)
+    t2 = max(s2_bytes / bw, s2_flops / s2_peak)
+    return {"stage1_us": t1 * 1e6, "stage1_bound": "hbm" if s1_bytes / bw >= s1_flops / s1_peak else
+            ("tensor" if stage1_on_tensor_cores(cfg) else "alu"),
+            "stage1_bytes": s1_bytes, "stage1_flops": s1_flops,
+            "stage2_us": t2 * 1e6, "stage2_bound": "hbm" if s2_bytes / bw >= s2_flops / s2_peak else "alu",
+            "stage2_bytes_unique_rows": s2_bytes, "ideal_us": (t1 + t2) * 1e6}
+
+
+def kernel_algo(cfg, name, peaks):
+    """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
+    or tensor FLOPs of the dense contraction when those take longer at the peaks."""
+    e = 2 if cfg.dtype == "bf16" else 4
+    if name in ("scores_small", "scores_lsu", "scores_summary"):
         return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
-    if name == "proj_small":
+    if name in ("proj_small", "proj_partial"):
         return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
-    if name == "scores_summary":
-        return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
-    if name == "lowrank_mma":
-        return "tensor", 2.0 * cfg.B * cfg.r * cfg.vocab, "TFLOP/s"
-    if name == "proj_mma":
-        return "tensor", 2.0 * cfg.B * cfg.d * cfg.r, "TFLOP/s"
-    if name == "proj_partial":
-        return "hbm", cfg.d * cfg.r * e + cfg.B * cfg.d * e, "GB/s"
+    if name in ("lowrank_mma", "proj_mma"):
+        flops = 2.0 * cfg.B * cfg.r * (cfg.vocab if name == "lowrank_mma" else cfg.d)
+        nbytes = cfg.r * (cfg.vocab if name == "lowrank_mma" else cfg.d) * e + cfg.B * cfg.r * e
+        if flops / (peaks["bf16_tflops"] * 1e12) > nbytes / (peaks["hbm_gbs"] * 1e9):
+            return "tensor", flops, "TFLOP/s"
+        return "hbm", nbytes, "GB/s"
     if name == "expand":  # candidates' probabilities and ids in, children out
         return "hbm", cfg.B * cfg.K * 8 + cfg.B * 4 * 8 + cfg.B * 8, "GB/s"
     if name == "head_cluster":  # records read once, the candidates' W rows, h
@@ -252,10 +334,37 @@ def kernel_algo(cfg, name):
     return "hbm", 0, "GB/s"
 
 
-def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
+def kernel_roofline(cfg, name, stages, peaks, peak_src, workload):
+    bound, algo, unit = kernel_algo(cfg, name, peaks)
+    dur_s = stages[name]["us_avg"] * 1e-6
+    if bound == "tensor":
+        achieved, peak = algo / dur_s / 1e12, peaks["bf16_tflops"]
+        src = f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"
+    else:
+        achieved, peak = algo / dur_s / 1e9, peaks["hbm_gbs"]
+        src = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+    traffic = traffic_from_profiles(name, workload, KERNEL_FILES.get(name, []))
+    out = {"kernel": name, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+           "frac": round(achieved / peak, 4), "traffic": traffic,
+           ("algorithmic_flops_per_launch" if bound == "tensor" else "algorithmic_bytes_per_launch"): algo,
+           "us_per_launch": round(stages[name]["us_avg"], 3), "peak_source": src}
+    if traffic and bound == "hbm" and algo:
+        out["traffic_over_algorithmic"] = round(traffic / algo, 3)
+    return out
+
+
+def auto_steps(per_step_us: float, chunk: int, floor: int) -> int:
+    """Steps for a timed region of at least MIN_TIMED_S, a multiple of chunk."""
+    n = max(floor, math.ceil(MIN_TIMED_S / (per_step_us * 1e-6)))
+    return int(math.ceil(n / chunk) * chunk)
+
+
+def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warmup=None, cpu_seconds=None):
+    """Times one head workload.  steps None: enough steps for MIN_TIMED_S."""
     from speculative_decoding_draft_dh_gb300 import binding as dh
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    warmup = a.warmup if warmup is None else warmup
     hb = head_bytes(cfg)
     per_step = sum(hb.values())
     copies = max(2, min(8, math.ceil(2 * L2_BYTES / per_step)))
@@ -293,14 +402,13 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
                                child_token=x["ctok"], child_prob=x["cprob"], n_keep=x["keep"])
 
     with torch.cuda.stream(stream):
-        for i in range(a.warmup):
+        for i in range(warmup):
             step(sets[i % copies])
     torch.cuda.synchronize()
     # One graph holds S consecutive steps over the rotating copies (S a multiple of the copy count),
-    # so that host-side replay overhead (tens of µs per replay from Python) is spread over many
-    # steps and the GPU never waits for the host; a second graph holds the remainder of the steps.
+    # so that host-side replay overhead is spread over many steps and the GPU never waits for the
+    # host; a second graph holds the remainder of the steps.
     per_graph = max(copies, (64 // copies) * copies)
-    S = min(a.steps, per_graph)
 
     def capture(n):
         g = torch.cuda.CUDAGraph()
@@ -309,8 +417,25 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
                 step(sets[j % copies])
         return g
 
-    g_full = capture(S)
-    rem = a.steps % S
+    g_full = capture(per_graph)
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, math.ceil(max(3, warmup) / per_graph))):
+            g_full.replay()
+    torch.cuda.synchronize()
+    if steps is None:  # calibrate on a few replays
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record(stream)
+            for _ in range(3):
+                g_full.replay()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        steps = auto_steps(c0.elapsed_time(c1) * 1e3 / (3 * per_graph), per_graph, per_graph)
+        steps = int(max_over_ranks(steps, world))
+    S = min(steps, per_graph)
+    if S != per_graph:
+        g_full = capture(S)
+    rem = steps % S
     g_rem = capture(rem) if rem else None
 
     def run_steps(n):
@@ -320,15 +445,10 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
             assert n % S == rem
             g_rem.replay()
 
-    with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(max(3, a.warmup) / S))):
-            g_full.replay()
-    torch.cuda.synchronize()
-
     sampler = ClockSampler(local)
     time.sleep(0.15)
     with torch.cuda.stream(stream):
-        for _ in range(max(1, math.ceil(min(a.warmup, 50) / S))):
+        for _ in range(max(1, math.ceil(min(warmup, 50) / S))):
             g_full.replay()
     barrier(world)
     torch.cuda.synchronize()
@@ -336,7 +456,7 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        run_steps(a.steps)
+        run_steps(steps)
         ev1.record(stream)
     torch.cuda.synchronize()
     t1 = time.perf_counter()
@@ -345,11 +465,11 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     sampler.stop()
     ms = ev0.elapsed_time(ev1)
     ms = max_over_ranks(ms, world)
-    us_per_call = ms * 1e3 / a.steps
-    value = weak_scaling_value(cfg.B, a.steps, world, ms)
+    us_per_call = ms * 1e3 / steps
+    value = weak_scaling_value(cfg.B, steps, world, ms)
 
     # spread: each replay of the S-step graph timed on its own (after the headline measurement)
-    n_rep = max(5, min(50, a.steps // S))
+    n_rep = max(5, min(50, steps // S))
     rep_us = []
     with torch.cuda.stream(stream):
         for _ in range(n_rep):
@@ -365,7 +485,7 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
               "us_per_call_p90": round(rep_us[(9 * len(rep_us)) // 10], 3), "replays": n_rep,
               "steps_per_replay": S}
     # stream-queued: the same calls launched eagerly back to back (no graph)
-    n_eager = min(a.steps, 1000 if cfg.B <= 64 else 50)
+    n_eager = min(steps, 1000 if cfg.B <= 64 else 50)
     with torch.cuda.stream(stream):
         for i in range(3):
             step(sets[i % copies])
@@ -376,13 +496,12 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
         e1.record(stream)
     torch.cuda.synchronize()
     spread["us_per_call_stream_queued"] = round(e0.elapsed_time(e1) * 1e3 / n_eager, 3)
-    # distinct W rows among the candidates of one step (stage 2 reads each once from HBM; repeats
-    # may hit L2)
+    # distinct W rows among the candidates of one step (the rescoring's algorithmic bytes)
     e_sz = 2 if cfg.dtype == "bf16" else 4
     uniq = int(torch.unique(sets[0]["idx"]).numel())
 
     # per-kernel events on the launch stream (separate pass, eager launches)
-    n_prof = min(a.steps, 2000 if cfg.B <= 64 else 200)
+    n_prof = min(steps, 2000 if cfg.B <= 64 else 200)
     dh.prof_enable(True)
     with torch.cuda.stream(stream):
         for i in range(n_prof):
@@ -392,85 +511,40 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
     prof = dh.prof_read()
     stages = {k: {"us_avg": v[0] * 1e3 / v[1], "launches": v[1]} for k, v in prof.items()}
     launches_per_step = sum(v[1] for v in prof.values()) / n_prof
+    name = ROOFLINE_KERNEL.get(cfg.name)
+    if name not in stages:
+        name = max(stages, key=lambda k: stages[k]["us_avg"])
+    roofline = kernel_roofline(cfg, name, stages, peaks, peak_src, cfg.name)
     dom = max(stages, key=lambda k: stages[k]["us_avg"])
-    bound, algo, unit = kernel_algo(cfg, dom)
-    dur_s = stages[dom]["us_avg"] * 1e-6
-    if bound == "tensor":
-        achieved = algo / dur_s / 1e12
-        peak = peaks["bf16_tflops"]
-        peak_src_s = f"{peak_src} (MEASURED_PEAKS.json bf16_tflops, burst)"
-    else:
-        achieved = algo / dur_s / 1e9
-        peak = peaks["hbm_gbs"]
-        peak_src_s = f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-    traffic = traffic_from_profiles(dom, cfg.name, KERNEL_FILES.get(dom, []))
-    roofline = {"kernel": dom, "bound": bound, "achieved": round(achieved, 1), "peak": peak,
-                "unit": unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                ("algorithmic_flops_per_launch" if bound == "tensor" else "algorithmic_bytes_per_launch"): algo,
-                "us_per_launch": round(stages[dom]["us_avg"], 3), "peak_source": peak_src_s}
-    # the kernel that moves the most bytes, against the copy bandwidth (when it is not the one above)
-    roofline_stream = None
-    hbm_k = [k for k in stages if kernel_algo(cfg, k)[0] == "hbm" and kernel_algo(cfg, k)[1] > 0]
-    if hbm_k:
-        sk = max(hbm_k, key=lambda k: kernel_algo(cfg, k)[1])
-        if sk != dom:
-            s_algo = kernel_algo(cfg, sk)[1]
-            s_ach = s_algo / (stages[sk]["us_avg"] * 1e-6) / 1e9
-            roofline_stream = {"kernel": sk, "bound": "hbm", "achieved": round(s_ach, 1), "peak": peaks["hbm_gbs"],
-                               "unit": "GB/s", "frac": round(s_ach / peaks["hbm_gbs"], 4),
-                               "traffic": traffic_from_profiles(sk, cfg.name, KERNEL_FILES.get(sk, [])),
-                               "algorithmic_bytes_per_launch": s_algo,
-                               "us_per_launch": round(stages[sk]["us_avg"], 3)}
-    path_ach = per_step / (us_per_call * 1e-6) / 1e9
-    hbm = peaks["hbm_gbs"]
-    path_roofline = {"bound": "hbm", "bytes_per_call": per_step, "achieved": round(path_ach, 1),
-                     "peak": hbm, "unit": "GB/s", "frac": round(path_ach / hbm, 4),
-                     "ideal_us": round(per_step / (hbm * 1e9) * 1e6, 3)}
-    uniq_bytes = per_step - hb["W_rows"] + uniq * cfg.d * e_sz
-    path_roofline["unique_w_rows"] = uniq
-    path_roofline["bytes_per_call_unique_rows"] = uniq_bytes
-    path_roofline["frac_unique_rows"] = round(uniq_bytes / (us_per_call * 1e-6) / 1e9 / hbm, 4)
+    roofline_time_dominant = None
+    if dom != name:
+        roofline_time_dominant = kernel_roofline(cfg, dom, stages, peaks, peak_src, cfg.name)
 
-    # end to end through the public API with host buffers
+    ideal = path_ideal(cfg, uniq, peaks)
+    hbm = peaks["hbm_gbs"]
+    path_roofline = {"rule": "sum over stages of max(bytes / copy bandwidth, FLOPs / unit peak); stage 2 at "
+                             "distinct W rows",
+                     "ideal_us": round(ideal["ideal_us"], 3), "measured_us": round(us_per_call, 3),
+                     "frac": round(ideal["ideal_us"] / us_per_call, 4),
+                     "stage1_us": round(ideal["stage1_us"], 3), "stage1_bound": ideal["stage1_bound"],
+                     "stage2_us": round(ideal["stage2_us"], 3), "stage2_bound": ideal["stage2_bound"],
+                     "unique_w_rows": uniq, "gathered_w_rows": cfg.B * cfg.K,
+                     "peaks": {"hbm_gbs": hbm, "bf16_tflops": peaks["bf16_tflops"],
+                               "fp32_core_tflops": round(FP32_CORE_TFLOPS, 1)}}
+    # secondary: every byte over the copy bandwidth, with the B*K gathered rows
+    path_roofline["frac_hbm_bytes_bk_rows"] = round(per_step / (us_per_call * 1e-6) / 1e9 / hbm, 4)
+
     e2e = None
     if not a.no_e2e:
-        n_e2e = min(a.steps, 2000 if cfg.B <= 64 else 100)
-        hosts = [x["h"].cpu().pin_memory() for x in sets]
-        # the three outputs live in one device buffer (idx, logits, probs as int32 / fp32 views),
-        # so one device-to-host copy returns a step's results
-        BK = cfg.B * cfg.K
-        packed = [torch.empty(3 * BK, dtype=torch.int32, device=dev) for _ in sets]
-        outs = [torch.empty(3 * BK, dtype=torch.int32).pin_memory() for _ in sets]
-        views = [(p[:BK].view(cfg.B, cfg.K), p[BK:2 * BK].view(torch.float32).view(cfg.B, cfg.K),
-                  p[2 * BK:].view(torch.float32).view(cfg.B, cfg.K)) for p in packed]
-        def e2e_step(i):
-            j = i % copies
-            x = sets[j]
-            idx, logits, probs = views[j]
-            with torch.cuda.stream(stream):
-                x["h"].copy_(hosts[j], non_blocking=True)
-                step(x, idx, logits, probs)
-                outs[j].copy_(packed[j], non_blocking=True)
-            stream.synchronize()
-        for i in range(3):
-            e2e_step(i)
-        barrier(world)
-        te0 = time.perf_counter()
-        for i in range(n_e2e):
-            e2e_step(i)
-        te = max_over_ranks(time.perf_counter() - te0, world)
-        e2e = {"value": round(cfg.B * n_e2e * world / te, 2), "unit": "rows/s",
-               "us_per_call": round(te * 1e6 / n_e2e, 2), "steps": n_e2e,
-               "h2d_bytes_per_step": int(cfg.B * cfg.d * (2 if cfg.dtype == "bf16" else 4)),
-               "d2h_bytes_per_step": int(cfg.B * cfg.K * 12)}
+        e2e = head_e2e(a, cfg, sets, copies, step, stream, world, e_sz, S)
 
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu = cpu_head_baseline(cfg, sets[0], a.cpu_seconds)
+        cpu = cpu_head_baseline(cfg, sets[0], a.cpu_seconds if cpu_seconds is None else cpu_seconds)
     clocks = sampler.summary(t0, t1)
     return {
         "metric": METRIC, "value": round(value, 2), "unit": "rows/s", "n_gpus": world,
-        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 6),
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms / steps, 6), "timed_ms": round(ms, 3),
         "us_per_call": round(us_per_call, 3), "timing_spread": spread, "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic (seeded generators, random weights)",
@@ -479,11 +553,89 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src):
                    "dh_lowrank_topk + dh_exact_rescore", "graph": f"CUDA graphs of {S} steps",
                    "l2": f"inputs rotate over {copies} independent copies "
                          f"({copies * per_step / 2**20:.0f} MiB per cycle > 2x L2)",
-                   "parallelism": f"replicas x{world} (rows independent)"},
-        "roofline": roofline, "roofline_stream": roofline_stream, "path_roofline": path_roofline, "stages": stages,
-        "gpu_launches": int(round(launches_per_step * a.steps)), "e2e": e2e,
+                   "parallelism": f"replicas x{world} (rows independent; no collective in the data path)"},
+        "roofline": roofline, "roofline_time_dominant": roofline_time_dominant,
+        "path_roofline": path_roofline, "stages": stages,
+        "gpu_launches": int(round(launches_per_step * steps)), "e2e": e2e,
         "cpu_baseline": cpu, "clocks": clocks,
     }
+
+
+def head_e2e(a, cfg, sets, copies, step, stream, world, e_sz, S):
+    """End to end through the public API: each step copies its h from pinned host memory, runs
+    the head and copies its results (idx, logits, probs) back, in stream order."""
+    dev = sets[0]["h"].device
+    hosts = [x["h"].cpu().pin_memory() for x in sets]
+    BK = cfg.B * cfg.K
+    # the three outputs live in one device buffer (idx, logits, probs as int32 / fp32 views), so
+    # one device-to-host copy returns a step's results
+    packed = [torch.empty(3 * BK, dtype=torch.int32, device=dev) for _ in sets]
+    outs = [torch.empty(3 * BK, dtype=torch.int32).pin_memory() for _ in sets]
+    views = [(p[:BK].view(cfg.B, cfg.K), p[BK:2 * BK].view(torch.float32).view(cfg.B, cfg.K),
+              p[2 * BK:].view(torch.float32).view(cfg.B, cfg.K)) for p in packed]
+
+    def one(j):
+        x = sets[j]
+        idx, logits, probs = views[j]
+        x["h"].copy_(hosts[j], non_blocking=True)
+        step(x, idx, logits, probs)
+        outs[j].copy_(packed[j], non_blocking=True)
+
+    # (1) graphs of S steps, each step with its own copies, queued in stream order (the host never
+    # waits): a caller that keeps the GPU fed
+    g_steps = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_steps, stream=stream):
+        for j in range(S):
+            one(j % copies)
+    n = S * max(1, min(2000 if cfg.B <= 64 else 200, 20 * S) // S)
+    with torch.cuda.stream(stream):
+        g_steps.replay()
+    stream.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(n // S):
+            g_steps.replay()
+    stream.synchronize()
+    te = max_over_ranks(time.perf_counter() - t0, world)
+    # (2) one graph replay per step, synchronising after every step (a caller that waits for each
+    # result before the next step)
+    graphs = []
+    for j in range(copies):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            one(j)
+        graphs.append(g)
+    n_sync = max(copies, n // 4)
+    with torch.cuda.stream(stream):
+        for j in range(copies):
+            graphs[j].replay()
+    stream.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_sync):
+            graphs[i % copies].replay()
+            stream.synchronize()
+    ts = max_over_ranks(time.perf_counter() - t0, world)
+    # (3) eager launches through the Python binding, synchronising every step
+    n_py = max(copies, n // 4)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i % copies)
+    stream.synchronize()
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for i in range(n_py):
+            one(i % copies)
+            stream.synchronize()
+    tp = max_over_ranks(time.perf_counter() - t0, world)
+    return {"value": round(cfg.B * n * world / te, 2), "unit": "rows/s",
+            "us_per_call": round(te * 1e6 / n, 3), "steps": n,
+            "how": f"wall clock; every step copies its h from pinned host memory, runs dh_draft_head and "
+                   f"copies its results to pinned host memory, in stream order; CUDA graphs of {S} such steps",
+            "h2d_bytes_per_step": int(cfg.B * cfg.d * e_sz), "d2h_bytes_per_step": int(BK * 12),
+            "synchronized_each_step": {"us_per_call": round(ts * 1e6 / n_sync, 3), "steps": n_sync},
+            "python_eager_each_step": {"us_per_call": round(tp * 1e6 / n_py, 3), "steps": n_py}}
 
 
 def cpu_head_baseline(cfg, x, seconds):
@@ -507,16 +659,18 @@ def cpu_head_baseline(cfg, x, seconds):
     dt = time.perf_counter() - t0
     used = min(cfg.B, cores)
     what = "stage 1 + stage 2" + (" + expansion" if EXPAND_W.get(cfg.name, 0) else "")
-    return {"value": round(rows_done / dt, 4), "unit": "rows/s", "cores": used, "kind": "oracle",
+    return {"value": round(rows_done / dt, 4), "unit": "rows/s", "cores": used, "cpu_model": cpu_model(),
+            "kind": "oracle",
             "sample": f"{rows_done} rows of the {cfg.name} workload ({what}), {dt:.1f} s, OpenMP over rows"}
 
 
 # ------------------------------------------------------------------------------------- tree
 
-def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
+def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src, steps=None, warmup=None, cpu_seconds=None):
     from speculative_decoding_draft_dh_gb300 import binding as dh
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    warmup = a.warmup if warmup is None else warmup
     t = inputs.make_tree(tcfg, seed=a.seed + 1000 * rank, device=dev)
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
@@ -528,12 +682,21 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
         return dh.tree_accept(t["logits"], t["parent"], t["token"], workspace=ws)
 
     with torch.cuda.stream(stream):
-        for _ in range(a.warmup):
+        for _ in range(warmup):
             step()
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g, stream=stream):
         step()
+    if steps is None:
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            c0.record(stream)
+            for _ in range(5):
+                g.replay()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        steps = int(max_over_ranks(auto_steps(c0.elapsed_time(c1) * 1e3 / 5, 1, 10), world))
     sampler = ClockSampler(local)
     time.sleep(0.15)
     with torch.cuda.stream(stream):
@@ -545,7 +708,7 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
     t0 = time.perf_counter()
     with torch.cuda.stream(stream):
         ev0.record(stream)
-        for _ in range(a.steps):
+        for _ in range(steps):
             g.replay()
         ev1.record(stream)
     torch.cuda.synchronize()
@@ -554,9 +717,9 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
     time.sleep(0.12)
     sampler.stop()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
-    us = ms * 1e3 / a.steps
-    value = weak_scaling_value(B, a.steps, world, ms)
-    n_prof = min(a.steps, 50)
+    us = ms * 1e3 / steps
+    value = weak_scaling_value(B, steps, world, ms)
+    n_prof = min(steps, 50)
     dh.prof_enable(True)
     with torch.cuda.stream(stream):
         for _ in range(n_prof):
@@ -568,49 +731,65 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src):
     dom = "tree_argmax"
     achieved = logit_bytes / (stages[dom]["us_avg"] * 1e-6) / 1e9
     peak = peaks["hbm_gbs"]
+    traffic = traffic_from_profiles(dom, tcfg.name, KERNEL_FILES[dom])
     roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
-                "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic_from_profiles(dom, tcfg.name, KERNEL_FILES[dom]),
+                "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                 "algorithmic_bytes_per_launch": logit_bytes,
                 "us_per_launch": round(stages[dom]["us_avg"], 3),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+    if traffic:
+        roofline["traffic_over_algorithmic"] = round(traffic / logit_bytes, 3)
+    path_bytes = logit_bytes + 2 * B * N * 4
+    ideal_us = path_bytes / (peak * 1e9) * 1e6
+    path_roofline = {"rule": "logits, parents and tokens read once over the copy bandwidth",
+                     "ideal_us": round(ideal_us, 3), "measured_us": round(us, 3), "frac": round(ideal_us / us, 4)}
     e2e = None
     if not a.no_e2e:
-        n_e2e = min(a.steps, 10)
+        n_e2e = min(steps, 10)
         host = {k: t[k].cpu().pin_memory() for k in ("logits", "parent", "token")}
-        outs = {k: None for k in ("path", "len", "bonus")}
-        def e2e_step():
-            with torch.cuda.stream(stream):
-                for k in host:
-                    t[k].copy_(host[k], non_blocking=True)
-                o = step()
-                res = [o[k].to("cpu", non_blocking=True) for k in ("path", "len", "bonus")]
-            stream.synchronize()
-            return res
-        e2e_step()
+        out_host = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in step().items()
+                    if k in ("path", "len", "bonus")}
+
+        def one():
+            for k in host:
+                t[k].copy_(host[k], non_blocking=True)
+            o = step()
+            for k in out_host:
+                out_host[k].copy_(o[k], non_blocking=True)
+        torch.cuda.synchronize()
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=stream):
+            one()
+        with torch.cuda.stream(stream):
+            ge.replay()
+        stream.synchronize()
         te0 = time.perf_counter()
-        for _ in range(n_e2e):
-            e2e_step()
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                ge.replay()
+        stream.synchronize()
         te = max_over_ranks(time.perf_counter() - te0, world)
         e2e = {"value": round(B * n_e2e * world / te, 2), "unit": "requests/s",
                "us_per_call": round(te * 1e6 / n_e2e, 1), "steps": n_e2e,
+               "how": "wall clock; per step one CUDA-graph replay of: logits, parents and tokens copied from "
+                      "pinned host memory, dh_tree_accept, path / len / bonus copied back",
                "h2d_bytes_per_step": int(logit_bytes + 2 * B * N * 4),
                "d2h_bytes_per_step": int(B * N * 4 + 2 * B * 4)}
     cpu = None
     if rank == 0 and world == 1 and not a.no_cpu_baseline:
-        cpu = cpu_tree_baseline(tcfg, t, a.cpu_seconds)
+        cpu = cpu_tree_baseline(tcfg, t, a.cpu_seconds if cpu_seconds is None else cpu_seconds)
     return {
         "metric": TREE_METRIC, "value": round(value, 2), "unit": "requests/s", "n_gpus": world,
-        "steps": a.steps, "warmup": a.warmup, "ms_per_step": round(ms / a.steps, 6),
+        "steps": steps, "warmup": warmup, "ms_per_step": round(ms / steps, 6), "timed_ms": round(ms, 3),
         "us_per_call": round(us, 3), "node_rows_per_s": round(value * N, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": tcfg.dtype,
         "data": "synthetic (seeded generators)",
         "config": {"workload": tcfg.name, "B": B, "N": N, "vocab": vocab, "seed": a.seed,
                    "graph": "one CUDA graph per step",
                    "l2": f"logits {logit_bytes / 2**30:.2f} GiB per step > L2",
-                   "parallelism": f"replicas x{world}"},
-        "roofline": roofline, "stages": stages,
-        "gpu_launches": int(round(sum(v[1] for v in prof.values()) / n_prof * a.steps)),
+                   "parallelism": f"replicas x{world} (requests independent; no collective in the data path)"},
+        "roofline": roofline, "path_roofline": path_roofline, "stages": stages,
+        "gpu_launches": int(round(sum(v[1] for v in prof.values()) / n_prof * steps)),
         "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(t0, t1),
     }
 
@@ -628,8 +807,16 @@ def cpu_tree_baseline(tcfg, t, seconds):
         oracle.tree_accept(sl, pa, to)
         done += n
     dt = time.perf_counter() - t0
-    return {"value": round(done / dt, 3), "unit": "requests/s", "cores": n, "kind": "oracle",
-            "sample": f"{done} requests (first {n} of the tree workload, repeated), {dt:.1f} s"}
+    return {"value": round(done / dt, 3), "unit": "requests/s", "cores": n, "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": f"{done} requests (first {n} of the tree workload, repeated), {dt:.1f} s"}
+
+
+def summarize(line):
+    """The fields of a workload's line kept in the headline's `workloads` object."""
+    keep = ("metric", "value", "unit", "us_per_call", "steps", "timed_ms", "node_rows_per_s", "config",
+            "path_roofline", "roofline", "roofline_time_dominant", "stages", "gpu_launches", "e2e",
+            "cpu_baseline", "clocks", "timing_spread")
+    return {k: line[k] for k in keep if k in line and line[k] is not None}
 
 
 # -------------------------------------------------------------------------------- reference
@@ -702,7 +889,7 @@ def run_reference(a, rank, world):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded generators)", "config": cfgd,
             "cpu_baseline": {"value": round(value, 4), "unit": unit, "kind": "oracle", "cores": threads,
-                             "sample": sample},
+                             "cpu_model": cpu_model(), "sample": sample},
             "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
 
@@ -718,24 +905,61 @@ def profile_run(a):
     else:
         cfg = inputs.HEAD_CONFIGS[a.workload]
         x = inputs.make_head(cfg, seed=a.seed, device=dev)
+        ew = EXPAND_W.get(cfg.name, 0)
         for _ in range(a.warmup + a.steps):
             if a.api == "head":
-                dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K)
+                idx, _, _, probs = dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K)
             else:
                 idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
-                dh.exact_rescore(x["h"], x["W"], idx)
+                _, probs = dh.exact_rescore(x["h"], x["W"], idx)
+            if ew:
+                dh.expand_children(probs, idx, ew, min_benefit=1e-3)
     torch.cuda.synchronize()
     print(json.dumps({"profile_run": a.workload, "steps": a.warmup + a.steps}), flush=True)
 
 
+def dry_run(a, rank, world):
+    """Multi-rank plumbing without a GPU: gloo rendezvous, a timed host loop per rank, the barrier,
+    the max over ranks and the weak-scaling aggregate, as the GPU run does them."""
+    import torch.distributed as dist
+    dist_init(world, rank, backend="gloo")
+    try:
+        barrier(world)
+        t0 = time.perf_counter()
+        acc = 0.0
+        for i in range(20000 * (1 + rank)):
+            acc += math.sqrt(i)
+        ms = (time.perf_counter() - t0) * 1e3
+        slowest = max_over_ranks(ms, world)
+        ranks = [None] * world
+        if world > 1:
+            dist.all_gather_object(ranks, {"rank": rank, "ms": ms})
+        else:
+            ranks = [{"rank": 0, "ms": ms}]
+        barrier(world)
+        if rank == 0:
+            print(json.dumps({"dry_run": True, "n_gpus": world, "gpus_requested": a.gpus, "scaling": "weak",
+                              "value": weak_scaling_value(1, 1, world, slowest), "ms_slowest": slowest,
+                              "ranks": ranks}), flush=True)
+    finally:
+        if world > 1:
+            dist.destroy_process_group()
+
+
 def main():
-    a = parse_args()
+    argv = sys.argv[1:]
+    a = parse_args(argv)
+    if a.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(spawn_ranks(a.gpus, argv))
+    rank, world, local = dist_env()
+    if a.dry_run:
+        dry_run(a, rank, world)
+        return
     if a.profile_run:
         from speculative_decoding_draft_dh_gb300 import build
         build.build()
         profile_run(a)
         return
-    rank, world, local = dist_env()
     if a.impl == "reference":
         line = run_reference(a, rank, world)
         if line is not None:
@@ -743,6 +967,8 @@ def main():
         return
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device")
+    if world != a.gpus:
+        raise SystemExit(f"bench.py --gpus {a.gpus} but the launcher started {world} ranks")
     dist_init(world, local)
     from speculative_decoding_draft_dh_gb300 import build
     if rank == 0:
@@ -751,9 +977,22 @@ def main():
     build.build()
     peaks, src = load_peaks()
     if a.workload == "tree":
-        line = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src)
+        line = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src, steps=a.steps)
     else:
-        line = run_head_bench(a, inputs.HEAD_CONFIGS[a.workload], rank, world, local, peaks, src)
+        line = run_head_bench(a, inputs.HEAD_CONFIGS[a.workload], rank, world, local, peaks, src, steps=a.steps)
+    if not a.only and a.workload == "batch1":
+        work = {}
+        for w in EXTRA_WORKLOADS:
+            cpu_s = min(a.cpu_seconds, 5.0)
+            if w == "tree":
+                sub = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src,
+                                     warmup=DEFAULT_WARMUP[w], cpu_seconds=cpu_s)
+            else:
+                sub = run_head_bench(a, inputs.HEAD_CONFIGS[w], rank, world, local, peaks, src,
+                                     warmup=DEFAULT_WARMUP[w], cpu_seconds=cpu_s)
+            work[w] = summarize(sub)
+            torch.cuda.empty_cache()
+        line["workloads"] = work
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

@@ -47,6 +47,9 @@ def bind(path: str):
     lib.oracle_exact_rescore.argtypes = [P, P, P, I, I, I, I, I, P, I, P, P]
     lib.oracle_tree_accept.argtypes = [P, P, P, I, I, I, I, P, I, P, P, P, P]
     lib.oracle_expand_children.argtypes = [P, P, P, I, I, I, ctypes.c_float, P, P, P]
+    D = ctypes.c_double
+    lib.oracle_verify_chain.argtypes = [P, I, I, I, I, I, P, P, P, P, P, D, D, P, P, P, P, P]
+    lib.oracle_verify_chain.restype = I
     for f in ("oracle_round_bf16", "oracle_lowrank_project", "oracle_lowrank_scores",
               "oracle_lowrank_topk", "oracle_exact_rescore", "oracle_tree_accept"):
         getattr(lib, f).restype = I
@@ -195,3 +198,28 @@ def expand_children(probs, idx, w, parent_prob=None, min_benefit=0.0):
     _check(load().oracle_expand_children(_ptr(pp), _ptr(ii), None if par is None else _ptr(par), B, K, w,
                                          float(min_benefit), _ptr(tok), _ptr(cp), _ptr(keep)), "expand_children")
     return tok, cp, keep
+
+
+def verify_chain(logits, cand_idx, cand_prob, draft_token, u_accept, u_sample, temperature=1.0, tol=1e-4):
+    """Step 8: speculative sampling over a chain of L drafted tokens per request.
+
+    logits [B, L+1, vocab] (fp32 or bf16), cand_idx int32 [B, L, K], cand_prob fp32 [B, L, K],
+    draft_token int32 [B, L], u_accept fp32 [B, L], u_sample fp32 [B].  Returns a dict with
+    n_accept, token (the emitted correction or bonus token), and for comparisons in other
+    precisions first_close (first decision within tol of its threshold, L+1 if none) and
+    token_lo / token_hi (the tokens within tol x total of the sampling point)."""
+    ll, dt = _raw(logits)
+    B, L1, vocab = ll.shape
+    L = L1 - 1
+    ci = np.ascontiguousarray(np.asarray(cand_idx, dtype=np.int32)).reshape(B, L, -1)
+    K = ci.shape[2]
+    cp = np.ascontiguousarray(np.asarray(cand_prob, dtype=np.float32)).reshape(B, L, K)
+    xt = np.ascontiguousarray(np.asarray(draft_token, dtype=np.int32)).reshape(B, L)
+    ua = np.ascontiguousarray(np.asarray(u_accept, dtype=np.float32)).reshape(B, L)
+    us = np.ascontiguousarray(np.asarray(u_sample, dtype=np.float32)).reshape(B)
+    out = {k: np.empty((B,), dtype=np.int32) for k in ("n_accept", "token", "first_close", "token_lo", "token_hi")}
+    _check(load().oracle_verify_chain(_ptr(ll), dt, B, L, vocab, K, _ptr(ci), _ptr(cp), _ptr(xt), _ptr(ua),
+                                      _ptr(us), float(temperature), float(tol), _ptr(out["n_accept"]),
+                                      _ptr(out["token"]), _ptr(out["first_close"]), _ptr(out["token_lo"]),
+                                      _ptr(out["token_hi"])), "verify_chain")
+    return out

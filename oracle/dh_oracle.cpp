@@ -40,6 +40,22 @@
 //        child path probability = parent path probability x p (rounded to fp32), and the node
 //        keeps its first n_keep children, those whose path probability exceeds min_benefit.
 //
+//   EAGLE-4 summary page, section "Distribution preservation has algorithmic and implementation
+//   conditions": at positive temperature the target verifies the drafted tokens and a rejection
+//   correction keeps the target's distribution; each round's depth is fixed before the round.  For
+//   a chain of drafted tokens that correction is standard speculative sampling (Leviathan, Kalman
+//   and Matias 2023, "Fast Inference from Transformers via Speculative Decoding"; Chen et al. 2023,
+//   "Accelerating Large Language Model Decoding with Speculative Sampling"), restated here:
+//     8. request b drafted L tokens x_0..x_{L-1}; target logit rows l_0..l_L (row i: the target's
+//        next-token logits after the prefix and x_0..x_{i-1}); temperature T > 0:
+//          p_i(v) = exp(l_i(v)/T - m_i) / S_i,  m_i = max_v l_i(v)/T,  S_i = sum_v exp(l_i(v)/T - m_i)
+//          q_i(v) = the draft's probability of v at position i (listed for K candidate ids, 0 elsewhere)
+//        token i is accepted when u_i < p_i(x_i) / q_i(x_i) (always when q_i(x_i) = 0);
+//        n = the number of leading accepted tokens;
+//        the emitted token y: n < L: y ~ max(0, p_n - q_n) (normalised); n = L: y ~ p_L (bonus);
+//        drawn by inverse CDF in vocabulary order with the uniform w_b: y = the smallest v whose
+//        running sum of the weights exceeds w_b times their total (a zero total: the weights p_n).
+//
 // Build: g++ -O2 -std=c++17 -fopenmp -ffp-contract=off -shared -fPIC dh_oracle.cpp
 #include <algorithm>
 #include <cmath>
@@ -263,6 +279,92 @@ int oracle_expand_children(const float* probs, const int32_t* idx, const float* 
       if (a > min_benefit) ++keep;
     }
     if (n_keep) n_keep[b] = keep;
+  }
+  return 0;
+}
+
+// Step 8 for every request.  logits: B x (L+1) x vocab; cand_idx, cand_prob: B x L x K;
+// draft_token, u_accept: B x L; u_sample: B.  Outputs per request: n_accept, token (the emitted
+// token).  For comparisons made in other precisions it also reports, with a relative tolerance tol:
+// first_close = the first decision i <= n whose |u_i - ratio_i| <= tol * ratio_i (L + 1 if none),
+// and [token_lo, token_hi] = the tokens whose cumulative interval meets the target sum +- tol x total.
+int oracle_verify_chain(const void* logits, int dtype, int B, int L, int vocab, int K, const int32_t* cand_idx,
+                        const float* cand_prob, const int32_t* draft_token, const float* u_accept,
+                        const float* u_sample, double temperature, double tol, int32_t* n_accept,
+                        int32_t* token, int32_t* first_close, int32_t* token_lo, int32_t* token_hi) {
+  if (!valid_dtype(dtype) || B < 0 || L < 0 || vocab <= 0 || K < 0 || !(temperature > 0.0)) return -1;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b) {
+    const size_t row0 = (size_t)b * (L + 1);
+    // p_i(v) for row i of request b, over the whole vocabulary
+    auto probs_of_row = [&](int i, std::vector<double>& p) {
+      p.assign(vocab, 0.0);
+      double m = -INFINITY;
+      for (int v = 0; v < vocab; ++v) {
+        p[v] = stored_value(logits, dtype, (row0 + i) * (size_t)vocab + v) / temperature;
+        m = std::max(m, p[v]);
+      }
+      double S = 0.0;
+      for (int v = 0; v < vocab; ++v) { p[v] = std::exp(p[v] - m); S += p[v]; }
+      for (int v = 0; v < vocab; ++v) p[v] /= S;
+    };
+    // q_i(v): the draft's probability mass at v (summed over the candidate list)
+    auto q_of = [&](int i, int v) {
+      double q = 0.0;
+      for (int k = 0; k < K; ++k)
+        if (cand_idx[((size_t)b * L + i) * K + k] == v) q += cand_prob[((size_t)b * L + i) * K + k];
+      return q;
+    };
+    std::vector<double> p;
+    int n = 0, close = L + 1;
+    for (; n < L; ++n) {
+      probs_of_row(n, p);
+      const int x = draft_token[(size_t)b * L + n];
+      const double px = (x >= 0 && x < vocab) ? p[x] : 0.0;
+      const double qx = (x >= 0 && x < vocab) ? q_of(n, x) : 0.0;
+      const double u = u_accept[(size_t)b * L + n];
+      if (qx <= 0.0) continue;  // ratio +inf: accepted
+      const double ratio = px / qx;
+      if (close > L && std::fabs(u - ratio) <= tol * ratio) close = n;
+      if (!(u < ratio)) break;
+    }
+    std::vector<double> w(vocab);
+    if (n < L) {
+      for (int v = 0; v < vocab; ++v) w[v] = p[v];
+      for (int k = 0; k < K; ++k) {
+        const int v = cand_idx[((size_t)b * L + n) * K + k];
+        if (v >= 0 && v < vocab) w[v] -= cand_prob[((size_t)b * L + n) * K + k];
+      }
+      for (int v = 0; v < vocab; ++v) w[v] = std::max(0.0, w[v]);
+    } else {
+      probs_of_row(L, p);
+      for (int v = 0; v < vocab; ++v) w[v] = p[v];
+    }
+    double total = 0.0;
+    for (int v = 0; v < vocab; ++v) total += w[v];
+    if (total <= 0.0) {
+      for (int v = 0; v < vocab; ++v) w[v] = p[v];
+      total = 0.0;
+      for (int v = 0; v < vocab; ++v) total += w[v];
+    }
+    const double target = (double)u_sample[b] * total, lo = target - tol * total, hi = target + tol * total;
+    int y = -1, ylo = -1, yhi = -1, last = 0;
+    double c = 0.0;
+    for (int v = 0; v < vocab; ++v) {
+      if (w[v] > 0.0) last = v;
+      c += w[v];
+      if (ylo < 0 && c > lo) ylo = v;
+      if (y < 0 && c > target) y = v;
+      if (yhi < 0 && c > hi) yhi = v;
+    }
+    if (y < 0) y = last;
+    if (ylo < 0) ylo = last;
+    if (yhi < 0) yhi = last;
+    n_accept[b] = n;
+    token[b] = y;
+    if (first_close) first_close[b] = close;
+    if (token_lo) token_lo[b] = ylo;
+    if (token_hi) token_hi[b] = yhi;
   }
   return 0;
 }

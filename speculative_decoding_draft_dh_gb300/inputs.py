@@ -82,12 +82,43 @@ TREE_CONFIGS = {
 }
 
 
+@dataclass(frozen=True)
+class VerifyConfig:
+    """Chain verification at positive temperature: B requests, each with L drafted tokens (the
+    round's depth, fixed before the round), target logits for the L+1 positions, and the draft's
+    distribution at each drafted position given as K candidate ids with their probabilities."""
+    name: str
+    B: int
+    L: int
+    vocab: int
+    K: int
+    dtype: str
+    logit_std: float = 3.0
+    match: float = 0.7
+    boost: float = 2.0
+    temperature: float = 1.0
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+
+VERIFY_CONFIGS = {
+    "tiny_verify": VerifyConfig("tiny_verify", 8, 4, 4096, 16, "f32", 1.0),
+    "verify": VerifyConfig("verify", 64, 7, 151936, 64, "bf16"),
+}
+
+
 def head_config(name: str, **overrides) -> HeadConfig:
     return replace(HEAD_CONFIGS[name], **overrides)
 
 
 def tree_config(name: str, **overrides) -> TreeConfig:
     return replace(TREE_CONFIGS[name], **overrides)
+
+
+def verify_config(name: str, **overrides) -> VerifyConfig:
+    return replace(VERIFY_CONFIGS[name], **overrides)
 
 
 def _gen(device, seed):
@@ -191,3 +222,61 @@ def make_tree(cfg: TreeConfig, seed: int = 0, device="cpu") -> dict:
         logits[bi, pi, ti] = (rowmax + cfg.boost).to(cfg.torch_dtype)
     return {"logits": logits, "parent": torch.from_numpy(parent).to(dev),
             "token": torch.from_numpy(token).to(dev)}
+
+
+def _distinct_ids(rng, vocab: int, k: int) -> np.ndarray:
+    """k distinct ids, uniform over [0, vocab), in the order first drawn."""
+    out, seen = [], set()
+    while len(out) < k:
+        for v in rng.integers(0, vocab, size=2 * k).tolist():
+            if v not in seen:
+                seen.add(v)
+                out.append(v)
+                if len(out) == k:
+                    break
+    return np.asarray(out, dtype=np.int32)
+
+
+def make_verify(cfg: VerifyConfig, seed: int = 0, device="cpu") -> dict:
+    """Draw the inputs of chain verification.
+
+    cand_idx int32 [B, L, K] (distinct ids per position), cand_prob fp32 [B, L, K] (a Dirichlet(0.5)
+    draw per position), draft_token int32 [B, L] (drawn from that distribution), the uniforms
+    u_accept fp32 [B, L] and u_sample fp32 [B] in [0, 1), and target logits [B, L+1, vocab] ~
+    N(0, logit_std^2) in the workload dtype; at a fraction ``match`` of the drafted positions the
+    drafted token's target logit is set to rowmax + boost, so that the target often agrees.
+    """
+    dev = torch.device(device)
+    rng = np.random.default_rng(seed)
+    B, L, K = cfg.B, cfg.L, cfg.K
+    cand = np.stack([_distinct_ids(rng, cfg.vocab, K) for _ in range(B * L)]).reshape(B, L, K) if L else \
+        np.zeros((B, 0, K), dtype=np.int32)
+    q64 = rng.dirichlet(np.full(K, 0.5), size=(B, L)) if L else np.zeros((B, 0, K))
+    q = q64.astype(np.float32)
+    draft = np.zeros((B, L), dtype=np.int32)
+    for b in range(B):
+        for i in range(L):
+            w = q64[b, i] / q64[b, i].sum()
+            draft[b, i] = cand[b, i, int(rng.choice(K, p=w))]
+    u_accept = rng.random((B, L), dtype=np.float32)
+    u_sample = rng.random(B, dtype=np.float32)
+    marked = rng.random((B, L)) < cfg.match
+    g = _gen(dev, seed)
+    logits = torch.empty(B, L + 1, cfg.vocab, device=dev, dtype=cfg.torch_dtype)
+    for b in range(B):
+        blk = torch.randn(L + 1, cfg.vocab, generator=g, device=dev, dtype=torch.float32)
+        logits[b] = (blk * cfg.logit_std).to(cfg.torch_dtype)
+    bs, is_, ts = [], [], []
+    for b in range(B):
+        for i in range(L):
+            if marked[b, i]:
+                bs.append(b); is_.append(i); ts.append(int(draft[b, i]))
+    if bs:
+        bi = torch.tensor(bs, device=dev)
+        ii = torch.tensor(is_, device=dev)
+        ti = torch.tensor(ts, device=dev)
+        rowmax = logits[bi, ii].float().amax(dim=-1)
+        logits[bi, ii, ti] = (rowmax + cfg.boost).to(cfg.torch_dtype)
+    to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    return {"logits": logits, "cand_idx": to(cand), "cand_prob": to(q), "draft_token": to(draft),
+            "u_accept": to(u_accept), "u_sample": to(u_sample)}

@@ -122,6 +122,24 @@ def _run(worker, world=2):
     return sorted(out, key=lambda t: t[0])
 
 
+def test_bench_spawns_one_rank_per_requested_gpu():
+    """bench.py --gpus 2 without a launcher starts two ranks itself; with --dry-run they meet over
+    gloo on the CPU, and rank 0 reports both ranks and the world size."""
+    import json
+    import subprocess
+    import sys
+    env = {k: v for k, v in os.environ.items() if k not in ("RANK", "WORLD_SIZE", "LOCAL_RANK", "MASTER_PORT")}
+    res = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2", "--dry-run"],
+                         capture_output=True, text=True, timeout=300, env=env)
+    assert res.returncode == 0, res.stderr[-2000:]
+    lines = [json.loads(x) for x in res.stdout.splitlines() if x.startswith("{")]
+    assert len(lines) == 1, res.stdout
+    line = lines[0]
+    assert line["n_gpus"] == 2 and line["gpus_requested"] == 2
+    assert sorted(r["rank"] for r in line["ranks"]) == [0, 1]
+    assert line["ms_slowest"] == pytest.approx(max(r["ms"] for r in line["ranks"]))
+
+
 def test_replicas_take_the_slowest_rank_and_scale_weakly():
     out = _run(_bench_worker)
     for rank, slowest, value in out:

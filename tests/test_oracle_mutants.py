@@ -7,6 +7,7 @@ import pytest
 
 import oracle
 from tests import test_oracle_pins as pins
+from tests import test_oracle_verify as vpins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dh_oracle.cpp")
 
@@ -44,12 +45,25 @@ MUTANTS = [
      ["test_golden_expansions", "test_expansion_matches_lexsort"]),
     ("expand_keeps_at_threshold", "if (a > min_benefit) ++keep;", "if (a >= min_benefit) ++keep;",
      ["test_golden_expansions"]),
+    ("verify_residual_keeps_draft_mass", "if (v >= 0 && v < vocab) w[v] -= cand_prob[((size_t)b * L + n) * K + k];",
+     "if (v >= 0 && v < vocab) w[v] -= 0.0;",
+     ["vpins.test_golden_verify", "vpins.test_emitted_tokens_follow_the_target_distribution"]),
+    ("verify_accept_inverted", "if (!(u < ratio)) break;", "if (u < ratio) break;",
+     ["vpins.test_golden_verify", "vpins.test_emitted_tokens_follow_the_target_distribution"]),
+    ("verify_ignores_temperature", "p[v] = stored_value(logits, dtype, (row0 + i) * (size_t)vocab + v) / temperature;",
+     "p[v] = stored_value(logits, dtype, (row0 + i) * (size_t)vocab + v);",
+     ["vpins.test_golden_verify", "vpins.test_temperature_scales_the_target"]),
+    ("verify_bonus_from_last_drafted_row", "probs_of_row(L, p);", "probs_of_row(L > 0 ? L - 1 : 0, p);",
+     ["vpins.test_golden_verify", "vpins.test_emitted_tokens_follow_the_target_distribution"]),
+    ("verify_draft_outside_list_rejected", "if (qx <= 0.0) continue;  // ratio +inf: accepted",
+     "if (qx <= 0.0) break;", ["vpins.test_golden_verify"]),
 ]
 
 
 def _run_pin(name):
     """Run every parametrisation of one pin; return True if any of them fails."""
-    fn = getattr(pins, name)
+    mod, _, attr = name.rpartition(".")
+    fn = getattr(vpins if mod == "vpins" else pins, attr)
     marks = getattr(fn, "pytestmark", [])
     params = [m for m in marks if m.name == "parametrize"]
     if not params:
