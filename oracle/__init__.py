@@ -50,6 +50,8 @@ def bind(path: str):
     D = ctypes.c_double
     lib.oracle_verify_chain.argtypes = [P, I, I, I, I, I, P, P, P, P, P, D, D, P, P, P, P, P]
     lib.oracle_verify_chain.restype = I
+    lib.oracle_size_level.argtypes = [P, P, P, I, I, I, P, P, I, I, I, ctypes.c_float, P, P, P, P]
+    lib.oracle_size_level.restype = I
     for f in ("oracle_round_bf16", "oracle_lowrank_project", "oracle_lowrank_scores",
               "oracle_lowrank_topk", "oracle_exact_rescore", "oracle_tree_accept"):
         getattr(lib, f).restype = I
@@ -222,4 +224,26 @@ def verify_chain(logits, cand_idx, cand_prob, draft_token, u_accept, u_sample, t
                                       _ptr(us), float(temperature), float(tol), _ptr(out["n_accept"]),
                                       _ptr(out["token"]), _ptr(out["first_close"]), _ptr(out["token_lo"]),
                                       _ptr(out["token_hi"])), "verify_chain")
+    return out
+
+
+def size_level(child_prob, child_token, cost, bin_batch, batch, theta, n_valid=None):
+    """Step 9: the next level's width and children for each request.
+
+    child_prob fp32 / child_token int32 [R, F, Wc]; n_valid int32 [R, F] or None; cost fp32
+    [n_bins, wmax + 1]; bin_batch int32 [n_bins].  Returns dict(width [R], parent, token, prob
+    [R, wmax])."""
+    cp = np.ascontiguousarray(np.asarray(child_prob, dtype=np.float32))
+    R, F, Wc = cp.shape
+    ct = np.ascontiguousarray(np.asarray(child_token, dtype=np.int32)).reshape(R, F, Wc)
+    nv = None if n_valid is None else np.ascontiguousarray(np.asarray(n_valid, dtype=np.int32)).reshape(R, F)
+    c = np.ascontiguousarray(np.asarray(cost, dtype=np.float32))
+    n_bins, w1 = c.shape
+    wmax = w1 - 1
+    bb = np.ascontiguousarray(np.asarray(bin_batch, dtype=np.int32)).reshape(n_bins)
+    out = {"width": np.empty(R, dtype=np.int32), "parent": np.empty((R, wmax), dtype=np.int32),
+           "token": np.empty((R, wmax), dtype=np.int32), "prob": np.empty((R, wmax), dtype=np.float32)}
+    _check(load().oracle_size_level(_ptr(cp), _ptr(ct), None if nv is None else _ptr(nv), R, F, Wc, _ptr(c), _ptr(bb),
+                                    n_bins, wmax, int(batch), float(theta), _ptr(out["width"]), _ptr(out["parent"]),
+                                    _ptr(out["token"]), _ptr(out["prob"])), "size_level")
     return out

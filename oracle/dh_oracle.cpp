@@ -56,6 +56,21 @@
 //        drawn by inverse CDF in vocabulary order with the uniform w_b: y = the smallest v whose
 //        running sum of the weights exceeds w_b times their total (a zero total: the weights p_n).
 //
+//   EAGLE-4 summary page, section "Why a draft tree needs a cost model": latency tables indexed by
+//   batch and verification width price another level; products of draft probabilities estimate its
+//   benefit A in accepted tokens; each round decides whether to deepen and how wide to go at the
+//   current load, by comparing A with its latency cost C against a threshold (the page's formula
+//   is lost; this is its plainest per-branch reading).  AlphaSignal page, section "Runtime-sized
+//   speculation": depth and branching are chosen for the active batch size.
+//     9. sizing the next level of request r: its frontier's candidate children (path probability
+//        A, token, parent slot) are ordered by (A desc, parent asc, slot asc; NaN below every
+//        number); with the cost row of the current batch (the first bin whose batch bound is at
+//        least the batch, else the last), the j-th child (j = 0, 1, ...) is kept while
+//          A_j > theta x (cost[j+1] - cost[j])      (fp32: one rounding for the difference, one
+//                                                    for the product; the comparison is exact)
+//        i.e. while its benefit per unit of its marginal latency passes theta; the first child
+//        that fails, or the width limit, ends the level.  width 0 means: do not deepen.
+//
 // Build: g++ -O2 -std=c++17 -fopenmp -ffp-contract=off -shared -fPIC dh_oracle.cpp
 #include <algorithm>
 #include <cmath>
@@ -365,6 +380,50 @@ int oracle_verify_chain(const void* logits, int dtype, int B, int L, int vocab, 
     if (first_close) first_close[b] = close;
     if (token_lo) token_lo[b] = ylo;
     if (token_hi) token_hi[b] = yhi;
+  }
+  return 0;
+}
+
+// Step 9 for every request.  child_prob, child_token: R x F x Wc (per frontier node, its candidate
+// children); n_valid: R x F (children valid per node, null = all Wc); cost: n_bins x (wmax + 1)
+// latencies in any unit, bin_batch: n_bins batch bounds (ascending); outputs: width R,
+// sel_parent / sel_token / sel_prob R x wmax (the kept children in order; -1 / -1 / 0 after width).
+int oracle_size_level(const float* child_prob, const int32_t* child_token, const int32_t* n_valid, int R, int F,
+                      int Wc, const float* cost, const int32_t* bin_batch, int n_bins, int wmax, int batch, float theta,
+                      int32_t* width, int32_t* sel_parent, int32_t* sel_token, float* sel_prob) {
+  if (R < 0 || F <= 0 || Wc <= 0 || n_bins <= 0 || wmax <= 0) return -1;
+  int bin = n_bins - 1;
+  for (int i = 0; i < n_bins; ++i)
+    if (batch <= bin_batch[i]) { bin = i; break; }
+  const float* c = cost + (size_t)bin * (wmax + 1);
+  for (int r = 0; r < R; ++r) {
+    struct Child { float a; int f, slot; };
+    std::vector<Child> kids;
+    for (int f = 0; f < F; ++f) {
+      const int nv = n_valid ? std::min(std::max(n_valid[(size_t)r * F + f], 0), Wc) : Wc;
+      for (int k = 0; k < nv; ++k) kids.push_back({child_prob[((size_t)r * F + f) * Wc + k], f, k});
+    }
+    std::stable_sort(kids.begin(), kids.end(), [](const Child& x, const Child& y) {
+      const bool nx = std::isnan(x.a), ny = std::isnan(y.a);
+      if (nx != ny) return ny;  // the number ranks first
+      if (!nx && x.a != y.a) return x.a > y.a;
+      if (x.f != y.f) return x.f < y.f;
+      return x.slot < y.slot;
+    });
+    int w = 0;
+    while (w < wmax && w < (int)kids.size()) {
+      const float dc = c[w + 1] - c[w];
+      const float thr = theta * dc;
+      if (!(kids[w].a > thr)) break;
+      ++w;
+    }
+    width[r] = w;
+    for (int j = 0; j < wmax; ++j) {
+      const bool on = j < w;
+      sel_parent[(size_t)r * wmax + j] = on ? kids[j].f : -1;
+      sel_token[(size_t)r * wmax + j] = on ? child_token[((size_t)r * F + kids[j].f) * Wc + kids[j].slot] : -1;
+      sel_prob[(size_t)r * wmax + j] = on ? kids[j].a : 0.0f;
+    }
   }
   return 0;
 }

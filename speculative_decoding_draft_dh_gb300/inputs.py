@@ -280,3 +280,32 @@ def make_verify(cfg: VerifyConfig, seed: int = 0, device="cpu") -> dict:
     to = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     return {"logits": logits, "cand_idx": to(cand), "cand_prob": to(q), "draft_token": to(draft),
             "u_accept": to(u_accept), "u_sample": to(u_sample)}
+
+
+# Synthetic latency table for sizing a draft level (the pages' tables come from engine profiling,
+# which is out of scope): bins of batch size and, per bin, the latency in microseconds of a draft
+# level of w nodes and its verification, base + slope x w for w >= 1 and 0 for w = 0.  Heavier
+# loads cost more per node, so they favour narrower, shallower trees.
+SIZING_BINS = (1, 8, 64, 512)
+SIZING_BASE_US = (30.0, 35.0, 50.0, 120.0)
+SIZING_SLOPE_US = (1.0, 2.5, 12.0, 80.0)
+
+
+def latency_table(wmax: int) -> tuple:
+    """(cost fp32 [len(SIZING_BINS), wmax + 1], bin_batch int32 [len(SIZING_BINS)])."""
+    cost = np.zeros((len(SIZING_BINS), wmax + 1), dtype=np.float32)
+    for i, (b0, s0) in enumerate(zip(SIZING_BASE_US, SIZING_SLOPE_US)):
+        cost[i, 1:] = [b0 + s0 * w for w in range(1, wmax + 1)]
+    return cost, np.asarray(SIZING_BINS, dtype=np.int32)
+
+
+def make_frontier_children(R: int, F: int, Wc: int, seed: int = 0, vocab: int = 151936) -> dict:
+    """Candidate children of R requests' frontiers of F nodes, Wc children each, as an expansion
+    would leave them: per node a path probability (uniform in [0.05, 1)) times Dirichlet(0.3)
+    child probabilities in descending order; tokens uniform; n_valid = Wc."""
+    rng = np.random.default_rng(seed)
+    par = rng.uniform(0.05, 1.0, size=(R, F, 1))
+    kid = -np.sort(-rng.dirichlet(np.full(max(Wc, 2), 0.3), size=(R, F))[..., :Wc], axis=-1)
+    prob = (par * kid).astype(np.float32)
+    token = rng.integers(0, vocab, size=(R, F, Wc)).astype(np.int32)
+    return {"child_prob": prob, "child_token": token, "n_valid": np.full((R, F), Wc, dtype=np.int32)}

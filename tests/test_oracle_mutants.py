@@ -8,6 +8,7 @@ import pytest
 import oracle
 from tests import test_oracle_pins as pins
 from tests import test_oracle_verify as vpins
+from tests import test_oracle_sizing as spins
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "dh_oracle.cpp")
 
@@ -57,13 +58,21 @@ MUTANTS = [
      ["vpins.test_golden_verify", "vpins.test_emitted_tokens_follow_the_target_distribution"]),
     ("verify_draft_outside_list_rejected", "if (qx <= 0.0) continue;  // ratio +inf: accepted",
      "if (qx <= 0.0) break;", ["vpins.test_golden_verify"]),
+    ("sizing_keeps_at_threshold", "if (!(kids[w].a > thr)) break;", "if (!(kids[w].a >= thr)) break;",
+     ["spins.test_golden_sizing"]),
+    ("sizing_total_not_marginal_cost", "const float dc = c[w + 1] - c[w];", "const float dc = c[w + 1];",
+     ["spins.test_golden_sizing", "spins.test_random_frontiers_against_brute_force"]),
+    ("sizing_ties_to_higher_parent", "if (x.f != y.f) return x.f < y.f;", "if (x.f != y.f) return x.f > y.f;",
+     ["spins.test_golden_sizing", "spins.test_random_frontiers_against_brute_force"]),
+    ("sizing_first_bin_always", "if (batch <= bin_batch[i]) { bin = i; break; }", "{ bin = 0; break; }",
+     ["spins.test_golden_sizing", "spins.test_random_frontiers_against_brute_force"]),
 ]
 
 
 def _run_pin(name):
     """Run every parametrisation of one pin; return True if any of them fails."""
     mod, _, attr = name.rpartition(".")
-    fn = getattr(vpins if mod == "vpins" else pins, attr)
+    fn = getattr({"vpins": vpins, "spins": spins}.get(mod, pins), attr)
     marks = getattr(fn, "pytestmark", [])
     params = [m for m in marks if m.name == "parametrize"]
     if not params:
