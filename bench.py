@@ -52,11 +52,14 @@ L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # fp32 FMA peak of the CUDA cores: 152 SMs x 128 fp32 lanes x 2 FLOP x 2.07 GHz
 FP32_CORE_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
-DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200, "level": 10000}
-DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5, "level": 100}
-EXTRA_WORKLOADS = ["moderate", "high", "level", "tree"]
+DEFAULT_STEPS = {"batch1": 20000, "moderate": 5000, "high": 500, "tree": 200, "level": 10000, "verify": 2000}
+DEFAULT_WARMUP = {"batch1": 200, "moderate": 50, "high": 10, "tree": 5, "level": 100, "verify": 10}
+EXTRA_WORKLOADS = ["moderate", "high", "level", "tree", "verify"]
 MIN_TIMED_S = 0.1  # every added workload's timed region
 EXPAND_W = {"level": 4}  # children per frontier node in the draft-level workload
+# the draft level then sizes the next level: requests (the frontier nodes split evenly), width limit,
+# threshold in accepted tokens per microsecond of the synthetic latency table
+SIZE_LEVEL = {"level": {"requests": 2, "wmax": 8, "theta": 0.01}}
 # the kernel each workload's `roofline` reports (the one that moves the step's bytes)
 ROOFLINE_KERNEL = {"batch1": "scores_lsu", "moderate": "rescore_ring", "high": "rescore_ring",
                    "level": "lowrank_mma", "tree": "tree_argmax"}
@@ -68,7 +71,8 @@ def parse_args(argv=None):
     ap.add_argument("--steps", type=int, default=None)
     ap.add_argument("--warmup", type=int, default=None)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--workload", default="batch1", choices=["batch1", "moderate", "high", "tree", "level"])
+    ap.add_argument("--workload", default="batch1",
+                    choices=["batch1", "moderate", "high", "tree", "level", "verify"])
     ap.add_argument("--only", action="store_true", help="time the named workload alone (no `workloads`)")
     ap.add_argument("--api", default="head", choices=["head", "split"],
                     help="head: dh_draft_head (both stages in one call); split: dh_lowrank_topk + "
@@ -274,7 +278,10 @@ KERNEL_FILES = {"scores_summary": ["gemv_topk.cu", "dh_internal.cuh"],
                 "proj_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
                 "proj_reduce_mma": ["mma_topk.cu", "sm100.cuh", "dh_internal.cuh"],
                 "tree_argmax": ["tree.cu", "dh_internal.cuh"],
-                "tree_walk": ["tree.cu", "dh_internal.cuh"]}
+                "tree_walk": ["tree.cu", "dh_internal.cuh"],
+                "size_level": ["sizing.cu", "dh_internal.cuh"],
+                "verify_stats": ["verify.cu", "dh_internal.cuh"],
+                "verify_walk": ["verify.cu", "dh_internal.cuh"]}
 
 
 def head_bytes(cfg):
@@ -331,6 +338,9 @@ def kernel_algo(cfg, name, peaks):
         return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name == "select":
         return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16, "GB/s"
+    if name == "size_level":  # the children in, the next frontier out
+        sz = SIZE_LEVEL.get(cfg.name, {"wmax": 0})
+        return "hbm", cfg.B * EXPAND_W.get(cfg.name, 0) * 8 + cfg.B * 4 + sz.get("requests", 0) * sz["wmax"] * 12, "GB/s"
     return "hbm", 0, "GB/s"
 
 
@@ -380,12 +390,23 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warm
     stream = torch.cuda.Stream(device=dev)
 
     expand_w = EXPAND_W.get(cfg.name, 0)
+    sizing = SIZE_LEVEL.get(cfg.name)
+    if sizing:
+        cost, bins = inputs.latency_table(sizing["wmax"])
+        cost_d, bins_d = torch.from_numpy(cost).to(dev), torch.from_numpy(bins).to(dev)
+        R = sizing["requests"]
     for x in sets:
         if expand_w:
             x["par"] = torch.linspace(1.0, 0.25, cfg.B, device=dev, dtype=torch.float32)
             x["ctok"] = torch.empty(cfg.B, expand_w, dtype=torch.int32, device=dev)
             x["cprob"] = torch.empty(cfg.B, expand_w, dtype=torch.float32, device=dev)
             x["keep"] = torch.empty(cfg.B, dtype=torch.int32, device=dev)
+        if sizing:
+            w = sizing["wmax"]
+            x["next"] = {"width": torch.empty(R, dtype=torch.int32, device=dev),
+                         "parent": torch.empty(R, w, dtype=torch.int32, device=dev),
+                         "token": torch.empty(R, w, dtype=torch.int32, device=dev),
+                         "prob": torch.empty(R, w, dtype=torch.float32, device=dev)}
 
     def step(x, idx=None, logits=None, probs=None):
         idx = x["idx"] if idx is None else idx
@@ -400,6 +421,10 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warm
         if expand_w:  # one draft level: the frontier nodes' children by exact probability
             dh.expand_children(probs, idx, expand_w, parent_prob=x["par"], min_benefit=1e-3,
                                child_token=x["ctok"], child_prob=x["cprob"], n_keep=x["keep"])
+        if sizing:  # and the next level's width at the current load
+            F = cfg.B // R
+            dh.size_level(x["cprob"].view(R, F, expand_w), x["ctok"].view(R, F, expand_w), cost_d, bins_d, R,
+                          sizing["theta"], n_valid=x["keep"].view(R, F), out=x["next"])
 
     with torch.cuda.stream(stream):
         for i in range(warmup):
@@ -556,6 +581,11 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warm
                    "parallelism": f"replicas x{world} (rows independent; no collective in the data path)"},
         "roofline": roofline, "roofline_time_dominant": roofline_time_dominant,
         "path_roofline": path_roofline, "stages": stages,
+        "draft_level": None if not expand_w else {
+            "frontier_nodes_per_s": round(value, 1), "levels_per_s": round(value / cfg.B, 1),
+            "children_per_node": expand_w,
+            "sizing": None if not sizing else dict(sizing, table="synthetic latency table (inputs.latency_table)",
+                                                    next_width=sets[0]["next"]["width"].tolist())},
         "gpu_launches": int(round(launches_per_step * steps)), "e2e": e2e,
         "cpu_baseline": cpu, "clocks": clocks,
     }
@@ -581,12 +611,39 @@ def head_e2e(a, cfg, sets, copies, step, stream, world, e_sz, S):
         step(x, idx, logits, probs)
         outs[j].copy_(packed[j], non_blocking=True)
 
-    # (1) graphs of S steps, each step with its own copies, queued in stream order (the host never
-    # waits): a caller that keeps the GPU fed
+    # (1) graphs of S steps: step j copies its h in on a copy stream (as soon as step j - copies,
+    # the last user of that buffer, is done), runs on the compute stream, and copies its results
+    # out on a third stream, so the copies of one step overlap the kernels of the others: a
+    # pipelined caller that keeps the GPU fed
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     g_steps = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_steps, stream=stream):
+        done = [None] * copies   # event after the kernels of the last step that used each buffer set
+        out_free = [None] * copies
         for j in range(S):
-            one(j % copies)
+            c = j % copies
+            x = sets[c]
+            idx, logits, probs = views[c]
+            h2d_s.wait_stream(stream) if done[c] is None else h2d_s.wait_event(done[c])
+            with torch.cuda.stream(h2d_s):
+                x["h"].copy_(hosts[c], non_blocking=True)
+                h_in = torch.cuda.Event()
+                h_in.record(h2d_s)
+            stream.wait_event(h_in)
+            if out_free[c] is not None:
+                stream.wait_event(out_free[c])
+            step(x, idx, logits, probs)
+            ev = torch.cuda.Event()
+            ev.record(stream)
+            done[c] = ev
+            d2h_s.wait_event(ev)
+            with torch.cuda.stream(d2h_s):
+                outs[c].copy_(packed[c], non_blocking=True)
+                of = torch.cuda.Event()
+                of.record(d2h_s)
+            out_free[c] = of
+        stream.wait_stream(h2d_s)
+        stream.wait_stream(d2h_s)
     n = S * max(1, min(2000 if cfg.B <= 64 else 200, 20 * S) // S)
     with torch.cuda.stream(stream):
         g_steps.replay()
@@ -632,7 +689,8 @@ def head_e2e(a, cfg, sets, copies, step, stream, world, e_sz, S):
     return {"value": round(cfg.B * n * world / te, 2), "unit": "rows/s",
             "us_per_call": round(te * 1e6 / n, 3), "steps": n,
             "how": f"wall clock; every step copies its h from pinned host memory, runs dh_draft_head and "
-                   f"copies its results to pinned host memory, in stream order; CUDA graphs of {S} such steps",
+                   f"copies its results to pinned host memory; copies on their own streams overlap other steps' "
+                   f"kernels; CUDA graphs of {S} such steps",
             "h2d_bytes_per_step": int(cfg.B * cfg.d * e_sz), "d2h_bytes_per_step": int(BK * 12),
             "synchronized_each_step": {"us_per_call": round(ts * 1e6 / n_sync, 3), "steps": n_sync},
             "python_eager_each_step": {"us_per_call": round(tp * 1e6 / n_py, 3), "steps": n_py}}
@@ -811,9 +869,163 @@ def cpu_tree_baseline(tcfg, t, seconds):
             "kind": "oracle", "sample": f"{done} requests (first {n} of the tree workload, repeated), {dt:.1f} s"}
 
 
+VERIFY_METRIC = ("chain-verification requests/sec and µs per call (speculative sampling: target softmax "
+                 "statistics, acceptance tests, residual or bonus draw); % of HBM roofline")
+
+
+def run_verify_bench(a, vcfg, rank, world, local, peaks, peak_src, steps=None, warmup=None, cpu_seconds=None):
+    """Times dh_verify_chain on the chain-verification workload (B requests of L drafted tokens)."""
+    from speculative_decoding_draft_dh_gb300 import binding as dh
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    warmup = a.warmup if warmup is None else warmup
+    B, L, vocab = vcfg.B, vcfg.L, vcfg.vocab
+    elem = 2 if vcfg.dtype == "bf16" else 4
+    logit_bytes = B * (L + 1) * vocab * elem
+    copies = max(2, min(8, math.ceil(2 * L2_BYTES / logit_bytes)))
+    sets = [inputs.make_verify(vcfg, seed=a.seed + 1000 * rank + i, device=dev) for i in range(copies)]
+    for v in sets:
+        v["n"] = torch.empty(B, dtype=torch.int32, device=dev)
+        v["tok"] = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = dh.Workspace()
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(v):
+        dh.verify_chain(v["logits"], v["cand_idx"], v["cand_prob"], v["draft_token"], v["u_accept"], v["u_sample"],
+                        temperature=vcfg.temperature, n_accept_out=v["n"], token_out=v["tok"], workspace=ws)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(sets[i % copies])
+    torch.cuda.synchronize()
+    S = copies * max(1, 16 // copies)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for j in range(S):
+            step(sets[j % copies])
+    if steps is None:
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            c0.record(stream)
+            for _ in range(3):
+                g.replay()
+            c1.record(stream)
+        torch.cuda.synchronize()
+        steps = int(max_over_ranks(auto_steps(c0.elapsed_time(c1) * 1e3 / (3 * S), S, S), world))
+    steps = max(S, steps // S * S)
+    sampler = ClockSampler(local)
+    time.sleep(0.15)
+    with torch.cuda.stream(stream):
+        g.replay()
+    barrier(world)
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        ev0.record(stream)
+        for _ in range(steps // S):
+            g.replay()
+        ev1.record(stream)
+    torch.cuda.synchronize()
+    t1 = time.perf_counter()
+    barrier(world)
+    time.sleep(0.12)
+    sampler.stop()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    us = ms * 1e3 / steps
+    value = weak_scaling_value(B, steps, world, ms)
+    n_prof = min(steps, 200)
+    dh.prof_enable(True)
+    with torch.cuda.stream(stream):
+        for i in range(n_prof):
+            step(sets[i % copies])
+    torch.cuda.synchronize()
+    dh.prof_enable(False)
+    prof = dh.prof_read()
+    stages = {k: {"us_avg": v[0] * 1e3 / v[1], "launches": v[1]} for k, v in prof.items()}
+    dom = "verify_stats"
+    achieved = logit_bytes / (stages[dom]["us_avg"] * 1e-6) / 1e9
+    peak = peaks["hbm_gbs"]
+    traffic = traffic_from_profiles(dom, vcfg.name, ["verify.cu", "dh_internal.cuh"])
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic_bytes_per_launch": logit_bytes,
+                "us_per_launch": round(stages[dom]["us_avg"], 3),
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+    in_bytes = logit_bytes + B * L * vcfg.K * 8 + B * L * 8 + B * 4
+    ideal_us = in_bytes / (peak * 1e9) * 1e6
+    path_roofline = {"rule": "target logits and the draft's inputs read once over the copy bandwidth",
+                     "ideal_us": round(ideal_us, 3), "measured_us": round(us, 3), "frac": round(ideal_us / us, 4)}
+    accept = float(sets[0]["n"].float().mean().item())
+    e2e = None
+    if not a.no_e2e:
+        v = sets[0]
+        keys = ("logits", "cand_idx", "cand_prob", "draft_token", "u_accept", "u_sample")
+        host = {k: v[k].cpu().pin_memory() for k in keys}
+        out_host = {k: torch.empty(B, dtype=torch.int32).pin_memory() for k in ("n", "tok")}
+
+        def one():
+            for k in keys:
+                v[k].copy_(host[k], non_blocking=True)
+            step(v)
+            for k in out_host:
+                out_host[k].copy_(v[k], non_blocking=True)
+        ge = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ge, stream=stream):
+            one()
+        with torch.cuda.stream(stream):
+            ge.replay()
+        stream.synchronize()
+        n_e2e = 50
+        te0 = time.perf_counter()
+        with torch.cuda.stream(stream):
+            for _ in range(n_e2e):
+                ge.replay()
+        stream.synchronize()
+        te = max_over_ranks(time.perf_counter() - te0, world)
+        e2e = {"value": round(B * n_e2e * world / te, 2), "unit": "requests/s", "us_per_call": round(te * 1e6 / n_e2e, 1),
+               "steps": n_e2e, "how": "wall clock; per step one CUDA-graph replay of: every input copied from pinned "
+                                      "host memory, dh_verify_chain, n_accept and token copied back",
+               "h2d_bytes_per_step": int(in_bytes), "d2h_bytes_per_step": int(B * 8)}
+    cpu = None
+    if rank == 0 and world == 1 and not a.no_cpu_baseline:
+        cpu = cpu_verify_baseline(vcfg, sets[0], a.cpu_seconds if cpu_seconds is None else cpu_seconds)
+    return {
+        "metric": VERIFY_METRIC, "value": round(value, 2), "unit": "requests/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": round(ms / steps, 6), "timed_ms": round(ms, 3), "us_per_call": round(us, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": vcfg.dtype,
+        "data": "synthetic (seeded generators)",
+        "config": {"workload": vcfg.name, "B": B, "L": L, "vocab": vocab, "K": vcfg.K, "T": vcfg.temperature,
+                   "seed": a.seed, "graph": f"CUDA graphs of {S} steps",
+                   "l2": f"inputs rotate over {copies} copies ({copies * logit_bytes / 2**20:.0f} MiB per cycle > 2x L2)",
+                   "accepted_per_request": round(accept, 3),
+                   "parallelism": f"replicas x{world} (requests independent; no collective in the data path)"},
+        "roofline": roofline, "path_roofline": path_roofline, "stages": stages,
+        "gpu_launches": int(round(sum(x[1] for x in prof.values()) / n_prof * steps)),
+        "e2e": e2e, "cpu_baseline": cpu, "clocks": sampler.summary(t0, t1),
+    }
+
+
+def cpu_verify_baseline(vcfg, v, seconds):
+    import oracle
+    oracle.build()
+    cores = len(os.sched_getaffinity(0))
+    n = min(vcfg.B, cores)
+    cpu = {k: t[:n].cpu() for k, t in v.items() if k not in ("n", "tok")}
+    done = 0
+    t0 = time.perf_counter()
+    while time.perf_counter() - t0 < seconds or done == 0:
+        oracle.verify_chain(cpu["logits"], cpu["cand_idx"], cpu["cand_prob"], cpu["draft_token"], cpu["u_accept"],
+                            cpu["u_sample"], temperature=vcfg.temperature)
+        done += n
+    dt = time.perf_counter() - t0
+    return {"value": round(done / dt, 3), "unit": "requests/s", "cores": n, "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": f"{done} requests (first {n} of the verify workload, repeated), {dt:.1f} s"}
+
+
 def summarize(line):
     """The fields of a workload's line kept in the headline's `workloads` object."""
-    keep = ("metric", "value", "unit", "us_per_call", "steps", "timed_ms", "node_rows_per_s", "config",
+    keep = ("metric", "value", "unit", "us_per_call", "steps", "timed_ms", "node_rows_per_s", "draft_level", "config",
             "path_roofline", "roofline", "roofline_time_dominant", "stages", "gpu_launches", "e2e",
             "cpu_baseline", "clocks", "timing_spread")
     return {k: line[k] for k in keep if k in line and line[k] is not None}
@@ -835,7 +1047,30 @@ def run_reference(a, rank, world):
     if rank != 0:
         return None
     budget = 60.0
-    if a.workload == "tree":
+    if a.workload == "verify":
+        vcfg = inputs.VERIFY_CONFIGS["verify"]
+        import oracle
+        oracle.build()
+        cores = len(os.sched_getaffinity(0))
+        n = min(vcfg.B, cores)
+        v = {k: t[:n] for k, t in inputs.make_verify(vcfg, seed=a.seed, device="cpu").items()}
+
+        def one_v():
+            oracle.verify_chain(v["logits"], v["cand_idx"], v["cand_prob"], v["draft_token"], v["u_accept"],
+                                v["u_sample"], temperature=vcfg.temperature)
+        warm = warm_up(one_v, a.warmup)
+        steps = 0
+        t0 = time.perf_counter()
+        while steps < a.steps and (time.perf_counter() - t0 < budget or steps == 0):
+            one_v()
+            steps += 1
+        dt = time.perf_counter() - t0
+        value = n * steps / dt
+        unit, metric = "requests/s", VERIFY_METRIC
+        sample = f"{steps} steps of {n} requests of the verify workload (L={vcfg.L}, vocab={vcfg.vocab})"
+        cfgd = {"workload": "verify", "B": vcfg.B, "L": vcfg.L, "vocab": vcfg.vocab, "K": vcfg.K}
+        threads = n
+    elif a.workload == "tree":
         tcfg = inputs.TREE_CONFIGS["tree"]
         small = inputs.tree_config("tree", B=min(16, tcfg.B))
         t = inputs.make_tree(small, seed=a.seed, device="cpu")
@@ -902,6 +1137,11 @@ def profile_run(a):
         t = inputs.make_tree(inputs.TREE_CONFIGS["tree"], seed=a.seed, device=dev)
         for _ in range(a.warmup + a.steps):
             dh.tree_accept(t["logits"], t["parent"], t["token"])
+    elif a.workload == "verify":
+        v = inputs.make_verify(inputs.VERIFY_CONFIGS["verify"], seed=a.seed, device=dev)
+        for _ in range(a.warmup + a.steps):
+            dh.verify_chain(v["logits"], v["cand_idx"], v["cand_prob"], v["draft_token"], v["u_accept"],
+                            v["u_sample"])
     else:
         cfg = inputs.HEAD_CONFIGS[a.workload]
         x = inputs.make_head(cfg, seed=a.seed, device=dev)
@@ -978,6 +1218,8 @@ def main():
     peaks, src = load_peaks()
     if a.workload == "tree":
         line = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src, steps=a.steps)
+    elif a.workload == "verify":
+        line = run_verify_bench(a, inputs.VERIFY_CONFIGS["verify"], rank, world, local, peaks, src, steps=a.steps)
     else:
         line = run_head_bench(a, inputs.HEAD_CONFIGS[a.workload], rank, world, local, peaks, src, steps=a.steps)
     if not a.only and a.workload == "batch1":
@@ -987,6 +1229,9 @@ def main():
             if w == "tree":
                 sub = run_tree_bench(a, inputs.TREE_CONFIGS["tree"], rank, world, local, peaks, src,
                                      warmup=DEFAULT_WARMUP[w], cpu_seconds=cpu_s)
+            elif w == "verify":
+                sub = run_verify_bench(a, inputs.VERIFY_CONFIGS["verify"], rank, world, local, peaks, src,
+                                       warmup=DEFAULT_WARMUP[w], cpu_seconds=cpu_s)
             else:
                 sub = run_head_bench(a, inputs.HEAD_CONFIGS[w], rank, world, local, peaks, src,
                                      warmup=DEFAULT_WARMUP[w], cpu_seconds=cpu_s)

@@ -175,6 +175,87 @@ int dh_expand_children(const float* probs, const int32_t* idx, const float* pare
                        void* stream);
 
 /* ---------------------------------------------------------------------------------------------
+ * Vocabulary-sharded draft head (tensor-parallel serving).
+ *
+ * EAGLE-4 summary page, section "Adaptation has not eliminated high-load regressions" (the release
+ * serves the target with tensor parallelism over four GPUs), and section "Retrieve vocabulary
+ * candidates cheaply, then score them exactly".  The vocabulary is split into P contiguous shards;
+ * shard p holds V_p = V[:, o_p : o_p + n_p] (its own contiguous [r x n_p] array) and
+ * W_p = W[o_p : o_p + n_p, :].  One step of the head on P shards:
+ *   1. every shard: dh_lowrank_topk_shard -> its K best (global id, score) per row
+ *   2. exchange the P lists (all-gather: 8 x B x K bytes per shard), then dh_merge_topk -> the K
+ *      best of the union, the candidates of dh_lowrank_topk on the whole vocabulary: a global top-K
+ *      member is in its shard's top K.  (Scores agree to rounding: where the selection re-scores a
+ *      group exactly, its summation order differs from the scores kernel's, and which groups it
+ *      re-scores depends on the shard; so ids may differ only between near-equal scores.)
+ *   3. every shard: dh_exact_rescore_shard on the merged ids -> the logits of the ids it owns (-inf
+ *      elsewhere) and its (max, sum of exp) per row
+ *   4. exchange logits and pairs (all-gather: (4 x B x K + 8 x B) bytes per shard), then
+ *      dh_combine_softmax -> every candidate's logit from its owner and the softmax over the K
+ *      candidates (the unsharded probabilities up to rounding)
+ * The exchange itself is the caller's (e.g. NCCL); all buffers are device memory.
+ *
+ * dh_lowrank_topk_shard: dh_lowrank_topk on V_shard [r x vocab_shard] (same arguments, workspace
+ *   from dh_lowrank_topk_workspace with vocab_shard), then idx_out += vocab_offset.  Needs
+ *   K <= vocab_shard; vocab_offset >= 0 and vocab_offset + vocab_shard <= DH_MAX_VOCAB.
+ * dh_merge_topk: idx_parts int32 / score_parts fp32 [P x B x K] (part p = shard p's output) ->
+ *   idx_out int32 / score_out fp32 [B x K], ordered by (score desc, id asc); entries with id < 0
+ *   or a NaN score are skipped; a row with fewer than K entries is padded with (-1, -inf).
+ *   P x K <= DH_MAX_MERGE_ENTRIES.  No workspace.
+ * dh_exact_rescore_shard: idx [B x K] global ids; for the ids in [vocab_offset, vocab_offset +
+ *   vocab_shard): logits_out[b,k] = h[b,:] . W_shard[idx - vocab_offset, :] as dh_exact_rescore
+ *   computes it; other ids: -inf.  stats_out fp32 [B x 2]: per row the maximum m of its logits and
+ *   the sum of exp(logit - m) (m = -inf, sum 0 when the shard owns none).  Workspace:
+ *   dh_exact_rescore_shard_workspace bytes, zero-filled before first use, as for dh_exact_rescore.
+ * dh_combine_softmax: logits_parts [P x B x K] and stats_parts [P x B x 2] from the P shards ->
+ *   logits_out [B x K] (each candidate's owned logit: the maximum over the parts) and probs_out
+ *   [B x K] (may be NULL): exp(logit - M) / S with M = max_p m_p, S = sum_p sum_p' exp(m_p - M).
+ * ------------------------------------------------------------------------------------------- */
+#define DH_MAX_MERGE_ENTRIES 8192
+int dh_lowrank_topk_shard(const void* h, const void* U, const void* V_shard, int B, int d, int r, int vocab_shard,
+                          int vocab_offset, int K, int dtype, int32_t* idx_out, float* score_out, void* workspace,
+                          size_t ws_bytes, void* stream);
+int dh_merge_topk(const int32_t* idx_parts, const float* score_parts, int P, int B, int K, int32_t* idx_out,
+                  float* score_out, void* stream);
+size_t dh_exact_rescore_shard_workspace(int B, int d, int vocab_shard, int K, int dtype);
+int dh_exact_rescore_shard(const void* h, const void* W_shard, const int32_t* idx, int B, int d, int vocab_shard,
+                           int vocab_offset, int K, int dtype, float* logits_out, float* stats_out, void* workspace,
+                           size_t ws_bytes, void* stream);
+int dh_combine_softmax(const float* logits_parts, const float* stats_parts, int P, int B, int K, float* logits_out,
+                       float* probs_out, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Sizing the next draft level by benefit over latency cost.
+ *
+ * EAGLE-4 summary page, section "Why a draft tree needs a cost model": products of draft
+ * probabilities estimate a branch's benefit A in accepted tokens, latency tables indexed by batch
+ * and verification width price another level, and each round decides whether to deepen and how wide
+ * to go by comparing A with its cost against a threshold (the page's formula is lost; this is its
+ * per-branch reading).  AlphaSignal page, section "Runtime-sized speculation": depth and branching
+ * are chosen for the active batch size.
+ *
+ * Request r's frontier has F nodes with Wc candidate children each (e.g. dh_expand_children's
+ * outputs): path probabilities child_prob[r,f,k] and tokens child_token[r,f,k], of which the first
+ * n_valid[r,f] are valid (n_valid NULL: all Wc).  With the cost row of the current batch (row i of
+ * cost [n_bins x (wmax+1)] for the first i with batch <= bin_batch[i], else the last row):
+ *   order      = the valid children by (A desc, f asc, k asc); a NaN probability ranks below every
+ *                number
+ *   child j of the order is kept while A_j > theta x (cost[j+1] - cost[j])  (fp32: the difference
+ *                and the product each rounded once; no fused multiply-add), j < wmax
+ *   width_out[r] = the number kept (0: do not deepen)
+ *   sel_parent[r,j], sel_token[r,j], sel_prob[r,j] = f, token and A of kept child j; -1, -1, 0 for
+ *                j >= width (the next frontier, in order)
+ * All pointers device; child_* [R x F x Wc], n_valid [R x F], cost fp32, bin_batch int32 [n_bins]
+ * (ascending), outputs [R] and [R x wmax].  Limits: F x Wc <= DH_MAX_LEVEL_CHILDREN, wmax <= DH_MAX_K.
+ * No workspace.  Launched with programmatic dependent launch after an expansion on the same stream.
+ * R = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+#define DH_MAX_LEVEL_CHILDREN 8192
+int dh_size_level(const float* child_prob, const int32_t* child_token, const int32_t* n_valid, int R, int F, int Wc,
+                  const float* cost, const int32_t* bin_batch, int n_bins, int wmax, int batch, float theta,
+                  int32_t* width_out, int32_t* sel_parent, int32_t* sel_token, float* sel_prob, void* stream);
+
+/* ---------------------------------------------------------------------------------------------
  * Greedy draft-tree acceptance.
  *
  * daily.dev "EAGLE-4 speeds up LLM inference ...", section "How it works"; EAGLE-4 summary page,
@@ -204,6 +285,38 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
                    int vocab, int dtype, int32_t* argmax_out, int32_t* path_out, int32_t* len_out,
                    int32_t* bonus_out, int32_t* err_out, void* workspace, size_t ws_bytes,
                    void* stream);
+
+/* ---------------------------------------------------------------------------------------------
+ * Chain verification at positive temperature (speculative sampling).
+ *
+ * EAGLE-4 summary page, section "Distribution preservation has algorithmic and implementation
+ * conditions": at positive temperature the target verifies the drafted tokens and a rejection
+ * correction keeps the target's distribution; each round's depth is fixed before the round.  For a
+ * chain of L drafted tokens that is standard speculative sampling (Leviathan, Kalman and Matias
+ * 2023; Chen et al. 2023).  For request b, with target logit rows l_0..l_L (row i: the target's
+ * next-token logits after the prefix and the drafted x_0..x_{i-1}) and temperature T:
+ *   p_i(v)  = exp(l_i(v)/T - max) / sum_v' exp(l_i(v')/T - max)
+ *   q_i(v)  = sum of cand_prob[b,i,k] over the k with cand_idx[b,i,k] = v (0 for other ids)
+ *   token i is accepted when u_accept[b,i] < p_i(x_i) / q_i(x_i) (always when q_i(x_i) = 0)
+ *   n_accept[b] = n, the number of leading accepted tokens
+ *   token[b]    = the emitted token: n < L: a draw from max(0, p_n - q_n); n = L: a draw from p_L;
+ *                 drawn by inverse CDF in vocabulary order: the smallest v whose running sum of the
+ *                 weights exceeds u_sample[b] times their total (a zero total: the weights p_n)
+ * The uniforms are inputs, so a call is deterministic; decisions are taken in fp32, so where a
+ * uniform lies within rounding of its threshold the outcome may differ from exact arithmetic.
+ *
+ * logits [B x (L+1) x vocab]: device, `dtype` (finite values), 16-byte aligned rows.
+ * cand_idx int32, cand_prob fp32 [B x L x K]; draft_token int32, u_accept fp32 [B x L]; u_sample
+ * fp32 [B] (uniforms in [0, 1)): device; the L-sized inputs may be NULL when L = 0.
+ * n_accept_out, token_out int32 [B]: device.  0 <= L <= 64, K <= DH_MAX_K (K >= 1 when L > 0),
+ * temperature > 0 and finite.  Workspace: dh_verify_chain_workspace bytes (256-byte aligned; need
+ * not be zeroed).  B = 0 is a no-op.
+ * ------------------------------------------------------------------------------------------- */
+size_t dh_verify_chain_workspace(int B, int L, int vocab, int dtype);
+int dh_verify_chain(const void* logits, const int32_t* cand_idx, const float* cand_prob, const int32_t* draft_token,
+                    const float* u_accept, const float* u_sample, int B, int L, int vocab, int K, int dtype,
+                    float temperature, int32_t* n_accept_out, int32_t* token_out, void* workspace, size_t ws_bytes,
+                    void* stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Greedy draft-tree acceptance without a caller-provided workspace (no counterpart on the pages:
@@ -267,8 +380,10 @@ int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int
  *   "DH_FORCE_PATH"    "auto" | "gemv" | "mma" | "fused"  stage-1 path, when it supports the shape
  *   "DH_FORCE_HEAD"    "auto" | "split"                  dh_draft_head without the cluster head
  *   "DH_HEAD_CTAS"     "16" | "8" | "4"                  largest cluster of the fused head
- *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket"  stage-2 kernel
+ *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket" | "sweep"  stage-2 kernel
  *   "DH_SCORES_SMALL"  "lsu" | "tma"                     small-batch scores kernel
+ *   "DH_HEAD_SELECT"   "auto" | "radix"                  fused head: the cooperative radix selection
+ *                                                        instead of the group-best threshold
  * value NULL or "" restores the default.  Unknown names or values return DH_ERR_INVALID_ARG.  Not
  * synchronised with calls running on other host threads: set switches before such calls.
  * ------------------------------------------------------------------------------------------- */

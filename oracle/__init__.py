@@ -213,8 +213,9 @@ def verify_chain(logits, cand_idx, cand_prob, draft_token, u_accept, u_sample, t
     ll, dt = _raw(logits)
     B, L1, vocab = ll.shape
     L = L1 - 1
-    ci = np.ascontiguousarray(np.asarray(cand_idx, dtype=np.int32)).reshape(B, L, -1)
-    K = ci.shape[2]
+    ci = np.ascontiguousarray(np.asarray(cand_idx, dtype=np.int32))
+    K = ci.shape[2] if ci.ndim == 3 else 0
+    ci = ci.reshape(B, L, K)
     cp = np.ascontiguousarray(np.asarray(cand_prob, dtype=np.float32)).reshape(B, L, K)
     xt = np.ascontiguousarray(np.asarray(draft_token, dtype=np.int32)).reshape(B, L)
     ua = np.ascontiguousarray(np.asarray(u_accept, dtype=np.float32)).reshape(B, L)

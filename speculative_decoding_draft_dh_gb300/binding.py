@@ -25,7 +25,9 @@ EXPORTS = ["dh_status_string", "dh_version", "dh_last_error", "dh_lowrank_topk_w
            "dh_expand_children",
            "dh_tree_accept_workspace",
            "dh_tree_accept", "dh_tree_accept_noalloc", "dh_workspace_status", "dh_selftest_wait_timeout", "dh_prof_enable", "dh_prof_read",
-           "dh_set_tuning"]
+           "dh_set_tuning", "dh_verify_chain_workspace", "dh_verify_chain", "dh_size_level",
+           "dh_lowrank_topk_shard", "dh_merge_topk", "dh_exact_rescore_shard_workspace", "dh_exact_rescore_shard",
+           "dh_combine_softmax"]
 
 _lib = None
 _lock = threading.Lock()
@@ -82,6 +84,22 @@ def load_library(path: str | None = None):
         lib.dh_prof_enable.restype = I
         lib.dh_prof_read.argtypes = [P, I, P, P, I]
         lib.dh_prof_read.restype = I
+        lib.dh_verify_chain_workspace.argtypes = [I, I, I, I]
+        lib.dh_verify_chain_workspace.restype = Z
+        lib.dh_verify_chain.argtypes = [P, P, P, P, P, P, I, I, I, I, I, ctypes.c_float, P, P, P, Z, P]
+        lib.dh_verify_chain.restype = I
+        lib.dh_size_level.argtypes = [P, P, P, I, I, I, P, P, I, I, I, ctypes.c_float, P, P, P, P, P]
+        lib.dh_size_level.restype = I
+        lib.dh_lowrank_topk_shard.argtypes = [P, P, P, I, I, I, I, I, I, I, P, P, P, Z, P]
+        lib.dh_lowrank_topk_shard.restype = I
+        lib.dh_merge_topk.argtypes = [P, P, I, I, I, P, P, P]
+        lib.dh_merge_topk.restype = I
+        lib.dh_exact_rescore_shard_workspace.argtypes = [I, I, I, I, I]
+        lib.dh_exact_rescore_shard_workspace.restype = Z
+        lib.dh_exact_rescore_shard.argtypes = [P, P, P, I, I, I, I, I, I, P, P, P, Z, P]
+        lib.dh_exact_rescore_shard.restype = I
+        lib.dh_combine_softmax.argtypes = [P, P, I, I, I, P, P, P]
+        lib.dh_combine_softmax.restype = I
         lib.dh_set_tuning.argtypes = [ctypes.c_char_p, ctypes.c_char_p]
         lib.dh_set_tuning.restype = I
         if path is None:
@@ -265,6 +283,149 @@ def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stre
                               _ptr(out["bonus"]), _ptr(out["err"]), _ptr(ws), nbytes,
                               _stream(stream)), "dh_tree_accept")
     return out
+
+
+def lowrank_topk_shard(h, U, V_shard, K, vocab_offset, *, idx_out=None, score_out=None, workspace=None,
+                       stream=None):
+    """Stage 1 on one vocabulary shard (V_shard [r, n] holds the columns vocab_offset .. + n):
+    the shard's K best (global id, score) per row."""
+    lib = load_library()
+    _dev(h, "h"), _dev(U, "U"), _dev(V_shard, "V_shard")
+    B, d = h.shape
+    r, n = V_shard.shape
+    dt = _dtype_code(h)
+    if U.dtype != h.dtype or V_shard.dtype != h.dtype or U.shape != (d, r):
+        raise ValueError("h, U, V_shard must share a dtype and have shapes [B,d], [d,r], [r,n]")
+    if idx_out is None:
+        idx_out = torch.empty(B, K, dtype=torch.int32, device=h.device)
+    if score_out is None:
+        score_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    nbytes = lib.dh_lowrank_topk_workspace(B, d, r, n, K, dt)
+    ws = (workspace or _default_ws).get(nbytes, h.device, "topk")
+    _check(lib.dh_lowrank_topk_shard(_ptr(h), _ptr(U), _ptr(V_shard), B, d, r, n, int(vocab_offset), K, dt,
+                                     _ptr(idx_out), _ptr(score_out), _ptr(ws), nbytes, _stream(stream)),
+           "dh_lowrank_topk_shard")
+    return idx_out, score_out
+
+
+def merge_topk(idx_parts, score_parts, *, idx_out=None, score_out=None, stream=None):
+    """The K best of P shard lists per row (dh_merge_topk).  idx_parts int32 / score_parts fp32
+    [P, B, K]."""
+    lib = load_library()
+    _dev(idx_parts, "idx_parts"), _dev(score_parts, "score_parts")
+    P, B, K = idx_parts.shape
+    if idx_parts.dtype != torch.int32 or score_parts.dtype != torch.float32 or score_parts.shape != (P, B, K):
+        raise ValueError("idx_parts int32 and score_parts fp32 [P, B, K]")
+    dev = idx_parts.device
+    if idx_out is None:
+        idx_out = torch.empty(B, K, dtype=torch.int32, device=dev)
+    if score_out is None:
+        score_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    _check(lib.dh_merge_topk(_ptr(idx_parts), _ptr(score_parts), P, B, K, _ptr(idx_out), _ptr(score_out),
+                             _stream(stream)), "dh_merge_topk")
+    return idx_out, score_out
+
+
+def exact_rescore_shard(h, W_shard, idx, vocab_offset, *, logits_out=None, stats_out=None, workspace=None,
+                        stream=None):
+    """Stage 2 on one shard: logits of the candidates this shard owns (-inf elsewhere) and the row's
+    (max, sum of exp) pair [B, 2]."""
+    lib = load_library()
+    _dev(h, "h"), _dev(W_shard, "W_shard"), _dev(idx, "idx")
+    B, d = h.shape
+    n = W_shard.shape[0]
+    K = idx.shape[1]
+    dt = _dtype_code(h)
+    if W_shard.dtype != h.dtype or W_shard.shape[1] != d or idx.dtype != torch.int32 or idx.shape[0] != B:
+        raise ValueError("h [B,d], W_shard [n,d] share a dtype; idx is int32 [B,K]")
+    if logits_out is None:
+        logits_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
+    if stats_out is None:
+        stats_out = torch.empty(B, 2, dtype=torch.float32, device=h.device)
+    nbytes = lib.dh_exact_rescore_shard_workspace(B, d, n, K, dt)
+    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore_shard")
+    _check(lib.dh_exact_rescore_shard(_ptr(h), _ptr(W_shard), _ptr(idx), B, d, n, int(vocab_offset), K, dt,
+                                      _ptr(logits_out), _ptr(stats_out), _ptr(ws), nbytes, _stream(stream)),
+           "dh_exact_rescore_shard")
+    return logits_out, stats_out
+
+
+def combine_softmax(logits_parts, stats_parts, *, with_probs=True, logits_out=None, probs_out=None, stream=None):
+    """Each candidate's logit from its owner shard and the softmax over the K candidates
+    (dh_combine_softmax).  logits_parts [P, B, K], stats_parts [P, B, 2] fp32."""
+    lib = load_library()
+    _dev(logits_parts, "logits_parts"), _dev(stats_parts, "stats_parts")
+    P, B, K = logits_parts.shape
+    if logits_parts.dtype != torch.float32 or stats_parts.dtype != torch.float32 or stats_parts.shape != (P, B, 2):
+        raise ValueError("logits_parts [P, B, K] and stats_parts [P, B, 2], fp32")
+    dev = logits_parts.device
+    if logits_out is None:
+        logits_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    if with_probs and probs_out is None:
+        probs_out = torch.empty(B, K, dtype=torch.float32, device=dev)
+    _check(lib.dh_combine_softmax(_ptr(logits_parts), _ptr(stats_parts), P, B, K, _ptr(logits_out),
+                                  _ptr(probs_out if with_probs else None), _stream(stream)), "dh_combine_softmax")
+    return logits_out, (probs_out if with_probs else None)
+
+
+def size_level(child_prob, child_token, cost, bin_batch, batch, theta, *, n_valid=None, out=None, stream=None):
+    """Width and children of the next draft level per request (dh_size_level).  child_prob fp32 /
+    child_token int32 [R, F, Wc]; cost fp32 [n_bins, wmax+1] and bin_batch int32 [n_bins] on the
+    device.  Returns dict(width int32 [R], parent, token int32 [R, wmax], prob fp32 [R, wmax])."""
+    lib = load_library()
+    _dev(child_prob, "child_prob"), _dev(child_token, "child_token"), _dev(cost, "cost"), _dev(bin_batch, "bin_batch")
+    R, F, Wc = child_prob.shape
+    n_bins, w1 = cost.shape
+    wmax = w1 - 1
+    if child_prob.dtype != torch.float32 or child_token.dtype != torch.int32 or child_token.shape != (R, F, Wc) \
+            or cost.dtype != torch.float32 or bin_batch.dtype != torch.int32 or bin_batch.shape != (n_bins,):
+        raise ValueError("child_prob fp32 / child_token int32 [R,F,Wc], cost fp32 [n_bins,wmax+1], "
+                         "bin_batch int32 [n_bins]")
+    if n_valid is not None:
+        _dev(n_valid, "n_valid")
+    dev = child_prob.device
+    if out is None:
+        out = {"width": torch.empty(R, dtype=torch.int32, device=dev),
+               "parent": torch.empty(R, wmax, dtype=torch.int32, device=dev),
+               "token": torch.empty(R, wmax, dtype=torch.int32, device=dev),
+               "prob": torch.empty(R, wmax, dtype=torch.float32, device=dev)}
+    _check(lib.dh_size_level(_ptr(child_prob), _ptr(child_token), _ptr(n_valid), R, F, Wc, _ptr(cost), _ptr(bin_batch),
+                             n_bins, wmax, int(batch), float(theta), _ptr(out["width"]), _ptr(out["parent"]),
+                             _ptr(out["token"]), _ptr(out["prob"]), _stream(stream)), "dh_size_level")
+    return out
+
+
+def verify_chain(logits, cand_idx, cand_prob, draft_token, u_accept, u_sample, *, temperature=1.0,
+                 n_accept_out=None, token_out=None, workspace=None, stream=None):
+    """Speculative sampling over a chain of L drafted tokens per request (dh_verify_chain).
+    logits [B, L+1, vocab] (bf16 or fp32); cand_idx int32 / cand_prob fp32 [B, L, K]; draft_token
+    int32 / u_accept fp32 [B, L]; u_sample fp32 [B].  Returns (n_accept int32 [B], token int32 [B])."""
+    lib = load_library()
+    _dev(logits, "logits"), _dev(u_sample, "u_sample")
+    B, L1, vocab = logits.shape
+    L = L1 - 1
+    K = cand_idx.shape[2] if L > 0 else 0
+    for t, name, dt in ((cand_idx, "cand_idx", torch.int32), (cand_prob, "cand_prob", torch.float32),
+                        (draft_token, "draft_token", torch.int32), (u_accept, "u_accept", torch.float32)):
+        if L > 0:
+            _dev(t, name)
+            if t.dtype != dt:
+                raise ValueError(f"{name} must be {dt}")
+    if u_sample.dtype != torch.float32 or u_sample.shape != (B,):
+        raise ValueError("u_sample must be fp32 [B]")
+    dev = logits.device
+    if n_accept_out is None:
+        n_accept_out = torch.empty(B, dtype=torch.int32, device=dev)
+    if token_out is None:
+        token_out = torch.empty(B, dtype=torch.int32, device=dev)
+    dt = _dtype_code(logits)
+    nbytes = lib.dh_verify_chain_workspace(B, L, vocab, dt)
+    ws = (workspace or _default_ws).get(nbytes, dev, "verify")
+    _check(lib.dh_verify_chain(_ptr(logits), _ptr(cand_idx if L > 0 else None), _ptr(cand_prob if L > 0 else None),
+                               _ptr(draft_token if L > 0 else None), _ptr(u_accept if L > 0 else None),
+                               _ptr(u_sample), B, L, vocab, K, dt, float(temperature), _ptr(n_accept_out),
+                               _ptr(token_out), _ptr(ws), nbytes, _stream(stream)), "dh_verify_chain")
+    return n_accept_out, token_out
 
 
 def workspace_status(workspace: "Workspace | None" = None, device=None, stream=None) -> int:

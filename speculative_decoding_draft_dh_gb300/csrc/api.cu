@@ -27,7 +27,7 @@ bool row16(long long n, int dt) { return (n * elem_bytes(dt)) % 16 == 0; }
 // ---- workspace layouts (all offsets 256-byte aligned)
 
 struct TopkLayout {
-  size_t fix, t, partial, recs, total;
+  size_t fix, t, partial, recs, gkeys, total;
   int nsplit;
 };
 
@@ -50,6 +50,8 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
   off = align_up(off + partial_floats * 4, 256);
   L.recs = off;
   off = align_up(off + (size_t)B * n_groups * sizeof(GroupRec), 256);
+  L.gkeys = off;
+  off = align_up(off + (size_t)B * n_groups * sizeof(uint32_t), 256);
   L.total = off;
   return L;
 }
@@ -164,6 +166,7 @@ struct Stage1 {
   const void* t;
   unsigned long long* acc;
   GroupRec* recs;
+  const uint32_t* gkeys;  // the groups' best keys (small-batch path), else null
 };
 
 // Stage 1 up to the group records: projection and scores with group summaries.
@@ -173,13 +176,17 @@ int run_records(const Ctx& c, const void* h, const void* U, const void* V, int B
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
   out->recs = recs;
+  out->gkeys = nullptr;
   const Path path = choose_path(B, r, dtype);
   if (path == PATH_FUSED) {
     unsigned long long* acc = reinterpret_cast<unsigned long long*>(ws + L.fix);
-    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+    uint32_t* gkeys = reinterpret_cast<uint32_t*>(ws + L.gkeys);
+    if (launch_small_b(c, h, U, V, B, d, r, vocab, dtype, acc, recs, gkeys, reinterpret_cast<int*>(ws)) !=
+        cudaSuccess)
       return DH_ERR_CUDA;
     out->t = nullptr;
     out->acc = acc;
+    out->gkeys = gkeys;
     return DH_OK;
   }
   if (path == PATH_MMA && proj_mma_supported(B, d, r, dtype)) {
@@ -213,10 +220,17 @@ int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, i
 }
 
 // Stage 2 after validation: the ring kernel from 2048 pairs, the direct kernels below.  The
-// DH_FORCE_RESCORE switch (direct or ring) overrides the choice by batch size (tests and tuning).
+// DH_FORCE_RESCORE switch (direct, ring or sweep) overrides the choice by batch size (tests and
+// tuning); the vocabulary sweep runs only when asked for.
 int run_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
                 int dtype, float* logits_out, float* probs_out, uint32_t* tickets, int* status) {
   const Tuning::Rescore f = tuning().rescore;
+  const bool sweep = f == Tuning::RESCORE_SWEEP && rescore_sweep_supported(B, K, d, vocab, dtype, c.num_sms);
+  if (sweep)
+    return note_error(launch_rescore_sweep(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, status),
+                      "rescore (sweep)") == cudaSuccess
+               ? DH_OK
+               : DH_ERR_CUDA;
   const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
   bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
   if (f == Tuning::RESCORE_DIRECT || f == Tuning::RESCORE_TICKET) ring = false;
@@ -321,8 +335,9 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
   if (st != DH_OK) return st;
   if (ctas) {
-    if (note_error(launch_head_cluster(c, ctas, s1.recs, s1.acc, s1.t, V, h, W, B, d, r, vocab, K, dtype, idx_out,
-                                       score_out, logits_out, probs_out),
+    if (note_error(launch_head_cluster(c, ctas, s1.recs, tuning().head_select_radix ? nullptr : s1.gkeys, s1.acc,
+                                       s1.t, V, h, W, B, d, r, vocab, K, dtype, idx_out, score_out, logits_out,
+                                       probs_out),
                    "selection and rescoring (cluster)") != cudaSuccess)
       return DH_ERR_CUDA;
     return DH_OK;
@@ -345,6 +360,105 @@ int dh_expand_children(const float* probs, const int32_t* idx, const float* pare
   if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
   if (note_error(launch_expand(c, probs, idx, parent_prob, B, K, w, min_benefit, child_token, child_prob, n_keep),
                  "expand") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ vocabulary-sharded head
+
+int dh_lowrank_topk_shard(const void* h, const void* U, const void* V_shard, int B, int d, int r, int vocab_shard,
+                          int vocab_offset, int K, int dtype, int32_t* idx_out, float* score_out, void* workspace,
+                          size_t ws_bytes, void* stream) {
+  if (vocab_offset < 0 || (long long)vocab_offset + vocab_shard > DH_MAX_VOCAB) return DH_ERR_INVALID_ARG;
+  const int st = dh_lowrank_topk(h, U, V_shard, B, d, r, vocab_shard, K, dtype, idx_out, score_out, workspace,
+                                 ws_bytes, stream);
+  if (st != DH_OK || B == 0 || vocab_offset == 0) return st;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (note_error(launch_add_offset(c, idx_out, (long long)B * K, vocab_offset), "shard id offset") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+int dh_merge_topk(const int32_t* idx_parts, const float* score_parts, int P, int B, int K, int32_t* idx_out,
+                  float* score_out, void* stream) {
+  if (P < 1 || B < 0 || K < 1 || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if ((long long)P * K > DH_MAX_MERGE_ENTRIES) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!idx_parts || !score_parts || !idx_out || !score_out) return DH_ERR_INVALID_ARG;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (note_error(launch_merge_topk(c, idx_parts, score_parts, P, B, K, idx_out, score_out), "merge top-K") !=
+      cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+size_t dh_exact_rescore_shard_workspace(int B, int d, int vocab_shard, int K, int dtype) {
+  if (B <= 0 || K <= 0) return 0;
+  return align_up(dh_exact_rescore_workspace(B, d, vocab_shard, K, dtype), 256) +
+         align_up((size_t)B * K * sizeof(int32_t), 256);
+}
+
+int dh_exact_rescore_shard(const void* h, const void* W_shard, const int32_t* idx, int B, int d, int vocab_shard,
+                           int vocab_offset, int K, int dtype, float* logits_out, float* stats_out, void* workspace,
+                           size_t ws_bytes, void* stream) {
+  if (B < 0 || d <= 0 || vocab_shard <= 0 || K < 1 || K > DH_MAX_K || vocab_offset < 0) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!h || !W_shard || !idx || !logits_out || !stats_out) return DH_ERR_INVALID_ARG;
+  if (vocab_shard > DH_MAX_VOCAB) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(h) || !aligned16(W_shard) || !row16(d, dtype)) return DH_ERR_UNSUPPORTED;
+  if ((long long)B * K > 0x7FFFFFFFLL || !rescore_supported(d)) return DH_ERR_UNSUPPORTED;
+  const size_t rs = align_up(dh_exact_rescore_workspace(B, d, vocab_shard, K, dtype), 256);
+  if (!workspace || !aligned256(workspace) || ws_bytes < dh_exact_rescore_shard_workspace(B, d, vocab_shard, K, dtype))
+    return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  int32_t* local = reinterpret_cast<int32_t*>(ws + rs);
+  if (note_error(launch_localize(c, idx, (long long)B * K, vocab_offset, vocab_shard, local), "shard localize") !=
+      cudaSuccess)
+    return DH_ERR_CUDA;
+  // ids owned by another shard are -1 here: the rescoring leaves their logits NaN, unread rows
+  const int st = run_rescore(c, h, W_shard, local, B, d, vocab_shard, K, dtype, logits_out, nullptr,
+                             reinterpret_cast<uint32_t*>(ws + WS_HEADER), reinterpret_cast<int*>(ws));
+  if (st != DH_OK) return st;
+  if (note_error(launch_shard_stats(c, local, B, K, logits_out, stats_out), "shard softmax statistics") !=
+      cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+int dh_combine_softmax(const float* logits_parts, const float* stats_parts, int P, int B, int K, float* logits_out,
+                       float* probs_out, void* stream) {
+  if (P < 1 || B < 0 || K < 1 || K > DH_MAX_K) return DH_ERR_INVALID_ARG;
+  if (B == 0) return DH_OK;
+  if (!logits_parts || !stats_parts || !logits_out) return DH_ERR_INVALID_ARG;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (note_error(launch_combine_softmax(c, logits_parts, stats_parts, P, B, K, logits_out, probs_out),
+                 "combine softmax") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ sizing the next level
+
+int dh_size_level(const float* child_prob, const int32_t* child_token, const int32_t* n_valid, int R, int F, int Wc,
+                  const float* cost, const int32_t* bin_batch, int n_bins, int wmax, int batch, float theta,
+                  int32_t* width_out, int32_t* sel_parent, int32_t* sel_token, float* sel_prob, void* stream) {
+  if (R < 0 || F < 1 || Wc < 1 || n_bins < 1 || wmax < 1 || batch < 0) return DH_ERR_INVALID_ARG;
+  if (theta != theta) return DH_ERR_INVALID_ARG;
+  if ((long long)F * Wc > DH_MAX_LEVEL_CHILDREN || wmax > DH_MAX_K) return DH_ERR_UNSUPPORTED;
+  if (R == 0) return DH_OK;
+  if (!child_prob || !child_token || !cost || !bin_batch || !width_out || !sel_parent || !sel_token || !sel_prob)
+    return DH_ERR_INVALID_ARG;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  if (note_error(launch_size_level(c, child_prob, child_token, n_valid, R, F, Wc, cost, bin_batch, n_bins, wmax, batch,
+                                   theta, width_out, sel_parent, sel_token, sel_prob),
+                 "size level") != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }
@@ -373,6 +487,51 @@ int dh_tree_accept(const void* logits, const int32_t* parent, const int32_t* tok
   if (note_error(launch_tree(c, logits, parent, token, B, N, vocab, dtype, am_ws, argmax_out, path_out, len_out,
                              bonus_out, err_out),
                  "tree") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
+// ------------------------------------------------------------------ chain verification
+
+namespace {
+constexpr int kVerifyMaxL = 64;
+struct VerifyLayout {
+  size_t segs, total;
+};
+VerifyLayout verify_layout(int B, int L, int vocab, int dtype) {
+  VerifyLayout v;
+  const size_t nrow = (size_t)B * (L + 1);
+  v.segs = WS_HEADER;
+  v.total = align_up(v.segs + nrow * (size_t)verify_segments(vocab, dtype) * sizeof(float2), 256);
+  return v;
+}
+}  // namespace
+
+size_t dh_verify_chain_workspace(int B, int L, int vocab, int dtype) {
+  if (B <= 0 || L < 0 || L > kVerifyMaxL || vocab <= 0 || !valid_dtype(dtype)) return 0;
+  return verify_layout(B, L, vocab, dtype).total;
+}
+
+int dh_verify_chain(const void* logits, const int32_t* cand_idx, const float* cand_prob, const int32_t* draft_token,
+                    const float* u_accept, const float* u_sample, int B, int L, int vocab, int K, int dtype,
+                    float temperature, int32_t* n_accept_out, int32_t* token_out, void* workspace, size_t ws_bytes,
+                    void* stream) {
+  if (B < 0 || L < 0 || vocab <= 0 || K < 0 || K > DH_MAX_K || (L > 0 && K < 1)) return DH_ERR_INVALID_ARG;
+  if (!(temperature > 0.f) || !(temperature < INFINITY)) return DH_ERR_INVALID_ARG;
+  if (!valid_dtype(dtype)) return DH_ERR_UNSUPPORTED;
+  if (B == 0) return DH_OK;
+  if (!logits || !u_sample || !n_accept_out || !token_out) return DH_ERR_INVALID_ARG;
+  if (L > 0 && (!cand_idx || !cand_prob || !draft_token || !u_accept)) return DH_ERR_INVALID_ARG;
+  if (L > kVerifyMaxL || vocab > DH_MAX_VOCAB || (long long)B * (L + 1) > 0x7FFFFFFFLL) return DH_ERR_UNSUPPORTED;
+  if (!aligned16(logits) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
+  const VerifyLayout Lw = verify_layout(B, L, vocab, dtype);
+  if (!workspace || !aligned256(workspace) || ws_bytes < Lw.total) return DH_ERR_WORKSPACE;
+  Ctx c;
+  if (!get_ctx(stream, &c)) return DH_ERR_CUDA;
+  char* ws = static_cast<char*>(workspace);
+  if (note_error(launch_verify(c, logits, dtype, B, L, vocab, K, cand_idx, cand_prob, draft_token, u_accept, u_sample,
+                               temperature, n_accept_out, token_out, reinterpret_cast<float2*>(ws + Lw.segs)),
+                 "verify chain") != cudaSuccess)
     return DH_ERR_CUDA;
   return DH_OK;
 }

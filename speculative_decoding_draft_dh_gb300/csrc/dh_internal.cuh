@@ -180,12 +180,13 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 // dh_set_tuning.  They select kernels; results do not depend on them.
 struct Tuning {
   enum Path { PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_FUSED };
-  enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET };
+  enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET, RESCORE_SWEEP };
   Path force_path = PATH_AUTO;      // stage-1 path, when the forced one supports the shape
   bool head_split = false;          // dh_draft_head: the two calls' kernels, not the cluster head
   int head_ctas_max = 16;           // largest cluster of the fused head (16, 8 or 4)
   Rescore rescore = RESCORE_AUTO;   // stage-2 kernel choice
   bool scores_tma = false;          // small-batch scores: the TMA variant for every rank
+  bool head_select_radix = false;   // fused head: the cooperative radix selection, not the fast one
 };
 const Tuning& tuning();
 
@@ -215,8 +216,10 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
 // Small-batch stage 1: the projection leaves t in the fixed-point accumulators `acc` (ACC_COPIES
 // copies of B*r values, zero between calls); the scores kernel and the selection read t from there
 // and the selection clears them.
+// gkeys [B][n_groups]: each group's best score as an order-preserving key (0: empty group).
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, int* status);
+                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, uint32_t* gkeys,
+                           int* status);
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                GroupRec* recs, int* status);
 
@@ -236,22 +239,52 @@ bool head_cluster_supported(int B, int d, int vocab, int K, int dtype);
 int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype);
 // Fused selection and rescoring with clusters of `ctas` CTAs: t from the small-batch accumulators
 // (acc) or, with acc null, from t [B][r] in the activation dtype.
-cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, unsigned long long* acc,
-                                const void* t, const void* V, const void* h, const void* W, int B, int d, int r,
-                                int vocab, int K, int dtype, int32_t* idx_out, float* score_out, float* logits,
-                                float* probs);
+// gkeys: the groups' best keys from the small-batch scores kernel (the fast selection), or null.
+cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, const uint32_t* gkeys,
+                                unsigned long long* acc, const void* t, const void* V, const void* h, const void* W,
+                                int B, int d, int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out,
+                                float* logits, float* probs);
 
 cudaError_t launch_expand(const Ctx& c, const float* probs, const int32_t* idx, const float* parent_prob, int B,
                           int K, int w, float min_benefit, int32_t* child_token, float* child_prob,
                           int32_t* n_keep);
 
 bool rescore_supported(int d);
+// Large batches: the vocabulary-sweep rescoring (W rows shared by rows of the batch read once).
+bool rescore_sweep_supported(int B, int K, int d, int vocab, int dtype, int num_sms);
+cudaError_t launch_rescore_sweep(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
+                                 int vocab, int K, int dtype, float* logits, float* probs, int* status);
 bool rescore_ring_used(int B, int K, int d, int dtype);
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                 int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
                                 int* status);
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
                            int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
+
+// Vocabulary-sharded head (shard.cu).
+cudaError_t launch_add_offset(const Ctx& c, int32_t* idx, long long n, int offset);
+cudaError_t launch_merge_topk(const Ctx& c, const int32_t* idx_parts, const float* score_parts, int P, int B, int K,
+                              int32_t* idx_out, float* score_out);
+cudaError_t launch_localize(const Ctx& c, const int32_t* idx, long long n, int offset, int vocab_shard,
+                            int32_t* local);
+cudaError_t launch_shard_stats(const Ctx& c, const int32_t* local, int B, int K, float* logits, float* stats);
+cudaError_t launch_combine_softmax(const Ctx& c, const float* logits_parts, const float* stats_parts, int P, int B,
+                                   int K, float* logits_out, float* probs_out);
+
+// Sizing the next draft level (sizing.cu).
+size_t size_level_smem(int F, int Wc, int wmax);
+cudaError_t launch_size_level(const Ctx& c, const float* child_prob, const int32_t* child_token,
+                              const int32_t* n_valid, int R, int F, int Wc, const float* cost,
+                              const int32_t* bin_batch, int n_bins, int wmax, int batch, float theta,
+                              int32_t* width, int32_t* sel_parent, int32_t* sel_token, float* sel_prob);
+
+// Chain verification at positive temperature (verify.cu).  seg_stats: B*(L+1)*verify_segments(vocab,
+// dtype) float2.
+int verify_segments(int vocab, int dtype);
+cudaError_t launch_verify(const Ctx& c, const void* logits, int dtype, int B, int L, int vocab, int K,
+                          const int32_t* cand_idx, const float* cand_prob, const int32_t* draft, const float* u_accept,
+                          const float* u_sample, float temperature, int32_t* n_accept, int32_t* token,
+                          float2* seg_stats);
 
 cudaError_t launch_tree(const Ctx& c, const void* logits, const int32_t* parent, const int32_t* token,
                         int B, int N, int vocab, int dtype, int32_t* argmax_ws, int32_t* argmax_out,

@@ -69,6 +69,7 @@ struct HeadCtl {
 
 struct HeadParams {
   const GroupRec* recs;     // [B][n_groups]
+  const uint32_t* gkeys;    // [B][n_groups] the groups' best keys (fast selection), or null
   unsigned long long* acc;  // the small-batch projection's fixed-point accumulators (cleared here), or
   const void* t;            // t [B][r] in the activation dtype (tensor-core stage 1)
   const void* V;
@@ -135,6 +136,197 @@ __host__ __device__ constexpr size_t hc_fb_offset(int d, int elem) {
   return hc_h_offset() + align_up((size_t)d * elem, 128);
 }
 
+// Block-local state of the fast selection.
+struct FastShared {
+  uint32_t hist[HC_BINS];
+  uint32_t wsc[HC_WARPS], wmin[HC_WARPS], wmax[HC_WARPS];
+  uint32_t digit, run, bincount, total, nb, theta;
+  uint32_t bk[HC_RANK];  // the last level's bin
+};
+
+// Fast selection from the groups' best keys (written by the small-batch scores kernel).
+// theta = the K-th largest of the row's group bests; each CTA finds it alone (radix levels over
+// the keys' own range with block barriers, then ranking inside the last bin).  The K groups whose
+// bests reach theta put K pool entries at or above it, so the pool's K-th best is >= theta and
+// every entry of the pool's top K is >= theta: the entries >= theta (K to 2K of them on random
+// rows) are compacted into every CTA's list behind one cluster barrier and ranked there, which
+// also orders them.  Then the certificate, the exact logits of the winners (each CTA its share)
+// and one more cluster barrier; the leader computes the softmax.  Returns true when the row must
+// take the leader's exact selection instead: more than HC_BOUND entries reach theta, fewer than K
+// groups hold entries, or the certificate flags a group.  Every CTA takes the same decision at
+// the same barrier.
+template <typename T, int HC_CTAS, int HC_RPT, int HC_ENT>
+__device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group& cl, HeadCtl& my, HeadCtl& L,
+                                          FastShared& fs, const T* hs, int b, int g0, int g1,
+                                          const GroupRec (&rec)[HC_RPT], const uint32_t (&key)[HC_ENT],
+                                          const uint32_t (&id)[HC_ENT]) {
+  constexpr int GK = HC_MAX_GROUPS / HC_THREADS;  // group keys per thread
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = p.K, n_groups = p.n_groups;
+  const bool leader = cl.block_rank() == 0;
+  // every group's best key of the row (written by the previous kernel: read through L2)
+  const uint32_t* grow = p.gkeys + (size_t)b * n_groups;
+  uint32_t y[GK];
+  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+#pragma unroll
+  for (int q = 0; q < GK; ++q) {
+    const int g = (int)threadIdx.x + q * HC_THREADS;
+    y[q] = g < n_groups ? __ldcg(grow + g) : 0u;
+    if (y[q]) { kmin = min(kmin, y[q]); kmax = max(kmax, y[q]); }
+  }
+  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+  if (lane == 0) { fs.wmin[warp] = kmin; fs.wmax[warp] = kmax; }
+  fs.hist[threadIdx.x] = 0u;
+  if (threadIdx.x == 0) fs.nb = 0u;
+  __syncthreads();
+#pragma unroll
+  for (int w = 0; w < HC_WARPS; ++w) { kmin = min(kmin, fs.wmin[w]); kmax = max(kmax, fs.wmax[w]); }
+  // every CTA's control block is zeroed (the initial arrive) before the compaction writes into it
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  bool ok = kmax != 0u;
+  uint32_t theta = 0u;
+  if (ok) {
+#pragma unroll
+    for (int q = 0; q < GK; ++q) y[q] = y[q] ? y[q] - kmin + 1u : 0u;  // 0 = empty group
+    const uint32_t range = kmax - kmin + 1u;
+    int shift = range >= 0x80000000u ? 32 - HC_BITS : max(0, (32 - __clz((int)range)) - HC_BITS);
+    uint32_t prefix = 0u, mask = 0u, krem = (uint32_t)K, bc = 0u;
+    bool first = true;
+#pragma unroll 1
+    for (;;) {
+#pragma unroll
+      for (int q = 0; q < GK; ++q)
+        if (y[q] && (y[q] & mask) == prefix) atomicAdd(&fs.hist[(y[q] >> shift) & (HC_BINS - 1)], 1u);
+      __syncthreads();
+      const int bin = HC_BINS - 1 - (int)threadIdx.x;  // from the top
+      const uint32_t cnt = fs.hist[bin];
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (lane == 31) fs.wsc[warp] = incl;
+      __syncthreads();
+      uint32_t before = 0u;
+#pragma unroll
+      for (int w = 0; w < HC_WARPS; ++w) before += w < warp ? fs.wsc[w] : 0u;
+      incl += before;
+      if (incl - cnt < krem && krem <= incl) { fs.digit = (uint32_t)bin; fs.run = incl - cnt; fs.bincount = cnt; }
+      if (threadIdx.x == HC_THREADS - 1) fs.total = incl;
+      fs.hist[bin] = 0u;  // this thread's own bin, for the next level
+      __syncthreads();
+      if (first && fs.total < (uint32_t)K) { ok = false; break; }  // fewer nonempty groups than K
+      first = false;
+      prefix |= fs.digit << shift;
+      mask |= (uint32_t)(HC_BINS - 1) << shift;
+      krem -= fs.run;
+      bc = fs.bincount;
+      if (bc <= (uint32_t)HC_RANK || shift == 0) break;
+      shift = max(0, shift - HC_BITS);
+    }
+    if (ok) {
+      uint32_t ty = prefix;  // shift 0: every key of the last bin equals prefix
+      if (shift > 0) {
+        // the last bin holds at most HC_RANK keys: the krem-th largest of them by counting
+#pragma unroll
+        for (int q = 0; q < GK; ++q)
+          if (y[q] && (y[q] & mask) == prefix) fs.bk[atomicAdd(&fs.nb, 1u)] = y[q];
+        __syncthreads();
+        if (threadIdx.x < bc) {
+          const uint32_t yi = fs.bk[threadIdx.x];
+          uint32_t rank = 0u;
+          for (uint32_t j = 0; j < bc; ++j) {
+            const uint32_t yj = fs.bk[j];
+            rank += (yj > yi || (yj == yi && j < threadIdx.x)) ? 1u : 0u;
+          }
+          if (rank == krem - 1u) fs.theta = yi;
+        }
+        __syncthreads();
+        ty = fs.theta;
+      }
+      theta = ty - 1u + kmin;
+    }
+  }
+  // the pool entries at or above theta into every CTA's list (positions from warp ballots and one
+  // remote atomic per warp on the leader's counter); their W rows start towards L2 now
+  const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+  for (int q = 0; q < HC_ENT; ++q) {
+    const bool c = ok && key[q] && key[q] >= theta;
+    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
+    uint32_t base = 0u;
+    if (lane == 0 && bal) base = atomicAdd(&L.n_bound, (uint32_t)__popc(bal));
+    base = __shfl_sync(0xFFFFFFFFu, base, 0);
+    if (c) {
+      const uint32_t pos = base + (uint32_t)__popc(bal & below);
+      if (pos < (uint32_t)HC_BOUND) {
+        const unsigned long long e = pack(key[q], id[q]);
+#pragma unroll
+        for (int c2 = 0; c2 < HC_CTAS; ++c2) *cl.map_shared_rank(&my.bp[pos], (unsigned)c2) = e;
+      }
+      if (id[q] < (uint32_t)p.vocab)
+        prefetch_l2(static_cast<const T*>(p.W) + (size_t)id[q] * p.d, (uint32_t)(p.d * sizeof(T)));
+    }
+  }
+  cluster_sync_all();
+  const uint32_t n_cand = L.n_bound;  // the leader passes one more barrier below before it exits
+  if (!ok || n_cand > (uint32_t)HC_BOUND || n_cand < (uint32_t)K) return true;
+  // rank the candidates by counting: winner of rank k < K into sp[k] (every CTA, its own copy)
+  {
+    int P = 1;
+    while (P < 32 && (int)n_cand * (2 * P) <= HC_THREADS) P <<= 1;
+    for (int base = 0; base < (int)n_cand * P; base += HC_THREADS) {
+      const int t = base + (int)threadIdx.x;
+      const int i = t / P, hh = t % P;
+      unsigned long long pi;
+      const int rank = sel::rank_by_count(my.bp, (int)n_cand, P, i, hh, &pi);
+      if (i < (int)n_cand && hh == 0 && rank < K) my.sp[rank] = pi;
+    }
+  }
+  __syncthreads();
+  // certificate: a group whose third score reaches tau (the K-th best) may hide a top-K member
+  const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
+  bool flag = false;
+#pragma unroll
+  for (int q = 0; q < HC_RPT; ++q)
+    flag |= (g0 + (int)threadIdx.x + q * HC_THREADS) < g1 && fkey(rec[q].m3) >= tau;
+  const uint32_t fm = __ballot_sync(0xFFFFFFFFu, flag);
+  if (lane == 0 && fm)
+#pragma unroll
+    for (int c2 = 0; c2 < HC_CTAS; ++c2) atomicAdd(cl.map_shared_rank(&my.nref, (unsigned)c2), (uint32_t)__popc(fm));
+  // exact logits of this CTA's winners, written out and stored into the leader for the softmax
+  const int crank = (int)cl.block_rank();
+  float* zl = cl.map_shared_rank(&my.z[0], 0u);
+  for (int k = warp * HC_CTAS + crank; k < K; k += HC_CTAS * HC_WARPS) {
+    const unsigned long long e = my.sp[k];
+    const int v = (int)(~(uint32_t)e);
+    const bool okv = v >= 0 && v < p.vocab;
+    const float acc = okv ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
+    const float z = okv ? acc : __int_as_float(0x7FC00000);
+    if (lane == 0) {
+      p.idx_out[(size_t)b * K + k] = v;
+      p.score_out[(size_t)b * K + k] = fkey_inv((uint32_t)(e >> 32));
+      p.logits[(size_t)b * K + k] = z;
+      zl[k] = z;
+    }
+  }
+  cluster_sync_all();
+  if (my.nref != 0u) return true;
+  if (!leader) return false;
+  // the row's accumulators are cleared for the next call (select_row does it on the other branch)
+  if (p.acc) {
+    const int BR = p.B * p.r;
+    unsigned long long* acc_row = p.acc + (size_t)b * p.r;
+    for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
+#pragma unroll
+      for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+  }
+  if (p.probs && warp == 0) warp_softmax(my.z, K, p.probs + (size_t)b * K);
+  return false;
+}
+
 template <typename T, int HC_CTAS>
 __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   constexpr int HC_RPT = 16 / HC_CTAS;  // group records per thread
@@ -187,6 +379,12 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
       if (o2 != NO_OFFSET) { key[2 * q + 1] = fkey(rec[q].m2); id[2 * q + 1] = (uint32_t)g * GROUP + o2; }
     }
   }
+  bool fallback = false;
+  if (p.gkeys) {
+    __shared__ FastShared fs;
+    if (!head_fast<T, HC_CTAS, HC_RPT, HC_ENT>(p, cl, my, L, fs, hs, b, g0, g1, rec, key, id)) return;
+    fallback = true;
+  } else {
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int q = 0; q < HC_ENT; ++q)
@@ -208,7 +406,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   kmax = L.kmax;
 
   // ---------------------------------------------------------------- cooperative radix descent
-  bool fallback = kmax == 0u;  // empty pool
+  fallback = kmax == 0u;  // empty pool
   uint32_t prefix = 0, mask = 0, krem = (uint32_t)K, above = 0, bc = 0;
   if (!fallback) {
 #pragma unroll
@@ -381,6 +579,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
       return;
     }
   }
+  }  // the cooperative radix selection
   // the leader selects the row alone: exact, with refinement or a full rescan as needed
   if (leader)
     sel::select_row<T, HC_THREADS>(fb, rrow, t_row, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
@@ -511,13 +710,14 @@ bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
          d <= 8192 && smem <= 200 * 1024;
 }
 
-cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, unsigned long long* acc,
-                                const void* t, const void* V, const void* h, const void* W, int B, int d, int r,
-                                int vocab, int K, int dtype, int32_t* idx_out, float* score_out, float* logits,
-                                float* probs) {
+cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, const uint32_t* gkeys,
+                                unsigned long long* acc, const void* t, const void* V, const void* h, const void* W,
+                                int B, int d, int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out,
+                                float* logits, float* probs) {
   if (ctas != 4 && ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
   HeadParams p;
   p.recs = recs;
+  p.gkeys = gkeys;
   p.acc = acc;
   p.t = t;
   p.V = V;

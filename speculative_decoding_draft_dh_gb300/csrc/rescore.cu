@@ -1,3 +1,4 @@
+#include <algorithm>
 // Stage 2: exact full-rank logits of the retrieved candidates and their softmax.
 //
 // EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
@@ -421,6 +422,217 @@ cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* 
   return cudaGetLastError();
 }
 
+// Sweep variant for large batches: block j owns SW_ROWS batch rows, keeps their h rows in shared
+// memory, and orders its SW_ROWS x K (row, candidate) pairs by vocabulary bucket (ids >> SW_SHIFT,
+// a counting sort); a producer thread then streams the pairs' W rows through a ring of bulk-copy
+// slots in that order while the consumer warps take the slots in turn.  Every block walks the
+// vocabulary from low to high ids at the same pace, so a W row that several rows of the batch
+// share is requested by their blocks within a few buckets of each other: HBM delivers it once and
+// L2 serves the rest (the B x K candidates of a batch hold each distinct row about 1.5 times at
+// batch 512).  A block owns its rows' K logits, so it computes their softmax itself at the end.
+// Per-candidate dot products have the order of the other rescoring kernels (bit-identical logits).
+constexpr int SW_CONSUMERS = 16;
+constexpr int SW_THREADS = (SW_CONSUMERS + 1) * 32;
+// One slot per consumer warp: warp w takes items w, w + SW_SLOTS, ..., all in slot w, so the slot's
+// mbarrier phases advance one round per item of that warp.  (With fewer slots than consumers a warp
+// could wait for round r + 2 of a slot still in round r, and an mbarrier's parity cannot tell the
+// two apart; a fresh mbarrier also reports its odd phase complete, which a warp starting at round
+// 1 would take as data.)
+constexpr int SW_SLOTS = SW_CONSUMERS;
+static_assert(SW_SLOTS == SW_CONSUMERS, "each consumer warp owns one ring slot");
+constexpr int SW_ROWS_MAX = 4;
+constexpr int SW_SHIFT = 11;  // bucket = 2048 ids
+
+// Rows per block: enough that the grid fits the SMs in one wave (one block per SM).
+inline int sweep_rows(int B, int num_sms) { return std::min(SW_ROWS_MAX, std::max(1, (B + num_sms - 1) / num_sms)); }
+
+__host__ __device__ inline size_t sweep_smem(int rows, int d, int elem, int K, int n_buckets) {
+  return 128 + align_up((size_t)rows * d * elem, 128) + (size_t)SW_SLOTS * d * elem +
+         align_up((size_t)rows * K * 8, 16) + (size_t)n_buckets * 4;
+}
+
+template <typename T>
+__global__ void __launch_bounds__(SW_THREADS, 1)
+    k_rescore_sweep(const T* __restrict__ h, const T* __restrict__ W, const int32_t* __restrict__ idx, int B, int d,
+                    int vocab, int K, int rows, int n_buckets, float* __restrict__ logits, float* __restrict__ probs,
+                    int* __restrict__ status) {
+  using namespace sm100;
+  constexpr int PER = Elem<T>::PER16;
+  extern __shared__ unsigned char smem_raw[];
+  __shared__ uint64_t h_full, full[SW_SLOTS], empty[SW_SLOTS];
+  __shared__ int slot_pair[SW_SLOTS], slot_ok[SW_SLOTS];
+  __shared__ volatile int s_fail;
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
+                                                         ~static_cast<uintptr_t>(127));
+  const uint32_t row_bytes = (uint32_t)d * sizeof(T);
+  const int b0 = blockIdx.x * rows;
+  const int nrows = min(rows, B - b0);
+  const int n_pairs = nrows * K;
+  const T* hs = reinterpret_cast<const T*>(base);
+  unsigned char* ring = base + align_up((size_t)rows * row_bytes, 128);
+  int2* order = reinterpret_cast<int2*>(ring + (size_t)SW_SLOTS * row_bytes);  // (pair, id) by bucket
+  uint32_t* bucket = reinterpret_cast<uint32_t*>(reinterpret_cast<unsigned char*>(order) +
+                                                 align_up((size_t)rows * K * 8, 16));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    s_fail = 0;
+    mbar_init(&h_full, 1);
+    for (int s = 0; s < SW_SLOTS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    fence_barrier_init();
+    // the block's h rows do not depend on the previous kernel
+    mbar_arrive_expect_tx(&h_full, (uint32_t)nrows * row_bytes);
+    for (int r = 0; r < nrows; ++r) bulk_load(base + (size_t)r * row_bytes, h + (size_t)(b0 + r) * d, row_bytes, &h_full);
+  }
+  for (int z = threadIdx.x; z < n_buckets; z += SW_THREADS) bucket[z] = 0u;
+  __syncthreads();
+  asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
+  // counting sort of the pairs by bucket: counts, exclusive prefix (one warp), scatter
+  const int32_t* ib = idx + (size_t)b0 * K;
+  for (int q = threadIdx.x; q < n_pairs; q += SW_THREADS) {
+    const int v = ib[q];
+    atomicAdd(&bucket[(v >= 0 && v < vocab) ? (v >> SW_SHIFT) : 0], 1u);
+  }
+  __syncthreads();
+  if (warp == 0) {
+    uint32_t run = 0u;
+    for (int z0 = 0; z0 < n_buckets; z0 += 32) {
+      const int z = z0 + lane;
+      const uint32_t cnt = z < n_buckets ? bucket[z] : 0u;
+      uint32_t incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      if (z < n_buckets) bucket[z] = run + incl - cnt;
+      run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+    }
+  }
+  __syncthreads();
+  for (int q = threadIdx.x; q < n_pairs; q += SW_THREADS) {
+    const int v = ib[q];
+    order[atomicAdd(&bucket[(v >= 0 && v < vocab) ? (v >> SW_SHIFT) : 0], 1u)] = make_int2(q, v);
+  }
+  __syncthreads();
+  if (warp == SW_CONSUMERS) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int i = 0; i < n_pairs && !s_fail; ++i) {
+        const int s = i % SW_SLOTS;
+        if (!mbar_wait(&empty[s], ((uint32_t)(i / SW_SLOTS) & 1u) ^ 1u, RING_WAIT_NS)) {
+          s_fail = 1;
+          atomicOr(status, 1 << DH_ERR_TIMEOUT);
+          break;
+        }
+        const int2 qv = order[i];  // shared memory: the issue loop never waits on a global load
+        const int q = qv.x, v = qv.y;
+        const bool ok = v >= 0 && v < vocab;
+        slot_pair[s] = q;
+        slot_ok[s] = ok;
+        if (ok) {
+          mbar_arrive_expect_tx(&full[s], row_bytes);
+          bulk_load(ring + (size_t)s * row_bytes, W + (size_t)v * d, row_bytes, &full[s]);
+        } else {
+          mbar_arrive(&full[s]);
+        }
+      }
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ consumers
+    const bool h_ok = __all_sync(0xFFFFFFFFu, mbar_wait(&h_full, 0, RING_WAIT_NS));
+    if (!h_ok) {
+      if (lane == 0) atomicOr(status, 1 << DH_ERR_TIMEOUT);
+      s_fail = 1;
+    }
+    for (int i = warp; h_ok && i < n_pairs; i += SW_CONSUMERS) {
+      const int s = i % SW_SLOTS;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (uint32_t)(i / SW_SLOTS) & 1u, RING_WAIT_NS))) {
+        if (lane == 0) atomicOr(status, 1 << DH_ERR_TIMEOUT);
+        s_fail = 1;
+        break;
+      }
+      const int q = slot_pair[s];
+      const bool ok = slot_ok[s] != 0;
+      const T* hr = hs + (size_t)(q / K) * d;
+      float acc = 0.f;
+      if (ok) {
+        const T* wr = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
+        for (int c = lane * PER; c < d; c += 32 * PER) {
+          float wf[PER], xf[PER];
+          Elem<T>::unpack(*reinterpret_cast<const uint4*>(wr + c), wf);
+          Elem<T>::unpack(*reinterpret_cast<const uint4*>(hr + c), xf);
+#pragma unroll
+          for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+      __syncwarp();
+      if (lane == 0) {
+        logits[(size_t)b0 * K + q] = ok ? acc : __int_as_float(0x7FC00000);
+        mbar_arrive(&empty[s]);  // the slot is free once the warp has read it
+      }
+    }
+  }
+  __syncthreads();
+  if (s_fail) {
+    // let every copy issued into this block's shared memory land before it exits
+    if (threadIdx.x == 0) {
+      mbar_wait(&h_full, 0, RING_WAIT_NS);
+      for (int s = 0; s < SW_SLOTS && s < n_pairs; ++s) {
+        const int last = s + ((n_pairs - 1 - s) / SW_SLOTS) * SW_SLOTS;
+        mbar_wait(&full[s], (uint32_t)(last / SW_SLOTS) & 1u, RING_WAIT_NS);
+      }
+    }
+    __syncthreads();
+    return;
+  }
+  // the softmax of each owned row, one warp per row (the logits were written by this block)
+  if (probs && warp < nrows) {
+    const float* z = logits + (size_t)(b0 + warp) * K;
+    float m = -INFINITY;
+    for (int i = lane; i < K; i += 32) m = fmaxf(m, __ldcg(z + i));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    float ssum = 0.f;
+    for (int i = lane; i < K; i += 32) ssum += expf(__ldcg(z + i) - m);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
+    const float inv = 1.f / ssum;
+    for (int i = lane; i < K; i += 32) probs[(size_t)(b0 + warp) * K + i] = expf(__ldcg(z + i) - m) * inv;
+  }
+}
+
+template <typename T>
+cudaError_t run_sweep(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                      float* logits, float* probs, int* status) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_rescore_sweep<T>, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  const int rows = sweep_rows(B, c.num_sms);
+  const int n_buckets = ((vocab - 1) >> SW_SHIFT) + 1;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)((B + rows - 1) / rows));
+  cfg.blockDim = dim3(SW_THREADS);
+  cfg.dynamicSmemBytes = sweep_smem(rows, d, (int)sizeof(T), K, n_buckets);
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_before("rescore_sweep", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_rescore_sweep<T>, static_cast<const T*>(h), static_cast<const T*>(W), idx, B, d,
+                         vocab, K, rows, n_buckets, logits, probs, status);
+  prof_after(c.stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab,
                 int K, float* logits, float* probs, uint32_t* tickets) {
@@ -462,6 +674,18 @@ bool rescore_supported(int d) { return d <= MAX_D_SMEM; }
 // The ring variant from this many (row, candidate) pairs on: below it, one warp per pair with all
 // of a row's loads in flight has the lower latency.
 // (It needs RING_SLOTS + 1 rows of shared memory: up to d = 11264 bf16 or 5632 fp32.)
+bool rescore_sweep_supported(int B, int K, int d, int vocab, int dtype, int num_sms) {
+  const int elem = dtype == DH_BF16 ? 2 : 4;
+  const int rows = sweep_rows(B, num_sms);
+  return sweep_smem(rows, d, elem, K, ((vocab - 1) >> SW_SHIFT) + 1) <= 220 * 1024;
+}
+
+cudaError_t launch_rescore_sweep(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
+                                 int vocab, int K, int dtype, float* logits, float* probs, int* status) {
+  if (dtype == DH_BF16) return run_sweep<__nv_bfloat16>(c, h, W, idx, B, d, vocab, K, logits, probs, status);
+  return run_sweep<float>(c, h, W, idx, B, d, vocab, K, logits, probs, status);
+}
+
 bool rescore_ring_used(int B, int K, int d, int dtype) {
   const size_t row = (size_t)d * (dtype == DH_BF16 ? 2 : 4);
   return (long long)B * K >= 2048 && (RING_SLOTS + 1) * row + 256 <= 200 * 1024;

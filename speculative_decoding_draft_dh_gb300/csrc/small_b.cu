@@ -157,10 +157,84 @@ __global__ void __launch_bounds__(PJ_THREADS) k_proj_small(ProjSmall p) {
   if (!triggered) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Vector form of the projection (r / (16 / sizeof(T)) a power of two up to PV_THREADS): one light
+// block of PV_THREADS threads per SM, so that every block of the scores kernel fits beside it
+// and issues its V loads as soon as it is launched.  Block c owns a slice of d; thread t loads one
+// 16-byte vector (VEC columns) of row (t / tpr) of each pass of rpp rows, all passes in flight at
+// once; the rpp row groups' partials are added in a fixed order in shared memory and each (b, j)
+// is added once into the fixed-point accumulators.
+constexpr int PV_THREADS = 128;
+constexpr int PV_LOADS = 8;  // 16-byte loads per thread in flight
+
+bool proj_vec_ok(int r, int elem) {
+  const int tpr = r * elem / 16;
+  return r * elem % 16 == 0 && tpr >= 1 && tpr <= PV_THREADS && (tpr & (tpr - 1)) == 0;
+}
+
+template <typename T, int NB>
+__global__ void __launch_bounds__(PV_THREADS) k_proj_vec(ProjSmall p) {
+  constexpr int VEC = Elem<T>::PER16;
+  extern __shared__ float pv_red[];  // [rpp][NB * r]
+  const T* h = static_cast<const T*>(p.h);
+  const T* U = static_cast<const T*>(p.U);
+  const int r = p.r, BR = p.B * r;
+  const int tpr = r / VEC, rpp = PV_THREADS / tpr;
+  const int G = gridDim.x, c = blockIdx.x;
+  const int i0 = (int)((long long)p.d * c / G), i1 = (int)((long long)p.d * (c + 1) / G);
+  const int grp = threadIdx.x / tpr, col = (threadIdx.x % tpr) * VEC;
+  float acc[NB][VEC];
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[b][e] = 0.f;
+  // launched with programmatic dependent launch: h may come from the kernel before this one
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  bool triggered = false;
+  for (int base = i0; base < i1; base += PV_LOADS * rpp) {
+    uint4 u[PV_LOADS];
+#pragma unroll
+    for (int q = 0; q < PV_LOADS; ++q) {
+      const int row = base + q * rpp + grp;
+      u[q] = row < i1 ? __ldg(reinterpret_cast<const uint4*>(U + (size_t)row * r + col)) : make_uint4(0, 0, 0, 0);
+    }
+    if (!triggered) {  // U is in flight: the scores kernel may launch and start streaming V
+      asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+      triggered = true;
+    }
+#pragma unroll
+    for (int q = 0; q < PV_LOADS; ++q) {
+      const int row = base + q * rpp + grp;
+      if (row < i1) {
+        float x[VEC];
+        Elem<T>::unpack(u[q], x);
+#pragma unroll
+        for (int b = 0; b < NB; ++b) {
+          const float hv = Elem<T>::to_f(h[(size_t)b * p.d + row]);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[b][e] = fmaf(hv, x[e], acc[b][e]);
+        }
+      }
+    }
+  }
+  if (!triggered) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) pv_red[(size_t)grp * BR + b * r + col + e] = acc[b][e];
+  __syncthreads();
+  for (int q = threadIdx.x; q < BR; q += PV_THREADS) {
+    float v = 0.f;
+    for (int g = 0; g < rpp; ++g) v += pv_red[(size_t)g * BR + q];
+    if (!(fabsf(v) < FIX_LIMIT)) atomicOr(p.status, 1 << DH_ERR_UNSUPPORTED);
+    atomicAdd(p.acc + (size_t)(c % ACC_COPIES) * BR + q, (unsigned long long)__float2ll_rn(v * FIX_SCALE));
+  }
+}
+
 struct ScoresSmall {
   const unsigned long long* acc;  // the projection's accumulators: t = acc_to_t(acc, B*r, e)
   int B, r, vocab, n_groups, n_tiles;
   GroupRec* recs;
+  uint32_t* gkeys;  // [B][n_groups]: order-preserving key of each group's best score (0: empty group)
   int* status;
 };
 
@@ -273,7 +347,10 @@ __global__ void __launch_bounds__(SB_THREADS, 1)
             if ((int)id0 + 1 < p.vocab) sm.push(acc[b][1], id0 + 1);
 #pragma unroll
             for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
-            if (lane == 0 && g < p.n_groups) p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
+            if (lane == 0 && g < p.n_groups) {
+              p.recs[(size_t)b * p.n_groups + g] = sm.record((uint32_t)(g * GROUP));
+              p.gkeys[(size_t)b * p.n_groups + g] = sm.i1 == 0xFFFFFFFFu ? 0u : fkey(sm.v1);
+            }
           }
         }
 #pragma unroll
@@ -433,7 +510,10 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
       if ((int)id0 + 1 < p.vocab) sm.push(s1, id0 + 1);
 #pragma unroll
       for (int x = 1; x < 32; x <<= 1) sm.merge_shfl(0xFFFFFFFFu, x);
-      if (lane == 0 && gg < p.n_groups && write) p.recs[(size_t)b * p.n_groups + gg] = sm.record((uint32_t)gg * GROUP);
+      if (lane == 0 && gg < p.n_groups && write) {
+        p.recs[(size_t)b * p.n_groups + gg] = sm.record((uint32_t)gg * GROUP);
+        p.gkeys[(size_t)b * p.n_groups + gg] = sm.i1 == 0xFFFFFFFFu ? 0u : fkey(sm.v1);
+      }
     }
   }
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -449,7 +529,7 @@ cudaError_t launch_tma(const Ctx& c, cudaLaunchConfig_t& cfg, const CUtensorMap&
 
 template <typename T>
 cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
-                unsigned long long* acc, GroupRec* recs, int* status) {
+                unsigned long long* acc, GroupRec* recs, uint32_t* gkeys, int* status) {
   constexpr int RB = STAGE_BYTES / (SET_TILES * TILE * (int)sizeof(T));
   cudaError_t e = cudaSuccess;
   cudaLaunchAttribute attr[1];
@@ -465,19 +545,33 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   pp.acc = acc;
   pp.status = status;
   cudaLaunchConfig_t cfg = {};
-  // three blocks per SM: more row slices keep more of U in flight (batch 1, µs per call: 21.5 with
-  // one block per SM, 19.4 with two, 19.05 with three, 19.2 with four)
-  cfg.gridDim = dim3((unsigned)max(1, min(3 * c.num_sms, d / 4)));
-  cfg.blockDim = dim3(PJ_THREADS);
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   prof_before("proj_small", c.stream);
-  switch (B) {
+  if (proj_vec_ok(r, (int)sizeof(T))) {
+    // one block per SM: room for four blocks of the scores kernel beside it
+    const int rpp = PV_THREADS / (r / Elem<T>::PER16);
+    cfg.gridDim = dim3((unsigned)max(1, min(c.num_sms, d / rpp)));
+    cfg.blockDim = dim3(PV_THREADS);
+    cfg.dynamicSmemBytes = (size_t)rpp * B * r * sizeof(float);
+    switch (B) {
+#define DH_PV_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_proj_vec<T, n>, pp); break;
+      DH_PV_CASE(1) DH_PV_CASE(2) DH_PV_CASE(3) DH_PV_CASE(4) DH_PV_CASE(5) DH_PV_CASE(6) DH_PV_CASE(7) DH_PV_CASE(8)
+#undef DH_PV_CASE
+      default: e = cudaErrorInvalidValue;
+    }
+  } else {
+    // three blocks per SM: more row slices keep more of U in flight (batch 1, µs per call: 21.5
+    // with one block per SM, 19.4 with two, 19.05 with three, 19.2 with four)
+    cfg.gridDim = dim3((unsigned)max(1, min(3 * c.num_sms, d / 4)));
+    cfg.blockDim = dim3(PJ_THREADS);
+    switch (B) {
 #define DH_PJ_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_proj_small<T, n>, pp); break;
-    DH_PJ_CASE(1) DH_PJ_CASE(2) DH_PJ_CASE(3) DH_PJ_CASE(4) DH_PJ_CASE(5) DH_PJ_CASE(6) DH_PJ_CASE(7) DH_PJ_CASE(8)
+      DH_PJ_CASE(1) DH_PJ_CASE(2) DH_PJ_CASE(3) DH_PJ_CASE(4) DH_PJ_CASE(5) DH_PJ_CASE(6) DH_PJ_CASE(7) DH_PJ_CASE(8)
 #undef DH_PJ_CASE
-    default: e = cudaErrorInvalidValue;
+      default: e = cudaErrorInvalidValue;
+    }
   }
   prof_after(c.stream);
   if (e != cudaSuccess) return note_error(e, "cudaLaunchKernelEx(k_proj_small)");
@@ -490,6 +584,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   sp.n_groups = (vocab + GROUP - 1) / GROUP;
   sp.n_tiles = (vocab + TILE - 1) / TILE;
   sp.recs = recs;
+  sp.gkeys = gkeys;
   sp.status = status;
   const bool lsu = r % (LSU_WARPS * 16) == 0 && !tuning().scores_tma;
   if (lsu) {
@@ -545,9 +640,10 @@ bool small_b_supported(int B, int r, int dtype) {
 }
 
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
-                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, int* status) {
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, U, V, B, d, r, vocab, acc, recs, status);
-  return run<float>(c, h, U, V, B, d, r, vocab, acc, recs, status);
+                           int vocab, int dtype, unsigned long long* acc, GroupRec* recs, uint32_t* gkeys,
+                           int* status) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, h, U, V, B, d, r, vocab, acc, recs, gkeys, status);
+  return run<float>(c, h, U, V, B, d, r, vocab, acc, recs, gkeys, status);
 }
 
 }  // namespace dh

@@ -3,7 +3,7 @@
 // the GPU tests.
 //
 // The switches are read from the environment once per process, on first use (DH_FORCE_PATH,
-// DH_FORCE_HEAD, DH_HEAD_CTAS, DH_FORCE_RESCORE, DH_SCORES_SMALL), and can be changed afterwards
+// DH_FORCE_HEAD, DH_HEAD_CTAS, DH_FORCE_RESCORE, DH_SCORES_SMALL, DH_HEAD_SELECT), and can be changed afterwards
 // only through dh_set_tuning, so a process's kernel choice never changes behind its back.
 #include <cstdlib>
 #include <cstring>
@@ -49,6 +49,13 @@ bool apply(Tuning& t, const char* name, const char* value) {
     else if (is("direct")) t.rescore = Tuning::RESCORE_DIRECT;
     else if (is("ring")) t.rescore = Tuning::RESCORE_RING;
     else if (is("ticket")) t.rescore = Tuning::RESCORE_TICKET;
+    else if (is("sweep")) t.rescore = Tuning::RESCORE_SWEEP;
+    else return false;
+    return true;
+  }
+  if (std::strcmp(name, "DH_HEAD_SELECT") == 0) {
+    if (dflt || is("auto") || is("fast")) t.head_select_radix = false;
+    else if (is("radix")) t.head_select_radix = true;
     else return false;
     return true;
   }
@@ -62,7 +69,8 @@ bool apply(Tuning& t, const char* name, const char* value) {
 }
 
 void init_from_env() {
-  for (const char* n : {"DH_FORCE_PATH", "DH_FORCE_HEAD", "DH_HEAD_CTAS", "DH_FORCE_RESCORE", "DH_SCORES_SMALL"}) {
+  for (const char* n :
+       {"DH_FORCE_PATH", "DH_FORCE_HEAD", "DH_HEAD_CTAS", "DH_FORCE_RESCORE", "DH_SCORES_SMALL", "DH_HEAD_SELECT"}) {
     Tuning t = g_tuning;
     if (apply(t, n, std::getenv(n))) g_tuning = t;  // an unknown value keeps the default
   }

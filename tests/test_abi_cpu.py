@@ -132,3 +132,47 @@ def test_expand_rejects_bad_arguments_on_host(lib):
 def test_binding_fails_loudly_without_library(tmp_path):
     with pytest.raises(RuntimeError, match="libdh.so not found"):
         binding.load_library(str(tmp_path / "libdh.so"))
+
+
+def test_verify_chain_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = ctypes.c_float
+
+    def call(B=4, L=3, vocab=4096, K=16, dt=binding.F32, T=1.0, logits=FAKE, cand=FAKE, ws=FAKE * 16,
+             nbytes=1 << 30):
+        return lib.dh_verify_chain(P(logits), P(cand) if cand else None, P(FAKE), P(FAKE), P(FAKE), P(FAKE), B, L,
+                                   vocab, K, dt, f(T), P(FAKE), P(FAKE), P(ws) if ws else None, nbytes, None)
+    assert call(T=0.0) == 1
+    assert call(T=float("inf")) == 1
+    assert call(T=float("nan")) == 1
+    assert call(K=0) == 1                    # candidates needed when L > 0
+    assert call(K=2048) == 1
+    assert call(cand=0) == 1
+    assert call(dt=5) == 2
+    assert call(L=65) == 2                   # deeper than a round may be
+    assert call(vocab=4095) == 2             # fp32 row not a multiple of 16 bytes
+    assert call(logits=FAKE + 4) == 2        # misaligned
+    assert call(nbytes=64) == 3
+    assert call(B=0) == 0
+    need = lib.dh_verify_chain_workspace(64, 7, 151936, binding.BF16)
+    assert need >= 64 * 8 * (151936 // 1024) * 8 and need % 256 == 0  # one (max, sum) pair per 1024 ids
+    assert lib.dh_verify_chain_workspace(4, 65, 4096, binding.F32) == 0
+
+
+def test_size_level_rejects_bad_arguments_on_host(lib):
+    P = ctypes.c_void_p
+    f = ctypes.c_float
+
+    def call(R=2, F=4, Wc=4, n_bins=2, wmax=8, batch=1, theta=0.01, prob=FAKE, out=FAKE):
+        return lib.dh_size_level(P(prob) if prob else None, P(FAKE), None, R, F, Wc, P(FAKE), P(FAKE), n_bins, wmax,
+                                 batch, f(theta), P(out) if out else None, P(FAKE), P(FAKE), P(FAKE), None)
+    assert call(F=0) == 1
+    assert call(n_bins=0) == 1
+    assert call(wmax=0) == 1
+    assert call(batch=-1) == 1
+    assert call(theta=float("nan")) == 1
+    assert call(prob=0) == 1
+    assert call(out=0) == 1
+    assert call(F=4096, Wc=4) == 2           # more children than one block ranks
+    assert call(wmax=2048) == 2
+    assert call(R=0) == 0

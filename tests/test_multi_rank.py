@@ -51,27 +51,42 @@ def _bench_worker(rank, world, port, q):
 
 
 def _shard_worker(rank, world, port, q):
+    """One rank of the vocabulary-sharded head on the CPU: its shard's candidates and owned logits
+    from the oracle, exchanged with the package's own all-gather (sharded.all_gather_parts, gloo),
+    merged and combined here as the library's merge and softmax kernels do."""
     import sys
     sys.path.insert(0, ROOT)
     import oracle
-    from speculative_decoding_draft_dh_gb300 import inputs
+    from speculative_decoding_draft_dh_gb300 import inputs, sharded
     _init(rank, world, port)
     try:
         cfg = inputs.head_config("tiny", B=3, K=16)
-        x = inputs.make_head(cfg, seed=21, with_W=False)
-        lo = cfg.vocab * rank // world
-        hi = cfg.vocab * (rank + 1) // world
-        idx, sc = oracle.lowrank_topk(x["h"], x["U"], x["V"][:, lo:hi].contiguous(), cfg.K)
-        mine = torch.from_numpy(np.stack([sc, (idx + lo).astype(np.float64)], axis=-1))
-        gathered = [torch.empty_like(mine) for _ in range(world)]
-        dist.all_gather(gathered, mine)
-        union = torch.cat(gathered, dim=1).numpy()  # [B, world*K, 2]
+        x = inputs.make_head(cfg, seed=21)
+        lo, n = sharded.shard_bounds(cfg.vocab, world, align=4)[rank]
+        idx, sc = oracle.lowrank_topk(x["h"], x["U"], x["V"][:, lo:lo + n].contiguous(), cfg.K)
+        ids = torch.from_numpy((idx + lo).astype(np.int32))
+        scores = torch.from_numpy(sc.astype(np.float32))
+        all_ids = sharded.all_gather_parts(ids).numpy()        # [P, B, K]
+        all_sc = sharded.all_gather_parts(scores).numpy()
         merged = []
         for b in range(cfg.B):
-            s, ids = union[b, :, 0], union[b, :, 1].astype(np.int64)
-            order = np.lexsort((ids, -s))[: cfg.K]
-            merged.append(ids[order])
-        q.put((rank, np.stack(merged)))
+            s_, i_ = all_sc[:, b].ravel(), all_ids[:, b].ravel().astype(np.int64)
+            merged.append(i_[np.lexsort((i_, -s_))[: cfg.K]])
+        merged = np.stack(merged).astype(np.int32)
+        # owner-only logits, the shard's (max, sum of exp), exchanged and combined
+        z, _ = oracle.exact_rescore(x["h"], x["W"], merged)
+        own = (merged >= lo) & (merged < lo + n)
+        zl = np.where(own, z, -np.inf)
+        m = zl.max(axis=1)
+        ssum = np.where(np.isfinite(m), np.exp(zl - np.where(np.isfinite(m), m, 0)[:, None]).sum(axis=1), 0.0)
+        parts_z = sharded.all_gather_parts(torch.from_numpy(zl)).numpy()
+        parts_st = sharded.all_gather_parts(torch.from_numpy(np.stack([m, ssum], axis=1))).numpy()
+        logits = parts_z.max(axis=0)
+        M = parts_st[:, :, 0].max(axis=0)
+        S = sum(np.where(np.isfinite(parts_st[p, :, 0]), parts_st[p, :, 1] * np.exp(parts_st[p, :, 0] - M), 0.0)
+                for p in range(world))
+        probs = np.exp(logits - M[:, None]) / S[:, None]
+        q.put((rank, merged, logits, probs))
     finally:
         dist.destroy_process_group()
 
@@ -147,15 +162,22 @@ def test_replicas_take_the_slowest_rank_and_scale_weakly():
         assert value == pytest.approx(64 * 100 * 2 / 0.015)
 
 
-def test_vocab_sharded_merge_equals_unsharded_topk():
+@pytest.mark.parametrize("world", [2, 3])
+def test_vocab_sharded_step_equals_unsharded(world):
+    """The sharded head's exchange path (all-gather of the candidate lists, merge; all-gather of
+    owned logits and (max, sum) pairs, combination) gives the unsharded oracle's candidates,
+    logits and probabilities on every rank."""
     import oracle
     from speculative_decoding_draft_dh_gb300 import inputs
-    out = _run(_shard_worker)
+    out = _run(_shard_worker, world=world)
     cfg = inputs.head_config("tiny", B=3, K=16)
-    x = inputs.make_head(cfg, seed=21, with_W=False)
+    x = inputs.make_head(cfg, seed=21)
     idx, _ = oracle.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
-    for _, merged in out:
+    z, p = oracle.exact_rescore(x["h"], x["W"], idx)
+    for _, merged, logits, probs in out:
         np.testing.assert_array_equal(merged, idx)
+        np.testing.assert_array_equal(logits, z)
+        np.testing.assert_allclose(probs, p, rtol=1e-12, atol=1e-15)
 
 
 def test_vocab_sharded_tree_argmax_equals_unsharded():

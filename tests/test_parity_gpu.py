@@ -143,6 +143,22 @@ def test_many_clustered_groups_use_full_rescan(api):
     run_head(x, cfg.K, api=api)
 
 
+def test_fast_selection_overflow_takes_the_exact_path():
+    """Every group's two best scores tie with the K-th group best (identical V columns), so far more
+    than the candidate list's capacity reach the threshold: the fused head falls back to the
+    leader's exact selection, and still equals the two calls and the oracle (ties to the lowest id)."""
+    cfg = inputs.head_config("batch1", B=1, d=512, vocab=65536, r=128, K=64)
+    x = inputs.make_head(cfg, seed=9, device=DEV)
+    x["V"][:, 1:] = x["V"][:, :1]
+    idx, score, logits, probs = run_head(x, cfg.K, api="head")
+    i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    l2, p2 = dh.exact_rescore(x["h"], x["W"], i2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, i2) and torch.equal(score, s2)
+    assert torch.equal(logits, l2) and torch.equal(probs, p2)
+    assert idx[0].tolist() == list(range(cfg.K))
+
+
 @pytest.mark.parametrize("api", ["split", "head"])
 def test_equal_scores_resolve_to_lowest_id(api):
     cfg = inputs.head_config("tiny", B=1, K=16)
@@ -179,7 +195,7 @@ def test_rescore_bad_index_gives_nan_row():
     assert np.isfinite(lg[0]).all() and np.isfinite(pr[0]).all()
 
 
-@pytest.mark.parametrize("path", ["direct", "ring", "ticket"])
+@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep"])
 def test_rescore_paths_small_shapes(path, tune):
     """Each stage-2 kernel (direct = the cluster kernel for K <= 128) on fp32 and bf16 rows, K not a
     multiple of the ring's chunk nor of the cluster's warps."""
@@ -214,7 +230,7 @@ def test_batch1_full_size(api):
     run_head(x, cfg.K, api=api)
 
 
-@pytest.mark.parametrize("mode", ["auto", "cluster8", "split"])
+@pytest.mark.parametrize("mode", ["auto", "cluster8", "split", "radix"])
 @pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
                                     ("high", 512)])
 def test_draft_head_matches_the_two_calls(name, B, mode, tune):
@@ -225,6 +241,8 @@ def test_draft_head_matches_the_two_calls(name, B, mode, tune):
     with 8-CTA clusters, "split" the two kernels."""
     if mode == "cluster8":
         tune("DH_HEAD_CTAS", "8")
+    elif mode == "radix":
+        tune("DH_HEAD_SELECT", "radix")
     elif mode != "auto":
         tune("DH_FORCE_HEAD", mode)
     cfg = inputs.head_config(name, B=B)
@@ -243,13 +261,15 @@ def test_draft_head_matches_the_two_calls(name, B, mode, tune):
     assert dh.workspace_status(ws) == 0
 
 
+@pytest.mark.parametrize("select", ["auto", "radix"])
 @pytest.mark.parametrize("ctas", ["auto", "8", "4"])
 @pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
-def test_fused_head_matches_the_two_calls_over_K(K, ctas, tune):
+def test_fused_head_matches_the_two_calls_over_K(K, ctas, select, tune):
     """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
     of candidates per CTA, and beyond one candidate per warp), with 16-CTA clusters where they fit
-    and with 8 and 4."""
+    and with 8 and 4; with the group-best threshold selection (auto) and the cooperative radix one."""
     tune("DH_FORCE_HEAD", "cluster")
+    tune("DH_HEAD_SELECT", select)
     if ctas != "auto":
         tune("DH_HEAD_CTAS", ctas)
     cfg = inputs.head_config("tiny", B=3, K=K)
@@ -290,17 +310,23 @@ def test_draft_head_without_probs_and_bad_rows():
         check_logits(l2[b].cpu().numpy(), None, oz[b], None, where=f"row {b}")
 
 
-def test_moderate_load_sampled_rows():
+@pytest.mark.parametrize("api", ["split", "head"])
+def test_moderate_load_every_row(api):
     cfg = inputs.HEAD_CONFIGS["moderate"]
     x = inputs.make_head(cfg, seed=0, device=DEV)
-    run_head(x, cfg.K, rows=[0, 1, 17, 42, 63])
+    run_head(x, cfg.K, api=api)
+
+
+# 64 rows of the 512: in each of the four 128-row tiles of the tensor-core stage 1, in each of
+# the four 32-row lane quarters of its accumulator, the first and last row of each half
+HIGH_ROWS = [t * 128 + q * 32 + o for t in range(4) for q in range(4) for o in (0, 15, 16, 31)]
 
 
 @pytest.mark.parametrize("api", ["split", "head"])
-def test_high_load_sampled_rows(api):
+def test_high_load_stratified_rows(api):
     cfg = inputs.HEAD_CONFIGS["high"]
     x = inputs.make_head(cfg, seed=0, device=DEV)
-    run_head(x, cfg.K, rows=[0, 151, 152, 255, 303, 304, 511], api=api)
+    run_head(x, cfg.K, rows=HIGH_ROWS, api=api)
 
 
 # ---------------------------------------------------------------- trees
@@ -539,7 +565,7 @@ def test_bounded_waits_time_out_and_leave_the_context_usable():
     run_head(x, cfg.K)
 
 
-@pytest.mark.parametrize("path", ["direct", "ring", "ticket"])
+@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep"])
 def test_rescore_large_batch_with_repeats(path, tune):
     """Stage 2 on a large batch whose rows draw from a small candidate pool (many repeated W rows),
     with two out-of-range ids; a second call reuses the workspace tickets."""
@@ -568,6 +594,23 @@ def test_rescore_large_batch_with_repeats(path, tune):
     torch.cuda.synchronize()
     assert torch.equal(torch.nan_to_num(logits2), torch.nan_to_num(logits))
     assert torch.equal(torch.nan_to_num(probs2), torch.nan_to_num(probs))
+
+
+def test_sweep_matches_ring_at_high_load(tune):
+    """The vocabulary-sweep rescoring (the default from two rows per SM) against the bulk-copy ring on
+    the high-load candidates: the same dot products, so bit-identical logits; the softmax sums in
+    another order, so probabilities agree to rounding."""
+    cfg = inputs.HEAD_CONFIGS["high"]
+    x = inputs.make_head(cfg, seed=2, device=DEV)
+    idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+    tune("DH_FORCE_RESCORE", "sweep")
+    l1, p1 = dh.exact_rescore(x["h"], x["W"], idx)
+    tune("DH_FORCE_RESCORE", "ring")
+    l2, p2 = dh.exact_rescore(x["h"], x["W"], idx)
+    torch.cuda.synchronize()
+    assert torch.equal(l1, l2)
+    np.testing.assert_allclose(p1.cpu().numpy(), p2.cpu().numpy(), atol=1e-7, rtol=1e-5)
+    assert dh.workspace_status() == 0
 
 
 # ---------------------------------------------------------------- expanding frontier nodes
