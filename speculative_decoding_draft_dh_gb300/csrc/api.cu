@@ -133,6 +133,19 @@ void prof_after(cudaStream_t s) {
   if (!g_prof_recs.empty()) cudaEventRecord(g_prof_recs.back().b, s);
 }
 
+cudaError_t carveout_max_shared(const void* kernel, int device) {
+  static std::mutex mu;
+  static std::vector<std::pair<const void*, int>> done;
+  std::lock_guard<std::mutex> lk(mu);
+  for (const auto& d : done)
+    if (d.first == kernel && d.second == device) return cudaSuccess;
+  const cudaError_t e =
+      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, (int)cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return note_error(e, "cudaFuncSetAttribute(PreferredSharedMemoryCarveout)");
+  done.emplace_back(kernel, device);
+  return cudaSuccess;
+}
+
 }  // namespace dh
 
 using namespace dh;
@@ -331,13 +344,14 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
   const bool split = tuning().head_split;
   const int ctas = split || !head_cluster_supported(B, d, vocab, K, dtype) ? 0
                                                                           : head_cluster_ctas(c, B, K, d, vocab, dtype);
+  const bool fast = ctas && !tuning().head_select_radix;
   Stage1 s1;
   const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
   if (st != DH_OK) return st;
   if (ctas) {
-    if (note_error(launch_head_cluster(c, ctas, s1.recs, tuning().head_select_radix ? nullptr : s1.gkeys, s1.acc,
-                                       s1.t, V, h, W, B, d, r, vocab, K, dtype, idx_out, score_out, logits_out,
-                                       probs_out),
+    if (note_error(launch_head_cluster(c, ctas, s1.recs, fast ? s1.gkeys : nullptr, s1.acc, s1.t, V, h, W, B, d, r,
+                                       vocab, K, dtype, idx_out, score_out, logits_out, probs_out,
+                                       reinterpret_cast<int*>(ws)),
                    "selection and rescoring (cluster)") != cudaSuccess)
       return DH_ERR_CUDA;
     return DH_OK;
@@ -522,7 +536,9 @@ int dh_verify_chain(const void* logits, const int32_t* cand_idx, const float* ca
   if (B == 0) return DH_OK;
   if (!logits || !u_sample || !n_accept_out || !token_out) return DH_ERR_INVALID_ARG;
   if (L > 0 && (!cand_idx || !cand_prob || !draft_token || !u_accept)) return DH_ERR_INVALID_ARG;
-  if (L > kVerifyMaxL || vocab > DH_MAX_VOCAB || (long long)B * (L + 1) > 0x7FFFFFFFLL) return DH_ERR_UNSUPPORTED;
+  if (L > kVerifyMaxL || vocab > DH_MAX_VOCAB ||
+      (long long)B * (L + 1) * verify_segments(vocab, dtype) > 0x7FFFFFFFLL)
+    return DH_ERR_UNSUPPORTED;
   if (!aligned16(logits) || !row16(vocab, dtype)) return DH_ERR_UNSUPPORTED;
   const VerifyLayout Lw = verify_layout(B, L, vocab, dtype);
   if (!workspace || !aligned256(workspace) || ws_bytes < Lw.total) return DH_ERR_WORKSPACE;

@@ -239,11 +239,12 @@ bool head_cluster_supported(int B, int d, int vocab, int K, int dtype);
 int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype);
 // Fused selection and rescoring with clusters of `ctas` CTAs: t from the small-batch accumulators
 // (acc) or, with acc null, from t [B][r] in the activation dtype.
-// gkeys: the groups' best keys from the small-batch scores kernel (the fast selection), or null.
+// gkeys: the groups' best keys from the small-batch scores kernel (the fast selection), or null
+// (the cooperative radix selection).
 cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, const uint32_t* gkeys,
                                 unsigned long long* acc, const void* t, const void* V, const void* h, const void* W,
                                 int B, int d, int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out,
-                                float* logits, float* probs);
+                                float* logits, float* probs, int* status);
 
 cudaError_t launch_expand(const Ctx& c, const float* probs, const int32_t* idx, const float* parent_prob, int B,
                           int K, int w, float min_benefit, int32_t* child_token, float* child_prob,
@@ -294,6 +295,12 @@ __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + 
 
 // Records the failing CUDA call of the current thread for dh_last_error(); returns e.
 cudaError_t note_error(cudaError_t e, const char* where);
+
+// Sets a kernel's preferred shared-memory carveout to the largest, once per (kernel, device).
+// Blocks of kernels with different carveouts cannot share an SM (the SM is reconfigured only when
+// empty), so the kernels of one pipeline that are meant to overlap through programmatic dependent
+// launch all take the same one.
+cudaError_t carveout_max_shared(const void* kernel, int device);
 
 // Raises a kernel's dynamic shared memory limit to the device maximum minus its static shared
 // memory, once per device (a plain attribute call, so it is also safe during stream capture).

@@ -5,20 +5,23 @@
 // the K candidates of a row are its K best low-rank scores (score desc, id asc); their exact
 // logits come from the full-rank head, and the softmax runs over the K candidates.
 //
-// At batch 1 the selection is a short chain of dependent steps over about 4700 pool entries, and
-// each kernel boundary in the pipeline costs one to two microseconds.  Here the cluster's CTAs
-// split the row's group records and select cooperatively through distributed shared memory, with
-// the steps of the register fast path of the selection kernel (radix levels over the pool's own
-// key range, compaction, ranking by counting):
-//  - the key range is combined in the leader CTA (rank 0) behind one cluster barrier;
-//  - each radix level: every CTA histograms its own entries locally, and after one cluster barrier
-//    every CTA sums the CTAs' histograms and finds the boundary bin itself;
-//  - compaction writes the entries above and in the boundary bin into every CTA's lists;
-//  - every CTA ranks the boundary bin itself, so it knows the K winners and tau, checks the
-//    certificate on its groups and scores its share of the winners against h (staged in shared
-//    memory before the wait on the previous kernel), storing the logits into the leader, while the
-//    leader ranks the winners and writes them in order;
-//  - after one more barrier the leader orders the logits and computes the softmax.
+// At batch 1 the selection is a short chain of dependent steps, and each kernel boundary or
+// cluster barrier costs about half a microsecond to a microsecond.  Two selections run here:
+//  - the fast selection (default after the small-batch scores kernel, which also writes every
+//    group's best key): every CTA selects the K winners itself (a bound from K disjoint subsets of
+//    the groups' best keys, one histogram, then the records of the few candidate groups, read
+//    through L2, ranked by counting), so the CTAs exchange nothing until the exact logits; each CTA
+//    starts the W rows of its share of the candidate groups towards L2 as soon as it knows them,
+//    scores its share of the winners against h (bulk-copied into shared memory at the start), and
+//    stores the logits into the leader (rank 0), which computes the softmax after one cluster
+//    barrier;
+//  - the cooperative radix selection (DH_HEAD_SELECT=radix): the CTAs split the row's group records;
+//    the key range is combined in the leader behind one cluster barrier; each radix level every CTA
+//    histograms its own entries and, after one cluster barrier, sums the CTAs' histograms and finds
+//    the boundary bin itself; compaction writes the entries above and in the boundary bin into
+//    every CTA's lists; every CTA ranks the boundary bin, knows the K winners and tau, checks the
+//    certificate on its groups and scores its share of the winners while the leader ranks them;
+//    after one more barrier the leader orders the logits and computes the softmax.
 // A row whose certificate finds groups to re-score, or whose pool is degenerate, is selected again
 // by the leader alone with the block selection (select_row: exact, with refinement and full
 // rescan) and then rescored.
@@ -31,6 +34,7 @@
 #include <mutex>
 
 #include "select.cuh"
+#include "sm100.cuh"
 
 namespace dh {
 namespace {
@@ -65,6 +69,8 @@ struct HeadCtl {
   float z[HC_MAX_K];                            // the row's logits in rank order (leader)
   float zu[HC_MAX_K];                           // the logits by winner position (leader)
   int32_t rk[HC_MAX_K];                         // rank of each winner position (leader)
+  alignas(16) unsigned long long cmp[HC_BOUND];  // fast selection: the candidates, compacted
+  uint32_t cnt[16];                              // fast selection: each CTA's candidate count
 };
 
 struct HeadParams {
@@ -80,6 +86,7 @@ struct HeadParams {
   float* score_out;
   float* logits;
   float* probs;  // may be null
+  int* status;  // workspace status word
 };
 
 __device__ __forceinline__ void cluster_sync_all() {
@@ -91,6 +98,15 @@ __device__ __forceinline__ void cluster_sync_all() {
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
                : "memory");
+}
+
+// A group record read through L2 (not L1).
+__device__ __forceinline__ GroupRec ld_cg_rec(const GroupRec* r) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(r));
+  GroupRec g;
+  static_assert(sizeof(GroupRec) == 16, "a record is one 16-byte vector");
+  memcpy(&g, &v, sizeof g);
+  return g;
 }
 
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t id) {
@@ -135,169 +151,198 @@ __host__ __device__ constexpr size_t hc_h_offset() { return align_up(sizeof(Head
 __host__ __device__ constexpr size_t hc_fb_offset(int d, int elem) {
   return hc_h_offset() + align_up((size_t)d * elem, 128);
 }
+__host__ __device__ constexpr size_t hc_smem_bytes(int d, int elem, int n_groups) {
+  return hc_fb_offset(d, elem) + sel::select_smem_bytes(n_groups);
+}
+
+constexpr int HC_GK = HC_MAX_GROUPS / HC_THREADS;  // group keys per thread in the fast selection
+constexpr int HC_FBITS = 11;
+constexpr int HC_FBINS = 1 << HC_FBITS;  // the fast selection's histogram
+constexpr int HC_FBPT = HC_FBINS / HC_THREADS;
+static_assert(HC_FBPT == 8, "each thread scans two 16-byte vectors of bins");
+constexpr int HC_CG = 384;  // candidate groups of the fast selection (K <= 256 plus the boundary bin)
+constexpr uint64_t HC_WAIT_NS = 2000000000ull;  // limit of the wait for h's bulk copy (2 s)
 
 // Block-local state of the fast selection.
 struct FastShared {
-  uint32_t hist[HC_BINS];
-  uint32_t wsc[HC_WARPS], wmin[HC_WARPS], wmax[HC_WARPS];
-  uint32_t digit, run, bincount, total, nb, theta;
-  uint32_t bk[HC_RANK];  // the last level's bin
+  alignas(16) uint32_t hist[HC_FBINS];
+  alignas(16) unsigned long long ce[2 * HC_CG];  // the candidate entries, packed key << 32 | ~id
+  uint32_t smax[HC_MAX_K];                       // the largest key of each of the K subsets
+  int32_t cg[HC_CG];                             // the candidate groups
+  uint32_t cm3[HC_CG];                           // their third-best keys (certificate)
+  uint32_t wsc[HC_WARPS];
+  uint32_t bb;     // the boundary bin
+  uint32_t n_ent;  // candidate entries
 };
 
-// Fast selection from the groups' best keys (written by the small-batch scores kernel).
-// theta = the K-th largest of the row's group bests; each CTA finds it alone (radix levels over
-// the keys' own range with block barriers, then ranking inside the last bin).  The K groups whose
-// bests reach theta put K pool entries at or above it, so the pool's K-th best is >= theta and
-// every entry of the pool's top K is >= theta: the entries >= theta (K to 2K of them on random
-// rows) are compacted into every CTA's list behind one cluster barrier and ranked there, which
-// also orders them.  Then the certificate, the exact logits of the winners (each CTA its share)
-// and one more cluster barrier; the leader computes the softmax.  Returns true when the row must
-// take the leader's exact selection instead: more than HC_BOUND entries reach theta, fewer than K
-// groups hold entries, or the certificate flags a group.  Every CTA takes the same decision at
-// the same barrier.
-template <typename T, int HC_CTAS, int HC_RPT, int HC_ENT>
-__device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group& cl, HeadCtl& my, HeadCtl& L,
-                                          FastShared& fs, const T* hs, int b, int g0, int g1,
-                                          const GroupRec (&rec)[HC_RPT], const uint32_t (&key)[HC_ENT],
-                                          const uint32_t (&id)[HC_ENT]) {
-  constexpr int GK = HC_MAX_GROUPS / HC_THREADS;  // group keys per thread
+// Bounded wait for a bulk copy into shared memory; a copy that does not land in time raises
+// DH_ERR_TIMEOUT in the status word, and the thread waits once more so that the copy has landed
+// (or the second limit has passed) before the CTA reuses or releases the memory.
+__device__ __forceinline__ bool wait_copy(uint64_t* bar, int* status) {
+  if (sm100::mbar_wait(bar, 0, HC_WAIT_NS)) return true;
+  if ((threadIdx.x & 31) == 0) atomicOr(status, 1 << DH_ERR_TIMEOUT);
+  sm100::mbar_wait(bar, 0, HC_WAIT_NS);
+  return false;
+}
+
+// Fast selection from the groups' best keys (written by the small-batch scores kernel).  Every CTA
+// selects the row's K winners itself, from every group's best key and the records of a few groups,
+// so the CTAs exchange nothing before the exact logits:
+//  1. A lower bound lo on theta, the K-th largest group best: the keys are split into K disjoint
+//     subsets (thread t's keys form part of subset t mod K); each subset's largest key is a
+//     distinct key, so K keys reach the smallest of them.  On random rows about the top tenth
+//     of the keys reach lo.
+//  2. One histogram of the keys at or above lo, in bins of 2^sh keys over [lo, largest key]
+//     (monotone in the key), and a block scan from the top: the boundary bin bb holds theta, and
+//     theta' = lo + bb 2^sh <= theta.  The K groups whose bests reach theta put K pool entries at
+//     or above theta', so every entry of the pool's top K is at or above theta', and only groups
+//     whose best reaches theta' (the candidate groups: about K) hold such entries.
+//  3. The candidate groups' records are read (through L2); their entries at or above theta' are
+//     collected (their W rows start towards L2, each group's by one CTA) and ranked by counting,
+//     which also orders the K winners.  Certificate: a group whose third score reaches tau (the
+//     K-th winner's) may hide a member of the top K; only a candidate group can (its third score is
+//     at most its best).
+//  4. Each CTA scores winners k = warp x CTAs + rank and writes them in rank order; the logits go to
+//     the leader.  One cluster barrier; the leader computes the softmax.
+// Returns true when the row must take the leader's exact selection instead: fewer than K groups
+// hold entries, more than HC_CG groups reach theta', or the certificate flags a group.  Every CTA
+// takes the same decision from the same data.
+template <typename T, int HC_CTAS>
+__device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group& cl, HeadCtl& my, FastShared& fs,
+                                          const T* hs, uint64_t* hbar, int b, const uint32_t (&y)[HC_GK]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int K = p.K, n_groups = p.n_groups;
-  const bool leader = cl.block_rank() == 0;
-  // every group's best key of the row (written by the previous kernel: read through L2)
-  const uint32_t* grow = p.gkeys + (size_t)b * n_groups;
-  uint32_t y[GK];
-  uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
+  const int K = p.K;
+  const int crank = (int)cl.block_rank();
+  const bool leader = crank == 0;
+  const GroupRec* rrow = p.recs + (size_t)b * p.n_groups;
+  // ---- 1. lo: the smallest of the K subsets' largest keys (an empty subset leaves it 0)
+  uint32_t ymax = 0u;
 #pragma unroll
-  for (int q = 0; q < GK; ++q) {
-    const int g = (int)threadIdx.x + q * HC_THREADS;
-    y[q] = g < n_groups ? __ldcg(grow + g) : 0u;
-    if (y[q]) { kmin = min(kmin, y[q]); kmax = max(kmax, y[q]); }
-  }
-  kmin = __reduce_min_sync(0xFFFFFFFFu, kmin);
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-  if (lane == 0) { fs.wmin[warp] = kmin; fs.wmax[warp] = kmax; }
-  fs.hist[threadIdx.x] = 0u;
-  if (threadIdx.x == 0) fs.nb = 0u;
+  for (int q = 0; q < HC_GK; ++q) ymax = max(ymax, y[q]);
+  if (ymax) atomicMax(&fs.smax[threadIdx.x % K], ymax);
   __syncthreads();
+  uint32_t lo = 0xFFFFFFFFu, hi = 0u;
+  for (int s = lane; s < K; s += 32) {
+    const uint32_t v = fs.smax[s];
+    lo = min(lo, v);
+    hi = max(hi, v);
+  }
+  lo = max(__reduce_min_sync(0xFFFFFFFFu, lo), 1u);  // key 0 marks an empty group
+  hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  // ---- 2. histogram of the keys in [lo, hi], bins of 2^sh keys
+  const uint32_t span = hi >= lo ? hi - lo : 0u;
+  const int sh = max(0, (32 - __clz((int)span)) - HC_FBITS);
+  if (hi >= lo)
 #pragma unroll
-  for (int w = 0; w < HC_WARPS; ++w) { kmin = min(kmin, fs.wmin[w]); kmax = max(kmax, fs.wmax[w]); }
-  // every CTA's control block is zeroed (the initial arrive) before the compaction writes into it
-  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  bool ok = kmax != 0u;
-  uint32_t theta = 0u;
-  if (ok) {
+    for (int q = 0; q < HC_GK; ++q)
+      if (y[q] >= lo) atomicAdd(&fs.hist[(y[q] - lo) >> sh], 1u);
+  __syncthreads();
+  // thread t scans bins [HC_FBINS - 8(t + 1), HC_FBINS - 8t), from the top
+  const int base = HC_FBINS - HC_FBPT * ((int)threadIdx.x + 1);
+  const uint4 h0 = *reinterpret_cast<const uint4*>(&fs.hist[base]);
+  const uint4 h1 = *reinterpret_cast<const uint4*>(&fs.hist[base + 4]);
+  const uint32_t c[HC_FBPT] = {h1.w, h1.z, h1.y, h1.x, h0.w, h0.z, h0.y, h0.x};  // bins base+7 .. base
+  uint32_t own = 0u;
 #pragma unroll
-    for (int q = 0; q < GK; ++q) y[q] = y[q] ? y[q] - kmin + 1u : 0u;  // 0 = empty group
-    const uint32_t range = kmax - kmin + 1u;
-    int shift = range >= 0x80000000u ? 32 - HC_BITS : max(0, (32 - __clz((int)range)) - HC_BITS);
-    uint32_t prefix = 0u, mask = 0u, krem = (uint32_t)K, bc = 0u;
-    bool first = true;
-#pragma unroll 1
-    for (;;) {
+  for (int j = 0; j < HC_FBPT; ++j) own += c[j];
+  uint32_t incl = own;
 #pragma unroll
-      for (int q = 0; q < GK; ++q)
-        if (y[q] && (y[q] & mask) == prefix) atomicAdd(&fs.hist[(y[q] >> shift) & (HC_BINS - 1)], 1u);
-      __syncthreads();
-      const int bin = HC_BINS - 1 - (int)threadIdx.x;  // from the top
-      const uint32_t cnt = fs.hist[bin];
-      uint32_t incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) fs.wsc[warp] = incl;
+  __syncthreads();
+  uint32_t before = 0u, total = 0u;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += v;
-      }
-      if (lane == 31) fs.wsc[warp] = incl;
-      __syncthreads();
-      uint32_t before = 0u;
+  for (int w = 0; w < HC_WARPS; ++w) {
+    before += w < warp ? fs.wsc[w] : 0u;
+    total += fs.wsc[w];
+  }
+  uint32_t run = before + incl - own;  // keys in the bins above this thread's
 #pragma unroll
-      for (int w = 0; w < HC_WARPS; ++w) before += w < warp ? fs.wsc[w] : 0u;
-      incl += before;
-      if (incl - cnt < krem && krem <= incl) { fs.digit = (uint32_t)bin; fs.run = incl - cnt; fs.bincount = cnt; }
-      if (threadIdx.x == HC_THREADS - 1) fs.total = incl;
-      fs.hist[bin] = 0u;  // this thread's own bin, for the next level
-      __syncthreads();
-      if (first && fs.total < (uint32_t)K) { ok = false; break; }  // fewer nonempty groups than K
-      first = false;
-      prefix |= fs.digit << shift;
-      mask |= (uint32_t)(HC_BINS - 1) << shift;
-      krem -= fs.run;
-      bc = fs.bincount;
-      if (bc <= (uint32_t)HC_RANK || shift == 0) break;
-      shift = max(0, shift - HC_BITS);
-    }
-    if (ok) {
-      uint32_t ty = prefix;  // shift 0: every key of the last bin equals prefix
-      if (shift > 0) {
-        // the last bin holds at most HC_RANK keys: the krem-th largest of them by counting
+  for (int j = 0; j < HC_FBPT; ++j) {
+    if (run < (uint32_t)K && run + c[j] >= (uint32_t)K) fs.bb = (uint32_t)(base + HC_FBPT - 1 - j);
+    run += c[j];
+  }
+  if (threadIdx.x == 0) fs.n_ent = 0u;
+  __syncthreads();
+  const bool ok = hi >= lo && total >= (uint32_t)K;  // else fewer than K groups hold entries
+  const uint32_t theta = ok ? lo + (fs.bb << sh) : 0xFFFFFFFFu;
+  // ---- 3. the candidate groups (block scan for their positions), their records, their entries
+  uint32_t mine = 0u;
 #pragma unroll
-        for (int q = 0; q < GK; ++q)
-          if (y[q] && (y[q] & mask) == prefix) fs.bk[atomicAdd(&fs.nb, 1u)] = y[q];
-        __syncthreads();
-        if (threadIdx.x < bc) {
-          const uint32_t yi = fs.bk[threadIdx.x];
-          uint32_t rank = 0u;
-          for (uint32_t j = 0; j < bc; ++j) {
-            const uint32_t yj = fs.bk[j];
-            rank += (yj > yi || (yj == yi && j < threadIdx.x)) ? 1u : 0u;
-          }
-          if (rank == krem - 1u) fs.theta = yi;
-        }
-        __syncthreads();
-        ty = fs.theta;
-      }
-      theta = ty - 1u + kmin;
+  for (int q = 0; q < HC_GK; ++q) mine += (y[q] && y[q] >= theta) ? 1u : 0u;
+  incl = mine;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t v = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  if (lane == 31) fs.wsc[warp] = incl;
+  __syncthreads();
+  before = 0u;
+  total = 0u;
+#pragma unroll
+  for (int w = 0; w < HC_WARPS; ++w) {
+    before += w < warp ? fs.wsc[w] : 0u;
+    total += fs.wsc[w];
+  }
+  uint32_t pos = before + incl - mine;
+#pragma unroll
+  for (int q = 0; q < HC_GK; ++q) {
+    if (y[q] && y[q] >= theta) {
+      if (pos < (uint32_t)HC_CG) fs.cg[pos] = (int)threadIdx.x + q * HC_THREADS;
+      ++pos;
     }
   }
-  // the pool entries at or above theta into every CTA's list (positions from warp ballots and one
-  // remote atomic per warp on the leader's counter); their W rows start towards L2 now
-  const uint32_t below = (1u << lane) - 1u;
-#pragma unroll
-  for (int q = 0; q < HC_ENT; ++q) {
-    const bool c = ok && key[q] && key[q] >= theta;
-    const uint32_t bal = __ballot_sync(0xFFFFFFFFu, c);
-    uint32_t base = 0u;
-    if (lane == 0 && bal) base = atomicAdd(&L.n_bound, (uint32_t)__popc(bal));
-    base = __shfl_sync(0xFFFFFFFFu, base, 0);
-    if (c) {
-      const uint32_t pos = base + (uint32_t)__popc(bal & below);
-      if (pos < (uint32_t)HC_BOUND) {
-        const unsigned long long e = pack(key[q], id[q]);
-#pragma unroll
-        for (int c2 = 0; c2 < HC_CTAS; ++c2) *cl.map_shared_rank(&my.bp[pos], (unsigned)c2) = e;
+  const uint32_t n_cg = total;
+  bool fall = !ok || n_cg > (uint32_t)HC_CG;
+  __syncthreads();
+  if (!fall) {
+    for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) {
+      const int g = fs.cg[i];
+      const GroupRec r = ld_cg_rec(rrow + g);
+      fs.cm3[i] = fkey(r.m3);
+      const uint32_t o1 = r.offs & 0xFFu, o2 = (r.offs >> 8) & 0xFFu;
+      const uint32_t k2 = o2 != NO_OFFSET ? fkey(r.m2) : 0u;
+      const bool two = k2 && k2 >= theta;
+      const uint32_t slot = atomicAdd(&fs.n_ent, two ? 2u : 1u);  // at most 2 n_cg <= 2 HC_CG entries
+      const uint32_t v1 = (uint32_t)g * GROUP + o1, v2 = (uint32_t)g * GROUP + o2;
+      fs.ce[slot] = pack(fkey(r.m1), v1);
+      if (two) fs.ce[slot + 1] = pack(k2, v2);
+      if (g % HC_CTAS == crank) {  // each candidate group's W rows towards L2, by one CTA
+        const T* W = static_cast<const T*>(p.W);
+        const uint32_t row_bytes = (uint32_t)(p.d * sizeof(T));
+        if (v1 < (uint32_t)p.vocab) prefetch_l2(W + (size_t)v1 * p.d, row_bytes);
+        if (two && v2 < (uint32_t)p.vocab) prefetch_l2(W + (size_t)v2 * p.d, row_bytes);
       }
-      if (id[q] < (uint32_t)p.vocab)
-        prefetch_l2(static_cast<const T*>(p.W) + (size_t)id[q] * p.d, (uint32_t)(p.d * sizeof(T)));
     }
   }
-  cluster_sync_all();
-  const uint32_t n_cand = L.n_bound;  // the leader passes one more barrier below before it exits
-  if (!ok || n_cand > (uint32_t)HC_BOUND || n_cand < (uint32_t)K) return true;
-  // rank the candidates by counting: winner of rank k < K into sp[k] (every CTA, its own copy)
-  {
+  __syncthreads();
+  // ---- 4. rank the entries: the K winners in order; the certificate
+  bool flag = false;
+  if (!fall) {
+    const int n_ent = (int)fs.n_ent;  // at least n_cg >= K
     int P = 1;
-    while (P < 32 && (int)n_cand * (2 * P) <= HC_THREADS) P <<= 1;
-    for (int base = 0; base < (int)n_cand * P; base += HC_THREADS) {
-      const int t = base + (int)threadIdx.x;
+    while (P < 32 && n_ent * (2 * P) <= HC_THREADS) P <<= 1;
+    for (int base2 = 0; base2 < n_ent * P; base2 += HC_THREADS) {
+      const int t = base2 + (int)threadIdx.x;
       const int i = t / P, hh = t % P;
       unsigned long long pi;
-      const int rank = sel::rank_by_count(my.bp, (int)n_cand, P, i, hh, &pi);
-      if (i < (int)n_cand && hh == 0 && rank < K) my.sp[rank] = pi;
+      const int rank = sel::rank_by_count(fs.ce, n_ent, P, i, hh, &pi);
+      if (i < n_ent && hh == 0 && rank < K) my.sp[rank] = pi;
     }
+    __syncthreads();
+    const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
+    for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) flag |= fs.cm3[i] >= tau;
   }
-  __syncthreads();
-  // certificate: a group whose third score reaches tau (the K-th best) may hide a top-K member
-  const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
-  bool flag = false;
-#pragma unroll
-  for (int q = 0; q < HC_RPT; ++q)
-    flag |= (g0 + (int)threadIdx.x + q * HC_THREADS) < g1 && fkey(rec[q].m3) >= tau;
-  const uint32_t fm = __ballot_sync(0xFFFFFFFFu, flag);
-  if (lane == 0 && fm)
-#pragma unroll
-    for (int c2 = 0; c2 < HC_CTAS; ++c2) atomicAdd(cl.map_shared_rank(&my.nref, (unsigned)c2), (uint32_t)__popc(fm));
-  // exact logits of this CTA's winners, written out and stored into the leader for the softmax
-  const int crank = (int)cl.block_rank();
+  fall = __syncthreads_or(fall || flag) != 0;
+  // every CTA has started (the arrive at its start) before any CTA writes into the leader
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+  if (fall) return true;
+  // ---- 5. exact logits of winners k = warp x CTAs + rank, in rank order; into the leader
+  wait_copy(hbar, p.status);
   float* zl = cl.map_shared_rank(&my.z[0], 0u);
   for (int k = warp * HC_CTAS + crank; k < K; k += HC_CTAS * HC_WARPS) {
     const unsigned long long e = my.sp[k];
@@ -313,7 +358,6 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
     }
   }
   cluster_sync_all();
-  if (my.nref != 0u) return true;
   if (!leader) return false;
   // the row's accumulators are cleared for the next call (select_row does it on the other branch)
   if (p.acc) {
@@ -331,7 +375,6 @@ template <typename T, int HC_CTAS>
 __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   constexpr int HC_RPT = 16 / HC_CTAS;  // group records per thread
   constexpr int HC_ENT = 2 * HC_RPT;    // pool entries per thread
-  constexpr int PER = Elem<T>::PER16;
   extern __shared__ __align__(128) unsigned char smem[];
   cg::cluster_group cl = cg::this_cluster();
   const uint32_t crank = cl.block_rank();
@@ -347,20 +390,43 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   unsigned long long* acc_row = p.acc ? p.acc + (size_t)b * p.r : nullptr;
   const T* t_row = p.acc ? nullptr : static_cast<const T*>(p.t) + (size_t)b * p.r;
 
+  __shared__ FastShared fs;
+  __shared__ uint64_t hbar;  // h's bulk copy into shared memory
+  if (p.gkeys) {
+    for (int i = threadIdx.x; i < HC_FBINS; i += HC_THREADS) fs.hist[i] = 0u;
+    for (int i = threadIdx.x; i < HC_MAX_K; i += HC_THREADS) fs.smax[i] = 0u;
+  }
   // zero this CTA's control block; the barrier's wait (below) makes the leader's visible
   for (int i = threadIdx.x; i < HC_BINS; i += HC_THREADS) my.hist[0][i] = my.hist[1][i] = 0u;
   if (threadIdx.x == 0) {
     my.kmin = 0xFFFFFFFFu;
     my.kmax = 0u;
     my.n_above = my.n_bound = my.nref = 0u;
+    // h does not depend on the previous kernels: one bulk copy, waited for before the first dot
+    // product (every path waits, so no copy is in flight when the CTA exits)
+    const uint32_t h_bytes = (uint32_t)(p.d * sizeof(T));
+    sm100::mbar_init(&hbar, 1);
+    sm100::fence_barrier_init();
+    sm100::mbar_arrive_expect_tx(&hbar, h_bytes);
+    sm100::bulk_load(hs, static_cast<const T*>(p.h) + (size_t)b * p.d, h_bytes, &hbar);
   }
+  __syncthreads();
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-  // h does not depend on the previous kernels
-  const T* hrow = static_cast<const T*>(p.h) + (size_t)b * p.d;
-  for (int c = threadIdx.x * PER; c < p.d; c += HC_THREADS * PER)
-    *reinterpret_cast<uint4*>(hs + c) = __ldg(reinterpret_cast<const uint4*>(hrow + c));
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the scores kernel
 
+  bool fallback = false;
+  if (p.gkeys) {
+    // every group's best key of the row
+    uint32_t gk[HC_GK];
+    const uint32_t* grow = p.gkeys + (size_t)b * n_groups;
+#pragma unroll
+    for (int q = 0; q < HC_GK; ++q) {
+      const int g = (int)threadIdx.x + q * HC_THREADS;
+      gk[q] = g < n_groups ? __ldcg(grow + g) : 0u;
+    }
+    if (!head_fast<T, HC_CTAS>(p, cl, my, fs, hs, &hbar, b, gk)) return;
+    fallback = true;
+  } else {
   // this CTA's slice of the row's groups
   const int slice = (n_groups + HC_CTAS - 1) / HC_CTAS;
   const int g0 = (int)crank * slice, g1 = min(n_groups, g0 + slice);
@@ -379,12 +445,6 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
       if (o2 != NO_OFFSET) { key[2 * q + 1] = fkey(rec[q].m2); id[2 * q + 1] = (uint32_t)g * GROUP + o2; }
     }
   }
-  bool fallback = false;
-  if (p.gkeys) {
-    __shared__ FastShared fs;
-    if (!head_fast<T, HC_CTAS, HC_RPT, HC_ENT>(p, cl, my, L, fs, hs, b, g0, g1, rec, key, id)) return;
-    fallback = true;
-  } else {
   uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
 #pragma unroll
   for (int q = 0; q < HC_ENT; ++q)
@@ -554,6 +614,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     }
     // exact logits of the winners by position, into the leader, while it sorts; they are used
     // unless the certificate sends the row to the leader's block selection
+    wait_copy(&hbar, p.status);
     for (int k = k_first; k < K; k += n_sc * HC_WARPS) {
       const int v = (int)(~(uint32_t)my.sp[k]);
       const bool ok = v >= 0 && v < p.vocab;
@@ -588,6 +649,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
 
   // ---------------------------------------------------------------- exact logits and softmax
   const int32_t* cand = p.idx_out + (size_t)b * K;
+  wait_copy(&hbar, p.status);
   for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
     const int v = cand[k];
     const bool ok = v >= 0 && v < p.vocab;
@@ -619,8 +681,10 @@ cudaError_t launch(const Ctx& c, const HeadParams& p, size_t smem) {
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  cudaError_t e = carveout_max_shared(reinterpret_cast<const void*>(k_head_cl<T, CTAS>), c.device);
+  if (e != cudaSuccess) return e;
   prof_before("head_cluster", c.stream);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, k_head_cl<T, CTAS>, p);
+  e = cudaLaunchKernelEx(&cfg, k_head_cl<T, CTAS>, p);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -660,7 +724,7 @@ int clusters_at_once(int device, size_t smem) {
 // The DH_HEAD_CTAS switch (8 or 4) skips the larger forms (tests).
 template <typename T>
 int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
-  const size_t smem = hc_fb_offset(d, (int)sizeof(T)) + sel::select_smem_bytes(n_groups);
+  const size_t smem = hc_smem_bytes(d, (int)sizeof(T), n_groups);
   static std::mutex mu;
   static int cap[64][3] = {};  // [device]: clusters of 16, 8 and 4 at once, +1 (0: not queried)
   static size_t smem_at[64] = {};
@@ -688,7 +752,7 @@ int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
 
 template <typename T>
 cudaError_t run(const Ctx& c, const HeadParams& p, int ctas) {
-  const size_t smem = hc_fb_offset(p.d, (int)sizeof(T)) + sel::select_smem_bytes(p.n_groups);
+  const size_t smem = hc_smem_bytes(p.d, (int)sizeof(T), p.n_groups);
   if (ctas == 4) return launch<T, 4>(c, p, smem);
   return ctas == 16 ? launch<T, 16>(c, p, smem) : launch<T, 8>(c, p, smem);
 }
@@ -705,7 +769,7 @@ int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype) {
 
 bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
   const int n_groups = (vocab + GROUP - 1) / GROUP;
-  const size_t smem = hc_fb_offset(d, dtype == DH_BF16 ? 2 : 4) + sel::select_smem_bytes(n_groups);
+  const size_t smem = hc_smem_bytes(d, dtype == DH_BF16 ? 2 : 4, n_groups);
   return B >= 1 && K <= HC_MAX_K && n_groups <= HC_MAX_GROUPS && n_groups <= sel::CACHE_GROUPS &&
          d <= 8192 && smem <= 200 * 1024;
 }
@@ -713,7 +777,7 @@ bool head_cluster_supported(int B, int d, int vocab, int K, int dtype) {
 cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, const uint32_t* gkeys,
                                 unsigned long long* acc, const void* t, const void* V, const void* h, const void* W,
                                 int B, int d, int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out,
-                                float* logits, float* probs) {
+                                float* logits, float* probs, int* status) {
   if (ctas != 4 && ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
   HeadParams p;
   p.recs = recs;
@@ -733,6 +797,7 @@ cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, co
   p.score_out = score_out;
   p.logits = logits;
   p.probs = probs;
+  p.status = status;
   if (dtype == DH_BF16) return run<__nv_bfloat16>(c, p, ctas);
   return run<float>(c, p, ctas);
 }

@@ -524,6 +524,8 @@ cudaError_t launch_tma(const Ctx& c, cudaLaunchConfig_t& cfg, const CUtensorMap&
   static unsigned long long smem_done = 0;
   cudaError_t e = allow_max_smem(k_scores_small<T, NB>, c.device, &smem_done);
   if (e != cudaSuccess) return e;
+  e = carveout_max_shared(reinterpret_cast<const void*>(k_scores_small<T, NB>), c.device);
+  if (e != cudaSuccess) return e;
   return cudaLaunchKernelEx(&cfg, k_scores_small<T, NB>, tmV, sp);
 }
 
@@ -544,6 +546,7 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   pp.r = r;
   pp.acc = acc;
   pp.status = status;
+  const bool lsu = r % (LSU_WARPS * 16) == 0 && !tuning().scores_tma;
   cudaLaunchConfig_t cfg = {};
   cfg.stream = c.stream;
   cfg.attrs = attr;
@@ -556,7 +559,11 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
     cfg.blockDim = dim3(PV_THREADS);
     cfg.dynamicSmemBytes = (size_t)rpp * B * r * sizeof(float);
     switch (B) {
-#define DH_PV_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_proj_vec<T, n>, pp); break;
+#define DH_PV_CASE(n)                                                                    \
+  case n:                                                                                \
+    e = carveout_max_shared(reinterpret_cast<const void*>(k_proj_vec<T, n>), c.device); \
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_proj_vec<T, n>, pp);           \
+    break;
       DH_PV_CASE(1) DH_PV_CASE(2) DH_PV_CASE(3) DH_PV_CASE(4) DH_PV_CASE(5) DH_PV_CASE(6) DH_PV_CASE(7) DH_PV_CASE(8)
 #undef DH_PV_CASE
       default: e = cudaErrorInvalidValue;
@@ -567,7 +574,11 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
     cfg.gridDim = dim3((unsigned)max(1, min(3 * c.num_sms, d / 4)));
     cfg.blockDim = dim3(PJ_THREADS);
     switch (B) {
-#define DH_PJ_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_proj_small<T, n>, pp); break;
+#define DH_PJ_CASE(n)                                                                      \
+  case n:                                                                                  \
+    e = carveout_max_shared(reinterpret_cast<const void*>(k_proj_small<T, n>), c.device); \
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_proj_small<T, n>, pp);           \
+    break;
       DH_PJ_CASE(1) DH_PJ_CASE(2) DH_PJ_CASE(3) DH_PJ_CASE(4) DH_PJ_CASE(5) DH_PJ_CASE(6) DH_PJ_CASE(7) DH_PJ_CASE(8)
 #undef DH_PJ_CASE
       default: e = cudaErrorInvalidValue;
@@ -586,7 +597,6 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
   sp.recs = recs;
   sp.gkeys = gkeys;
   sp.status = status;
-  const bool lsu = r % (LSU_WARPS * 16) == 0 && !tuning().scores_tma;
   if (lsu) {
     constexpr int TW = 32 * Elem<T>::PER16;
     cfg.gridDim = dim3((unsigned)((vocab + TW - 1) / TW));
@@ -594,7 +604,11 @@ cudaError_t run(const Ctx& c, const void* h, const void* U, const void* V, int B
     cfg.dynamicSmemBytes = 0;
     prof_before("scores_lsu", c.stream);
     switch (B) {
-#define DH_LSU_CASE(n) case n: e = cudaLaunchKernelEx(&cfg, k_scores_lsu<T, n>, static_cast<const T*>(V), sp); break;
+#define DH_LSU_CASE(n)                                                                     \
+  case n:                                                                                  \
+    e = carveout_max_shared(reinterpret_cast<const void*>(k_scores_lsu<T, n>), c.device); \
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, k_scores_lsu<T, n>, static_cast<const T*>(V), sp); \
+    break;
       DH_LSU_CASE(1) DH_LSU_CASE(2) DH_LSU_CASE(3) DH_LSU_CASE(4) DH_LSU_CASE(5) DH_LSU_CASE(6) DH_LSU_CASE(7)
       DH_LSU_CASE(8)
 #undef DH_LSU_CASE

@@ -36,9 +36,11 @@ constexpr int VW_THREADS = 256;
 constexpr int VW_MAX_L = 64;   // drafted tokens per request
 constexpr float LOG2E = 1.4426950408889634f;
 
+// 2^x on the special-function unit, subnormal results flushed to zero (one instruction; the terms
+// it flushes are below 2^-126 of the row maximum's and do not move a sum).
 __device__ __forceinline__ float ex2(float x) {
   float y;
-  asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
 
@@ -52,17 +54,15 @@ __device__ __forceinline__ void combine(float& m, float& s, float m2, float s2) 
 
 template <typename T>
 __global__ void __launch_bounds__(VS_THREADS) k_verify_stats(const T* __restrict__ logits, int vocab, float c,
-                                                           int n_seg, long long n_items,
-                                                           float2* __restrict__ seg_stats) {
+                                                           int n_seg, int n_items, float2* __restrict__ seg_stats) {
   constexpr int PER = Elem<T>::PER16;
   constexpr int SEG = 32 * PER * SEG_VECS;
   const int lane = threadIdx.x & 31;
-  const long long nw = (long long)gridDim.x * (VS_THREADS / 32);
-  const long long w0 = (long long)blockIdx.x * (VS_THREADS / 32) + (threadIdx.x >> 5);
-  // the loads of item g: its SEG_VECS vectors per lane
-  auto load = [&](long long g, uint4 (&u)[SEG_VECS]) {
-    const long long row = g / n_seg;
-    const int sgi = (int)(g - row * n_seg);
+  const int nw = gridDim.x * (VS_THREADS / 32);
+  const int w0 = blockIdx.x * (VS_THREADS / 32) + (threadIdx.x >> 5);
+  // the loads of item g (row g / n_seg, segment g % n_seg): its SEG_VECS vectors per lane
+  auto load = [&](int g, uint4 (&u)[SEG_VECS]) {
+    const int row = g / n_seg, sgi = g - row * n_seg;
 #pragma unroll
     for (int v = 0; v < SEG_VECS; ++v) {
       const int id = sgi * SEG + (v * 32 + lane) * PER;
@@ -71,32 +71,38 @@ __global__ void __launch_bounds__(VS_THREADS) k_verify_stats(const T* __restrict
   };
   uint4 cur[SEG_VECS], nxt[SEG_VECS];
   load(w0, cur);
-  for (long long g = w0; g < n_items; g += nw) {
+  for (int g = w0; g < n_items; g += nw) {
     load(g + nw, nxt);  // the next item's loads are in flight while this one is reduced
-    const int sgi = (int)(g % n_seg);
+    const int sgi = g % n_seg;
+    // the maximum of the raw logits (the scale c > 0 keeps the order), then
+    // sum 2^(l c - m c) with one fused multiply-add per term; only the last segment of a row has ids
+    // past the vocabulary, whose terms are left out
     float z[SEG_VECS][PER];
     float m = -INFINITY;
+    const bool full = (sgi + 1) * SEG <= vocab;
 #pragma unroll
     for (int v = 0; v < SEG_VECS; ++v) {
-      const int id = sgi * SEG + (v * 32 + lane) * PER;
       Elem<T>::unpack(cur[v], z[v]);
+      if (!full) {
+        const int id = sgi * SEG + (v * 32 + lane) * PER;
 #pragma unroll
-      for (int e = 0; e < PER; ++e) {
-        z[v][e] = id < vocab ? z[v][e] * c : -INFINITY;
-        m = fmaxf(m, z[v][e]);
+        for (int e = 0; e < PER; ++e) z[v][e] = id < vocab ? z[v][e] : -INFINITY;
       }
+#pragma unroll
+      for (int e = 0; e < PER; ++e) m = fmaxf(m, z[v][e]);
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    const float mc = m * c;
     float sum = 0.f;
     if (m != -INFINITY)
 #pragma unroll
       for (int v = 0; v < SEG_VECS; ++v)
 #pragma unroll
-        for (int e = 0; e < PER; ++e) sum += ex2(z[v][e] - m);
+        for (int e = 0; e < PER; ++e) sum += ex2(fmaf(z[v][e], c, -mc));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xFFFFFFFFu, sum, o);
-    if (lane == 0) seg_stats[g] = make_float2(m, sum);
+    if (lane == 0) seg_stats[g] = make_float2(m == -INFINITY ? m : mc, sum);
 #pragma unroll
     for (int v = 0; v < SEG_VECS; ++v) cur[v] = nxt[v];
   }
@@ -382,10 +388,10 @@ cudaError_t run(const Ctx& c, const void* logits, int B, int L, int vocab, int K
   constexpr int SEG = 32 * Elem<T>::PER16 * SEG_VECS;
   const int n_seg = (vocab + SEG - 1) / SEG;
   const float cf = LOG2E / temperature;
-  const long long n_items = (long long)B * (L + 1) * n_seg;
+  const int n_items = B * (L + 1) * n_seg;  // < 2^31: checked by the caller
   // persistent grid: two blocks per SM stream the (row, segment) items
-  const long long per_block = VS_THREADS / 32;
-  const unsigned grid = (unsigned)max(1LL, min((long long)2 * c.num_sms, (n_items + per_block - 1) / per_block));
+  const int per_block = VS_THREADS / 32;
+  const unsigned grid = (unsigned)max(1, min(2 * c.num_sms, (n_items + per_block - 1) / per_block));
   prof_before("verify_stats", c.stream);
   k_verify_stats<T><<<grid, VS_THREADS, 0, c.stream>>>(static_cast<const T*>(logits), vocab, cf, n_seg, n_items,
                                                        seg_stats);

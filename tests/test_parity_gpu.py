@@ -231,14 +231,15 @@ def test_batch1_full_size(api):
 
 
 @pytest.mark.parametrize("mode", ["auto", "cluster8", "split", "radix"])
-@pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 8), ("tiny", 4), ("moderate", 64),
+@pytest.mark.parametrize("name,B", [("batch1", 1), ("batch1", 3), ("batch1", 8), ("tiny", 4), ("moderate", 64),
                                     ("high", 512)])
 def test_draft_head_matches_the_two_calls(name, B, mode, tune):
     """dh_draft_head gives bit-identical outputs to dh_lowrank_topk + dh_exact_rescore: the same
     selection rule on the same records and the same per-candidate dot product order; twice in a
     row with one workspace (its state resets itself).  "auto" takes the fused cluster kernel
     (selection and rescoring in one launch) where the batch is small enough, "cluster8" the same
-    with 8-CTA clusters, "split" the two kernels."""
+    with 8-CTA clusters, "split" the two kernels, "radix" the cooperative radix selection in the
+    cluster kernel."""
     if mode == "cluster8":
         tune("DH_HEAD_CTAS", "8")
     elif mode == "radix":
@@ -281,6 +282,30 @@ def test_fused_head_matches_the_two_calls_over_K(K, ctas, select, tune):
     torch.cuda.synchronize()
     assert torch.equal(i2, idx) and torch.equal(s2, score)
     assert torch.equal(l2, logits) and torch.equal(p2, probs)
+
+
+@pytest.mark.parametrize("B", [1, 2, 3])
+def test_fused_head_back_to_back_calls(B):
+    """Calls queued back to back on one stream with one workspace and no host synchronisation in
+    between (each call's kernels start, by programmatic dependent launch, while the previous ones
+    finish, and the workspace state resets itself): every call equals the two calls on its own
+    inputs, bit for bit."""
+    cfg = inputs.head_config("batch1", B=B)
+    base = inputs.make_head(cfg, seed=31, device=DEV)
+    U, V, W = base["U"], base["V"], base["W"]
+    g = torch.Generator(device="cpu").manual_seed(32)
+    hs = [(torch.randn(B, cfg.d, generator=g) * base["h"].float().std().item()).to(base["h"].dtype).to(DEV)
+          for _ in range(12)]
+    ws = dh.Workspace()
+    outs = [dh.draft_head(h, U, V, W, cfg.K, workspace=ws) for h in hs]
+    torch.cuda.synchronize()
+    for h, (i2, s2, l2, p2) in zip(hs, outs):
+        idx, score = dh.lowrank_topk(h, U, V, cfg.K)
+        logits, probs = dh.exact_rescore(h, W, idx)
+        torch.cuda.synchronize()
+        assert torch.equal(i2, idx) and torch.equal(s2, score)
+        assert torch.equal(l2, logits) and torch.equal(p2, probs)
+    assert dh.workspace_status(ws) == 0
 
 
 @pytest.mark.parametrize("B", [16, 32])
