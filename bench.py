@@ -59,7 +59,7 @@ MIN_TIMED_S = 0.1  # every added workload's timed region
 EXPAND_W = {"level": 4}  # children per frontier node in the draft-level workload
 # the draft level then sizes the next level: requests (the frontier nodes split evenly), width limit,
 # threshold in accepted tokens per microsecond of the synthetic latency table
-SIZE_LEVEL = {"level": {"requests": 2, "wmax": 8, "theta": 0.01}}
+SIZE_LEVEL = {"level": {"requests": 2, "wmax": 8, "theta": 0.002}}
 # the kernel each workload's `roofline` reports (the one that moves the step's bytes)
 ROOFLINE_KERNEL = {"batch1": "scores_lsu", "moderate": "rescore_ring", "high": "rescore_ring",
                    "level": "lowrank_mma", "tree": "tree_argmax"}
