@@ -30,7 +30,6 @@ namespace dh {
 namespace {
 
 constexpr int VS_THREADS = 512;
-constexpr int VS_WARPS = VS_THREADS / 32;
 constexpr int SEG_VECS = 4;    // 16-byte vectors per lane in a segment
 constexpr int VW_THREADS = 256;
 constexpr int VW_MAX_L = 64;   // drafted tokens per request
@@ -69,6 +68,8 @@ __global__ void __launch_bounds__(VS_THREADS) k_verify_stats(const T* __restrict
       u[v] = (g < n_items && id < vocab) ? ld_nc_v4(logits + (size_t)row * vocab + id) : make_uint4(0, 0, 0, 0);
     }
   };
+  // the walk kernel's blocks may launch as these retire (they wait for the statistics themselves)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   uint4 cur[SEG_VECS], nxt[SEG_VECS];
   load(w0, cur);
   for (int g = w0; g < n_items; g += nw) {
@@ -381,6 +382,285 @@ __global__ void __launch_bounds__(VW_THREADS) k_verify_walk(WalkParams p) {
   }
 }
 
+// Staged form of the walk (K <= VW_FK candidates per position and L K <= VW_CAP in all): before
+// its wait on the statistics, the block prepares every position's candidate list, so that after
+// the wait nothing of it needs memory: warp i sorts position i's entries by (id, k) (ranking by
+// counting), marks each id's first entry with q summed over the id's entries, and loads that id's
+// logit in row i.  After the wait: the rows' pairs and the acceptance tests give n as before; the
+// corrections -min(p, q) of position n's entries follow from shared memory, and, with the entries
+// in id order, each segment's corrections form one run, summed in order by the thread at its start.
+// Row n is prefetched into L2 for the final rescan of the claiming segment, whose corrections are
+// found by a binary search of the sorted ids.  Results repeat bit for bit (fixed orders throughout);
+// they agree with the general form of the walk to rounding.
+constexpr int VW_FK = 128;   // candidates per position on the staged path
+constexpr int VW_CAP = 2048;  // staged entries over all positions
+
+__device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+               : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(VW_THREADS) k_verify_walk_staged(WalkParams p) {
+  constexpr int PER = Elem<T>::PER16;
+  constexpr int SEG = 32 * PER * SEG_VECS;
+  constexpr int LANE_IDS = PER * SEG_VECS;
+  constexpr int NOID = 0x7FFFFFFF;           // sort key of an id outside the vocabulary (last)
+  extern __shared__ float sw[];             // [n_seg] segment weights, then [n_seg] correction sums
+  __shared__ int32_t e_v[VW_CAP];           // each position's entries sorted by (id, k)
+  __shared__ float e_q[VW_CAP];             // at an id's first entry: q(id) over its entries; else -1
+  __shared__ float e_l[VW_CAP];             // at an id's first entry: the id's logit in the row
+  __shared__ float s_corr[VW_FK];           // corrections of position n's entries (sorted order)
+  __shared__ int s_n, s_seg, s_last;
+  __shared__ float s_wtot[VW_THREADS / 32];
+  __shared__ float s_local;
+  __shared__ float2 s_row[VW_MAX_L + 1];
+  __shared__ float s_qx[VW_MAX_L], s_lx[VW_MAX_L];
+  const int b = blockIdx.x;
+  const int L = p.L, K = p.K, n_seg = p.n_seg;
+  float* cseg = sw + n_seg;
+  const T* rows = static_cast<const T*>(p.logits) + (size_t)b * (L + 1) * p.vocab;
+  const float2* segs = p.seg_stats + (size_t)b * (L + 1) * n_seg;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) { s_n = L; s_seg = 0x7FFFFFFF; s_last = -1; }
+  for (int s = threadIdx.x; s < n_seg; s += VW_THREADS) cseg[s] = 0.f;
+  // ---- before the wait: q_i(x_i), the logit of x_i, and position i's sorted entries (warp i)
+  for (int i = warp; i < L; i += VW_THREADS / 32) {
+    const int x = p.draft[(size_t)b * L + i];
+    const int32_t* ci = p.cand_idx + ((size_t)b * L + i) * K;
+    const float* cq = p.cand_prob + ((size_t)b * L + i) * K;
+    const T* row = rows + (size_t)i * p.vocab;
+    const int base = i * K;
+    float qx = 0.f;
+    for (int k = lane; k < K; k += 32) {
+      const int v = ci[k];
+      const float q = cq[k];
+      if (v == x) qx += q;
+      e_v[base + k] = (v >= 0 && v < p.vocab) ? v : NOID;
+      e_q[base + k] = q;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) qx += __shfl_xor_sync(0xFFFFFFFFu, qx, o);
+    if (lane == 0) {
+      const bool in_range = x >= 0 && x < p.vocab;
+      s_qx[i] = in_range ? qx : 0.f;  // outside the vocabulary: accepted, as q(x) = 0
+      s_lx[i] = in_range ? logit_at(row, x) : 0.f;
+    }
+    __syncwarp();
+    // rank by (id, k): at most VW_FK / 32 entries per lane
+    int rk[VW_FK / 32], kv[VW_FK / 32];
+    float kq[VW_FK / 32];
+#pragma unroll
+    for (int j = 0; j < VW_FK / 32; ++j) {
+      const int k = lane + 32 * j;
+      rk[j] = -1;
+      if (k < K) {
+        kv[j] = e_v[base + k];
+        kq[j] = e_q[base + k];
+        int r = 0;
+        for (int k2 = 0; k2 < K; ++k2) {
+          const int v2 = e_v[base + k2];
+          r += (v2 < kv[j] || (v2 == kv[j] && k2 < k)) ? 1 : 0;
+        }
+        rk[j] = r;
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < VW_FK / 32; ++j)
+      if (rk[j] >= 0) {
+        e_v[base + rk[j]] = kv[j];
+        e_q[base + rk[j]] = kq[j];
+      }
+    __syncwarp();
+    // first entries: q summed over the id's run (k order), and the id's logit
+    float fq[VW_FK / 32], fl[VW_FK / 32];
+#pragma unroll
+    for (int j = 0; j < VW_FK / 32; ++j) {
+      const int r = lane + 32 * j;
+      fq[j] = -1.f;
+      fl[j] = 0.f;
+      if (r < K) {
+        const int v = e_v[base + r];
+        if (v != NOID && (r == 0 || e_v[base + r - 1] != v)) {
+          float q = 0.f;
+          for (int r2 = r; r2 < K && e_v[base + r2] == v; ++r2) q += e_q[base + r2];
+          fq[j] = q;
+          fl[j] = logit_at(row, v);
+        }
+      }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < VW_FK / 32; ++j) {
+      const int r = lane + 32 * j;
+      if (r < K) {
+        e_q[base + r] = fq[j];
+        e_l[base + r] = fl[j];
+      }
+    }
+  }
+  // the statistics come from k_verify_stats (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // ---- warp i combines row i's segment pairs, then takes the acceptance test of position i
+  for (int i = warp; i <= L; i += VW_THREADS / 32) {
+    const float2 rp = row_pair(segs + (size_t)i * n_seg, n_seg);
+    if (lane == 0) {
+      s_row[i] = rp;
+      if (i < L) {
+        const float qx = s_qx[i];
+        const float px = ex2(s_lx[i] * p.c - rp.x) / rp.y;
+        const bool accepted = qx <= 0.f || p.u_accept[(size_t)b * L + i] < px / qx;
+        if (!accepted) atomicMin(&s_n, i);
+      }
+    }
+  }
+  __syncthreads();
+  const int n = s_n;
+  const T* row = rows + (size_t)n * p.vocab;
+  // row n towards L2 for the final rescan (64 KB pieces)
+  if (warp == VW_THREADS / 32 - 1) {
+    const uint32_t row_bytes = (uint32_t)((size_t)p.vocab * sizeof(T));  // a multiple of 16
+    for (uint32_t off = (uint32_t)lane * 65536u; off < row_bytes; off += 32u * 65536u)
+      prefetch_l2_bytes(reinterpret_cast<const char*>(row) + off, min(65536u, row_bytes - off));
+  }
+  const float2 st = s_row[n];
+  const float inv_s = 1.f / st.y;
+  const float2* seg = segs + (size_t)n * n_seg;
+  const int Kn = n < L ? K : 0;
+  const int base = n < L ? n * K : 0;
+  // ---- corrections -min(p, q) of position n's entries, then each segment's run summed in order
+  for (int r = threadIdx.x; r < Kn; r += VW_THREADS) {
+    const float q = e_q[base + r];
+    s_corr[r] = q >= 0.f ? -fminf(ex2(e_l[base + r] * p.c - st.x) * inv_s, q) : 0.f;
+  }
+  __syncthreads();
+  for (int r = threadIdx.x; r < Kn; r += VW_THREADS) {
+    const int v = e_v[base + r];
+    if (v == NOID) continue;
+    const int sg = v / SEG;
+    if (r > 0 && e_v[base + r - 1] / SEG == sg) continue;  // not the start of its segment's run
+    float cs = 0.f;
+    for (int r2 = r; r2 < Kn && e_v[base + r2] != NOID && e_v[base + r2] / SEG == sg; ++r2) cs += s_corr[r2];
+    cseg[sg] = cs;
+  }
+  __syncthreads();
+  // ---- per-segment weights; thread t owns segments [t * per, (t + 1) * per)
+  const int per = (n_seg + VW_THREADS - 1) / VW_THREADS;
+  const int sa = min(n_seg, (int)threadIdx.x * per), sb = min(n_seg, sa + per);
+  auto seg_mass = [&](int s) {
+    const float2 sg = seg[s];
+    return sg.x == -INFINITY ? 0.f : sg.y * ex2(sg.x - st.x) * inv_s;
+  };
+  float tsum = 0.f;
+  for (int s = sa; s < sb; ++s) {
+    const float w = fmaxf(seg_mass(s) + cseg[s], 0.f);
+    sw[s] = w;
+    tsum += w;
+  }
+  float total;
+  float excl = block_excl_scan(tsum, s_wtot, &total);
+  // a zero residual (p_n = q_n on the candidates, no mass elsewhere): draw from p_n itself
+  const bool use_p = !(total > 0.f);
+  if (use_p) {
+    tsum = 0.f;
+    for (int s = sa; s < sb; ++s) {
+      sw[s] = seg_mass(s);
+      tsum += sw[s];
+    }
+    excl = block_excl_scan(tsum, s_wtot, &total);
+  }
+  const float target = p.u_sample[b] * total;
+  int mine = -1, last_pos = -1;
+  float before = 0.f;
+  if (sb > sa && excl <= target && target < excl + tsum) {
+    float run = excl;
+    for (int s = sa; s < sb; ++s) {
+      if (sw[s] > 0.f && run + sw[s] > target) { mine = s; before = run; break; }
+      run += sw[s];
+    }
+  }
+  for (int s = sa; s < sb; ++s)
+    if (sw[s] > 0.f) last_pos = s;
+  if (mine >= 0) atomicMin(&s_seg, mine);
+  if (last_pos >= 0) atomicMax(&s_last, last_pos);
+  __syncthreads();
+  const bool claimed = s_seg != 0x7FFFFFFF;
+  if (mine >= 0 && mine == s_seg) s_local = target - before;
+  __syncthreads();
+  // ---- warp 0 recomputes the chosen segment's weights id by id and finds the token
+  if (warp == 0) {
+    const int sg = claimed ? s_seg : (s_last < 0 ? 0 : s_last);
+    const float local = claimed ? s_local : INFINITY;  // unclaimed: the segment's last positive id
+    const int id0 = sg * SEG + lane * LANE_IDS;
+    float w[LANE_IDS];
+#pragma unroll
+    for (int v = 0; v < SEG_VECS; ++v) {
+      const int id = id0 + v * PER;
+      uint4 u = make_uint4(0, 0, 0, 0);
+      if (id < p.vocab) u = *reinterpret_cast<const uint4*>(row + id);
+      Elem<T>::unpack(u, w + v * PER);
+#pragma unroll
+      for (int e = 0; e < PER; ++e) w[v * PER + e] = id + e < p.vocab ? ex2(w[v * PER + e] * p.c - st.x) * inv_s : 0.f;
+    }
+    if (!use_p && Kn > 0) {
+      // the segment's entries: the first sorted entry with id >= sg * SEG (binary search), onwards
+      int lo = 0, hi = Kn;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (e_v[base + mid] < sg * SEG) lo = mid + 1; else hi = mid;
+      }
+      for (int r = lo; r < Kn; ++r) {
+        const int v = e_v[base + r];
+        if (v == NOID || v >= (sg + 1) * SEG) break;
+        if (e_q[base + r] < 0.f || v < id0 || v >= id0 + LANE_IDS) continue;  // not a first entry, or another lane's
+#pragma unroll
+        for (int e = 0; e < LANE_IDS; ++e)
+          if (id0 + e == v) w[e] = fmaxf(w[e] + s_corr[r], 0.f);
+      }
+    }
+    float lsum = 0.f;
+#pragma unroll
+    for (int e = 0; e < LANE_IDS; ++e) lsum += w[e];
+    float incl = lsum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    const float ex = incl - lsum;
+    const uint32_t bm = __ballot_sync(0xFFFFFFFFu, lsum > 0.f && ex <= local && local < incl);
+    int tok = -1;
+    if (bm) {
+      const int src = __ffs(bm) - 1;
+      if (lane == src) {
+        float run = ex;
+#pragma unroll
+        for (int e = 0; e < LANE_IDS; ++e) {
+          if (tok < 0 && w[e] > 0.f && run + w[e] > local) tok = id0 + e;
+          run += w[e];
+        }
+        if (tok < 0)
+#pragma unroll
+          for (int e = 0; e < LANE_IDS; ++e)
+            if (w[e] > 0.f) tok = id0 + e;
+      }
+      tok = __shfl_sync(0xFFFFFFFFu, tok, src);
+    } else {
+      int lastv = -1;
+#pragma unroll
+      for (int e = 0; e < LANE_IDS; ++e)
+        if (w[e] > 0.f) lastv = id0 + e;
+      lastv = __reduce_max_sync(0xFFFFFFFFu, lastv);
+      tok = lastv < 0 ? sg * SEG : lastv;
+    }
+    if (lane == 0) {
+      p.n_accept[b] = n;
+      p.token[b] = tok;
+    }
+  }
+}
+
 template <typename T>
 cudaError_t run(const Ctx& c, const void* logits, int B, int L, int vocab, int K, const int32_t* cand_idx,
                 const float* cand_prob, const int32_t* draft, const float* u_accept, const float* u_sample,
@@ -419,15 +699,21 @@ cudaError_t run(const Ctx& c, const void* logits, int B, int L, int vocab, int K
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)B);
   cfg.blockDim = dim3(VW_THREADS);
-  cfg.dynamicSmemBytes = (size_t)n_seg * sizeof(float);
   cfg.stream = c.stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  static unsigned long long smem_done = 0;
-  e = allow_max_smem(k_verify_walk<T>, c.device, &smem_done);
+  const bool staged = K <= VW_FK && (long long)L * K <= VW_CAP;
+  static unsigned long long smem_done = 0, smem_done_st = 0;
+  if (staged) {
+    cfg.dynamicSmemBytes = 2 * (size_t)n_seg * sizeof(float);
+    e = allow_max_smem(k_verify_walk_staged<T>, c.device, &smem_done_st);
+  } else {
+    cfg.dynamicSmemBytes = (size_t)n_seg * sizeof(float);
+    e = allow_max_smem(k_verify_walk<T>, c.device, &smem_done);
+  }
   if (e != cudaSuccess) return e;
   prof_before("verify_walk", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_verify_walk<T>, wp);
+  e = staged ? cudaLaunchKernelEx(&cfg, k_verify_walk_staged<T>, wp) : cudaLaunchKernelEx(&cfg, k_verify_walk<T>, wp);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();

@@ -58,8 +58,9 @@ def test_tiny_verify_matches_oracle(T, seed):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 def test_ragged_segments_and_depths(dtype):
-    """A vocabulary that ends inside a segment, depths 1 to 9, K from 1 to 100."""
-    for L, K, vocab in ((1, 1, 1000), (3, 7, 2056), (9, 100, 5000)):
+    """A vocabulary that ends inside a segment, depths 1 to 30, K from 1 to 200 (the staged walk up
+    to 128 candidates and 2048 entries in all, the general one beyond)."""
+    for L, K, vocab in ((1, 1, 1000), (3, 7, 2056), (9, 100, 5000), (5, 200, 4000), (30, 100, 3000)):
         cfg = inputs.verify_config("tiny_verify", B=16, L=L, K=K, vocab=vocab, dtype=dtype)
         v = inputs.make_verify(cfg, seed=L, device=DEV)
         check_against_oracle(v, 1.0)
@@ -86,10 +87,16 @@ def test_bonus_only_and_outside_candidates():
     assert np.all(gn >= 1)
 
 
-def test_duplicate_candidates_and_extreme_uniforms():
-    cfg = inputs.verify_config("tiny_verify", B=16, L=2, K=8)
+@pytest.mark.parametrize("K", [8, 160])
+def test_duplicate_candidates_and_extreme_uniforms(K):
+    """Every id listed twice (q adds both), ids outside the vocabulary (no correction), uniforms at
+    0 and just below 1; K = 8 takes the staged walk, K = 160 the general one."""
+    cfg = inputs.verify_config("tiny_verify", B=16, L=2, K=K)
     v = inputs.make_verify(cfg, seed=6, device=DEV)
-    v["cand_idx"][:, :, 4:] = v["cand_idx"][:, :, :4]  # every id listed twice: q(v) adds both
+    h = K // 2
+    v["cand_idx"][:, :, h:2 * h] = v["cand_idx"][:, :, :h]
+    v["cand_idx"][:, 1, 0] = -1
+    v["cand_idx"][:, 1, 1] = cfg.vocab + 5
     v["u_sample"][:8] = 0.0
     v["u_sample"][8:] = float(np.nextafter(np.float32(1.0), np.float32(0.0)))
     v["u_accept"][:4] = 0.0
