@@ -1146,6 +1146,11 @@ def profile_run(a):
         cfg = inputs.HEAD_CONFIGS[a.workload]
         x = inputs.make_head(cfg, seed=a.seed, device=dev)
         ew = EXPAND_W.get(cfg.name, 0)
+        sizing = SIZE_LEVEL.get(cfg.name)
+        if sizing:
+            cost, bins = inputs.latency_table(sizing["wmax"])
+            cost_d, bins_d = torch.from_numpy(cost).to(dev), torch.from_numpy(bins).to(dev)
+            par = torch.linspace(1.0, 0.25, cfg.B, device=dev, dtype=torch.float32)
         for _ in range(a.warmup + a.steps):
             if a.api == "head":
                 idx, _, _, probs = dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K)
@@ -1153,7 +1158,13 @@ def profile_run(a):
                 idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
                 _, probs = dh.exact_rescore(x["h"], x["W"], idx)
             if ew:
-                dh.expand_children(probs, idx, ew, min_benefit=1e-3)
+                ctok, cprob, keep = dh.expand_children(probs, idx, ew, parent_prob=par if sizing else None,
+                                                       min_benefit=1e-3)
+                if sizing:
+                    R = sizing["requests"]
+                    F = cfg.B // R
+                    dh.size_level(cprob.view(R, F, ew), ctok.view(R, F, ew), cost_d, bins_d, R, sizing["theta"],
+                                  n_valid=keep.view(R, F))
     torch.cuda.synchronize()
     print(json.dumps({"profile_run": a.workload, "steps": a.warmup + a.steps}), flush=True)
 
