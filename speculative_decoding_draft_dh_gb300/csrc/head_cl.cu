@@ -146,6 +146,24 @@ __device__ __forceinline__ float row_dot(const T* __restrict__ W, int v, int d, 
   return acc;
 }
 
+// The same dot product with the W row in shared memory (lane-strided 16-byte chunks in row_dot's
+// order, fp32 fused multiply-adds, the same xor reduction): bit-identical to row_dot.
+template <typename T>
+__device__ __forceinline__ float row_dot_smem(const T* wrow, int d, const T* hs, int lane) {
+  constexpr int PER = Elem<T>::PER16;
+  float acc = 0.f;
+  for (int c = lane * PER; c < d; c += 32 * PER) {
+    float wf[PER], xf[PER];
+    Elem<T>::unpack(*reinterpret_cast<const uint4*>(wrow + c), wf);
+    Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
+#pragma unroll
+    for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+  return acc;
+}
+
 // Dynamic shared memory layout: control block, h, then the block selection's area (leader only).
 __host__ __device__ constexpr size_t hc_h_offset() { return align_up(sizeof(HeadCtl), 128); }
 __host__ __device__ constexpr size_t hc_fb_offset(int d, int elem) {
@@ -173,6 +191,7 @@ struct FastShared {
   uint32_t wsc[HC_WARPS];
   uint32_t bb;     // the boundary bin
   uint32_t n_ent;  // candidate entries
+  uint64_t wbar[HC_WARPS];  // each warp's first winner's W row, bulk-copied into the selection area
 };
 
 // Bounded wait for a bulk copy into shared memory; a copy that does not land in time raises
@@ -209,7 +228,7 @@ __device__ __forceinline__ bool wait_copy(uint64_t* bar, int* status) {
 // takes the same decision from the same data.
 template <typename T, int HC_CTAS>
 __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group& cl, HeadCtl& my, FastShared& fs,
-                                          const T* hs, uint64_t* hbar, int b, const uint32_t (&y)[HC_GK]) {
+                                          const T* hs, uint64_t* hbar, T* slots, int b, const uint32_t (&y)[HC_GK]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = p.K;
   const int crank = (int)cl.block_rank();
@@ -334,21 +353,48 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
       if (i < n_ent && hh == 0 && rank < K) my.sp[rank] = pi;
     }
     __syncthreads();
+  }
+  // each warp's first winner's W row starts into the warp's slot of the selection area now (a bulk
+  // copy), ahead of the certificate and the cluster wait
+  const uint32_t row_bytes = (uint32_t)(p.d * sizeof(T));
+  const int n_slot = min(HC_WARPS, (int)(sel::select_smem_bytes(p.n_groups) / row_bytes));
+  const int k_first = warp * HC_CTAS + crank;
+  bool slotted = false;
+  if (!fall && warp < n_slot && k_first < K) {
+    const int v = (int)(~(uint32_t)my.sp[k_first]);
+    slotted = v >= 0 && v < p.vocab;
+    if (slotted && lane == 0) {
+      sm100::mbar_arrive_expect_tx(&fs.wbar[warp], row_bytes);
+      sm100::bulk_load(slots + (size_t)warp * p.d, static_cast<const T*>(p.W) + (size_t)v * p.d, row_bytes,
+                       &fs.wbar[warp]);
+    }
+  }
+  if (!fall) {
     const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
     for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) flag |= fs.cm3[i] >= tau;
   }
   fall = __syncthreads_or(fall || flag) != 0;
   // every CTA has started (the arrive at its start) before any CTA writes into the leader
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-  if (fall) return true;
+  if (fall) {
+    if (slotted) wait_copy(&fs.wbar[warp], p.status);  // landed before the selection area is reused
+    __syncthreads();
+    return true;
+  }
   // ---- 5. exact logits of winners k = warp x CTAs + rank, in rank order; into the leader
   wait_copy(hbar, p.status);
   float* zl = cl.map_shared_rank(&my.z[0], 0u);
-  for (int k = warp * HC_CTAS + crank; k < K; k += HC_CTAS * HC_WARPS) {
+  for (int k = k_first; k < K; k += HC_CTAS * HC_WARPS) {
     const unsigned long long e = my.sp[k];
     const int v = (int)(~(uint32_t)e);
     const bool okv = v >= 0 && v < p.vocab;
-    const float acc = okv ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
+    float acc = 0.f;
+    if (k == k_first && slotted) {
+      wait_copy(&fs.wbar[warp], p.status);
+      acc = row_dot_smem<T>(slots + (size_t)warp * p.d, p.d, hs, lane);
+    } else if (okv) {
+      acc = row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane);
+    }
     const float z = okv ? acc : __int_as_float(0x7FC00000);
     if (lane == 0) {
       p.idx_out[(size_t)b * K + k] = v;
@@ -406,6 +452,8 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     // product (every path waits, so no copy is in flight when the CTA exits)
     const uint32_t h_bytes = (uint32_t)(p.d * sizeof(T));
     sm100::mbar_init(&hbar, 1);
+    if (p.gkeys)
+      for (int w = 0; w < HC_WARPS; ++w) sm100::mbar_init(&fs.wbar[w], 1);
     sm100::fence_barrier_init();
     sm100::mbar_arrive_expect_tx(&hbar, h_bytes);
     sm100::bulk_load(hs, static_cast<const T*>(p.h) + (size_t)b * p.d, h_bytes, &hbar);
@@ -424,7 +472,7 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
       const int g = (int)threadIdx.x + q * HC_THREADS;
       gk[q] = g < n_groups ? __ldcg(grow + g) : 0u;
     }
-    if (!head_fast<T, HC_CTAS>(p, cl, my, fs, hs, &hbar, b, gk)) return;
+    if (!head_fast<T, HC_CTAS>(p, cl, my, fs, hs, &hbar, reinterpret_cast<T*>(fb), b, gk)) return;
     fallback = true;
   } else {
   // this CTA's slice of the row's groups
