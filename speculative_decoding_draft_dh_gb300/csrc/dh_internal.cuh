@@ -115,18 +115,61 @@ struct Top2 {
   }
 };
 
+// fp32 fused multiply-add of two bf16 inputs, taken from the low (or high) halves of 32-bit words.
+// The mixed-precision form (bf16 inputs, fp32 addend and result) widens both inputs exactly and
+// rounds once, so it returns fmaf(float(a), float(b), c) bit for bit, without separate widening
+// instructions.
+__device__ __forceinline__ float fma_bf16_lo(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, al, bl, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+__device__ __forceinline__ float fma_bf16_hi(uint32_t a, uint32_t b, float c) {
+  float d;
+  asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+      "fma.rn.f32.bf16 %0, ah, bh, %3;\n\t}"
+      : "=f"(d)
+      : "r"(a), "r"(b), "f"(c));
+  return d;
+}
+
+// Per-dtype element access.  For the dot products:
+// - dot16(x, w, acc): acc = fma(x[e], w[e], acc) for e = 0, 1, ... over the elements of two
+//   16-byte vectors, one fp32 rounding per step (the order every rescoring kernel shares);
+// - Scalar: a scalar operand in the form axpy16 takes (fp32; for bf16 the value's bits in both
+//   halves of a word), from scalar(v) of a value v that the dtype represents exactly;
+// - axpy16(t, w, acc): acc[e] = fma(t, w[e], acc[e]) for each element of one 16-byte vector.
 template <typename T> struct Elem;
 template <> struct Elem<float> {
   static constexpr int PER16 = 4;  // elements per 16-byte vector
+  using Scalar = float;
   __device__ __forceinline__ static void unpack(const uint4& u, float* out) {
     out[0] = __uint_as_float(u.x); out[1] = __uint_as_float(u.y);
     out[2] = __uint_as_float(u.z); out[3] = __uint_as_float(u.w);
   }
   __device__ __forceinline__ static float to_f(float x) { return x; }
   __device__ __forceinline__ static float from_f(float x) { return x; }
+  __device__ __forceinline__ static float dot16(const uint4& x, const uint4& w, float acc) {
+    acc = fmaf(__uint_as_float(x.x), __uint_as_float(w.x), acc);
+    acc = fmaf(__uint_as_float(x.y), __uint_as_float(w.y), acc);
+    acc = fmaf(__uint_as_float(x.z), __uint_as_float(w.z), acc);
+    return fmaf(__uint_as_float(x.w), __uint_as_float(w.w), acc);
+  }
+  __device__ __forceinline__ static Scalar scalar(float v) { return v; }
+  __device__ __forceinline__ static Scalar scalar_of(float x) { return x; }
+  __device__ __forceinline__ static void axpy16(Scalar t, const uint4& w, float* acc) {
+    acc[0] = fmaf(t, __uint_as_float(w.x), acc[0]);
+    acc[1] = fmaf(t, __uint_as_float(w.y), acc[1]);
+    acc[2] = fmaf(t, __uint_as_float(w.z), acc[2]);
+    acc[3] = fmaf(t, __uint_as_float(w.w), acc[3]);
+  }
 };
 template <> struct Elem<__nv_bfloat16> {
   static constexpr int PER16 = 8;
+  using Scalar = uint32_t;
   __device__ __forceinline__ static void unpack(const uint4& u, float* out) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
@@ -137,6 +180,35 @@ template <> struct Elem<__nv_bfloat16> {
   }
   __device__ __forceinline__ static float to_f(__nv_bfloat16 x) { return __bfloat162float(x); }
   __device__ __forceinline__ static __nv_bfloat16 from_f(float x) { return __float2bfloat16_rn(x); }
+  __device__ __forceinline__ static float dot16(const uint4& x, const uint4& w, float acc) {
+    acc = fma_bf16_lo(x.x, w.x, acc);
+    acc = fma_bf16_hi(x.x, w.x, acc);
+    acc = fma_bf16_lo(x.y, w.y, acc);
+    acc = fma_bf16_hi(x.y, w.y, acc);
+    acc = fma_bf16_lo(x.z, w.z, acc);
+    acc = fma_bf16_hi(x.z, w.z, acc);
+    acc = fma_bf16_lo(x.w, w.w, acc);
+    return fma_bf16_hi(x.w, w.w, acc);
+  }
+  // v must be a bf16 value (its low 16 bits are zero)
+  __device__ __forceinline__ static Scalar scalar(float v) {
+    const uint32_t u = __float_as_uint(v) >> 16;
+    return u | (u << 16);
+  }
+  __device__ __forceinline__ static Scalar scalar_of(__nv_bfloat16 x) {
+    const uint32_t u = __bfloat16_as_ushort(x);
+    return u | (u << 16);
+  }
+  __device__ __forceinline__ static void axpy16(Scalar t, const uint4& w, float* acc) {
+    acc[0] = fma_bf16_lo(t, w.x, acc[0]);
+    acc[1] = fma_bf16_hi(t, w.x, acc[1]);
+    acc[2] = fma_bf16_lo(t, w.y, acc[2]);
+    acc[3] = fma_bf16_hi(t, w.y, acc[3]);
+    acc[4] = fma_bf16_lo(t, w.z, acc[4]);
+    acc[5] = fma_bf16_hi(t, w.z, acc[5]);
+    acc[6] = fma_bf16_lo(t, w.w, acc[6]);
+    acc[7] = fma_bf16_hi(t, w.w, acc[7]);
+  }
 };
 
 // Softmax over z[0..K) by one warp (lane i takes elements i, i + 32, ...; max and sum by xor

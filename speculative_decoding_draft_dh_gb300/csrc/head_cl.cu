@@ -132,13 +132,7 @@ __device__ __forceinline__ float row_dot(const T* __restrict__ W, int v, int d, 
 #pragma unroll
     for (int q = 0; q < MAXW; ++q) {
       const int c = c0 + (q * 32 + lane) * PER;
-      if (c < d) {
-        float wf[PER], xf[PER];
-        Elem<T>::unpack(wa[q], wf);
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-      }
+      if (c < d) acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hs + c), wa[q], acc);
     }
   }
 #pragma unroll
@@ -152,13 +146,8 @@ template <typename T>
 __device__ __forceinline__ float row_dot_smem(const T* wrow, int d, const T* hs, int lane) {
   constexpr int PER = Elem<T>::PER16;
   float acc = 0.f;
-  for (int c = lane * PER; c < d; c += 32 * PER) {
-    float wf[PER], xf[PER];
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(wrow + c), wf);
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
-#pragma unroll
-    for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-  }
+  for (int c = lane * PER; c < d; c += 32 * PER)
+    acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hs + c), *reinterpret_cast<const uint4*>(wrow + c), acc);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
   return acc;

@@ -40,13 +40,7 @@ __device__ __forceinline__ float warp_row_dot(const T* __restrict__ W, int v, in
 #pragma unroll
     for (int q = 0; q < MAXW; ++q) {
       const int c = c0 + (q * 32 + lane) * PER;
-      if (c < d) {
-        float wf[PER], xf[PER];
-        Elem<T>::unpack(wa[q], wf);
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(sh_h + c), xf);
-#pragma unroll
-        for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-      }
+      if (c < d) acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(sh_h + c), wa[q], acc);
     }
   }
 #pragma unroll
@@ -327,13 +321,8 @@ __global__ void __launch_bounds__(RING_THREADS, 2)
       float acc = 0.f;
       if (ok) {
         const T* wr = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
-        for (int c = lane * PER; c < d; c += 32 * PER) {
-          float wf[PER], xf[PER];
-          Elem<T>::unpack(*reinterpret_cast<const uint4*>(wr + c), wf);
-          Elem<T>::unpack(*reinterpret_cast<const uint4*>(hs + c), xf);
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-        }
+        for (int c = lane * PER; c < d; c += 32 * PER)
+          acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hs + c), *reinterpret_cast<const uint4*>(wr + c), acc);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
@@ -561,13 +550,8 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
       float acc = 0.f;
       if (ok) {
         const T* wr = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
-        for (int c = lane * PER; c < d; c += 32 * PER) {
-          float wf[PER], xf[PER];
-          Elem<T>::unpack(*reinterpret_cast<const uint4*>(wr + c), wf);
-          Elem<T>::unpack(*reinterpret_cast<const uint4*>(hr + c), xf);
-#pragma unroll
-          for (int e = 0; e < PER; ++e) acc = fmaf(xf[e], wf[e], acc);
-        }
+        for (int c = lane * PER; c < d; c += 32 * PER)
+          acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hr + c), *reinterpret_cast<const uint4*>(wr + c), acc);
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);

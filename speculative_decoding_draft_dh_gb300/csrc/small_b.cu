@@ -205,14 +205,8 @@ __global__ void __launch_bounds__(PV_THREADS) k_proj_vec(ProjSmall p) {
     for (int q = 0; q < PV_LOADS; ++q) {
       const int row = base + q * rpp + grp;
       if (row < i1) {
-        float x[VEC];
-        Elem<T>::unpack(u[q], x);
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-          const float hv = Elem<T>::to_f(h[(size_t)b * p.d + row]);
-#pragma unroll
-          for (int e = 0; e < VEC; ++e) acc[b][e] = fmaf(hv, x[e], acc[b][e]);
-        }
+        for (int b = 0; b < NB; ++b) Elem<T>::axpy16(Elem<T>::scalar_of(h[(size_t)b * p.d + row]), u[q], acc[b]);
       }
     }
   }
@@ -405,7 +399,7 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
   static_assert(TW * (int)sizeof(T) == LSU_SEG, "a tile row is one 512-byte segment");
   static_assert(LSU_WARPS * NB * TW * 4 <= LSU_WARPS * LSU_SROWS * LSU_SEG, "partial sums fit the staging area");
   __shared__ __align__(128) unsigned char vs[LSU_WARPS][LSU_SROWS][LSU_SEG];
-  __shared__ float st[MAX_BR];
+  __shared__ typename Elem<T>::Scalar st[MAX_BR];  // t, in the form axpy16 takes
   __shared__ uint64_t vbar[LSU_WARPS];
   __shared__ int s_fail;
   float(*part)[NB][TW] = reinterpret_cast<float(*)[NB][TW]>(&vs[0][0][0]);
@@ -439,7 +433,7 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
   // the selection kernel may launch now (it waits for this grid's records itself)
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // t comes from the projection kernel
-  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = acc_to_t<T>(p.acc, BR, e);
+  for (int e = threadIdx.x; e < BR; e += blockDim.x) st[e] = Elem<T>::scalar(acc_to_t<T>(p.acc, BR, e));
   __syncthreads();
   float acc[NB][PER];
 #pragma unroll
@@ -447,14 +441,8 @@ __global__ void __launch_bounds__(LSU_WARPS * 32) k_scores_lsu(const T* __restri
 #pragma unroll
     for (int e = 0; e < PER; ++e) acc[b][e] = 0.f;
   auto fma_row = [&](const uint4& u, int j) {
-    float x[PER];
-    Elem<T>::unpack(u, x);
 #pragma unroll
-    for (int b = 0; b < NB; ++b) {
-      const float tb = st[b * r + j];
-#pragma unroll
-      for (int e = 0; e < PER; ++e) acc[b][e] = fmaf(tb, x[e], acc[b][e]);
-    }
+    for (int b = 0; b < NB; ++b) Elem<T>::axpy16(st[b * r + j], u, acc[b]);
   };
 #pragma unroll
   for (int q = 0; q < LSU_BATCH; ++q)
