@@ -16,6 +16,7 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 int g_sms[kMaxDevices];
+long long g_l2[kMaxDevices];
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned256(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
@@ -33,7 +34,7 @@ struct TopkLayout {
 
 TopkLayout topk_layout(int B, int d, int r, int vocab) {
   TopkLayout L;
-  Ctx dummy{0, 0, nullptr};
+  Ctx dummy{0, 0, 0, nullptr};
   L.nsplit = proj_splits(dummy, B, d, r);
   const size_t n_groups = (size_t)(vocab + GROUP - 1) / GROUP;
   // state that must be zero between calls sits at fixed offsets, so that a call with other
@@ -109,12 +110,18 @@ bool get_ctx(void* stream, Ctx* ctx) {
   ctx->stream = static_cast<cudaStream_t>(stream);
   if (dev < kMaxDevices && g_sms[dev] > 0) {
     ctx->num_sms = g_sms[dev];
+    ctx->l2_bytes = g_l2[dev];
     return true;
   }
-  int sms = 0;
+  int sms = 0, l2 = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return false;
-  if (dev < kMaxDevices) g_sms[dev] = sms;
+  if (cudaDeviceGetAttribute(&l2, cudaDevAttrL2CacheSize, dev) != cudaSuccess) return false;
+  if (dev < kMaxDevices) {
+    g_l2[dev] = l2;
+    g_sms[dev] = sms;
+  }
   ctx->num_sms = sms;
+  ctx->l2_bytes = l2;
   return true;
 }
 
@@ -244,7 +251,7 @@ int run_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, 
                       "rescore (sweep)") == cudaSuccess
                ? DH_OK
                : DH_ERR_CUDA;
-  const bool ring_ok = rescore_ring_used(1 << 20, 1, d, dtype);  // shape fits the ring's shared memory
+  const bool ring_ok = rescore_ring_fits(K, d, dtype);  // shape fits the ring's shared memory
   bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
   if (f == Tuning::RESCORE_DIRECT || f == Tuning::RESCORE_TICKET) ring = false;
   if (f == Tuning::RESCORE_RING) ring = ring_ok;

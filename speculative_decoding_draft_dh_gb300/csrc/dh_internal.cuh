@@ -214,19 +214,25 @@ template <> struct Elem<__nv_bfloat16> {
 // Softmax over z[0..K) by one warp (lane i takes elements i, i + 32, ...; max and sum by xor
 // shuffles, so every lane gets the same values): out[k] = exp(z[k] - max) / sum.  For the small
 // K of the cluster kernels this avoids a block barrier per reduction.
-__device__ __forceinline__ void warp_softmax(const float* z, int K, float* out) {
+// Every kernel that computes probabilities uses this one order, so that all stage-2 paths agree
+// bit for bit.  With L2 set, z is global memory written by other blocks and is read through L2.
+template <bool L2>
+__device__ __forceinline__ void warp_softmax_impl(const float* z, int K, float* out) {
   const int lane = threadIdx.x & 31;
+  auto ld = [&](int i) { return L2 ? __ldcg(z + i) : z[i]; };
   float m = -INFINITY;
-  for (int i = lane; i < K; i += 32) m = fmaxf(m, z[i]);
+  for (int i = lane; i < K; i += 32) m = fmaxf(m, ld(i));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
   float ssum = 0.f;
-  for (int i = lane; i < K; i += 32) ssum += expf(z[i] - m);
+  for (int i = lane; i < K; i += 32) ssum += expf(ld(i) - m);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
   const float inv = 1.f / ssum;
-  for (int i = lane; i < K; i += 32) out[i] = expf(z[i] - m) * inv;
+  for (int i = lane; i < K; i += 32) out[i] = expf(ld(i) - m) * inv;
 }
+__device__ __forceinline__ void warp_softmax(const float* z, int K, float* out) { warp_softmax_impl<false>(z, K, out); }
+__device__ __forceinline__ void warp_softmax_l2(const float* z, int K, float* out) { warp_softmax_impl<true>(z, K, out); }
 
 // Element e of t from the fixed-point accumulator copies (copy q at acc + q*BR), rounded to the
 // activation dtype.  The integer sum is exact and order independent, so every reader derives the
@@ -265,6 +271,7 @@ const Tuning& tuning();
 struct Ctx {
   int device;
   int num_sms;
+  long long l2_bytes;
   cudaStream_t stream;
 };
 
@@ -328,6 +335,7 @@ bool rescore_sweep_supported(int B, int K, int d, int vocab, int dtype, int num_
 cudaError_t launch_rescore_sweep(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                  int vocab, int K, int dtype, float* logits, float* probs, int* status);
 bool rescore_ring_used(int B, int K, int d, int dtype);
+bool rescore_ring_fits(int K, int d, int dtype);
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                 int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
                                 int* status);

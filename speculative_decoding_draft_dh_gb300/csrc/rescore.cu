@@ -1,4 +1,3 @@
-#include <algorithm>
 // Stage 2: exact full-rank logits of the retrieved candidates and their softmax.
 //
 // EAGLE-4 summary page, section "Retrieve vocabulary candidates cheaply, then score them exactly":
@@ -9,6 +8,8 @@
 // Gather-GEMV: one warp per (row, candidate) streams W[idx] (d contiguous values) with 16-byte
 // loads against h[row] staged in shared memory, accumulates in fp32 and reduces with shuffles.  An index outside [0, vocab)
 // is never dereferenced: its logit becomes NaN (and so do the row's probabilities).
+#include <algorithm>
+#include <climits>
 #include <cstdlib>
 #include <cstring>
 
@@ -61,8 +62,6 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h,
   constexpr int PER = Elem<T>::PER16;
   extern __shared__ __align__(16) unsigned char smem_raw[];
   T* sh_h = reinterpret_cast<T*>(smem_raw);
-  __shared__ float red[NWARP];
-  __shared__ float s_bcast;
   __shared__ int s_last;
   const int kblocks = (K + NWARP - 1) / NWARP;
   const int b = blockIdx.x / kblocks, kb = blockIdx.x % kblocks;
@@ -90,37 +89,9 @@ __global__ void __launch_bounds__(NWARP * 32) k_rescore(const T* __restrict__ h,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  // softmax over the row's K logits (written by other blocks: read through L2)
-  const float* z = logits + (size_t)b * K;
-  float m = -INFINITY;
-  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) m = fmaxf(m, __ldcg(z + i));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int i = 1; i < NWARP; ++i) mm = fmaxf(mm, red[i]);
-    s_bcast = mm;
-  }
-  __syncthreads();
-  m = s_bcast;
-  float ssum = 0.f;
-  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) ssum += expf(__ldcg(z + i) - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = ssum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < NWARP; ++i) tot += red[i];
-    s_bcast = 1.f / tot;
-    tickets[b] = 0u;
-  }
-  __syncthreads();
-  const float inv = s_bcast;
-  for (int i = threadIdx.x; i < K; i += (NWARP * 32)) probs[(size_t)b * K + i] = expf(__ldcg(z + i) - m) * inv;
+  // softmax over the row's K logits (written by other blocks: read through L2), by one warp
+  if (warp == 0) warp_softmax_l2(logits + (size_t)b * K, K, probs + (size_t)b * K);
+  if (threadIdx.x == 0) tickets[b] = 0u;
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -228,125 +199,179 @@ cudaError_t run_cl(const Ctx& c, const void* h, const void* W, const int32_t* id
 }
 
 // ------------------------------------------------------------------------------------------------
-// Ring variant for larger batches: block (b, chunk) scores RING_PAIRS candidates of row b.  h[b]
-// is bulk-copied into shared memory once (before waiting on the previous kernel); a producer warp
-// resolves the chunk's ids and keeps RING_SLOTS W rows in flight in a shared-memory ring with 1-D
-// bulk copies (cp.async.bulk); eight consumer warps take the slots in turn.  With two blocks per
-// SM that is 160 KB in flight per SM at d = 5120 bf16, independent of the consumers' latency.
+// Ring variant for larger batches.  Block (c, b) scores a share of row b's candidates:
+// - bucket mode (bw > 0, when the gathered rows exceed what L2 keeps): the vocabulary is cut into
+//   buckets of bw consecutive ids and the share is the candidates whose ids fall in bucket c.
+//   Blocks are numbered bucket by bucket, so the blocks running at any time gather W rows from one
+//   or two buckets: a W row that several rows of the batch selected is read from HBM by the first
+//   of them and found in L2 by the others.  Warp 0 lists the bucket's candidates;
+// - chunk mode (bw = 0): the share is candidates [RING_CHUNK c, RING_CHUNK (c + 1)).
+// h[b] is bulk-copied into shared memory once (before waiting on the previous kernel).  Each of
+// the NW warps gathers the W rows of its part of the share itself, one at a time, with a 1-D bulk
+// copy (cp.async.bulk) into a slot of its own.  The copy engine serves one issuing thread at about
+// 45 GB/s, so every warp issues; with small blocks, several of them per SM, the copies of one
+// block run while another starts.  An id outside [0, vocab) belongs to bucket 0 and is never
+// dereferenced.
 
-constexpr int RING_CONSUMERS = 8;
-constexpr int RING_THREADS = (RING_CONSUMERS + 1) * 32;
-constexpr int RING_SLOTS = 8;
-constexpr int RING_PAIRS = 32;
+constexpr int RING_WARPS_BUCKET = 4;   // warps per block in bucket mode (four blocks per SM)
+constexpr int RING_WARPS_CHUNK = 8;    // warps per block in chunk mode (two blocks per SM)
+constexpr int RING_CHUNK = 32;         // candidates per block in chunk mode
+constexpr int RING_BUCKET_PAIRS = 32;  // candidates per block on average in bucket mode
+constexpr int RING_SORT = 64;          // bucket lists up to this long are put in id order
+constexpr int RING_MAX_K = 4096;       // the bucket's list holds up to a whole row
 constexpr uint64_t RING_WAIT_NS = 2000000000ull;
 
-template <typename T>
-__global__ void __launch_bounds__(RING_THREADS, 2)
-    k_rescore_ring(const T* __restrict__ h, const T* __restrict__ W, const int32_t* __restrict__ idx, int d,
-                   int vocab, int K, float* __restrict__ logits, float* __restrict__ probs,
+inline size_t ring_smem(int K, int d, int elem, int nw) {
+  const size_t row = (size_t)d * elem;
+  return 128 + align_up(row, 128) + (size_t)nw * row + (size_t)K * sizeof(int2);
+}
+
+template <typename T, int NW>
+__global__ void __launch_bounds__(NW * 32)
+    k_rescore_ring(const T* __restrict__ h, const T* __restrict__ W, const int32_t* __restrict__ idx, int B, int d,
+                   int vocab, int K, int bw, float* __restrict__ logits, float* __restrict__ probs,
                    uint32_t* __restrict__ tickets, int* __restrict__ status) {
   using namespace sm100;
-  constexpr int PER = Elem<T>::PER16;
+  constexpr int RING_WARPS = NW, RING_THREADS = NW * 32, RING_WSLOTS = 1;
   extern __shared__ unsigned char smem_raw[];
-  __shared__ uint64_t h_full, full[RING_SLOTS], empty[RING_SLOTS];
-  __shared__ int slot_k[RING_SLOTS], slot_ok[RING_SLOTS];
-  __shared__ float red[RING_THREADS / 32];
-  __shared__ float s_bcast;
-  __shared__ int s_last;
+  __shared__ uint64_t h_full, full[RING_WARPS][RING_WSLOTS];
+  __shared__ int s_last, s_n;
   __shared__ volatile int s_fail;
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 127) &
                                                          ~static_cast<uintptr_t>(127));
   const uint32_t row_bytes = (uint32_t)d * sizeof(T);
   const T* hs = reinterpret_cast<const T*>(base);
   unsigned char* ring = base + align_up(row_bytes, 128);
-  const int nchunks = (K + RING_PAIRS - 1) / RING_PAIRS;
-  const int b = blockIdx.x / nchunks, k0 = (blockIdx.x % nchunks) * RING_PAIRS;
-  const int n_here = min(RING_PAIRS, K - k0);
+  int2* list = reinterpret_cast<int2*>(ring + (size_t)RING_WARPS * RING_WSLOTS * row_bytes);  // (k, id)
+  const int c = blockIdx.x / B, b = blockIdx.x % B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
     s_fail = 0;
     mbar_init(&h_full, 1);
-    for (int s = 0; s < RING_SLOTS; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
+    for (int w = 0; w < RING_WARPS; ++w)
+      for (int s = 0; s < RING_WSLOTS; ++s) mbar_init(&full[w][s], 1);
     fence_barrier_init();
+    // h does not depend on the previous kernel
+    mbar_arrive_expect_tx(&h_full, row_bytes);
+    bulk_load(base, h + (size_t)b * d, row_bytes, &h_full);
   }
-  __syncthreads();
-  if (warp == RING_CONSUMERS) {
-    // ------------------------------------------------------------ producer warp
-    if (lane == 0) {  // h does not depend on the previous kernel
-      mbar_arrive_expect_tx(&h_full, row_bytes);
-      bulk_load(base, h + (size_t)b * d, row_bytes, &h_full);
-    }
+  if (bw > 0 && warp == 0) {
+    // the row's candidates in bucket c, in candidate order
     asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
-    const int v = lane < n_here ? idx[(size_t)b * K + k0 + lane] : -1;
-    for (int i = 0; i < n_here && !s_fail; ++i) {
-      const int vi = __shfl_sync(0xFFFFFFFFu, v, i);
-      if (lane == 0) {
-        const int s = i % RING_SLOTS;
-        if (!mbar_wait(&empty[s], ((uint32_t)(i / RING_SLOTS) & 1u) ^ 1u, RING_WAIT_NS)) {
-          s_fail = 1;
-          atomicOr(status, 1 << DH_ERR_TIMEOUT);
-        } else {
-          const bool ok = vi >= 0 && vi < vocab;
-          slot_k[s] = k0 + i;
-          slot_ok[s] = ok;
-          if (ok) {
-            mbar_arrive_expect_tx(&full[s], row_bytes);
-            bulk_load(ring + (size_t)s * row_bytes, W + (size_t)vi * d, row_bytes, &full[s]);
-          } else {
-            mbar_arrive(&full[s]);
-          }
-        }
-      }
-      __syncwarp();
-    }
-  } else {
-    // ------------------------------------------------------------ consumer warps
-    const bool h_ok = __all_sync(0xFFFFFFFFu, mbar_wait(&h_full, 0, RING_WAIT_NS));
-    if (!h_ok) {
-      if (lane == 0) atomicOr(status, 1 << DH_ERR_TIMEOUT);
-      s_fail = 1;
-    }
-    for (int i = warp; h_ok && i < n_here; i += RING_CONSUMERS) {
-      const int s = i % RING_SLOTS;
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[s], (uint32_t)(i / RING_SLOTS) & 1u, RING_WAIT_NS))) {
-        if (lane == 0) atomicOr(status, 1 << DH_ERR_TIMEOUT);
-        s_fail = 1;
-        break;
-      }
-      const int k = slot_k[s];
-      const bool ok = slot_ok[s] != 0;
-      float acc = 0.f;
-      if (ok) {
-        const T* wr = reinterpret_cast<const T*>(ring + (size_t)s * row_bytes);
-        for (int c = lane * PER; c < d; c += 32 * PER)
-          acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hs + c), *reinterpret_cast<const uint4*>(wr + c), acc);
+    const int32_t* ib = idx + (size_t)b * K;
+    int cnt = 0;
+    for (int k0 = 0; k0 < K; k0 += 8 * 32) {
+      int vv[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * 32 + lane;
+        vv[u] = k < K ? ib[k] : 0;
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
-      __syncwarp();
-      if (lane == 0) {
-        logits[(size_t)b * K + k] = ok ? acc : __int_as_float(0x7FC00000);
-        mbar_arrive(&empty[s]);  // the slot is free once the warp has read it
+      for (int u = 0; u < 8; ++u) {
+        const int k = k0 + u * 32 + lane;
+        const int v = vv[u];
+        const bool in = k < K && ((v >= 0 && v < vocab) ? v / bw : 0) == c;
+        const uint32_t m = __ballot_sync(0xFFFFFFFFu, in);
+        if (in) list[cnt + __popc(m & ((1u << lane) - 1u))] = make_int2(k, v);
+        cnt += __popc(m);
       }
     }
+    if (cnt <= RING_SORT) {
+      // a short list goes into id order (ranked by counting; the keys are distinct), so that the
+      // blocks sweep their buckets from low to high ids at about the same pace
+      __syncwarp();
+      auto key = [&](int i) {
+        return i < cnt ? (long long)list[i].y * 4294967296LL + (long long)(uint32_t)list[i].x : LLONG_MAX;
+      };
+      const long long k0 = key(lane), k1 = key(lane + 32);
+      const int2 e0 = lane < cnt ? list[lane] : make_int2(0, 0);
+      const int2 e1 = lane + 32 < cnt ? list[lane + 32] : make_int2(0, 0);
+      int r0 = 0, r1 = 0;
+      for (int q = 0; q < 32; ++q) {
+        const long long a = __shfl_sync(0xFFFFFFFFu, k0, q), a1 = __shfl_sync(0xFFFFFFFFu, k1, q);
+        r0 += (a < k0) + (a1 < k0);
+        r1 += (a < k1) + (a1 < k1);
+      }
+      __syncwarp();
+      if (lane < cnt) list[r0] = e0;
+      if (lane + 32 < cnt) list[r1] = e1;
+    }
+    if (lane == 0) s_n = cnt;
   }
   __syncthreads();
-  if (s_fail) {
-    // let every copy issued into this block's shared memory land before it exits
-    if (threadIdx.x == 0) {
-      mbar_wait(&h_full, 0, RING_WAIT_NS);
-      for (int s = 0; s < RING_SLOTS && s < n_here; ++s) {
-        const int last = s + ((n_here - 1 - s) / RING_SLOTS) * RING_SLOTS;
-        mbar_wait(&full[s], (uint32_t)(last / RING_SLOTS) & 1u, RING_WAIT_NS);
+  if (bw == 0) {
+    // chunk mode: each warp stages the ids of its own candidates
+    asm volatile("griddepcontrol.wait;" ::: "memory");  // idx comes from the previous kernel
+    const int n_chunk = min(RING_CHUNK, K - c * RING_CHUNK);
+    const int i = warp + lane * RING_WARPS;
+    if (i < n_chunk) {
+      const int k = c * RING_CHUNK + i;
+      list[i] = make_int2(k, idx[(size_t)b * K + k]);
+    }
+    __syncwarp();
+  }
+  const int n_here = bw > 0 ? s_n : min(RING_CHUNK, K - c * RING_CHUNK);
+  // this warp's candidates: entries warp, warp + RING_WARPS, ... of the share
+  const int n_mine = n_here > warp ? (n_here - 1 - warp) / RING_WARPS + 1 : 0;
+  unsigned char* mine = ring + (size_t)warp * RING_WSLOTS * row_bytes;
+  auto entry = [&](int j) { return list[warp + j * RING_WARPS]; };  // (k, id) of the warp's j-th candidate
+  auto issue = [&](int j) {  // lane 0: the copy of the warp's j-th candidate into slot j % RING_WSLOTS
+    const int2 kv = entry(j);
+    uint64_t* bar = &full[warp][j % RING_WSLOTS];
+    if (kv.y >= 0 && kv.y < vocab) {
+      mbar_arrive_expect_tx(bar, row_bytes);
+      bulk_load(mine + (size_t)(j % RING_WSLOTS) * row_bytes, W + (size_t)kv.y * d, row_bytes, bar);
+    } else {
+      mbar_arrive(bar);
+    }
+  };
+  int issued = 0, consumed = 0;  // lane 0's counts
+  if (lane == 0)
+    for (; issued < RING_WSLOTS && issued < n_mine; ++issued) issue(issued);
+  bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(&h_full, 0, RING_WAIT_NS));
+  if (!ok && lane == 0) {
+    atomicOr(status, 1 << DH_ERR_TIMEOUT);
+    s_fail = 1;
+  }
+  for (int j = 0; ok && j < n_mine; ++j) {
+    const int s = j % RING_WSLOTS;
+    if (!__all_sync(0xFFFFFFFFu, mbar_wait(&full[warp][s], (uint32_t)(j / RING_WSLOTS) & 1u, RING_WAIT_NS))) {
+      if (lane == 0) {
+        atomicOr(status, 1 << DH_ERR_TIMEOUT);
+        s_fail = 1;
+      }
+      ok = false;
+      break;
+    }
+    consumed = j + 1;
+    const int2 kv = entry(j);
+    const bool valid = kv.y >= 0 && kv.y < vocab;
+    float acc = 0.f;
+    if (valid) {
+      const T* wr = reinterpret_cast<const T*>(mine + (size_t)s * row_bytes);
+      for (int e = lane * Elem<T>::PER16; e < d; e += 32 * Elem<T>::PER16)
+        acc = Elem<T>::dot16(*reinterpret_cast<const uint4*>(hs + e), *reinterpret_cast<const uint4*>(wr + e), acc);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xFFFFFFFFu, acc, o);
+    __syncwarp();  // every lane has read slot s
+    if (lane == 0) {
+      logits[(size_t)b * K + kv.x] = valid ? acc : __int_as_float(0x7FC00000);
+      if (issued < n_mine) {
+        fence_proxy_async_smem();
+        issue(issued);
+        ++issued;
       }
     }
-    __syncthreads();
-    return;
   }
-  if (!probs) return;
+  if (!ok && lane == 0)  // let this warp's copies in flight land before the block exits
+    for (int j = consumed; j < issued; ++j)
+      mbar_wait(&full[warp][j % RING_WSLOTS], (uint32_t)(j / RING_WSLOTS) & 1u, RING_WAIT_NS);
+  __syncthreads();
+  if (s_fail) return;
+  // (a block with no candidates takes no ticket: the row's count may already have been reset)
+  if (!probs || n_here == 0) return;
   if (threadIdx.x == 0) {
     __threadfence();
     s_last = atomicAdd(&tickets[b], (uint32_t)n_here) + (uint32_t)n_here == (uint32_t)K;
@@ -354,61 +379,47 @@ __global__ void __launch_bounds__(RING_THREADS, 2)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  const float* z = logits + (size_t)b * K;
-  float m = -INFINITY;
-  for (int i = threadIdx.x; i < K; i += RING_THREADS) m = fmaxf(m, __ldcg(z + i));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-  if (lane == 0) red[warp] = m;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float mm = red[0];
-    for (int i = 1; i < RING_THREADS / 32; ++i) mm = fmaxf(mm, red[i]);
-    s_bcast = mm;
-  }
-  __syncthreads();
-  m = s_bcast;
-  float ssum = 0.f;
-  for (int i = threadIdx.x; i < K; i += RING_THREADS) ssum += expf(__ldcg(z + i) - m);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
-  __syncthreads();
-  if (lane == 0) red[warp] = ssum;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float tot = 0.f;
-    for (int i = 0; i < RING_THREADS / 32; ++i) tot += red[i];
-    s_bcast = 1.f / tot;
-    tickets[b] = 0u;
-  }
-  __syncthreads();
-  const float inv = s_bcast;
-  for (int i = threadIdx.x; i < K; i += RING_THREADS) probs[(size_t)b * K + i] = expf(__ldcg(z + i) - m) * inv;
+  // softmax over the row's K logits (written by other blocks: read through L2), by one warp
+  if (warp == 0) warp_softmax_l2(logits + (size_t)b * K, K, probs + (size_t)b * K);
+  if (threadIdx.x == 0) tickets[b] = 0u;
+}
+
+template <typename T, int NW>
+cudaError_t launch_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
+                        int nbk, int bw, float* logits, float* probs, uint32_t* tickets, int* status) {
+  static unsigned long long smem_done = 0;
+  cudaError_t e = allow_max_smem(k_rescore_ring<T, NW>, c.device, &smem_done);
+  if (e != cudaSuccess) return e;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)(B * nbk));
+  cfg.blockDim = dim3(NW * 32);
+  cfg.dynamicSmemBytes = ring_smem(K, d, (int)sizeof(T), NW);
+  cfg.stream = c.stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  prof_before("rescore_ring", c.stream);
+  e = cudaLaunchKernelEx(&cfg, k_rescore_ring<T, NW>, static_cast<const T*>(h), static_cast<const T*>(W), idx, B, d,
+                         vocab, K, bw, logits, probs, tickets, status);
+  prof_after(c.stream);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
                      float* logits, float* probs, uint32_t* tickets, int* status) {
-  static unsigned long long smem_done = 0;
-  cudaError_t e = allow_max_smem(k_rescore_ring<T>, c.device, &smem_done);
-  if (e != cudaSuccess) return e;
-  const size_t row_bytes = (size_t)d * sizeof(T);
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((unsigned)(B * ((K + RING_PAIRS - 1) / RING_PAIRS)));
-  cfg.blockDim = dim3(RING_THREADS);
-  cfg.dynamicSmemBytes = 128 + align_up(row_bytes, 128) + RING_SLOTS * row_bytes;
-  cfg.stream = c.stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  prof_before("rescore_ring", c.stream);
-  e = cudaLaunchKernelEx(&cfg, k_rescore_ring<T>, static_cast<const T*>(h), static_cast<const T*>(W), idx, d, vocab,
-                         K, logits, probs, tickets, status);
-  prof_after(c.stream);
-  if (e != cudaSuccess) return e;
-  return cudaGetLastError();
+  // bucket mode once the gathered rows are larger than L2; chunk mode below
+  if ((double)B * K * d * sizeof(T) > (double)c.l2_bytes) {
+    const int nbk0 = std::max(1, std::min(K / RING_BUCKET_PAIRS, vocab));
+    const int bw = (vocab + nbk0 - 1) / nbk0;
+    return launch_ring<T, RING_WARPS_BUCKET>(c, h, W, idx, B, d, vocab, K, (vocab + bw - 1) / bw, bw, logits, probs,
+                                             tickets, status);
+  }
+  return launch_ring<T, RING_WARPS_CHUNK>(c, h, W, idx, B, d, vocab, K, (K + RING_CHUNK - 1) / RING_CHUNK, 0, logits,
+                                          probs, tickets, status);
 }
 
 // Sweep variant for large batches: block j owns SW_ROWS batch rows, keeps their h rows in shared
@@ -576,19 +587,7 @@ __global__ void __launch_bounds__(SW_THREADS, 1)
     return;
   }
   // the softmax of each owned row, one warp per row (the logits were written by this block)
-  if (probs && warp < nrows) {
-    const float* z = logits + (size_t)(b0 + warp) * K;
-    float m = -INFINITY;
-    for (int i = lane; i < K; i += 32) m = fmaxf(m, __ldcg(z + i));
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-    float ssum = 0.f;
-    for (int i = lane; i < K; i += 32) ssum += expf(__ldcg(z + i) - m);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ssum += __shfl_xor_sync(0xFFFFFFFFu, ssum, o);
-    const float inv = 1.f / ssum;
-    for (int i = lane; i < K; i += 32) probs[(size_t)(b0 + warp) * K + i] = expf(__ldcg(z + i) - m) * inv;
-  }
+  if (probs && warp < nrows) warp_softmax_l2(logits + (size_t)(b0 + warp) * K, K, probs + (size_t)(b0 + warp) * K);
 }
 
 template <typename T>
@@ -655,9 +654,6 @@ cudaError_t run(const Ctx& c, const void* h, const void* W, const int32_t* idx, 
 
 bool rescore_supported(int d) { return d <= MAX_D_SMEM; }
 
-// The ring variant from this many (row, candidate) pairs on: below it, one warp per pair with all
-// of a row's loads in flight has the lower latency.
-// (It needs RING_SLOTS + 1 rows of shared memory: up to d = 11264 bf16 or 5632 fp32.)
 bool rescore_sweep_supported(int B, int K, int d, int vocab, int dtype, int num_sms) {
   const int elem = dtype == DH_BF16 ? 2 : 4;
   const int rows = sweep_rows(B, num_sms);
@@ -670,9 +666,17 @@ cudaError_t launch_rescore_sweep(const Ctx& c, const void* h, const void* W, con
   return run_sweep<float>(c, h, W, idx, B, d, vocab, K, logits, probs, status);
 }
 
+// The ring needs up to RING_WARPS_CHUNK + 1 rows of shared memory and the share's list (K
+// entries): at K = 256 up to d = 11256 bf16 or 5628 fp32.
+bool rescore_ring_fits(int K, int d, int dtype) {
+  const int elem = dtype == DH_BF16 ? 2 : 4;
+  return K <= RING_MAX_K && ring_smem(K, d, elem, std::max(RING_WARPS_CHUNK, RING_WARPS_BUCKET)) <= 200 * 1024;
+}
+
+// The ring variant from this many (row, candidate) pairs on: below it, one warp per pair with all
+// of a row's loads in flight has the lower latency.
 bool rescore_ring_used(int B, int K, int d, int dtype) {
-  const size_t row = (size_t)d * (dtype == DH_BF16 ? 2 : 4);
-  return (long long)B * K >= 2048 && (RING_SLOTS + 1) * row + 256 <= 200 * 1024;
+  return (long long)B * K >= 2048 && rescore_ring_fits(K, d, dtype);
 }
 
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,

@@ -211,6 +211,29 @@ def test_rescore_paths_small_shapes(path, tune):
     assert dh.workspace_status() == 0
 
 
+def test_rescore_paths_agree_bit_for_bit(tune):
+    """Every stage-2 kernel gives the same logits and probabilities bit for bit: one dot-product
+    order and one softmax order, whatever the kernel (cluster, ticket, bucketed ring, sweep); on
+    rows whose candidates spread over the vocabulary and on rows that all fall in one bucket."""
+    cfgs = (inputs.head_config("tiny", B=3, K=45), inputs.HeadConfig("r", 5, 768, 4096, 64, 70, "bf16", 0.1, True),
+            inputs.HeadConfig("rr", 40, 512, 4096, 64, 256, "bf16", 0.1, True))
+    for cfg in cfgs:
+        x = inputs.make_head(cfg, seed=23, device=DEV)
+        idx, _ = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
+        idx_lo = torch.sort(idx % 700, dim=1).values.contiguous()  # every row's ids in the lowest bucket
+        for ids in (idx, idx_lo):
+            outs = {}
+            for path in ("direct", "ring", "ticket", "sweep"):
+                tune("DH_FORCE_RESCORE", path)
+                outs[path] = dh.exact_rescore(x["h"], x["W"], ids)
+            torch.cuda.synchronize()
+            lg0, pr0 = outs["direct"]
+            for path, (lg, pr) in outs.items():
+                assert torch.equal(lg, lg0), (cfg.name, path)
+                assert torch.equal(pr, pr0), (cfg.name, path)
+    assert dh.workspace_status() == 0
+
+
 def test_rescore_without_probs():
     cfg = inputs.head_config("tiny", B=2)
     x = inputs.make_head(cfg, seed=0, device=DEV)
