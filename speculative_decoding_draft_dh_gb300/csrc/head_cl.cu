@@ -100,15 +100,6 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
                : "memory");
 }
 
-// A group record read through L2 (not L1).
-__device__ __forceinline__ GroupRec ld_cg_rec(const GroupRec* r) {
-  const float4 v = __ldcg(reinterpret_cast<const float4*>(r));
-  GroupRec g;
-  static_assert(sizeof(GroupRec) == 16, "a record is one 16-byte vector");
-  memcpy(&g, &v, sizeof g);
-  return g;
-}
-
 __device__ __forceinline__ unsigned long long pack(uint32_t key, uint32_t id) {
   return ((unsigned long long)key << 32) | (unsigned long long)(~id);
 }
@@ -183,6 +174,11 @@ struct FastShared {
   uint64_t wbar[HC_WARPS];  // each warp's first winner's W row, bulk-copied into the selection area
 };
 
+// 16-byte asynchronous copy global -> shared, read through L2 (completed by cp.async.wait_all).
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sm100::smem_u32(dst)), "l"(src) : "memory");
+}
+
 // Bounded wait for a bulk copy into shared memory; a copy that does not land in time raises
 // DH_ERR_TIMEOUT in the status word, and the thread waits once more so that the copy has landed
 // (or the second limit has passed) before the CTA reuses or releases the memory.
@@ -205,8 +201,9 @@ __device__ __forceinline__ bool wait_copy(uint64_t* bar, int* status) {
 //     theta' = lo + bb 2^sh <= theta.  The K groups whose bests reach theta put K pool entries at
 //     or above theta', so every entry of the pool's top K is at or above theta', and only groups
 //     whose best reaches theta' (the candidate groups: about K) hold such entries.
-//  3. The candidate groups' records are read (through L2); their entries at or above theta' are
-//     collected (their W rows start towards L2, each group's by one CTA) and ranked by counting,
+//  3. The candidate groups' records (copied into shared memory through L2 as soon as lo is known,
+//     for every group whose best reaches lo, while the histogram is built): their entries at or
+//     above theta' are collected (their W rows start towards L2, each group's by one CTA) and ranked by counting,
 //     which also orders the K winners.  Certificate: a group whose third score reaches tau (the
 //     K-th winner's) may hide a member of the top K; only a candidate group can (its third score is
 //     at most its best).
@@ -237,6 +234,15 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
   }
   lo = max(__reduce_min_sync(0xFFFFFFFFu, lo), 1u);  // key 0 marks an empty group
   hi = __reduce_max_sync(0xFFFFFFFFu, hi);
+  // the records of the groups whose bests reach lo (every candidate group among them; about a
+  // tenth of the row) start towards the selection area now, indexed by group, while the
+  // histogram is built
+  GroupRec* recs_s = reinterpret_cast<GroupRec*>(slots);
+#pragma unroll
+  for (int q = 0; q < HC_GK; ++q) {
+    const int g = (int)threadIdx.x + q * HC_THREADS;
+    if (y[q] && y[q] >= lo) cp_async16(&recs_s[g], rrow + g);
+  }
   // ---- 2. histogram of the keys in [lo, hi], bins of 2^sh keys
   const uint32_t span = hi >= lo ? hi - lo : 0u;
   const int sh = max(0, (32 - __clz((int)span)) - HC_FBITS);
@@ -306,11 +312,12 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
   }
   const uint32_t n_cg = total;
   bool fall = !ok || n_cg > (uint32_t)HC_CG;
+  asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (!fall) {
     for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) {
       const int g = fs.cg[i];
-      const GroupRec r = ld_cg_rec(rrow + g);
+      const GroupRec r = recs_s[g];
       fs.cm3[i] = fkey(r.m3);
       const uint32_t o1 = r.offs & 0xFFu, o2 = (r.offs >> 8) & 0xFFu;
       const uint32_t k2 = o2 != NO_OFFSET ? fkey(r.m2) : 0u;
@@ -353,6 +360,7 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
     const int v = (int)(~(uint32_t)my.sp[k_first]);
     slotted = v >= 0 && v < p.vocab;
     if (slotted && lane == 0) {
+      sm100::fence_proxy_async_smem();  // the records read from this area are done with (barriers above)
       sm100::mbar_arrive_expect_tx(&fs.wbar[warp], row_bytes);
       sm100::bulk_load(slots + (size_t)warp * p.d, static_cast<const T*>(p.W) + (size_t)v * p.d, row_bytes,
                        &fs.wbar[warp]);
