@@ -316,9 +316,10 @@ def path_ideal(cfg, unique_rows, peaks):
             "stage2_bytes_unique_rows": s2_bytes, "ideal_us": (t1 + t2) * 1e6}
 
 
-def kernel_algo(cfg, name, peaks):
+def kernel_algo(cfg, name, peaks, unique_rows=None):
     """(bound, algorithmic work per launch, unit) of a head kernel: HBM bytes the step must move,
-    or tensor FLOPs of the dense contraction when those take longer at the peaks."""
+    or tensor FLOPs of the dense contraction when those take longer at the peaks.  The rescoring
+    kernels are charged at the distinct W rows of the step (unique_rows; all B*K when not given)."""
     e = 2 if cfg.dtype == "bf16" else 4
     if name in ("scores_small", "scores_lsu", "scores_summary"):
         return "hbm", cfg.r * cfg.vocab * e + cfg.B * cfg.r * e, "GB/s"
@@ -335,7 +336,8 @@ def kernel_algo(cfg, name, peaks):
     if name == "head_cluster":  # records read once, the candidates' W rows, h
         return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16 + cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name in ("rescore", "rescore_ring", "rescore_cluster"):
-        return "hbm", cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
+        rows = cfg.B * cfg.K if unique_rows is None else unique_rows
+        return "hbm", rows * cfg.d * e + cfg.B * cfg.d * e, "GB/s"
     if name == "select":
         return "hbm", cfg.B * ((cfg.vocab + 63) // 64) * 16, "GB/s"
     if name == "size_level":  # the children in, the next frontier out
@@ -344,8 +346,8 @@ def kernel_algo(cfg, name, peaks):
     return "hbm", 0, "GB/s"
 
 
-def kernel_roofline(cfg, name, stages, peaks, peak_src, workload):
-    bound, algo, unit = kernel_algo(cfg, name, peaks)
+def kernel_roofline(cfg, name, stages, peaks, peak_src, workload, unique_rows=None):
+    bound, algo, unit = kernel_algo(cfg, name, peaks, unique_rows)
     dur_s = stages[name]["us_avg"] * 1e-6
     if bound == "tensor":
         achieved, peak = algo / dur_s / 1e12, peaks["bf16_tflops"]
@@ -360,6 +362,10 @@ def kernel_roofline(cfg, name, stages, peaks, peak_src, workload):
            "us_per_launch": round(stages[name]["us_avg"], 3), "peak_source": src}
     if traffic and bound == "hbm" and algo:
         out["traffic_over_algorithmic"] = round(traffic / algo, 3)
+    if unique_rows is not None and name in ("rescore", "rescore_ring", "rescore_cluster"):
+        e = 2 if cfg.dtype == "bf16" else 4
+        out["algorithmic_bytes_bk_rows"] = cfg.B * cfg.K * cfg.d * e + cfg.B * cfg.d * e  # every gathered row
+        out["unique_w_rows"] = unique_rows
     return out
 
 
@@ -539,11 +545,11 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warm
     name = ROOFLINE_KERNEL.get(cfg.name)
     if name not in stages:
         name = max(stages, key=lambda k: stages[k]["us_avg"])
-    roofline = kernel_roofline(cfg, name, stages, peaks, peak_src, cfg.name)
+    roofline = kernel_roofline(cfg, name, stages, peaks, peak_src, cfg.name, uniq)
     dom = max(stages, key=lambda k: stages[k]["us_avg"])
     roofline_time_dominant = None
     if dom != name:
-        roofline_time_dominant = kernel_roofline(cfg, dom, stages, peaks, peak_src, cfg.name)
+        roofline_time_dominant = kernel_roofline(cfg, dom, stages, peaks, peak_src, cfg.name, uniq)
 
     ideal = path_ideal(cfg, uniq, peaks)
     hbm = peaks["hbm_gbs"]
