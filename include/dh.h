@@ -380,7 +380,8 @@ int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int
  *   "DH_FORCE_PATH"    "auto" | "gemv" | "mma" | "fused"  stage-1 path, when it supports the shape
  *   "DH_FORCE_HEAD"    "auto" | "split"                  dh_draft_head without the cluster head
  *   "DH_HEAD_CTAS"     "16" | "8" | "4"                  largest cluster of the fused head
- *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket" | "sweep"  stage-2 kernel
+ *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket" | "sweep" | "bucket"  stage-2 kernel
+ *                      ("bucket": the ring kernel in its vocabulary-bucket mode at any size)
  *   "DH_SCORES_SMALL"  "lsu" | "tma"                     small-batch scores kernel
  *   "DH_HEAD_SELECT"   "auto" | "radix"                  fused head: the cooperative radix selection
  *                                                        instead of the group-best threshold

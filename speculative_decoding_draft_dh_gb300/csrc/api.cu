@@ -254,10 +254,10 @@ int run_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, 
   const bool ring_ok = rescore_ring_fits(K, d, dtype);  // shape fits the ring's shared memory
   bool ring = ring_ok && rescore_ring_used(B, K, d, dtype);
   if (f == Tuning::RESCORE_DIRECT || f == Tuning::RESCORE_TICKET) ring = false;
-  if (f == Tuning::RESCORE_RING) ring = ring_ok;
+  if (f == Tuning::RESCORE_RING || f == Tuning::RESCORE_BUCKET) ring = ring_ok;
   const cudaError_t e =
       ring ? note_error(launch_rescore_ring(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets,
-                                            status),
+                                            status, f == Tuning::RESCORE_BUCKET),
                         "rescore (ring)")
            : note_error(launch_rescore(c, h, W, idx, B, d, vocab, K, dtype, logits_out, probs_out, tickets), "rescore");
   return e == cudaSuccess ? DH_OK : DH_ERR_CUDA;

@@ -258,7 +258,7 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 // dh_set_tuning.  They select kernels; results do not depend on them.
 struct Tuning {
   enum Path { PATH_AUTO, PATH_GEMV, PATH_MMA, PATH_FUSED };
-  enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET, RESCORE_SWEEP };
+  enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET, RESCORE_SWEEP, RESCORE_BUCKET };
   Path force_path = PATH_AUTO;      // stage-1 path, when the forced one supports the shape
   bool head_split = false;          // dh_draft_head: the two calls' kernels, not the cluster head
   int head_ctas_max = 16;           // largest cluster of the fused head (16, 8 or 4)
@@ -338,7 +338,7 @@ bool rescore_ring_used(int B, int K, int d, int dtype);
 bool rescore_ring_fits(int K, int d, int dtype);
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                 int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
-                                int* status);
+                                int* status, bool force_buckets = false);
 cudaError_t launch_rescore(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B,
                            int d, int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets);
 

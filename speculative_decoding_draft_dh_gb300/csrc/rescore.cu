@@ -410,9 +410,9 @@ cudaError_t launch_ring(const Ctx& c, const void* h, const void* W, const int32_
 
 template <typename T>
 cudaError_t run_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d, int vocab, int K,
-                     float* logits, float* probs, uint32_t* tickets, int* status) {
-  // bucket mode once the gathered rows are larger than L2; chunk mode below
-  if ((double)B * K * d * sizeof(T) > (double)c.l2_bytes) {
+                     float* logits, float* probs, uint32_t* tickets, int* status, bool force_buckets) {
+  // bucket mode once the gathered rows are larger than L2 (or when asked for); chunk mode below
+  if (force_buckets || (double)B * K * d * sizeof(T) > (double)c.l2_bytes) {
     const int nbk0 = std::max(1, std::min(K / RING_BUCKET_PAIRS, vocab));
     const int bw = (vocab + nbk0 - 1) / nbk0;
     return launch_ring<T, RING_WARPS_BUCKET>(c, h, W, idx, B, d, vocab, K, (vocab + bw - 1) / bw, bw, logits, probs,
@@ -681,9 +681,10 @@ bool rescore_ring_used(int B, int K, int d, int dtype) {
 
 cudaError_t launch_rescore_ring(const Ctx& c, const void* h, const void* W, const int32_t* idx, int B, int d,
                                 int vocab, int K, int dtype, float* logits, float* probs, uint32_t* tickets,
-                                int* status) {
-  if (dtype == DH_BF16) return run_ring<__nv_bfloat16>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets, status);
-  return run_ring<float>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets, status);
+                                int* status, bool force_buckets) {
+  if (dtype == DH_BF16)
+    return run_ring<__nv_bfloat16>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets, status, force_buckets);
+  return run_ring<float>(c, h, W, idx, B, d, vocab, K, logits, probs, tickets, status, force_buckets);
 }
 
 // The deduplicated path holds a W row in registers (MAXW 16-byte vectors per lane).

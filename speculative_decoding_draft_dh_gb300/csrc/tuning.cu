@@ -50,6 +50,7 @@ bool apply(Tuning& t, const char* name, const char* value) {
     else if (is("ring")) t.rescore = Tuning::RESCORE_RING;
     else if (is("ticket")) t.rescore = Tuning::RESCORE_TICKET;
     else if (is("sweep")) t.rescore = Tuning::RESCORE_SWEEP;
+    else if (is("bucket")) t.rescore = Tuning::RESCORE_BUCKET;  // the ring in bucket mode at any size
     else return false;
     return true;
   }

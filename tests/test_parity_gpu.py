@@ -195,7 +195,7 @@ def test_rescore_bad_index_gives_nan_row():
     assert np.isfinite(lg[0]).all() and np.isfinite(pr[0]).all()
 
 
-@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep"])
+@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep", "bucket"])
 def test_rescore_paths_small_shapes(path, tune):
     """Each stage-2 kernel (direct = the cluster kernel for K <= 128) on fp32 and bf16 rows, K not a
     multiple of the ring's chunk nor of the cluster's warps."""
@@ -223,7 +223,7 @@ def test_rescore_paths_agree_bit_for_bit(tune):
         idx_lo = torch.sort(idx % 700, dim=1).values.contiguous()  # every row's ids in the lowest bucket
         for ids in (idx, idx_lo):
             outs = {}
-            for path in ("direct", "ring", "ticket", "sweep"):
+            for path in ("direct", "ring", "ticket", "sweep", "bucket"):
                 tune("DH_FORCE_RESCORE", path)
                 outs[path] = dh.exact_rescore(x["h"], x["W"], ids)
             torch.cuda.synchronize()
@@ -613,7 +613,7 @@ def test_bounded_waits_time_out_and_leave_the_context_usable():
     run_head(x, cfg.K)
 
 
-@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep"])
+@pytest.mark.parametrize("path", ["direct", "ring", "ticket", "sweep", "bucket"])
 def test_rescore_large_batch_with_repeats(path, tune):
     """Stage 2 on a large batch whose rows draw from a small candidate pool (many repeated W rows),
     with two out-of-range ids; a second call reuses the workspace tickets."""
