@@ -292,8 +292,8 @@ def head_bytes(cfg):
 
 
 def stage1_on_tensor_cores(cfg) -> bool:
-    """The library runs stage 1 on the tensor cores for bf16 batches above three rows."""
-    return cfg.dtype == "bf16" and cfg.B > 3
+    """The library runs stage 1 on the tensor cores for bf16 batches above four rows."""
+    return cfg.dtype == "bf16" and cfg.B > 4
 
 
 def path_ideal(cfg, unique_rows, peaks):

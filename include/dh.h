@@ -88,7 +88,7 @@ const char* dh_last_error(void);
  * idx_out [B x K] int32, score_out [B x K] fp32: device.
  * B = 0 is a no-op.  Limits: r <= DH_MAX_RANK, vocab <= DH_MAX_VOCAB, K <= min(vocab, DH_MAX_K).
  *
- * Precision of t on the small-batch path (bf16 with B <= 3, fp32 with B <= 8, r a multiple of 16):
+ * Precision of t on the small-batch path (bf16 with B <= 4, fp32 with B <= 8, r a multiple of 16):
  * the projection is split over G <= 3 x (SM count) slices of d, each slice summed in fp32 and then
  * added exactly as a 64-bit fixed-point number with 32 fraction bits, so t is bit-identical from
  * call to call.  Range: every slice's partial sum and every |t[b,j]| must stay below 2^31; a slice

@@ -58,9 +58,10 @@ TopkLayout topk_layout(int B, int d, int r, int vocab) {
 }
 
 // Largest batch for the small-batch pipeline when the tensor-core path also applies (measured on
-// the batch-1 shapes through dh_draft_head, us per call, small-batch against tensor-core path:
-// 20.0 / 24.6 at B = 1, 23.1 / 24.8 at B = 2, 26.8 / 24.9 at B = 4, 40.0 / 24.9 at B = 5).
-constexpr int SMALL_MAX_B = 3;
+// the batch-1 shapes through dh_draft_head in CUDA graphs, us per call, small-batch against
+// tensor-core path: 20.0 / 25.5 at B = 3, 22.7 / 26.5 at B = 4, 37.1 / 26.5 at B = 5, 43.6 / 27.1
+// at B = 8; from five rows the scores kernel's registers no longer let four blocks share an SM).
+constexpr int SMALL_MAX_B = 4;
 
 enum Path { PATH_GEMV, PATH_MMA, PATH_FUSED };
 
