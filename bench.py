@@ -958,6 +958,8 @@ def run_verify_bench(a, vcfg, rank, world, local, peaks, peak_src, steps=None, w
                 "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic_bytes_per_launch": logit_bytes,
                 "us_per_launch": round(stages[dom]["us_avg"], 3),
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"}
+    if traffic:
+        roofline["traffic_over_algorithmic"] = round(traffic / logit_bytes, 3)
     in_bytes = logit_bytes + B * L * vcfg.K * 8 + B * L * 8 + B * 4
     ideal_us = in_bytes / (peak * 1e9) * 1e6
     path_roofline = {"rule": "target logits and the draft's inputs read once over the copy bandwidth",
