@@ -228,16 +228,23 @@ int run_records(const Ctx& c, const void* h, const void* U, const void* V, int B
   return DH_OK;
 }
 
+// The selection after the records, one block per row.  tickets (may be null): the rescoring's
+// per-row tickets, which the selection clears for the rescoring that follows in the same call.
+int run_select(const Ctx& c, const Stage1& s1, const void* V, int B, int r, int vocab, int K, int dtype,
+               int32_t* idx_out, float* score_out, uint32_t* tickets = nullptr) {
+  if (note_error(launch_select(c, s1.recs, s1.t, s1.acc, V, B, r, vocab, K, dtype, idx_out, score_out, tickets),
+                 "select") != cudaSuccess)
+    return DH_ERR_CUDA;
+  return DH_OK;
+}
+
 // Stage 1 after validation: projection, scores with group summaries, selection.
 int run_topk(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab, int K,
              int dtype, int32_t* idx_out, float* score_out, char* ws, const TopkLayout& L) {
   Stage1 s1;
   const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
   if (st != DH_OK) return st;
-  if (note_error(launch_select(c, s1.recs, s1.t, s1.acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
-      cudaSuccess)
-    return DH_ERR_CUDA;
-  return DH_OK;
+  return run_select(c, s1, V, B, r, vocab, K, dtype, idx_out, score_out);
 }
 
 // Stage 2 after validation: the ring kernel from 2048 pairs, the direct kernels below.  The
@@ -364,9 +371,11 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
       return DH_ERR_CUDA;
     return DH_OK;
   }
-  if (note_error(launch_select(c, s1.recs, s1.t, s1.acc, V, B, r, vocab, K, dtype, idx_out, score_out), "select") !=
-      cudaSuccess)
-    return DH_ERR_CUDA;
+  // the rescoring's tickets sit after stage 1's layout, which depends on the shape: the selection
+  // clears them for this call
+  const int ss =
+      run_select(c, s1, V, B, r, vocab, K, dtype, idx_out, score_out, reinterpret_cast<uint32_t*>(ws + roff));
+  if (ss != DH_OK) return ss;
   return run_rescore(c, h, W, idx_out, B, d, vocab, K, dtype, logits_out, probs_out,
                      reinterpret_cast<uint32_t*>(ws + roff), reinterpret_cast<int*>(ws));
 }

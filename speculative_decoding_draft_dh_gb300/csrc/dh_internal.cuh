@@ -309,7 +309,7 @@ cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, in
 // the projection's fixed-point accumulators, which the selection then clears).
 cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc,
                           const void* V, int B, int r, int vocab, int K, int dtype, int32_t* idx_out,
-                          float* score_out);
+                          float* score_out, uint32_t* tickets = nullptr);
 
 // Small batches: selection and rescoring in one thread-block cluster per row (head_cl.cu).
 bool head_cluster_supported(int B, int d, int vocab, int K, int dtype);

@@ -15,8 +15,12 @@ __global__ void __launch_bounds__(sel::SEL_THREADS, MINB) k_select(const GroupRe
                                                                const T* __restrict__ t, unsigned long long* acc,
                                                                const T* __restrict__ V, int r, int vocab, int K,
                                                                int32_t* __restrict__ idx_out,
-                                                               float* __restrict__ score_out) {
+                                                               float* __restrict__ score_out,
+                                                               uint32_t* __restrict__ tickets) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
+  // the rescoring kernel that follows counts the row's candidates with a ticket that starts at zero
+  // (where the caller's workspace keeps other calls' data, it may hold anything before)
+  if (tickets && threadIdx.x == 0) tickets[blockIdx.x] = 0u;
   // the rescoring kernel may launch now (it stages h, then waits for this grid's candidates)
   if (MINB == 1) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the previous kernel
@@ -30,7 +34,7 @@ __global__ void __launch_bounds__(sel::SEL_THREADS, MINB) k_select(const GroupRe
 
 template <typename T>
 cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc, const void* V, int B,
-                int r, int vocab, int K, int32_t* idx_out, float* score_out) {
+                int r, int vocab, int K, int32_t* idx_out, float* score_out, uint32_t* tickets) {
   const int n_groups = (vocab + GROUP - 1) / GROUP;
   const size_t smem = sel::select_smem_bytes(n_groups);
   const bool waves = 2 * B > 3 * c.num_sms;
@@ -56,9 +60,9 @@ cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, unsigned long
   cfg.numAttrs = 1;
   prof_before("select", c.stream);
   e = waves ? cudaLaunchKernelEx(&cfg, k_select<T, 2>, recs, static_cast<const T*>(t), acc, static_cast<const T*>(V), r,
-                                 vocab, K, idx_out, score_out)
+                                 vocab, K, idx_out, score_out, tickets)
             : cudaLaunchKernelEx(&cfg, k_select<T, 1>, recs, static_cast<const T*>(t), acc, static_cast<const T*>(V), r,
-                                 vocab, K, idx_out, score_out);
+                                 vocab, K, idx_out, score_out, tickets);
   prof_after(c.stream);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
@@ -68,9 +72,9 @@ cudaError_t run(const Ctx& c, const GroupRec* recs, const void* t, unsigned long
 
 cudaError_t launch_select(const Ctx& c, const GroupRec* recs, const void* t, unsigned long long* acc,
                           const void* V, int B, int r, int vocab, int K, int dtype, int32_t* idx_out,
-                          float* score_out) {
-  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out);
-  return run<float>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out);
+                          float* score_out, uint32_t* tickets) {
+  if (dtype == DH_BF16) return run<__nv_bfloat16>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out, tickets);
+  return run<float>(c, recs, t, acc, V, B, r, vocab, K, idx_out, score_out, tickets);
 }
 
 }  // namespace dh

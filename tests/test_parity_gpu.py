@@ -588,6 +588,27 @@ def test_one_workspace_across_shapes():
     assert dh.workspace_status(ws) == 0
 
 
+def test_draft_head_one_workspace_across_shapes():
+    """dh_draft_head calls of different shapes sharing one workspace: the rescoring's per-row tickets
+    sit after stage 1's layout, which depends on the shape, so a larger call leaves its records where
+    a smaller call keeps its tickets; the smaller call must still give the two calls' outputs."""
+    ws = dh.Workspace()
+    big = inputs.head_config("moderate", B=64, K=128)
+    x = inputs.make_head(big, seed=3, device=DEV)
+    dh.draft_head(x["h"], x["U"], x["V"], x["W"], big.K, workspace=ws)
+    del x
+    for cfg in (inputs.HeadConfig("ring_small", 40, 512, 4096, 64, 64, "bf16", 0.1, True),
+                inputs.HeadConfig("ticket_small", 24, 512, 4096, 64, 160, "bf16", 0.1, True)):
+        y = inputs.make_head(cfg, seed=4, device=DEV)
+        i2, s2, l2, p2 = dh.draft_head(y["h"], y["U"], y["V"], y["W"], cfg.K, workspace=ws)
+        idx, score = dh.lowrank_topk(y["h"], y["U"], y["V"], cfg.K)
+        logits, probs = dh.exact_rescore(y["h"], y["W"], idx)
+        torch.cuda.synchronize()
+        assert torch.equal(i2, idx) and torch.equal(s2, score), cfg.name
+        assert torch.equal(l2, logits) and torch.equal(p2, probs), cfg.name
+    assert dh.workspace_status(ws) == 0
+
+
 def test_repeated_calls_are_identical():
     cfg = inputs.head_config("tiny", B=4)
     x = inputs.make_head(cfg, seed=13, device=DEV)
