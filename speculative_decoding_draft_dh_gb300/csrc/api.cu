@@ -187,12 +187,14 @@ struct Stage1 {
   const void* t;
   unsigned long long* acc;
   GroupRec* recs;
-  const uint32_t* gkeys;  // the groups' best keys (small-batch path), else null
+  const uint32_t* gkeys;  // the groups' best keys (small-batch path, or tensor-core path when asked), else null
 };
 
-// Stage 1 up to the group records: projection and scores with group summaries.
+// Stage 1 up to the group records: projection and scores with group summaries.  want_keys: the
+// tensor-core path writes the groups' best keys too (for the fused head's fast selection); the
+// small-batch path always does.
 int run_records(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r, int vocab,
-                int dtype, char* ws, const TopkLayout& L, Stage1* out) {
+                int dtype, char* ws, const TopkLayout& L, Stage1* out, bool want_keys = false) {
   void* t = ws + L.t;
   float* partial = reinterpret_cast<float*>(ws + L.partial);
   GroupRec* recs = reinterpret_cast<GroupRec*>(ws + L.recs);
@@ -218,8 +220,10 @@ int run_records(const Ctx& c, const void* h, const void* U, const void* V, int B
     return DH_ERR_CUDA;
   }
   if (path == PATH_MMA) {
-    if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, reinterpret_cast<int*>(ws)) != cudaSuccess)
+    uint32_t* gkeys = want_keys ? reinterpret_cast<uint32_t*>(ws + L.gkeys) : nullptr;
+    if (launch_lowrank_mma(c, t, V, B, r, vocab, recs, gkeys, reinterpret_cast<int*>(ws)) != cudaSuccess)
       return DH_ERR_CUDA;
+    out->gkeys = gkeys;
   } else if (note_error(launch_scores_summary(c, t, V, B, r, vocab, dtype, recs), "scores") != cudaSuccess) {
     return DH_ERR_CUDA;
   }
@@ -361,7 +365,7 @@ int dh_draft_head(const void* h, const void* U, const void* V, const void* W, in
                                                                           : head_cluster_ctas(c, B, K, d, vocab, dtype);
   const bool fast = ctas && !tuning().head_select_radix;
   Stage1 s1;
-  const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1);
+  const int st = run_records(c, h, U, V, B, d, r, vocab, dtype, ws, L, &s1, fast);
   if (st != DH_OK) return st;
   if (ctas) {
     if (note_error(launch_head_cluster(c, ctas, s1.recs, fast ? s1.gkeys : nullptr, s1.acc, s1.t, V, h, W, B, d, r,

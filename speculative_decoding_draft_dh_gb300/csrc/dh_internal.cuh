@@ -299,8 +299,9 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
 cudaError_t launch_small_b(const Ctx& c, const void* h, const void* U, const void* V, int B, int d, int r,
                            int vocab, int dtype, unsigned long long* acc, GroupRec* recs, uint32_t* gkeys,
                            int* status);
+// gkeys (may be null): as for the small-batch path, each group's best key (0: empty group).
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
-                               GroupRec* recs, int* status);
+                               GroupRec* recs, uint32_t* gkeys, int* status);
 
 cudaError_t launch_scores_summary(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
                                   int dtype, GroupRec* recs);

@@ -7,8 +7,8 @@
 //
 // At batch 1 the selection is a short chain of dependent steps, and each kernel boundary or
 // cluster barrier costs about half a microsecond to a microsecond.  Two selections run here:
-//  - the fast selection (default after the small-batch scores kernel, which also writes every
-//    group's best key): every CTA selects the K winners itself (a bound from K disjoint subsets of
+//  - the fast selection (the default: the stage-1 scores kernels, small-batch or tensor-core, also
+//    write every group's best key when this kernel follows): every CTA selects the K winners itself (a bound from K disjoint subsets of
 //    the groups' best keys, one histogram, then the records of the few candidate groups, read
 //    through L2, ranked by counting), so the CTAs exchange nothing until the exact logits; each CTA
 //    starts the W rows of its share of the candidate groups towards L2 as soon as it knows them,

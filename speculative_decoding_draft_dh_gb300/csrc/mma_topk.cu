@@ -52,6 +52,7 @@ struct MmaParams {
   int B, r, vocab, n_groups, n_tiles, n_split, stages;
   int rep;  // copies of T's rows in the 128-row A tile (1, 2 or 4; see the epilogue)
   GroupRec* recs;
+  uint32_t* gkeys;  // [B][n_groups] each group's best key for the fused head's fast selection, or null
   int* status;
 };
 
@@ -232,7 +233,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               if (gc0 + h2 * 32 + i < p.vocab) sm.push(v[i], (uint32_t)(gc0 + h2 * 32 + i));
           }
         }
-        if (row < p.B && gc0 < p.vocab) p.recs[(size_t)row * p.n_groups + gc0 / GROUP] = sm.record((uint32_t)gc0);
+        if (row < p.B && gc0 < p.vocab) {
+          p.recs[(size_t)row * p.n_groups + gc0 / GROUP] = sm.record((uint32_t)gc0);
+          if (p.gkeys) p.gkeys[(size_t)row * p.n_groups + gc0 / GROUP] = sm.i1 == 0xFFFFFFFFu ? 0u : fkey(sm.v1);
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -507,7 +511,7 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
 }
 
 cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B, int r, int vocab,
-                               GroupRec* recs, int* status) {
+                               GroupRec* recs, uint32_t* gkeys, int* status) {
   static unsigned long long smem_done = 0;
   cudaError_t e = allow_max_smem(k_lowrank_mma, c.device, &smem_done);
   if (e != cudaSuccess) return e;
@@ -537,6 +541,7 @@ cudaError_t launch_lowrank_mma(const Ctx& c, const void* t, const void* V, int B
   p.rep = rep;
   p.stages = stages;
   p.recs = recs;
+  p.gkeys = gkeys;
   p.status = status;
   // programmatic dependent launch: set-up and the first V stages overlap the projection's tail
   cudaLaunchAttribute attr[1];

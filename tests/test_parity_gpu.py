@@ -111,12 +111,15 @@ def test_clustered_candidates_are_refined(api):
     run_head(x, cfg.K, api=api)
 
 
+@pytest.mark.parametrize("select", ["auto", "radix"])
 @pytest.mark.parametrize("B", [1, 8])
-def test_tensor_core_path_fused_head_refines_clustered_rows(B, tune):
-    """Tensor-core stage 1 (t in bf16) followed by the fused cluster head, on rows whose top
-    candidates crowd one group (refinement by the leader's block selection) and on plain rows:
-    against the oracle, and bit for bit against the two calls."""
+def test_tensor_core_path_fused_head_refines_clustered_rows(B, select, tune):
+    """Tensor-core stage 1 (t in bf16, and the groups' best keys) followed by the fused cluster
+    head, on rows whose top candidates crowd one group (refinement by the leader's block selection)
+    and on plain rows: against the oracle, and bit for bit against the two calls; with the fast
+    selection (auto) and the cooperative radix one."""
     tune("DH_FORCE_PATH", "mma")
+    tune("DH_HEAD_SELECT", select)
     cfg = inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=32)
     x = inputs.make_head(cfg, seed=8, device=DEV)
     v = _best_column(x)
@@ -143,10 +146,14 @@ def test_many_clustered_groups_use_full_rescan(api):
     run_head(x, cfg.K, api=api)
 
 
-def test_fast_selection_overflow_takes_the_exact_path():
+@pytest.mark.parametrize("path", ["auto", "mma"])
+def test_fast_selection_overflow_takes_the_exact_path(path, tune):
     """Every group's two best scores tie with the K-th group best (identical V columns), so far more
     than the candidate list's capacity reach the threshold: the fused head falls back to the
-    leader's exact selection, and still equals the two calls and the oracle (ties to the lowest id)."""
+    leader's exact selection, and still equals the two calls and the oracle (ties to the lowest id).
+    After the small-batch scores kernel (auto) and after the tensor-core one."""
+    if path != "auto":
+        tune("DH_FORCE_PATH", path)
     cfg = inputs.head_config("batch1", B=1, d=512, vocab=65536, r=128, K=64)
     x = inputs.make_head(cfg, seed=9, device=DEV)
     x["V"][:, 1:] = x["V"][:, :1]
