@@ -394,6 +394,7 @@ def run_head_bench(a, cfg, rank, world, local, peaks, peak_src, steps=None, warm
         sets.append(x)
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs were made on the current stream
 
     expand_w = EXPAND_W.get(cfg.name, 0)
     sizing = SIZE_LEVEL.get(cfg.name)
@@ -738,6 +739,7 @@ def run_tree_bench(a, tcfg, rank, world, local, peaks, peak_src, steps=None, war
     t = inputs.make_tree(tcfg, seed=a.seed + 1000 * rank, device=dev)
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs were made on the current stream
     B, N, vocab = tcfg.B, tcfg.N, tcfg.vocab
     elem = 2 if tcfg.dtype == "bf16" else 4
     logit_bytes = B * N * vocab * elem
@@ -895,6 +897,7 @@ def run_verify_bench(a, vcfg, rank, world, local, peaks, peak_src, steps=None, w
         v["tok"] = torch.empty(B, dtype=torch.int32, device=dev)
     ws = dh.Workspace()
     stream = torch.cuda.Stream(device=dev)
+    stream.wait_stream(torch.cuda.current_stream(dev))  # the inputs were made on the current stream
 
     def step(v):
         dh.verify_chain(v["logits"], v["cand_idx"], v["cand_prob"], v["draft_token"], v["u_accept"], v["u_sample"],

@@ -139,13 +139,16 @@ class Workspace:
     def __init__(self):
         self.buf = {}
 
-    def get(self, nbytes: int, device, kind: str) -> torch.Tensor | None:
+    def get(self, nbytes: int, device, kind: str, stream=None) -> torch.Tensor | None:
+        """The buffer for one call kind, at least nbytes long; a new one is zeroed on `stream` (the
+        call's stream, else the current one), so that the call that follows finds it zeroed."""
         if nbytes == 0:
             return None
         key = (torch.device(device), kind)
         cur = self.buf.get(key)
         if cur is None or cur.numel() < nbytes:
-            cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=key[0])
+            with torch.cuda.stream(torch.cuda.current_stream(key[0]) if stream is None else stream):
+                cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=key[0])
             self.buf[key] = cur
         return cur
 
@@ -175,7 +178,7 @@ def lowrank_topk(h, U, V, K, *, idx_out=None, score_out=None, workspace=None, st
     if score_out is None:
         score_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_lowrank_topk_workspace(B, d, r, vocab, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device, "topk")
+    ws = (workspace or _default_ws).get(nbytes, h.device, "topk", stream)
     _check(lib.dh_lowrank_topk(_ptr(h), _ptr(U), _ptr(V), B, d, r, vocab, K, dt, _ptr(idx_out),
                                _ptr(score_out), _ptr(ws), nbytes, _stream(stream)), "dh_lowrank_topk")
     return idx_out, score_out
@@ -197,7 +200,7 @@ def exact_rescore(h, W, idx, *, with_probs=True, logits_out=None, probs_out=None
     if with_probs and probs_out is None:
         probs_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_exact_rescore_workspace(B, d, vocab, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore")
+    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore", stream)
     _check(lib.dh_exact_rescore(_ptr(h), _ptr(W), _ptr(idx), B, d, vocab, K, dt, _ptr(logits_out),
                                 _ptr(probs_out if with_probs else None), _ptr(ws), nbytes,
                                 _stream(stream)), "dh_exact_rescore")
@@ -228,7 +231,7 @@ def draft_head(h, U, V, W, K, *, with_probs=True, idx_out=None, score_out=None, 
     if with_probs and probs_out is None:
         probs_out = torch.empty(B, K, dtype=torch.float32, device=dev)
     nbytes = lib.dh_draft_head_workspace(B, d, r, vocab, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, dev, "head")
+    ws = (workspace or _default_ws).get(nbytes, dev, "head", stream)
     _check(lib.dh_draft_head(_ptr(h), _ptr(U), _ptr(V), _ptr(W), B, d, r, vocab, K, dt, _ptr(idx_out),
                              _ptr(score_out), _ptr(logits_out), _ptr(probs_out if with_probs else None),
                              _ptr(ws), nbytes, _stream(stream)), "dh_draft_head")
@@ -277,7 +280,7 @@ def tree_accept(logits, parent, token, *, with_argmax=True, workspace=None, stre
            "bonus": torch.empty(B, dtype=torch.int32, device=dev),
            "err": torch.empty(B, dtype=torch.int32, device=dev)}
     nbytes = lib.dh_tree_accept_workspace(B, N, vocab)
-    ws = (workspace or _default_ws).get(nbytes, dev, "tree")
+    ws = (workspace or _default_ws).get(nbytes, dev, "tree", stream)
     _check(lib.dh_tree_accept(_ptr(logits), _ptr(parent), _ptr(token), B, N, vocab, dt,
                               _ptr(out["argmax"]), _ptr(out["path"]), _ptr(out["len"]),
                               _ptr(out["bonus"]), _ptr(out["err"]), _ptr(ws), nbytes,
@@ -301,7 +304,7 @@ def lowrank_topk_shard(h, U, V_shard, K, vocab_offset, *, idx_out=None, score_ou
     if score_out is None:
         score_out = torch.empty(B, K, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_lowrank_topk_workspace(B, d, r, n, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device, "topk")
+    ws = (workspace or _default_ws).get(nbytes, h.device, "topk", stream)
     _check(lib.dh_lowrank_topk_shard(_ptr(h), _ptr(U), _ptr(V_shard), B, d, r, n, int(vocab_offset), K, dt,
                                      _ptr(idx_out), _ptr(score_out), _ptr(ws), nbytes, _stream(stream)),
            "dh_lowrank_topk_shard")
@@ -343,7 +346,7 @@ def exact_rescore_shard(h, W_shard, idx, vocab_offset, *, logits_out=None, stats
     if stats_out is None:
         stats_out = torch.empty(B, 2, dtype=torch.float32, device=h.device)
     nbytes = lib.dh_exact_rescore_shard_workspace(B, d, n, K, dt)
-    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore_shard")
+    ws = (workspace or _default_ws).get(nbytes, h.device, "rescore_shard", stream)
     _check(lib.dh_exact_rescore_shard(_ptr(h), _ptr(W_shard), _ptr(idx), B, d, n, int(vocab_offset), K, dt,
                                       _ptr(logits_out), _ptr(stats_out), _ptr(ws), nbytes, _stream(stream)),
            "dh_exact_rescore_shard")
@@ -420,7 +423,7 @@ def verify_chain(logits, cand_idx, cand_prob, draft_token, u_accept, u_sample, *
         token_out = torch.empty(B, dtype=torch.int32, device=dev)
     dt = _dtype_code(logits)
     nbytes = lib.dh_verify_chain_workspace(B, L, vocab, dt)
-    ws = (workspace or _default_ws).get(nbytes, dev, "verify")
+    ws = (workspace or _default_ws).get(nbytes, dev, "verify", stream)
     _check(lib.dh_verify_chain(_ptr(logits), _ptr(cand_idx if L > 0 else None), _ptr(cand_prob if L > 0 else None),
                                _ptr(draft_token if L > 0 else None), _ptr(u_accept if L > 0 else None),
                                _ptr(u_sample), B, L, vocab, K, dt, float(temperature), _ptr(n_accept_out),
@@ -446,7 +449,8 @@ def selftest_wait_timeout(limit_us: int = 50000, stream=None) -> int:
     """Run the bounded-wait self-test (an mbarrier wait that nothing completes) on a fresh workspace
     and return the status word it left (expected: 1 << DH_ERR_TIMEOUT)."""
     lib = load_library()
-    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    with torch.cuda.stream(torch.cuda.current_stream() if stream is None else stream):
+        ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
     _check(lib.dh_selftest_wait_timeout(0, limit_us, _ptr(ws), 256, _stream(stream)),
            "dh_selftest_wait_timeout")
     out = ctypes.c_int(0)

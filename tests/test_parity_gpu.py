@@ -616,6 +616,29 @@ def test_draft_head_one_workspace_across_shapes():
     assert dh.workspace_status(ws) == 0
 
 
+def test_fresh_workspace_on_a_side_stream():
+    """A call on a stream other than the current one, with a fresh workspace (zeroed on the call's
+    stream) while the current stream is still busy: it equals the same call on the current stream
+    and leaves no status bit."""
+    cfg = inputs.head_config("batch1", B=2)
+    x = inputs.make_head(cfg, seed=5, device=DEV)
+    ref = dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K, workspace=dh.Workspace())
+    torch.cuda.synchronize()
+    nbytes = dh.load_library().dh_draft_head_workspace(cfg.B, cfg.d, cfg.r, cfg.vocab, cfg.K, dh._dtype_code(x["h"]))
+    junk = torch.full((nbytes + 4096,), 255, dtype=torch.uint8, device=DEV)
+    del junk  # its block is free again, with ones in it
+    a = torch.randn(2048, 2048, device=DEV)
+    for _ in range(20):  # keeps the current stream busy
+        a = torch.tanh(a @ a)
+    side = torch.cuda.Stream()
+    ws = dh.Workspace()
+    out = dh.draft_head(x["h"], x["U"], x["V"], x["W"], cfg.K, workspace=ws, stream=side)
+    torch.cuda.synchronize()
+    for o, r_ in zip(out, ref):
+        assert torch.equal(o, r_)
+    assert dh.workspace_status(ws) == 0
+
+
 def test_repeated_calls_are_identical():
     cfg = inputs.head_config("tiny", B=4)
     x = inputs.make_head(cfg, seed=13, device=DEV)
