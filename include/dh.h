@@ -134,10 +134,11 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
  * for the two calls (bit for bit, except that where the two calls would use their bulk-copy
  * rescoring kernel, from 2048 (row, candidate) pairs, probabilities agree to rounding).  When the
  * device runs one thread-block cluster of 16, 8 or 4 CTAs per row for all B rows at once (with 4
- * CTAs, for at most 2048 pairs: up to 32 rows of 64 candidates on a GB300), the selection and the
- * rescoring run as one kernel, which removes a kernel boundary from the critical path; on the
- * first call per device the library queries how many such clusters fit (the switch DH_FORCE_HEAD=split,
- * see dh_set_tuning, runs the two calls' kernels instead).
+ * CTAs, for at most 2048 pairs: up to 32 rows of 64 candidates on a GB300) and K <= 192, the
+ * selection and the rescoring run as one kernel, which removes a kernel boundary from the critical
+ * path; on the first call per device the library queries how many such clusters fit (the switch
+ * DH_FORCE_HEAD, see dh_set_tuning, runs the two calls' kernels instead, or the cluster kernel
+ * whatever K).
  * The workspace (dh_draft_head_workspace bytes, 256-byte aligned, caller-owned) must be zero-filled
  * before its first use and not shared by calls that overlap in time; the library leaves it ready
  * for the next call.
@@ -378,7 +379,8 @@ int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int
  * Each switch is read once per process from the environment variable of the same name, on the
  * library's first use of it, and afterwards changes only through this call.  name / value:
  *   "DH_FORCE_PATH"    "auto" | "gemv" | "mma" | "fused"  stage-1 path, when it supports the shape
- *   "DH_FORCE_HEAD"    "auto" | "split"                  dh_draft_head without the cluster head
+ *   "DH_FORCE_HEAD"    "auto" | "split" | "cluster"      dh_draft_head without the cluster head, or
+ *                                                        with it wherever it fits, whatever K
  *   "DH_HEAD_CTAS"     "16" | "8" | "4"                  largest cluster of the fused head
  *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket" | "sweep" | "bucket"  stage-2 kernel
  *                      ("bucket": the ring kernel in its vocabulary-bucket mode at any size)

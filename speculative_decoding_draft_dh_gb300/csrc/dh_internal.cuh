@@ -261,6 +261,7 @@ struct Tuning {
   enum Rescore { RESCORE_AUTO, RESCORE_DIRECT, RESCORE_RING, RESCORE_TICKET, RESCORE_SWEEP, RESCORE_BUCKET };
   Path force_path = PATH_AUTO;      // stage-1 path, when the forced one supports the shape
   bool head_split = false;          // dh_draft_head: the two calls' kernels, not the cluster head
+  bool head_cluster = false;        // dh_draft_head: the cluster head wherever it fits, whatever K
   int head_ctas_max = 16;           // largest cluster of the fused head (16, 8 or 4)
   Rescore rescore = RESCORE_AUTO;   // stage-2 kernel choice
   bool scores_tma = false;          // small-batch scores: the TMA variant for every rank

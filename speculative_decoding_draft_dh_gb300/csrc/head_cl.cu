@@ -189,6 +189,89 @@ __device__ __forceinline__ bool wait_copy(uint64_t* bar, int* status) {
   return false;
 }
 
+// In-place refinement of a row the certificate flags, in every CTA (each reaches the same winners
+// from the same data): the flagged groups' members are scored exactly with the block selection's
+// score_groups, and the K winners are ranked again among the winners outside those groups and the
+// flagged groups' members at or above tau.  That is select_row's own refinement on the same
+// candidates, so the winners are the same.  `area` is the selection area, laid out as select_row's
+// Shared block (its W-row slots must have landed).  Returns false where select_row would settle the
+// row another way (more than RMAX flagged groups, or a candidate count outside [K, CMAX]); the
+// leader's block selection then takes the row.
+template <typename T>
+__device__ bool refine_in_place(const HeadParams& p, HeadCtl& my, const FastShared& fs, unsigned char* area, int b,
+                                uint32_t n_cg, uint32_t tau) {
+  sel::Shared& sh = *reinterpret_cast<sel::Shared*>(area);
+  const int K = p.K, r = p.r;
+  for (int w = threadIdx.x; w < (int)sel::BITMAP_WORDS; w += HC_THREADS) sh.bitmap[w] = 0u;
+  if (p.acc) {
+    const unsigned long long* acc_row = p.acc + (size_t)b * r;
+    for (int j = threadIdx.x; j < r; j += HC_THREADS) sh.t[j] = acc_to_t<T>(acc_row, p.B * r, j);
+  } else {
+    const T* t_row = static_cast<const T*>(p.t) + (size_t)b * r;
+    for (int j = threadIdx.x; j < r; j += HC_THREADS) sh.t[j] = Elem<T>::to_f(t_row[j]);
+  }
+  if (threadIdx.x == 0) sh.nref = 0u;
+  __syncthreads();
+  for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) {
+    if (fs.cm3[i] >= tau) {
+      const int g = fs.cg[i];
+      const uint32_t pos = atomicAdd(&sh.nref, 1u);
+      if (pos < (uint32_t)sel::RMAX) sh.rg[pos] = g;
+      atomicOr(&sh.bitmap[g >> 5], 1u << (g & 31));
+    }
+  }
+  __syncthreads();
+  const int nref = (int)sh.nref;
+  if (nref > sel::RMAX) return false;
+  const T* V = static_cast<const T*>(p.V);
+  for (int i = 0; i < nref; i += sel::SG_BATCH)
+    sel::score_groups(sh.t, V, r, p.vocab, sh.rg + i, min(sel::SG_BATCH, nref - i), sh.rs + i * GROUP,
+                      reinterpret_cast<float*>(sh.hist));
+  unsigned long long* cp = reinterpret_cast<unsigned long long*>(sh.hist);  // the candidates, packed
+  constexpr int CMAX = sel::HIST_BINS / 2;
+  if (threadIdx.x == 0) sh.cnt = 0u;
+  __syncthreads();
+  for (int k0 = 0; k0 < K; k0 += HC_THREADS) {
+    const int k = k0 + (int)threadIdx.x;
+    bool take = false;
+    unsigned long long e = 0ull;
+    if (k < K) {
+      e = my.sp[k];
+      const uint32_t g = (~(uint32_t)e) / GROUP;
+      take = !((sh.bitmap[g >> 5] >> (g & 31)) & 1u);
+    }
+    const uint32_t pos = sel::warp_append(take, &sh.cnt);
+    if (take && pos < (uint32_t)CMAX) cp[pos] = e;
+  }
+  for (int e0 = 0; e0 < nref * GROUP; e0 += HC_THREADS) {
+    const int e = e0 + (int)threadIdx.x;
+    bool take = false;
+    uint32_t key = 0u;
+    int c = 0;
+    if (e < nref * GROUP) {
+      c = sh.rg[e / GROUP] * GROUP + (e % GROUP);
+      key = fkey(sh.rs[e]);
+      take = c < p.vocab && key >= tau;
+    }
+    const uint32_t pos = sel::warp_append(take, &sh.cnt);
+    if (take && pos < (uint32_t)CMAX) cp[pos] = pack(key, (uint32_t)c);
+  }
+  __syncthreads();
+  const int n = (int)sh.cnt;
+  if (n < K || n > CMAX) return false;
+  int P = 1;
+  while (P < 32 && n * (2 * P) <= HC_THREADS) P <<= 1;
+  for (int base = 0; base < n * P; base += HC_THREADS) {
+    const int t = base + (int)threadIdx.x;
+    const int i = t / P, h = t % P;
+    unsigned long long pi;
+    const int rank = sel::rank_by_count(cp, n, P, i, h, &pi);
+    if (i < n && h == 0 && rank < K) my.sp[rank] = pi;
+  }
+  __syncthreads();
+  return true;
+}
+
 // Fast selection from the groups' best keys (written by the small-batch scores kernel).  Every CTA
 // selects the row's K winners itself, from every group's best key and the records of a few groups,
 // so the CTAs exchange nothing before the exact logits:
@@ -366,11 +449,18 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
                        &fs.wbar[warp]);
     }
   }
-  if (!fall) {
-    const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
+  const uint32_t tau = fall ? 0u : (uint32_t)(my.sp[K - 1] >> 32);
+  if (!fall)
     for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) flag |= fs.cm3[i] >= tau;
+  fall = __syncthreads_or(fall) != 0;
+  if (!fall && __syncthreads_or(flag)) {
+    // a flagged group: refined here, unless the leader's block selection must take the row; the
+    // W-row slots are reused as the refinement's area, and the winners are scored from L2
+    if (slotted) wait_copy(&fs.wbar[warp], p.status);
+    slotted = false;
+    __syncthreads();
+    fall = !refine_in_place<T>(p, my, fs, reinterpret_cast<unsigned char*>(slots), b, n_cg, tau);
   }
-  fall = __syncthreads_or(fall || flag) != 0;
   // every CTA has started (the arrive at its start) before any CTA writes into the leader
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
   if (fall) {
@@ -759,9 +849,16 @@ int clusters_at_once(int device, size_t smem) {
   return n;
 }
 
+// Largest K for which the fused head is chosen by default.  At K = 256 the two kernels are as fast or
+// faster (µs per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels: 33.8 / 32.2
+// at B = 2, 39.4 / 37.8 at B = 4, 47.1 / 46.1 at B = 8; 26.3 / 26.5 at B = 1), while up to K = 192
+// the fused head is faster at every batch that fits (8 x 192: 37.9 / 40.1; 16 x 128: 36.1 / 40.1).
+constexpr int HC_AUTO_MAX_K = 192;
+
 // Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
 // clusters of 8 do, else 4 for up to 2048 (row, candidate) pairs when all B clusters of 4 do, else
-// 0 (the batch goes to the selection and rescoring kernels).  Four CTAs score eight or more
+// 0 (the batch goes to the selection and rescoring kernels); 0 as well above HC_AUTO_MAX_K
+// candidates unless DH_FORCE_HEAD=cluster.  Four CTAs score eight or more
 // candidates per warp, one row after another; that pays against the two kernels up to about 2048
 // pairs (32 rows x 64: 31.0 against 39.0 µs per call; 16 x 64: 29.3 against 32.6) but not beyond
 // (64 x 128: 77.6 against 56.4).  The device's capacities are queried once per device and element
@@ -788,6 +885,7 @@ int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
     n8 = cap[c.device][1] - 1;
     n4 = cap[c.device][2] - 1;
   }
+  if (K > HC_AUTO_MAX_K && !tuning().head_cluster) return 0;
   const int most = tuning().head_ctas_max;
   if (most >= 16 && B <= n16) return 16;
   if (most >= 8 && B <= n8) return 8;

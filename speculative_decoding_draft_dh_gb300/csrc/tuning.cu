@@ -31,8 +31,9 @@ bool apply(Tuning& t, const char* name, const char* value) {
     return true;
   }
   if (std::strcmp(name, "DH_FORCE_HEAD") == 0) {
-    if (dflt || is("auto") || is("cluster")) t.head_split = false;
-    else if (is("split")) t.head_split = true;
+    if (dflt || is("auto")) t.head_split = t.head_cluster = false;
+    else if (is("split")) { t.head_split = true; t.head_cluster = false; }
+    else if (is("cluster")) { t.head_split = false; t.head_cluster = true; }
     else return false;
     return true;
   }

@@ -134,6 +134,22 @@ def test_tensor_core_path_fused_head_refines_clustered_rows(B, select, tune):
     assert torch.equal(logits, l2) and torch.equal(probs, p2)
 
 
+@pytest.mark.parametrize("B,K,seed", [(3, 84, 1), (1, 256, 0), (2, 256, 1), (2, 192, 1), (8, 128, 2)])
+def test_fused_head_refines_flagged_rows_in_place(B, K, seed, tune):
+    """Rows whose certificate flags a group (a third score at or above tau; common from K = 128 on
+    random rows) are refined inside the fused head, every CTA re-ranking the winners with the
+    flagged groups scored exactly: bit for bit the two calls' outputs, and the oracle's top K."""
+    tune("DH_FORCE_HEAD", "cluster")
+    cfg = inputs.head_config("batch1", B=B, K=K)
+    x = inputs.make_head(cfg, seed=seed, device=DEV)
+    idx, score, logits, probs = run_head(x, K, api="head")
+    i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], K)
+    l2, p2 = dh.exact_rescore(x["h"], x["W"], i2)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, i2) and torch.equal(score, s2)
+    assert torch.equal(logits, l2) and torch.equal(probs, p2)
+
+
 @pytest.mark.parametrize("api", ["split", "head"])
 def test_many_clustered_groups_use_full_rescan(api):
     cfg = inputs.head_config("tiny", B=1, K=128)
