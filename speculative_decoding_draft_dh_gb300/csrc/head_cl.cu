@@ -856,14 +856,16 @@ int clusters_at_once(int device, size_t smem) {
 constexpr int HC_AUTO_MAX_K = 192;
 
 // Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
-// clusters of 8 do, else 4 for up to 2048 (row, candidate) pairs when all B clusters of 4 do, else
-// 0 (the batch goes to the selection and rescoring kernels); 0 as well above HC_AUTO_MAX_K
-// candidates unless DH_FORCE_HEAD=cluster.  Four CTAs score eight or more
-// candidates per warp, one row after another; that pays against the two kernels up to about 2048
-// pairs (32 rows x 64: 31.0 against 39.0 µs per call; 16 x 64: 29.3 against 32.6) but not beyond
-// (64 x 128: 77.6 against 56.4).  The device's capacities are queried once per device and element
-// type (set-up calls: shared memory limit, the non-portable size, the occupancy query).
-// The DH_HEAD_CTAS switch (8 or 4) skips the larger forms (tests).
+// clusters of 8 do, else 4 when all B clusters of 4 do, for up to 8192 (row, candidate) pairs with
+// K <= 128 and 2048 above, else 0 (the batch goes to the selection and rescoring kernels); 0 as well
+// above HC_AUTO_MAX_K candidates unless DH_FORCE_HEAD=cluster.  Four CTAs score several candidates
+// per warp, one after another.  Measured per call in CUDA graphs at d 5120, vocab 151936, fused
+// against two kernels: 33 x 64: 30.9 / 39.6 µs; 36 x 64: 32.0 / 39.7; 24 x 128: 38.8 / 41.8;
+// 32 x 128: 39.4 / 44.2; 36 x 128: 42.6 / 47.6; but 16 x 192: 46.7 / 45.2 and 20 x 192: 47.8 / 46.5.
+// Clusters of 4 in two waves lose (64 x 128: 58.1 / 52.5; 64 x 64: 43.3 / 42.7).  The device's
+// capacities are queried once per device and element type (set-up calls: shared memory limit, the
+// non-portable size, the occupancy query).  The DH_HEAD_CTAS switch (8 or 4) skips the larger forms
+// (tests).
 template <typename T>
 int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const size_t smem = hc_smem_bytes(d, (int)sizeof(T), n_groups);
@@ -889,7 +891,7 @@ int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const int most = tuning().head_ctas_max;
   if (most >= 16 && B <= n16) return 16;
   if (most >= 8 && B <= n8) return 8;
-  if (most >= 4 && B <= n4 && (long long)B * K <= 2048) return 4;
+  if (most >= 4 && B <= n4 && (long long)B * K <= (K <= 128 ? 8192 : 2048)) return 4;
   return 0;
 }
 
