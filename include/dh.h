@@ -133,8 +133,9 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
  * aligned, with d, r and vocab rows a multiple of 16 bytes; d <= 8192; limits and error codes as
  * for the two calls (bit for bit, except that where the two calls would use their bulk-copy
  * rescoring kernel, from 2048 (row, candidate) pairs, probabilities agree to rounding).  When the
- * device runs one thread-block cluster of 16, 8 or 4 CTAs per row for all B rows at once (with 4
- * CTAs, for at most 8192 pairs with K <= 128 and 2048 above: up to 36 rows on a GB300) and K <= 192, the
+ * device runs one thread-block cluster of 16, 8, 4 or 2 CTAs per row for all B rows at once (with 4
+ * CTAs, for at most 8192 pairs with K <= 128 and 2048 above: up to 36 rows on a GB300; with 2, for
+ * K <= 64: up to 76 rows) and K <= 192, the
  * selection and the rescoring run as one kernel, which removes a kernel boundary from the critical
  * path; on the first call per device the library queries how many such clusters fit (the switch
  * DH_FORCE_HEAD, see dh_set_tuning, runs the two calls' kernels instead, or the cluster kernel
@@ -381,7 +382,7 @@ int dh_prof_read(char* names, int name_len, double* total_ms, int* launches, int
  *   "DH_FORCE_PATH"    "auto" | "gemv" | "mma" | "fused"  stage-1 path, when it supports the shape
  *   "DH_FORCE_HEAD"    "auto" | "split" | "cluster"      dh_draft_head without the cluster head, or
  *                                                        with it wherever it fits, whatever K
- *   "DH_HEAD_CTAS"     "16" | "8" | "4"                  largest cluster of the fused head
+ *   "DH_HEAD_CTAS"     "16" | "8" | "4" | "2"            largest cluster of the fused head
  *   "DH_FORCE_RESCORE" "auto" | "direct" | "ring" | "ticket" | "sweep" | "bucket"  stage-2 kernel
  *                      ("bucket": the ring kernel in its vocabulary-bucket mode at any size)
  *   "DH_SCORES_SMALL"  "lsu" | "tma"                     small-batch scores kernel

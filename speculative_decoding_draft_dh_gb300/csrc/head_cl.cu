@@ -857,12 +857,14 @@ constexpr int HC_AUTO_MAX_K = 192;
 
 // Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
 // clusters of 8 do, else 4 when all B clusters of 4 do, for up to 8192 (row, candidate) pairs with
-// K <= 128 and 2048 above, else 0 (the batch goes to the selection and rescoring kernels); 0 as well
-// above HC_AUTO_MAX_K candidates unless DH_FORCE_HEAD=cluster.  Four CTAs score several candidates
-// per warp, one after another.  Measured per call in CUDA graphs at d 5120, vocab 151936, fused
-// against two kernels: 33 x 64: 30.9 / 39.6 µs; 36 x 64: 32.0 / 39.7; 24 x 128: 38.8 / 41.8;
-// 32 x 128: 39.4 / 44.2; 36 x 128: 42.6 / 47.6; but 16 x 192: 46.7 / 45.2 and 20 x 192: 47.8 / 46.5.
-// Clusters of 4 in two waves lose (64 x 128: 58.1 / 52.5; 64 x 64: 43.3 / 42.7).  The device's
+// K <= 128 and 2048 above, else 2 when all B clusters of 2 do and K <= 64, else 0 (the batch goes to
+// the selection and rescoring kernels); 0 as well above HC_AUTO_MAX_K candidates unless
+// DH_FORCE_HEAD=cluster.  Small clusters score several candidates per warp, one after another.
+// Measured per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels: 33 x 64:
+// 30.9 / 39.6 µs; 36 x 64: 32.0 / 39.7; 24 x 128: 38.8 / 41.8; 32 x 128: 39.4 / 44.2; 36 x 128:
+// 42.6 / 47.6; but 16 x 192: 46.7 / 45.2 and 20 x 192: 47.8 / 46.5 with 4 CTAs.  With 2 CTAs:
+// 40 x 64: 36.9 / 40.6; 64 x 64: 38.2 / 42.6; 76 x 64: 43.8 / 48.3; but 40 x 128: 51.7 / 47.8 and
+// 64 x 128: 53.5 / 52.5.  Clusters in two waves lose (4 CTAs, 64 x 128: 58.1 / 52.5).  The device's
 // capacities are queried once per device and element type (set-up calls: shared memory limit, the
 // non-portable size, the occupancy query).  The DH_HEAD_CTAS switch (8 or 4) skips the larger forms
 // (tests).
@@ -870,28 +872,32 @@ template <typename T>
 int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const size_t smem = hc_smem_bytes(d, (int)sizeof(T), n_groups);
   static std::mutex mu;
-  static int cap[64][3] = {};  // [device]: clusters of 16, 8 and 4 at once, +1 (0: not queried)
+  static int cap[64][4] = {};  // [device]: clusters of 16, 8, 4 and 2 at once, +1 (0: not queried)
   static size_t smem_at[64] = {};
   if (c.device < 0 || c.device >= 64) return 0;
-  int n16, n8, n4;
+  int n16, n8, n4, n2;
   {
     std::lock_guard<std::mutex> lk(mu);
     if (cap[c.device][0] == 0 || smem_at[c.device] < smem) {
       cap[c.device][0] = clusters_at_once<T, 16>(c.device, smem) + 1;
       cap[c.device][1] = clusters_at_once<T, 8>(c.device, smem) + 1;
       cap[c.device][2] = clusters_at_once<T, 4>(c.device, smem) + 1;
+      cap[c.device][3] = clusters_at_once<T, 2>(c.device, smem) + 1;
       smem_at[c.device] = smem;
       (void)cudaGetLastError();  // a refused query leaves no sticky error behind
     }
     n16 = cap[c.device][0] - 1;
     n8 = cap[c.device][1] - 1;
     n4 = cap[c.device][2] - 1;
+    n2 = cap[c.device][3] - 1;
   }
-  if (K > HC_AUTO_MAX_K && !tuning().head_cluster) return 0;
+  const bool forced = tuning().head_cluster;  // wherever it fits, whatever the candidates
+  if (K > HC_AUTO_MAX_K && !forced) return 0;
   const int most = tuning().head_ctas_max;
   if (most >= 16 && B <= n16) return 16;
   if (most >= 8 && B <= n8) return 8;
-  if (most >= 4 && B <= n4 && (long long)B * K <= (K <= 128 ? 8192 : 2048)) return 4;
+  if (most >= 4 && B <= n4 && (forced || (long long)B * K <= (K <= 128 ? 8192 : 2048))) return 4;
+  if (most >= 2 && B <= n2 && (forced || K <= 64)) return 2;
   return 0;
 }
 
@@ -899,14 +905,15 @@ template <typename T>
 cudaError_t run(const Ctx& c, const HeadParams& p, int ctas) {
   const size_t smem = hc_smem_bytes(p.d, (int)sizeof(T), p.n_groups);
   if (ctas == 4) return launch<T, 4>(c, p, smem);
+  if (ctas == 2) return launch<T, 2>(c, p, smem);
   return ctas == 16 ? launch<T, 16>(c, p, smem) : launch<T, 8>(c, p, smem);
 }
 
 }  // namespace
 
 int head_cluster_ctas(const Ctx& c, int B, int K, int d, int vocab, int dtype) {
-  // a wave of clusters holds at most one row per 4 SMs: larger batches need no query
-  if (B > c.num_sms / 4) return 0;
+  // a wave of clusters holds at most one row per 2 SMs: larger batches need no query
+  if (B > c.num_sms / 2) return 0;
   const int n_groups = (vocab + GROUP - 1) / GROUP;
   return dtype == DH_BF16 ? choose_ctas<__nv_bfloat16>(c, B, K, d, n_groups)
                           : choose_ctas<float>(c, B, K, d, n_groups);
@@ -923,7 +930,7 @@ cudaError_t launch_head_cluster(const Ctx& c, int ctas, const GroupRec* recs, co
                                 unsigned long long* acc, const void* t, const void* V, const void* h, const void* W,
                                 int B, int d, int r, int vocab, int K, int dtype, int32_t* idx_out, float* score_out,
                                 float* logits, float* probs, int* status) {
-  if (ctas != 4 && ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
+  if (ctas != 2 && ctas != 4 && ctas != 8 && ctas != 16) return cudaErrorInvalidValue;
   HeadParams p;
   p.recs = recs;
   p.gkeys = gkeys;

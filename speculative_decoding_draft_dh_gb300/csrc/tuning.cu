@@ -42,6 +42,7 @@ bool apply(Tuning& t, const char* name, const char* value) {
     else if (is("16")) t.head_ctas_max = 16;
     else if (is("8")) t.head_ctas_max = 8;
     else if (is("4")) t.head_ctas_max = 4;
+    else if (is("2")) t.head_ctas_max = 2;
     else return false;
     return true;
   }

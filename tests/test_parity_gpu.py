@@ -309,12 +309,12 @@ def test_draft_head_matches_the_two_calls(name, B, mode, tune):
 
 
 @pytest.mark.parametrize("select", ["auto", "radix"])
-@pytest.mark.parametrize("ctas", ["auto", "8", "4"])
+@pytest.mark.parametrize("ctas", ["auto", "8", "4", "2"])
 @pytest.mark.parametrize("K", [1, 7, 64, 100, 128, 256])
 def test_fused_head_matches_the_two_calls_over_K(K, ctas, select, tune):
     """The fused small-batch head against the two calls, bit for bit, over K (up to a full warp
     of candidates per CTA, and beyond one candidate per warp), with 16-CTA clusters where they fit
-    and with 8 and 4; with the group-best threshold selection (auto) and the cooperative radix one."""
+    and with 8, 4 and 2; with the group-best threshold selection (auto) and the cooperative radix one."""
     tune("DH_FORCE_HEAD", "cluster")
     tune("DH_HEAD_SELECT", select)
     if ctas != "auto":
@@ -354,15 +354,17 @@ def test_fused_head_back_to_back_calls(B):
     assert dh.workspace_status(ws) == 0
 
 
-@pytest.mark.parametrize("B", [16, 32])
-def test_fused_head_four_cta_clusters(B):
-    """Batches of 16 and 32 rows of 64 candidates (the four-CTA clusters where eight- and
-    sixteen-CTA ones do not fit one wave): against the oracle on every row, logits bit for bit
-    against the two calls (same per-candidate dot product order); the softmax of the two calls'
-    bulk-copy kernel adds in another order, so probabilities agree to rounding."""
-    cfg = inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=64)
+@pytest.mark.parametrize("B,K,full", [(16, 64, False), (32, 64, False), (33, 128, True), (64, 64, True)])
+def test_fused_head_small_clusters(B, K, full):
+    """Batches of 16 and 32 rows of 64 candidates, and 33 rows of 128 at the full shape (the
+    four-CTA clusters where eight- and sixteen-CTA ones do not fit one wave; 4224 pairs), and 64
+    rows of 64 at the full shape (two-CTA clusters): against
+    the oracle on every row (on five rows at the full shape), logits bit for bit against the two
+    calls (same per-candidate dot product order); probabilities to rounding."""
+    cfg = (inputs.head_config("batch1", B=B, K=K) if full
+           else inputs.head_config("batch1", B=B, d=512, vocab=8192, r=64, K=K))
     x = inputs.make_head(cfg, seed=9, device=DEV)
-    idx, score, logits, probs = run_head(x, cfg.K, api="head")
+    idx, score, logits, probs = run_head(x, cfg.K, api="head", rows=[0, 1, B // 2, B - 2, B - 1] if full else None)
     i2, s2 = dh.lowrank_topk(x["h"], x["U"], x["V"], cfg.K)
     l2, p2 = dh.exact_rescore(x["h"], x["W"], i2)
     torch.cuda.synchronize()
