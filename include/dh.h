@@ -134,8 +134,8 @@ int dh_exact_rescore(const void* h, const void* W, const int32_t* idx, int B, in
  * for the two calls (bit for bit, except that where the two calls would use their bulk-copy
  * rescoring kernel, from 2048 (row, candidate) pairs, probabilities agree to rounding).  When the
  * device runs one thread-block cluster of 16, 8, 4 or 2 CTAs per row for all B rows at once (with 4
- * CTAs, for at most 8192 pairs with K <= 128 and 2048 above: up to 36 rows on a GB300; with 2, for
- * K <= 64: up to 76 rows) and K <= 192, the
+ * CTAs, for at most 8192 pairs with K <= 64 and 2048 above: up to 36 rows on a GB300; with 2, for
+ * K <= 64: up to 76 rows) and K <= 128, the
  * selection and the rescoring run as one kernel, which removes a kernel boundary from the critical
  * path; on the first call per device the library queries how many such clusters fit (the switch
  * DH_FORCE_HEAD, see dh_set_tuning, runs the two calls' kernels instead, or the cluster kernel

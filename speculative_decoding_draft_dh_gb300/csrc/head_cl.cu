@@ -171,6 +171,8 @@ struct FastShared {
   uint32_t wsc[HC_WARPS];
   uint32_t bb;     // the boundary bin
   uint32_t n_ent;  // candidate entries
+  uint32_t n_cg;   // candidate groups (for the refinement)
+  int refine;      // the certificate flagged a group: the row is refined after the fast path
   uint64_t wbar[HC_WARPS];  // each warp's first winner's W row, bulk-copied into the selection area
 };
 
@@ -189,14 +191,14 @@ __device__ __forceinline__ bool wait_copy(uint64_t* bar, int* status) {
   return false;
 }
 
-// In-place refinement of a row the certificate flags, in every CTA (each reaches the same winners
-// from the same data): the flagged groups' members are scored exactly with the block selection's
-// score_groups, and the K winners are ranked again among the winners outside those groups and the
-// flagged groups' members at or above tau.  That is select_row's own refinement on the same
-// candidates, so the winners are the same.  `area` is the selection area, laid out as select_row's
-// Shared block (its W-row slots must have landed).  Returns false where select_row would settle the
-// row another way (more than RMAX flagged groups, or a candidate count outside [K, CMAX]); the
-// leader's block selection then takes the row.
+// In-place refinement of a row the fast selection's certificate flags (in every CTA, from the fast
+// selection's winners, candidate groups and tau): the flagged groups' members are scored exactly
+// with the block selection's score_groups, and the K winners are ranked again among the winners
+// outside those groups and the flagged groups' members at or above tau.  That is select_row's own
+// refinement on the same candidates, so the winners are the same.  `area` is the selection area,
+// laid out as select_row's Shared block (its W-row slots must have landed).  Returns false where
+// select_row would settle the row another way (more than RMAX flagged groups, or a candidate count
+// outside [K, CMAX]); the block selection then takes the row.
 template <typename T>
 __device__ bool refine_in_place(const HeadParams& p, HeadCtl& my, const FastShared& fs, unsigned char* area, int b,
                                 uint32_t n_cg, uint32_t tau) {
@@ -395,6 +397,10 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
   }
   const uint32_t n_cg = total;
   bool fall = !ok || n_cg > (uint32_t)HC_CG;
+  if (threadIdx.x == 0) {
+    fs.n_cg = n_cg;
+    fs.refine = 0;
+  }
   asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
   if (!fall) {
@@ -449,17 +455,15 @@ __device__ __forceinline__ bool head_fast(const HeadParams& p, cg::cluster_group
                        &fs.wbar[warp]);
     }
   }
-  const uint32_t tau = fall ? 0u : (uint32_t)(my.sp[K - 1] >> 32);
-  if (!fall)
+  if (!fall) {
+    const uint32_t tau = (uint32_t)(my.sp[K - 1] >> 32);
     for (uint32_t i = threadIdx.x; i < n_cg; i += HC_THREADS) flag |= fs.cm3[i] >= tau;
-  fall = __syncthreads_or(fall) != 0;
+  }
+  // fall is uniform over the block (from shared state): one block-wide vote, on the certificate; a
+  // flagged row leaves the fast path and is refined by the caller (refine_in_place)
   if (!fall && __syncthreads_or(flag)) {
-    // a flagged group: refined here, unless the leader's block selection must take the row; the
-    // W-row slots are reused as the refinement's area, and the winners are scored from L2
-    if (slotted) wait_copy(&fs.wbar[warp], p.status);
-    slotted = false;
-    __syncthreads();
-    fall = !refine_in_place<T>(p, my, fs, reinterpret_cast<unsigned char*>(slots), b, n_cg, tau);
+    if (threadIdx.x == 0) fs.refine = 1;
+    fall = true;
   }
   // every CTA has started (the arrive at its start) before any CTA writes into the leader
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -776,7 +780,36 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
     }
   }
   }  // the cooperative radix selection
-  // the leader selects the row alone: exact, with refinement or a full rescan as needed
+  // A row the fast selection's certificate flagged is refined in place by every CTA (its W-row slots
+  // have landed); each reaches the same winners from the same data, as it reached the same decision
+  // to refine, and scores its share of them.
+  if (p.gkeys && fs.refine &&
+      refine_in_place<T>(p, my, fs, fb, b, fs.n_cg, (uint32_t)(my.sp[K - 1] >> 32))) {
+    wait_copy(&hbar, p.status);
+    float* zl = cl.map_shared_rank(&my.z[0], 0u);
+    for (int k = warp * HC_CTAS + (int)crank; k < K; k += HC_CTAS * HC_WARPS) {
+      const unsigned long long e = my.sp[k];
+      const int v = (int)(~(uint32_t)e);
+      const bool okv = v >= 0 && v < p.vocab;
+      const float acc = okv ? row_dot<T>(static_cast<const T*>(p.W), v, p.d, hs, lane) : 0.f;
+      const float z = okv ? acc : __int_as_float(0x7FC00000);
+      if (lane == 0) {
+        p.idx_out[(size_t)b * K + k] = v;
+        p.score_out[(size_t)b * K + k] = fkey_inv((uint32_t)(e >> 32));
+        p.logits[(size_t)b * K + k] = z;
+        zl[k] = z;
+      }
+    }
+    cluster_sync_all();
+    if (!leader) return;
+    if (acc_row)  // zeroed for the next call (select_row does it on the other branch)
+      for (int j = threadIdx.x; j < p.r; j += HC_THREADS)
+#pragma unroll
+        for (int q = 0; q < ACC_COPIES; ++q) acc_row[(size_t)q * BR + j] = 0ull;
+    if (p.probs && warp == 0) warp_softmax(my.z, K, p.probs + (size_t)b * K);
+    return;
+  }
+  // otherwise the leader selects the row alone: exact, with refinement or a full rescan as needed
   if (leader)
     sel::select_row<T, HC_THREADS>(fb, rrow, t_row, acc_row, BR, static_cast<const T*>(p.V), p.r, p.vocab, K,
                                    p.idx_out + (size_t)b * K, p.score_out + (size_t)b * K);
@@ -849,25 +882,24 @@ int clusters_at_once(int device, size_t smem) {
   return n;
 }
 
-// Largest K for which the fused head is chosen by default.  At K = 256 the two kernels are as fast or
-// faster (µs per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels: 33.8 / 32.2
-// at B = 2, 39.4 / 37.8 at B = 4, 47.1 / 46.1 at B = 8; 26.3 / 26.5 at B = 1), while up to K = 192
-// the fused head is faster at every batch that fits (8 x 192: 37.9 / 40.1; 16 x 128: 36.1 / 40.1).
-constexpr int HC_AUTO_MAX_K = 192;
+// Largest K for which the fused head is chosen by default.  Above it the two kernels are as fast or
+// faster (µs per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels: 8 x 192:
+// 40.9 / 40.5; at K = 256, 33.8 / 32.2 at B = 2 and 47.1 / 46.1 at B = 8), while up to K = 128 the
+// fused head is as fast or faster at every batch that fits one wave (3 x 96: 24.3 / 28.6; 8 x 128:
+// 33.9 / 34.7; 16 x 128: 39.3 / 40.0).
+constexpr int HC_AUTO_MAX_K = 128;
 
 // Cluster size for B rows: 16 CTAs when all B clusters of 16 run at once, else 8 when all B
 // clusters of 8 do, else 4 when all B clusters of 4 do, for up to 8192 (row, candidate) pairs with
-// K <= 128 and 2048 above, else 2 when all B clusters of 2 do and K <= 64, else 0 (the batch goes to
+// K <= 64 and 2048 above, else 2 when all B clusters of 2 do and K <= 64, else 0 (the batch goes to
 // the selection and rescoring kernels); 0 as well above HC_AUTO_MAX_K candidates unless
 // DH_FORCE_HEAD=cluster.  Small clusters score several candidates per warp, one after another.
-// Measured per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels: 33 x 64:
-// 30.9 / 39.6 µs; 36 x 64: 32.0 / 39.7; 24 x 128: 38.8 / 41.8; 32 x 128: 39.4 / 44.2; 36 x 128:
-// 42.6 / 47.6; but 16 x 192: 46.7 / 45.2 and 20 x 192: 47.8 / 46.5 with 4 CTAs.  With 2 CTAs:
-// 40 x 64: 36.9 / 40.6; 64 x 64: 38.2 / 42.6; 76 x 64: 43.8 / 48.3; but 40 x 128: 51.7 / 47.8 and
-// 64 x 128: 53.5 / 52.5.  Clusters in two waves lose (4 CTAs, 64 x 128: 58.1 / 52.5).  The device's
-// capacities are queried once per device and element type (set-up calls: shared memory limit, the
-// non-portable size, the occupancy query).  The DH_HEAD_CTAS switch (8 or 4) skips the larger forms
-// (tests).
+// Measured per call in CUDA graphs at d 5120, vocab 151936, fused against two kernels, with 4 CTAs:
+// 33 x 64: 30.9 / 39.6 µs; 36 x 64: 32.0 / 39.7; but 24 x 128: 43.8 / 42.1; with 2 CTAs: 40 x 64:
+// 36.9 / 40.6; 64 x 64: 38.2 / 42.6; 76 x 64: 43.8 / 48.3; but 40 x 128: 51.7 / 47.8.  Clusters in
+// two waves lose (4 CTAs, 64 x 128: 58.1 / 52.5).  The device's capacities are queried once per
+// device and element type (set-up calls: shared memory limit, the non-portable size, the occupancy
+// query).  The DH_HEAD_CTAS switch (8, 4 or 2) skips the larger forms (tests).
 template <typename T>
 int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const size_t smem = hc_smem_bytes(d, (int)sizeof(T), n_groups);
@@ -896,7 +928,7 @@ int choose_ctas(const Ctx& c, int B, int K, int d, int n_groups) {
   const int most = tuning().head_ctas_max;
   if (most >= 16 && B <= n16) return 16;
   if (most >= 8 && B <= n8) return 8;
-  if (most >= 4 && B <= n4 && (forced || (long long)B * K <= (K <= 128 ? 8192 : 2048))) return 4;
+  if (most >= 4 && B <= n4 && (forced || (long long)B * K <= (K <= 64 ? 8192 : 2048))) return 4;
   if (most >= 2 && B <= n2 && (forced || K <= 64)) return 2;
   return 0;
 }
