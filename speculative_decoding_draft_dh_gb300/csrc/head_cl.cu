@@ -22,12 +22,16 @@
 //    every CTA's lists; every CTA ranks the boundary bin, knows the K winners and tau, checks the
 //    certificate on its groups and scores its share of the winners while the leader ranks them;
 //    after one more barrier the leader orders the logits and computes the softmax.
-// A row whose certificate finds groups to re-score, or whose pool is degenerate, is selected again
-// by the leader alone with the block selection (select_row: exact, with refinement and full
-// rescan) and then rescored.
+// A row whose certificate (fast selection) finds groups to re-score is refined in place by every
+// CTA (those groups scored exactly, the winners ranked again), then rescored.  A row the radix
+// certificate flags, or whose pool is degenerate, or that the in-place refinement cannot settle, is
+// selected again by the leader alone with the block selection (select_row: exact, with refinement
+// and full rescan) and then rescored.
 //
-// Cluster barriers are hardware barriers that every CTA passes unconditionally, so they always
-// complete.
+// Cluster barriers are hardware barriers.  Each path has a fixed sequence of them, and every CTA of
+// a cluster takes the same path: its decisions come from the same data in every CTA (the fast
+// selection, the in-place refinement) or from state combined across the cluster (the radix
+// selection), so the barriers always complete.
 #include <cooperative_groups.h>
 #include <cstdlib>
 #include <cstring>
