@@ -30,7 +30,9 @@ __global__ void __launch_bounds__(EX_THREADS) k_expand(const float* __restrict__
   __shared__ float sp[DH_MAX_K];
   __shared__ int s_keep;
   const int b = blockIdx.x;
-  // the expansion follows the rescoring kernel (programmatic dependent launch)
+  // the next kernel may launch now (its own wait orders it after this grid); the expansion
+  // follows the rescoring kernel (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   for (int k = threadIdx.x; k < K; k += EX_THREADS) {
     const float p = probs[(size_t)b * K + k];

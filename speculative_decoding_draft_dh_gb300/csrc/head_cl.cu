@@ -555,6 +555,9 @@ __global__ void __launch_bounds__(HC_THREADS, 1) k_head_cl(HeadParams p) {
   }
   __syncthreads();
   asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+  // the next kernel may launch now: every kernel of the library that follows waits
+  // (griddepcontrol.wait) for this grid before it reads anything, so its launch latency is hidden
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");  // the records come from the scores kernel
 
   bool fallback = false;

@@ -44,7 +44,9 @@ __global__ void __launch_bounds__(SZ_THREADS) k_size_level(SizeParams p) {
   __shared__ int s_width, s_bin;
   const int r = blockIdx.x;
   const size_t base = (size_t)r * n_all;
-  // the children come from the expansion kernel (programmatic dependent launch)
+  // the next kernel may launch now (its own wait orders it after this grid); the children come
+  // from the expansion kernel (programmatic dependent launch)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (threadIdx.x == 0) {
     int bin = p.n_bins - 1;
