@@ -305,6 +305,9 @@ __global__ void __launch_bounds__(THREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  // launched with programmatic dependent launch: h may come from the kernel before this one, which
+  // may also still read the workspace, so nothing is loaded or stored before the wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the reduce kernel may launch now; it waits (griddepcontrol.wait) for the partial sums
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
@@ -487,15 +490,23 @@ cudaError_t launch_proj_mma(const Ctx& c, const void* h, const void* U, int B, i
   if (!make_map(&tmU, U, (uint64_t)r, (uint64_t)d, 64, BK)) return note_error(cudaErrorInvalidValue, "cuTensorMapEncodeTiled(U)");
   const int m_tiles = (B + BM - 1) / BM;
   const int grid = p.splits * m_tiles * p.n_ntiles;
-  prof_before("proj_mma", c.stream);
-  k_proj_mma<<<grid, THREADS, smem, c.stream>>>(tmH, tmU, p);
-  prof_after(c.stream);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return note_error(e, "launch k_proj_mma");
-  const int BR = B * r;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  {  // programmatic dependent launch: the set-up overlaps the previous kernel's tail
+    cudaLaunchConfig_t pc = {};
+    pc.gridDim = dim3((unsigned)grid);
+    pc.blockDim = dim3(THREADS);
+    pc.dynamicSmemBytes = smem;
+    pc.stream = c.stream;
+    pc.attrs = attr;
+    pc.numAttrs = 1;
+    prof_before("proj_mma", c.stream);
+    e = cudaLaunchKernelEx(&pc, k_proj_mma, tmH, tmU, p);
+    prof_after(c.stream);
+  }
+  if (e != cudaSuccess) return note_error(e, "launch k_proj_mma");
+  const int BR = B * r;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((unsigned)((BR / 4 + 255) / 256));
   cfg.blockDim = dim3(256);

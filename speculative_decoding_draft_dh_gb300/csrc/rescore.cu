@@ -245,6 +245,9 @@ __global__ void __launch_bounds__(NW * 32)
   int2* list = reinterpret_cast<int2*>(ring + (size_t)RING_WARPS * RING_WSLOTS * row_bytes);  // (k, id)
   const int c = blockIdx.x / B, b = blockIdx.x % B;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // the next kernel may launch as these blocks start (every library kernel launched with
+  // programmatic dependent launch waits for this grid before it touches what it touches)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   if (threadIdx.x == 0) {
     s_fail = 0;
     mbar_init(&h_full, 1);
