@@ -59,6 +59,9 @@ __global__ void __launch_bounds__(VS_THREADS) k_verify_stats(const T* __restrict
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * (VS_THREADS / 32);
   const int w0 = blockIdx.x * (VS_THREADS / 32) + (threadIdx.x >> 5);
+  // launched with programmatic dependent launch: the logits may come from the kernel before this
+  // one, which may also still read the workspace, so nothing is loaded or stored before the wait
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   // the loads of item g (row g / n_seg, segment g % n_seg): its SEG_VECS vectors per lane
   auto load = [&](int g, uint4 (&u)[SEG_VECS]) {
     const int row = g / n_seg, sgi = g - row * n_seg;
@@ -176,6 +179,9 @@ __device__ __forceinline__ float block_excl_scan(float x, float* wtot, float* to
 
 template <typename T>
 __global__ void __launch_bounds__(VW_THREADS) k_verify_walk(WalkParams p) {
+  // the next kernel may launch as these blocks start (every library kernel launched with
+  // programmatic dependent launch waits for this grid before it touches what it touches)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int PER = Elem<T>::PER16;
   constexpr int SEG = 32 * PER * SEG_VECS;
   constexpr int LANE_IDS = PER * SEG_VECS;  // ids of a segment per lane in the final rescan
@@ -402,6 +408,9 @@ __device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes)
 
 template <typename T>
 __global__ void __launch_bounds__(VW_THREADS) k_verify_walk_staged(WalkParams p) {
+  // the next kernel may launch as these blocks start (every library kernel launched with
+  // programmatic dependent launch waits for this grid before it touches what it touches)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   constexpr int PER = Elem<T>::PER16;
   constexpr int SEG = 32 * PER * SEG_VECS;
   constexpr int LANE_IDS = PER * SEG_VECS;
@@ -672,11 +681,22 @@ cudaError_t run(const Ctx& c, const void* logits, int B, int L, int vocab, int K
   // persistent grid: two blocks per SM stream the (row, segment) items
   const int per_block = VS_THREADS / 32;
   const unsigned grid = (unsigned)max(1, min(2 * c.num_sms, (n_items + per_block - 1) / per_block));
-  prof_before("verify_stats", c.stream);
-  k_verify_stats<T><<<grid, VS_THREADS, 0, c.stream>>>(static_cast<const T*>(logits), vocab, cf, n_seg, n_items,
-                                                       seg_stats);
-  prof_after(c.stream);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e;
+  {  // programmatic dependent launch: the launch overlaps the previous kernel's tail
+    cudaLaunchAttribute sa[1];
+    sa[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    sa[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t sc = {};
+    sc.gridDim = dim3(grid);
+    sc.blockDim = dim3(VS_THREADS);
+    sc.stream = c.stream;
+    sc.attrs = sa;
+    sc.numAttrs = 1;
+    prof_before("verify_stats", c.stream);
+    e = cudaLaunchKernelEx(&sc, k_verify_stats<T>, static_cast<const T*>(logits), vocab, cf, n_seg, n_items,
+                           seg_stats);
+    prof_after(c.stream);
+  }
   if (e != cudaSuccess) return e;
   WalkParams wp;
   wp.logits = logits;
